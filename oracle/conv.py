@@ -1,0 +1,235 @@
+"""CG tensor product and fused CG-tensor-product convolution, forward and backward.
+
+Test infrastructure only (see the package docstring).  FP64 throughout; inputs
+of any float type are promoted exactly.
+
+Definitions followed
+--------------------
+"An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks":
+
+* Figure 1 / Figure 4A (batched product, no graph), for every sample b and path
+  (l1, l2 -> l3) of the plan::
+
+      z[b][path, u, m3] = W[b][path, u] * sum_{m1, m2} C[m1, m2, m3] x1[b][u, m1] x2[b][m2]
+
+* Figure 4B (fused graph convolution): the same message per edge e = (src -> dst)
+  with x1 = x[src], x2 = Y[e], W = W[e], summed into the receiver::
+
+      out[n] = sum_{e in row n of the CSR, in CSR order} message(e)
+
+* Abstract ("optimized kernels for the gradient"): the adjoints with respect to
+  x (or x1), Y (or x2) and W, written out by the chain rule.
+
+"Sobek: Streaming Equivariant Tensor Product Convolutions", Abstract (radial
+projection with fully connected multiplicity mixing): the uvw message with
+per-edge weights W_e[path, u, w] = sum_k R[e, k] M[k, path, u, w], which this
+oracle forms explicitly for every edge (the plain definition), summed into
+output block i_out::
+
+      out[dst][i_out][w, m3] += sum_u W_e[path, u, w] sum_{m1,m2} C x[src][u,m1] Y[e][m2]
+
+``C`` is ``cg.real_cg_block(l1, l2, l3)``.  No path normalisation factor.
+"""
+
+import numpy as np
+
+from .cg import real_cg_block
+from .graph import csr_dst
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def _blocks(p, x1, y2):
+    D1, D2 = 2 * p.l1 + 1, 2 * p.l2 + 1
+    xs = x1[:, p.off1:p.off1 + p.mul1 * D1].reshape(-1, p.mul1, D1)
+    ys = y2[:, p.off2:p.off2 + D2]
+    return xs, ys
+
+
+def _edges_of(rowptr, nodes):
+    if len(nodes) == 0:
+        return np.zeros(0, np.int64), np.zeros(0, np.int64)
+    eidx = np.concatenate([np.arange(rowptr[n], rowptr[n + 1]) for n in nodes]).astype(np.int64)
+    owner = np.repeat(np.arange(len(nodes)), rowptr[nodes + 1] - rowptr[nodes])
+    return eidx, owner
+
+
+# ---------------------------------------------------------------------------
+# uvu: batched product (Figure 4A) and per-edge message
+# ---------------------------------------------------------------------------
+
+def tp_uvu_forward(plan, x1, x2, W):
+    """z[b] for every sample: x1 [B, d1], x2 [B, d2], W [B, w_numel] -> [B, d_out]."""
+    x1, x2, W = _f64(x1), _f64(x2), _f64(W)
+    out = np.zeros((x1.shape[0], plan.d_out))
+    for p in plan.paths:
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        xs, ys = _blocks(p, x1, x2)
+        w = W[:, p.woff:p.woff + p.mul1]
+        z = np.einsum("ijk,bui,bj->buk", C, xs, ys) * w[:, :, None]
+        D3 = 2 * p.l3 + 1
+        out[:, p.ooff:p.ooff + p.mul1 * D3] += z.reshape(z.shape[0], -1)
+    return out
+
+
+def tp_uvu_backward(plan, g, x1, x2, W):
+    """Adjoints of tp_uvu_forward: (gx1 [B,d1], gx2 [B,d2], gW [B,w_numel])."""
+    g, x1, x2, W = _f64(g), _f64(x1), _f64(x2), _f64(W)
+    B = x1.shape[0]
+    gx1, gx2, gW = np.zeros((B, plan.d1)), np.zeros((B, plan.d2)), np.zeros((B, plan.w_numel))
+    for p in plan.paths:
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+        xs, ys = _blocks(p, x1, x2)
+        w = W[:, p.woff:p.woff + p.mul1]
+        gz = g[:, p.ooff:p.ooff + p.mul1 * D3].reshape(B, p.mul1, D3)
+        gW[:, p.woff:p.woff + p.mul1] += np.einsum("ijk,bui,bj,buk->bu", C, xs, ys, gz)
+        gx2[:, p.off2:p.off2 + D2] += np.einsum("ijk,bui,bu,buk->bj", C, xs, w, gz)
+        gx1[:, p.off1:p.off1 + p.mul1 * D1] += np.einsum(
+            "ijk,bj,bu,buk->bui", C, ys, w, gz).reshape(B, -1)
+    return gx1, gx2, gW
+
+
+# ---------------------------------------------------------------------------
+# uvu fused convolution (Figure 4B)
+# ---------------------------------------------------------------------------
+
+def conv_uvu_forward(plan, x, Y, W, rowptr, col, nodes=None):
+    """out[N, d_out] (or the rows of `nodes`, in that order)."""
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    x, Y, W = _f64(x), _f64(Y), _f64(W)
+    if nodes is None:
+        nodes = np.arange(len(rowptr) - 1)
+    nodes = np.asarray(nodes, dtype=np.int64)
+    eidx, owner = _edges_of(rowptr, nodes)
+    out = np.zeros((len(nodes), plan.d_out))
+    if eidx.size == 0:
+        return out
+    msg = tp_uvu_forward(plan, x[col[eidx]], Y[eidx], W[eidx])
+    np.add.at(out, owner, msg)          # CSR order within each receiver
+    return out
+
+
+def conv_uvu_backward(plan, g, x, Y, W, rowptr, col, edges=None):
+    """(gx [N,d1], gY [Es,d2], gW [Es,w_numel]) over CSR positions `edges` (all by default).
+
+    gx only collects the contributions of the selected edges, summed over each
+    sender's edges in CSR order.
+    """
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    g, x, Y, W = _f64(g), _f64(x), _f64(Y), _f64(W)
+    N = len(rowptr) - 1
+    if edges is None:
+        edges = np.arange(col.shape[0])
+    edges = np.asarray(edges, dtype=np.int64)
+    dst = csr_dst(rowptr)[edges]
+    src = col[edges]
+    gxe, gY, gW = tp_uvu_backward(plan, g[dst], x[src], Y[edges], W[edges])
+    gx = np.zeros((N, plan.d1))
+    np.add.at(gx, src, gxe)
+    return gx, gY, gW
+
+
+# ---------------------------------------------------------------------------
+# uvw with radial weights (Sobek): plain definition, W_e formed per edge
+# ---------------------------------------------------------------------------
+
+def conv_uvw_radial_forward(plan, x, Y, R, M, rowptr, col, nodes=None, block=256):
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    x, Y, R, M = _f64(x), _f64(Y), _f64(R), _f64(M)
+    if nodes is None:
+        nodes = np.arange(len(rowptr) - 1)
+    nodes = np.asarray(nodes, dtype=np.int64)
+    out = np.zeros((len(nodes), plan.d_out))
+    eidx, owner = _edges_of(rowptr, nodes)
+    for s in range(0, eidx.size, block):
+        e = eidx[s:s + block]
+        We = R[e] @ M                       # per-edge weights, formed explicitly
+        x1, y2 = x[col[e]], Y[e]
+        msg = np.zeros((e.size, plan.d_out))
+        for p in plan.paths:
+            C = real_cg_block(p.l1, p.l2, p.l3)
+            D3 = 2 * p.l3 + 1
+            xs, ys = _blocks(p, x1, y2)
+            t = np.einsum("ijk,eui,ej->euk", C, xs, ys)
+            w = We[:, p.woff:p.woff + p.mul1 * p.mul_out].reshape(-1, p.mul1, p.mul_out)
+            msg[:, p.ooff:p.ooff + p.mul_out * D3] += np.einsum("euw,euk->ewk", w, t).reshape(e.size, -1)
+        np.add.at(out, owner[s:s + block], msg)
+    return out
+
+
+def conv_uvw_radial_backward(plan, g, x, Y, R, M, rowptr, col, edges=None, block=256):
+    """(gx [N,d1], gY [Es,d2], gR [Es,K], gM [K,w_numel]) over CSR positions `edges`."""
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    g, x, Y, R, M = _f64(g), _f64(x), _f64(Y), _f64(R), _f64(M)
+    N = len(rowptr) - 1
+    if edges is None:
+        edges = np.arange(col.shape[0])
+    edges = np.asarray(edges, dtype=np.int64)
+    dst_all = csr_dst(rowptr)
+    gx = np.zeros((N, plan.d1))
+    gY = np.zeros((edges.size, plan.d2))
+    gR = np.zeros((edges.size, R.shape[1]))
+    gM = np.zeros_like(M)
+    for s in range(0, edges.size, block):
+        e = edges[s:s + block]
+        We = R[e] @ M
+        gWe = np.zeros_like(We)
+        x1, y2, gd = x[col[e]], Y[e], g[dst_all[e]]
+        gxe = np.zeros((e.size, plan.d1))
+        for p in plan.paths:
+            C = real_cg_block(p.l1, p.l2, p.l3)
+            D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+            xs, ys = _blocks(p, x1, y2)
+            t = np.einsum("ijk,eui,ej->euk", C, xs, ys)
+            sl = slice(p.woff, p.woff + p.mul1 * p.mul_out)
+            w = We[:, sl].reshape(-1, p.mul1, p.mul_out)
+            go = gd[:, p.ooff:p.ooff + p.mul_out * D3].reshape(-1, p.mul_out, D3)
+            gWe[:, sl] = np.einsum("ewk,euk->euw", go, t).reshape(e.size, -1)
+            gt = np.einsum("euw,ewk->euk", w, go)
+            gxe[:, p.off1:p.off1 + p.mul1 * D1] += np.einsum("ijk,ej,euk->eui", C, ys, gt).reshape(e.size, -1)
+            gY[s:s + e.size, p.off2:p.off2 + D2] += np.einsum("ijk,eui,euk->ej", C, xs, gt)
+        gR[s:s + e.size] = gWe @ M.T
+        gM += R[e].T @ gWe
+        np.add.at(gx, col[e], gxe)
+    return gx, gY, gR, gM
+
+
+# ---------------------------------------------------------------------------
+# brute force: one dense bilinear tensor per edge (tiny inputs only)
+# ---------------------------------------------------------------------------
+
+def dense_tensor(plan, w_edge):
+    """T[d1, d2, d_out] with out = einsum('ijk,i,j->k', T, x1, x2) for one edge.
+
+    w_edge is that edge's uvu weight row [w_numel] or uvw weight row
+    [sum_path mul1*mul_out].  Built entry by entry with explicit index
+    arithmetic, independently of the vectorised per-path code above.
+    """
+    T = np.zeros((plan.d1, plan.d2, plan.d_out))
+    for p in plan.paths:
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+        for u in range(p.mul1):
+            for m1 in range(D1):
+                i = p.off1 + u * D1 + m1
+                for m2 in range(D2):
+                    j = p.off2 + m2
+                    for m3 in range(D3):
+                        c = C[m1, m2, m3]
+                        if c == 0.0:
+                            continue
+                        if plan.mode == "uvu":
+                            k = p.ooff + u * D3 + m3
+                            T[i, j, k] += w_edge[p.woff + u] * c
+                        else:
+                            for w in range(p.mul_out):
+                                k = p.ooff + w * D3 + m3
+                                T[i, j, k] += w_edge[p.woff + u * p.mul_out + w] * c
+    return T
