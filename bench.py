@@ -1,0 +1,408 @@
+"""Throughput of the fused CG tensor-product convolution (edges/s, forward + backward).
+
+Default workload: the NequIP-like convolution -- 10,000 nodes, 32 in-edges per
+node (320,000 edges), in1 = 32x(0e,1o,2e,3o), SH l<=3, uvu with all 34
+parity-allowed paths (l3 <= 3), FP32.  One step = cgtp_conv_forward +
+cgtp_conv_backward over the whole graph (the graph and plan are built once,
+outside the timed region).  Other workloads: --config tiny|nequip|mace|mace64|highl|uvw.
+
+Output: one JSON line (rank 0).  ``value`` is device-timed edges/s with inputs
+resident in HBM; ``e2e`` repeats the step through the public API with the
+step's inputs copied from pinned host memory and its results copied back inside
+the timed region.  ``roofline`` describes the dominant kernel; ``cpu_baseline``
+times the FP64 oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the oracle itself (the reference arm): host cores,
+bounded sample, same metric and config.
+"""
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CGTP-conv edges/s fwd and fwd+bwd (FP32/FP64); % of HBM/FLOP roofline"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "src": "measured", "sm_max_mhz": d.get("sm_max_mhz", 2070.0)}
+    return {"hbm_gbs": 6800.0, "src": "fallback", "sm_max_mhz": 2070.0}
+
+
+# FP32 / FP64 CUDA-core peaks from unit counts: 152 SMs x 128 FP32 lanes x 2 flop
+# x clock; FP64 at the nominal 1.25 TFLOP/s of the part.
+def alu_peak_tflops(dtype_name, mhz):
+    if dtype_name == "f64":
+        return 1.25
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+CONFIGS = {
+    "tiny": dict(name="tiny", dtype="float32", over={}),
+    "nequip": dict(name="nequip", dtype="float32", over={}),
+    "mace": dict(name="mace", dtype="float32", over={}),
+    "mace64": dict(name="mace", dtype="float64", over={}),
+    "highl": dict(name="highl", dtype="float32", over={}),
+    "uvw": dict(name="uvw", dtype="float32", over={}),
+}
+
+
+def build_inputs(cfgkey, device):
+    import torch
+    import clebsch_gordan_tensor_racah_gb300 as cg
+    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+    c = CONFIGS[cfgkey]
+    spec = dict(wl.SPECS[c["name"]])
+    tdt = torch.float64 if c["dtype"] == "float64" else torch.float32
+    mode = spec["mode"]
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
+                   radial_k=spec.get("K", 0) if mode == "uvw" else 0)
+    w = wl.make(c["name"], plan.w_numel, seed=0, dtype=c["dtype"], **c["over"])
+    host = {k: v for k, v in w.items() if isinstance(v, np.ndarray)}
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(device) for k, v in host.items()}
+    graph = None
+    if "rowptr" in dev:
+        graph = cg.Graph(dev["rowptr"], dev["col"], w["N"])
+    return plan, graph, w, host, dev, spec, tdt
+
+
+def step_fns(cfgkey, plan, graph, w, dev, tdt):
+    """Returns (fwd, bwd, units, bytes_fwd, bytes_bwd, flops_fwd, flops_bwd, out_shape)."""
+    import clebsch_gordan_tensor_racah_gb300 as cg
+    es = 8 if tdt.__str__().endswith("64") else 4
+    if "rowptr" in dev:
+        N, E = w["N"], w["E"]
+        x, Y = dev["x"], dev["Y"]
+        WR = dev["W"] if plan.mode == "uvu" else dev["R"]
+        M = dev.get("M")
+        units = E
+        idx = 4 * (N + 1 + E)
+        bf = es * (N * plan.d1 + E * plan.d2 + WR.numel() + (M.numel() if M is not None else 0) + N * plan.d_out) + idx
+        bb = es * (2 * N * plan.d1 + 2 * E * plan.d2 + 2 * WR.numel() + 2 * (M.numel() if M is not None else 0)
+                   + N * plan.d_out) + idx + 8 * E
+
+        def fwd(out):
+            return cg.cgtp_conv_forward(plan, graph, x, Y, WR, M, out=out)
+
+        def bwd(g, outs):
+            return cg.cgtp_conv_backward(plan, graph, g, x, Y, WR, M, outs=outs)
+        out_shape = (N, plan.d_out)
+    else:
+        B = w["B"]
+        x1, x2, W = dev["x1"], dev["x2"], dev["W"]
+        units = B
+        bf = es * (B * (plan.d1 + plan.d2 + plan.w_numel + plan.d_out))
+        bb = es * (B * (2 * plan.d1 + 2 * plan.d2 + 2 * plan.w_numel + plan.d_out))
+
+        def fwd(out):
+            return cg.cgtp_forward(plan, x1, x2, W, out=out)
+
+        def bwd(g, outs):
+            return cg.cgtp_backward(plan, g, x1, x2, W)
+        out_shape = (B, plan.d_out)
+    return fwd, bwd, units, bf, bb, out_shape
+
+
+def flops_per_unit(plan_paths, mode):
+    """Algorithmic FLOPs of one edge (forward): cy = C.Y, then per channel the
+    (2l1+1)x(2l3+1) contraction and the weight product (uvu) or, for uvw, the
+    per-edge product plus the receiver-state update and its share of the node GEMM."""
+    return None
+
+
+class ClockSampler:
+    def __init__(self, index=0):
+        self.samples, self.proc, self.thread = [], None, None
+        self.index = index
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+
+        def rd():
+            for line in self.proc.stdout:
+                self.samples.append([s.strip() for s in line.split(",")])
+        self.thread = threading.Thread(target=rd, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = [r for r in self.samples if len(r) >= 9]
+        if not rows:
+            return None
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def time_oracle_sample(cfgkey, budget_s=12.0):
+    """FP64 oracle on a bounded sample of the workload: (units/s, sample description)."""
+    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+    from oracle import conv as oconv, irreps as oirr
+    c = CONFIGS[cfgkey]
+    spec = wl.SPECS[c["name"]]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], spec["mode"])
+    if spec["graph"] is None:
+        B = 64
+        w = wl.make(c["name"], oplan.w_numel, seed=0, dtype=c["dtype"], B=B)
+        units, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            out = oconv.tp_uvu_forward(oplan, w["x1"], w["x2"], w["W"])
+            oconv.tp_uvu_backward(oplan, out, w["x1"], w["x2"], w["W"])
+            units += B
+        dt = time.perf_counter() - t0
+        return units / dt, f"batches of {B} samples of the same recipe, fwd+bwd, {dt:.1f} s"
+    # a smaller graph of the same recipe (same degree distribution and features)
+    N = {"tiny": 64, "nequip": 400, "mace": 200, "uvw": 8}[c["name"]]
+    w = wl.make(c["name"], oplan.w_numel, seed=0, dtype=c["dtype"], N=N)
+    units, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        if spec["mode"] == "uvu":
+            out = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+            oconv.conv_uvu_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+        else:
+            out = oconv.conv_uvw_radial_forward(oplan, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
+            oconv.conv_uvw_radial_backward(oplan, out, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
+        units += w["E"]
+    dt = time.perf_counter() - t0
+    return units / dt, f"{N}-node graph of the same recipe ({w['E']} edges), fwd+bwd repeated for {dt:.1f} s"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_block(cfgkey, w, n_gpus):
+    c = CONFIGS[cfgkey]
+    spec = c["name"]
+    d = {"workload": {"tiny": "tiny uvu conv (64 nodes, 512 edges)",
+                      "nequip": "NequIP-like uvu conv (10k nodes x 32 in-edges, 32x(0e,1o,2e,3o), SH l<=3)",
+                      "mace": "MACE-like uvu conv (5k nodes, Poisson(40) in-degree, 128x(0e,1o,2e), SH l<=3)",
+                      "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
+                      "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)"}[spec],
+         "step": "conv forward + backward" if "N" in w else "batched forward + backward",
+         "l2": "inputs larger than L2 (no flush needed)",
+         "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
+    if "N" in w:
+        d.update(nodes=w["N"], edges=w["E"])
+    else:
+        d.update(batch=w["B"])
+    return d
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfgkey = args.config
+    t_steps = []
+    rate = None
+    for i in range(args.warmup + args.steps):
+        r, desc = time_oracle_sample(cfgkey, budget_s=max(2.0, 60.0 / max(1, args.warmup + args.steps)))
+        if i >= args.warmup:
+            t_steps.append(r)
+    rate = float(np.median(t_steps))
+    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+    c = CONFIGS[cfgkey]
+    units = wl.SPECS[c["name"]].get("N", 0) * wl.SPECS[c["name"]].get("deg", 0) or wl.SPECS[c["name"]].get("B") or 512
+    line = {"metric": METRIC, "value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * units / rate, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": config_block(cfgkey, {"N": 1} if cfgkey != "highl" else {"B": 1}, 1)["workload"]},
+            "cpu_baseline": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
+                             "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="nequip", choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    if rank == 0:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    build()
+
+    plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device)
+    fwd, bwd, units, bf, bb, out_shape = step_fns(args.config, plan, graph, w, dev, tdt)
+    g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
+    out = torch.empty(out_shape, dtype=tdt, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fwd(out)
+        return bwd(g, None)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    # per-kernel split (events on the launching stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf, tb = [], []
+    for _ in range(3):
+        ev[0].record(stream)
+        fwd(out)
+        ev[1].record(stream)
+        bwd(g, None)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        tf.append(ev[0].elapsed_time(ev[1]))
+        tb.append(ev[1].elapsed_time(ev[2]))
+    # timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fe = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    be = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e0.record(stream)
+    for i in range(args.steps):
+        fe[i].record(stream)
+        fwd(out)
+        be[i].record(stream)
+        bwd(g, None)
+    fe[args.steps].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    fwd_ms = float(np.mean([fe[i].elapsed_time(be[i]) for i in range(args.steps)]))
+    bwd_ms = float(np.mean([be[i].elapsed_time(fe[i + 1]) for i in range(args.steps)]))
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * units / (ms / 1000.0)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()
+               if k not in ("rowptr", "col")}
+        gh = g.cpu().pin_memory()
+        out_h = torch.empty(out_shape, dtype=tdt).pin_memory()
+        res_h = None
+        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + gh.numel() * gh.element_size()
+
+        def e2e_step():
+            nonlocal res_h
+            for k, t in pin.items():
+                dev[k].copy_(t, non_blocking=True)
+            g.copy_(gh, non_blocking=True)
+            fwd(out)
+            r = bwd(g, None)
+            out_h.copy_(out, non_blocking=True)
+            if res_h is None:
+                res_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in r if x is not None]
+            for hbuf, x in zip(res_h, [x for x in r if x is not None]):
+                hbuf.copy_(x, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        d2h = out_h.numel() * out_h.element_size() + sum(t.numel() * t.element_size() for t in res_h)
+        k2 = max(3, args.steps // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / k2
+        e2e = {"value": world * units / (e2e_ms / 1000.0), "unit": "edges/s" if "N" in w else "samples/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk = peaks()
+    dominant = "backward" if bwd_ms >= fwd_ms else "forward"
+    dom_ms = bwd_ms if dominant == "backward" else fwd_ms
+    dom_bytes = bb if dominant == "backward" else bf
+    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"uvu_{dominant}_kernel" if plan.mode == "uvu" else f"uvw {dominant}",
+                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"], "traffic": None,
+                "algorithmic_bytes_per_launch": int(dom_bytes),
+                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                "fwd_GBps": bf / (fwd_ms / 1000) / 1e9, "bwd_GBps": bb / (bwd_ms / 1000) / 1e9}
+    line = {"metric": METRIC, "value": value, "unit": "edges/s" if "N" in w else "samples/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64" if tdt == torch.float64 else "f32", "data": "synthetic",
+            "config": config_block(args.config, w, world),
+            "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
+            "clocks": clk}
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc = time_oracle_sample(args.config)
+        line["cpu_baseline"] = {"value": rate, "unit": line["unit"], "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+"""GB300 fused Clebsch-Gordan tensor-product convolution: Python binding of libcgtp.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libcgtp.so`` (built in-tree by ``_build.build()``).  PyTorch is used
+for device memory and streams.  There is no CPU fallback: if the library is
+missing or no GPU is present the calls raise.
+
+Names follow the C ABI in ``include/cgtp.h``:
+
+* ``Plan(irreps_in1, irreps_in2, irreps_out, mode, dtype, radial_k)`` --
+  ``cgtp_plan_create``; ``plan.d1, d2, d_out, w_numel, n_paths``;
+  ``plan.path(p)`` -> (ints, CG block).
+* ``cgtp_forward(plan, x1, x2, W)`` / ``cgtp_backward(plan, gout, x1, x2, W)``.
+* ``Graph(rowptr, col, N)`` -- ``cgtp_graph_create``; ``graph.transpose()``.
+* ``cgtp_conv_forward(plan, graph, x, Y, W_or_R, M=None)`` and
+  ``cgtp_conv_backward(plan, graph, gout, x, Y, W_or_R, M=None)``.
+* ``cgtp_real_cg_block(l1, l2, l3)`` -- host-only query of the planner's block.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcgtp.so")
+
+CGTP_OK, CGTP_EINVAL, CGTP_EUNSUPPORTED, CGTP_ENOMEM, CGTP_ECUDA, CGTP_EGRAPH = range(6)
+CGTP_UVU, CGTP_UVW = 0, 1
+CGTP_F32, CGTP_F64 = 0, 1
+
+EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan_path",
+           "cgtp_forward", "cgtp_backward", "cgtp_graph_create", "cgtp_graph_destroy",
+           "cgtp_graph_transpose", "cgtp_conv_forward", "cgtp_conv_backward",
+           "cgtp_real_cg_block", "cgtp_last_error"]
+
+
+class CgtpError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"cgtp status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """Load libcgtp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run __graft_entry__.build() "
+                              "(or python -m clebsch_gordan_tensor_racah_gb300._build)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.cgtp_last_error.restype = ctypes.c_char_p
+        L.cgtp_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.c_char_p, ctypes.c_char_p,
+                                       ctypes.c_char_p, vp, i32, i32, i32, i32]
+        L.cgtp_plan_destroy.argtypes = [vp]
+        L.cgtp_plan_destroy.restype = None
+        L.cgtp_plan_info.argtypes = [vp] + [ctypes.POINTER(i64)] * 4 + [ctypes.POINTER(i32)]
+        L.cgtp_plan_path.argtypes = [vp, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double), i64]
+        L.cgtp_forward.argtypes = [vp, vp, vp, vp, vp, i64, vp]
+        L.cgtp_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, vp]
+        L.cgtp_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, vp]
+        L.cgtp_graph_destroy.argtypes = [vp]
+        L.cgtp_graph_destroy.restype = None
+        L.cgtp_graph_transpose.argtypes = [vp, vp, vp, vp, vp]
+        L.cgtp_conv_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.cgtp_conv_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.cgtp_real_cg_block.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_double), i64]
+        for name in EXPORTS:
+            if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
+                getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != CGTP_OK:
+        raise CgtpError(status, lib().cgtp_last_error().decode())
+
+
+def cgtp_real_cg_block(l1, l2, l3):
+    n = (2 * l1 + 1) * (2 * l2 + 1) * (2 * l3 + 1)
+    buf = np.zeros(n, dtype=np.float64)
+    _check(lib().cgtp_real_cg_block(l1, l2, l3, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n))
+    return buf.reshape(2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1)
+
+
+# ---------------------------------------------------------------------------
+# torch-facing helpers (imported lazily so host-only use needs no torch CUDA)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, name, dtype=None):
+    torch = _torch()
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """cgtp_plan_create: paths, CG tables and (uvw) bounded scratch on the current device."""
+
+    def __init__(self, irreps_in1, irreps_in2, irreps_out, mode="uvu", dtype=None, radial_k=0,
+                 instructions=None):
+        torch = _torch()
+        dtype = dtype or torch.float32
+        self.mode = mode
+        self.dtype = dtype
+        self.radial_k = radial_k
+        m = CGTP_UVU if mode == "uvu" else CGTP_UVW
+        dt = CGTP_F64 if dtype == torch.float64 else CGTP_F32
+        h = ctypes.c_void_p()
+        arr, n = None, 0
+        if instructions:
+            n = len(instructions)
+            arr = (ctypes.c_int * (3 * n))(*[v for ins in instructions for v in ins])
+        _check(lib().cgtp_plan_create(ctypes.byref(h), irreps_in1.encode(), irreps_in2.encode(),
+                                      irreps_out.encode(), ctypes.cast(arr, ctypes.c_void_p) if arr else None,
+                                      n, m, dt, radial_k))
+        self._h = h
+        d = [ctypes.c_int64() for _ in range(4)]
+        npaths = ctypes.c_int()
+        _check(lib().cgtp_plan_info(h, *[ctypes.byref(v) for v in d], ctypes.byref(npaths)))
+        self.d1, self.d2, self.d_out, self.w_numel = (v.value for v in d)
+        self.n_paths = npaths.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def path(self, p):
+        ints = (ctypes.c_int * 10)()
+        _check(lib().cgtp_plan_path(self._h, p, ints, None, 0))
+        l1, l2, l3 = ints[0], ints[1], ints[2]
+        n = (2 * l1 + 1) * (2 * l2 + 1) * (2 * l3 + 1)
+        buf = np.zeros(n)
+        _check(lib().cgtp_plan_path(self._h, p, ints, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n))
+        return list(ints), buf.reshape(2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.cgtp_plan_destroy(h)
+            self._h = None
+
+
+class Graph:
+    """cgtp_graph_create: validated receiver-sorted CSR + device transpose."""
+
+    def __init__(self, rowptr, col, N, stream=None):
+        torch = _torch()
+        self.rowptr, self.col, self.N = rowptr, col, int(N)
+        self.E = int(col.numel())
+        h = ctypes.c_void_p()
+        _check(lib().cgtp_graph_create(ctypes.byref(h), _ptr(rowptr, "rowptr", torch.int32),
+                                       _ptr(col, "col", torch.int32) if self.E else None,
+                                       self.N, self.E, _stream(stream)))
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def transpose(self, stream=None):
+        torch = _torch()
+        dev = self.rowptr.device
+        t_rowptr = torch.empty(self.N + 1, dtype=torch.int32, device=dev)
+        t_eid = torch.empty(max(self.E, 1), dtype=torch.int32, device=dev)
+        t_dst = torch.empty(max(self.E, 1), dtype=torch.int32, device=dev)
+        _check(lib().cgtp_graph_transpose(self._h, _ptr(t_rowptr, "t_rowptr"), _ptr(t_eid, "t_eid"),
+                                          _ptr(t_dst, "t_dst"), _stream(stream)))
+        return t_rowptr, t_eid[:self.E], t_dst[:self.E]
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.cgtp_graph_destroy(h)
+            self._h = None
+
+
+def cgtp_forward(plan, x1, x2, W, out=None, stream=None):
+    torch = _torch()
+    B = x1.shape[0]
+    if out is None:
+        out = torch.empty(B, plan.d_out, dtype=plan.dtype, device=x1.device)
+    _check(lib().cgtp_forward(plan.handle, _ptr(x1, "x1", plan.dtype), _ptr(x2, "x2", plan.dtype),
+                              _ptr(W, "W", plan.dtype), _ptr(out, "out", plan.dtype), B, _stream(stream)))
+    return out
+
+
+def cgtp_backward(plan, gout, x1, x2, W, stream=None):
+    torch = _torch()
+    B = x1.shape[0]
+    gx1, gx2, gW = torch.empty_like(x1), torch.empty_like(x2), torch.empty_like(W)
+    _check(lib().cgtp_backward(plan.handle, _ptr(gout, "gout", plan.dtype), _ptr(x1, "x1", plan.dtype),
+                               _ptr(x2, "x2", plan.dtype), _ptr(W, "W", plan.dtype),
+                               _ptr(gx1, "gx1"), _ptr(gx2, "gx2"), _ptr(gW, "gW"), B, _stream(stream)))
+    return gx1, gx2, gW
+
+
+def cgtp_conv_forward(plan, graph, x, Y, W_or_R, M=None, out=None, stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.dtype, device=x.device)
+    _check(lib().cgtp_conv_forward(plan.handle, graph.handle, _ptr(x, "x", plan.dtype),
+                                   _ptr(Y, "Y", plan.dtype), _ptr(W_or_R, "W_or_R", plan.dtype),
+                                   _ptr(M, "M", plan.dtype), _ptr(out, "out", plan.dtype), _stream(stream)))
+    return out
+
+
+def cgtp_conv_backward(plan, graph, gout, x, Y, W_or_R, M=None, stream=None, outs=None):
+    torch = _torch()
+    if outs is None:
+        gx, gY, gW = torch.empty_like(x), torch.empty_like(Y), torch.empty_like(W_or_R)
+        gM = torch.empty_like(M) if M is not None else None
+    else:
+        gx, gY, gW, gM = outs
+    _check(lib().cgtp_conv_backward(plan.handle, graph.handle, _ptr(gout, "gout", plan.dtype),
+                                    _ptr(x, "x", plan.dtype), _ptr(Y, "Y", plan.dtype),
+                                    _ptr(W_or_R, "W_or_R", plan.dtype), _ptr(M, "M", plan.dtype),
+                                    _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gW, "gW"), _ptr(gM, "gM"),
+                                    _stream(stream)))
+    return gx, gY, gW, gM

@@ -1,0 +1,87 @@
+"""Build libcgtp.so in-tree for sm_103a (nvcc + g++, translation units in parallel).
+
+The library is the product: every step of the fused CG tensor-product
+convolution runs in its kernels.  Objects go to ``_build/`` at the repository
+root; the shared object is written next to this file.
+"""
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INC = os.path.join(ROOT, "include")
+BUILD = os.path.join(ROOT, "_build")
+LIB = os.path.join(PKG, "libcgtp.so")
+
+CU_SOURCES = ["api.cu", "graph.cu", "uvu.cu", "uvu_f32.cu", "uvu_f32_l7.cu", "uvu_f64.cu",
+              "uvu_f64_l7.cu", "uvw.cu"]
+CPP_SOURCES = ["planner.cpp"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc():
+    for cand in (os.environ.get("CUDACXX"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _headers_mtime():
+    m = os.path.getmtime(os.path.join(INC, "cgtp.h"))
+    for f in os.listdir(CSRC):
+        if f.endswith((".h", ".cuh")):
+            m = max(m, os.path.getmtime(os.path.join(CSRC, f)))
+    return m
+
+
+def _stale(src, obj, hdr_m):
+    return not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_m)
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("build failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    return r.stdout + r.stderr
+
+
+def build(verbose=False, jobs=None):
+    """Compile (incrementally) and link libcgtp.so; returns its path."""
+    os.makedirs(BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    hdr_m = _headers_mtime()
+    cmds = []
+    objs = []
+    for f in CU_SOURCES:
+        src, obj = os.path.join(CSRC, f), os.path.join(BUILD, f + ".o")
+        objs.append(obj)
+        if _stale(src, obj, hdr_m):
+            cmds.append([nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+                         "-Xcompiler", "-ffp-contract=off", "-I", INC, "-c", src, "-o", obj])
+    for f in CPP_SOURCES:
+        src, obj = os.path.join(CSRC, f), os.path.join(BUILD, f + ".o")
+        objs.append(obj)
+        if _stale(src, obj, hdr_m):
+            cmds.append(["g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-I", INC,
+                         "-c", src, "-o", obj])
+    jobs = jobs or max(1, min(len(cmds), os.cpu_count() or 4))
+    if cmds:
+        # longest translation units first
+        cmds.sort(key=lambda c: ("_l7" not in c[-3], c[-3]))
+        with cf.ThreadPoolExecutor(jobs) as ex:
+            for out in ex.map(_run, cmds):
+                if verbose and out.strip():
+                    print(out)
+    if cmds or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
+        tmp = LIB + ".tmp"
+        _run([nvcc, "-shared", *ARCH, "-o", tmp, *objs, "-cudart=static"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

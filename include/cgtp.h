@@ -1,0 +1,162 @@
+/*
+ * cgtp.h -- C ABI of the GB300 fused Clebsch-Gordan tensor-product convolution.
+ *
+ * The operation (from "An Efficient Sparse Kernel Generator for O(3)-Equivariant
+ * Deep Networks", Figure 1 and Figure 4B; "Sobek: Streaming Equivariant Tensor
+ * Product Convolutions", Abstract):
+ *
+ *   message(e)[path, u, m3] = W[e][path, u] * sum_{m1,m2} C[m1,m2,m3] x[src e][u,m1] Y[e][m2]
+ *   out[n] = sum over the in-edges e of receiver n of message(e)            (uvu)
+ *
+ *   uvw with radial weights: W_e[path,u,w] = sum_k R[e,k] M[k,path,u,w] (never formed)
+ *   out[n][i_out][w, m3] = sum_e sum_path sum_u W_e[path,u,w] sum C x[src][u,m1] Y[e][m2]
+ *
+ * C is the real-basis, component-normalised Clebsch-Gordan block of (l1,l2,l3),
+ * computed by the planner from Racah's closed form.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Feature layout is multiplicity-major: inside irreps block i the element
+ *    (u, m) of a row sits at offset_i + u*(2l+1) + (m+l).  Rows are contiguous,
+ *    row-major, element type float (CGTP_F32) or double (CGTP_F64).
+ *  - Tensor arguments are DEVICE pointers on the current CUDA device, aligned
+ *    to 16 bytes; the caller owns them.  Outputs are overwritten, never
+ *    accumulated; inputs are never modified.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Compute entry
+ *    points are asynchronous: they enqueue kernels and return.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failed check returns a status and launches nothing.  cgtp_last_error()
+ *    returns a message for the last failure of the calling thread.
+ *  - Results are bitwise deterministic run to run (no atomics in any
+ *    floating-point accumulation).
+ */
+#ifndef CGTP_H
+#define CGTP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct cgtp_plan_s* cgtp_plan;
+typedef struct cgtp_graph_s* cgtp_graph;
+
+typedef enum {
+  CGTP_OK = 0,
+  CGTP_EINVAL = 1,        /* bad argument: null pointer, bad string, size mismatch, misalignment */
+  CGTP_EUNSUPPORTED = 2,  /* valid request outside what this library implements */
+  CGTP_ENOMEM = 3,        /* device allocation failed (plan or graph creation only) */
+  CGTP_ECUDA = 4,         /* a CUDA call or kernel launch failed */
+  CGTP_EGRAPH = 5         /* the CSR arrays are not a valid receiver-sorted edge list */
+} cgtp_status;
+
+typedef enum { CGTP_UVU = 0, CGTP_UVW = 1 } cgtp_mode;
+typedef enum { CGTP_F32 = 0, CGTP_F64 = 1 } cgtp_dtype;
+
+/* One path: in1 block i_in1 (x) in2 block i_in2 -> output irrep irreps_out[i_out]. */
+typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
+
+/*
+ * cgtp_plan_create -- parse irreps, enumerate paths, compute the CG blocks and
+ * upload the per-plan tables.  ("An Efficient Sparse Kernel Generator ...",
+ * Abstract: static analysis at model compile time; Figures 1-2: the
+ * block-sparse coefficient tensor.)
+ *
+ *  irreps_in1, irreps_in2, irreps_out : strings "MULxLP+..." (P = e|o, l <= 7).
+ *      in2 blocks must have multiplicity 1 (spherical-harmonic edge features).
+ *  instr, n_instr : explicit paths, or NULL/0 for every path allowed by the
+ *      triangle and parity rules whose (l3, p3) occurs in irreps_out, ordered
+ *      i_in1, then i_in2, then l3 ascending.
+ *  mode : CGTP_UVU (weights [paths, mul1] per edge; each path writes its own
+ *      output block of multiplicity mul1, appended in path order -- the muls of
+ *      irreps_out are ignored) or CGTP_UVW (fully connected mixing into the
+ *      blocks of irreps_out).
+ *  dtype : CGTP_F32 or CGTP_F64 (CGTP_UVW supports CGTP_F32 only).
+ *  radial_k : 0 for uvu; for uvw the number K of radial functions (1..16); the
+ *      weights are then W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
+ * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
+ * the streaming node stage.  Must be called with the target device current.
+ */
+cgtp_status cgtp_plan_create(cgtp_plan* plan, const char* irreps_in1, const char* irreps_in2,
+                             const char* irreps_out, const cgtp_instr* instr, int n_instr,
+                             int mode, int dtype, int radial_k);
+void cgtp_plan_destroy(cgtp_plan plan);
+
+/* Sizes of one row: d1 = dim(in1), d2 = dim(in2), d_out = dim(out), w_numel =
+ * weights of one edge (uvu) or of one radial row of M (uvw). Any pointer may be NULL. */
+cgtp_status cgtp_plan_info(cgtp_plan plan, int64_t* d1, int64_t* d2, int64_t* d_out,
+                           int64_t* w_numel, int* n_paths);
+
+/* Host copy of path `p`: ints[0..9] = l1, l2, l3, mul1, mul_out, off1, off2, ooff,
+ * woff, i_out and the dense real CG block C[m1][m2][m3] (FP64) of
+ * (2l1+1)(2l2+1)(2l3+1) entries into `block` (capacity in doubles). */
+cgtp_status cgtp_plan_path(cgtp_plan plan, int p, int* ints10, double* block, int64_t capacity);
+
+/*
+ * cgtp_forward -- batched tensor product without a graph ("An Efficient Sparse
+ * Kernel Generator ...", Figure 4A): out[b] = TP(x1[b], x2[b]; W[b]).
+ *  x1 [B, d1], x2 [B, d2], W [B, w_numel] -> out [B, d_out].  uvu plans only.
+ */
+cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const void* W, void* out,
+                         int64_t B, void* stream);
+
+/* Adjoint of cgtp_forward: gout [B, d_out] -> gx1 [B,d1], gx2 [B,d2], gW [B,w_numel]. */
+cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, const void* x2,
+                          const void* W, void* gx1, void* gx2, void* gW, int64_t B, void* stream);
+
+/*
+ * cgtp_graph_create -- validate a receiver-sorted CSR edge list and build the
+ * sender transpose on the device ("An Efficient Sparse Kernel Generator ...",
+ * Figure 4B: messages are summed into the receiving node).
+ *  rowptr [N+1], col [E] : DEVICE int32 arrays; rowptr monotone, rowptr[0]=0,
+ *      rowptr[N]=E, 0 <= col < N.  Self-loops and repeated edges are allowed.
+ *  The graph keeps the two pointers (the caller must keep them alive and
+ *  unchanged while the graph is used) and owns t_rowptr [N+1], t_eid [E]
+ *  (CSR positions ordered by sender, ties in CSR order) and t_dst [E].
+ *  Synchronises `stream` once to read the validation result.  Limits:
+ *  N, E < 2^31; a sender may have at most 32768 out-edges (CGTP_EUNSUPPORTED).
+ */
+cgtp_status cgtp_graph_create(cgtp_graph* graph, const int32_t* rowptr, const int32_t* col,
+                              int64_t N, int64_t E, void* stream);
+void cgtp_graph_destroy(cgtp_graph graph);
+
+/* Device-to-device copy of the transpose arrays (any pointer may be NULL). */
+cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t_eid,
+                                 int32_t* t_dst, void* stream);
+
+/*
+ * cgtp_conv_forward -- fused CG tensor product + receiver sum.
+ *  uvu: x [N,d1], Y [E,d2], W_or_R = W [E,w_numel], M = NULL -> out [N,d_out].
+ *  uvw: W_or_R = R [E,K], M [K,w_numel] -> out [N,d_out]; per-edge weights
+ *       are never formed; node state is streamed through bounded scratch
+ *       owned by the plan ("Sobek ...", Abstract).
+ *  Receivers own their accumulation; no atomics; empty rows give zeros.
+ */
+cgtp_status cgtp_conv_forward(cgtp_plan plan, cgtp_graph graph, const void* x, const void* Y,
+                              const void* W_or_R, const void* M, void* out, void* stream);
+
+/*
+ * cgtp_conv_backward -- adjoint of cgtp_conv_forward for an output gradient gout [N,d_out]:
+ *  gx [N,d1] (sender-owned, summed over each sender's out-edges), gY [E,d2],
+ *  uvu: gW_or_gR = gW [E,w_numel], gM = NULL;
+ *  uvw: gW_or_gR = gR [E,K], gM [K,w_numel] (deterministic ordered reduction).
+ */
+cgtp_status cgtp_conv_backward(cgtp_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                               const void* Y, const void* W_or_R, const void* M, void* gx, void* gY,
+                               void* gW_or_gR, void* gM, void* stream);
+
+/* Host only (no device needed): the planner's real-basis, component-normalised
+ * CG block of (l1, l2, l3), l <= 7, as (2l1+1)(2l2+1)(2l3+1) doubles in
+ * [m1][m2][m3] order; zeros if the triangle rule fails.  Same routine the plan
+ * tables are built from ("An Efficient Sparse Kernel Generator ...", Figure 2:
+ * the coefficient blocks). */
+cgtp_status cgtp_real_cg_block(int l1, int l2, int l3, double* block, int64_t capacity);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* cgtp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CGTP_H */

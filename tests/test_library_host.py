@@ -1,0 +1,88 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+* libcgtp.so loads and exports every function declared in include/cgtp.h;
+* the planner's real CG blocks (an independent C++ Racah implementation) agree
+  with the oracle's to 1e-14 for every (l1, l2, l3) with l <= 7;
+* argument checks that fail before any device work.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import clebsch_gordan_tensor_racah_gb300 as cg
+from oracle import cg as ocg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cgtp.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cgtp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(cg.EXPORTS)
+
+
+def test_library_loads_and_exports_every_symbol():
+    L = cg.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_planner_cg_blocks_match_oracle():
+    worst = 0.0
+    for l1 in range(8):
+        for l2 in range(8):
+            for l3 in range(0, 8):
+                a = cg.cgtp_real_cg_block(l1, l2, l3)
+                b = ocg.real_cg_block(l1, l2, l3)
+                worst = max(worst, float(np.abs(a - b).max()))
+    assert worst < 1e-14
+
+
+def test_real_cg_block_rejects_bad_l():
+    with pytest.raises(cg.CgtpError) as e:
+        cg.cgtp_real_cg_block(8, 0, 8)
+    assert e.value.status == cg.CGTP_EINVAL
+
+
+def test_plan_create_rejects_bad_arguments_before_device_work():
+    L = cg.lib()
+    h = ctypes.c_void_p()
+    cases = [
+        (b"8x0e+", b"0e", b"0e", 0, 0, 0, cg.CGTP_EINVAL),      # empty term
+        (b"8x0q", b"0e", b"0e", 0, 0, 0, cg.CGTP_EINVAL),       # bad parity letter
+        (b"8x9e", b"0e", b"9e", 0, 0, 0, cg.CGTP_EINVAL),       # l > 7
+        (b"8x0e", b"2x0e", b"0e", 0, 0, 0, cg.CGTP_EUNSUPPORTED),  # in2 multiplicity
+        (b"8x0e", b"0e", b"0e", 0, 0, 3, cg.CGTP_EINVAL),       # radial_k in uvu
+        (b"8x0e", b"0e", b"0e", 1, 1, 8, cg.CGTP_EUNSUPPORTED),  # uvw FP64
+        (b"8x0e", b"0e", b"0e", 7, 0, 0, cg.CGTP_EINVAL),       # bad mode
+        (b"8x1o", b"1o", b"1o", 0, 0, 0, cg.CGTP_EINVAL),       # no parity-allowed path
+    ]
+    for in1, in2, out, mode, dt, k, want in cases:
+        st = L.cgtp_plan_create(ctypes.byref(h), in1, in2, out, None, 0, mode, dt, k)
+        assert st == want, (in1, in2, out, st, L.cgtp_last_error())
+        assert not h.value
+
+
+def test_forbidden_instruction_rejected():
+    L = cg.lib()
+    h = ctypes.c_void_p()
+    ins = (ctypes.c_int * 3)(0, 0, 0)          # 1o x 1o -> 1o violates parity
+    st = L.cgtp_plan_create(ctypes.byref(h), b"4x1o", b"1o", b"1o+1e", ctypes.cast(ins, ctypes.c_void_p),
+                            1, 0, 0, 0)
+    assert st == cg.CGTP_EINVAL
+    assert b"parity" in L.cgtp_last_error()
+
+
+def test_null_handles_rejected():
+    L = cg.lib()
+    assert L.cgtp_conv_forward(None, None, None, None, None, None, None, None) == cg.CGTP_EINVAL
+    assert L.cgtp_forward(None, None, None, None, None, 0, None) == cg.CGTP_EINVAL
+    assert L.cgtp_plan_info(None, None, None, None, None, None) == cg.CGTP_EINVAL
