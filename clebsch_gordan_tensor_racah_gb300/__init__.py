@@ -32,7 +32,7 @@ CGTP_F32, CGTP_F64 = 0, 1
 EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan_path",
            "cgtp_forward", "cgtp_backward", "cgtp_graph_create", "cgtp_graph_destroy",
            "cgtp_graph_transpose", "cgtp_conv_forward", "cgtp_conv_backward",
-           "cgtp_real_cg_block", "cgtp_last_error"]
+           "cgtp_real_cg_block", "cgtp_last_error", "cgtp_graph_transpose_noalloc"]
 
 
 class CgtpError(RuntimeError):
@@ -69,6 +69,7 @@ def lib():
         L.cgtp_conv_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.cgtp_conv_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.cgtp_real_cg_block.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_double), i64]
+        L.cgtp_graph_transpose_noalloc.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
         for name in EXPORTS:
             if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
                 getattr(L, name).restype = i32

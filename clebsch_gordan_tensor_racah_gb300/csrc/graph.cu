@@ -16,7 +16,10 @@
 // binary search of rowptr.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
+#include <mutex>
+#include <string>
 
 #include "internal.h"
 
@@ -226,3 +229,99 @@ cgtp_status graph_build(cgtp_graph_s* g, void* stream) {
 }
 
 }  // namespace cgtp
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the transpose build.
+//
+// Some callers cannot call cudaMalloc at the point where they need the
+// transpose: their framework owns all device memory through its own pool and
+// forbids raw allocations, or they run under a fixed device-memory budget
+// reserved at start-up, or they cannot afford the device-wide synchronisation
+// an allocation may imply.  This entry point writes the transpose into arrays
+// the caller provides and takes its working memory (validation flag, degree
+// counts / cursors, scan tile sums) from the file-scope array below, which
+// every GPU that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace cgtp {
+namespace {
+constexpr int64_t kNoAllocMaxN = int64_t(1) << 20;   // largest node count accepted
+constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + 1 + kScanTile - 1) / kScanTile;
+constexpr int64_t kNoAllocWords = 2 + (kNoAllocMaxN + 1) + kNoAllocTiles;  // ~4 MiB of int32
+
+static __device__ __align__(256) int g_transpose_scratch[kNoAllocWords];
+
+// Device address of g_transpose_scratch per device, looked up once with that
+// device current (in host code the symbol name is only a host-side stand-in).
+constexpr int kMaxDevices = 64;
+int* g_scratch_addr[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mu;
+
+cgtp_status scratch_for_current_device(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(CGTP_ECUDA, "no current CUDA device");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    int* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_transpose_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(CGTP_ECUDA, std::string("cudaGetSymbolAddress(transpose scratch): ") + cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return CGTP_OK;
+}
+}  // namespace
+}  // namespace cgtp
+
+extern "C" cgtp_status cgtp_graph_transpose_noalloc(const int32_t* rowptr, const int32_t* col,
+                                                    int64_t N, int64_t E, int32_t* t_rowptr,
+                                                    int32_t* t_eid, int32_t* t_dst, void* stream) {
+  using namespace cgtp;
+  clear_error();
+  if (N < 1 || N > kNoAllocMaxN)
+    return fail(CGTP_EINVAL, "cgtp_graph_transpose_noalloc: N must be in [1, 1048576]");
+  if (E < 0 || E >= (int64_t(1) << 31)) return fail(CGTP_EINVAL, "E must be in [0, 2^31)");
+  if (!rowptr || !t_rowptr) return fail(CGTP_EINVAL, "null rowptr or t_rowptr");
+  if (E > 0 && (!col || !t_eid || !t_dst)) return fail(CGTP_EINVAL, "null col, t_eid or t_dst");
+  int* scratch = nullptr;
+  cgtp_status s = scratch_for_current_device(&scratch);
+  if (s != CGTP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n = static_cast<int>(N), e = static_cast<int>(E);
+  const int ntiles = (n + 1 + kScanTile - 1) / kScanTile;
+  int* flag = scratch;
+  int* total = scratch + 1;
+  int* counts = scratch + 2;
+  int* sums = counts + (n + 1);
+  // the array keeps the previous call's contents: clear flag, total, counts and sums
+  const size_t words = 2 + static_cast<size_t>(n + 1) + ntiles;
+  if (cudaMemsetAsync(scratch, 0, words * sizeof(int), st) != cudaSuccess)
+    return fail(CGTP_ECUDA, "clearing the transpose scratch failed");
+  const int threads = 256;
+  auto blocks = [](int64_t k) { return static_cast<int>(std::min<int64_t>((k + 255) / 256, 4096)); };
+  csr_check_kernel<<<std::max(1, blocks(std::max(n + 1, e))), threads, 0, st>>>(rowptr, col, n, e, flag);
+  int hflag = 0;
+  cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, st);
+  cudaError_t err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph check: ") + cudaGetErrorString(err));
+  if (hflag) return fail(CGTP_EGRAPH, "invalid CSR (rowptr not a monotone prefix of E, or col out of range)");
+  if (e > 0) histogram_kernel<<<blocks(e), threads, 0, st>>>(col, e, counts);
+  scan_tiles_kernel<<<ntiles, 256, 0, st>>>(counts, n + 1, t_rowptr, sums);
+  scan_sums_kernel<<<1, 32, 0, st>>>(sums, ntiles, total);
+  add_offsets_kernel<<<blocks(n + 1), threads, 0, st>>>(t_rowptr, n + 1, sums);
+  if (e > 0) {
+    cudaMemcpyAsync(counts, t_rowptr, sizeof(int) * (n + 1), cudaMemcpyDeviceToDevice, st);
+    scatter_kernel<<<blocks(e), threads, 0, st>>>(col, e, counts, t_eid);
+    sort_short_kernel<<<std::max(1, std::min((n + 3) / 4, 4096)), 128, 0, st>>>(t_rowptr, n, t_eid, flag);
+    const size_t lsm = kSortBlock * sizeof(int);
+    cudaFuncSetAttribute(sort_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsm);
+    sort_long_kernel<<<std::max(1, std::min(n, 1024)), 1024, lsm, st>>>(t_rowptr, n, t_eid);
+    dst_kernel<<<blocks(e), threads, 0, st>>>(rowptr, n, t_eid, e, t_dst);
+  }
+  cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, st);
+  err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph transpose: ") + cudaGetErrorString(err));
+  if (hflag & kTooLong) return fail(CGTP_EUNSUPPORTED, "a sender has more than 32768 out-edges");
+  return CGTP_OK;
+}

@@ -126,6 +126,31 @@ cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t
                                  int32_t* t_dst, void* stream);
 
 /*
+ * cgtp_graph_transpose_noalloc -- the sender transpose of cgtp_graph_create,
+ * built without allocating any device memory.  The paper has no counterpart.
+ *
+ *  For callers that may not call cudaMalloc where they need the transpose
+ *  (their framework hands out all device memory from its own pool, they run
+ *  under a device-memory budget fixed at start-up, or they cannot accept the
+ *  device-wide synchronisation an allocation can cause).
+ *  rowptr [N+1], col [E] : DEVICE int32 CSR, as for cgtp_graph_create.
+ *  t_rowptr [N+1], t_eid [E], t_dst [E] : DEVICE int32 outputs owned by the
+ *      caller, filled exactly as cgtp_graph_transpose would fill them.
+ *  Working memory is a fixed ~4 MiB array inside the library that every GPU
+ *  which loads the library keeps until the process exits; N above 1,048,576
+ *  is rejected with CGTP_EINVAL.  The first call on a device looks up that
+ *  array's device address (with the device current) -- make that first call
+ *  before any stream capture.  All calls on a device share the one array and
+ *  clear it before use: calls whose work overlaps on the GPU (different
+ *  streams or threads, same device) race and must be serialised by the caller.
+ *  Synchronises `stream` twice (validation flag, long-segment flag).  Errors
+ *  as cgtp_graph_create.
+ */
+cgtp_status cgtp_graph_transpose_noalloc(const int32_t* rowptr, const int32_t* col, int64_t N,
+                                         int64_t E, int32_t* t_rowptr, int32_t* t_eid,
+                                         int32_t* t_dst, void* stream);
+
+/*
  * cgtp_conv_forward -- fused CG tensor product + receiver sum.
  *  uvu: x [N,d1], Y [E,d2], W_or_R = W [E,w_numel], M = NULL -> out [N,d_out].
  *  uvw: W_or_R = R [E,K], M [K,w_numel] -> out [N,d_out]; per-edge weights
