@@ -1,12 +1,939 @@
-// uvw.cu -- placeholder, replaced by the streaming uvw radial convolution.
+// uvw.cu -- fully connected (uvw) CG tensor-product convolution with radial
+// weights, streamed through bounded node state.
+//
+// "Sobek: Streaming Equivariant Tensor Product Convolutions", Abstract: the
+// edge-specific weights, messages and adjoints of the conventional schedule are
+// artefacts; reassociating radial projection, spherical-harmonic coupling and
+// aggregation lets edge-local products be consumed into bounded receiver-side
+// state, through forward and backward, keeping fully connected multiplicity
+// mixing.  With W_e[path,u,w] = sum_k R[e,k] M[k,path,u,w] (never formed):
+//
+// forward, per receiver n (edge stage, one CTA per receiver, state in shared memory):
+//   S[n][k,path,u,m3] = sum_{e in row n} R[e,k] sum_m1 cy_e[path][m1,m3] x[src][u,m1]
+// then a node GEMM over a chunk of receivers (M shared by all nodes):
+//   out[n][i_out][w,m3] = sum_{path -> i_out} sum_{k,u} M[k,path,u,w] S[n][k,path,u,m3]
+//
+// backward, sender-owned over the transpose (no scatter, no atomics):
+//   A[s][k,path,w,m1]  = sum_u x[s][u,m1] M[k,path,u,w]                  (node GEMM)
+//   per out-edge e = (s -> d):  p_e[path,w,m1] = sum_m3 cy_e[m1,m3] g[d][w,m3]
+//     H[s][k,path,w,m1] += R[e,k] p_e
+//     gR[e,k]  = sum A[s][k] . p_e
+//     gY[e][m2] = sum_path sum C[m1,m2,m3] (sum_w (sum_k R[e,k] A[s][k,path,w,m1]) g[d][w,m3])
+//   gx[s][u,m1] = sum_{k,path,w} M[k,path,u,w] H[s][k,path,w,m1]             (node GEMM)
+//   gM[k,path,u,w] += sum_{s,m1} x[s][u,m1] H[s][k,path,w,m1]   (per chunk, chunks in order)
+//
+// Node state lives in a scratch buffer owned by the plan and sized by a fixed
+// node chunk (not by the graph): the working set is bounded whatever E is.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
 #include "internal.h"
+#include "uvu_impl.cuh"
+
 namespace cgtp {
-cgtp_status uvw_create(cgtp_plan_s*) { return fail(CGTP_EUNSUPPORTED, "uvw not built yet"); }
-void uvw_destroy(cgtp_plan_s*) {}
-cgtp_status uvw_forward(const cgtp_plan_s*, const cgtp_graph_s*, const void*, const void*, const void*,
-                        const void*, void*, void*) { return fail(CGTP_EUNSUPPORTED, "uvw"); }
-cgtp_status uvw_backward(const cgtp_plan_s*, const cgtp_graph_s*, const void*, const void*, const void*,
-                         const void*, const void*, void*, void*, void*, void*, void*) {
-  return fail(CGTP_EUNSUPPORTED, "uvw");
+namespace uvw_detail {
+
+using uvu_detail::pad_up;
+using uvu_detail::reduce_outer;
+using uvu_detail::V16;
+
+constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (CGTP_UVW_CHUNK_NODES overrides)
+constexpr int kEdgeChunk = 16;      // edges staged per step of the edge stages
+constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
+constexpr int kBwdChunk = 8;        // edges staged per step of the backward edge stage
+
+struct UvwPath {
+  int l1, l2, l3, D1, D2, D3, mul1, mul_out;
+  int off1, off2, ooff, woff;
+  int soff;      // offset of [u][m3] (fwd state) inside one radial slice of a node's state
+  int aoff;      // offset of [w][m1] (bwd state) inside one radial slice
+  int cyoff;     // per-edge cy layout offset
+  int i1, io;
+};
+
+struct GemmSeg {
+  long long a_off, b_off;
+  int K;        // <0: use the launch's node count
+  int a_k, b_k;
+  int pad_;
+};
+
+struct GemmProb {
+  int a_base, b_base, c_base;  // which launch pointer
+  int Nn;                      // rows = Nn * D (Nn < 0: the launch's node count)
+  int D, J;
+  long long a_off, a_n, a_m;
+  int b_j, c_j;
+  long long c_off, c_n, c_m;
+  int beta;                    // 0 overwrite, 1 accumulate
+  int seg0, seg1;
+  int pad_;
+};
+
+struct UvwState {
+  std::vector<UvwPath> paths_h;
+  UvwPath* paths = nullptr;
+  int n_paths = 0;
+  int K = 0;
+  int s_slice = 0, a_slice = 0;  // elements of one radial slice of the node state
+  int s_node = 0, a_node = 0;    // K * slice
+  int chunk_nodes = kChunkNodes;
+  float* scratch = nullptr;      // [2][chunk_nodes][s_node]
+  size_t scratch_elems = 0;
+  // GEMM descriptor tables (device) per use
+  GemmProb* fwd_probs = nullptr;  int fwd_np = 0;  GemmSeg* fwd_segs = nullptr;
+  GemmProb* pre_probs = nullptr;  int pre_np = 0;  GemmSeg* pre_segs = nullptr;
+  GemmProb* gx_probs = nullptr;   int gx_np = 0;   GemmSeg* gx_segs = nullptr;
+  GemmProb* gm_probs = nullptr;   int gm_np = 0;   GemmSeg* gm_segs = nullptr;
+  void* tables = nullptr;
+  size_t smem_fwd = 0, smem_bwd = 0;
+};
+
+// ---------------------------------------------------------------------------
+// grouped SIMT GEMM:  C[(n,m), j] (+)= sum_seg sum_k A[(n,m), k] B[k, j]
+// ---------------------------------------------------------------------------
+constexpr int kGT = 64;   // tile rows and columns
+constexpr int kGK = 32;   // k per stage
+
+struct GemmLaunch {
+  const float* ptr[6];
+  int nodes;  // node count of this launch (chunk)
+  int nprob;
+  const GemmProb* probs;
+  const GemmSeg* segs;
+};
+
+__global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
+  __shared__ __align__(16) float As[kGK][kGT];
+  __shared__ __align__(16) float Bs[kGK][kGT];
+  // locate this CTA's problem and tile
+  int tile = blockIdx.x, pi = 0;
+  int rt = 0, ct = 0;
+  GemmProb P;
+  for (pi = 0; pi < L.nprob; ++pi) {
+    P = L.probs[pi];
+    const int Nn = P.Nn < 0 ? L.nodes : P.Nn;
+    const int rows = Nn * P.D;
+    const int ntr = (rows + kGT - 1) / kGT, ntc = (P.J + kGT - 1) / kGT;
+    if (tile < ntr * ntc) {
+      rt = tile / ntc;
+      ct = tile - rt * ntc;
+      break;
+    }
+    tile -= ntr * ntc;
+  }
+  if (pi >= L.nprob) return;
+  const int Nn = P.Nn < 0 ? L.nodes : P.Nn;
+  const int rows = Nn * P.D;
+  const float* A = L.ptr[P.a_base];
+  const float* B = L.ptr[P.b_base];
+  float* C = const_cast<float*>(L.ptr[P.c_base]);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = rt * kGT, c0 = ct * kGT;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int s = P.seg0; s < P.seg1; ++s) {
+    const GemmSeg S = L.segs[s];
+    const int K = S.K < 0 ? L.nodes : S.K;
+    for (int k0 = 0; k0 < K; k0 += kGK) {
+      for (int i = threadIdx.x; i < kGK * kGT; i += 256) {
+        const int kk = i / kGT, rr = i - kk * kGT;
+        const int r = r0 + rr, k = k0 + kk;
+        float v = 0.f;
+        if (r < rows && k < K) {
+          const int n = r / P.D, m = r - n * P.D;
+          v = A[P.a_off + S.a_off + n * P.a_n + m * P.a_m + (long long)k * S.a_k];
+        }
+        As[kk][rr] = v;
+        const int cc = rr, c = c0 + cc;
+        float b = 0.f;
+        if (c < P.J && k < K) b = B[S.b_off + (long long)k * S.b_k + (long long)c * P.b_j];
+        Bs[kk][cc] = b;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < kGK; ++kk) {
+        const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+        const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty * 4 + i;
+    if (r >= rows) continue;
+    const int n = r / P.D, m = r - n * P.D;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + tx * 4 + j;
+      if (c >= P.J) continue;
+      float* dst = C + P.c_off + n * P.c_n + m * P.c_m + (long long)c * P.c_j;
+      *dst = P.beta ? *dst + acc[i][j] : acc[i][j];
+    }
+  }
 }
+
+// ---------------------------------------------------------------------------
+// forward edge stage: S[n] for the receivers of one chunk
+// ---------------------------------------------------------------------------
+struct EdgeArgs {
+  const float* x;
+  const float* Y;
+  const float* R;
+  const float* g;      // backward: output gradient
+  const float* Astate; // backward: A chunk
+  float* state;        // fwd: S chunk; bwd: H chunk
+  float* gY;
+  float* gR;
+  const int* rowptr;   // fwd: CSR; bwd: transpose
+  const int* col;      // fwd: CSR col; bwd: t_eid
+  const int* t_dst;
+  int n0, n1;          // node range of this chunk
+  int d1, d2, d_out, K;
+  int s_node, s_slice;
+  const UvwPath* paths;
+  const GroupDev* group;
+  const int* cy_begin;
+  const int* cy_col;
+  const float* cy_coef;
+  const int* gy_begin;
+  const int* gy_slot;
+  const int* gy_nub;
+  const float* gy_coef;
+  const int* item_begin;
+  const Item* items;
+};
+
+template <int D1, int D3>
+__device__ __noinline__ void fwd_state_item(const float* __restrict__ x, int d1, int off1, int cyoff,
+                                            int soff, int s_slice, int K, int u, int cnt,
+                                            const int* src_s, const float* Rs, const float* cys,
+                                            int cy_size, float* Ss) {
+  using V = float4;
+  constexpr int NF = D1 * D3;
+  constexpr int NV = (NF + 3) / 4;
+  for (int kb = 0; kb < K; kb += kKB) {
+    float acc[kKB][D3];
+#pragma unroll
+    for (int k = 0; k < kKB; ++k)
+#pragma unroll
+      for (int m = 0; m < D3; ++m) acc[k][m] = 0.f;
+    for (int j = 0; j < cnt; ++j) {
+      const float* xr = x + (size_t)src_s[j] * d1 + off1 + u * D1;
+      float xv[D1];
+#pragma unroll
+      for (int m = 0; m < D1; ++m) xv[m] = __ldg(xr + m);
+      float t[D3];
+#pragma unroll
+      for (int m = 0; m < D3; ++m) t[m] = 0.f;
+      const V* c = reinterpret_cast<const V*>(cys + j * cy_size + cyoff);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const V cv = c[v];
+        const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int f = v * 4 + q;
+          if (f < NF) t[f % D3] += cs[q] * xv[f / D3];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        const float r = (kb + k < K) ? Rs[j * 16 + kb + k] : 0.f;
+#pragma unroll
+        for (int m = 0; m < D3; ++m) acc[k][m] += r * t[m];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kKB; ++k) {
+      if (kb + k >= K) break;
+      float* sp = Ss + (kb + k) * s_slice + soff + u * D3;
+#pragma unroll
+      for (int m = 0; m < D3; ++m) sp[m] += acc[k][m];
+    }
+  }
+}
+
+#define UVW_CASES(M)                                                                       \
+  M(0, 0) M(0, 1) M(0, 2) M(0, 3) M(1, 0) M(1, 1) M(1, 2) M(1, 3) M(2, 0) M(2, 1) M(2, 2) \
+  M(2, 3) M(3, 0) M(3, 1) M(3, 2) M(3, 3)
+
+#define UVW_FWD_CASE(L1, L3)                                                                     \
+  case (L1)*8 + (L3):                                                                            \
+    fwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(a.x, a.d1, p.off1, p.cyoff, p.soff, a.s_slice, a.K, \
+                                                u, cnt, src_s, Rs, cys, cy_size, Ss);              \
+    break;
+
+__global__ void __launch_bounds__(kThreads) uvw_fwd_edge_kernel(const EdgeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const GroupDev g = *a.group;
+  const int cy_size = g.cy_size;
+  const int d2p = pad_up(a.d2, 4);
+  float* Ss = reinterpret_cast<float*>(smem);
+  float* Ys = Ss + pad_up(a.s_node, 4);
+  float* Rs = Ys + kEdgeChunk * d2p;
+  float* cys = Rs + kEdgeChunk * 16;
+  int* src_s = reinterpret_cast<int*>(cys + kEdgeChunk * cy_size);
+  const int ib = a.item_begin[g.item_base + warp], ie = a.item_begin[g.item_base + warp + 1];
+  for (int n = a.n0 + blockIdx.x; n < a.n1; n += gridDim.x) {
+    const int e_begin = a.rowptr[n], e_end = a.rowptr[n + 1];
+    __syncthreads();
+    for (int i = tid; i < a.s_node; i += kThreads) Ss[i] = 0.f;
+    for (int e0 = e_begin; e0 < e_end; e0 += kEdgeChunk) {
+      const int cnt = min(kEdgeChunk, e_end - e0);
+      __syncthreads();
+      for (int i = tid; i < cnt; i += kThreads) src_s[i] = a.col[e0 + i];
+      for (int i = tid; i < cnt * a.d2; i += kThreads) {
+        const int j = i / a.d2, c = i - j * a.d2;
+        Ys[j * d2p + c] = a.Y[(size_t)(e0 + j) * a.d2 + c];
+      }
+      for (int i = tid; i < cnt * a.K; i += kThreads) {
+        const int j = i / a.K, k = i - j * a.K;
+        Rs[j * 16 + k] = a.R[(size_t)(e0 + j) * a.K + k];
+      }
+      __syncthreads();
+      for (int i = tid; i < cnt * cy_size; i += kThreads) {
+        const int j = i / cy_size, s = i - j * cy_size;
+        const int t0 = a.cy_begin[g.cy_base + s], t1 = a.cy_begin[g.cy_base + s + 1];
+        float v = 0.f;
+        for (int t = t0; t < t1; ++t) v += a.cy_coef[t] * Ys[j * d2p + a.cy_col[t]];
+        cys[i] = v;
+      }
+      __syncthreads();
+      for (int it = ib; it < ie; ++it) {
+        const Item item = a.items[it];
+        const UvwPath p = a.paths[item.path];
+        const int u = item.u0 + lane;
+        if (u >= p.mul1) continue;
+        switch (p.l1 * 8 + p.l3) { UVW_CASES(UVW_FWD_CASE) default: break; }
+      }
+    }
+    __syncthreads();
+    float* dst = a.state + (size_t)(n - a.n0) * a.s_node;
+    for (int i = tid; i < a.s_node; i += kThreads) dst[i] = Ss[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward edge stage (sender-owned)
+// ---------------------------------------------------------------------------
+// Sum eight values over the 32 lanes; lane l ends with the total of value
+// (l >> 2) & 7.
+__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int o = 16, n = 8; o >= 4; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i < n / 2) {
+        const float send = up ? v[i] : v[i + n / 2];
+        const float keep = up ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+  }
+  float r = v[0];
+  r += __shfl_xor_sync(0xffffffffu, r, 2);
+  r += __shfl_xor_sync(0xffffffffu, r, 1);
+  return r;
+}
+
+template <int D1, int D3>
+__device__ __noinline__ void bwd_state_item(int ooff, int cyoff, int aoff, int a_slice, int K,
+                                            int w0, int lane, int mul_out, int cnt,
+                                            const float* gs, int d_out_s, const float* Rs,
+                                            const float* cys, int cy_size, const float* As,
+                                            float* Hs, float* gcp, int nub, float* gRp,
+                                            int item_slot, int n_item_slots) {
+  using V = float4;
+  constexpr int NF = D1 * D3;
+  constexpr int NV = (NF + 3) / 4;
+  const int w = w0 + lane;
+  const bool active = w < mul_out;
+  const int wb = w0 >> 5;
+  for (int kb = 0; kb < K; kb += kKB) {
+    float hacc[kKB][D1];
+#pragma unroll
+    for (int k = 0; k < kKB; ++k)
+#pragma unroll
+      for (int m = 0; m < D1; ++m) hacc[k][m] = 0.f;
+    for (int j = 0; j < cnt; ++j) {
+      float gv[D3];
+      const float* gr = gs + j * d_out_s + ooff + w * D3;
+#pragma unroll
+      for (int m = 0; m < D3; ++m) gv[m] = active ? gr[m] : 0.f;
+      float pe[D1];
+#pragma unroll
+      for (int m = 0; m < D1; ++m) pe[m] = 0.f;
+      const V* c = reinterpret_cast<const V*>(cys + j * cy_size + cyoff);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const V cv = c[v];
+        const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int f = v * 4 + q;
+          if (f < NF) pe[f / D3] += cs[q] * gv[f % D3];
+        }
+      }
+      float gr8[kKB];
+      float ar[D1];
+#pragma unroll
+      for (int m = 0; m < D1; ++m) ar[m] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        const bool kin = kb + k < K;
+        const float r = kin ? Rs[j * 16 + kb + k] : 0.f;
+        float dot = 0.f;
+        const float* ap = As + (kin ? (kb + k) : 0) * a_slice + aoff + w * D1;
+#pragma unroll
+        for (int m = 0; m < D1; ++m) {
+          const float av = (active && kin) ? ap[m] : 0.f;
+          dot += av * pe[m];
+          ar[m] += r * av;
+          hacc[k][m] += r * pe[m];
+        }
+        gr8[k] = dot;
+      }
+      // gR partial of this item and edge: sum over the lanes (w)
+      const float tot = reduce8(gr8, lane);
+      if ((lane & 3) == 0) gRp[(j * n_item_slots + item_slot) * kKB + ((lane >> 2) & 7)] = tot;
+      // gc[m1][m3] = sum_w ar[w][m1] g[w][m3]
+      reduce_outer<float, D1, D3>(ar, gv, gcp + (j * nub + wb) * cy_size + cyoff, lane);
+    }
+    if (active) {
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        if (kb + k >= K) break;
+        float* hp = Hs + (kb + k) * a_slice + aoff + w * D1;
+#pragma unroll
+        for (int m = 0; m < D1; ++m) hp[m] += hacc[k][m];
+      }
+    }
+  }
+}
+
+#define UVW_BWD_CASE(L1, L3)                                                                     \
+  case (L1)*8 + (L3):                                                                            \
+    bwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(p.ooff, p.cyoff, p.aoff, a.s_slice, a.K, item.u0,  \
+                                                lane, p.mul_out, cnt, gs, a.d_out, Rs, cys,       \
+                                                cy_size, As, Hs, gcp, nub, gRp, it - items0,      \
+                                                n_items);                                         \
+    break;
+
+__global__ void __launch_bounds__(kThreads) uvw_bwd_edge_kernel(const EdgeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const GroupDev g = *a.group;
+  const int cy_size = g.cy_size, nub = g.nub;
+  const int d2p = pad_up(a.d2, 4);
+  const int items0 = a.item_begin[g.item_base];
+  const int n_items = a.item_begin[g.item_base + kWarps] - items0;
+  float* As = reinterpret_cast<float*>(smem);
+  float* Hs = As + pad_up(a.s_node, 4);
+  float* gs = Hs + pad_up(a.s_node, 4);
+  float* Ys = gs + kBwdChunk * a.d_out;
+  float* Rs = Ys + kBwdChunk * d2p;
+  float* cys = Rs + kBwdChunk * 16;
+  float* gcp = cys + kBwdChunk * cy_size;            // [chunk][nub][cy_size]
+  float* gRp = gcp + kBwdChunk * nub * cy_size;      // [chunk][items][8]
+  int* eid_s = reinterpret_cast<int*>(gRp + kBwdChunk * n_items * kKB);
+  int* dst_s = eid_s + kBwdChunk;
+  const int ib = a.item_begin[g.item_base + warp], ie = a.item_begin[g.item_base + warp + 1];
+  for (int s = a.n0 + blockIdx.x; s < a.n1; s += gridDim.x) {
+    const int e_begin = a.rowptr[s], e_end = a.rowptr[s + 1];
+    __syncthreads();
+    const float* Asrc = a.Astate + (size_t)(s - a.n0) * a.s_node;
+    for (int i = tid; i < a.s_node; i += kThreads) {
+      As[i] = Asrc[i];
+      Hs[i] = 0.f;
+    }
+    for (int e0 = e_begin; e0 < e_end; e0 += kBwdChunk) {
+      const int cnt = min(kBwdChunk, e_end - e0);
+      __syncthreads();
+      for (int i = tid; i < cnt; i += kThreads) {
+        eid_s[i] = a.col[e0 + i];
+        dst_s[i] = a.t_dst[e0 + i];
+      }
+      __syncthreads();
+      for (int i = tid; i < cnt * a.d_out; i += kThreads) {
+        const int j = i / a.d_out, c = i - j * a.d_out;
+        gs[i] = a.g[(size_t)dst_s[j] * a.d_out + c];
+      }
+      for (int i = tid; i < cnt * a.d2; i += kThreads) {
+        const int j = i / a.d2, c = i - j * a.d2;
+        Ys[j * d2p + c] = a.Y[(size_t)eid_s[j] * a.d2 + c];
+      }
+      for (int i = tid; i < cnt * a.K; i += kThreads) {
+        const int j = i / a.K, k = i - j * a.K;
+        Rs[j * 16 + k] = a.R[(size_t)eid_s[j] * a.K + k];
+      }
+      __syncthreads();
+      for (int i = tid; i < cnt * cy_size; i += kThreads) {
+        const int j = i / cy_size, sl = i - j * cy_size;
+        const int t0 = a.cy_begin[g.cy_base + sl], t1 = a.cy_begin[g.cy_base + sl + 1];
+        float v = 0.f;
+        for (int t = t0; t < t1; ++t) v += a.cy_coef[t] * Ys[j * d2p + a.cy_col[t]];
+        cys[i] = v;
+      }
+      __syncthreads();
+      for (int it = ib; it < ie; ++it) {
+        const Item item = a.items[it];
+        const UvwPath p = a.paths[item.path];
+        switch (p.l1 * 8 + p.l3) { UVW_CASES(UVW_BWD_CASE) default: break; }
+      }
+      __syncthreads();
+      // per-edge outputs: gY from the gc partials, gR from the item partials (fixed order)
+      for (int i = tid; i < cnt * a.d2; i += kThreads) {
+        const int j = i / a.d2, c = i - j * a.d2;
+        const int t0 = a.gy_begin[g.gy_base + c], t1 = a.gy_begin[g.gy_base + c + 1];
+        float v = 0.f;
+        for (int t = t0; t < t1; ++t) {
+          const int sl = a.gy_slot[t], nb = a.gy_nub[t];
+          float gsum = 0.f;
+          for (int b = 0; b < nb; ++b) gsum += gcp[(j * nub + b) * cy_size + sl];
+          v += a.gy_coef[t] * gsum;
+        }
+        a.gY[(size_t)eid_s[j] * a.d2 + c] = v;
+      }
+      for (int i = tid; i < cnt * a.K; i += kThreads) {
+        const int j = i / a.K, k = i - j * a.K;
+        float v = 0.f;
+        for (int q = 0; q < n_items; ++q) v += gRp[(j * n_items + q) * kKB + k];
+        a.gR[(size_t)eid_s[j] * a.K + k] = v;
+      }
+    }
+    __syncthreads();
+    float* dst = a.state + (size_t)(s - a.n0) * a.s_node;
+    for (int i = tid; i < a.s_node; i += kThreads) dst[i] = Hs[i];
+  }
+}
+
+}  // namespace uvw_detail
+
+using namespace uvw_detail;
+
+cgtp_status uvw_create(cgtp_plan_s* plan) {
+  UvwState* st = new UvwState();
+  plan->uvw = st;
+  st->K = plan->radial_k;
+  if (st->K > kKB) return fail(CGTP_EUNSUPPORTED, "uvw supports radial_k <= 8");
+  int lmax = 0;
+  for (const auto& p : plan->paths) lmax = std::max(lmax, std::max(p.l1, std::max(p.l2, p.l3)));
+  if (lmax > 3) return fail(CGTP_EUNSUPPORTED, "uvw supports l <= 3");
+  // state slices: forward [path][u][m3], backward [path][w][m1]
+  int soff = 0, aoff = 0;
+  LayoutHost lay;
+  cgtp_status s = build_layout(plan, kEdgeChunk, size_t(1) << 40, &lay);
+  if (s != CGTP_OK) return s;
+  if (lay.groups.size() != 1) return fail(CGTP_EUNSUPPORTED, "uvw plan too large");
+  // items: the uvu layout makes (path, 32-channel block of mul1) items; the
+  // backward runs over blocks of mul_out, so rebuild the item lists for it
+  for (size_t i = 0; i < plan->paths.size(); ++i) {
+    const auto& q = plan->paths[i];
+    UvwPath u{};
+    u.l1 = q.l1;
+    u.l2 = q.l2;
+    u.l3 = q.l3;
+    u.D1 = 2 * q.l1 + 1;
+    u.D2 = 2 * q.l2 + 1;
+    u.D3 = 2 * q.l3 + 1;
+    u.mul1 = q.mul1;
+    u.mul_out = q.mul_out;
+    u.off1 = q.off1;
+    u.off2 = q.off2;
+    u.ooff = q.ooff;
+    u.woff = q.woff;
+    u.soff = soff;
+    u.aoff = aoff;
+    u.cyoff = lay.paths[i].cyoff_g;
+    u.i1 = q.i1;
+    u.io = q.io;
+    soff += q.mul1 * u.D3;
+    aoff += q.mul_out * u.D1;
+    st->paths_h.push_back(u);
+  }
+  st->n_paths = static_cast<int>(plan->paths.size());
+  st->s_slice = std::max(soff, aoff);
+  st->s_node = st->K * st->s_slice;
+  // backward items: (path, 32-block of mul_out)
+  std::vector<std::vector<Item>> per_warp(kWarps);
+  {
+    struct It { int path, w0; double cost; };
+    std::vector<It> its;
+    for (int p = 0; p < st->n_paths; ++p) {
+      const auto& q = st->paths_h[p];
+      for (int w0 = 0; w0 < q.mul_out; w0 += 32) its.push_back({p, w0, double(q.D1 * q.D3 * 3 + 3 * st->K * q.D1)});
+    }
+    std::stable_sort(its.begin(), its.end(), [](const It& a, const It& b) { return a.cost > b.cost; });
+    std::vector<double> load(kWarps, 0.0);
+    for (const auto& it : its) {
+      const int w = int(std::min_element(load.begin(), load.end()) - load.begin());
+      per_warp[w].push_back({it.path, it.w0});
+      load[w] += it.cost;
+    }
+  }
+  std::vector<int> bwd_begin;
+  std::vector<Item> bwd_items;
+  for (int w = 0; w < kWarps; ++w) {
+    bwd_begin.push_back(int(bwd_items.size()));
+    for (auto& i : per_warp[w]) bwd_items.push_back(i);
+  }
+  bwd_begin.push_back(int(bwd_items.size()));
+  // gc layout channel blocks for the backward are blocks of mul_out
+  int nub_b = 1;
+  for (const auto& q : st->paths_h) nub_b = std::max(nub_b, (q.mul_out + 31) / 32);
+  {
+    // rebuild gy_nub entries for the backward: the number of w blocks of the slot's path
+    std::vector<int> slot_path(lay.groups[0].cy_size, 0);
+    for (int p = 0; p < st->n_paths; ++p) {
+      const auto& q = st->paths_h[p];
+      for (int f = 0; f < q.D1 * q.D3; ++f) slot_path[q.cyoff + f] = p;
+    }
+    for (size_t t = 0; t < lay.gy_slot.size(); ++t)
+      lay.gy_nub[t] = (st->paths_h[slot_path[lay.gy_slot[t]]].mul_out + 31) / 32;
+  }
+  GroupDev g0 = lay.groups[0];
+  g0.nub = std::max(g0.nub, nub_b);
+  lay.groups[0] = g0;
+  // the forward keeps the (path, u-block) items of the layout; the backward
+  // items go after them
+  const int bwd_item_base = static_cast<int>(lay.item_begin.size());
+  const int bwd_items_off = static_cast<int>(lay.items.size());
+  for (int w = 0; w <= kWarps; ++w) lay.item_begin.push_back(bwd_begin[w] + bwd_items_off);
+  for (auto& i : bwd_items) lay.items.push_back(i);
+  GroupDev gb = g0;
+  gb.item_base = bwd_item_base;
+  lay.groups.push_back(gb);  // group[1]: same tables, backward items
+  s = upload_layout(plan, lay, &plan->conv_layout);
+  if (s != CGTP_OK) return s;
+  // ---- GEMM descriptors -------------------------------------------------
+  // launch pointers: 0 = node state chunk, 1 = M, 2 = out / gx chunk rows,
+  //                  3 = x chunk rows, 4 = gM, 5 = second node state chunk
+  const int Kr = st->K;
+  const long long wn = plan->w_numel;
+  std::vector<GemmProb> fp, pp, xp, mp;
+  std::vector<GemmSeg> fs, ps, xs, ms;
+  const int n_out = static_cast<int>(plan->out.size());
+  int oo = 0;
+  std::vector<int> out_off;
+  for (const auto& o : plan->out) {
+    out_off.push_back(oo);
+    oo += o.mul * (2 * o.l + 1);
+  }
+  // forward: one problem per output block, K over (k, path -> block), rows (n, m3), cols w
+  for (int o = 0; o < n_out; ++o) {
+    GemmProb P{};
+    P.a_base = 0; P.b_base = 1; P.c_base = 2;
+    P.Nn = -1;
+    P.D = 2 * plan->out[o].l + 1;
+    P.J = plan->out[o].mul;
+    P.a_off = 0; P.a_n = st->s_node; P.a_m = 1;
+    P.b_j = 1;
+    P.c_off = out_off[o]; P.c_n = plan->d_out; P.c_m = 1; P.c_j = P.D;
+    P.beta = 0;
+    P.seg0 = int(fs.size());
+    for (int k = 0; k < Kr; ++k)
+      for (const auto& q : st->paths_h)
+        if (q.io == o) {
+          GemmSeg S{};
+          S.a_off = (long long)k * st->s_slice + q.soff;
+          S.b_off = (long long)k * wn + q.woff;
+          S.K = q.mul1;
+          S.a_k = q.D3;
+          S.b_k = q.mul_out;
+          fs.push_back(S);
+        }
+    P.seg1 = int(fs.size());
+    if (P.seg1 > P.seg0) fp.push_back(P);
+  }
+  // backward pre-GEMM: A[s][k][path][w][m1] = sum_u x[s][u,m1] M[k,path,u,w]
+  for (int k = 0; k < Kr; ++k)
+    for (const auto& q : st->paths_h) {
+      GemmProb P{};
+      P.a_base = 3; P.b_base = 1; P.c_base = 0;
+      P.Nn = -1; P.D = q.D1; P.J = q.mul_out;
+      P.a_off = q.off1; P.a_n = plan->d1; P.a_m = 1;
+      P.b_j = 1;
+      P.c_off = (long long)k * st->s_slice + q.aoff; P.c_n = st->s_node; P.c_m = 1; P.c_j = q.D1;
+      P.beta = 0;
+      P.seg0 = int(ps.size());
+      GemmSeg S{};
+      S.a_off = 0; S.b_off = (long long)k * wn + q.woff; S.K = q.mul1; S.a_k = q.D1; S.b_k = q.mul_out;
+      ps.push_back(S);
+      P.seg1 = int(ps.size());
+      pp.push_back(P);
+    }
+  // backward gx: per in1 block, rows (s, m1), cols u, K over (k, path with that block) of w
+  int o1 = 0;
+  for (int i1 = 0; i1 < (int)plan->in1.size(); ++i1) {
+    const auto& b = plan->in1[i1];
+    GemmProb P{};
+    P.a_base = 5; P.b_base = 1; P.c_base = 2;
+    P.Nn = -1; P.D = 2 * b.l + 1; P.J = b.mul;
+    P.a_off = 0; P.a_n = st->s_node; P.a_m = 1;
+    P.b_j = 0;  // set per segment through b_k / column stride below
+    P.c_off = o1; P.c_n = plan->d1; P.c_m = 1; P.c_j = P.D;
+    P.beta = 0;
+    P.seg0 = int(xs.size());
+    for (int k = 0; k < Kr; ++k)
+      for (const auto& q : st->paths_h)
+        if (q.i1 == i1) {
+          GemmSeg S{};
+          S.a_off = (long long)k * st->s_slice + q.aoff;
+          S.b_off = (long long)k * wn + q.woff;  // B[w][u] = M[k][woff + u*mul_out + w]
+          S.K = q.mul_out; S.a_k = q.D1; S.b_k = 1;
+          xs.push_back(S);
+        }
+    P.b_j = 0;
+    P.seg1 = int(xs.size());
+    // column (u) stride of B is mul_out of the paths (equal for all paths of a block)
+    for (const auto& q : st->paths_h)
+      if (q.i1 == i1) P.b_j = q.mul_out;
+    if (P.seg1 > P.seg0) xp.push_back(P);
+    o1 += b.mul * (2 * b.l + 1);
+  }
+  // backward gM: per (k, path): rows u (Nn = mul1, D = 1), cols w, K over (m1, s in chunk)
+  for (int k = 0; k < Kr; ++k)
+    for (const auto& q : st->paths_h) {
+      GemmProb P{};
+      P.a_base = 3; P.b_base = 5; P.c_base = 4;
+      P.Nn = q.mul1; P.D = 1; P.J = q.mul_out;
+      P.a_off = q.off1; P.a_n = q.D1; P.a_m = 0;
+      P.b_j = q.D1;
+      P.c_off = (long long)k * wn + q.woff; P.c_n = q.mul_out; P.c_m = 0; P.c_j = 1;
+      P.beta = 1;
+      P.seg0 = int(ms.size());
+      for (int m1 = 0; m1 < q.D1; ++m1) {
+        GemmSeg S{};
+        S.a_off = m1; S.b_off = (long long)k * st->s_slice + q.aoff + m1;
+        S.K = -1; S.a_k = plan->d1; S.b_k = st->s_node;
+        ms.push_back(S);
+      }
+      P.seg1 = int(ms.size());
+      mp.push_back(P);
+    }
+  // upload descriptor tables
+  std::vector<unsigned char> buf;
+  auto put = [&](const void* src, size_t bytes) {
+    size_t o = (buf.size() + 15) / 16 * 16;
+    buf.resize(o + bytes);
+    if (bytes) memcpy(buf.data() + o, src, bytes);
+    return o;
+  };
+  const size_t o_paths = put(st->paths_h.data(), st->paths_h.size() * sizeof(UvwPath));
+  const size_t o_fp = put(fp.data(), fp.size() * sizeof(GemmProb));
+  const size_t o_fs = put(fs.data(), fs.size() * sizeof(GemmSeg));
+  const size_t o_pp = put(pp.data(), pp.size() * sizeof(GemmProb));
+  const size_t o_ps = put(ps.data(), ps.size() * sizeof(GemmSeg));
+  const size_t o_xp = put(xp.data(), xp.size() * sizeof(GemmProb));
+  const size_t o_xs = put(xs.data(), xs.size() * sizeof(GemmSeg));
+  const size_t o_mp = put(mp.data(), mp.size() * sizeof(GemmProb));
+  const size_t o_ms = put(ms.data(), ms.size() * sizeof(GemmSeg));
+  if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "uvw tables");
+  cudaMemcpy(st->tables, buf.data(), buf.size(), cudaMemcpyHostToDevice);
+  auto at = [&](size_t o) { return static_cast<unsigned char*>(st->tables) + o; };
+  st->paths = reinterpret_cast<UvwPath*>(at(o_paths));
+  st->fwd_probs = reinterpret_cast<GemmProb*>(at(o_fp)); st->fwd_np = int(fp.size());
+  st->fwd_segs = reinterpret_cast<GemmSeg*>(at(o_fs));
+  st->pre_probs = reinterpret_cast<GemmProb*>(at(o_pp)); st->pre_np = int(pp.size());
+  st->pre_segs = reinterpret_cast<GemmSeg*>(at(o_ps));
+  st->gx_probs = reinterpret_cast<GemmProb*>(at(o_xp)); st->gx_np = int(xp.size());
+  st->gx_segs = reinterpret_cast<GemmSeg*>(at(o_xs));
+  st->gm_probs = reinterpret_cast<GemmProb*>(at(o_mp)); st->gm_np = int(mp.size());
+  st->gm_segs = reinterpret_cast<GemmSeg*>(at(o_ms));
+  // node-state scratch: two chunks of state (forward S; backward A and H)
+  if (const char* env = std::getenv("CGTP_UVW_CHUNK_NODES")) {
+    const long v = std::strtol(env, nullptr, 10);
+    if (v >= 1 && v <= (1 << 20)) st->chunk_nodes = static_cast<int>(v);
+  }
+  st->scratch_elems = size_t(2) * st->chunk_nodes * st->s_node;
+  if (cudaMalloc(&st->scratch, st->scratch_elems * sizeof(float)) != cudaSuccess)
+    return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
+  // shared memory of the edge stages
+  const GroupDev& G = lay.groups[0];
+  const int d2p = pad_up(int(plan->d2), 4);
+  st->smem_fwd = sizeof(float) * (pad_up(st->s_node, 4) + kEdgeChunk * d2p + kEdgeChunk * 16 +
+                                  kEdgeChunk * G.cy_size) + sizeof(int) * kEdgeChunk;
+  const int n_items_b = static_cast<int>(bwd_items.size());
+  st->smem_bwd = sizeof(float) * (2 * pad_up(st->s_node, 4) + kBwdChunk * plan->d_out + kBwdChunk * d2p +
+                                  kBwdChunk * 16 + kBwdChunk * G.cy_size +
+                                  kBwdChunk * g0.nub * G.cy_size + kBwdChunk * n_items_b * kKB) +
+                 2 * sizeof(int) * kBwdChunk;
+  if (st->smem_fwd > 227 * 1024 || st->smem_bwd > 227 * 1024)
+    return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
+  cudaFuncSetAttribute(uvw_fwd_edge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem_fwd);
+  cudaFuncSetAttribute(uvw_bwd_edge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem_bwd);
+  return CGTP_OK;
+}
+
+void uvw_destroy(cgtp_plan_s* plan) {
+  UvwState* st = static_cast<UvwState*>(plan->uvw);
+  if (!st) return;
+  if (st->tables) cudaFree(st->tables);
+  if (st->scratch) cudaFree(st->scratch);
+  delete st;
+  plan->uvw = nullptr;
+}
+
+namespace {
+EdgeArgs edge_args(const cgtp_plan_s* plan, const UvwState* st, int group) {
+  const LayoutDev& L = plan->conv_layout;
+  EdgeArgs a{};
+  a.d1 = int(plan->d1);
+  a.d2 = int(plan->d2);
+  a.d_out = int(plan->d_out);
+  a.K = st->K;
+  a.s_node = st->s_node;
+  a.s_slice = st->s_slice;
+  a.paths = st->paths;
+  a.group = L.groups + group;
+  a.cy_begin = L.cy_begin;
+  a.cy_col = L.cy_col;
+  a.cy_coef = static_cast<const float*>(L.cy_coef);
+  a.gy_begin = L.gy_begin;
+  a.gy_slot = L.gy_slot;
+  a.gy_nub = L.gy_nub;
+  a.gy_coef = static_cast<const float*>(L.gy_coef);
+  a.item_begin = L.item_begin;
+  a.items = L.items;
+  return a;
+}
+
+cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
+                        const float* const ptr[6], int nodes, int tiles, cudaStream_t s) {
+  GemmLaunch L{};
+  for (int i = 0; i < 6; ++i) L.ptr[i] = ptr[i];
+  L.nodes = nodes;
+  L.nprob = np;
+  L.probs = probs_dev;
+  L.segs = segs;
+  grouped_gemm_kernel<<<tiles, 256, 0, s>>>(L);
+  return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
+}
+
+// tiles of a descriptor set for `nodes` nodes (host copy of the descriptors needed)
+int count_tiles(const std::vector<std::pair<int, int>>& rows_cols) {
+  int t = 0;
+  for (auto& rc : rows_cols) t += ((rc.first + kGT - 1) / kGT) * ((rc.second + kGT - 1) / kGT);
+  return t;
+}
+}  // namespace
+
+// Host mirrors of the GEMM shapes (rows per node, cols, fixed rows) to size the grids.
+static int tiles_for(const cgtp_plan_s* plan, const UvwState* st, int which, int nodes) {
+  std::vector<std::pair<int, int>> rc;
+  if (which == 0) {
+    for (size_t o = 0; o < plan->out.size(); ++o) {
+      bool any = false;
+      for (const auto& q : st->paths_h) any |= (q.io == int(o));
+      if (any) rc.push_back({nodes * (2 * plan->out[o].l + 1), plan->out[o].mul});
+    }
+  } else if (which == 1) {
+    for (int k = 0; k < st->K; ++k)
+      for (const auto& q : st->paths_h) rc.push_back({nodes * q.D1, q.mul_out});
+  } else if (which == 2) {
+    for (size_t i1 = 0; i1 < plan->in1.size(); ++i1) {
+      bool any = false;
+      for (const auto& q : st->paths_h) any |= (q.i1 == int(i1));
+      if (any) rc.push_back({nodes * (2 * plan->in1[i1].l + 1), plan->in1[i1].mul});
+    }
+  } else {
+    for (int k = 0; k < st->K; ++k)
+      for (const auto& q : st->paths_h) rc.push_back({q.mul1, q.mul_out});
+  }
+  return count_tiles(rc);
+}
+
+cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x,
+                        const void* Y, const void* R, const void* M, void* out, void* stream) {
+  const UvwState* st = static_cast<const UvwState*>(plan->uvw);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EdgeArgs a = edge_args(plan, st, 0);
+  a.x = static_cast<const float*>(x);
+  a.Y = static_cast<const float*>(Y);
+  a.R = static_cast<const float*>(R);
+  a.rowptr = g->rowptr;
+  a.col = g->col;
+  a.state = st->scratch;
+  for (int64_t n0 = 0; n0 < g->N; n0 += st->chunk_nodes) {
+    const int n1 = static_cast<int>(std::min<int64_t>(g->N, n0 + st->chunk_nodes));
+    a.n0 = static_cast<int>(n0);
+    a.n1 = n1;
+    const int nodes = n1 - a.n0;
+    const int grid = std::min(nodes, plan->num_sms * 2);
+    uvw_fwd_edge_kernel<<<grid, kThreads, st->smem_fwd, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw forward edge stage launch failed");
+    const float* ptr[6] = {st->scratch, static_cast<const float*>(M),
+                           static_cast<float*>(out) + (size_t)n0 * plan->d_out, nullptr, nullptr, nullptr};
+    cgtp_status r = launch_gemm(st->fwd_probs, st->fwd_np, st->fwd_segs, ptr, nodes,
+                                tiles_for(plan, st, 0, nodes), s);
+    if (r != CGTP_OK) return r;
+  }
+  return CGTP_OK;
+}
+
+cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* gout,
+                         const void* x, const void* Y, const void* R, const void* M, void* gx,
+                         void* gY, void* gR, void* gM, void* stream) {
+  const UvwState* st = static_cast<const UvwState*>(plan->uvw);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* Abuf = st->scratch;
+  float* Hbuf = st->scratch + (size_t)st->chunk_nodes * st->s_node;
+  EdgeArgs a = edge_args(plan, st, 1);
+  a.x = static_cast<const float*>(x);
+  a.Y = static_cast<const float*>(Y);
+  a.R = static_cast<const float*>(R);
+  a.g = static_cast<const float*>(gout);
+  a.gY = static_cast<float*>(gY);
+  a.gR = static_cast<float*>(gR);
+  a.rowptr = g->t_rowptr;
+  a.col = g->t_eid;
+  a.t_dst = g->t_dst;
+  a.Astate = Abuf;
+  a.state = Hbuf;
+  bool first = true;
+  for (int64_t n0 = 0; n0 < g->N; n0 += st->chunk_nodes) {
+    const int n1 = static_cast<int>(std::min<int64_t>(g->N, n0 + st->chunk_nodes));
+    const int nodes = n1 - static_cast<int>(n0);
+    const float* xrows = static_cast<const float*>(x) + (size_t)n0 * plan->d1;
+    const float* pre[6] = {Abuf, static_cast<const float*>(M), nullptr, xrows, nullptr, nullptr};
+    cgtp_status r = launch_gemm(st->pre_probs, st->pre_np, st->pre_segs, pre, nodes,
+                                tiles_for(plan, st, 1, nodes), s);
+    if (r != CGTP_OK) return r;
+    a.n0 = static_cast<int>(n0);
+    a.n1 = n1;
+    const int grid = std::min(nodes, plan->num_sms * 1);
+    uvw_bwd_edge_kernel<<<grid, kThreads, st->smem_bwd, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw backward edge stage launch failed");
+    const float* post[6] = {nullptr, static_cast<const float*>(M),
+                            static_cast<float*>(gx) + (size_t)n0 * plan->d1, xrows,
+                            static_cast<float*>(gM), Hbuf};
+    r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s);
+    if (r != CGTP_OK) return r;
+    if (first) {
+      cudaMemsetAsync(gM, 0, sizeof(float) * plan->w_numel * st->K, s);
+      first = false;
+    }
+    r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, post, nodes, tiles_for(plan, st, 3, nodes), s);
+    if (r != CGTP_OK) return r;
+  }
+  if (g->N == 0) cudaMemsetAsync(gM, 0, sizeof(float) * plan->w_numel * st->K, s);
+  return CGTP_OK;
+}
+
 }  // namespace cgtp

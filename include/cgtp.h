@@ -76,7 +76,11 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *  radial_k : 0 for uvu; for uvw the number K of radial functions (1..16); the
  *      weights are then W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
- * the streaming node stage.  Must be called with the target device current.
+ * the streaming node stage: node state for a chunk of nodes (default 4096,
+ * overridable through the environment variable CGTP_UVW_CHUNK_NODES read at
+ * plan creation), 2 x chunk x K x sum_path mul*(2l+1) floats (~590 MB for
+ * 64x(0e,1o,2e), K = 8).  uvw limits: l <= 3, K <= 8.  Must be called with the
+ * target device current.
  */
 cgtp_status cgtp_plan_create(cgtp_plan* plan, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,

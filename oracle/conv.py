@@ -233,3 +233,28 @@ def dense_tensor(plan, w_edge):
                                 k = p.ooff + w * D3 + m3
                                 T[i, j, k] += w_edge[p.woff + u * p.mul_out + w] * c
     return T
+
+
+def conv_uvw_radial_gM_entries(plan, g, x, Y, R, rowptr, col, entries):
+    """Selected entries of gM, each summed over every edge (plain definition).
+
+    entries: iterable of (k, path index, u, w).  gM[k][woff + u*mul_out + w] =
+    sum_e R[e,k] sum_m3 g[dst][ooff + w*D3 + m3] t_e[u, m3] with
+    t_e[u, m3] = sum_{m1,m2} C x[src][u, m1] Y[e][m2].
+    """
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    g, x = np.asarray(g), np.asarray(x)
+    Y, R = _f64(Y), _f64(R)
+    dst = csr_dst(rowptr)
+    out = []
+    for (k, pi, u, w) in entries:
+        p = plan.paths[pi]
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+        xs = x[:, p.off1 + u * D1:p.off1 + (u + 1) * D1][col]
+        ys = Y[:, p.off2:p.off2 + D2]
+        t = np.einsum("ijk,ei,ej->ek", C, _f64(xs), ys)
+        gw = g[:, p.ooff + w * D3:p.ooff + (w + 1) * D3][dst]
+        out.append(float((R[:, k] * (_f64(gw) * t).sum(1)).sum()))
+    return np.array(out)

@@ -264,3 +264,22 @@ def test_workload_recipes_shapes():
     u = wl.make("uvw", 45056, N=10)
     assert u["R"].shape == (320, 8) and u["M"].shape == (8, 45056)
     assert np.all(u["R"] > 0) and np.all(u["R"] <= 1)
+
+
+def test_uvw_gM_entries_match_full_backward():
+    rng = np.random.default_rng(23)
+    plan = irreps.make_plan("2x0e+2x1o+1x2e", "0e+1o+2e", "2x0e+1x1o+2x2e", mode="uvw")
+    N, E, K = 5, 14, 3
+    rowptr, col = small_graph(rng, N, E)
+    x = rng.normal(size=(N, plan.d1))
+    Y = rng.normal(size=(E, plan.d2))
+    R = rng.normal(size=(E, K))
+    M = rng.normal(size=(K, plan.w_numel))
+    g = rng.normal(size=(N, plan.d_out))
+    _, _, _, gM = conv.conv_uvw_radial_backward(plan, g, x, Y, R, M, rowptr, col)
+    entries = [(k, pi, u, w) for k in range(K) for pi, p in enumerate(plan.paths)
+               for u in range(p.mul1) for w in range(p.mul_out)]
+    vals = conv.conv_uvw_radial_gM_entries(plan, g, x, Y, R, rowptr, col, entries)
+    for (k, pi, u, w), v in zip(entries, vals):
+        p = plan.paths[pi]
+        assert abs(gM[k, p.woff + u * p.mul_out + w] - v) < 1e-11
