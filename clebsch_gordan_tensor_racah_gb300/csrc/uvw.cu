@@ -59,7 +59,7 @@ struct GemmSeg {
   long long a_off, b_off;
   int K;        // <0: use the launch's node count
   int a_k, b_k;
-  int pad_;
+  int b_j;      // column stride of B (may differ between the segments of a problem)
 };
 
 struct GemmProb {
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
         As[kk][rr] = v;
         const int cc = rr, c = c0 + cc;
         float b = 0.f;
-        if (c < P.J && k < K) b = B[S.b_off + (long long)k * S.b_k + (long long)c * P.b_j];
+        if (c < P.J && k < K) b = B[S.b_off + (long long)k * S.b_k + (long long)c * S.b_j];
         Bs[kk][cc] = b;
       }
       __syncthreads();
@@ -656,6 +656,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
           S.K = q.mul1;
           S.a_k = q.D3;
           S.b_k = q.mul_out;
+          S.b_j = 1;
           fs.push_back(S);
         }
     P.seg1 = int(fs.size());
@@ -674,6 +675,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       P.seg0 = int(ps.size());
       GemmSeg S{};
       S.a_off = 0; S.b_off = (long long)k * wn + q.woff; S.K = q.mul1; S.a_k = q.D1; S.b_k = q.mul_out;
+      S.b_j = 1;
       ps.push_back(S);
       P.seg1 = int(ps.size());
       pp.push_back(P);
@@ -686,7 +688,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     P.a_base = 5; P.b_base = 1; P.c_base = 2;
     P.Nn = -1; P.D = 2 * b.l + 1; P.J = b.mul;
     P.a_off = 0; P.a_n = st->s_node; P.a_m = 1;
-    P.b_j = 0;  // set per segment through b_k / column stride below
     P.c_off = o1; P.c_n = plan->d1; P.c_m = 1; P.c_j = P.D;
     P.beta = 0;
     P.seg0 = int(xs.size());
@@ -697,13 +698,10 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
           S.a_off = (long long)k * st->s_slice + q.aoff;
           S.b_off = (long long)k * wn + q.woff;  // B[w][u] = M[k][woff + u*mul_out + w]
           S.K = q.mul_out; S.a_k = q.D1; S.b_k = 1;
+          S.b_j = q.mul_out;  // B[w][u] = M[k][woff + u*mul_out + w]
           xs.push_back(S);
         }
-    P.b_j = 0;
     P.seg1 = int(xs.size());
-    // column (u) stride of B is mul_out of the paths (equal for all paths of a block)
-    for (const auto& q : st->paths_h)
-      if (q.i1 == i1) P.b_j = q.mul_out;
     if (P.seg1 > P.seg0) xp.push_back(P);
     o1 += b.mul * (2 * b.l + 1);
   }
@@ -722,6 +720,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
         GemmSeg S{};
         S.a_off = m1; S.b_off = (long long)k * st->s_slice + q.aoff + m1;
         S.K = -1; S.a_k = plan->d1; S.b_k = st->s_node;
+        S.b_j = q.D1;
         ms.push_back(S);
       }
       P.seg1 = int(ms.size());
