@@ -18,7 +18,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcgtp.so")
 
 CU_SOURCES = ["api.cu", "graph.cu", "uvu.cu", "uvu_f32.cu", "uvu_f32_l7.cu", "uvu_f64.cu",
-              "uvu_f64_l7.cu", "uvw.cu"]
+              "uvu_f64_l7.cu", "uvu2.cu", "uvu3.cu", "uvu3_f32_2.cu", "uvu3_f32_8.cu", "uvu3_f32_32.cu",
+              "uvu3_f64_2.cu", "uvu3_f64_8.cu", "uvu3_f64_32.cu", "uvw.cu"]
 CPP_SOURCES = ["planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -49,11 +50,28 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
+GEN = os.path.join(BUILD, "gen")
+
+
+def _bake():
+    """Build and run gen_baked: the planner's CG blocks (l <= 3) as compile-time code."""
+    os.makedirs(GEN, exist_ok=True)
+    exe = os.path.join(GEN, "gen_baked")
+    out = os.path.join(GEN, "cg_baked.cuh")
+    srcs = [os.path.join(CSRC, "gen_baked.cpp"), os.path.join(CSRC, "planner.cpp")]
+    deps = srcs + [os.path.join(CSRC, "internal.h"), os.path.join(INC, "cgtp.h")]
+    if not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(d) for d in deps):
+        _run(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-I", INC, "-I", CSRC, *srcs, "-o", exe])
+        _run([exe, out + ".tmp"])
+        os.replace(out + ".tmp", out)
+    return os.path.getmtime(out)
+
+
 def build(verbose=False, jobs=None):
     """Compile (incrementally) and link libcgtp.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    hdr_m = _headers_mtime()
+    hdr_m = max(_headers_mtime(), _bake())
     cmds = []
     objs = []
     for f in CU_SOURCES:
@@ -61,7 +79,7 @@ def build(verbose=False, jobs=None):
         objs.append(obj)
         if _stale(src, obj, hdr_m):
             cmds.append([nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
-                         "-Xcompiler", "-ffp-contract=off", "-I", INC, "-c", src, "-o", obj])
+                         "-Xcompiler", "-ffp-contract=off", "-I", INC, "-I", GEN, "-c", src, "-o", obj])
     for f in CPP_SOURCES:
         src, obj = os.path.join(CSRC, f), os.path.join(BUILD, f + ".o")
         objs.append(obj)
@@ -71,7 +89,7 @@ def build(verbose=False, jobs=None):
     jobs = jobs or max(1, min(len(cmds), os.cpu_count() or 4))
     if cmds:
         # longest translation units first
-        cmds.sort(key=lambda c: ("_l7" not in c[-3], c[-3]))
+        cmds.sort(key=lambda c: ("_l7" not in c[-3] and "uvu3_" not in c[-3], c[-3]))
         with cf.ThreadPoolExecutor(jobs) as ex:
             for out in ex.map(_run, cmds):
                 if verbose and out.strip():

@@ -62,6 +62,15 @@ cgtp_status upload_layout(const cgtp_plan_s* plan, const LayoutHost& h, LayoutDe
   append(buf, h.items, &o_it);
   append(buf, h.gx_begin, &o_gxb);
   append(buf, h.gx_paths, &o_gxp);
+  size_t o_c2c, o_c2f, o_c2b;
+  append(buf, h.cy2_col, &o_c2c);
+  if (plan->dtype == CGTP_F64) {
+    append(buf, h.cy2_coef, &o_c2f);
+  } else {
+    std::vector<float> f(h.cy2_coef.begin(), h.cy2_coef.end());
+    append(buf, f, &o_c2f);
+  }
+  append(buf, h.cy2_base, &o_c2b);
   void* base = nullptr;
   if (cudaMalloc(&base, std::max<size_t>(buf.size(), 16)) != cudaSuccess)
     return fail(CGTP_ENOMEM, "plan table allocation failed");
@@ -90,6 +99,12 @@ cgtp_status upload_layout(const cgtp_plan_s* plan, const LayoutHost& h, LayoutDe
   d->gx_paths = reinterpret_cast<const int*>(at(o_gxp));
   d->smem_fwd = h.smem_fwd;
   d->smem_bwd = h.smem_bwd;
+  d->cy2_col = reinterpret_cast<const int*>(at(o_c2c));
+  d->cy2_coef = at(o_c2f);
+  d->cy2_base = reinterpret_cast<const int*>(at(o_c2b));
+  d->chunk2 = h.chunk2;
+  d->smem_fwd2 = h.smem_fwd2;
+  d->smem_bwd2 = h.smem_bwd2;
   d->groups_host = h.groups;
   return CGTP_OK;
 }
@@ -165,6 +180,7 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (s == CGTP_OK) s = build_layout(p, 1, budget, &batch);
     if (s == CGTP_OK) s = upload_layout(p, conv, &p->conv_layout);
     if (s == CGTP_OK) s = upload_layout(p, batch, &p->batch_layout);
+    if (s == CGTP_OK) s = build_v3(p);
   } else {
     s = uvw_create(p);
   }
@@ -180,6 +196,7 @@ void cgtp_plan_destroy(cgtp_plan plan) {
   if (!plan) return;
   free_layout(&plan->conv_layout);
   free_layout(&plan->batch_layout);
+  free_v3(plan);
   if (plan->uvw) uvw_destroy(plan);
   delete plan;
 }

@@ -67,6 +67,14 @@ struct LayoutHost {
   std::vector<int> gx_begin;       // per group: n_in1 + 1 offsets into gx_paths
   std::vector<int> gx_paths;       // global path indices, in path order
   size_t smem_fwd = 0, smem_bwd = 0;
+  // two-term coefficient tables (every cy slot has at most two CG terms):
+  // per group and slot, cy[slot] = c0 * Y[col0] + c1 * Y[col1]
+  std::vector<int> cy2_col;        // 2 per slot, concatenated over groups (offset cy_base2)
+  std::vector<double> cy2_coef;    // 2 per slot
+  std::vector<int> cy2_base;       // per group: first slot
+  // edge-chunk size of the pipelined kernels (even) and their shared memory
+  int chunk2 = 0;
+  size_t smem_fwd2 = 0, smem_bwd2 = 0;
 };
 
 // Device copy of a layout: one allocation, pointers into it.
@@ -89,8 +97,32 @@ struct LayoutDev {
   const int* gx_begin = nullptr;
   const int* gx_paths = nullptr;
   size_t smem_fwd = 0, smem_bwd = 0;
+  const int* cy2_col = nullptr;
+  const void* cy2_coef = nullptr;
+  const int* cy2_base = nullptr;
+  int chunk2 = 0;
+  size_t smem_fwd2 = 0, smem_bwd2 = 0;
   void* base = nullptr;            // owning allocation
   std::vector<GroupDev> groups_host;
+};
+
+// Tables of the warp-autonomous uvu kernels (uvu3_impl.cuh); lpe == 0 when the
+// plan does not qualify (it needs l <= 3 and one multiplicity m for all in1
+// blocks with m / 4 in {2, 8, 32} or m a multiple of 128).
+struct V3Dev {
+  int lpe = 0;
+  const PathDev* paths = nullptr;
+  const int* item_begin = nullptr;
+  const Item* items = nullptr;
+  const int* gxp_off = nullptr;
+  int gxp_size = 0;
+  const int* in1_off = nullptr;
+  int n_in1 = 0;
+  const int* gx_begin = nullptr;
+  const int* gx_paths = nullptr;
+  int chunk_b = 0;
+  size_t smem_bwd = 0;
+  void* base = nullptr;
 };
 
 struct PathHost {
@@ -111,6 +143,7 @@ struct cgtp_plan_s {
   int num_sms = 0;
   // uvu
   cgtp::LayoutDev conv_layout, batch_layout;
+  cgtp::V3Dev v3;
   // uvw (radial) state is kept opaque here; see uvw.cu
   void* uvw = nullptr;
 };
@@ -149,6 +182,16 @@ cgtp_status launch_uvu_backward(const cgtp_plan_s* plan, const LayoutDev& lay, c
                                 const void* x, const void* Y, const void* W, void* gx, void* gY,
                                 void* gW, const int32_t* t_rowptr, const int32_t* t_eid,
                                 const int32_t* t_dst, int64_t N, bool identity, void* stream);
+
+// uvu3.cu
+cgtp_status build_v3(cgtp_plan_s* plan);
+void free_v3(cgtp_plan_s* plan);
+bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
+                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st);
+bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
+                        const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
+                        const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
+                        cgtp_status* st);
 
 // graph.cu
 cgtp_status graph_build(cgtp_graph_s* g, void* stream);

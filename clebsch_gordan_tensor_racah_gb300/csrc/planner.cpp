@@ -520,6 +520,38 @@ cgtp_status build_layout(const cgtp_plan_s* plan, int chunk, size_t budget, Layo
     smem_of(g.p0, g.p1, &f, &b);
     L->smem_fwd = std::max(L->smem_fwd, f);
     L->smem_bwd = std::max(L->smem_bwd, b);
+    // two-term form of the same cy terms
+    L->cy2_base.push_back(static_cast<int>(L->cy2_col.size() / 2));
+    for (int sl = 0; sl < cy; ++sl) {
+      const auto& ts = slot_terms[sl];
+      if (ts.size() > 2) return fail(CGTP_EUNSUPPORTED, "a cy slot has more than two CG terms");
+      for (int k = 0; k < 2; ++k) {
+        L->cy2_col.push_back(k < static_cast<int>(ts.size()) ? ts[k].first : 0);
+        L->cy2_coef.push_back(k < static_cast<int>(ts.size()) ? ts[k].second : 0.0);
+      }
+    }
+  }
+  // pipelined forward kernel: [acc | 2 x (x rows, W rows, Y rows, src) | cy pairs]
+  {
+    int dog = 0, wg = 0, cy = 0;
+    for (const auto& g : L->groups) {
+      dog = std::max(dog, g.o1 - g.o0);
+      wg = std::max(wg, g.w1 - g.w0);
+      cy = std::max(cy, g.cy_size);
+    }
+    const int d1p = pad_to(static_cast<int>(plan->d1), vec);
+    auto fwd2 = [&](int ch) {
+      return es * (static_cast<size_t>(pad_to(dog, vec)) +
+                   2 * static_cast<size_t>(ch) * (d1p + pad_to(wg, vec) + d2p) +
+                   static_cast<size_t>(ch) * cy) + 2 * 4 * static_cast<size_t>(ch) + 64;
+    };
+    L->chunk2 = 0;
+    for (int ch : {8, 4, 2})            // two CTAs per SM if possible
+      if (fwd2(ch) <= 110 * 1024) { L->chunk2 = ch; break; }
+    if (!L->chunk2)
+      for (int ch : {8, 4, 2})          // else one CTA per SM
+        if (fwd2(ch) <= 220 * 1024) { L->chunk2 = ch; break; }
+    L->smem_fwd2 = L->chunk2 ? fwd2(L->chunk2) : 0;
   }
   return CGTP_OK;
 }

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "internal.h"
 
@@ -18,6 +19,12 @@ cgtp_status bwd_impl(const cgtp_plan_s* plan, const LayoutDev& lay, const void* 
                      const int32_t* t_rowptr, const int32_t* t_eid, const int32_t* t_dst,
                      int64_t N, cudaStream_t st);
 }  // namespace uvu_detail
+namespace uvu2_detail {
+template <typename T>
+cgtp_status fwd2_impl(const cgtp_plan_s* plan, const LayoutDev& lay, const void* x, const void* Y,
+                      const void* W, void* out, const int32_t* rowptr, const int32_t* col, int64_t N,
+                      cudaStream_t st);
+}  // namespace uvu2_detail
 using uvu_detail::fwd_impl;
 using uvu_detail::bwd_impl;
 
@@ -33,6 +40,15 @@ cgtp_status launch_uvu_forward(const cgtp_plan_s* plan, const LayoutDev& lay, co
   if (N == 0) return CGTP_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool small = plan_lmax(plan) <= 3;
+  if (!identity) {
+    cgtp_status st3 = CGTP_OK;
+    if (launch_v3_forward(plan, x, Y, W, out, rowptr, col, N, stream, &st3)) return st3;
+  }
+  // graph convolutions with l <= 3 take the pipelined kernel
+  if (!identity && small && lay.chunk2 > 0 && !std::getenv("CGTP_UVU_FORWARD_V1")) {
+    if (plan->dtype == CGTP_F64) return uvu2_detail::fwd2_impl<double>(plan, lay, x, Y, W, out, rowptr, col, N, st);
+    return uvu2_detail::fwd2_impl<float>(plan, lay, x, Y, W, out, rowptr, col, N, st);
+  }
 #define CGTP_FWD_DISPATCH(T)                                                                         \
   if (identity)                                                                                      \
     return small ? fwd_impl<T, true, 3>(plan, lay, x, Y, W, out, rowptr, col, N, st)                 \
@@ -53,6 +69,11 @@ cgtp_status launch_uvu_backward(const cgtp_plan_s* plan, const LayoutDev& lay, c
   if (N == 0) return CGTP_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool small = plan_lmax(plan) <= 3;
+  if (!identity) {
+    cgtp_status st3 = CGTP_OK;
+    if (launch_v3_backward(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, stream, &st3))
+      return st3;
+  }
 #define CGTP_BWD_DISPATCH(T)                                                                            \
   if (identity)                                                                                         \
     return small ? bwd_impl<T, true, 3>(plan, lay, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, st) \

@@ -1,0 +1,162 @@
+// uvu3.cu -- host side of the warp-autonomous uvu kernels (uvu3_impl.cuh):
+// qualification, work items, launches.  Kernels are instantiated in
+// uvu3_<type>_<lanes>.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+namespace cgtp {
+namespace uvu3_detail {
+template <typename T, int LPE>
+cgtp_status fwd3_launch(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
+                        const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
+template <typename T, int LPE>
+cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
+                        const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
+                        const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
+}  // namespace uvu3_detail
+
+cgtp_status build_v3(cgtp_plan_s* plan) {
+  plan->v3 = V3Dev{};
+  if (plan->mode != CGTP_UVU || plan->paths.empty()) return CGTP_OK;
+  const int m = plan->in1.front().mul;
+  for (const auto& b : plan->in1)
+    if (b.mul != m || b.l > 3) return CGTP_OK;
+  for (const auto& p : plan->paths)
+    if (p.l2 > 3 || p.l3 > 3) return CGTP_OK;
+  int lpe = 0;
+  if (m % 4 == 0 && (m / 4 == 2 || m / 4 == 8 || m / 4 == 32)) lpe = m / 4;
+  else if (m % 128 == 0) lpe = 32;
+  if (!lpe) return CGTP_OK;
+  const int ublock = 4 * lpe;
+  // work items: (path, channel block), longest first onto the least loaded warp
+  struct It { int path, u0; double cost; };
+  std::vector<It> its;
+  for (size_t p = 0; p < plan->paths.size(); ++p) {
+    const auto& q = plan->paths[p];
+    const int D1 = 2 * q.l1 + 1, D3 = 2 * q.l3 + 1;
+    for (int u0 = 0; u0 < q.mul1; u0 += ublock) its.push_back({int(p), u0, double(D1 * D3 + 2 * D1 + D3 + 8)});
+  }
+  std::stable_sort(its.begin(), its.end(), [](const It& a, const It& b) { return a.cost > b.cost; });
+  std::vector<std::vector<Item>> per(kWarps);
+  std::vector<double> load(kWarps, 0.0);
+  for (const auto& it : its) {
+    const int w = int(std::min_element(load.begin(), load.end()) - load.begin());
+    per[w].push_back({it.path, it.u0});
+    load[w] += it.cost;
+  }
+  std::vector<int> item_begin;
+  std::vector<Item> items;
+  for (int w = 0; w < kWarps; ++w) {
+    item_begin.push_back(int(items.size()));
+    for (auto& i : per[w]) items.push_back(i);
+  }
+  item_begin.push_back(int(items.size()));
+  // gx partial buffer: one [mul][D1] block per path
+  std::vector<int> gxp_off;
+  int gxp = 0;
+  for (const auto& q : plan->paths) {
+    gxp_off.push_back(gxp);
+    gxp += q.mul1 * (2 * q.l1 + 1);
+  }
+  std::vector<int> in1_off;
+  int o = 0;
+  for (const auto& b : plan->in1) {
+    in1_off.push_back(o);
+    o += b.mul * (2 * b.l + 1);
+  }
+  in1_off.push_back(o);
+  std::vector<int> gx_begin, gx_paths;
+  for (size_t b = 0; b < plan->in1.size(); ++b) {
+    gx_begin.push_back(int(gx_paths.size()));
+    for (size_t p = 0; p < plan->paths.size(); ++p)
+      if (plan->paths[p].i1 == int(b)) gx_paths.push_back(int(p));
+  }
+  gx_begin.push_back(int(gx_paths.size()));
+  // upload
+  std::vector<unsigned char> buf;
+  auto put = [&](const void* src, size_t bytes) {
+    const size_t off = (buf.size() + 15) / 16 * 16;
+    buf.resize(off + bytes);
+    if (bytes) std::memcpy(buf.data() + off, src, bytes);
+    return off;
+  };
+  const size_t o_ib = put(item_begin.data(), item_begin.size() * sizeof(int));
+  const size_t o_it = put(items.data(), items.size() * sizeof(Item));
+  const size_t o_gxo = put(gxp_off.data(), gxp_off.size() * sizeof(int));
+  const size_t o_in1 = put(in1_off.data(), in1_off.size() * sizeof(int));
+  const size_t o_gxb = put(gx_begin.data(), gx_begin.size() * sizeof(int));
+  const size_t o_gxq = put(gx_paths.data(), std::max<size_t>(gx_paths.size(), 1) * sizeof(int));
+  void* base = nullptr;
+  if (cudaMalloc(&base, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "plan table allocation failed");
+  if (cudaMemcpy(base, buf.data(), buf.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(base);
+    return fail(CGTP_ECUDA, "plan table upload failed");
+  }
+  auto at = [&](size_t off) { return static_cast<unsigned char*>(base) + off; };
+  V3Dev& v = plan->v3;
+  v.base = base;
+  v.lpe = lpe;
+  v.paths = plan->conv_layout.paths;  // global offsets off1, off2, ooff, woff
+  v.item_begin = reinterpret_cast<const int*>(at(o_ib));
+  v.items = reinterpret_cast<const Item*>(at(o_it));
+  v.gxp_off = reinterpret_cast<const int*>(at(o_gxo));
+  v.gxp_size = gxp;
+  v.in1_off = reinterpret_cast<const int*>(at(o_in1));
+  v.n_in1 = int(plan->in1.size());
+  v.gx_begin = reinterpret_cast<const int*>(at(o_gxb));
+  v.gx_paths = reinterpret_cast<const int*>(at(o_gxq));
+  const size_t es = plan->dtype == CGTP_F64 ? 8 : 4;
+  v.chunk_b = 64;
+  auto smem = [&](int cb) { return es * (size_t(gxp + 3) / 4 * 4 + size_t(kWarps) * cb * plan->d2); };
+  while (v.chunk_b > 8 && smem(v.chunk_b) > 200 * 1024) v.chunk_b /= 2;
+  v.smem_bwd = smem(v.chunk_b);
+  if (v.smem_bwd > 220 * 1024) v.lpe = 0;  // gx partials too large: the general kernels serve this plan
+  return CGTP_OK;
+}
+
+void free_v3(cgtp_plan_s* plan) {
+  if (plan->v3.base) cudaFree(plan->v3.base);
+  plan->v3 = V3Dev{};
+}
+
+bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
+                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st) {
+  using namespace uvu3_detail;
+  if (!plan->v3.lpe || std::getenv("CGTP_UVU_NO_V3")) return false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f64 = plan->dtype == CGTP_F64;
+  switch (plan->v3.lpe) {
+    case 2: *st = f64 ? fwd3_launch<double, 2>(plan, x, Y, W, out, rowptr, col, N, s)
+                      : fwd3_launch<float, 2>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+    case 8: *st = f64 ? fwd3_launch<double, 8>(plan, x, Y, W, out, rowptr, col, N, s)
+                      : fwd3_launch<float, 8>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+    case 32: *st = f64 ? fwd3_launch<double, 32>(plan, x, Y, W, out, rowptr, col, N, s)
+                       : fwd3_launch<float, 32>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+    default: return false;
+  }
+}
+
+bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
+                        const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
+                        const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
+                        cgtp_status* st) {
+  using namespace uvu3_detail;
+  if (!plan->v3.lpe || std::getenv("CGTP_UVU_NO_V3")) return false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f64 = plan->dtype == CGTP_F64;
+#define V3B(T, L) bwd3_launch<T, L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
+  switch (plan->v3.lpe) {
+    case 2: *st = f64 ? V3B(double, 2) : V3B(float, 2); return true;
+    case 8: *st = f64 ? V3B(double, 8) : V3B(float, 8); return true;
+    case 32: *st = f64 ? V3B(double, 32) : V3B(float, 32); return true;
+    default: return false;
+  }
+#undef V3B
+}
+
+}  // namespace cgtp

@@ -1,0 +1,457 @@
+// uvu3_impl.cuh -- warp-autonomous uvu convolution kernels for plans with l <= 3.
+//
+// Same operation as uvu_impl.cuh ("An Efficient Sparse Kernel Generator for
+// O(3)-Equivariant Deep Networks", Figure 4B: the CG tensor product fused with
+// the receiver sum; gradients from its Abstract).  GB300 organisation:
+//   * a lane owns four consecutive channels u of one edge; mul/4 lanes (LPE)
+//     cover a path's channels, so one warp instruction advances 32/LPE edges;
+//   * the CG nonzeros of each (l1, l2, l3) are compiled in as immediates
+//     (cg_baked.cuh, generated from the planner's Racah tables), so every lane
+//     forms its edge's coupling matrix cy[m1][m3] = sum_m2 C Y[m2] in registers
+//     -- no shared tables, no block-wide barriers in the forward;
+//   * node features, weights and output gradients arrive as 128-bit loads of
+//     four channels; the channel pairs (u0,u1), (u2,u3) go through the paired
+//     FP32 FMA (fma.rn.f32x2);
+//   * sums over the edge slots of a warp use xor shuffles; the backward's gY
+//     contraction applies the baked C per lane first, so only 2l2+1 values per
+//     (edge, path) cross lanes;
+//   * every result is written once by its owner (receiver or sender): no atomics.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace cgtp {
+namespace uvu3_detail {
+
+__host__ __device__ inline int pad_up(int v, int q) { return (v + q - 1) / q * q; }
+
+template <typename T>
+struct PairT;
+template <>
+struct PairT<float> {
+  using P = float2;
+};
+template <>
+struct PairT<double> {
+  using P = double2;
+};
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<unsigned long long*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ double2 fma2(double2 a, double2 b, double2 c) {
+  return make_double2(fma(a.x, b.x, c.x), fma(a.y, b.y, c.y));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ double2 mul2(double2 a, double2 b) { return make_double2(a.x * b.x, a.y * b.y); }
+
+template <typename T>
+__device__ __forceinline__ T shfl_x(T v, int o) {
+  return __shfl_xor_sync(0xffffffffu, v, o);
+}
+
+// Sum V values over the L lanes of a lane group (L a power of two <= 32; the
+// group's lanes differ in the low log2(L) bits of q).  Recursive halving: after
+// the call lane q of the group holds slots [q*V/L, (q+1)*V/L) of the group
+// total in v[0 .. V/L).  V must be a multiple of L.
+template <typename T, int V, int O, int N>
+__device__ __forceinline__ void gr_step(T (&v)[V], int q) {
+  if constexpr (O >= 1) {
+    constexpr int H = N / 2;
+    const bool up = (q & O) != 0;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const T send = up ? v[i] : v[i + H];
+      const T keep = up ? v[i + H] : v[i];
+      v[i] = keep + shfl_x(send, O);
+    }
+    gr_step<T, V, O / 2, H>(v, q);
+  }
+}
+template <typename T, int V, int L>
+__device__ __forceinline__ void group_reduce(T (&v)[V], int q) {
+  static_assert(V % L == 0, "pad V to a multiple of L");
+  gr_step<T, V, L / 2, V>(v, q);
+}
+
+}  // namespace uvu3_detail
+}  // namespace cgtp
+
+#include "cg_baked.cuh"
+
+namespace cgtp {
+namespace uvu3_detail {
+
+template <typename T>
+struct Uvu3Args {
+  const T* x;
+  const T* Y;
+  const T* W;
+  const T* gout;
+  T* out;
+  T* gx;
+  T* gY;
+  T* gW;
+  const int* rowptr;  // forward: CSR rowptr; backward: transpose rowptr
+  const int* col;     // forward: CSR col; backward: transpose edge ids
+  const int* t_dst;
+  int N, d1, d2, d_out, w_numel;
+  const PathDev* paths;
+  const int* item_begin;  // kWarps + 1
+  const Item* items;
+  // backward
+  const int* gxp_off;     // per path: offset of its [mul][D1] partial in the gx buffer
+  int gxp_size;
+  const int* in1_off;     // n_in1 + 1
+  int n_in1;
+  const int* gx_begin;    // n_in1 + 1 offsets into gx_paths
+  const int* gx_paths;
+  int chunk_b;            // edges of a sender processed per round (bounded by shared memory)
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void ldvec(const T* p, T (&v)[N]) {  // N consecutive, 16-byte aligned
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p) + i);
+      v[4 * i] = q.x;
+      v[4 * i + 1] = q.y;
+      v[4 * i + 2] = q.z;
+      v[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const double2 q = __ldg(reinterpret_cast<const double2*>(p) + i);
+      v[2 * i] = q.x;
+      v[2 * i + 1] = q.y;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes
+// ---------------------------------------------------------------------------
+template <typename T, int LPE, int L1, int L2, int L3>
+__device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
+                                       const T* __restrict__ W, T* __restrict__ out,
+                                       const int* __restrict__ col, int e_begin, int deg, int n,
+                                       int d1, int d2, int d_out, int w_numel, int off1, int off2,
+                                       int ooff, int woff, int u, bool active, int g) {
+  using P = typename PairT<T>::P;
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1, NF = D1 * D3;
+  constexpr int EPW = 32 / LPE;
+  P t01[D3], t23[D3];
+#pragma unroll
+  for (int k = 0; k < D3; ++k) t01[k] = t23[k] = P{T(0), T(0)};
+  if (active) {
+    for (int j = g; j < deg; j += EPW) {
+      const int e = e_begin + j;
+      const int s = __ldg(col + e);
+      T yv[D2];
+#pragma unroll
+      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+      T xs[4 * D1];
+      ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, xs);
+      T wv[4];
+      ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
+      T cy[NF];
+#pragma unroll
+      for (int f = 0; f < NF; ++f) cy[f] = T(0);
+      CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
+#pragma unroll
+      for (int m1 = 0; m1 < D1; ++m1) {
+        const P xw01{wv[0] * xs[m1], wv[1] * xs[D1 + m1]};
+        const P xw23{wv[2] * xs[2 * D1 + m1], wv[3] * xs[3 * D1 + m1]};
+#pragma unroll
+        for (int m3 = 0; m3 < D3; ++m3) {
+          const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
+          t01[m3] = fma2(cp, xw01, t01[m3]);
+          t23[m3] = fma2(cp, xw23, t23[m3]);
+        }
+      }
+    }
+  }
+  T v[4 * D3];
+#pragma unroll
+  for (int m = 0; m < D3; ++m) {
+    v[m] = t01[m].x;
+    v[D3 + m] = t01[m].y;
+    v[2 * D3 + m] = t23[m].x;
+    v[3 * D3 + m] = t23[m].y;
+  }
+#pragma unroll
+  for (int o = 16; o >= LPE; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4 * D3; ++i) v[i] += shfl_x(v[i], o);
+  if (active && g == 0) {
+    T* dst = out + (size_t)n * d_out + ooff + u * D3;
+#pragma unroll
+    for (int i = 0; i < 4 * D3; ++i) dst[i] = v[i];
+  }
+}
+
+#define CGTP3_TRIPLES(M)                                                                          \
+  M(0, 0, 0) M(0, 1, 1) M(0, 2, 2) M(0, 3, 3) M(1, 0, 1) M(1, 1, 0) M(1, 1, 1) M(1, 1, 2)         \
+  M(1, 2, 1) M(1, 2, 2) M(1, 2, 3) M(1, 3, 2) M(1, 3, 3) M(2, 0, 2) M(2, 1, 1) M(2, 1, 2)         \
+  M(2, 1, 3) M(2, 2, 0) M(2, 2, 1) M(2, 2, 2) M(2, 2, 3) M(2, 3, 1) M(2, 3, 2) M(2, 3, 3)         \
+  M(3, 0, 3) M(3, 1, 2) M(3, 1, 3) M(3, 2, 1) M(3, 2, 2) M(3, 2, 3) M(3, 3, 0) M(3, 3, 1)         \
+  M(3, 3, 2) M(3, 3, 3) M(1, 3, 4) M(0, 0, 1)
+
+// only triangle-valid triples with l <= 3 are instantiated; the two trailing
+// entries above are placeholders that never match a path (l3 = 4, or 0x0->1).
+#define CGTP3_FWD_CASE(L1, L2, L3)                                                                  \
+  case (L1)*16 + (L2)*4 + (L3):                                                                     \
+    if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
+      fwd3_item<T, LPE, L1, L2, L3>(a.x, a.Y, a.W, a.out, a.col, e_begin, deg, n, a.d1, a.d2, a.d_out, \
+                                    a.w_numel, p.off1, p.off2, p.ooff, p.woff, u, active, g);      \
+    break;
+
+template <typename T, int LPE>
+__global__ void __launch_bounds__(kThreads, 1) uvu_forward3_kernel(const Uvu3Args<T> a) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = lane % LPE, g = lane / LPE;
+  __shared__ int s_range[2];
+  if (tid == 0) {
+    const long long total = (long long)a.rowptr[a.N] + a.N;
+    const long long t0 = total * blockIdx.x / gridDim.x, t1 = total * (blockIdx.x + 1) / gridDim.x;
+    auto lb = [&](long long target) {
+      int lo = 0, hi = a.N;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)a.rowptr[mid] + mid < target) lo = mid + 1; else hi = mid;
+      }
+      return lo;
+    };
+    s_range[0] = lb(t0);
+    s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.N : lb(t1);
+  }
+  __syncthreads();
+  const int nb = s_range[0], ne = s_range[1];
+  const int ib = a.item_begin[warp], ie = a.item_begin[warp + 1];
+  for (int n = nb; n < ne; ++n) {
+    const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
+    for (int it = ib; it < ie; ++it) {
+      const Item item = a.items[it];
+      const PathDev p = a.paths[item.path];
+      const int u = item.u0 + 4 * q;
+      const bool active = u < p.mul;
+      switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+        CGTP3_TRIPLES(CGTP3_FWD_CASE)
+        default: break;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward: one (sender, path, channel block) per call over `cnt` out-edges
+// ---------------------------------------------------------------------------
+template <typename T, int LPE, int L1, int L2, int L3>
+__device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
+                                       const T* __restrict__ W, const T* __restrict__ gout,
+                                       T* __restrict__ gW, const int* __restrict__ t_eid,
+                                       const int* __restrict__ t_dst, int te_begin, int cnt, int s,
+                                       int d1, int d2, int d_out, int w_numel, int off1, int off2,
+                                       int ooff, int woff, int u, bool active, int g, int q,
+                                       T* gyw, T* gxp_path) {
+  using P = typename PairT<T>::P;
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1, NF = D1 * D3;
+  constexpr int EPW = 32 / LPE;
+  constexpr int HV = (D2 + LPE - 1) / LPE * LPE;  // h values padded to a multiple of LPE
+  T xs[4 * D1];
+  if (active) {
+    ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, xs);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4 * D1; ++i) xs[i] = T(0);
+  }
+  P x01[D1], x23[D1], gxa01[D1], gxa23[D1];
+#pragma unroll
+  for (int m = 0; m < D1; ++m) {
+    x01[m] = P{xs[m], xs[D1 + m]};
+    x23[m] = P{xs[2 * D1 + m], xs[3 * D1 + m]};
+    gxa01[m] = gxa23[m] = P{T(0), T(0)};
+  }
+  for (int j0 = 0; j0 < cnt; j0 += EPW) {  // uniform trip count: the h reduction shuffles
+    const int j = j0 + g;
+    const bool valid = active && j < cnt;
+    int e = 0, d = 0;
+    T yv[D2], gs[4 * D3], wv[4];
+    if (valid) {
+      e = __ldg(t_eid + te_begin + j);
+      d = __ldg(t_dst + te_begin + j);
+#pragma unroll
+      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+      ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
+      ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
+    } else {
+#pragma unroll
+      for (int m = 0; m < D2; ++m) yv[m] = T(0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wv[i] = T(0);
+#pragma unroll
+      for (int i = 0; i < 4 * D3; ++i) gs[i] = T(0);
+    }
+    T cy[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) cy[f] = T(0);
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
+    P wg01[D3], wg23[D3];
+    T gw[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+    for (int m3 = 0; m3 < D3; ++m3) {
+      wg01[m3] = P{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
+      wg23[m3] = P{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
+      P t01{T(0), T(0)}, t23{T(0), T(0)};
+#pragma unroll
+      for (int m1 = 0; m1 < D1; ++m1) {
+        const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
+        t01 = fma2(cp, x01[m1], t01);
+        t23 = fma2(cp, x23[m1], t23);
+        gxa01[m1] = fma2(cp, wg01[m3], gxa01[m1]);
+        gxa23[m1] = fma2(cp, wg23[m3], gxa23[m1]);
+      }
+      gw[0] += gs[m3] * t01.x;
+      gw[1] += gs[D3 + m3] * t01.y;
+      gw[2] += gs[2 * D3 + m3] * t23.x;
+      gw[3] += gs[3 * D3 + m3] * t23.y;
+    }
+    if (valid) {
+      T* gp = gW + (size_t)e * w_numel + woff + u;
+      if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4*>(gp) = make_float4(gw[0], gw[1], gw[2], gw[3]);
+      } else {
+        reinterpret_cast<double2*>(gp)[0] = make_double2(gw[0], gw[1]);
+        reinterpret_cast<double2*>(gp)[1] = make_double2(gw[2], gw[3]);
+      }
+    }
+    // h[m2] = sum C[m1,m2,m3] sum_{lane's channels} x[u][m1] w_u g[u][m3]
+    T h[HV];
+#pragma unroll
+    for (int i = 0; i < HV; ++i) h[i] = T(0);
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) {
+      const P pr = fma2(x23[m1], wg23[m3], mul2(x01[m1], wg01[m3]));
+      h[m2] += T(c) * (pr.x + pr.y);
+    });
+    group_reduce<T, HV, LPE>(h, q);
+    if (j < cnt) {
+#pragma unroll
+      for (int k = 0; k < HV / LPE; ++k) {
+        const int slot = q * (HV / LPE) + k;
+        if (slot < D2) gyw[j * d2 + off2 + slot] += h[k];
+      }
+    }
+  }
+  // gx partial of this path: sum over the edge slots, slot 0 accumulates into shared memory
+  T v[4 * D1];
+#pragma unroll
+  for (int m = 0; m < D1; ++m) {
+    v[m] = gxa01[m].x;
+    v[D1 + m] = gxa01[m].y;
+    v[2 * D1 + m] = gxa23[m].x;
+    v[3 * D1 + m] = gxa23[m].y;
+  }
+#pragma unroll
+  for (int o = 16; o >= LPE; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4 * D1; ++i) v[i] += shfl_x(v[i], o);
+  if (active && g == 0) {
+    T* dst = gxp_path + u * D1;
+#pragma unroll
+    for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
+  }
+}
+
+#define CGTP3_BWD_CASE(L1, L2, L3)                                                                   \
+  case (L1)*16 + (L2)*4 + (L3):                                                                      \
+    if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
+      bwd3_item<T, LPE, L1, L2, L3>(a.x, a.Y, a.W, a.gout, a.gW, a.col, a.t_dst, te0, cnt, s, a.d1,  \
+                                    a.d2, a.d_out, a.w_numel, p.off1, p.off2, p.ooff, p.woff, u,     \
+                                    active, g, q, gyw, gxp + a.gxp_off[item.path]);                  \
+    break;
+
+template <typename T, int LPE>
+__global__ void __launch_bounds__(kThreads, 1) uvu_backward3_kernel(const Uvu3Args<T> a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = lane % LPE, g = lane / LPE;
+  T* gxp = reinterpret_cast<T*>(smem);                       // [gxp_size]
+  T* gyw_all = gxp + pad_up(a.gxp_size, 4);                  // [kWarps][chunk_b][d2]
+  T* gyw = gyw_all + warp * a.chunk_b * a.d2;
+  __shared__ int s_range[2];
+  if (tid == 0) {
+    const long long total = (long long)a.rowptr[a.N] + a.N;
+    const long long t0 = total * blockIdx.x / gridDim.x, t1 = total * (blockIdx.x + 1) / gridDim.x;
+    auto lb = [&](long long target) {
+      int lo = 0, hi = a.N;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)a.rowptr[mid] + mid < target) lo = mid + 1; else hi = mid;
+      }
+      return lo;
+    };
+    s_range[0] = lb(t0);
+    s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.N : lb(t1);
+  }
+  __syncthreads();
+  const int sb = s_range[0], se = s_range[1];
+  const int ib = a.item_begin[warp], ie = a.item_begin[warp + 1];
+  for (int s = sb; s < se; ++s) {
+    const int tb = a.rowptr[s], te = a.rowptr[s + 1];
+    for (int i = tid; i < a.gxp_size; i += kThreads) gxp[i] = T(0);
+    for (int te0 = tb; te0 < te || te0 == tb; te0 += a.chunk_b) {
+      const int cnt = min(a.chunk_b, te - te0);
+      for (int i = lane; i < a.chunk_b * a.d2; i += 32) gyw[i] = T(0);
+      __syncthreads();  // gxp zeroing (first round) and the previous round's reads are done
+      for (int it = ib; it < ie && cnt > 0; ++it) {
+        const Item item = a.items[it];
+        const PathDev p = a.paths[item.path];
+        const int u = item.u0 + 4 * q;
+        const bool active = u < p.mul;
+        switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+          CGTP3_TRIPLES(CGTP3_BWD_CASE)
+          default: break;
+        }
+      }
+      __syncthreads();
+      // gY of this round's edges: sum of the warps' partials, in warp order
+      for (int i = tid; i < cnt * a.d2; i += kThreads) {
+        const int j = i / a.d2, c = i - j * a.d2;
+        T v = T(0);
+        for (int w = 0; w < kWarps; ++w) v += gyw_all[(w * a.chunk_b + j) * a.d2 + c];
+        const int e = a.col[te0 + j];
+        a.gY[(size_t)e * a.d2 + c] = v;
+      }
+      if (te0 + a.chunk_b >= te) break;
+    }
+    __syncthreads();
+    // gx[s] = sum over paths of the partials, in path order
+    for (int b = 0; b < a.n_in1; ++b) {
+      const int o0 = a.in1_off[b], len = a.in1_off[b + 1] - o0;
+      const int q0 = a.gx_begin[b], q1 = a.gx_begin[b + 1];
+      for (int i = tid; i < len; i += kThreads) {
+        T v = T(0);
+        for (int k = q0; k < q1; ++k) v += gxp[a.gxp_off[a.gx_paths[k]] + i];
+        a.gx[(size_t)s * a.d1 + o0 + i] = v;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace uvu3_detail
+}  // namespace cgtp
