@@ -113,7 +113,8 @@ struct V3Dev {
   int lpe = 0;
   const PathDev* paths = nullptr;
   const int* item_begin = nullptr;
-  const Item* items = nullptr;
+  const Item* items = nullptr;    // path order
+  int n_items = 0;
   const int* gxp_off = nullptr;
   int gxp_size = 0;
   const int* in1_off = nullptr;

@@ -33,29 +33,12 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   else if (m % 128 == 0) lpe = 32;
   if (!lpe) return CGTP_OK;
   const int ublock = 4 * lpe;
-  // work items: (path, channel block), longest first onto the least loaded warp
-  struct It { int path, u0; double cost; };
-  std::vector<It> its;
-  for (size_t p = 0; p < plan->paths.size(); ++p) {
-    const auto& q = plan->paths[p];
-    const int D1 = 2 * q.l1 + 1, D3 = 2 * q.l3 + 1;
-    for (int u0 = 0; u0 < q.mul1; u0 += ublock) its.push_back({int(p), u0, double(D1 * D3 + 2 * D1 + D3 + 8)});
-  }
-  std::stable_sort(its.begin(), its.end(), [](const It& a, const It& b) { return a.cost > b.cost; });
-  std::vector<std::vector<Item>> per(kWarps);
-  std::vector<double> load(kWarps, 0.0);
-  for (const auto& it : its) {
-    const int w = int(std::min_element(load.begin(), load.end()) - load.begin());
-    per[w].push_back({it.path, it.u0});
-    load[w] += it.cost;
-  }
-  std::vector<int> item_begin;
+  // work items: (path, channel block) in path order -- the kernels walk them
+  // path-major, all warps of a CTA on the same path at a time
   std::vector<Item> items;
-  for (int w = 0; w < kWarps; ++w) {
-    item_begin.push_back(int(items.size()));
-    for (auto& i : per[w]) items.push_back(i);
-  }
-  item_begin.push_back(int(items.size()));
+  for (size_t p = 0; p < plan->paths.size(); ++p)
+    for (int u0 = 0; u0 < plan->paths[p].mul1; u0 += ublock) items.push_back({int(p), u0});
+  std::vector<int> item_begin = {0, int(items.size())};
   // gx partial buffer: one [mul][D1] block per path
   std::vector<int> gxp_off;
   int gxp = 0;
@@ -104,6 +87,7 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   v.paths = plan->conv_layout.paths;  // global offsets off1, off2, ooff, woff
   v.item_begin = reinterpret_cast<const int*>(at(o_ib));
   v.items = reinterpret_cast<const Item*>(at(o_it));
+  v.n_items = int(items.size());
   v.gxp_off = reinterpret_cast<const int*>(at(o_gxo));
   v.gxp_size = gxp;
   v.in1_off = reinterpret_cast<const int*>(at(o_in1));

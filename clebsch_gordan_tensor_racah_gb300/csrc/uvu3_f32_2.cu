@@ -15,8 +15,8 @@ Uvu3Args<T> v3_args(const cgtp_plan_s* plan) {
   a.d_out = static_cast<int>(plan->d_out);
   a.w_numel = static_cast<int>(plan->w_numel);
   a.paths = v.paths;
-  a.item_begin = v.item_begin;
   a.items = v.items;
+  a.n_items = v.n_items;
   a.gxp_off = v.gxp_off;
   a.gxp_size = v.gxp_size;
   a.in1_off = v.in1_off;
@@ -66,9 +66,7 @@ cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x
   a.t_dst = t_dst;
   a.N = static_cast<int>(N);
   auto k = uvu_backward3_kernel<T, LPE>;
-  const size_t smem = plan->v3.smem_bwd;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return fail(CGTP_ECUDA, "uvu backward (v3): shared memory attribute rejected");
+  const size_t smem = 0;
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
   per_sm = std::max(per_sm, 1);

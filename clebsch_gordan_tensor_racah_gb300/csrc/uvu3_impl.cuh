@@ -109,8 +109,8 @@ struct Uvu3Args {
   const int* t_dst;
   int N, d1, d2, d_out, w_numel;
   const PathDev* paths;
-  const int* item_begin;  // kWarps + 1
-  const Item* items;
+  const Item* items;      // in path order (path-major schedule)
+  int n_items;
   // backward
   const int* gxp_off;     // per path: offset of its [mul][D1] partial in the gx buffer
   int gxp_size;
@@ -241,14 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1) uvu_forward3_kernel(const Uvu3Arg
   }
   __syncthreads();
   const int nb = s_range[0], ne = s_range[1];
-  const int ib = a.item_begin[warp], ie = a.item_begin[warp + 1];
-  for (int n = nb; n < ne; ++n) {
-    const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
-    for (int it = ib; it < ie; ++it) {
-      const Item item = a.items[it];
-      const PathDev p = a.paths[item.path];
-      const int u = item.u0 + 4 * q;
-      const bool active = u < p.mul;
+  // path-major: every warp of the CTA works on the same path at a time (one hot
+  // instruction stream per SM); the CTA's receivers are strided over its warps
+  for (int it = 0; it < a.n_items; ++it) {
+    const Item item = a.items[it];
+    const PathDev p = a.paths[item.path];
+    const int u = item.u0 + 4 * q;
+    const bool active = u < p.mul;
+    for (int n = nb + warp; n < ne; n += kWarps) {
+      const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_FWD_CASE)
         default: break;
@@ -267,7 +268,7 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
                                        const int* __restrict__ t_dst, int te_begin, int cnt, int s,
                                        int d1, int d2, int d_out, int w_numel, int off1, int off2,
                                        int ooff, int woff, int u, bool active, int g, int q,
-                                       T* gyw, T* gxp_path) {
+                                       T* __restrict__ gY, T* __restrict__ gx) {
   using P = typename PairT<T>::P;
   constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1, NF = D1 * D3;
   constexpr int EPW = 32 / LPE;
@@ -348,11 +349,11 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
       h[m2] += T(c) * (pr.x + pr.y);
     });
     group_reduce<T, HV, LPE>(h, q);
-    if (j < cnt) {
+    if (valid) {  // this warp owns edge e: read-modify-write in path order
 #pragma unroll
       for (int k = 0; k < HV / LPE; ++k) {
         const int slot = q * (HV / LPE) + k;
-        if (slot < D2) gyw[j * d2 + off2 + slot] += h[k];
+        if (slot < D2) gY[(size_t)e * d2 + off2 + slot] += h[k];
       }
     }
   }
@@ -369,8 +370,8 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
   for (int o = 16; o >= LPE; o >>= 1)
 #pragma unroll
     for (int i = 0; i < 4 * D1; ++i) v[i] += shfl_x(v[i], o);
-  if (active && g == 0) {
-    T* dst = gxp_path + u * D1;
+  if (active && g == 0) {  // this warp owns sender s
+    T* dst = gx + (size_t)s * d1 + off1 + u * D1;
 #pragma unroll
     for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
   }
@@ -381,17 +382,13 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
       bwd3_item<T, LPE, L1, L2, L3>(a.x, a.Y, a.W, a.gout, a.gW, a.col, a.t_dst, te0, cnt, s, a.d1,  \
                                     a.d2, a.d_out, a.w_numel, p.off1, p.off2, p.ooff, p.woff, u,     \
-                                    active, g, q, gyw, gxp + a.gxp_off[item.path]);                  \
+                                    active, g, q, a.gY, a.gx);                                       \
     break;
 
 template <typename T, int LPE>
 __global__ void __launch_bounds__(kThreads, 1) uvu_backward3_kernel(const Uvu3Args<T> a) {
-  extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
-  T* gxp = reinterpret_cast<T*>(smem);                       // [gxp_size]
-  T* gyw_all = gxp + pad_up(a.gxp_size, 4);                  // [kWarps][chunk_b][d2]
-  T* gyw = gyw_all + warp * a.chunk_b * a.d2;
   __shared__ int s_range[2];
   if (tid == 0) {
     const long long total = (long long)a.rowptr[a.N] + a.N;
@@ -409,47 +406,30 @@ __global__ void __launch_bounds__(kThreads, 1) uvu_backward3_kernel(const Uvu3Ar
   }
   __syncthreads();
   const int sb = s_range[0], se = s_range[1];
-  const int ib = a.item_begin[warp], ie = a.item_begin[warp + 1];
-  for (int s = sb; s < se; ++s) {
+  // the warp that owns sender s (s - sb) % kWarps clears gx[s] and gY of its out-edges,
+  // then accumulates into them path by path; nobody else touches those rows
+  for (int s = sb + warp; s < se; s += kWarps) {
+    for (int i = lane; i < a.d1; i += 32) a.gx[(size_t)s * a.d1 + i] = T(0);
     const int tb = a.rowptr[s], te = a.rowptr[s + 1];
-    for (int i = tid; i < a.gxp_size; i += kThreads) gxp[i] = T(0);
-    for (int te0 = tb; te0 < te || te0 == tb; te0 += a.chunk_b) {
-      const int cnt = min(a.chunk_b, te - te0);
-      for (int i = lane; i < a.chunk_b * a.d2; i += 32) gyw[i] = T(0);
-      __syncthreads();  // gxp zeroing (first round) and the previous round's reads are done
-      for (int it = ib; it < ie && cnt > 0; ++it) {
-        const Item item = a.items[it];
-        const PathDev p = a.paths[item.path];
-        const int u = item.u0 + 4 * q;
-        const bool active = u < p.mul;
-        switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
-          CGTP3_TRIPLES(CGTP3_BWD_CASE)
-          default: break;
-        }
-      }
-      __syncthreads();
-      // gY of this round's edges: sum of the warps' partials, in warp order
-      for (int i = tid; i < cnt * a.d2; i += kThreads) {
-        const int j = i / a.d2, c = i - j * a.d2;
-        T v = T(0);
-        for (int w = 0; w < kWarps; ++w) v += gyw_all[(w * a.chunk_b + j) * a.d2 + c];
-        const int e = a.col[te0 + j];
-        a.gY[(size_t)e * a.d2 + c] = v;
-      }
-      if (te0 + a.chunk_b >= te) break;
+    for (int i = lane; i < (te - tb) * a.d2; i += 32) {
+      const int j = i / a.d2, c = i - j * a.d2;
+      a.gY[(size_t)a.col[tb + j] * a.d2 + c] = T(0);
     }
-    __syncthreads();
-    // gx[s] = sum over paths of the partials, in path order
-    for (int b = 0; b < a.n_in1; ++b) {
-      const int o0 = a.in1_off[b], len = a.in1_off[b + 1] - o0;
-      const int q0 = a.gx_begin[b], q1 = a.gx_begin[b + 1];
-      for (int i = tid; i < len; i += kThreads) {
-        T v = T(0);
-        for (int k = q0; k < q1; ++k) v += gxp[a.gxp_off[a.gx_paths[k]] + i];
-        a.gx[(size_t)s * a.d1 + o0 + i] = v;
+  }
+  __syncwarp();
+  // path-major: one hot instruction stream per SM
+  for (int it = 0; it < a.n_items; ++it) {
+    const Item item = a.items[it];
+    const PathDev p = a.paths[item.path];
+    const int u = item.u0 + 4 * q;
+    const bool active = u < p.mul;
+    for (int s = sb + warp; s < se; s += kWarps) {
+      const int te0 = a.rowptr[s], cnt = a.rowptr[s + 1] - te0;
+      switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+        CGTP3_TRIPLES(CGTP3_BWD_CASE)
+        default: break;
       }
     }
-    __syncthreads();
   }
 }
 
