@@ -145,6 +145,59 @@ __device__ __forceinline__ void ldvec(const T* p, T (&v)[N]) {  // N consecutive
 // ---------------------------------------------------------------------------
 // forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes
 // ---------------------------------------------------------------------------
+template <typename T, int D1, int D2, int D3>
+struct FwdEdge {  // one edge's operands, loaded before any arithmetic
+  T yv[D2];
+  T xs[4 * D1];
+  T wv[4];
+};
+
+template <typename T, int LPE, int L1, int L2, int L3>
+__device__ __forceinline__ void fwd3_load(FwdEdge<T, 2 * L1 + 1, 2 * L2 + 1, 2 * L3 + 1>& E,
+                                          const T* __restrict__ x, const T* __restrict__ Y,
+                                          const T* __restrict__ W, int e, int s, bool ok, int d1,
+                                          int d2, int w_numel, int off1, int off2, int woff, int u) {
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1;
+  if (ok) {
+#pragma unroll
+    for (int m = 0; m < D2; ++m) E.yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+    ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, E.xs);
+    ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, E.wv);
+  } else {
+#pragma unroll
+    for (int m = 0; m < D2; ++m) E.yv[m] = T(0);
+#pragma unroll
+    for (int i = 0; i < 4 * D1; ++i) E.xs[i] = T(0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) E.wv[i] = T(0);
+  }
+}
+
+template <typename T, int LPE, int L1, int L2, int L3>
+__device__ __forceinline__ void fwd3_math(const FwdEdge<T, 2 * L1 + 1, 2 * L2 + 1, 2 * L3 + 1>& E,
+                                          typename PairT<T>::P (&t01)[2 * L3 + 1],
+                                          typename PairT<T>::P (&t23)[2 * L3 + 1]) {
+  using P = typename PairT<T>::P;
+  constexpr int D1 = 2 * L1 + 1, D3 = 2 * L3 + 1, NF = D1 * D3;
+  T cy[NF];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) cy[f] = T(0);
+  CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * E.yv[m2]; });
+#pragma unroll
+  for (int m1 = 0; m1 < D1; ++m1) {
+    const P xw01{E.wv[0] * E.xs[m1], E.wv[1] * E.xs[D1 + m1]};
+    const P xw23{E.wv[2] * E.xs[2 * D1 + m1], E.wv[3] * E.xs[3 * D1 + m1]};
+#pragma unroll
+    for (int m3 = 0; m3 < D3; ++m3) {
+      const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
+      t01[m3] = fma2(cp, xw01, t01[m3]);
+      t23[m3] = fma2(cp, xw23, t23[m3]);
+    }
+  }
+}
+
+// forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes;
+// each lane walks its edge slot two edges at a time, loads first
 template <typename T, int LPE, int L1, int L2, int L3>
 __device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
                                        const T* __restrict__ W, T* __restrict__ out,
@@ -152,37 +205,22 @@ __device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restr
                                        int d1, int d2, int d_out, int w_numel, int off1, int off2,
                                        int ooff, int woff, int u, bool active, int g) {
   using P = typename PairT<T>::P;
-  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1, NF = D1 * D3;
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1;
   constexpr int EPW = 32 / LPE;
   P t01[D3], t23[D3];
 #pragma unroll
   for (int k = 0; k < D3; ++k) t01[k] = t23[k] = P{T(0), T(0)};
   if (active) {
-    for (int j = g; j < deg; j += EPW) {
-      const int e = e_begin + j;
-      const int s = __ldg(col + e);
-      T yv[D2];
-#pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
-      T xs[4 * D1];
-      ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, xs);
-      T wv[4];
-      ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
-      T cy[NF];
-#pragma unroll
-      for (int f = 0; f < NF; ++f) cy[f] = T(0);
-      CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
-#pragma unroll
-      for (int m1 = 0; m1 < D1; ++m1) {
-        const P xw01{wv[0] * xs[m1], wv[1] * xs[D1 + m1]};
-        const P xw23{wv[2] * xs[2 * D1 + m1], wv[3] * xs[3 * D1 + m1]};
-#pragma unroll
-        for (int m3 = 0; m3 < D3; ++m3) {
-          const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
-          t01[m3] = fma2(cp, xw01, t01[m3]);
-          t23[m3] = fma2(cp, xw23, t23[m3]);
-        }
-      }
+    for (int j = g; j < deg; j += 2 * EPW) {
+      const int ja = j, jb = j + EPW;
+      const bool okb = jb < deg;
+      const int ea = e_begin + ja, eb = e_begin + (okb ? jb : ja);
+      const int sa = __ldg(col + ea), sb = __ldg(col + eb);
+      FwdEdge<T, D1, D2, D3> A, B;
+      fwd3_load<T, LPE, L1, L2, L3>(A, x, Y, W, ea, sa, true, d1, d2, w_numel, off1, off2, woff, u);
+      fwd3_load<T, LPE, L1, L2, L3>(B, x, Y, W, eb, sb, okb, d1, d2, w_numel, off1, off2, woff, u);
+      fwd3_math<T, LPE, L1, L2, L3>(A, t01, t23);
+      fwd3_math<T, LPE, L1, L2, L3>(B, t01, t23);
     }
   }
   T v[4 * D3];
@@ -221,7 +259,7 @@ __device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restr
     break;
 
 template <typename T, int LPE>
-__global__ void __launch_bounds__(kThreads, 1) uvu_forward3_kernel(const Uvu3Args<T> a) {
+__global__ void __launch_bounds__(kThreads, 2) uvu_forward3_kernel(const Uvu3Args<T> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
@@ -261,6 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1) uvu_forward3_kernel(const Uvu3Arg
 // ---------------------------------------------------------------------------
 // backward: one (sender, path, channel block) per call over `cnt` out-edges
 // ---------------------------------------------------------------------------
+// backward, one (sender, path, channel block) per call over the sender's
+// out-edges, in two passes whose loop bodies each fit the instruction cache:
+//   pass A: cy, t = cy.x -> gW (stored), gx partial (registers)
+//   pass B: h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over
+//           the path's lanes -> read-modify-write of gY (this warp owns the edge)
 template <typename T, int LPE, int L1, int L2, int L3>
 __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
                                        const T* __restrict__ W, const T* __restrict__ gout,
@@ -280,67 +323,99 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
 #pragma unroll
     for (int i = 0; i < 4 * D1; ++i) xs[i] = T(0);
   }
-  P x01[D1], x23[D1], gxa01[D1], gxa23[D1];
+  P x01[D1], x23[D1];
 #pragma unroll
   for (int m = 0; m < D1; ++m) {
     x01[m] = P{xs[m], xs[D1 + m]};
     x23[m] = P{xs[2 * D1 + m], xs[3 * D1 + m]};
-    gxa01[m] = gxa23[m] = P{T(0), T(0)};
   }
-  for (int j0 = 0; j0 < cnt; j0 += EPW) {  // uniform trip count: the h reduction shuffles
+  // ---- pass A
+  {
+    P gxa01[D1], gxa23[D1];
+#pragma unroll
+    for (int m = 0; m < D1; ++m) gxa01[m] = gxa23[m] = P{T(0), T(0)};
+    if (active) {
+      for (int j = g; j < cnt; j += EPW) {
+        const int e = __ldg(t_eid + te_begin + j), d = __ldg(t_dst + te_begin + j);
+        T yv[D2], gs[4 * D3], wv[4];
+#pragma unroll
+        for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+        ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
+        ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
+        T cy[NF];
+#pragma unroll
+        for (int f = 0; f < NF; ++f) cy[f] = T(0);
+        CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
+        T gw[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+        for (int m3 = 0; m3 < D3; ++m3) {
+          const P wg01{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
+          const P wg23{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
+          P t01{T(0), T(0)}, t23{T(0), T(0)};
+#pragma unroll
+          for (int m1 = 0; m1 < D1; ++m1) {
+            const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
+            t01 = fma2(cp, x01[m1], t01);
+            t23 = fma2(cp, x23[m1], t23);
+            gxa01[m1] = fma2(cp, wg01, gxa01[m1]);
+            gxa23[m1] = fma2(cp, wg23, gxa23[m1]);
+          }
+          gw[0] += gs[m3] * t01.x;
+          gw[1] += gs[D3 + m3] * t01.y;
+          gw[2] += gs[2 * D3 + m3] * t23.x;
+          gw[3] += gs[3 * D3 + m3] * t23.y;
+        }
+        T* gp = gW + (size_t)e * w_numel + woff + u;
+        if constexpr (sizeof(T) == 4) {
+          *reinterpret_cast<float4*>(gp) = make_float4(gw[0], gw[1], gw[2], gw[3]);
+        } else {
+          reinterpret_cast<double2*>(gp)[0] = make_double2(gw[0], gw[1]);
+          reinterpret_cast<double2*>(gp)[1] = make_double2(gw[2], gw[3]);
+        }
+      }
+    }
+    // gx partial of this path: sum over the edge slots; slot 0 accumulates (owner warp)
+    T v[4 * D1];
+#pragma unroll
+    for (int m = 0; m < D1; ++m) {
+      v[m] = gxa01[m].x;
+      v[D1 + m] = gxa01[m].y;
+      v[2 * D1 + m] = gxa23[m].x;
+      v[3 * D1 + m] = gxa23[m].y;
+    }
+#pragma unroll
+    for (int o = 16; o >= LPE; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < 4 * D1; ++i) v[i] += shfl_x(v[i], o);
+    if (active && g == 0) {
+      T* dst = gx + (size_t)s * d1 + off1 + u * D1;
+#pragma unroll
+      for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
+    }
+  }
+  // ---- pass B (uniform trip count: the h reduction shuffles across the path's lanes)
+  for (int j0 = 0; j0 < cnt; j0 += EPW) {
     const int j = j0 + g;
     const bool valid = active && j < cnt;
-    int e = 0, d = 0;
-    T yv[D2], gs[4 * D3], wv[4];
+    int e = 0;
+    T gs[4 * D3], wv[4];
     if (valid) {
       e = __ldg(t_eid + te_begin + j);
-      d = __ldg(t_dst + te_begin + j);
-#pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+      const int d = __ldg(t_dst + te_begin + j);
       ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
       ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
     } else {
-#pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = T(0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) wv[i] = T(0);
 #pragma unroll
       for (int i = 0; i < 4 * D3; ++i) gs[i] = T(0);
     }
-    T cy[NF];
-#pragma unroll
-    for (int f = 0; f < NF; ++f) cy[f] = T(0);
-    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
     P wg01[D3], wg23[D3];
-    T gw[4] = {T(0), T(0), T(0), T(0)};
 #pragma unroll
     for (int m3 = 0; m3 < D3; ++m3) {
       wg01[m3] = P{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
       wg23[m3] = P{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
-      P t01{T(0), T(0)}, t23{T(0), T(0)};
-#pragma unroll
-      for (int m1 = 0; m1 < D1; ++m1) {
-        const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
-        t01 = fma2(cp, x01[m1], t01);
-        t23 = fma2(cp, x23[m1], t23);
-        gxa01[m1] = fma2(cp, wg01[m3], gxa01[m1]);
-        gxa23[m1] = fma2(cp, wg23[m3], gxa23[m1]);
-      }
-      gw[0] += gs[m3] * t01.x;
-      gw[1] += gs[D3 + m3] * t01.y;
-      gw[2] += gs[2 * D3 + m3] * t23.x;
-      gw[3] += gs[3 * D3 + m3] * t23.y;
     }
-    if (valid) {
-      T* gp = gW + (size_t)e * w_numel + woff + u;
-      if constexpr (sizeof(T) == 4) {
-        *reinterpret_cast<float4*>(gp) = make_float4(gw[0], gw[1], gw[2], gw[3]);
-      } else {
-        reinterpret_cast<double2*>(gp)[0] = make_double2(gw[0], gw[1]);
-        reinterpret_cast<double2*>(gp)[1] = make_double2(gw[2], gw[3]);
-      }
-    }
-    // h[m2] = sum C[m1,m2,m3] sum_{lane's channels} x[u][m1] w_u g[u][m3]
     T h[HV];
 #pragma unroll
     for (int i = 0; i < HV; ++i) h[i] = T(0);
@@ -349,31 +424,13 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
       h[m2] += T(c) * (pr.x + pr.y);
     });
     group_reduce<T, HV, LPE>(h, q);
-    if (valid) {  // this warp owns edge e: read-modify-write in path order
+    if (valid) {
 #pragma unroll
       for (int k = 0; k < HV / LPE; ++k) {
         const int slot = q * (HV / LPE) + k;
         if (slot < D2) gY[(size_t)e * d2 + off2 + slot] += h[k];
       }
     }
-  }
-  // gx partial of this path: sum over the edge slots, slot 0 accumulates into shared memory
-  T v[4 * D1];
-#pragma unroll
-  for (int m = 0; m < D1; ++m) {
-    v[m] = gxa01[m].x;
-    v[D1 + m] = gxa01[m].y;
-    v[2 * D1 + m] = gxa23[m].x;
-    v[3 * D1 + m] = gxa23[m].y;
-  }
-#pragma unroll
-  for (int o = 16; o >= LPE; o >>= 1)
-#pragma unroll
-    for (int i = 0; i < 4 * D1; ++i) v[i] += shfl_x(v[i], o);
-  if (active && g == 0) {  // this warp owns sender s
-    T* dst = gx + (size_t)s * d1 + off1 + u * D1;
-#pragma unroll
-    for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
   }
 }
 
@@ -386,7 +443,7 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
     break;
 
 template <typename T, int LPE>
-__global__ void __launch_bounds__(kThreads, 1) uvu_backward3_kernel(const Uvu3Args<T> a) {
+__global__ void __launch_bounds__(kThreads, 2) uvu_backward3_kernel(const Uvu3Args<T> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
