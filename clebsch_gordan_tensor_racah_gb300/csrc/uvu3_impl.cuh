@@ -142,6 +142,23 @@ __device__ __forceinline__ void ldvec(const T* p, T (&v)[N]) {  // N consecutive
   }
 }
 
+// Rows [nb, ne) of a CTA split into contiguous warp ranges of about equal work
+// (edges + rows): warp w gets [lo, hi).
+__device__ __forceinline__ void warp_rows(const int* rowptr, int nb, int ne, int warp, int nwarps,
+                                          int* lo, int* hi) {
+  const long long w0 = (long long)rowptr[nb] + nb, w1 = (long long)rowptr[ne] + ne;
+  auto lb = [&](long long target) {
+    int a = nb, b = ne;
+    while (a < b) {
+      const int mid = (a + b) >> 1;
+      if ((long long)rowptr[mid] + mid < target) a = mid + 1; else b = mid;
+    }
+    return a;
+  };
+  *lo = lb(w0 + (w1 - w0) * warp / nwarps);
+  *hi = (warp + 1 == nwarps) ? ne : lb(w0 + (w1 - w0) * (warp + 1) / nwarps);
+}
+
 // ---------------------------------------------------------------------------
 // forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes
 // ---------------------------------------------------------------------------
@@ -279,14 +296,18 @@ __global__ void __launch_bounds__(kThreads, 2) uvu_forward3_kernel(const Uvu3Arg
   }
   __syncthreads();
   const int nb = s_range[0], ne = s_range[1];
-  // path-major: every warp of the CTA works on the same path at a time (one hot
-  // instruction stream per SM); the CTA's receivers are strided over its warps
+  int wlo, whi;
+  warp_rows(a.rowptr, nb, ne, warp, kWarps, &wlo, &whi);
+  // path-major: all warps of the CTA work on the same path (one hot instruction
+  // stream), each on an edge-balanced contiguous range of receivers; a barrier
+  // at each path boundary keeps them together
   for (int it = 0; it < a.n_items; ++it) {
     const Item item = a.items[it];
     const PathDev p = a.paths[item.path];
     const int u = item.u0 + 4 * q;
     const bool active = u < p.mul;
-    for (int n = nb + warp; n < ne; n += kWarps) {
+    if (it) __syncthreads();
+    for (int n = wlo; n < whi; ++n) {
       const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_FWD_CASE)
@@ -463,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 2) uvu_backward3_kernel(const Uvu3Ar
   }
   __syncthreads();
   const int sb = s_range[0], se = s_range[1];
-  // the warp that owns sender s (s - sb) % kWarps clears gx[s] and gY of its out-edges,
-  // then accumulates into them path by path; nobody else touches those rows
-  for (int s = sb + warp; s < se; s += kWarps) {
+  int wlo, whi;
+  warp_rows(a.rowptr, sb, se, warp, kWarps, &wlo, &whi);
+  // the warp that owns sender s clears gx[s] and gY of its out-edges, then
+  // accumulates into them path by path; nobody else touches those rows
+  for (int s = wlo; s < whi; ++s) {
     for (int i = lane; i < a.d1; i += 32) a.gx[(size_t)s * a.d1 + i] = T(0);
     const int tb = a.rowptr[s], te = a.rowptr[s + 1];
     for (int i = lane; i < (te - tb) * a.d2; i += 32) {
@@ -480,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 2) uvu_backward3_kernel(const Uvu3Ar
     const PathDev p = a.paths[item.path];
     const int u = item.u0 + 4 * q;
     const bool active = u < p.mul;
-    for (int s = sb + warp; s < se; s += kWarps) {
+    if (it) __syncthreads();
+    for (int s = wlo; s < whi; ++s) {
       const int te0 = a.rowptr[s], cnt = a.rowptr[s + 1] - te0;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_BWD_CASE)
