@@ -45,6 +45,7 @@ constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (CGTP_UV
 constexpr int kEdgeChunk = 16;      // edges staged per step of the edge stages
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
 constexpr int kBwdChunk = 8;        // edges staged per step of the backward edge stage
+constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over nodes
 
 struct UvwPath {
   int l1, l2, l3, D1, D2, D3, mul1, mul_out;
@@ -83,6 +84,7 @@ struct UvwState {
   int s_node = 0, a_node = 0;    // K * slice
   int chunk_nodes = kChunkNodes;
   float* scratch = nullptr;      // [2][chunk_nodes][s_node]
+  float* gm_part = nullptr;      // [kGmSplits][K][w_numel] split-K partials of gM
   size_t scratch_elems = 0;
   // GEMM descriptor tables (device) per use
   GemmProb* fwd_probs = nullptr;  int fwd_np = 0;  GemmSeg* fwd_segs = nullptr;
@@ -105,6 +107,10 @@ struct GemmLaunch {
   int nprob;
   const GemmProb* probs;
   const GemmSeg* segs;
+  // split-K over node-sized segments (K < 0): blockIdx.y takes node slice
+  // [y*ceil(nodes/splits), ...) and writes its partial to C + y*c_split_stride
+  int splits;
+  long long c_split_stride;
 };
 
 __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
@@ -132,32 +138,60 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
   const float* A = L.ptr[P.a_base];
   const float* B = L.ptr[P.b_base];
   float* C = const_cast<float*>(L.ptr[P.c_base]);
+  const int split = blockIdx.y;
+  const int slice = (L.nodes + L.splits - 1) / L.splits;
+  if (L.splits > 1) C += split * L.c_split_stride;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int r0 = rt * kGT, c0 = ct * kGT;
+  // each thread stages 8 (k, row) A elements and 8 (k, col) B elements per k tile
+  int arow_off[8];
+  bool arow_ok[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const int i = threadIdx.x + t * 256;
+    const int rr = i % kGT;
+    const int r = r0 + rr;
+    arow_ok[t] = r < rows;
+    const int n = arow_ok[t] ? r / P.D : 0, m = arow_ok[t] ? r - n * P.D : 0;
+    arow_off[t] = n * (int)P.a_n + m * (int)P.a_m;
+  }
   float acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  float ra[8], rb[8];
   for (int s = P.seg0; s < P.seg1; ++s) {
     const GemmSeg S = L.segs[s];
-    const int K = S.K < 0 ? L.nodes : S.K;
-    for (int k0 = 0; k0 < K; k0 += kGK) {
-      for (int i = threadIdx.x; i < kGK * kGT; i += 256) {
+    int kb = 0, ke = S.K < 0 ? L.nodes : S.K;
+    if (S.K < 0 && L.splits > 1) {
+      kb = min(L.nodes, split * slice);
+      ke = min(L.nodes, kb + slice);
+    }
+    const float* Ab = A + P.a_off + S.a_off;
+    const float* Bb = B + S.b_off;
+    auto fetch = [&](int k0) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int i = threadIdx.x + t * 256;
         const int kk = i / kGT, rr = i - kk * kGT;
-        const int r = r0 + rr, k = k0 + kk;
-        float v = 0.f;
-        if (r < rows && k < K) {
-          const int n = r / P.D, m = r - n * P.D;
-          v = A[P.a_off + S.a_off + n * P.a_n + m * P.a_m + (long long)k * S.a_k];
-        }
-        As[kk][rr] = v;
-        const int cc = rr, c = c0 + cc;
-        float b = 0.f;
-        if (c < P.J && k < K) b = B[S.b_off + (long long)k * S.b_k + (long long)c * S.b_j];
-        Bs[kk][cc] = b;
+        const int k = k0 + kk;
+        ra[t] = (arow_ok[t] && k < ke) ? __ldg(Ab + arow_off[t] + (long long)k * S.a_k) : 0.f;
+        const int c = c0 + rr;
+        rb[t] = (c < P.J && k < ke) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
+      }
+    };
+    if (kb < ke) fetch(kb);
+    for (int k0 = kb; k0 < ke; k0 += kGK) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int i = threadIdx.x + t * 256;
+        const int kk = i / kGT, rr = i - kk * kGT;
+        As[kk][rr] = ra[t];
+        Bs[kk][rr] = rb[t];
       }
       __syncthreads();
+      if (k0 + kGK < ke) fetch(k0 + kGK);  // next tile's loads overlap this tile's math
 #pragma unroll 8
       for (int kk = 0; kk < kGK; ++kk) {
         const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
@@ -171,6 +205,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
       __syncthreads();
     }
   }
+  const int beta = L.splits > 1 ? 0 : P.beta;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = r0 + ty * 4 + i;
@@ -181,8 +216,18 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
       const int c = c0 + tx * 4 + j;
       if (c >= P.J) continue;
       float* dst = C + P.c_off + n * P.c_n + m * P.c_m + (long long)c * P.c_j;
-      *dst = P.beta ? *dst + acc[i][j] : acc[i][j];
+      *dst = beta ? *dst + acc[i][j] : acc[i][j];
     }
+  }
+}
+
+// gM (+)= sum over the split-K partials, in split order (deterministic)
+__global__ void splitk_reduce_kernel(float* __restrict__ gM, const float* __restrict__ part, int splits,
+                                     long long n, int accumulate) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    float v = accumulate ? gM[i] : 0.f;
+    for (int s = 0; s < splits; ++s) v += part[s * n + i];
+    gM[i] = v;
   }
 }
 
@@ -763,6 +808,8 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->scratch_elems = size_t(2) * st->chunk_nodes * st->s_node;
   if (cudaMalloc(&st->scratch, st->scratch_elems * sizeof(float)) != cudaSuccess)
     return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
+  if (cudaMalloc(&st->gm_part, sizeof(float) * kGmSplits * st->K * plan->w_numel) != cudaSuccess)
+    return fail(CGTP_ENOMEM, "uvw gM partial allocation failed");
   // shared memory of the edge stages
   const GroupDev& G = lay.groups[0];
   const int d2p = pad_up(int(plan->d2), 4);
@@ -785,6 +832,7 @@ void uvw_destroy(cgtp_plan_s* plan) {
   if (!st) return;
   if (st->tables) cudaFree(st->tables);
   if (st->scratch) cudaFree(st->scratch);
+  if (st->gm_part) cudaFree(st->gm_part);
   delete st;
   plan->uvw = nullptr;
 }
@@ -814,14 +862,17 @@ EdgeArgs edge_args(const cgtp_plan_s* plan, const UvwState* st, int group) {
 }
 
 cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
-                        const float* const ptr[6], int nodes, int tiles, cudaStream_t s) {
+                        const float* const ptr[6], int nodes, int tiles, cudaStream_t s,
+                        int splits = 1, long long c_split_stride = 0) {
   GemmLaunch L{};
   for (int i = 0; i < 6; ++i) L.ptr[i] = ptr[i];
   L.nodes = nodes;
   L.nprob = np;
   L.probs = probs_dev;
   L.segs = segs;
-  grouped_gemm_kernel<<<tiles, 256, 0, s>>>(L);
+  L.splits = splits;
+  L.c_split_stride = c_split_stride;
+  grouped_gemm_kernel<<<dim3(tiles, splits), 256, 0, s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
 
@@ -924,12 +975,17 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
                             static_cast<float*>(gM), Hbuf};
     r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s);
     if (r != CGTP_OK) return r;
-    if (first) {
-      cudaMemsetAsync(gM, 0, sizeof(float) * plan->w_numel * st->K, s);
-      first = false;
-    }
-    r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, post, nodes, tiles_for(plan, st, 3, nodes), s);
+    // gM over this chunk's senders: split-K partials, then an ordered reduction
+    const float* postp[6] = {post[0], post[1], post[2], post[3], st->gm_part, post[5]};
+    const int splits = std::min(kGmSplits, std::max(1, nodes / 64));
+    const long long n_gm = (long long)st->K * plan->w_numel;
+    r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, postp, nodes, tiles_for(plan, st, 3, nodes), s,
+                    splits, n_gm);
     if (r != CGTP_OK) return r;
+    splitk_reduce_kernel<<<std::min<long long>((n_gm + 255) / 256, 4096), 256, 0, s>>>(
+        static_cast<float*>(gM), st->gm_part, splits, n_gm, first ? 0 : 1);
+    if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw gM reduction launch failed");
+    first = false;
   }
   if (g->N == 0) cudaMemsetAsync(gM, 0, sizeof(float) * plan->w_numel * st->K, s);
   return CGTP_OK;
