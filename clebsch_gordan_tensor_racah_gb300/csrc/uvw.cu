@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
       __syncthreads();
     }
   }
-  const int beta = L.splits > 1 ? 0 : P.beta;
+  const int beta = P.beta;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = r0 + ty * 4 + i;
@@ -759,7 +759,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       P.a_off = q.off1; P.a_n = q.D1; P.a_m = 0;
       P.b_j = q.D1;
       P.c_off = (long long)k * wn + q.woff; P.c_n = q.mul_out; P.c_m = 0; P.c_j = 1;
-      P.beta = 1;
+      P.beta = 0;  // writes a split-K partial; splitk_reduce_kernel accumulates into gM
       P.seg0 = int(ms.size());
       for (int m1 = 0; m1 < q.D1; ++m1) {
         GemmSeg S{};
