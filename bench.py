@@ -59,7 +59,7 @@ CONFIGS = {
 }
 
 
-def build_inputs(cfgkey, device):
+def build_inputs(cfgkey, device, nodes=None):
     import torch
     import clebsch_gordan_tensor_racah_gb300 as cg
     from clebsch_gordan_tensor_racah_gb300 import workloads as wl
@@ -69,7 +69,10 @@ def build_inputs(cfgkey, device):
     mode = spec["mode"]
     plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
                    radial_k=spec.get("K", 0) if mode == "uvw" else 0)
-    w = wl.make(c["name"], plan.w_numel, seed=0, dtype=c["dtype"], **c["over"])
+    over = dict(c["over"])
+    if nodes:
+        over["B" if spec["graph"] is None else "N"] = int(nodes)
+    w = wl.make(c["name"], plan.w_numel, seed=0, dtype=c["dtype"], **over)
     host = {k: v for k, v in w.items() if isinstance(v, np.ndarray)}
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(device) for k, v in host.items()}
     graph = None
@@ -115,10 +118,47 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     return fwd, bwd, units, bf, bb, out_shape
 
 
-def flops_per_unit(plan_paths, mode):
-    """Algorithmic FLOPs of one edge (forward): cy = C.Y, then per channel the
-    (2l1+1)x(2l3+1) contraction and the weight product (uvu) or, for uvw, the
-    per-edge product plus the receiver-state update and its share of the node GEMM."""
+def algorithmic_flops(plan, n_nodes, n_edges):
+    """Algorithmic FLOPs of one forward and one backward launch (FMA = 2 flops).
+
+    Per (edge, path) with D1 = 2l1+1, D3 = 2l3+1, NF = D1*D3 and nnz the CG
+    nonzeros of the path:
+      uvu forward : 2 nnz (cy = C.Y) + mul * (D1 + 2 NF)      (weight product, contraction)
+      uvu backward: 4 nnz + mul * (6 NF + 3 D3)               (t, gW, w*g, gx, x (x) wg; C.Y and C.gc)
+      uvw forward : 2 nnz + mul1 * 2 NF + 2 K mul1 D3 per edge, and the node GEMM
+                    2 K mul1 mul_out D3 per node
+      uvw backward: 4 nnz + 2 mul_out NF * 2 + 6 K mul_out D1 per edge, and three node
+                    GEMMs (x M, M H, x^T H) of 2 K mul1 mul_out D1 each per node
+    """
+    fe = be = fn = bn = 0
+    K = getattr(plan, "radial_k", 0)
+    for p in range(plan.n_paths):
+        ints, C = plan.path(p)
+        l1, l2, l3, mul1, mul_out = ints[:5]
+        D1, D3 = 2 * l1 + 1, 2 * l3 + 1
+        NF, nnz = D1 * D3, int(np.count_nonzero(C))
+        if plan.mode == "uvu":
+            fe += 2 * nnz + mul1 * (D1 + 2 * NF)
+            be += 4 * nnz + mul1 * (6 * NF + 3 * D3)
+        else:
+            fe += 2 * nnz + mul1 * 2 * NF + 2 * K * mul1 * D3
+            fn += 2 * K * mul1 * mul_out * D3
+            be += 4 * nnz + 4 * mul_out * NF + 6 * K * mul_out * D1
+            bn += 3 * 2 * K * mul1 * mul_out * D1
+    return fe * n_edges + fn * n_nodes, be * n_edges + bn * n_nodes
+
+
+def traffic_for(kname, cfgkey, algorithmic_bytes):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.txt: kernel, workload, dram bytes per algorithmic byte measured on a
+    smaller case of the same recipe); None when no capture matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kname and f[1] == cfgkey:
+            return float(f[2]) * algorithmic_bytes
     return None
 
 
@@ -170,7 +210,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def time_oracle_sample(cfgkey, budget_s=12.0):
+def time_oracle_sample(cfgkey, budget_s=8.0):
     """FP64 oracle on a bounded sample of the workload: (units/s, sample description)."""
     from clebsch_gordan_tensor_racah_gb300 import workloads as wl
     from oracle import conv as oconv, irreps as oirr
@@ -188,7 +228,7 @@ def time_oracle_sample(cfgkey, budget_s=12.0):
         dt = time.perf_counter() - t0
         return units / dt, f"batches of {B} samples of the same recipe, fwd+bwd, {dt:.1f} s"
     # a smaller graph of the same recipe (same degree distribution and features)
-    N = {"tiny": 64, "nequip": 400, "mace": 200, "uvw": 8}[c["name"]]
+    N = {"tiny": 64, "nequip": 120, "mace": 60, "uvw": 4}[c["name"]]
     w = wl.make(c["name"], oplan.w_numel, seed=0, dtype=c["dtype"], N=N)
     units, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
@@ -236,7 +276,7 @@ def run_reference(args):
     t_steps = []
     rate = None
     for i in range(args.warmup + args.steps):
-        r, desc = time_oracle_sample(cfgkey, budget_s=max(2.0, 60.0 / max(1, args.warmup + args.steps)))
+        r, desc = time_oracle_sample(cfgkey, budget_s=max(2.0, 40.0 / max(1, args.warmup + args.steps)))
         if i >= args.warmup:
             t_steps.append(r)
     rate = float(np.median(t_steps))
@@ -247,7 +287,7 @@ def run_reference(args):
             "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * units / rate, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": config_block(cfgkey, {"N": 1} if cfgkey != "highl" else {"B": 1}, 1)["workload"]},
+            "config": {"workload": config_block(cfgkey, {"N": 1, "E": 0} if cfgkey != "highl" else {"B": 1}, 1)["workload"]},
             "cpu_baseline": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
                              "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
@@ -258,12 +298,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="nequip", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--nodes", type=int, default=None,
+                    help="smaller instance of the same recipe (nodes, or batch for highl)")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="build, two warm-up steps and one step, no timing or JSON (for ncu captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -282,7 +326,7 @@ def main():
         torch.distributed.barrier()
     build()
 
-    plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device)
+    plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device, args.nodes)
     fwd, bwd, units, bf, bb, out_shape = step_fns(args.config, plan, graph, w, dev, tdt)
     g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
     out = torch.empty(out_shape, dtype=tdt, device=device)
@@ -291,6 +335,13 @@ def main():
     def step():
         fwd(out)
         return bwd(g, None)
+
+    if args.profile_run:
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        print(f"profile run done: {args.config}, {units} units", flush=True)
+        return
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -376,16 +427,38 @@ def main():
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     pk = peaks()
+    mhz = (clk or {}).get("sm_max_mhz") or pk["sm_max_mhz"]
+    dt_name = "f64" if tdt == torch.float64 else "f32"
+    alu_peak = alu_peak_tflops(dt_name, mhz)
+    n_nodes = w.get("N", w.get("B", 0))
+    ff, fb = algorithmic_flops(plan, n_nodes, units)
     dominant = "backward" if bwd_ms >= fwd_ms else "forward"
     dom_ms = bwd_ms if dominant == "backward" else fwd_ms
     dom_bytes = bb if dominant == "backward" else bf
-    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
-    roofline = {"bound": "hbm", "kernel": f"uvu_{dominant}_kernel" if plan.mode == "uvu" else f"uvw {dominant}",
-                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"], "traffic": None,
-                "algorithmic_bytes_per_launch": int(dom_bytes),
-                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-                "fwd_GBps": bf / (fwd_ms / 1000) / 1e9, "bwd_GBps": bb / (bwd_ms / 1000) / 1e9}
+    dom_flops = fb if dominant == "backward" else ff
+    t_hbm = dom_bytes / (pk["hbm_gbs"] * 1e9)
+    t_alu = dom_flops / (alu_peak * 1e12)
+    kname = {("uvu", "forward"): "uvu_forward3_kernel", ("uvu", "backward"): "uvu_backward3_kernel",
+             ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
+             ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[(plan.mode, dominant)]
+    if "N" not in w:
+        kname = "uvu batched " + dominant
+    if t_hbm >= t_alu:
+        achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"] + " (copy bandwidth)"}
+    else:
+        achieved = dom_flops / (dom_ms / 1000.0) / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": achieved / alu_peak,
+                    "peak_src": f"derived: 152 SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz" if dt_name == "f32"
+                    else "nominal FP64 1.25 TFLOP/s"}
+    roofline.update({"kernel": kname, "traffic": traffic_for(kname, args.config, dom_bytes),
+                     "algorithmic_bytes_per_launch": int(dom_bytes), "algorithmic_flops_per_launch": int(dom_flops),
+                     "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                     "fwd_roofline_ms": 1000 * max(bf / (pk["hbm_gbs"] * 1e9), ff / (alu_peak * 1e12)),
+                     "bwd_roofline_ms": 1000 * max(bb / (pk["hbm_gbs"] * 1e9), fb / (alu_peak * 1e12))})
+    roofline["step_frac"] = (roofline["fwd_roofline_ms"] + roofline["bwd_roofline_ms"]) / (fwd_ms + bwd_ms)
     line = {"metric": METRIC, "value": value, "unit": "edges/s" if "N" in w else "samples/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
