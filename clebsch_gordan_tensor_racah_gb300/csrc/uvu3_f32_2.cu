@@ -40,10 +40,10 @@ cgtp_status fwd3_launch(const cgtp_plan_s* plan, const void* x, const void* Y, c
   a.N = static_cast<int>(N);
   auto k = uvu_forward3_kernel<T, LPE>;
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kV3Threads, 0);
   per_sm = std::max(per_sm, 1);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, (int64_t)plan->num_sms * per_sm)));
-  k<<<grid, kThreads, 0, st>>>(a);
+  k<<<grid, kV3Threads, 0, st>>>(a);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("uvu forward (v3) launch: ") + cudaGetErrorString(err));
   return CGTP_OK;
@@ -68,10 +68,10 @@ cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x
   auto k = uvu_backward3_kernel<T, LPE>;
   const size_t smem = 0;
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kV3Threads, smem);
   per_sm = std::max(per_sm, 1);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, (int64_t)plan->num_sms * per_sm)));
-  k<<<grid, kThreads, smem, st>>>(a);
+  k<<<grid, kV3Threads, smem, st>>>(a);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("uvu backward (v3) launch: ") + cudaGetErrorString(err));
   return CGTP_OK;

@@ -26,6 +26,10 @@ namespace uvu3_detail {
 
 __host__ __device__ inline int pad_up(int v, int q) { return (v + q - 1) / q * q; }
 
+// one 16-warp CTA per SM: the whole SM walks one path at a time
+constexpr int kV3Warps = 16;
+constexpr int kV3Threads = kV3Warps * 32;
+
 template <typename T>
 struct PairT;
 template <>
@@ -276,7 +280,7 @@ __device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restr
     break;
 
 template <typename T, int LPE>
-__global__ void __launch_bounds__(kThreads, 2) uvu_forward3_kernel(const Uvu3Args<T> a) {
+__global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3Args<T> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2) uvu_forward3_kernel(const Uvu3Arg
   __syncthreads();
   const int nb = s_range[0], ne = s_range[1];
   int wlo, whi;
-  warp_rows(a.rowptr, nb, ne, warp, kWarps, &wlo, &whi);
+  warp_rows(a.rowptr, nb, ne, warp, kV3Warps, &wlo, &whi);
   // path-major: all warps of the CTA work on the same path (one hot instruction
   // stream), each on an edge-balanced contiguous range of receivers; a barrier
   // at each path boundary keeps them together
@@ -464,7 +468,7 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
     break;
 
 template <typename T, int LPE>
-__global__ void __launch_bounds__(kThreads, 2) uvu_backward3_kernel(const Uvu3Args<T> a) {
+__global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3Args<T> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) uvu_backward3_kernel(const Uvu3Ar
   __syncthreads();
   const int sb = s_range[0], se = s_range[1];
   int wlo, whi;
-  warp_rows(a.rowptr, sb, se, warp, kWarps, &wlo, &whi);
+  warp_rows(a.rowptr, sb, se, warp, kV3Warps, &wlo, &whi);
   // the warp that owns sender s clears gx[s] and gY of its out-edges, then
   // accumulates into them path by path; nobody else touches those rows
   for (int s = wlo; s < whi; ++s) {
