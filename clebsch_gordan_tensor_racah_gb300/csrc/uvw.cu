@@ -33,6 +33,7 @@
 
 #include "internal.h"
 #include "uvu_impl.cuh"
+#include "uvu3_impl.cuh"
 
 namespace cgtp {
 namespace uvw_detail {
@@ -44,7 +45,6 @@ using uvu_detail::V16;
 constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (CGTP_UVW_CHUNK_NODES overrides)
 constexpr int kEdgeChunk = 16;      // edges staged per step of the edge stages
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
-constexpr int kBwdChunk = 8;        // edges staged per step of the backward edge stage
 constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over nodes
 
 struct UvwPath {
@@ -85,6 +85,8 @@ struct UvwState {
   int chunk_nodes = kChunkNodes;
   float* scratch = nullptr;      // [2][chunk_nodes][s_node]
   float* gm_part = nullptr;      // [kGmSplits][K][w_numel] split-K partials of gM
+  Item* bwd3_items = nullptr;    // (path, 32-block of mul_out) in path order
+  int bwd3_n_items = 0;
   size_t scratch_elems = 0;
   // GEMM descriptor tables (device) per use
   GemmProb* fwd_probs = nullptr;  int fwd_np = 0;  GemmSeg* fwd_segs = nullptr;
@@ -397,174 +399,154 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
   return r;
 }
 
-template <int D1, int D3>
-__device__ __noinline__ void bwd_state_item(int ooff, int cyoff, int aoff, int a_slice, int K,
-                                            int w0, int lane, int mul_out, int cnt,
-                                            const float* gs, int d_out_s, const float* Rs,
-                                            const float* cys, int cy_size, const float* As,
-                                            float* Hs, float* gcp, int nub, float* gRp,
-                                            int item_slot, int n_item_slots) {
-  using V = float4;
-  constexpr int NF = D1 * D3;
-  constexpr int NV = (NF + 3) / 4;
+// ---------------------------------------------------------------------------
+// backward edge stage, warp-autonomous and path-major (replaces the block-
+// cooperative uvw_bwd_edge_kernel): one warp owns a contiguous, edge-balanced
+// range of senders; a unit is (sender, path, 32 output channels w), lanes <-> w.
+// A[s][k][path][w][m1] and the accumulating H[s][k][path][w][m1] of the unit
+// stay in registers; the CG nonzeros of (l1, l2, l3) are compiled in, so
+//   p_e[m1]  = sum_{m2,m3} C Y[e][m2] g[d][w][m3]
+//   h[m2]    = sum_{m1,m3} C ar[m1] g[d][w][m3],  ar[m1] = sum_k R[e,k] A[k][m1]
+// and only gR (K values) and h (2l2+1 values) cross the 32 lanes; the owner
+// warp accumulates gR and gY in path order (deterministic, no atomics).
+// ---------------------------------------------------------------------------
+struct Bwd3Args {
+  const float* Y;
+  const float* R;
+  const float* g;
+  const float* Astate;  // [chunk][K][s_slice]
+  float* Hstate;        // [chunk][K][s_slice]
+  float* gY;
+  float* gR;
+  const int* t_rowptr;
+  const int* t_eid;
+  const int* t_dst;
+  int n0, n1;
+  int d2, d_out, K, s_node, s_slice;
+  const UvwPath* paths;
+  const Item* items;    // (path, w0), path order
+  int n_items;
+};
+
+template <int L1, int L2, int L3>
+__device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const float* __restrict__ Rp,
+                                           const float* __restrict__ gp_, const float* __restrict__ Astate,
+                                           float* __restrict__ Hstate, float* __restrict__ gY,
+                                           float* __restrict__ gR, const int* __restrict__ t_eid,
+                                           const int* __restrict__ t_dst, int tb, int te, size_t node_off,
+                                           int d2, int d_out, int K, int s_slice, int off2, int ooff,
+                                           int aoff, int mul_out, int w0, int lane) {
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1;
   const int w = w0 + lane;
   const bool active = w < mul_out;
-  const int wb = w0 >> 5;
-  for (int kb = 0; kb < K; kb += kKB) {
-    float hacc[kKB][D1];
+  float A[kKB][D1], H[kKB][D1];
+  const float* As = Astate + node_off + aoff + w * D1;
+#pragma unroll
+  for (int k = 0; k < kKB; ++k)
+#pragma unroll
+    for (int m = 0; m < D1; ++m) {
+      A[k][m] = (active && k < K) ? __ldg(As + k * s_slice + m) : 0.f;
+      H[k][m] = 0.f;
+    }
+  for (int t = tb; t < te; ++t) {
+    const int e = __ldg(t_eid + t), d = __ldg(t_dst + t);
+    float yv[D2], r[kKB], gv[D3];
+#pragma unroll
+    for (int m = 0; m < D2; ++m) yv[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
+#pragma unroll
+    for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
+    const float* gp = gp_ + (size_t)d * d_out + ooff + w * D3;
+#pragma unroll
+    for (int m = 0; m < D3; ++m) gv[m] = active ? __ldg(gp + m) : 0.f;
+    float pe[D1];
+#pragma unroll
+    for (int m = 0; m < D1; ++m) pe[m] = 0.f;
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { pe[m1] += float(c) * yv[m2] * gv[m3]; });
+    float gr[kKB], ar[D1];
+#pragma unroll
+    for (int m = 0; m < D1; ++m) ar[m] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kKB; ++k) {
+      float dot = 0.f;
+#pragma unroll
+      for (int m = 0; m < D1; ++m) {
+        H[k][m] += r[k] * pe[m];
+        dot += A[k][m] * pe[m];
+        ar[m] += r[k] * A[k][m];
+      }
+      gr[k] = dot;
+    }
+    float h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = 0.f;
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { h[m2] += float(c) * ar[m1] * gv[m3]; });
+    const float grt = reduce8(gr, lane);   // lane holds the total of index (lane >> 2) & 7
+    const float ht = reduce8(h, lane);
+    const int idx = (lane >> 2) & 7;
+    if ((lane & 3) == 0) {
+      if (idx < K) gR[(size_t)e * K + idx] += grt;
+      if (idx < D2) gY[(size_t)e * d2 + off2 + idx] += ht;
+    }
+  }
+  if (active) {
+    float* Hs = Hstate + node_off + aoff + w * D1;
 #pragma unroll
     for (int k = 0; k < kKB; ++k)
+      if (k < K)
 #pragma unroll
-      for (int m = 0; m < D1; ++m) hacc[k][m] = 0.f;
-    for (int j = 0; j < cnt; ++j) {
-      float gv[D3];
-      const float* gr = gs + j * d_out_s + ooff + w * D3;
-#pragma unroll
-      for (int m = 0; m < D3; ++m) gv[m] = active ? gr[m] : 0.f;
-      float pe[D1];
-#pragma unroll
-      for (int m = 0; m < D1; ++m) pe[m] = 0.f;
-      const V* c = reinterpret_cast<const V*>(cys + j * cy_size + cyoff);
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const V cv = c[v];
-        const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int f = v * 4 + q;
-          if (f < NF) pe[f / D3] += cs[q] * gv[f % D3];
-        }
-      }
-      float gr8[kKB];
-      float ar[D1];
-#pragma unroll
-      for (int m = 0; m < D1; ++m) ar[m] = 0.f;
-#pragma unroll
-      for (int k = 0; k < kKB; ++k) {
-        const bool kin = kb + k < K;
-        const float r = kin ? Rs[j * 16 + kb + k] : 0.f;
-        float dot = 0.f;
-        const float* ap = As + (kin ? (kb + k) : 0) * a_slice + aoff + w * D1;
-#pragma unroll
-        for (int m = 0; m < D1; ++m) {
-          const float av = (active && kin) ? ap[m] : 0.f;
-          dot += av * pe[m];
-          ar[m] += r * av;
-          hacc[k][m] += r * pe[m];
-        }
-        gr8[k] = dot;
-      }
-      // gR partial of this item and edge: sum over the lanes (w)
-      const float tot = reduce8(gr8, lane);
-      if ((lane & 3) == 0) gRp[(j * n_item_slots + item_slot) * kKB + ((lane >> 2) & 7)] = tot;
-      // gc[m1][m3] = sum_w ar[w][m1] g[w][m3]
-      reduce_outer<float, D1, D3>(ar, gv, gcp + (j * nub + wb) * cy_size + cyoff, lane);
-    }
-    if (active) {
-#pragma unroll
-      for (int k = 0; k < kKB; ++k) {
-        if (kb + k >= K) break;
-        float* hp = Hs + (kb + k) * a_slice + aoff + w * D1;
-#pragma unroll
-        for (int m = 0; m < D1; ++m) hp[m] += hacc[k][m];
-      }
-    }
+        for (int m = 0; m < D1; ++m) Hs[k * s_slice + m] = H[k][m];
   }
 }
 
-#define UVW_BWD_CASE(L1, L3)                                                                     \
-  case (L1)*8 + (L3):                                                                            \
-    bwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(p.ooff, p.cyoff, p.aoff, a.s_slice, a.K, item.u0,  \
-                                                lane, p.mul_out, cnt, gs, a.d_out, Rs, cys,       \
-                                                cy_size, As, Hs, gcp, nub, gRp, it - items0,      \
-                                                n_items);                                         \
+#define UVW3_BWD_CASE(L1, L2, L3)                                                                  \
+  case (L1)*16 + (L2)*4 + (L3):                                                                    \
+    if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
+      uvw_bwd3_unit<L1, L2, L3>(a.Y, a.R, a.g, a.Astate, a.Hstate, a.gY, a.gR, a.t_eid, a.t_dst,     \
+                                rp[s], rp[s + 1], (size_t)(s - a.n0) * a.s_node, a.d2, a.d_out, a.K,  \
+                                a.s_slice, p.off2, p.ooff, p.aoff, p.mul_out, item.u0, lane);        \
     break;
 
-__global__ void __launch_bounds__(kThreads) uvw_bwd_edge_kernel(const EdgeArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+constexpr int kBwd3Warps = 16;
+
+__global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const Bwd3Args a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const GroupDev g = *a.group;
-  const int cy_size = g.cy_size, nub = g.nub;
-  const int d2p = pad_up(a.d2, 4);
-  const int items0 = a.item_begin[g.item_base];
-  const int n_items = a.item_begin[g.item_base + kWarps] - items0;
-  float* As = reinterpret_cast<float*>(smem);
-  float* Hs = As + pad_up(a.s_node, 4);
-  float* gs = Hs + pad_up(a.s_node, 4);
-  float* Ys = gs + kBwdChunk * a.d_out;
-  float* Rs = Ys + kBwdChunk * d2p;
-  float* cys = Rs + kBwdChunk * 16;
-  float* gcp = cys + kBwdChunk * cy_size;            // [chunk][nub][cy_size]
-  float* gRp = gcp + kBwdChunk * nub * cy_size;      // [chunk][items][8]
-  int* eid_s = reinterpret_cast<int*>(gRp + kBwdChunk * n_items * kKB);
-  int* dst_s = eid_s + kBwdChunk;
-  const int ib = a.item_begin[g.item_base + warp], ie = a.item_begin[g.item_base + warp + 1];
-  for (int s = a.n0 + blockIdx.x; s < a.n1; s += gridDim.x) {
-    const int e_begin = a.rowptr[s], e_end = a.rowptr[s + 1];
-    __syncthreads();
-    const float* Asrc = a.Astate + (size_t)(s - a.n0) * a.s_node;
-    for (int i = tid; i < a.s_node; i += kThreads) {
-      As[i] = Asrc[i];
-      Hs[i] = 0.f;
+  __shared__ int s_range[2];
+  const int* rp = a.t_rowptr;
+  if (tid == 0) {
+    const long long base = (long long)rp[a.n0] + a.n0, total = (long long)rp[a.n1] + a.n1 - base;
+    const long long t0 = base + total * blockIdx.x / gridDim.x, t1 = base + total * (blockIdx.x + 1) / gridDim.x;
+    auto lb = [&](long long target) {
+      int lo = a.n0, hi = a.n1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)rp[mid] + mid < target) lo = mid + 1; else hi = mid;
+      }
+      return lo;
+    };
+    s_range[0] = lb(t0);
+    s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.n1 : lb(t1);
+  }
+  __syncthreads();
+  int wlo, whi;
+  uvu3_detail::warp_rows(rp, s_range[0], s_range[1], warp, kBwd3Warps, &wlo, &whi);
+  // the owner warp clears gY and gR of its senders' out-edges
+  for (int s = wlo; s < whi; ++s)
+    for (int t = rp[s]; t < rp[s + 1]; ++t) {
+      const int e = a.t_eid[t];
+      for (int i = lane; i < a.d2; i += 32) a.gY[(size_t)e * a.d2 + i] = 0.f;
+      for (int i = lane; i < a.K; i += 32) a.gR[(size_t)e * a.K + i] = 0.f;
     }
-    for (int e0 = e_begin; e0 < e_end; e0 += kBwdChunk) {
-      const int cnt = min(kBwdChunk, e_end - e0);
-      __syncthreads();
-      for (int i = tid; i < cnt; i += kThreads) {
-        eid_s[i] = a.col[e0 + i];
-        dst_s[i] = a.t_dst[e0 + i];
-      }
-      __syncthreads();
-      for (int i = tid; i < cnt * a.d_out; i += kThreads) {
-        const int j = i / a.d_out, c = i - j * a.d_out;
-        gs[i] = a.g[(size_t)dst_s[j] * a.d_out + c];
-      }
-      for (int i = tid; i < cnt * a.d2; i += kThreads) {
-        const int j = i / a.d2, c = i - j * a.d2;
-        Ys[j * d2p + c] = a.Y[(size_t)eid_s[j] * a.d2 + c];
-      }
-      for (int i = tid; i < cnt * a.K; i += kThreads) {
-        const int j = i / a.K, k = i - j * a.K;
-        Rs[j * 16 + k] = a.R[(size_t)eid_s[j] * a.K + k];
-      }
-      __syncthreads();
-      for (int i = tid; i < cnt * cy_size; i += kThreads) {
-        const int j = i / cy_size, sl = i - j * cy_size;
-        const int t0 = a.cy_begin[g.cy_base + sl], t1 = a.cy_begin[g.cy_base + sl + 1];
-        float v = 0.f;
-        for (int t = t0; t < t1; ++t) v += a.cy_coef[t] * Ys[j * d2p + a.cy_col[t]];
-        cys[i] = v;
-      }
-      __syncthreads();
-      for (int it = ib; it < ie; ++it) {
-        const Item item = a.items[it];
-        const UvwPath p = a.paths[item.path];
-        switch (p.l1 * 8 + p.l3) { UVW_CASES(UVW_BWD_CASE) default: break; }
-      }
-      __syncthreads();
-      // per-edge outputs: gY from the gc partials, gR from the item partials (fixed order)
-      for (int i = tid; i < cnt * a.d2; i += kThreads) {
-        const int j = i / a.d2, c = i - j * a.d2;
-        const int t0 = a.gy_begin[g.gy_base + c], t1 = a.gy_begin[g.gy_base + c + 1];
-        float v = 0.f;
-        for (int t = t0; t < t1; ++t) {
-          const int sl = a.gy_slot[t], nb = a.gy_nub[t];
-          float gsum = 0.f;
-          for (int b = 0; b < nb; ++b) gsum += gcp[(j * nub + b) * cy_size + sl];
-          v += a.gy_coef[t] * gsum;
-        }
-        a.gY[(size_t)eid_s[j] * a.d2 + c] = v;
-      }
-      for (int i = tid; i < cnt * a.K; i += kThreads) {
-        const int j = i / a.K, k = i - j * a.K;
-        float v = 0.f;
-        for (int q = 0; q < n_items; ++q) v += gRp[(j * n_items + q) * kKB + k];
-        a.gR[(size_t)eid_s[j] * a.K + k] = v;
+  __syncwarp();
+  for (int it = 0; it < a.n_items; ++it) {
+    const Item item = a.items[it];
+    const UvwPath p = a.paths[item.path];
+    if (it) __syncthreads();  // path-major: one hot instruction stream per SM
+    for (int s = wlo; s < whi; ++s) {
+      switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+        CGTP3_TRIPLES(UVW3_BWD_CASE)
+        default: break;
       }
     }
-    __syncthreads();
-    float* dst = a.state + (size_t)(s - a.n0) * a.s_node;
-    for (int i = tid; i < a.s_node; i += kThreads) dst[i] = Hs[i];
   }
 }
 
@@ -615,55 +597,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->n_paths = static_cast<int>(plan->paths.size());
   st->s_slice = std::max(soff, aoff);
   st->s_node = st->K * st->s_slice;
-  // backward items: (path, 32-block of mul_out)
-  std::vector<std::vector<Item>> per_warp(kWarps);
-  {
-    struct It { int path, w0; double cost; };
-    std::vector<It> its;
-    for (int p = 0; p < st->n_paths; ++p) {
-      const auto& q = st->paths_h[p];
-      for (int w0 = 0; w0 < q.mul_out; w0 += 32) its.push_back({p, w0, double(q.D1 * q.D3 * 3 + 3 * st->K * q.D1)});
-    }
-    std::stable_sort(its.begin(), its.end(), [](const It& a, const It& b) { return a.cost > b.cost; });
-    std::vector<double> load(kWarps, 0.0);
-    for (const auto& it : its) {
-      const int w = int(std::min_element(load.begin(), load.end()) - load.begin());
-      per_warp[w].push_back({it.path, it.w0});
-      load[w] += it.cost;
-    }
-  }
-  std::vector<int> bwd_begin;
-  std::vector<Item> bwd_items;
-  for (int w = 0; w < kWarps; ++w) {
-    bwd_begin.push_back(int(bwd_items.size()));
-    for (auto& i : per_warp[w]) bwd_items.push_back(i);
-  }
-  bwd_begin.push_back(int(bwd_items.size()));
-  // gc layout channel blocks for the backward are blocks of mul_out
-  int nub_b = 1;
-  for (const auto& q : st->paths_h) nub_b = std::max(nub_b, (q.mul_out + 31) / 32);
-  {
-    // rebuild gy_nub entries for the backward: the number of w blocks of the slot's path
-    std::vector<int> slot_path(lay.groups[0].cy_size, 0);
-    for (int p = 0; p < st->n_paths; ++p) {
-      const auto& q = st->paths_h[p];
-      for (int f = 0; f < q.D1 * q.D3; ++f) slot_path[q.cyoff + f] = p;
-    }
-    for (size_t t = 0; t < lay.gy_slot.size(); ++t)
-      lay.gy_nub[t] = (st->paths_h[slot_path[lay.gy_slot[t]]].mul_out + 31) / 32;
-  }
-  GroupDev g0 = lay.groups[0];
-  g0.nub = std::max(g0.nub, nub_b);
-  lay.groups[0] = g0;
-  // the forward keeps the (path, u-block) items of the layout; the backward
-  // items go after them
-  const int bwd_item_base = static_cast<int>(lay.item_begin.size());
-  const int bwd_items_off = static_cast<int>(lay.items.size());
-  for (int w = 0; w <= kWarps; ++w) lay.item_begin.push_back(bwd_begin[w] + bwd_items_off);
-  for (auto& i : bwd_items) lay.items.push_back(i);
-  GroupDev gb = g0;
-  gb.item_base = bwd_item_base;
-  lay.groups.push_back(gb);  // group[1]: same tables, backward items
   s = upload_layout(plan, lay, &plan->conv_layout);
   if (s != CGTP_OK) return s;
   // ---- GEMM descriptors -------------------------------------------------
@@ -788,6 +721,10 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   const size_t o_xs = put(xs.data(), xs.size() * sizeof(GemmSeg));
   const size_t o_mp = put(mp.data(), mp.size() * sizeof(GemmProb));
   const size_t o_ms = put(ms.data(), ms.size() * sizeof(GemmSeg));
+  std::vector<Item> b3;
+  for (int p = 0; p < st->n_paths; ++p)
+    for (int w0 = 0; w0 < st->paths_h[p].mul_out; w0 += 32) b3.push_back({p, w0});
+  const size_t o_b3 = put(b3.data(), b3.size() * sizeof(Item));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "uvw tables");
   cudaMemcpy(st->tables, buf.data(), buf.size(), cudaMemcpyHostToDevice);
   auto at = [&](size_t o) { return static_cast<unsigned char*>(st->tables) + o; };
@@ -800,6 +737,8 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->gx_segs = reinterpret_cast<GemmSeg*>(at(o_xs));
   st->gm_probs = reinterpret_cast<GemmProb*>(at(o_mp)); st->gm_np = int(mp.size());
   st->gm_segs = reinterpret_cast<GemmSeg*>(at(o_ms));
+  st->bwd3_items = reinterpret_cast<Item*>(at(o_b3));
+  st->bwd3_n_items = int(b3.size());
   // node-state scratch: two chunks of state (forward S; backward A and H)
   if (const char* env = std::getenv("CGTP_UVW_CHUNK_NODES")) {
     const long v = std::strtol(env, nullptr, 10);
@@ -815,15 +754,9 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   const int d2p = pad_up(int(plan->d2), 4);
   st->smem_fwd = sizeof(float) * (pad_up(st->s_node, 4) + kEdgeChunk * d2p + kEdgeChunk * 16 +
                                   kEdgeChunk * G.cy_size) + sizeof(int) * kEdgeChunk;
-  const int n_items_b = static_cast<int>(bwd_items.size());
-  st->smem_bwd = sizeof(float) * (2 * pad_up(st->s_node, 4) + kBwdChunk * plan->d_out + kBwdChunk * d2p +
-                                  kBwdChunk * 16 + kBwdChunk * G.cy_size +
-                                  kBwdChunk * g0.nub * G.cy_size + kBwdChunk * n_items_b * kKB) +
-                 2 * sizeof(int) * kBwdChunk;
-  if (st->smem_fwd > 227 * 1024 || st->smem_bwd > 227 * 1024)
+  if (st->smem_fwd > 227 * 1024)
     return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
   cudaFuncSetAttribute(uvw_fwd_edge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem_fwd);
-  cudaFuncSetAttribute(uvw_bwd_edge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem_bwd);
   return CGTP_OK;
 }
 
@@ -944,18 +877,6 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* Abuf = st->scratch;
   float* Hbuf = st->scratch + (size_t)st->chunk_nodes * st->s_node;
-  EdgeArgs a = edge_args(plan, st, 1);
-  a.x = static_cast<const float*>(x);
-  a.Y = static_cast<const float*>(Y);
-  a.R = static_cast<const float*>(R);
-  a.g = static_cast<const float*>(gout);
-  a.gY = static_cast<float*>(gY);
-  a.gR = static_cast<float*>(gR);
-  a.rowptr = g->t_rowptr;
-  a.col = g->t_eid;
-  a.t_dst = g->t_dst;
-  a.Astate = Abuf;
-  a.state = Hbuf;
   bool first = true;
   for (int64_t n0 = 0; n0 < g->N; n0 += st->chunk_nodes) {
     const int n1 = static_cast<int>(std::min<int64_t>(g->N, n0 + st->chunk_nodes));
@@ -965,10 +886,29 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     cgtp_status r = launch_gemm(st->pre_probs, st->pre_np, st->pre_segs, pre, nodes,
                                 tiles_for(plan, st, 1, nodes), s);
     if (r != CGTP_OK) return r;
-    a.n0 = static_cast<int>(n0);
-    a.n1 = n1;
-    const int grid = std::min(nodes, plan->num_sms * 1);
-    uvw_bwd_edge_kernel<<<grid, kThreads, st->smem_bwd, s>>>(a);
+    Bwd3Args b{};
+    b.Y = static_cast<const float*>(Y);
+    b.R = static_cast<const float*>(R);
+    b.g = static_cast<const float*>(gout);
+    b.Astate = Abuf;
+    b.Hstate = Hbuf;
+    b.gY = static_cast<float*>(gY);
+    b.gR = static_cast<float*>(gR);
+    b.t_rowptr = g->t_rowptr;
+    b.t_eid = g->t_eid;
+    b.t_dst = g->t_dst;
+    b.n0 = static_cast<int>(n0);
+    b.n1 = n1;
+    b.d2 = static_cast<int>(plan->d2);
+    b.d_out = static_cast<int>(plan->d_out);
+    b.K = st->K;
+    b.s_node = st->s_node;
+    b.s_slice = st->s_slice;
+    b.paths = st->paths;
+    b.items = st->bwd3_items;
+    b.n_items = st->bwd3_n_items;
+    const int grid = std::min(nodes, plan->num_sms);
+    uvw_bwd_edge3_kernel<<<grid, kBwd3Warps * 32, 0, s>>>(b);
     if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw backward edge stage launch failed");
     const float* post[6] = {nullptr, static_cast<const float*>(M),
                             static_cast<float*>(gx) + (size_t)n0 * plan->d1, xrows,
