@@ -448,64 +448,44 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
       A[k][m] = (active && k < K) ? __ldg(As + k * s_slice + m) : 0.f;
       H[k][m] = 0.f;
     }
-  // edge ids 32 at a time (one per lane, broadcast by shuffle); the next edge's
-  // operands are loaded while the current one is computed
-  float yv[D2], r[kKB], gv[D3], yn[D2], rn[kKB], gn[D3];
-  auto load = [&](int e, int d, float (&yy)[D2], float (&rr)[kKB], float (&gg)[D3]) {
+  for (int t = tb; t < te; ++t) {
+    const int e = __ldg(t_eid + t), d = __ldg(t_dst + t);
+    float yv[D2], r[kKB], gv[D3];
 #pragma unroll
-    for (int m = 0; m < D2; ++m) yy[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
+    for (int m = 0; m < D2; ++m) yv[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
 #pragma unroll
-    for (int k = 0; k < kKB; ++k) rr[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
+    for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
     const float* gp = gp_ + (size_t)d * d_out + ooff + w * D3;
 #pragma unroll
-    for (int m = 0; m < D3; ++m) gg[m] = active ? __ldg(gp + m) : 0.f;
-  };
-  for (int t0 = tb; t0 < te; t0 += 32) {
-    const int cnt = min(32, te - t0);
-    const int my_e = lane < cnt ? __ldg(t_eid + t0 + lane) : 0;
-    const int my_d = lane < cnt ? __ldg(t_dst + t0 + lane) : 0;
-    int e = __shfl_sync(0xffffffffu, my_e, 0);
-    load(e, __shfl_sync(0xffffffffu, my_d, 0), yv, r, gv);
-    for (int j = 0; j < cnt; ++j) {
-      const int jn = j + 1 < cnt ? j + 1 : j;
-      const int en = __shfl_sync(0xffffffffu, my_e, jn), dn = __shfl_sync(0xffffffffu, my_d, jn);
-      if (j + 1 < cnt) load(en, dn, yn, rn, gn);
-      float pe[D1];
+    for (int m = 0; m < D3; ++m) gv[m] = active ? __ldg(gp + m) : 0.f;
+    float pe[D1];
 #pragma unroll
-      for (int m = 0; m < D1; ++m) pe[m] = 0.f;
-      CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { pe[m1] += float(c) * yv[m2] * gv[m3]; });
-      float gr[kKB], ar[D1];
+    for (int m = 0; m < D1; ++m) pe[m] = 0.f;
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { pe[m1] += float(c) * yv[m2] * gv[m3]; });
+    float gr[kKB], ar[D1];
 #pragma unroll
-      for (int m = 0; m < D1; ++m) ar[m] = 0.f;
+    for (int m = 0; m < D1; ++m) ar[m] = 0.f;
 #pragma unroll
-      for (int k = 0; k < kKB; ++k) {
-        float dot = 0.f;
+    for (int k = 0; k < kKB; ++k) {
+      float dot = 0.f;
 #pragma unroll
-        for (int m = 0; m < D1; ++m) {
-          H[k][m] += r[k] * pe[m];
-          dot += A[k][m] * pe[m];
-          ar[m] += r[k] * A[k][m];
-        }
-        gr[k] = dot;
+      for (int m = 0; m < D1; ++m) {
+        H[k][m] += r[k] * pe[m];
+        dot += A[k][m] * pe[m];
+        ar[m] += r[k] * A[k][m];
       }
-      float h[8];
+      gr[k] = dot;
+    }
+    float h[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = 0.f;
-      CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { h[m2] += float(c) * ar[m1] * gv[m3]; });
-      const float grt = reduce8(gr, lane);  // lane holds the total of index (lane >> 2) & 7
-      const float ht = reduce8(h, lane);
-      const int idx = (lane >> 2) & 7;
-      if ((lane & 3) == 0) {
-        if (idx < K) gR[(size_t)e * K + idx] += grt;
-        if (idx < D2) gY[(size_t)e * d2 + off2 + idx] += ht;
-      }
-      e = en;
-#pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = yn[m];
-#pragma unroll
-      for (int k = 0; k < kKB; ++k) r[k] = rn[k];
-#pragma unroll
-      for (int m = 0; m < D3; ++m) gv[m] = gn[m];
+    for (int i = 0; i < 8; ++i) h[i] = 0.f;
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { h[m2] += float(c) * ar[m1] * gv[m3]; });
+    const float grt = reduce8(gr, lane);   // lane holds the total of index (lane >> 2) & 7
+    const float ht = reduce8(h, lane);
+    const int idx = (lane >> 2) & 7;
+    if ((lane & 3) == 0) {
+      if (idx < K) gR[(size_t)e * K + idx] += grt;
+      if (idx < D2) gY[(size_t)e * d2 + off2 + idx] += ht;
     }
   }
   if (active) {
@@ -526,7 +506,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
                                 a.s_slice, p.off2, p.ooff, p.aoff, p.mul_out, item.u0, lane);        \
     break;
 
-constexpr int kBwd3Warps = 8;
+constexpr int kBwd3Warps = 16;
 
 __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const Bwd3Args a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
