@@ -86,6 +86,8 @@ struct UvwState {
   float* scratch = nullptr;      // [2][chunk_nodes][s_node]
   float* gm_part = nullptr;      // [kGmSplits][K][w_numel] split-K partials of gM
   Item* bwd3_items = nullptr;    // (path, 32-block of mul_out) in path order
+  int* err_dev = nullptr;        // set by a tensor-core wait that gave up
+  int* err_host = nullptr;       // pinned copy, refreshed after every call (sticky error)
   int bwd3_n_items = 0;
   size_t scratch_elems = 0;
   // GEMM descriptor tables (device) per use
@@ -98,10 +100,21 @@ struct UvwState {
 };
 
 // ---------------------------------------------------------------------------
-// grouped SIMT GEMM:  C[(n,m), j] (+)= sum_seg sum_k A[(n,m), k] B[k, j]
+// grouped GEMM on the tensor cores (tcgen05, kind::tf32, 3xTF32):
+//   C[(n,m), j] (+)= sum_seg sum_k A[(n,m), k] B[k, j]
+// One CTA (4 warps) computes a 128-row x 64-column tile.  Per K step of 32:
+// every thread loads its share of the A and B tiles through the generic
+// strided addressing of the descriptors, splits each value into a TF32 high
+// part and a TF32 residual, and writes both into shared memory in the K-major
+// 128-byte-swizzled layout; one thread issues hi*hi + hi*lo + lo*hi as
+// tcgen05.mma into a TMEM accumulator (128 lanes x 64 columns) and commits to an
+// mbarrier (waited with a bounded spin that records an error instead of
+// hanging).  The epilogue reads TMEM with tcgen05.ld and scatters through the
+// descriptor's (n, m, j) strides.  The three products give FP32-level accuracy.
 // ---------------------------------------------------------------------------
-constexpr int kGT = 64;   // tile rows and columns
-constexpr int kGK = 32;   // k per stage
+constexpr int kTM = 128, kTN = 64, kTK = 32;
+constexpr int kATile = kTM * kTK * 4, kBTile = kTN * kTK * 4;
+constexpr int kTcSmem = 2 * kATile + 2 * kBTile + 1024 + 64;
 
 struct GemmLaunch {
   const float* ptr[6];
@@ -113,20 +126,48 @@ struct GemmLaunch {
   // [y*ceil(nodes/splits), ...) and writes its partial to C + y*c_split_stride
   int splits;
   long long c_split_stride;
+  int* err;  // set when a tensor-core wait gives up
 };
 
-__global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
-  __shared__ __align__(16) float As[kGK][kGT];
-  __shared__ __align__(16) float Bs[kGK][kGT];
-  // locate this CTA's problem and tile
-  int tile = blockIdx.x, pi = 0;
-  int rt = 0, ct = 0;
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// byte offset of element (row r, k) in a K-major tile of 128-byte rows, 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int r, int k) {
+  const uint32_t chunk = (uint32_t)(k >> 2) ^ (uint32_t)(r & 7);
+  return (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u + chunk * 16u + (uint32_t)(k & 3) * 4u;
+}
+// shared-memory matrix descriptor: start >> 4, leading offset 16 B, stride 1024 B
+// (8 rows x 128 B), descriptor version 1, 128-byte swizzle
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+               ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunch L) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* a_hi = sm;
+  unsigned char* a_lo = sm + kATile;
+  unsigned char* b_hi = sm + 2 * kATile;
+  unsigned char* b_lo = sm + 2 * kATile + kBTile;
+  uint64_t* mbar = (uint64_t*)(sm + 2 * kATile + 2 * kBTile);
+  uint32_t* tmem_holder = (uint32_t*)(sm + 2 * kATile + 2 * kBTile + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // locate this CTA's problem and tile (uniform over the CTA)
+  int tile = blockIdx.x, pi = 0, rt = 0, ct = 0;
   GemmProb P;
   for (pi = 0; pi < L.nprob; ++pi) {
     P = L.probs[pi];
-    const int Nn = P.Nn < 0 ? L.nodes : P.Nn;
-    const int rows = Nn * P.D;
-    const int ntr = (rows + kGT - 1) / kGT, ntc = (P.J + kGT - 1) / kGT;
+    const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
+    const int ntr = (rows + kTM - 1) / kTM, ntc = (P.J + kTN - 1) / kTN;
     if (tile < ntr * ntc) {
       rt = tile / ntc;
       ct = tile - rt * ntc;
@@ -135,34 +176,37 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
     tile -= ntr * ntc;
   }
   if (pi >= L.nprob) return;
-  const int Nn = P.Nn < 0 ? L.nodes : P.Nn;
-  const int rows = Nn * P.D;
+  const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
   const float* A = L.ptr[P.a_base];
   const float* B = L.ptr[P.b_base];
   float* C = const_cast<float*>(L.ptr[P.c_base]);
   const int split = blockIdx.y;
   const int slice = (L.nodes + L.splits - 1) / L.splits;
   if (L.splits > 1) C += split * L.c_split_stride;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int r0 = rt * kGT, c0 = ct * kGT;
-  // each thread stages 8 (k, row) A elements and 8 (k, col) B elements per k tile
-  int arow_off[8];
-  bool arow_ok[8];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int i = threadIdx.x + t * 256;
-    const int rr = i % kGT;
-    const int r = r0 + rr;
-    arow_ok[t] = r < rows;
-    const int n = arow_ok[t] ? r / P.D : 0, m = arow_ok[t] ? r - n * P.D : 0;
-    arow_off[t] = n * (int)P.a_n + m * (int)P.a_m;
+  const int r0 = rt * kTM, c0 = ct * kTN;
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
+    asm volatile("fence.mbarrier_init.release.cluster;");
   }
-  float acc[4][4];
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)), "r"(64));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTN >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
+  // this thread stages column k = lane of rows warp + 4 t (A) and of columns warp + 4 t (B)
+  int aoff[kTM / 4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  float ra[8], rb[8];
+  for (int t = 0; t < kTM / 4; ++t) {
+    const int r = r0 + warp + 4 * t;
+    const int n = r < rows ? r / P.D : 0, m = r < rows ? r - n * P.D : 0;
+    aoff[t] = r < rows ? (int)(n * P.a_n + m * P.a_m) : -1;
+  }
+  uint32_t phase = 0;
+  bool first = true;
   for (int s = P.seg0; s < P.seg1; ++s) {
     const GemmSeg S = L.segs[s];
     int kb = 0, ke = S.K < 0 ? L.nodes : S.K;
@@ -172,55 +216,94 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(const GemmLaunch L) {
     }
     const float* Ab = A + P.a_off + S.a_off;
     const float* Bb = B + S.b_off;
-    auto fetch = [&](int k0) {
+    for (int k0 = kb; k0 < ke; k0 += kTK) {
+      const int k = k0 + lane;
+      const bool kin = k < ke;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = threadIdx.x + t * 256;
-        const int kk = i / kGT, rr = i - kk * kGT;
-        const int k = k0 + kk;
-        ra[t] = (arow_ok[t] && k < ke) ? __ldg(Ab + arow_off[t] + (long long)k * S.a_k) : 0.f;
-        const int c = c0 + rr;
-        rb[t] = (c < P.J && k < ke) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
+      for (int t = 0; t < kTM / 4; ++t) {
+        const int rr = warp + 4 * t;
+        const float v = (kin && aoff[t] >= 0) ? __ldg(Ab + aoff[t] + (long long)k * S.a_k) : 0.f;
+        const float hi = tf32_round(v);
+        *(float*)(a_hi + sw128(rr, lane)) = hi;
+        *(float*)(a_lo + sw128(rr, lane)) = tf32_round(v - hi);
       }
-    };
-    if (kb < ke) fetch(kb);
-    for (int k0 = kb; k0 < ke; k0 += kGK) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = threadIdx.x + t * 256;
-        const int kk = i / kGT, rr = i - kk * kGT;
-        As[kk][rr] = ra[t];
-        Bs[kk][rr] = rb[t];
+      for (int t = 0; t < kTN / 4; ++t) {
+        const int jj = warp + 4 * t, c = c0 + jj;
+        const float v = (kin && c < P.J) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
+        const float hi = tf32_round(v);
+        *(float*)(b_hi + sw128(jj, lane)) = hi;
+        *(float*)(b_lo + sw128(jj, lane)) = tf32_round(v - hi);
       }
+      asm volatile("fence.proxy.async.shared::cta;");
       __syncthreads();
-      if (k0 + kGK < ke) fetch(k0 + kGK);  // next tile's loads overlap this tile's math
-#pragma unroll 8
-      for (int kk = 0; kk < kGK; ++kk) {
-        const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-        const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      if (tid == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi), bl = smem_u32(b_lo);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];
+        for (int ks = 0; ks < kTK / 8; ++ks) {
+          const uint32_t off = ks * 32;  // 8 TF32 values along K
+          mma_tf32(tmem, sdesc(ah + off), sdesc(bh + off), idesc, first ? 0u : 1u);
+          mma_tf32(tmem, sdesc(ah + off), sdesc(bl + off), idesc, 1u);
+          mma_tf32(tmem, sdesc(al + off), sdesc(bh + off), idesc, 1u);
+          first = false;
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar)));
       }
-      __syncthreads();
+      first = false;
+      uint32_t done = 0;
+      for (int it = 0; it < (1 << 22) && !done; ++it)
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(smem_u32(mbar)), "r"(phase));
+      phase ^= 1;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      if (__syncthreads_or(!done)) {  // the tensor core did not signal in time: record, clean up, return
+        if (tid == 0) atomicOr(L.err, 1);
+        for (int it = 0; it < (1 << 22); ++it) {  // one more bounded wait for the work in flight
+          uint32_t d2 = 0;
+          asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(d2) : "r"(smem_u32(mbar)), "r"(phase ^ 1));
+          if (d2) break;
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncthreads();
+        if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
+        return;
+      }
     }
   }
-  const int beta = P.beta;
+  // epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w+31
+  const int r = r0 + 32 * warp + lane;
+  const bool rok = r < rows;
+  const int n = rok ? r / P.D : 0, m = rok ? r - n * P.D : 0;
+  float* crow = C + P.c_off + n * P.c_n + m * P.c_m;
+  const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = r0 + ty * 4 + i;
-    if (r >= rows) continue;
-    const int n = r / P.D, m = r - n * P.D;
+  for (int cc = 0; cc < kTN; cc += 16) {
+    uint32_t v[16];
+    if (!first) {
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                   : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                     "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                   : "r"(taddr + cc));
+      asm volatile("tcgen05.wait::ld.sync.aligned;");
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + tx * 4 + j;
-      if (c >= P.J) continue;
-      float* dst = C + P.c_off + n * P.c_n + m * P.c_m + (long long)c * P.c_j;
-      *dst = beta ? *dst + acc[i][j] : acc[i][j];
+      for (int j = 0; j < 16; ++j) v[j] = 0u;  // empty K range: the product is zero
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = c0 + cc + j;
+      if (rok && c < P.J) {
+        float* dst = crow + (long long)c * P.c_j;
+        const float val = __uint_as_float(v[j]);
+        *dst = P.beta ? *dst + val : val;
+      }
     }
   }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
 }
 
 // gM (+)= sum over the split-K partials, in split order (deterministic)
@@ -749,6 +832,13 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
   if (cudaMalloc(&st->gm_part, sizeof(float) * kGmSplits * st->K * plan->w_numel) != cudaSuccess)
     return fail(CGTP_ENOMEM, "uvw gM partial allocation failed");
+  if (cudaMalloc(&st->err_dev, sizeof(int)) != cudaSuccess ||
+      cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocDefault) != cudaSuccess)
+    return fail(CGTP_ENOMEM, "uvw error flag allocation failed");
+  cudaMemset(st->err_dev, 0, sizeof(int));
+  *st->err_host = 0;
+  if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+    return fail(CGTP_ECUDA, "tensor-core GEMM shared memory attribute rejected");
   // shared memory of the edge stages
   const GroupDev& G = lay.groups[0];
   const int d2p = pad_up(int(plan->d2), 4);
@@ -766,6 +856,8 @@ void uvw_destroy(cgtp_plan_s* plan) {
   if (st->tables) cudaFree(st->tables);
   if (st->scratch) cudaFree(st->scratch);
   if (st->gm_part) cudaFree(st->gm_part);
+  if (st->err_dev) cudaFree(st->err_dev);
+  if (st->err_host) cudaFreeHost(st->err_host);
   delete st;
   plan->uvw = nullptr;
 }
@@ -795,7 +887,7 @@ EdgeArgs edge_args(const cgtp_plan_s* plan, const UvwState* st, int group) {
 }
 
 cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
-                        const float* const ptr[6], int nodes, int tiles, cudaStream_t s,
+                        const float* const ptr[6], int nodes, int tiles, cudaStream_t s, int* err,
                         int splits = 1, long long c_split_stride = 0) {
   GemmLaunch L{};
   for (int i = 0; i < 6; ++i) L.ptr[i] = ptr[i];
@@ -805,14 +897,15 @@ cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
   L.segs = segs;
   L.splits = splits;
   L.c_split_stride = c_split_stride;
-  grouped_gemm_kernel<<<dim3(tiles, splits), 256, 0, s>>>(L);
+  L.err = err;
+  grouped_gemm_tc_kernel<<<dim3(tiles, splits), 128, kTcSmem, s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
 
 // tiles of a descriptor set for `nodes` nodes (host copy of the descriptors needed)
 int count_tiles(const std::vector<std::pair<int, int>>& rows_cols) {
   int t = 0;
-  for (auto& rc : rows_cols) t += ((rc.first + kGT - 1) / kGT) * ((rc.second + kGT - 1) / kGT);
+  for (auto& rc : rows_cols) t += ((rc.first + kTM - 1) / kTM) * ((rc.second + kTN - 1) / kTN);
   return t;
 }
 }  // namespace
@@ -842,10 +935,20 @@ static int tiles_for(const cgtp_plan_s* plan, const UvwState* st, int which, int
   return count_tiles(rc);
 }
 
+static cgtp_status sticky_error(const UvwState* st) {
+  if (*st->err_host)
+    return fail(CGTP_ECUDA, "a tensor-core wait gave up in an earlier uvw call on this plan");
+  return CGTP_OK;
+}
+static void refresh_error(const UvwState* st, cudaStream_t s) {
+  cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s);
+}
+
 cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x,
                         const void* Y, const void* R, const void* M, void* out, void* stream) {
   const UvwState* st = static_cast<const UvwState*>(plan->uvw);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cgtp_status e = sticky_error(st)) return e;
   EdgeArgs a = edge_args(plan, st, 0);
   a.x = static_cast<const float*>(x);
   a.Y = static_cast<const float*>(Y);
@@ -864,9 +967,10 @@ cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const vo
     const float* ptr[6] = {st->scratch, static_cast<const float*>(M),
                            static_cast<float*>(out) + (size_t)n0 * plan->d_out, nullptr, nullptr, nullptr};
     cgtp_status r = launch_gemm(st->fwd_probs, st->fwd_np, st->fwd_segs, ptr, nodes,
-                                tiles_for(plan, st, 0, nodes), s);
+                                tiles_for(plan, st, 0, nodes), s, st->err_dev);
     if (r != CGTP_OK) return r;
   }
+  refresh_error(st, s);
   return CGTP_OK;
 }
 
@@ -875,6 +979,7 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
                          void* gY, void* gR, void* gM, void* stream) {
   const UvwState* st = static_cast<const UvwState*>(plan->uvw);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cgtp_status e = sticky_error(st)) return e;
   float* Abuf = st->scratch;
   float* Hbuf = st->scratch + (size_t)st->chunk_nodes * st->s_node;
   bool first = true;
@@ -884,7 +989,7 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     const float* xrows = static_cast<const float*>(x) + (size_t)n0 * plan->d1;
     const float* pre[6] = {Abuf, static_cast<const float*>(M), nullptr, xrows, nullptr, nullptr};
     cgtp_status r = launch_gemm(st->pre_probs, st->pre_np, st->pre_segs, pre, nodes,
-                                tiles_for(plan, st, 1, nodes), s);
+                                tiles_for(plan, st, 1, nodes), s, st->err_dev);
     if (r != CGTP_OK) return r;
     Bwd3Args b{};
     b.Y = static_cast<const float*>(Y);
@@ -913,13 +1018,13 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     const float* post[6] = {nullptr, static_cast<const float*>(M),
                             static_cast<float*>(gx) + (size_t)n0 * plan->d1, xrows,
                             static_cast<float*>(gM), Hbuf};
-    r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s);
+    r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s, st->err_dev);
     if (r != CGTP_OK) return r;
     // gM over this chunk's senders: split-K partials, then an ordered reduction
     const float* postp[6] = {post[0], post[1], post[2], post[3], st->gm_part, post[5]};
     const int splits = std::min(kGmSplits, std::max(1, nodes / 64));
     const long long n_gm = (long long)st->K * plan->w_numel;
-    r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, postp, nodes, tiles_for(plan, st, 3, nodes), s,
+    r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, postp, nodes, tiles_for(plan, st, 3, nodes), s, st->err_dev,
                     splits, n_gm);
     if (r != CGTP_OK) return r;
     splitk_reduce_kernel<<<std::min<long long>((n_gm + 255) / 256, 4096), 256, 0, s>>>(
@@ -927,6 +1032,7 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw gM reduction launch failed");
     first = false;
   }
+  refresh_error(st, s);
   if (g->N == 0) cudaMemsetAsync(gM, 0, sizeof(float) * plan->w_numel * st->K, s);
   return CGTP_OK;
 }
