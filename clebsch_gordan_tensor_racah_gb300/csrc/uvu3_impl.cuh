@@ -300,18 +300,22 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
   }
   __syncthreads();
   const int nb = s_range[0], ne = s_range[1];
-  int wlo, whi;
-  warp_rows(a.rowptr, nb, ne, warp, kV3Warps, &wlo, &whi);
   // path-major: all warps of the CTA work on the same path (one hot instruction
-  // stream), each on an edge-balanced contiguous range of receivers; a barrier
-  // at each path boundary keeps them together
+  // stream); inside a path, warps take the CTA's receivers one at a time from a
+  // shared counter (each receiver's slice of that path is written by one warp)
+  __shared__ int s_next[2];
   for (int it = 0; it < a.n_items; ++it) {
     const Item item = a.items[it];
     const PathDev p = a.paths[item.path];
     const int u = item.u0 + 4 * q;
     const bool active = u < p.mul;
-    if (it) __syncthreads();
-    for (int n = wlo; n < whi; ++n) {
+    if (tid == 0) s_next[it & 1] = nb;
+    __syncthreads();
+    for (;;) {
+      int n = 0;
+      if (lane == 0) n = atomicAdd(&s_next[it & 1], 1);
+      n = __shfl_sync(0xffffffffu, n, 0);
+      if (n >= ne) break;
       const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_FWD_CASE)
@@ -488,11 +492,8 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
   }
   __syncthreads();
   const int sb = s_range[0], se = s_range[1];
-  int wlo, whi;
-  warp_rows(a.rowptr, sb, se, warp, kV3Warps, &wlo, &whi);
-  // the warp that owns sender s clears gx[s] and gY of its out-edges, then
-  // accumulates into them path by path; nobody else touches those rows
-  for (int s = wlo; s < whi; ++s) {
+  // clear gx and gY of the CTA's senders (and their out-edges) before the first path
+  for (int s = sb + warp; s < se; s += kV3Warps) {
     for (int i = lane; i < a.d1; i += 32) a.gx[(size_t)s * a.d1 + i] = T(0);
     const int tb = a.rowptr[s], te = a.rowptr[s + 1];
     for (int i = lane; i < (te - tb) * a.d2; i += 32) {
@@ -500,15 +501,23 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
       a.gY[(size_t)a.col[tb + j] * a.d2 + c] = T(0);
     }
   }
-  __syncwarp();
-  // path-major: one hot instruction stream per SM
+  // path-major: all warps on the same path (one hot instruction stream); inside a
+  // path, warps take senders one at a time from a shared counter.  Paths are
+  // separated by block barriers, so every gx / gY row receives its path
+  // contributions one after another in path order (no races, deterministic).
+  __shared__ int s_next[2];
   for (int it = 0; it < a.n_items; ++it) {
     const Item item = a.items[it];
     const PathDev p = a.paths[item.path];
     const int u = item.u0 + 4 * q;
     const bool active = u < p.mul;
-    if (it) __syncthreads();
-    for (int s = wlo; s < whi; ++s) {
+    if (tid == 0) s_next[it & 1] = sb;
+    __syncthreads();
+    for (;;) {
+      int s = 0;
+      if (lane == 0) s = atomicAdd(&s_next[it & 1], 1);
+      s = __shfl_sync(0xffffffffu, s, 0);
+      if (s >= se) break;
       const int te0 = a.rowptr[s], cnt = a.rowptr[s + 1] - te0;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_BWD_CASE)

@@ -610,21 +610,28 @@ __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const
     s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.n1 : lb(t1);
   }
   __syncthreads();
-  int wlo, whi;
-  uvu3_detail::warp_rows(rp, s_range[0], s_range[1], warp, kBwd3Warps, &wlo, &whi);
-  // the owner warp clears gY and gR of its senders' out-edges
-  for (int s = wlo; s < whi; ++s)
+  const int sb = s_range[0], se = s_range[1];
+  // clear gY and gR of the CTA's senders' out-edges before the first path
+  for (int s = sb + warp; s < se; s += kBwd3Warps)
     for (int t = rp[s]; t < rp[s + 1]; ++t) {
       const int e = a.t_eid[t];
       for (int i = lane; i < a.d2; i += 32) a.gY[(size_t)e * a.d2 + i] = 0.f;
       for (int i = lane; i < a.K; i += 32) a.gR[(size_t)e * a.K + i] = 0.f;
     }
-  __syncwarp();
+  // path-major (one hot instruction stream per SM); inside a path, warps take
+  // senders one at a time from a shared counter, and block barriers between
+  // paths order every row's path contributions (deterministic, race-free)
+  __shared__ int s_next[2];
   for (int it = 0; it < a.n_items; ++it) {
     const Item item = a.items[it];
     const UvwPath p = a.paths[item.path];
-    if (it) __syncthreads();  // path-major: one hot instruction stream per SM
-    for (int s = wlo; s < whi; ++s) {
+    if (tid == 0) s_next[it & 1] = sb;
+    __syncthreads();
+    for (;;) {
+      int s = 0;
+      if (lane == 0) s = atomicAdd(&s_next[it & 1], 1);
+      s = __shfl_sync(0xffffffffu, s, 0);
+      if (s >= se) break;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(UVW3_BWD_CASE)
         default: break;
