@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -181,6 +182,7 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (s == CGTP_OK) s = upload_layout(p, conv, &p->conv_layout);
     if (s == CGTP_OK) s = upload_layout(p, batch, &p->batch_layout);
     if (s == CGTP_OK) s = build_v3(p);
+    if (s == CGTP_OK) s = bt_create(p);
   } else {
     s = uvw_create(p);
   }
@@ -197,6 +199,7 @@ void cgtp_plan_destroy(cgtp_plan plan) {
   free_layout(&plan->conv_layout);
   free_layout(&plan->batch_layout);
   free_v3(plan);
+  bt_destroy(plan);
   if (plan->uvw) uvw_destroy(plan);
   delete plan;
 }
@@ -238,6 +241,7 @@ cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const v
   if (B == 0) return CGTP_OK;
   cgtp_status s;
   if ((s = need(x1, "x1")) || (s = need(x2, "x2")) || (s = need(W, "W")) || (s = need(out, "out"))) return s;
+  if (!std::getenv("CGTP_UVU_NO_BT") && bt_forward(plan, x1, x2, W, out, B, stream, &s)) return s;
   return launch_uvu_forward(plan, plan->batch_layout, x1, x2, W, out, nullptr, nullptr, B, true, stream);
 }
 
@@ -252,6 +256,7 @@ cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, cons
   if ((s = need(gout, "gout")) || (s = need(x1, "x1")) || (s = need(x2, "x2")) || (s = need(W, "W")) ||
       (s = need(gx1, "gx1")) || (s = need(gx2, "gx2")) || (s = need(gW, "gW")))
     return s;
+  if (!std::getenv("CGTP_UVU_NO_BT") && bt_backward(plan, gout, x1, x2, W, gx1, gx2, gW, B, stream, &s)) return s;
   return launch_uvu_backward(plan, plan->batch_layout, gout, x1, x2, W, gx1, gx2, gW, nullptr, nullptr,
                              nullptr, B, true, stream);
 }

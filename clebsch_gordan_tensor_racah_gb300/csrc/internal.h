@@ -147,6 +147,8 @@ struct cgtp_plan_s {
   cgtp::V3Dev v3;
   // uvw (radial) state is kept opaque here; see uvw.cu
   void* uvw = nullptr;
+  // batched-product kernels for multiplicity 16 / 32 (bt.cu); null when the plan does not qualify
+  void* bt = nullptr;
 };
 
 struct cgtp_graph_s {
@@ -193,6 +195,14 @@ bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
                         cgtp_status* st);
+
+// bt.cu (batched product without a graph; return false when the plan does not qualify)
+cgtp_status bt_create(cgtp_plan_s* plan);
+void bt_destroy(cgtp_plan_s* plan);
+bool bt_forward(const cgtp_plan_s* plan, const void* x1, const void* x2, const void* W, void* out,
+                int64_t B, void* stream, cgtp_status* status);
+bool bt_backward(const cgtp_plan_s* plan, const void* gout, const void* x1, const void* x2, const void* W,
+                 void* gx1, void* gx2, void* gW, int64_t B, void* stream, cgtp_status* status);
 
 // graph.cu
 cgtp_status graph_build(cgtp_graph_s* g, void* stream);

@@ -189,6 +189,38 @@ def test_batched_high_l_small():
     close("gW", gW, rW, np.float32)
 
 
+def _batched_case(in1, in2, out, B, seed):
+    oplan = oirr.make_plan(in1, in2, out, "uvu")
+    rng = np.random.default_rng(seed)
+    x1 = rng.standard_normal((B, oplan.d1)).astype(np.float32)
+    x2 = rng.standard_normal((B, oplan.d2)).astype(np.float32)
+    W = rng.standard_normal((B, oplan.w_numel)).astype(np.float32)
+    plan = cg.Plan(in1, in2, out, "uvu", torch.float32)
+    out_d = cg.cgtp_forward(plan, T(x1), T(x2), T(W))
+    close("out", out_d, oconv.tp_uvu_forward(oplan, x1, x2, W), np.float32)
+    g = rng.standard_normal((B, oplan.d_out)).astype(np.float32)
+    gx1, gx2, gW = cg.cgtp_backward(plan, T(g), T(x1), T(x2), T(W))
+    r1, r2, rW = oconv.tp_uvu_backward(oplan, g, x1, x2, W)
+    close("gx1", gx1, r1, np.float32)
+    close("gx2", gx2, r2, np.float32)
+    close("gW", gW, rW, np.float32)
+
+
+def test_batched_high_l_odd_batch():
+    # 16 channels: two samples per warp, an odd tail; l up to 7 spans several path groups
+    spec = wl.SPECS["highl"]
+    _batched_case(spec["in1"], spec["in2"], spec["out"], 37, 11)
+    _batched_case(spec["in1"], spec["in2"], spec["out"], 1, 12)
+
+
+def test_batched_mul32_mixed_l():
+    # 32 channels: one sample per warp; in1 blocks shared by several path groups
+    in1 = "32x0e+32x1o+32x2e+32x3o+32x4e+32x5o"
+    in2 = "1x0e+1x1o+1x2e+1x3o+1x4e+1x5o"
+    out = "1x0e+1x1o+1x2e+1x3o+1x4e+1x5o+1x0o+1x1e+1x2o+1x3e+1x4o+1x5e"
+    _batched_case(in1, in2, out, 23, 13)
+
+
 def test_deterministic_bitwise():
     plan, graph, w = run_conv("nequip", N=200, check_grad=False)
     x, Y, W = T(w["x"]), T(w["Y"]), T(w["W"])
