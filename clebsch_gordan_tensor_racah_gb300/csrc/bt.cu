@@ -15,24 +15,29 @@
 //   gy[b][m2]    = sum_p sum_{m1,m3} C[m1,m2,m3] G[m3][m1]
 //
 // GB300 organisation.  At L = 7 there are 260 paths and ~24k CG nonzeros, far
-// too many to bake into code, so the coefficients are tables: every cy entry
-// has at most two CG terms (real basis), and the gy contraction is a list of
-// (G slot, coefficient) per m2.  The paths are cut into contiguous groups whose
-// tables fit a CTA's shared memory; grid.y is the group and grid.x a slice of
-// the samples, so each CTA loads its tables once and then streams samples.
-// Lanes map to channels (lanes per sample = multiplicity, 16 -> two samples a
-// warp), every warp works on its own samples with only warp barriers:
-//   * cy is formed by the sample's lanes into a per-warp buffer, rows padded
-//     to a multiple of four so the contraction reads it as broadcast float4;
-//   * the channel contraction uses the paired FP32 FMA (fma.rn.f32x2);
-//   * outputs go through a per-warp tile and leave as streaming float4 stores
-//     (the forward writes 7.7 GB at L = 7: the kernel is write-bandwidth bound);
-//   * backward: lane u forms W*g for its channel and the lane holding m1 forms
-//     G[.][m1] from the transposed W*g rows (into the dead cy buffer); lanes m2
-//     then apply the gy table.
-// gx blocks shared by several groups and gy (every group touches it) leave as
-// per-group partials in a bounded plan-owned scratch (chunks of samples) and a
-// reduce kernel adds them in group order: deterministic, no atomics.
+// too many to bake into code, so the coefficients are tables in shared memory:
+// every cy entry has at most two CG terms (real basis), and the gy contraction
+// is a list of (G slot, coefficient) per m2.  The paths are cut into contiguous
+// groups whose tables fit a CTA's shared memory.
+//
+// A lane owns one channel u of a PAIR of samples: every paired FP32 FMA
+// (fma.rn.f32x2) advances both samples, so the table reads, the index
+// arithmetic and the loop overhead are shared by two samples and no
+// horizontal adds are needed.  Multiplicity 16 gives two pairs per warp.
+//   * cy of the pair is formed by the pair's lanes into a per-warp buffer as
+//     interleaved (sample 0, sample 1) values, rows padded to a multiple of
+//     four, read back as broadcast float4 (two m1 of both samples);
+//   * x of the pair stays in registers for a run of paths on one in1 block;
+//   * forward outputs go through per-sample tiles and leave as streaming
+//     float4 stores (7.7 GB at L = 7: the forward is write-bandwidth bound);
+//   * backward: lane u forms W*g of its channel; the lane of m1 contracts the
+//     transposed W*g rows with x[.][m1] into G; lanes m2 apply the gy table.
+// Both kernels are persistent (SMs x resident CTAs) and take work units from a
+// device counter zeroed before the launch.  Forward unit: (path group, chunk of
+// 32 samples), group-major, so a CTA reloads tables only when its group
+// changes.  Backward unit: a 32-sample batch that the CTA walks through all
+// groups (reloading the tables), so gx and gy of a sample are owned by one
+// warp: deterministic, no floating-point atomics, no scratch.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -48,21 +53,19 @@ namespace bt_detail {
 
 constexpr int kBtWarps = 8;
 constexpr int kBtThreads = kBtWarps * 32;
-constexpr int kMaxD = 15;                // largest block dimension (l <= 7)
-constexpr int kCyW = kMaxD * 16;         // per-sample cy / G buffer: [m3 < 15][m1 < 16]
-constexpr int kGStride = 16;             // row stride of the G buffer
-constexpr size_t kTableBudget = 44 * 1024;
-constexpr size_t kScratchBytes = size_t(64) << 20;
+constexpr int kMaxD = 15;                 // largest block dimension (l <= 7)
+constexpr int kCyPair = kMaxD * 16 + 8;   // float2 per pair: cy / G [m3][m1 < 16] (+8: bank offset)
+constexpr int kGStride = 16;              // row stride (float2) of the G buffer
+constexpr size_t kTableBudget = 24 * 1024;
 
 struct BtPath {   // 16 ints
   int D1, D2, D3, Q;        // Q = D1 rounded up to a multiple of 4, divided by 4
   int off1, off2, ooff, woff;
   int ctab;                 // first cy entry of the path (group-relative), D3 * 4Q entries
   int grow;                 // first gy row pointer (group-relative), D2 + 1 of them
-  int gxo;                  // gx destination: offset in the gx row (gxp = 0) or in the scratch row
-  int gxp;                  // 1: the path's in1 block is shared with other groups
-  int flush;                // 1: last path of its in1 run inside the group
-  int pad0, pad1, pad2;
+  int run;                  // first path of a run on one in1 block: paths in the run; else 0
+  int gxfirst;              // backward: the run is the first to touch its in1 block (store, not add)
+  int pad0, pad1, pad2, pad3;
 };
 static_assert(sizeof(BtPath) == 64, "BtPath is 64 bytes");
 
@@ -71,8 +74,6 @@ struct BtGroup {
   int ctab0, ctab_n;        // cy entries
   int grow0, grow_n;        // gy row pointers
   int gent0, gent_n;        // gy entries
-  int gy_part;              // offset of the group's gy partial in the scratch row
-  int pad0, pad1, pad2;
 };
 
 struct BtArgs {
@@ -82,19 +83,27 @@ struct BtArgs {
   const float* gout;
   float* out;
   float* gx;
+  float* gy;
   float* gW;
-  float* scratch;
-  int b0, b1;               // samples [b0, b1) of this launch
-  int d1, d2, d2p, d_out, w_numel;
-  int scratch_row;
-  int slices;
+  int B;
+  int d1, d2, d_out, w_numel;
+  int G;
+  int unit;                 // samples per work unit (8 warps x 2 pairs x 2 samples for multiplicity 16)
+  int chunks;               // forward: sample chunks per group (units = G * chunks)
+  int n_units;
+  int* counter;             // work-unit counter, zeroed before each launch
+  int y2s;                  // float2 stride of a pair's y / gy buffer
+  int tile;                 // float stride of a sample's output tile (forward)
+  int wgs;                  // float2 stride of a pair's W*g buffer (backward)
   int warp_floats;
+  int table_bytes;          // backward: shared-memory bytes reserved for one group's tables
+  int n_zero;               // in1 blocks no path touches (gx = 0 there)
+  const int* zero_blk;      // (offset, size) pairs
   const BtPath* paths;
   const BtGroup* groups;
-  const float2* ccoef;
-  const uint16_t* ccol;
+  const float4* ctab;       // (c_a, c_b, byte offset of y[m2_a], byte offset of y[m2_b]) in the pair's y row
   const int* grow;
-  const float2* gent;
+  const float2* gent;       // (coefficient, byte offset of the G slot)
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) / 16 * 16; }
@@ -107,311 +116,363 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
         "l"(*reinterpret_cast<unsigned long long*>(&c)));
   return *reinterpret_cast<float2*>(&d);
 }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 ld_pair(const float* a, const float* b, bool va, bool vb) {
+  return make_float2(va ? __ldg(a) : 0.f, vb ? __ldg(b) : 0.f);
+}
 
-// cy[m3][m1] of one sample: the sample's lanes split the D3 x 4Q entries
-template <int LPS, int Q>
-__device__ __forceinline__ void coupling(const BtPath& p, const float2* sc, const uint16_t* scol,
-                                         const float* ysw, float* cyw, int q) {
-  const int ne = p.D3 * 4 * Q;
-  const float* yb = ysw + p.off2;
-  for (int e = q; e < ne; e += LPS) {
-    const float2 c = sc[p.ctab + e];
-    const unsigned cc = scol[p.ctab + e];
-    cyw[e] = fmaf(c.y, yb[cc >> 8], c.x * yb[cc & 255u]);
+// Group tables into shared memory: paths, cy entries [, gy row pointers, gy entries].
+__device__ __forceinline__ void load_tables(const BtArgs& a, const BtGroup& g, unsigned char* smem,
+                                            bool with_gy) {
+  const int np = g.p1 - g.p0;
+  int4* sp = reinterpret_cast<int4*>(smem);
+  const int4* gp = reinterpret_cast<const int4*>(a.paths + g.p0);
+  for (int i = threadIdx.x; i < np * 4; i += blockDim.x) sp[i] = gp[i];
+  float4* sc = reinterpret_cast<float4*>(smem + (size_t)np * sizeof(BtPath));
+  for (int i = threadIdx.x; i < g.ctab_n; i += blockDim.x) sc[i] = a.ctab[g.ctab0 + i];
+  if (with_gy) {
+    const size_t o_grow = (size_t)np * sizeof(BtPath) + (size_t)g.ctab_n * 16;
+    int* sg = reinterpret_cast<int*>(smem + o_grow);
+    for (int i = threadIdx.x; i < g.grow_n; i += blockDim.x) sg[i] = a.grow[g.grow0 + i];
+    float2* se = reinterpret_cast<float2*>(smem + al16(o_grow + (size_t)g.grow_n * 4));
+    for (int i = threadIdx.x; i < g.gent_n; i += blockDim.x) se[i] = a.gent[g.gent0 + i];
   }
+}
+
+// cy of a sample pair: the pair's lanes split the D3 x 4Q entries
+template <int LPP, int Q>
+__device__ __forceinline__ void coupling(const BtPath& p, const float4* sc, const float2* y2, float2* cy2,
+                                         int u) {
+  const int ne = p.D3 * 4 * Q;
+  const char* yb = reinterpret_cast<const char*>(y2);
+  for (int e = u; e < ne; e += LPP) {
+    const float4 c = sc[p.ctab + e];
+    const float2 ya = *reinterpret_cast<const float2*>(yb + __float_as_int(c.z));
+    const float2 yv = *reinterpret_cast<const float2*>(yb + __float_as_int(c.w));
+    cy2[e] = fma2(make_float2(c.y, c.y), yv, mul2(make_float2(c.x, c.x), ya));
+  }
+}
+
+// x of the lane's channel for both samples of the pair (zero past D1)
+template <int Q>
+__device__ __forceinline__ void load_x2(const BtArgs& a, const BtPath& p, int b0, int b1, bool v0, bool v1,
+                                        int u, float2 (&x2)[4 * Q]) {
+  const float* xa = a.x + (size_t)b0 * a.d1 + p.off1 + u * p.D1;
+  const float* xb = a.x + (size_t)b1 * a.d1 + p.off1 + u * p.D1;
+#pragma unroll
+  for (int m = 0; m < 4 * Q; ++m) x2[m] = ld_pair(xa + m, xb + m, v0 && m < p.D1, v1 && m < p.D1);
 }
 
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
-template <int LPS, int Q>
-__device__ __forceinline__ void fwd_path(const BtPath& p, const BtArgs& a, const float2* sc,
-                                         const uint16_t* scol, const float* ysw, float* cyw, float* tw,
-                                         int b, bool valid, int q) {
+template <int LPP, int Q>
+__device__ __forceinline__ void fwd_run(const BtArgs& a, const BtPath* sp, int n, const float4* sc,
+                                        const float2* y2, float2* cy2, float* t0, float* t1, int b0, int b1,
+                                        bool v0, bool v1, int u) {
   constexpr int D1P = 4 * Q;
-  float xv[D1P];
-  const float* xr = a.x + (size_t)b * a.d1 + p.off1 + q * p.D1;
+  float2 x2[D1P];
+  load_x2<Q>(a, sp[0], b0, b1, v0, v1, u, x2);
+  for (int k = 0; k < n; ++k) {
+    const BtPath p = sp[k];
+    const float2 w2 = ld_pair(a.W + (size_t)b0 * a.w_numel + p.woff + u,
+                              a.W + (size_t)b1 * a.w_numel + p.woff + u, v0, v1);
+    coupling<LPP, Q>(p, sc, y2, cy2, u);
+    __syncwarp();
+    // D3 = 2 l3 + 1 is odd: (D3 - 1) / 2 guarded row pairs and the last row,
+    // each row as two independent FMA chains
+    auto row_out = [&](int m3) {
+      const float4* row = reinterpret_cast<const float4*>(cy2 + m3 * D1P);
+      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int m = 0; m < D1P; ++m) xv[m] = (valid && m < p.D1) ? __ldg(xr + m) : 0.f;
-  const float w = valid ? __ldg(a.W + (size_t)b * a.w_numel + p.woff + q) : 0.f;
-  coupling<LPS, Q>(p, sc, scol, ysw, cyw, q);
-  __syncwarp();
-  // m3 unrolled to its bound (warp-uniform guards): independent accumulators
-#pragma unroll
-  for (int m3 = 0; m3 < kMaxD; ++m3) {
-    if (m3 < p.D3) {
-      const float4* row = reinterpret_cast<const float4*>(cyw + m3 * D1P);
-      float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < Q; ++j) {
+      for (int j = 0; j < 2 * Q; ++j) {
         const float4 c = row[j];
-        acc = fma2(make_float2(c.x, c.y), make_float2(xv[4 * j], xv[4 * j + 1]), acc);
-        acc = fma2(make_float2(c.z, c.w), make_float2(xv[4 * j + 2], xv[4 * j + 3]), acc);
+        a0 = fma2(make_float2(c.x, c.y), x2[2 * j], a0);
+        a1 = fma2(make_float2(c.z, c.w), x2[2 * j + 1], a1);
       }
-      tw[q * p.D3 + m3] = w * (acc.x + acc.y);
+      const float2 o = mul2(make_float2(a0.x + a1.x, a0.y + a1.y), w2);
+      t0[u * p.D3 + m3] = o.x;
+      t1[u * p.D3 + m3] = o.y;
+    };
+#pragma unroll
+    for (int m3 = 0; m3 + 1 < kMaxD; m3 += 2) {
+      if (m3 + 1 < p.D3) {
+        row_out(m3);
+        row_out(m3 + 1);
+      }
     }
-  }
-  __syncwarp();
-  if (valid) {
-    const int nv = p.D3 * LPS / 4;
-    float4* dst = reinterpret_cast<float4*>(a.out + (size_t)b * a.d_out + p.ooff);
-    const float4* src = reinterpret_cast<const float4*>(tw);
-    for (int i = q; i < nv; i += LPS) __stcs(dst + i, src[i]);
+    row_out(p.D3 - 1);
+    __syncwarp();
+    const int nv = p.D3 * LPP / 4;
+    if (v0) {
+      float4* dst = reinterpret_cast<float4*>(a.out + (size_t)b0 * a.d_out + p.ooff);
+      for (int i = u; i < nv; i += LPP) __stcs(dst + i, reinterpret_cast<const float4*>(t0)[i]);
+    }
+    if (v1) {
+      float4* dst = reinterpret_cast<float4*>(a.out + (size_t)b1 * a.d_out + p.ooff);
+      for (int i = u; i < nv; i += LPP) __stcs(dst + i, reinterpret_cast<const float4*>(t1)[i]);
+    }
   }
 }
 
-template <int LPS>
+template <int LPP>
 __global__ void __launch_bounds__(kBtThreads, 2) bt_forward_kernel(const BtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int SPW = 32 / LPS;
-  const BtGroup grp = a.groups[blockIdx.y];
-  const int np = grp.p1 - grp.p0;
-  BtPath* sp = reinterpret_cast<BtPath*>(smem);
-  float2* sc = reinterpret_cast<float2*>(smem + (size_t)np * sizeof(BtPath));
-  uint16_t* scol = reinterpret_cast<uint16_t*>(sc + grp.ctab_n);
-  float* wbuf = reinterpret_cast<float*>(smem + al16((size_t)np * sizeof(BtPath) + (size_t)grp.ctab_n * 10));
-  const int tid = threadIdx.x;
-  for (int i = tid; i < np * 16; i += kBtThreads)
-    reinterpret_cast<int*>(sp)[i] = reinterpret_cast<const int*>(a.paths + grp.p0)[i];
-  for (int i = tid; i < grp.ctab_n; i += kBtThreads) {
-    sc[i] = a.ccoef[grp.ctab0 + i];
-    scol[i] = a.ccol[grp.ctab0 + i];
-  }
-  __syncthreads();
-  const int lane = tid & 31, warp = tid >> 5, q = lane % LPS, s = lane / LPS;
-  float* ys = wbuf + (size_t)warp * a.warp_floats;
-  float* ysw = ys + s * a.d2p;
-  float* cyw = ys + SPW * a.d2p + s * kCyW;
-  float* tw = ys + SPW * (a.d2p + kCyW) + s * (LPS * kMaxD);
-  const int nS = a.b1 - a.b0;
-  const int sb = a.b0 + (int)((long long)nS * blockIdx.x / a.slices);
-  const int se = a.b0 + (int)((long long)nS * (blockIdx.x + 1) / a.slices);
-  for (int base = sb + warp * SPW; base < se; base += kBtWarps * SPW) {
-    const int bs = base + s;
-    const bool valid = bs < se;
-    const int b = valid ? bs : base;
-    for (int i = q; i < a.d2; i += LPS) ysw[i] = valid ? __ldg(a.y + (size_t)b * a.d2 + i) : 0.f;
-    __syncwarp();
-    for (int pi = 0; pi < np; ++pi) {
-      const BtPath p = sp[pi];
-      switch (p.Q) {
-        case 1: fwd_path<LPS, 1>(p, a, sc, scol, ysw, cyw, tw, b, valid, q); break;
-        case 2: fwd_path<LPS, 2>(p, a, sc, scol, ysw, cyw, tw, b, valid, q); break;
-        case 3: fwd_path<LPS, 3>(p, a, sc, scol, ysw, cyw, tw, b, valid, q); break;
-        default: fwd_path<LPS, 4>(p, a, sc, scol, ysw, cyw, tw, b, valid, q); break;
-      }
+  constexpr int PPW = 32 / LPP;
+  __shared__ int s_unit;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, pr = lane / LPP, u = lane % LPP;
+  // persistent CTAs take (group, sample chunk) units in group-major order from a
+  // counter, so a CTA reloads its tables only when its group changes
+  int cur = -1, np = 0;
+  const BtPath* sp = reinterpret_cast<const BtPath*>(smem);
+  const float4* sc = nullptr;
+  float* wb = nullptr;
+  for (;;) {
+    __syncthreads();  // the previous unit is done with the tables and buffers
+    if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
+    __syncthreads();
+    const int unit = s_unit;
+    if (unit >= a.n_units) break;
+    const int gi = unit / a.chunks, chunk = unit - gi * a.chunks;
+    if (gi != cur) {
+      const BtGroup grp = a.groups[gi];
+      load_tables(a, grp, smem, false);
+      __syncthreads();
+      cur = gi;
+      np = grp.p1 - grp.p0;
+      sc = reinterpret_cast<const float4*>(smem + (size_t)np * sizeof(BtPath));
+      wb = reinterpret_cast<float*>(smem + al16((size_t)np * sizeof(BtPath) + (size_t)grp.ctab_n * 16)) +
+           (size_t)warp * a.warp_floats;
     }
+    float2* y2 = reinterpret_cast<float2*>(wb) + pr * a.y2s;
+    float2* cy2 = reinterpret_cast<float2*>(wb) + PPW * a.y2s + pr * kCyPair;
+    float* t0 = wb + 2 * (PPW * a.y2s + PPW * kCyPair) + (2 * pr) * a.tile;
+    float* t1 = t0 + a.tile;
+    const int base = chunk * a.unit + warp * 2 * PPW;
+    if (base >= a.B) continue;
+    const int s0 = base + 2 * pr, s1 = s0 + 1;
+    const bool v0 = s0 < a.B, v1 = s1 < a.B;
+    const int b0 = v0 ? s0 : base, b1 = v1 ? s1 : base;
+    for (int i = u; i < a.d2; i += LPP)
+      y2[i] = ld_pair(a.y + (size_t)b0 * a.d2 + i, a.y + (size_t)b1 * a.d2 + i, v0, v1);
     __syncwarp();
+    for (int pi = 0; pi < np;) {
+      const int n = sp[pi].run;
+      switch (sp[pi].Q) {
+        case 1: fwd_run<LPP, 1>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        case 2: fwd_run<LPP, 2>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        case 3: fwd_run<LPP, 3>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        default: fwd_run<LPP, 4>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+      }
+      pi += n;
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
-template <int LPS, int Q>
-__device__ __forceinline__ void bwd_path(const BtPath& p, const BtArgs& a, const float2* sc,
-                                         const uint16_t* scol, const int* sgrow, const float2* sgent,
-                                         const float* ysw, float* cyw, float* wgw, float* gyw,
-                                         float2 (&gxa)[8], int b, bool valid, int q, float* srow) {
+template <int LPP, int Q>
+__device__ __forceinline__ void bwd_run(const BtArgs& a, const BtPath* sp, int n, const float4* sc,
+                                        const int* sgrow, const float2* sgent, const float2* y2, float2* gy2,
+                                        float2* cy2, float2* wg2, int b0, int b1, bool v0, bool v1, int u) {
   constexpr int D1P = 4 * Q;
-  const float* xr = a.x + (size_t)b * a.d1 + p.off1;
-  float xv[D1P], xt[LPS];
+  const BtPath p0 = sp[0];
+  float2 x2[D1P], gxa[D1P];
+  load_x2<Q>(a, p0, b0, b1, v0, v1, u, x2);
 #pragma unroll
-  for (int m = 0; m < D1P; ++m) xv[m] = (valid && m < p.D1) ? __ldg(xr + q * p.D1 + m) : 0.f;
-  const bool own_m1 = valid && q < p.D1;
+  for (int m = 0; m < D1P; ++m) gxa[m] = make_float2(0.f, 0.f);
+  const float* xa = a.x + (size_t)b0 * a.d1 + p0.off1;
+  const float* xb = a.x + (size_t)b1 * a.d1 + p0.off1;
+  // G stage lanes: m1 = u % 16, channel half h = u / 16 (multiplicity 32 only)
+  const int gm1 = u & 15, gh = u >> 4;
+  const unsigned gmask = LPP == 32 ? (((1u << p0.D1) - 1u) | (((1u << p0.D1) - 1u) << 16)) : 0u;
+  for (int k = 0; k < n; ++k) {
+    const BtPath p = sp[k];
+    const float2 w2 = ld_pair(a.W + (size_t)b0 * a.w_numel + p.woff + u,
+                              a.W + (size_t)b1 * a.w_numel + p.woff + u, v0, v1);
+    const float* ga = a.gout + (size_t)b0 * a.d_out + p.ooff + u * p.D3;
+    const float* gb = a.gout + (size_t)b1 * a.d_out + p.ooff + u * p.D3;
+    float2 g2[kMaxD];
 #pragma unroll
-  for (int u = 0; u < LPS; ++u) xt[u] = own_m1 ? __ldg(xr + u * p.D1 + q) : 0.f;
-  const float w = valid ? __ldg(a.W + (size_t)b * a.w_numel + p.woff + q) : 0.f;
-  // the path's output-gradient slice of this channel, all loads in flight at once
-  const float* gr = a.gout + (size_t)b * a.d_out + p.ooff + q * p.D3;
-  float gv[kMaxD];
+    for (int m3 = 0; m3 < kMaxD; ++m3) g2[m3] = ld_pair(ga + m3, gb + m3, v0 && m3 < p.D3, v1 && m3 < p.D3);
+    coupling<LPP, Q>(p, sc, y2, cy2, u);
+    __syncwarp();
+    // t = cy x (-> gW), gx += cy^T (W g); W g goes to the transposed buffer.
+    // One row per guarded block (registers are full); the gx updates of a row
+    // are independent and t is split into two chains.
+    float2 gw = make_float2(0.f, 0.f);
+    auto row_bwd = [&](int m3, float2 gv) {
+      const float2 wg = mul2(w2, gv);
+      wg2[m3 * LPP + u] = wg;
+      const float4* row = reinterpret_cast<const float4*>(cy2 + m3 * D1P);
+      float2 ta = make_float2(0.f, 0.f), tb = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int m3 = 0; m3 < kMaxD; ++m3) gv[m3] = (valid && m3 < p.D3) ? __ldg(gr + m3) : 0.f;
-  coupling<LPS, Q>(p, sc, scol, ysw, cyw, q);
-  __syncwarp();
-  // t = cy x (-> gW), gx += cy^T (W g); W g goes to the transposed buffer
-  float gw = 0.f;
-#pragma unroll
-  for (int m3 = 0; m3 < kMaxD; ++m3) {
-    if (m3 < p.D3) {
-      const float wg = w * gv[m3];
-      wgw[m3 * LPS + q] = wg;
-      const float2 wg2 = make_float2(wg, wg);
-      const float4* row = reinterpret_cast<const float4*>(cyw + m3 * D1P);
-      float2 t = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < Q; ++j) {
+      for (int j = 0; j < 2 * Q; ++j) {
         const float4 c = row[j];
-        const float2 c01 = make_float2(c.x, c.y), c23 = make_float2(c.z, c.w);
-        t = fma2(c01, make_float2(xv[4 * j], xv[4 * j + 1]), t);
-        t = fma2(c23, make_float2(xv[4 * j + 2], xv[4 * j + 3]), t);
-        gxa[2 * j] = fma2(c01, wg2, gxa[2 * j]);
-        gxa[2 * j + 1] = fma2(c23, wg2, gxa[2 * j + 1]);
+        const float2 c0 = make_float2(c.x, c.y), c1 = make_float2(c.z, c.w);
+        ta = fma2(c0, x2[2 * j], ta);
+        tb = fma2(c1, x2[2 * j + 1], tb);
+        gxa[2 * j] = fma2(c0, wg, gxa[2 * j]);
+        gxa[2 * j + 1] = fma2(c1, wg, gxa[2 * j + 1]);
       }
-      gw = fmaf(gv[m3], t.x + t.y, gw);
-    }
-  }
-  if (valid) a.gW[(size_t)b * a.w_numel + p.woff + q] = gw;
-  __syncwarp();
-  // G[m3][m1] = sum_u x[u][m1] (W g)[u][m3]; lane q holds m1 = q.  G reuses the
-  // cy buffer (cy is dead once the contraction above is done).
-  float* Gw = cyw;
-  if (q < p.D1) {
+      gw = fma2(gv, make_float2(ta.x + tb.x, ta.y + tb.y), gw);
+    };
 #pragma unroll
-    for (int m3 = 0; m3 < kMaxD; ++m3) {
-      if (m3 < p.D3) {
-        const float4* r = reinterpret_cast<const float4*>(wgw + m3 * LPS);
-        float2 acc = make_float2(0.f, 0.f);
+    for (int m3 = 0; m3 < kMaxD; ++m3)
+      if (m3 < p.D3) row_bwd(m3, g2[m3]);
+    if (v0) a.gW[(size_t)b0 * a.w_numel + p.woff + u] = gw.x;
+    if (v1) a.gW[(size_t)b1 * a.w_numel + p.woff + u] = gw.y;
+    __syncwarp();
+    // G[m3][m1] = sum_u x[u][m1] (W g)[u][m3] into the dead cy buffer
+    float2* G2 = cy2;
+    if (gm1 < p.D1) {
+      float2 xt[16];
 #pragma unroll
-        for (int j = 0; j < LPS / 4; ++j) {
+      for (int v = 0; v < 16; ++v) {
+        const int uu = gh * 16 + v;
+        xt[v] = ld_pair(xa + uu * p.D1 + gm1, xb + uu * p.D1 + gm1, v0, v1);
+      }
+      auto row_g = [&](int m3) {
+        const float4* r = reinterpret_cast<const float4*>(wg2 + m3 * LPP + gh * 16);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
           const float4 c = r[j];
-          acc = fma2(make_float2(c.x, c.y), make_float2(xt[4 * j], xt[4 * j + 1]), acc);
-          acc = fma2(make_float2(c.z, c.w), make_float2(xt[4 * j + 2], xt[4 * j + 3]), acc);
+          a0 = fma2(make_float2(c.x, c.y), xt[2 * j], a0);
+          a1 = fma2(make_float2(c.z, c.w), xt[2 * j + 1], a1);
         }
-        Gw[m3 * kGStride + q] = acc.x + acc.y;
+        float2 acc = make_float2(a0.x + a1.x, a0.y + a1.y);
+        if (LPP == 32) {
+          acc.x += __shfl_xor_sync(gmask, acc.x, 16);
+          acc.y += __shfl_xor_sync(gmask, acc.y, 16);
+        }
+        if (gh == 0) G2[m3 * kGStride + gm1] = acc;
+      };
+#pragma unroll
+      for (int m3 = 0; m3 + 1 < kMaxD; m3 += 2) {
+        if (m3 + 1 < p.D3) {
+          row_g(m3);
+          row_g(m3 + 1);
+        }
       }
+      row_g(p.D3 - 1);
     }
+    __syncwarp();
+    // gy[m2] += sum C[m1,m2,m3] G[m3][m1]; lane u holds m2 = u
+    if (u < p.D2) {
+      const int r0 = sgrow[p.grow + u], r1 = sgrow[p.grow + u + 1];
+      const char* gbase = reinterpret_cast<const char*>(G2);
+      float2 v = make_float2(0.f, 0.f);
+      for (int r = r0; r < r1; ++r) {
+        const float2 t = sgent[r];
+        v = fma2(make_float2(t.x, t.x), *reinterpret_cast<const float2*>(gbase + __float_as_int(t.y)), v);
+      }
+      float2& acc = gy2[p.off2 + u];
+      acc = make_float2(acc.x + v.x, acc.y + v.y);
+    }
+    __syncwarp();  // G (the cy buffer) and W*g are rewritten by the next path
   }
-  __syncwarp();
-  // gy[m2] += sum C[m1,m2,m3] G[m3][m1]; lane q holds m2 = q
-  if (q < p.D2) {
-    const int r0 = sgrow[p.grow + q], r1 = sgrow[p.grow + q + 1];
-    float v = 0.f;
-    for (int r = r0; r < r1; ++r) {
-      const float2 t = sgent[r];
-      v = fmaf(t.x, Gw[__float_as_int(t.y)], v);
-    }
-    gyw[p.off2 + q] += v;
-  }
-  __syncwarp();  // G (the cy buffer) is rewritten by the next path's coupling stage
-  if (p.flush) {
-    if (valid) {
-      float* dst = (p.gxp ? srow + p.gxo : a.gx + (size_t)b * a.d1 + p.gxo) + q * p.D1;
+  // gx of the run's in1 block: the first run on the block stores, later runs add (group order)
+  float* da = a.gx + (size_t)b0 * a.d1 + p0.off1 + u * p0.D1;
+  float* db = a.gx + (size_t)b1 * a.d1 + p0.off1 + u * p0.D1;
 #pragma unroll
-      for (int m = 0; m < D1P; ++m)
-        if (m < p.D1) dst[m] = (m & 1) ? gxa[m >> 1].y : gxa[m >> 1].x;
+  for (int m = 0; m < D1P; ++m) {
+    if (m < p0.D1) {
+      if (v0) da[m] = p0.gxfirst ? gxa[m].x : da[m] + gxa[m].x;
+      if (v1) db[m] = p0.gxfirst ? gxa[m].y : db[m] + gxa[m].y;
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) gxa[j] = make_float2(0.f, 0.f);
   }
 }
 
-template <int LPS>
+template <int LPP>
 __global__ void __launch_bounds__(kBtThreads, 2) bt_backward_kernel(const BtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int SPW = 32 / LPS;
-  const BtGroup grp = a.groups[blockIdx.y];
-  const int np = grp.p1 - grp.p0;
-  BtPath* sp = reinterpret_cast<BtPath*>(smem);
-  float2* sc = reinterpret_cast<float2*>(smem + (size_t)np * sizeof(BtPath));
-  uint16_t* scol = reinterpret_cast<uint16_t*>(sc + grp.ctab_n);
-  const size_t o_grow = al16((size_t)np * sizeof(BtPath) + (size_t)grp.ctab_n * 10);
-  int* sgrow = reinterpret_cast<int*>(smem + o_grow);
-  const size_t o_gent = al16(o_grow + (size_t)grp.grow_n * 4);
-  float2* sgent = reinterpret_cast<float2*>(smem + o_gent);
-  float* wbuf = reinterpret_cast<float*>(smem + al16(o_gent + (size_t)grp.gent_n * 8));
-  const int tid = threadIdx.x;
-  for (int i = tid; i < np * 16; i += kBtThreads)
-    reinterpret_cast<int*>(sp)[i] = reinterpret_cast<const int*>(a.paths + grp.p0)[i];
-  for (int i = tid; i < grp.ctab_n; i += kBtThreads) {
-    sc[i] = a.ccoef[grp.ctab0 + i];
-    scol[i] = a.ccol[grp.ctab0 + i];
-  }
-  for (int i = tid; i < grp.grow_n; i += kBtThreads) sgrow[i] = a.grow[grp.grow0 + i];
-  for (int i = tid; i < grp.gent_n; i += kBtThreads) sgent[i] = a.gent[grp.gent0 + i];
-  __syncthreads();
-  const int lane = tid & 31, warp = tid >> 5, q = lane % LPS, s = lane / LPS;
-  float* wb = wbuf + (size_t)warp * a.warp_floats;
-  float* ysw = wb + s * a.d2p;
-  float* gyw = wb + SPW * a.d2p + s * a.d2p;
-  float* cyw = wb + 2 * SPW * a.d2p + s * kCyW;
-  float* wgw = wb + 2 * SPW * a.d2p + SPW * kCyW + s * (kMaxD * LPS);
-  const int nS = a.b1 - a.b0;
-  const int sb = a.b0 + (int)((long long)nS * blockIdx.x / a.slices);
-  const int se = a.b0 + (int)((long long)nS * (blockIdx.x + 1) / a.slices);
-  for (int base = sb + warp * SPW; base < se; base += kBtWarps * SPW) {
-    const int bs = base + s;
-    const bool valid = bs < se;
-    const int b = valid ? bs : base;
-    float* srow = a.scratch + (size_t)(b - a.b0) * a.scratch_row;
-    for (int i = q; i < a.d2; i += LPS) {
-      ysw[i] = valid ? __ldg(a.y + (size_t)b * a.d2 + i) : 0.f;
-      gyw[i] = 0.f;
+  constexpr int PPW = 32 / LPP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, pr = lane / LPP, u = lane % LPP;
+  float* wb = reinterpret_cast<float*>(smem + a.table_bytes) + (size_t)warp * a.warp_floats;
+  float2* y2 = reinterpret_cast<float2*>(wb) + pr * a.y2s;
+  float2* gy2 = reinterpret_cast<float2*>(wb) + PPW * a.y2s + pr * a.y2s;
+  float2* cy2 = reinterpret_cast<float2*>(wb) + 2 * PPW * a.y2s + pr * kCyPair;
+  float2* wg2 = reinterpret_cast<float2*>(wb) + 2 * PPW * a.y2s + PPW * kCyPair + pr * a.wgs;
+  __shared__ int s_unit;
+  // persistent CTAs take batches of a.unit samples from a counter
+  for (;;) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
+    __syncthreads();
+    const int unit = s_unit;
+    if (unit >= a.n_units) break;
+    const int base = unit * a.unit;
+    const int s0 = base + warp * 2 * PPW + 2 * pr, s1 = s0 + 1;
+    const bool v0 = s0 < a.B, v1 = s1 < a.B;
+    const int b0 = v0 ? s0 : base, b1 = v1 ? s1 : base;
+    for (int i = u; i < a.d2; i += LPP) {
+      y2[i] = ld_pair(a.y + (size_t)b0 * a.d2 + i, a.y + (size_t)b1 * a.d2 + i, v0, v1);
+      gy2[i] = make_float2(0.f, 0.f);
     }
-    __syncwarp();
-    float2 gxa[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) gxa[j] = make_float2(0.f, 0.f);
-    for (int pi = 0; pi < np; ++pi) {
-      const BtPath p = sp[pi];
-      switch (p.Q) {
-        case 1: bwd_path<LPS, 1>(p, a, sc, scol, sgrow, sgent, ysw, cyw, wgw, gyw, gxa, b, valid, q, srow); break;
-        case 2: bwd_path<LPS, 2>(p, a, sc, scol, sgrow, sgent, ysw, cyw, wgw, gyw, gxa, b, valid, q, srow); break;
-        case 3: bwd_path<LPS, 3>(p, a, sc, scol, sgrow, sgent, ysw, cyw, wgw, gyw, gxa, b, valid, q, srow); break;
-        default: bwd_path<LPS, 4>(p, a, sc, scol, sgrow, sgent, ysw, cyw, wgw, gyw, gxa, b, valid, q, srow); break;
+    for (int z = 0; z < a.n_zero; ++z) {
+      const int off = a.zero_blk[2 * z], size = a.zero_blk[2 * z + 1];
+      for (int i = u; i < size; i += LPP) {
+        if (v0) a.gx[(size_t)b0 * a.d1 + off + i] = 0.f;
+        if (v1) a.gx[(size_t)b1 * a.d1 + off + i] = 0.f;
       }
     }
     __syncwarp();
-    if (valid)
-      for (int i = q; i < a.d2; i += LPS) srow[grp.gy_part + i] = gyw[i];
-    __syncwarp();
-  }
-}
-
-// gy = sum of the groups' partials; gx blocks shared by several groups = sum of
-// their partials (in group order); blocks no path touches are zero.
-struct BtReduceArgs {
-  const float* scratch;
-  float* gx;
-  float* gy;
-  int scratch_row, d1, d2, G, n_in1;
-  const int* blk;       // per in1 block: off1, size, parts, first part
-  const int* part_off;  // scratch-row offsets of the parts
-  int b0, n;
-};
-
-__global__ void __launch_bounds__(256) bt_reduce_kernel(const BtReduceArgs r) {
-  for (int i = blockIdx.x; i < r.n; i += gridDim.x) {
-    const float* row = r.scratch + (size_t)i * r.scratch_row;
-    const size_t b = (size_t)(r.b0 + i);
-    for (int m = threadIdx.x; m < r.d2; m += blockDim.x) {
-      float v = 0.f;
-      for (int g = 0; g < r.G; ++g) v += row[g * r.d2 + m];
-      r.gy[b * r.d2 + m] = v;
-    }
-    for (int k = 0; k < r.n_in1; ++k) {
-      const int off1 = __ldg(r.blk + 4 * k), size = __ldg(r.blk + 4 * k + 1);
-      const int np = __ldg(r.blk + 4 * k + 2), p0 = __ldg(r.blk + 4 * k + 3);
-      if (np == 1) continue;
-      for (int j = threadIdx.x; j < size; j += blockDim.x) {
-        float v = 0.f;
-        for (int t = 0; t < np; ++t) v += row[__ldg(r.part_off + p0 + t) + j];
-        r.gx[b * r.d1 + off1 + j] = v;
+    for (int gi = 0; gi < a.G; ++gi) {
+      const BtGroup grp = a.groups[gi];
+      __syncthreads();  // every warp is done with the previous group's tables
+      load_tables(a, grp, smem, true);
+      __syncthreads();
+      const int np = grp.p1 - grp.p0;
+      const BtPath* sp = reinterpret_cast<const BtPath*>(smem);
+      const float4* sc = reinterpret_cast<const float4*>(smem + (size_t)np * sizeof(BtPath));
+      const size_t o_grow = (size_t)np * sizeof(BtPath) + (size_t)grp.ctab_n * 16;
+      const int* sgrow = reinterpret_cast<const int*>(smem + o_grow);
+      const float2* sgent = reinterpret_cast<const float2*>(smem + al16(o_grow + (size_t)grp.grow_n * 4));
+      for (int pi = 0; pi < np;) {
+        const int n = sp[pi].run;
+        switch (sp[pi].Q) {
+          case 1: bwd_run<LPP, 1>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          case 2: bwd_run<LPP, 2>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          case 3: bwd_run<LPP, 3>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          default: bwd_run<LPP, 4>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+        }
+        pi += n;
       }
     }
+    __syncwarp();
+    for (int i = u; i < a.d2; i += LPP) {
+      if (v0) a.gy[(size_t)b0 * a.d2 + i] = gy2[i].x;
+      if (v1) a.gy[(size_t)b1 * a.d2 + i] = gy2[i].y;
+    }
+    __syncwarp();
   }
 }
 
 struct BtState {
-  int lps = 0;
+  int lpp = 0;
   int G = 0;
-  int d2p = 0;
-  int scratch_row = 0;
-  int chunk = 0;
+  int y2s = 0, tile = 0, wgs = 0;
   int wf_fwd = 0, wf_bwd = 0;
+  int table_bytes = 0;      // largest group's full tables (backward)
   size_t smem_fwd = 0, smem_bwd = 0;
-  int slices_fwd = 1, slices_bwd = 1;
-  int n_in1 = 0;
+  int grid_fwd = 1, grid_bwd = 1;
+  int n_zero = 0;
   void* tables = nullptr;
-  float* scratch = nullptr;
+  int* counter = nullptr;   // [0] forward, [1] backward work-unit counters
   const BtPath* paths = nullptr;
   const BtGroup* groups = nullptr;
-  const float2* ccoef = nullptr;
-  const uint16_t* ccol = nullptr;
+  const float4* ctab = nullptr;
   const int* grow = nullptr;
   const float2* gent = nullptr;
-  const int* blk = nullptr;
-  const int* part_off = nullptr;
+  const int* zero_blk = nullptr;
 };
 
 }  // namespace bt_detail
@@ -424,17 +485,22 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
   const int m = plan->paths.front().mul1;
   if (m != 16 && m != 32) return CGTP_OK;
   for (const auto& p : plan->paths)
-    if (p.mul1 != m || p.l1 > 7 || p.l2 > 7 || p.l3 > 7 || p.ooff % 4 || p.woff % 4) return CGTP_OK;
+    if (p.mul1 != m || p.l1 > 7 || p.l2 > 7 || p.l3 > 7 || p.ooff % 4) return CGTP_OK;
   if (plan->d_out % 4) return CGTP_OK;
   const int P = static_cast<int>(plan->paths.size());
   const int d2 = static_cast<int>(plan->d2);
+  if (d2 > 4096) return CGTP_OK;
   // per-path tables
   std::vector<BtPath> bp(P);
-  std::vector<std::vector<float2>> pc(P);
-  std::vector<std::vector<uint16_t>> pcol(P);
+  std::vector<std::vector<float4>> pc(P);
   std::vector<std::vector<int>> prow(P);
   std::vector<std::vector<float2>> pent(P);
   std::vector<size_t> bytes(P);
+  auto as_float = [](int v) {
+    float f;
+    std::memcpy(&f, &v, 4);
+    return f;
+  };
   for (int i = 0; i < P; ++i) {
     const PathHost& h = plan->paths[i];
     const int D1 = 2 * h.l1 + 1, D2 = 2 * h.l2 + 1, D3 = 2 * h.l3 + 1;
@@ -444,8 +510,8 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
     std::memset(&b, 0, sizeof(b));
     b.D1 = D1; b.D2 = D2; b.D3 = D3; b.Q = Q;
     b.off1 = h.off1; b.off2 = h.off2; b.ooff = h.ooff; b.woff = h.woff;
-    pc[i].assign(size_t(D3) * D1P, make_float2(0.f, 0.f));
-    pcol[i].assign(size_t(D3) * D1P, 0);
+    const float zoff = as_float(h.off2 * 8);
+    pc[i].assign(size_t(D3) * D1P, make_float4(0.f, 0.f, zoff, zoff));
     for (int m3 = 0; m3 < D3; ++m3)
       for (int m1 = 0; m1 < D1; ++m1) {
         int k = 0;
@@ -459,8 +525,8 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
           cl[k] = m2;
           ++k;
         }
-        pc[i][size_t(m3) * D1P + m1] = make_float2(co[0], co[1]);
-        pcol[i][size_t(m3) * D1P + m1] = static_cast<uint16_t>(cl[0] | (cl[1] << 8));
+        pc[i][size_t(m3) * D1P + m1] =
+            make_float4(co[0], co[1], as_float((h.off2 + cl[0]) * 8), as_float((h.off2 + cl[1]) * 8));
       }
     prow[i].push_back(0);
     for (int m2 = 0; m2 < D2; ++m2) {
@@ -468,17 +534,13 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
         for (int m1 = 0; m1 < D1; ++m1) {
           const double c = C(m1, m2, m3);
           if (std::fabs(c) < 1e-15) continue;
-          int slot = m3 * kGStride + m1;
-          float sf;
-          std::memcpy(&sf, &slot, 4);
-          pent[i].push_back(make_float2(static_cast<float>(c), sf));
+          pent[i].push_back(make_float2(static_cast<float>(c), as_float((m3 * kGStride + m1) * 8)));
         }
       prow[i].push_back(static_cast<int>(pent[i].size()));
     }
-    bytes[i] = sizeof(BtPath) + pc[i].size() * 10 + prow[i].size() * 4 + pent[i].size() * 8;
+    bytes[i] = sizeof(BtPath) + pc[i].size() * 16 + prow[i].size() * 4 + pent[i].size() * 8 + 16;
   }
-  // contiguous path groups within the table budget; an in1 block's paths must
-  // be contiguous inside a group (one gx flush per block and group)
+  // contiguous path groups within the table budget
   std::vector<BtGroup> groups;
   {
     int p0 = 0;
@@ -486,7 +548,8 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
     for (int i = 0; i < P; ++i) {
       if (i > p0 && acc + bytes[i] > kTableBudget) {
         BtGroup g{};
-        g.p0 = p0; g.p1 = i;
+        g.p0 = p0;
+        g.p1 = i;
         groups.push_back(g);
         p0 = i;
         acc = 0;
@@ -494,97 +557,76 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
       acc += bytes[i];
     }
     BtGroup g{};
-    g.p0 = p0; g.p1 = P;
+    g.p0 = p0;
+    g.p1 = P;
     groups.push_back(g);
   }
   const int G = static_cast<int>(groups.size());
   const int n_in1 = static_cast<int>(plan->in1.size());
-  std::vector<std::vector<int>> touch(n_in1);  // groups touching each in1 block, in order
-  for (int g = 0; g < G; ++g) {
-    std::vector<int> seen;
-    int last = -1;
-    for (int i = groups[g].p0; i < groups[g].p1; ++i) {
-      const int i1 = plan->paths[i].i1;
-      if (i1 != last) {
-        if (std::find(seen.begin(), seen.end(), i1) != seen.end()) return CGTP_OK;  // non-contiguous
-        seen.push_back(i1);
-        touch[i1].push_back(g);
-        last = i1;
-      }
-    }
-  }
-  // scratch row: G gy partials, then the partial gx blocks
   std::vector<int> in1_off(n_in1 + 1, 0);
   for (int k = 0; k < n_in1; ++k) in1_off[k + 1] = in1_off[k] + plan->in1[k].mul * (2 * plan->in1[k].l + 1);
-  int row = G * d2;
-  std::vector<int> blk(4 * n_in1), part_off;
-  std::vector<std::vector<int>> part_of(n_in1);  // per block, per touching group: scratch offset
-  for (int k = 0; k < n_in1; ++k) {
-    const int size = in1_off[k + 1] - in1_off[k];
-    blk[4 * k] = in1_off[k];
-    blk[4 * k + 1] = size;
-    blk[4 * k + 2] = static_cast<int>(touch[k].size());
-    blk[4 * k + 3] = static_cast<int>(part_off.size());
-    if (touch[k].size() >= 2)
-      for (size_t t = 0; t < touch[k].size(); ++t) {
-        part_of[k].push_back(row);
-        part_off.push_back(row);
-        row += size;
-      }
-  }
-  row = (row + 3) / 4 * 4;
-  // finish the path records and the group tables
-  std::vector<float2> ccoef, gent;
-  std::vector<uint16_t> ccol;
+  std::vector<char> touched(n_in1, 0);
+  std::vector<float4> ctab;
+  std::vector<float2> gent;
   std::vector<int> growv;
   for (int g = 0; g < G; ++g) {
     BtGroup& gr = groups[g];
-    gr.ctab0 = static_cast<int>(ccoef.size());
+    gr.ctab0 = static_cast<int>(ctab.size());
     gr.grow0 = static_cast<int>(growv.size());
     gr.gent0 = static_cast<int>(gent.size());
-    gr.gy_part = g * d2;
+    int run_start = gr.p0;
     for (int i = gr.p0; i < gr.p1; ++i) {
       BtPath& b = bp[i];
       const int i1 = plan->paths[i].i1;
-      b.ctab = static_cast<int>(ccoef.size()) - gr.ctab0;
+      b.ctab = static_cast<int>(ctab.size()) - gr.ctab0;
       b.grow = static_cast<int>(growv.size()) - gr.grow0;
       const int ent_base = static_cast<int>(gent.size()) - gr.gent0;
-      ccoef.insert(ccoef.end(), pc[i].begin(), pc[i].end());
-      ccol.insert(ccol.end(), pcol[i].begin(), pcol[i].end());
+      ctab.insert(ctab.end(), pc[i].begin(), pc[i].end());
       for (int r : prow[i]) growv.push_back(ent_base + r);
       gent.insert(gent.end(), pent[i].begin(), pent[i].end());
-      b.flush = (i + 1 == gr.p1 || plan->paths[i + 1].i1 != i1) ? 1 : 0;
-      if (touch[i1].size() >= 2) {
-        const size_t t = std::find(touch[i1].begin(), touch[i1].end(), g) - touch[i1].begin();
-        b.gxp = 1;
-        b.gxo = part_of[i1][t];
-      } else {
-        b.gxp = 0;
-        b.gxo = in1_off[i1];
+      if (i == gr.p0 || plan->paths[i - 1].i1 != i1) {
+        run_start = i;
+        b.gxfirst = touched[i1] ? 0 : 1;
+        touched[i1] = 1;
       }
+      bp[run_start].run = i - run_start + 1;
     }
-    gr.ctab_n = static_cast<int>(ccoef.size()) - gr.ctab0;
+    gr.ctab_n = static_cast<int>(ctab.size()) - gr.ctab0;
     gr.grow_n = static_cast<int>(growv.size()) - gr.grow0;
     gr.gent_n = static_cast<int>(gent.size()) - gr.gent0;
   }
+  std::vector<int> zero_blk;
+  for (int k = 0; k < n_in1; ++k)
+    if (!touched[k] && in1_off[k + 1] > in1_off[k]) {
+      zero_blk.push_back(in1_off[k]);
+      zero_blk.push_back(in1_off[k + 1] - in1_off[k]);
+    }
   BtState* st = new BtState();
-  st->lps = m;
+  st->lpp = m;
   st->G = G;
-  st->n_in1 = n_in1;
-  st->d2p = (d2 + 3) / 4 * 4;
-  st->scratch_row = row;
-  const int spw = 32 / m;
-  st->wf_fwd = (spw * (st->d2p + kCyW + m * kMaxD) + 3) / 4 * 4;
-  st->wf_bwd = (spw * (2 * st->d2p + kCyW + m * kMaxD) + 3) / 4 * 4;
+  st->n_zero = static_cast<int>(zero_blk.size() / 2);
+  const int ppw = 32 / m;
+  auto eight_mod16 = [](int v) {  // smallest value >= v that is 8 (mod 16)
+    int r = (v + 15) / 16 * 16 - 8;
+    return r < v ? r + 16 : r;
+  };
+  st->y2s = eight_mod16(d2);                 // pairs' y rows 16 banks apart
+  st->tile = eight_mod16(m * kMaxD);         // sample tiles of a pair 16 banks apart
+  st->wgs = m * kMaxD + 8;
+  st->wf_fwd = 2 * (ppw * st->y2s + ppw * kCyPair) + 2 * ppw * st->tile;
+  st->wf_bwd = 2 * (2 * ppw * st->y2s + ppw * kCyPair + ppw * st->wgs);
+  size_t tb_max = 0;
   for (const BtGroup& g : groups) {
     const size_t np = g.p1 - g.p0;
-    const size_t t_fwd = al16(np * sizeof(BtPath) + size_t(g.ctab_n) * 10);
-    const size_t t_grow = al16(t_fwd + size_t(g.grow_n) * 4);
-    const size_t t_bwd = al16(t_grow + size_t(g.gent_n) * 8);
+    const size_t t_fwd = al16(np * sizeof(BtPath) + size_t(g.ctab_n) * 16);
+    const size_t t_grow = np * sizeof(BtPath) + size_t(g.ctab_n) * 16;
+    const size_t t_bwd = al16(al16(t_grow + size_t(g.grow_n) * 4) + size_t(g.gent_n) * 8);
     st->smem_fwd = std::max(st->smem_fwd, t_fwd + size_t(kBtWarps) * st->wf_fwd * 4);
-    st->smem_bwd = std::max(st->smem_bwd, t_bwd + size_t(kBtWarps) * st->wf_bwd * 4);
+    tb_max = std::max(tb_max, t_bwd);
   }
-  if (st->smem_fwd > 200 * 1024 || st->smem_bwd > 200 * 1024) {
+  st->table_bytes = static_cast<int>(tb_max);
+  st->smem_bwd = tb_max + size_t(kBtWarps) * st->wf_bwd * 4;
+  if (st->smem_fwd > 220 * 1024 || st->smem_bwd > 220 * 1024) {
     delete st;
     return CGTP_OK;
   }
@@ -598,12 +640,10 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
   };
   const size_t o_p = put(bp.data(), bp.size() * sizeof(BtPath));
   const size_t o_g = put(groups.data(), groups.size() * sizeof(BtGroup));
-  const size_t o_cc = put(ccoef.data(), ccoef.size() * sizeof(float2));
-  const size_t o_cl = put(ccol.data(), ccol.size() * sizeof(uint16_t));
-  const size_t o_gr = put(growv.data(), growv.size() * sizeof(int));
-  const size_t o_ge = put(gent.data(), gent.size() * sizeof(float2));
-  const size_t o_bk = put(blk.data(), blk.size() * sizeof(int));
-  const size_t o_po = put(part_off.data(), part_off.size() * sizeof(int));
+  const size_t o_c = put(ctab.data(), ctab.size() * sizeof(float4));
+  const size_t o_r = put(growv.data(), growv.size() * sizeof(int));
+  const size_t o_e = put(gent.data(), gent.size() * sizeof(float2));
+  const size_t o_z = put(zero_blk.data(), zero_blk.size() * sizeof(int));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) {
     delete st;
     return fail(CGTP_ENOMEM, "batched-product table allocation failed");
@@ -613,37 +653,31 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
     delete st;
     return fail(CGTP_ECUDA, "batched-product table upload failed");
   }
+  if (cudaMalloc(&st->counter, 2 * sizeof(int)) != cudaSuccess) {
+    cudaFree(st->tables);
+    delete st;
+    return fail(CGTP_ENOMEM, "batched-product counter allocation failed");
+  }
   auto at = [&](size_t off) { return static_cast<unsigned char*>(st->tables) + off; };
   st->paths = reinterpret_cast<const BtPath*>(at(o_p));
   st->groups = reinterpret_cast<const BtGroup*>(at(o_g));
-  st->ccoef = reinterpret_cast<const float2*>(at(o_cc));
-  st->ccol = reinterpret_cast<const uint16_t*>(at(o_cl));
-  st->grow = reinterpret_cast<const int*>(at(o_gr));
-  st->gent = reinterpret_cast<const float2*>(at(o_ge));
-  st->blk = reinterpret_cast<const int*>(at(o_bk));
-  st->part_off = reinterpret_cast<const int*>(at(o_po));
-  // backward partials: a bounded chunk of samples at a time
-  st->chunk = static_cast<int>(std::min<size_t>(16384, std::max<size_t>(256, kScratchBytes / (size_t(row) * 4))));
-  if (cudaMalloc(&st->scratch, size_t(st->chunk) * row * 4) != cudaSuccess) {
-    cudaFree(st->tables);
-    delete st;
-    return fail(CGTP_ENOMEM, "batched-product scratch allocation failed");
-  }
-  // kernel attributes and occupancy -> slices per group
-  auto setup = [&](const void* k, size_t smem, int* slices) {
+  st->ctab = reinterpret_cast<const float4*>(at(o_c));
+  st->grow = reinterpret_cast<const int*>(at(o_r));
+  st->gent = reinterpret_cast<const float2*>(at(o_e));
+  st->zero_blk = reinterpret_cast<const int*>(at(o_z));
+  // kernel attributes and occupancy -> grid sizes
+  auto occupancy = [&](const void* k, size_t smem) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBtThreads, smem);
-    per_sm = std::max(per_sm, 1);
-    *slices = std::max(1, (plan->num_sms * per_sm + G - 1) / G);
+    return std::max(per_sm, 1);
   };
-  if (m == 16) {
-    setup(reinterpret_cast<const void*>(bt_forward_kernel<16>), st->smem_fwd, &st->slices_fwd);
-    setup(reinterpret_cast<const void*>(bt_backward_kernel<16>), st->smem_bwd, &st->slices_bwd);
-  } else {
-    setup(reinterpret_cast<const void*>(bt_forward_kernel<32>), st->smem_fwd, &st->slices_fwd);
-    setup(reinterpret_cast<const void*>(bt_backward_kernel<32>), st->smem_bwd, &st->slices_bwd);
-  }
+  const void* kf = m == 16 ? reinterpret_cast<const void*>(bt_forward_kernel<16>)
+                           : reinterpret_cast<const void*>(bt_forward_kernel<32>);
+  const void* kb = m == 16 ? reinterpret_cast<const void*>(bt_backward_kernel<16>)
+                           : reinterpret_cast<const void*>(bt_backward_kernel<32>);
+  st->grid_fwd = plan->num_sms * occupancy(kf, st->smem_fwd);
+  st->grid_bwd = plan->num_sms * occupancy(kb, st->smem_bwd);
   cudaGetLastError();
   plan->bt = st;
   return CGTP_OK;
@@ -653,26 +687,31 @@ void bt_destroy(cgtp_plan_s* plan) {
   BtState* st = static_cast<BtState*>(plan->bt);
   if (!st) return;
   if (st->tables) cudaFree(st->tables);
-  if (st->scratch) cudaFree(st->scratch);
+  if (st->counter) cudaFree(st->counter);
   delete st;
   plan->bt = nullptr;
 }
 
-static BtArgs bt_args(const cgtp_plan_s* plan, const BtState* st) {
+static BtArgs bt_args(const cgtp_plan_s* plan, const BtState* st, int64_t B) {
   BtArgs a{};
+  a.B = static_cast<int>(B);
   a.d1 = static_cast<int>(plan->d1);
   a.d2 = static_cast<int>(plan->d2);
-  a.d2p = st->d2p;
   a.d_out = static_cast<int>(plan->d_out);
   a.w_numel = static_cast<int>(plan->w_numel);
-  a.scratch_row = st->scratch_row;
+  a.G = st->G;
+  a.unit = kBtWarps * 64 / st->lpp;
+  a.y2s = st->y2s;
+  a.tile = st->tile;
+  a.wgs = st->wgs;
+  a.table_bytes = st->table_bytes;
+  a.n_zero = st->n_zero;
+  a.zero_blk = st->zero_blk;
   a.paths = st->paths;
   a.groups = st->groups;
-  a.ccoef = st->ccoef;
-  a.ccol = st->ccol;
+  a.ctab = st->ctab;
   a.grow = st->grow;
   a.gent = st->gent;
-  a.scratch = st->scratch;
   return a;
 }
 
@@ -681,17 +720,21 @@ bool bt_forward(const cgtp_plan_s* plan, const void* x1, const void* x2, const v
   const BtState* st = static_cast<const BtState*>(plan->bt);
   if (!st) return false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  BtArgs a = bt_args(plan, st);
+  BtArgs a = bt_args(plan, st, B);
   a.x = static_cast<const float*>(x1);
   a.y = static_cast<const float*>(x2);
   a.W = static_cast<const float*>(W);
   a.out = static_cast<float*>(out);
-  a.b0 = 0;
-  a.b1 = static_cast<int>(B);
-  a.slices = st->slices_fwd;
   a.warp_floats = st->wf_fwd;
-  const dim3 grid(st->slices_fwd, st->G);
-  if (st->lps == 16)
+  a.chunks = static_cast<int>((B + a.unit - 1) / a.unit);
+  a.n_units = a.G * a.chunks;
+  a.counter = st->counter;
+  if (cudaMemsetAsync(st->counter, 0, sizeof(int), s) != cudaSuccess) {
+    *status = fail(CGTP_ECUDA, "batched forward: counter reset failed");
+    return true;
+  }
+  const int grid = std::max(1, std::min(st->grid_fwd, a.n_units));
+  if (st->lpp == 16)
     bt_forward_kernel<16><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
   else
     bt_forward_kernel<32><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
@@ -706,45 +749,29 @@ bool bt_backward(const cgtp_plan_s* plan, const void* gout, const void* x1, cons
   const BtState* st = static_cast<const BtState*>(plan->bt);
   if (!st) return false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  BtArgs a = bt_args(plan, st);
+  BtArgs a = bt_args(plan, st, B);
   a.x = static_cast<const float*>(x1);
   a.y = static_cast<const float*>(x2);
   a.W = static_cast<const float*>(W);
   a.gout = static_cast<const float*>(gout);
   a.gx = static_cast<float*>(gx1);
+  a.gy = static_cast<float*>(gx2);
   a.gW = static_cast<float*>(gW);
-  a.slices = st->slices_bwd;
   a.warp_floats = st->wf_bwd;
-  BtReduceArgs r{};
-  r.scratch = st->scratch;
-  r.gx = static_cast<float*>(gx1);
-  r.gy = static_cast<float*>(gx2);
-  r.scratch_row = st->scratch_row;
-  r.d1 = a.d1;
-  r.d2 = a.d2;
-  r.G = st->G;
-  r.n_in1 = st->n_in1;
-  r.blk = st->blk;
-  r.part_off = st->part_off;
-  const dim3 grid(st->slices_bwd, st->G);
-  for (int64_t c0 = 0; c0 < B; c0 += st->chunk) {
-    const int n = static_cast<int>(std::min<int64_t>(st->chunk, B - c0));
-    a.b0 = static_cast<int>(c0);
-    a.b1 = static_cast<int>(c0 + n);
-    if (st->lps == 16)
-      bt_backward_kernel<16><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
-    else
-      bt_backward_kernel<32><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
-    r.b0 = a.b0;
-    r.n = n;
-    bt_reduce_kernel<<<std::min(n, plan->num_sms * 8), 256, 0, s>>>(r);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-      *status = fail(CGTP_ECUDA, std::string("batched backward launch: ") + cudaGetErrorString(e));
-      return true;
-    }
+  a.n_units = static_cast<int>((B + a.unit - 1) / a.unit);
+  a.counter = st->counter + 1;
+  if (cudaMemsetAsync(st->counter + 1, 0, sizeof(int), s) != cudaSuccess) {
+    *status = fail(CGTP_ECUDA, "batched backward: counter reset failed");
+    return true;
   }
-  *status = CGTP_OK;
+  const int grid = std::max(1, std::min(st->grid_bwd, a.n_units));
+  if (st->lpp == 16)
+    bt_backward_kernel<16><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+  else
+    bt_backward_kernel<32><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  *status = e == cudaSuccess ? CGTP_OK
+                             : fail(CGTP_ECUDA, std::string("batched backward launch: ") + cudaGetErrorString(e));
   return true;
 }
 

@@ -29,6 +29,9 @@
  *    returns a message for the last failure of the calling thread.
  *  - Results are bitwise deterministic run to run (no atomics in any
  *    floating-point accumulation).
+ *  - A plan holds device state used by its launches (work counters of the
+ *    batched kernels, the uvw node-state scratch): calls that use the same
+ *    plan must not overlap on the GPU (issue them on one stream).
  */
 #ifndef CGTP_H
 #define CGTP_H
