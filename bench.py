@@ -442,7 +442,7 @@ def main():
              ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
              ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[(plan.mode, dominant)]
     if "N" not in w:
-        kname = "uvu batched " + dominant
+        kname = {"forward": "bt_forward_kernel", "backward": "bt_backward_kernel"}[dominant]
     if t_hbm >= t_alu:
         achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
