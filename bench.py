@@ -243,6 +243,47 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
     return units / dt, f"{N}-node graph of the same recipe ({w['E']} edges), fwd+bwd repeated for {dt:.1f} s"
 
 
+def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
+    """Second derivatives (cgtp_conv_double_backward / cgtp_double_backward) with random
+    cotangents, CUDA events on the launching stream, after warm-up.  It runs the
+    forward and backward kernels once per operand (3 + 3 for uvu, 4 + 4 for uvw),
+    so its roofline is that many forward and backward rooflines."""
+    import torch
+    import clebsch_gordan_tensor_racah_gb300 as cg
+    gen = torch.Generator(g.device).manual_seed(2)
+    if "rowptr" in dev:
+        keys = ["x", "Y", "W"] if plan.mode == "uvu" else ["x", "Y", "R", "M"]
+        c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen) for k in keys}
+        WR = dev["W"] if plan.mode == "uvu" else dev["R"]
+        cWR = c["W"] if plan.mode == "uvu" else c["R"]
+
+        def run():
+            return cg.cgtp_conv_double_backward(plan, graph, g, dev["x"], dev["Y"], WR, c["x"], c["Y"], cWR,
+                                                M=dev.get("M"), ggM=c.get("M"))
+        n_op = len(keys)
+    else:
+        c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen)
+             for k in ("x1", "x2", "W")}
+
+        def run():
+            return cg.cgtp_double_backward(plan, g, dev["x1"], dev["x2"], dev["W"], c["x1"], c["x2"], c["W"])
+        n_op = 3
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    a.record(stream)
+    for _ in range(reps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    roof = n_op * (roofline["fwd_roofline_ms"] + roofline["bwd_roofline_ms"])
+    return {"ms": ms, "units_per_s": units / (ms / 1000.0), "launch_sequence": f"{n_op} forwards + {n_op} backwards + adds",
+            "roofline_ms": roof, "frac": roof / ms}
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -304,6 +345,8 @@ def main():
     ap.add_argument("--config", default="nequip", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-double-backward", action="store_true",
+                    help="skip the (untimed-for-the-metric) second-derivative measurement")
     ap.add_argument("--nodes", type=int, default=None,
                     help="smaller instance of the same recipe (nodes, or batch for highl)")
     ap.add_argument("--profile-run", action="store_true",
@@ -467,6 +510,8 @@ def main():
             "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
             "clocks": clk}
+    if not args.no_double_backward:
+        line["double_backward"] = time_double_backward(plan, graph, w, dev, g, stream, units, roofline)
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc = time_oracle_sample(args.config)
         line["cpu_baseline"] = {"value": rate, "unit": line["unit"], "cores": 1, "kind": "oracle",

@@ -32,7 +32,9 @@ CGTP_F32, CGTP_F64 = 0, 1
 EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan_path",
            "cgtp_forward", "cgtp_backward", "cgtp_graph_create", "cgtp_graph_destroy",
            "cgtp_graph_transpose", "cgtp_conv_forward", "cgtp_conv_backward",
-           "cgtp_real_cg_block", "cgtp_last_error", "cgtp_graph_transpose_noalloc"]
+           "cgtp_real_cg_block", "cgtp_last_error", "cgtp_graph_transpose_noalloc",
+           "cgtp_conv_double_backward_workspace", "cgtp_conv_double_backward",
+           "cgtp_double_backward_workspace", "cgtp_double_backward"]
 
 
 class CgtpError(RuntimeError):
@@ -70,6 +72,10 @@ def lib():
         L.cgtp_conv_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.cgtp_real_cg_block.argtypes = [i32, i32, i32, ctypes.POINTER(ctypes.c_double), i64]
         L.cgtp_graph_transpose_noalloc.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
+        L.cgtp_conv_double_backward_workspace.argtypes = [vp, vp, ctypes.POINTER(i64)]
+        L.cgtp_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
+        L.cgtp_double_backward_workspace.argtypes = [vp, i64, ctypes.POINTER(i64)]
+        L.cgtp_double_backward.argtypes = [vp] * 12 + [i64, vp, i64, vp]
         for name in EXPORTS:
             if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
                 getattr(L, name).restype = i32
@@ -241,3 +247,45 @@ def cgtp_conv_backward(plan, graph, gout, x, Y, W_or_R, M=None, stream=None, out
                                     _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gW, "gW"), _ptr(gM, "gM"),
                                     _stream(stream)))
     return gx, gY, gW, gM
+
+
+def _workspace(nbytes, device):
+    torch = _torch()
+    # 256-byte aligned: torch's caching allocator hands out 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def cgtp_conv_double_backward(plan, graph, gout, x, Y, W_or_R, ggx, ggY, ggW_or_ggR, M=None, ggM=None,
+                              stream=None):
+    """Second derivatives: (d_gout, d_x, d_Y, d_W_or_dR, d_M) of
+    S = <ggx, gx> + <ggY, gY> + <ggW, gW> (+ <ggM, gM> for uvw)."""
+    torch = _torch()
+    nb = ctypes.c_int64()
+    _check(lib().cgtp_conv_double_backward_workspace(plan.handle, graph.handle, ctypes.byref(nb)))
+    ws = _workspace(nb.value, x.device)
+    d_g, d_x, d_Y, d_W = torch.empty_like(gout), torch.empty_like(x), torch.empty_like(Y), torch.empty_like(W_or_R)
+    d_M = torch.empty_like(M) if M is not None else None
+    dt = plan.dtype
+    _check(lib().cgtp_conv_double_backward(
+        plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(Y, "Y", dt),
+        _ptr(W_or_R, "W_or_R", dt), _ptr(M, "M", dt), _ptr(ggx, "ggx", dt), _ptr(ggY, "ggY", dt),
+        _ptr(ggW_or_ggR, "ggW_or_ggR", dt), _ptr(ggM, "ggM", dt), _ptr(d_g, "d_gout"), _ptr(d_x, "d_x"),
+        _ptr(d_Y, "d_Y"), _ptr(d_W, "d_W"), _ptr(d_M, "d_M"), _ptr(ws, "workspace"), nb.value, _stream(stream)))
+    return d_g, d_x, d_Y, d_W, d_M
+
+
+def cgtp_double_backward(plan, gout, x1, x2, W, gg1, gg2, ggW, stream=None):
+    """Second derivatives of the batched product: (d_gout, d_x1, d_x2, d_W)."""
+    torch = _torch()
+    B = x1.shape[0]
+    nb = ctypes.c_int64()
+    _check(lib().cgtp_double_backward_workspace(plan.handle, B, ctypes.byref(nb)))
+    ws = _workspace(nb.value, x1.device)
+    d_g, d_1, d_2, d_W = torch.empty_like(gout), torch.empty_like(x1), torch.empty_like(x2), torch.empty_like(W)
+    dt = plan.dtype
+    _check(lib().cgtp_double_backward(
+        plan.handle, _ptr(gout, "gout", dt), _ptr(x1, "x1", dt), _ptr(x2, "x2", dt), _ptr(W, "W", dt),
+        _ptr(gg1, "gg1", dt), _ptr(gg2, "gg2", dt), _ptr(ggW, "ggW", dt), _ptr(d_g, "d_gout"),
+        _ptr(d_1, "d_x1"), _ptr(d_2, "d_x2"), _ptr(d_W, "d_W"), B, _ptr(ws, "workspace"), nb.value,
+        _stream(stream)))
+    return d_g, d_1, d_2, d_W

@@ -178,6 +178,41 @@ cgtp_status cgtp_conv_backward(cgtp_plan plan, cgtp_graph graph, const void* gou
                                const void* Y, const void* W_or_R, const void* M, void* gx, void* gY,
                                void* gW_or_gR, void* gM, void* stream);
 
+/*
+ * cgtp_conv_double_backward -- second derivatives for force training
+ * ("An Efficient Sparse Kernel Generator ...", Abstract: higher partial
+ * derivatives from the gradient kernels through an identity; "Sobek ...",
+ * Abstract: double backward).  Given cotangents of the backward's outputs,
+ *   S = <ggx, gx> + <ggY, gY> + <ggW, gW>   (uvw: + <ggR, gR> + <ggM, gM>),
+ * it returns dS/dgout, dS/dx, dS/dY, dS/dW (uvw: dS/dR, dS/dM).  The message is
+ * multilinear in its operands, so dS/dgout is the sum of the forwards with one
+ * operand replaced by its cotangent, and dS/da_j the sum of the backwards with
+ * one other operand replaced (3 forwards + 3 backwards for uvu, 4 + 4 for uvw).
+ *  gout [N,d_out], x, Y, W_or_R, M : as for cgtp_conv_backward (M = NULL for uvu).
+ *  ggx [N,d1], ggY [E,d2], ggW_or_ggR [E,w_numel] or [E,K], ggM [K,w_numel] (uvw).
+ *  d_gout [N,d_out], d_x [N,d1], d_Y [E,d2], d_W_or_dR, d_M : outputs (overwritten).
+ *  workspace : caller-owned DEVICE buffer, 256-byte aligned, of at least the
+ *      size cgtp_conv_double_backward_workspace reports (N*d_out plus one
+ *      copy of every operand, in elements); nothing is allocated inside.
+ *  Errors: CGTP_EINVAL for a missing or small workspace or a null operand;
+ *  otherwise as cgtp_conv_forward / cgtp_conv_backward.
+ */
+cgtp_status cgtp_conv_double_backward_workspace(cgtp_plan plan, cgtp_graph graph, int64_t* bytes);
+cgtp_status cgtp_conv_double_backward(cgtp_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                                      const void* Y, const void* W_or_R, const void* M, const void* ggx,
+                                      const void* ggY, const void* ggW_or_ggR, const void* ggM,
+                                      void* d_gout, void* d_x, void* d_Y, void* d_W_or_dR, void* d_M,
+                                      void* workspace, int64_t workspace_size, void* stream);
+
+/* Double backward of the batched product (uvu plans): cotangents gg1 [B,d1],
+ * gg2 [B,d2], ggW [B,w_numel] of cgtp_backward's outputs -> d_gout [B,d_out],
+ * d_x1, d_x2, d_W.  Workspace as above, from cgtp_double_backward_workspace. */
+cgtp_status cgtp_double_backward_workspace(cgtp_plan plan, int64_t B, int64_t* bytes);
+cgtp_status cgtp_double_backward(cgtp_plan plan, const void* gout, const void* x1, const void* x2,
+                                 const void* W, const void* gg1, const void* gg2, const void* ggW,
+                                 void* d_gout, void* d_x1, void* d_x2, void* d_W, int64_t B,
+                                 void* workspace, int64_t workspace_size, void* stream);
+
 /* Host only (no device needed): the planner's real-basis, component-normalised
  * CG block of (l1, l2, l3), l <= 7, as (2l1+1)(2l2+1)(2l3+1) doubles in
  * [m1][m2][m3] order; zeros if the triangle rule fails.  Same routine the plan

@@ -258,3 +258,58 @@ def conv_uvw_radial_gM_entries(plan, g, x, Y, R, rowptr, col, entries):
         gw = g[:, p.ooff + w * D3:p.ooff + (w + 1) * D3][dst]
         out.append(float((R[:, k] * (_f64(gw) * t).sum(1)).sum()))
     return np.array(out)
+
+
+# ---------------------------------------------------------------------------
+# second derivatives ("double backward")
+# ---------------------------------------------------------------------------
+# "An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks",
+# Abstract: higher partial derivatives for force prediction, obtained from the
+# forward and gradient operations through an identity.  With the backward
+# (dL/da_j)_j = B_j(g; a) of a message that is linear in each operand a_j, and
+# cotangents c_j of those gradients, the scalar
+#     S = sum_j <c_j, B_j(g; a)> = <g, sum_i F(a with a_i replaced by c_i)>
+# has the derivatives
+#     dS/dg   = sum_i F(a with a_i -> c_i)
+#     dS/da_j = sum_{i != j} B_j(g; a with a_i -> c_i)
+# since B_j does not depend on a_j.  The tests pin these against exact
+# directional differences of S computed with the backward alone.
+
+def _double_backward(fwd, bwd, g, a, c):
+    n = len(a)
+    d_g = None
+    d = [None] * n
+    for i in range(n):
+        ai = list(a)
+        ai[i] = c[i]
+        f = fwd(*ai)
+        d_g = f if d_g is None else d_g + f
+        grads = bwd(g, *ai)
+        for j in range(n):
+            if j != i:
+                d[j] = grads[j] if d[j] is None else d[j] + grads[j]
+    return (d_g, *d)
+
+
+def conv_uvu_double_backward(plan, g, x, Y, W, ggx, ggY, ggW, rowptr, col):
+    """(d_g [N,d_out], d_x [N,d1], d_Y [E,d2], d_W [E,w_numel]) for the uvu convolution."""
+    fwd = lambda x_, Y_, W_: conv_uvu_forward(plan, x_, Y_, W_, rowptr, col)
+    bwd = lambda g_, x_, Y_, W_: conv_uvu_backward(plan, g_, x_, Y_, W_, rowptr, col)
+    return _double_backward(fwd, bwd, _f64(g), [_f64(x), _f64(Y), _f64(W)],
+                            [_f64(ggx), _f64(ggY), _f64(ggW)])
+
+
+def conv_uvw_radial_double_backward(plan, g, x, Y, R, M, ggx, ggY, ggR, ggM, rowptr, col):
+    """(d_g, d_x, d_Y, d_R, d_M) for the uvw convolution with radial weights W = R M."""
+    fwd = lambda x_, Y_, R_, M_: conv_uvw_radial_forward(plan, x_, Y_, R_, M_, rowptr, col)
+    bwd = lambda g_, x_, Y_, R_, M_: conv_uvw_radial_backward(plan, g_, x_, Y_, R_, M_, rowptr, col)
+    return _double_backward(fwd, bwd, _f64(g), [_f64(x), _f64(Y), _f64(R), _f64(M)],
+                            [_f64(ggx), _f64(ggY), _f64(ggR), _f64(ggM)])
+
+
+def tp_uvu_double_backward(plan, g, x1, x2, W, gg1, gg2, ggW):
+    """(d_g, d_x1, d_x2, d_W) for the batched product."""
+    fwd = lambda a_, b_, w_: tp_uvu_forward(plan, a_, b_, w_)
+    bwd = lambda g_, a_, b_, w_: tp_uvu_backward(plan, g_, a_, b_, w_)
+    return _double_backward(fwd, bwd, _f64(g), [_f64(x1), _f64(x2), _f64(W)],
+                            [_f64(gg1), _f64(gg2), _f64(ggW)])

@@ -283,3 +283,64 @@ def test_uvw_gM_entries_match_full_backward():
     for (k, pi, u, w), v in zip(entries, vals):
         p = plan.paths[pi]
         assert abs(gM[k, p.woff + u * p.mul_out + w] - v) < 1e-11
+
+
+@pytest.mark.parametrize("mode", ["uvu", "uvw", "batched"])
+def test_double_backward_exact_directional_differences(mode):
+    # S = sum_j <c_j, dL/da_j> is linear in g and in each operand separately, so
+    # S(v + d) - S(v) = <dS/dv, d> holds exactly (up to rounding) for any
+    # direction d; S itself is evaluated with the backward alone.
+    rng = np.random.default_rng(23)
+    N, E, K = 5, 11, 3
+    if mode == "uvw":
+        plan = irreps.make_plan("2x0e+1x1o+1x2e", "0e+1o+2e", "1x0e+2x1o+1x2e", mode="uvw")
+    else:
+        plan = irreps.make_plan("2x0e+1x1o+2x2e", "0e+1o+2e", wl._all_out(2), mode="uvu")
+    if mode == "batched":
+        B = 6
+        shapes = [(B, plan.d1), (B, plan.d2), (B, plan.w_numel)]
+        g = rng.normal(size=(B, plan.d_out))
+
+        def bwd(g_, *a):
+            return conv.tp_uvu_backward(plan, g_, *a)
+
+        def dbl(g_, a, c):
+            return conv.tp_uvu_double_backward(plan, g_, *a, *c)
+    else:
+        rowptr, col = small_graph(rng, N, E)
+        g = rng.normal(size=(N, plan.d_out))
+        if mode == "uvu":
+            shapes = [(N, plan.d1), (E, plan.d2), (E, plan.w_numel)]
+
+            def bwd(g_, *a):
+                return conv.conv_uvu_backward(plan, g_, *a, rowptr, col)
+
+            def dbl(g_, a, c):
+                return conv.conv_uvu_double_backward(plan, g_, *a, *c, rowptr, col)
+        else:
+            shapes = [(N, plan.d1), (E, plan.d2), (E, K), (K, plan.w_numel)]
+
+            def bwd(g_, *a):
+                return conv.conv_uvw_radial_backward(plan, g_, *a, rowptr, col)
+
+            def dbl(g_, a, c):
+                return conv.conv_uvw_radial_double_backward(plan, g_, *a, *c, rowptr, col)
+    a = [rng.normal(size=s) for s in shapes]
+    c = [rng.normal(size=s) for s in shapes]
+
+    def S(g_, a_):
+        return sum((cj * bj).sum() for cj, bj in zip(c, bwd(g_, *a_)))
+
+    d = dbl(g, a, c)
+    assert d[0].shape == g.shape and all(dj.shape == aj.shape for dj, aj in zip(d[1:], a))
+    base = S(g, a)
+    for trial in range(3):
+        dg = rng.normal(size=g.shape)
+        lhs = S(g + dg, a) - base
+        assert abs(lhs - (d[0] * dg).sum()) <= 1e-10 * (abs(lhs) + abs(base) + 1.0)
+        for j in range(len(a)):
+            dj = rng.normal(size=a[j].shape)
+            aj = list(a)
+            aj[j] = a[j] + dj
+            lhs = S(g, aj) - base
+            assert abs(lhs - (d[1 + j] * dj).sum()) <= 1e-10 * (abs(lhs) + abs(base) + 1.0), (mode, j)
