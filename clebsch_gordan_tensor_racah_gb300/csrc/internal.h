@@ -115,6 +115,9 @@ struct V3Dev {
   const int* item_begin = nullptr;
   const Item* items = nullptr;    // path order
   int n_items = 0;
+  const Item* items_bwd = nullptr;  // the same items grouped into backward phases
+  const int* phase_begin = nullptr; // n_phases + 1 offsets into items_bwd
+  int n_phases = 0;
   const int* gxp_off = nullptr;
   int gxp_size = 0;
   const int* in1_off = nullptr;

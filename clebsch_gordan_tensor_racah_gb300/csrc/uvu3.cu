@@ -39,6 +39,34 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   for (size_t p = 0; p < plan->paths.size(); ++p)
     for (int u0 = 0; u0 < plan->paths[p].mul1; u0 += ublock) items.push_back({int(p), u0});
   std::vector<int> item_begin = {0, int(items.size())};
+  // backward phases: at most kPhaseItems items that share no in1 block and no
+  // in2 block (their gx / gY slices are disjoint), taken greedily from the
+  // remaining items in path order
+  constexpr int kPhaseItems = 4;
+  std::vector<Item> items_bwd;
+  std::vector<int> phase_begin = {0};
+  {
+    std::vector<char> used(items.size(), 0);
+    size_t left = items.size();
+    while (left) {
+      std::vector<int> i1s, i2s;
+      int taken = 0;
+      for (size_t k = 0; k < items.size() && taken < kPhaseItems; ++k) {
+        if (used[k]) continue;
+        const PathHost& ph = plan->paths[items[k].path];
+        if (std::find(i1s.begin(), i1s.end(), ph.i1) != i1s.end() ||
+            std::find(i2s.begin(), i2s.end(), ph.i2) != i2s.end())
+          continue;
+        i1s.push_back(ph.i1);
+        i2s.push_back(ph.i2);
+        items_bwd.push_back(items[k]);
+        used[k] = 1;
+        --left;
+        ++taken;
+      }
+      phase_begin.push_back(int(items_bwd.size()));
+    }
+  }
   // gx partial buffer: one [mul][D1] block per path
   std::vector<int> gxp_off;
   int gxp = 0;
@@ -70,6 +98,8 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   };
   const size_t o_ib = put(item_begin.data(), item_begin.size() * sizeof(int));
   const size_t o_it = put(items.data(), items.size() * sizeof(Item));
+  const size_t o_ib2 = put(items_bwd.data(), items_bwd.size() * sizeof(Item));
+  const size_t o_ph = put(phase_begin.data(), phase_begin.size() * sizeof(int));
   const size_t o_gxo = put(gxp_off.data(), gxp_off.size() * sizeof(int));
   const size_t o_in1 = put(in1_off.data(), in1_off.size() * sizeof(int));
   const size_t o_gxb = put(gx_begin.data(), gx_begin.size() * sizeof(int));
@@ -88,6 +118,9 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   v.item_begin = reinterpret_cast<const int*>(at(o_ib));
   v.items = reinterpret_cast<const Item*>(at(o_it));
   v.n_items = int(items.size());
+  v.items_bwd = reinterpret_cast<const Item*>(at(o_ib2));
+  v.phase_begin = reinterpret_cast<const int*>(at(o_ph));
+  v.n_phases = int(phase_begin.size()) - 1;
   v.gxp_off = reinterpret_cast<const int*>(at(o_gxo));
   v.gxp_size = gxp;
   v.in1_off = reinterpret_cast<const int*>(at(o_in1));

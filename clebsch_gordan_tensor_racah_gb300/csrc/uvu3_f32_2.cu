@@ -63,6 +63,9 @@ cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x
   a.gW = static_cast<T*>(gW);
   a.rowptr = t_rowptr;
   a.col = t_eid;
+  a.items = plan->v3.items_bwd;
+  a.phase_begin = plan->v3.phase_begin;
+  a.n_phases = plan->v3.n_phases;
   a.t_dst = t_dst;
   a.N = static_cast<int>(N);
   auto k = uvu_backward3_kernel<T, LPE>;

@@ -113,8 +113,10 @@ struct Uvu3Args {
   const int* t_dst;
   int N, d1, d2, d_out, w_numel;
   const PathDev* paths;
-  const Item* items;      // in path order (path-major schedule)
+  const Item* items;      // in path order (forward); grouped by phase (backward)
   int n_items;
+  const int* phase_begin; // backward: n_phases + 1 offsets into items_bwd
+  int n_phases;
   // backward
   const int* gxp_off;     // per path: offset of its [mul][D1] partial in the gx buffer
   int gxp_size;
@@ -299,28 +301,28 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
     s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.N : lb(t1);
   }
   __syncthreads();
-  const int nb = s_range[0], ne = s_range[1];
-  // path-major: all warps of the CTA work on the same path (one hot instruction
-  // stream); inside a path, warps take the CTA's receivers one at a time from a
-  // shared counter (each receiver's slice of that path is written by one warp)
-  __shared__ int s_next[2];
-  for (int it = 0; it < a.n_items; ++it) {
+  const int nb = s_range[0], nr = s_range[1] - s_range[0];
+  // One counter sweeps the (item, receiver) pairs item-major: the warps stay on
+  // (nearly) the same path -- one hot instruction stream -- and never wait for
+  // each other.  Each receiver's slice of a path is written by one warp.
+  __shared__ int s_ctr;
+  if (tid == 0) s_ctr = 0;
+  __syncthreads();
+  const long long total = (long long)a.n_items * nr;
+  for (;;) {
+    int k = 0;
+    if (lane == 0) k = atomicAdd(&s_ctr, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    if (k >= total) break;
+    const int it = k / nr, n = nb + (k - it * nr);
     const Item item = a.items[it];
     const PathDev p = a.paths[item.path];
     const int u = item.u0 + 4 * q;
     const bool active = u < p.mul;
-    if (tid == 0) s_next[it & 1] = nb;
-    __syncthreads();
-    for (;;) {
-      int n = 0;
-      if (lane == 0) n = atomicAdd(&s_next[it & 1], 1);
-      n = __shfl_sync(0xffffffffu, n, 0);
-      if (n >= ne) break;
-      const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
-      switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
-        CGTP3_TRIPLES(CGTP3_FWD_CASE)
-        default: break;
-      }
+    const int e_begin = a.rowptr[n], deg = a.rowptr[n + 1] - e_begin;
+    switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+      CGTP3_TRIPLES(CGTP3_FWD_CASE)
+      default: break;
     }
   }
 }
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
     s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.N : lb(t1);
   }
   __syncthreads();
-  const int sb = s_range[0], se = s_range[1];
+  const int sb = s_range[0], se = s_range[1], nr = se - sb;
   // clear gx and gY of the CTA's senders (and their out-edges) before the first path
   for (int s = sb + warp; s < se; s += kV3Warps) {
     for (int i = lane; i < a.d1; i += 32) a.gx[(size_t)s * a.d1 + i] = T(0);
@@ -501,23 +503,28 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
       a.gY[(size_t)a.col[tb + j] * a.d2 + c] = T(0);
     }
   }
-  // path-major: all warps on the same path (one hot instruction stream); inside a
-  // path, warps take senders one at a time from a shared counter.  Paths are
-  // separated by block barriers, so every gx / gY row receives its path
-  // contributions one after another in path order (no races, deterministic).
+  // Items come in phases whose items share no in1 block and no in2 block, so
+  // within a phase every gx / gY slice has one writer; a block barrier separates
+  // the phases, and every gx / gY element receives its contributions in phase
+  // order (deterministic).  Inside a phase a counter hands out (sender, item)
+  // pairs sender-major: the phase's few paths share the instruction cache and
+  // a sender's operands stay in L1.
   __shared__ int s_next[2];
-  for (int it = 0; it < a.n_items; ++it) {
-    const Item item = a.items[it];
-    const PathDev p = a.paths[item.path];
-    const int u = item.u0 + 4 * q;
-    const bool active = u < p.mul;
-    if (tid == 0) s_next[it & 1] = sb;
+  for (int ph = 0; ph < a.n_phases; ++ph) {
+    const int i0 = a.phase_begin[ph], ni = a.phase_begin[ph + 1] - i0;
+    if (tid == 0) s_next[ph & 1] = 0;
     __syncthreads();
+    const long long total = (long long)ni * nr;
     for (;;) {
-      int s = 0;
-      if (lane == 0) s = atomicAdd(&s_next[it & 1], 1);
-      s = __shfl_sync(0xffffffffu, s, 0);
-      if (s >= se) break;
+      int k = 0;
+      if (lane == 0) k = atomicAdd(&s_next[ph & 1], 1);
+      k = __shfl_sync(0xffffffffu, k, 0);
+      if (k >= total) break;
+      const int sl = k / ni, s = sb + sl;
+      const Item item = a.items[i0 + (k - sl * ni)];
+      const PathDev p = a.paths[item.path];
+      const int u = item.u0 + 4 * q;
+      const bool active = u < p.mul;
       const int te0 = a.rowptr[s], cnt = a.rowptr[s + 1] - te0;
       switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
         CGTP3_TRIPLES(CGTP3_BWD_CASE)
