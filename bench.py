@@ -284,6 +284,19 @@ def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
             "roofline_ms": roof, "frac": roof / ms}
 
 
+def job_throughput(ms, units, world, device=None):
+    """Whole-job throughput of N replicas (weak scaling: every rank processes its own
+    `units`).  The step time is the slowest rank's (max over ranks, one all-reduce
+    on the default process group when world > 1); value = world * units / time."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units / (ms / 1000.0)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -426,11 +439,7 @@ def main():
     ms = e0.elapsed_time(e1) / args.steps
     fwd_ms = float(np.mean([fe[i].elapsed_time(be[i]) for i in range(args.steps)]))
     bwd_ms = float(np.mean([be[i].elapsed_time(fe[i + 1]) for i in range(args.steps)]))
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * units / (ms / 1000.0)
+    ms, value = job_throughput(ms, units, world, device)
 
     # end to end through the public API with host buffers
     e2e = None
