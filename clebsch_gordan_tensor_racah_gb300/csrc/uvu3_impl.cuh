@@ -331,10 +331,10 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
 // backward: one (sender, path, channel block) per call over `cnt` out-edges
 // ---------------------------------------------------------------------------
 // backward, one (sender, path, channel block) per call over the sender's
-// out-edges, in two passes whose loop bodies each fit the instruction cache:
-//   pass A: cy, t = cy.x -> gW (stored), gx partial (registers)
-//   pass B: h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over
-//           the path's lanes -> read-modify-write of gY (this warp owns the edge)
+// out-edges in one pass (each edge's Y, W and output-gradient slice gathered once):
+//   cy, t = cy.x -> gW (stored), gx partial (registers);
+//   h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over the path's
+//   lanes -> read-modify-write of gY (this warp owns the edge in this phase)
 template <typename T, int LPE, int L1, int L2, int L3>
 __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
                                        const T* __restrict__ W, const T* __restrict__ gout,
@@ -360,42 +360,61 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
     x01[m] = P{xs[m], xs[D1 + m]};
     x23[m] = P{xs[2 * D1 + m], xs[3 * D1 + m]};
   }
-  // ---- pass A
-  {
-    P gxa01[D1], gxa23[D1];
+  // one pass over the out-edges (uniform trip count: the gY reduction shuffles
+  // across the path's lanes); every edge's operands are gathered once
+  P gxa01[D1], gxa23[D1];
 #pragma unroll
-    for (int m = 0; m < D1; ++m) gxa01[m] = gxa23[m] = P{T(0), T(0)};
-    if (active) {
-      for (int j = g; j < cnt; j += EPW) {
-        const int e = __ldg(t_eid + te_begin + j), d = __ldg(t_dst + te_begin + j);
-        T yv[D2], gs[4 * D3], wv[4];
+  for (int m = 0; m < D1; ++m) gxa01[m] = gxa23[m] = P{T(0), T(0)};
+  for (int j0 = 0; j0 < cnt; j0 += EPW) {
+    const int j = j0 + g;
+    const bool valid = active && j < cnt;
+    int e = 0;
+    T yv[D2], gs[4 * D3], wv[4];
+    if (valid) {
+      e = __ldg(t_eid + te_begin + j);
+      const int d = __ldg(t_dst + te_begin + j);
 #pragma unroll
-        for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
-        ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
-        ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
-        T cy[NF];
+      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+      ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
+      ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
+    } else {
 #pragma unroll
-        for (int f = 0; f < NF; ++f) cy[f] = T(0);
-        CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
-        T gw[4] = {T(0), T(0), T(0), T(0)};
+      for (int m = 0; m < D2; ++m) yv[m] = T(0);
 #pragma unroll
-        for (int m3 = 0; m3 < D3; ++m3) {
-          const P wg01{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
-          const P wg23{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
-          P t01{T(0), T(0)}, t23{T(0), T(0)};
+      for (int i = 0; i < 4; ++i) wv[i] = T(0);
 #pragma unroll
-          for (int m1 = 0; m1 < D1; ++m1) {
-            const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
-            t01 = fma2(cp, x01[m1], t01);
-            t23 = fma2(cp, x23[m1], t23);
-            gxa01[m1] = fma2(cp, wg01, gxa01[m1]);
-            gxa23[m1] = fma2(cp, wg23, gxa23[m1]);
-          }
-          gw[0] += gs[m3] * t01.x;
-          gw[1] += gs[D3 + m3] * t01.y;
-          gw[2] += gs[2 * D3 + m3] * t23.x;
-          gw[3] += gs[3 * D3 + m3] * t23.y;
+      for (int i = 0; i < 4 * D3; ++i) gs[i] = T(0);
+    }
+    P wg01[D3], wg23[D3];
+#pragma unroll
+    for (int m3 = 0; m3 < D3; ++m3) {
+      wg01[m3] = P{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
+      wg23[m3] = P{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
+    }
+    // gW and the gx partial through cy = C.Y
+    {
+      T cy[NF];
+#pragma unroll
+      for (int f = 0; f < NF; ++f) cy[f] = T(0);
+      CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1 * D3 + m3] += T(c) * yv[m2]; });
+      T gw[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+      for (int m3 = 0; m3 < D3; ++m3) {
+        P t01{T(0), T(0)}, t23{T(0), T(0)};
+#pragma unroll
+        for (int m1 = 0; m1 < D1; ++m1) {
+          const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
+          t01 = fma2(cp, x01[m1], t01);
+          t23 = fma2(cp, x23[m1], t23);
+          gxa01[m1] = fma2(cp, wg01[m3], gxa01[m1]);
+          gxa23[m1] = fma2(cp, wg23[m3], gxa23[m1]);
         }
+        gw[0] += gs[m3] * t01.x;
+        gw[1] += gs[D3 + m3] * t01.y;
+        gw[2] += gs[2 * D3 + m3] * t23.x;
+        gw[3] += gs[3 * D3 + m3] * t23.y;
+      }
+      if (valid) {
         T* gp = gW + (size_t)e * w_numel + woff + u;
         if constexpr (sizeof(T) == 4) {
           *reinterpret_cast<float4*>(gp) = make_float4(gw[0], gw[1], gw[2], gw[3]);
@@ -405,7 +424,25 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
         }
       }
     }
-    // gx partial of this path: sum over the edge slots; slot 0 accumulates (owner warp)
+    // gY: h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C), reduced over the path's lanes
+    T h[HV];
+#pragma unroll
+    for (int i = 0; i < HV; ++i) h[i] = T(0);
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) {
+      const P pr = fma2(x23[m1], wg23[m3], mul2(x01[m1], wg01[m3]));
+      h[m2] += T(c) * (pr.x + pr.y);
+    });
+    group_reduce<T, HV, LPE>(h, q);
+    if (valid) {
+#pragma unroll
+      for (int k = 0; k < HV / LPE; ++k) {
+        const int slot = q * (HV / LPE) + k;
+        if (slot < D2) gY[(size_t)e * d2 + off2 + slot] += h[k];
+      }
+    }
+  }
+  // gx partial of this path: sum over the edge slots; slot 0 accumulates (owner warp)
+  {
     T v[4 * D1];
 #pragma unroll
     for (int m = 0; m < D1; ++m) {
@@ -422,45 +459,6 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
       T* dst = gx + (size_t)s * d1 + off1 + u * D1;
 #pragma unroll
       for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
-    }
-  }
-  // ---- pass B (uniform trip count: the h reduction shuffles across the path's lanes)
-  for (int j0 = 0; j0 < cnt; j0 += EPW) {
-    const int j = j0 + g;
-    const bool valid = active && j < cnt;
-    int e = 0;
-    T gs[4 * D3], wv[4];
-    if (valid) {
-      e = __ldg(t_eid + te_begin + j);
-      const int d = __ldg(t_dst + te_begin + j);
-      ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
-      ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) wv[i] = T(0);
-#pragma unroll
-      for (int i = 0; i < 4 * D3; ++i) gs[i] = T(0);
-    }
-    P wg01[D3], wg23[D3];
-#pragma unroll
-    for (int m3 = 0; m3 < D3; ++m3) {
-      wg01[m3] = P{wv[0] * gs[m3], wv[1] * gs[D3 + m3]};
-      wg23[m3] = P{wv[2] * gs[2 * D3 + m3], wv[3] * gs[3 * D3 + m3]};
-    }
-    T h[HV];
-#pragma unroll
-    for (int i = 0; i < HV; ++i) h[i] = T(0);
-    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) {
-      const P pr = fma2(x23[m1], wg23[m3], mul2(x01[m1], wg01[m3]));
-      h[m2] += T(c) * (pr.x + pr.y);
-    });
-    group_reduce<T, HV, LPE>(h, q);
-    if (valid) {
-#pragma unroll
-      for (int k = 0; k < HV / LPE; ++k) {
-        const int slot = q * (HV / LPE) + k;
-        if (slot < D2) gY[(size_t)e * d2 + off2 + slot] += h[k];
-      }
     }
   }
 }
