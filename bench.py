@@ -55,6 +55,7 @@ CONFIGS = {
     "mace": dict(name="mace", dtype="float32", over={}),
     "mace64": dict(name="mace", dtype="float64", over={}),
     "highl": dict(name="highl", dtype="float32", over={}),
+    "nequip_bf16": dict(name="nequip", dtype="bfloat16", over={}),
     "uvw": dict(name="uvw", dtype="float32", over={}),
 }
 
@@ -65,16 +66,19 @@ def build_inputs(cfgkey, device, nodes=None):
     from clebsch_gordan_tensor_racah_gb300 import workloads as wl
     c = CONFIGS[cfgkey]
     spec = dict(wl.SPECS[c["name"]])
-    tdt = torch.float64 if c["dtype"] == "float64" else torch.float32
+    tdt = {"float64": torch.float64, "bfloat16": torch.bfloat16}.get(c["dtype"], torch.float32)
     mode = spec["mode"]
     plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
                    radial_k=spec.get("K", 0) if mode == "uvw" else 0)
     over = dict(c["over"])
     if nodes:
         over["B" if spec["graph"] is None else "N"] = int(nodes)
-    w = wl.make(c["name"], plan.w_numel, seed=0, dtype=c["dtype"], **over)
+    w = wl.make(c["name"], plan.w_numel, seed=0, dtype="float32" if tdt == torch.bfloat16 else c["dtype"], **over)
     host = {k: v for k, v in w.items() if isinstance(v, np.ndarray)}
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(device) for k, v in host.items()}
+    if tdt == torch.bfloat16:   # features and weights stored as bfloat16 (FP32 arithmetic and outputs)
+        dev = {k: (v.to(torch.bfloat16) if v.is_floating_point() else v) for k, v in dev.items()}
+        host = {k: (dev[k].cpu() if dev[k].dtype == torch.bfloat16 else v) for k, v in host.items()}
     graph = None
     if "rowptr" in dev:
         graph = cg.Graph(dev["rowptr"], dev["col"], w["N"])
@@ -85,6 +89,7 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     """Returns (fwd, bwd, units, bytes_fwd, bytes_bwd, flops_fwd, flops_bwd, out_shape)."""
     import clebsch_gordan_tensor_racah_gb300 as cg
     es = 8 if tdt.__str__().endswith("64") else 4
+    ei = 2 if tdt.__str__().endswith("bfloat16") else es   # input element size (outputs: es)
     if "rowptr" in dev:
         N, E = w["N"], w["E"]
         x, Y = dev["x"], dev["Y"]
@@ -92,9 +97,9 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
         M = dev.get("M")
         units = E
         idx = 4 * (N + 1 + E)
-        bf = es * (N * plan.d1 + E * plan.d2 + WR.numel() + (M.numel() if M is not None else 0) + N * plan.d_out) + idx
-        bb = es * (2 * N * plan.d1 + 2 * E * plan.d2 + 2 * WR.numel() + 2 * (M.numel() if M is not None else 0)
-                   + N * plan.d_out) + idx + 8 * E
+        nin = N * plan.d1 + E * plan.d2 + WR.numel() + (M.numel() if M is not None else 0)
+        bf = ei * nin + es * N * plan.d_out + idx
+        bb = ei * (nin + N * plan.d_out) + es * nin + idx + 8 * E
 
         def fwd(out):
             return cg.cgtp_conv_forward(plan, graph, x, Y, WR, M, out=out)
@@ -229,7 +234,7 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
         return units / dt, f"batches of {B} samples of the same recipe, fwd+bwd, {dt:.1f} s"
     # a smaller graph of the same recipe (same degree distribution and features)
     N = {"tiny": 64, "nequip": 120, "mace": 60, "uvw": 4}[c["name"]]
-    w = wl.make(c["name"], oplan.w_numel, seed=0, dtype=c["dtype"], N=N)
+    w = wl.make(c["name"], oplan.w_numel, seed=0, dtype="float32" if c["dtype"] == "bfloat16" else c["dtype"], N=N)
     units, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
         if spec["mode"] == "uvu":
@@ -313,6 +318,7 @@ def config_block(cfgkey, w, n_gpus):
                       "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
                       "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)"}[spec],
          "step": "conv forward + backward" if "N" in w else "batched forward + backward",
+         "precision": "bfloat16 inputs, FP32 arithmetic and outputs" if c["dtype"] == "bfloat16" else c["dtype"],
          "l2": "inputs larger than L2 (no flush needed)",
          "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
     if "N" in w:
@@ -385,7 +391,7 @@ def main():
     plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device, args.nodes)
     fwd, bwd, units, bf, bb, out_shape = step_fns(args.config, plan, graph, w, dev, tdt)
     g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
-    out = torch.empty(out_shape, dtype=tdt, device=device)
+    out = torch.empty(out_shape, dtype=plan.out_dtype, device=device)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -444,10 +450,10 @@ def main():
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()
-               if k not in ("rowptr", "col")}
+        pin = {k: (v if isinstance(v, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(v))).pin_memory()
+               for k, v in host.items() if k not in ("rowptr", "col")}
         gh = g.cpu().pin_memory()
-        out_h = torch.empty(out_shape, dtype=tdt).pin_memory()
+        out_h = torch.empty(out_shape, dtype=plan.out_dtype).pin_memory()
         res_h = None
         h2d = sum(t.numel() * t.element_size() for t in pin.values()) + gh.numel() * gh.element_size()
 
@@ -514,12 +520,13 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "edges/s" if "N" in w else "samples/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64" if tdt == torch.float64 else "f32", "data": "synthetic",
+            "dtype": {torch.float64: "f64", torch.bfloat16: "bf16 inputs, f32 arithmetic"}.get(tdt, "f32"),
+            "data": "synthetic",
             "config": config_block(args.config, w, world),
             "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
             "clocks": clk}
-    if not args.no_double_backward:
+    if not args.no_double_backward and tdt != torch.bfloat16:
         line["double_backward"] = time_double_backward(plan, graph, w, dev, g, stream, units, roofline)
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc = time_oracle_sample(args.config)

@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_PKG, "libcgtp.so")
 
 CGTP_OK, CGTP_EINVAL, CGTP_EUNSUPPORTED, CGTP_ENOMEM, CGTP_ECUDA, CGTP_EGRAPH = range(6)
 CGTP_UVU, CGTP_UVW = 0, 1
-CGTP_F32, CGTP_F64 = 0, 1
+CGTP_F32, CGTP_F64, CGTP_BF16 = 0, 1, 2
 
 EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan_path",
            "cgtp_forward", "cgtp_backward", "cgtp_graph_create", "cgtp_graph_destroy",
@@ -134,7 +134,9 @@ class Plan:
         self.dtype = dtype
         self.radial_k = radial_k
         m = CGTP_UVU if mode == "uvu" else CGTP_UVW
-        dt = CGTP_F64 if dtype == torch.float64 else CGTP_F32
+        dt = {torch.float64: CGTP_F64, torch.bfloat16: CGTP_BF16}.get(dtype, CGTP_F32)
+        # bfloat16 plans read bfloat16 inputs and write float32 outputs
+        self.out_dtype = torch.float32 if dtype == torch.bfloat16 else dtype
         h = ctypes.c_void_p()
         arr, n = None, 0
         if instructions:
@@ -227,24 +229,26 @@ def cgtp_backward(plan, gout, x1, x2, W, stream=None):
 def cgtp_conv_forward(plan, graph, x, Y, W_or_R, M=None, out=None, stream=None):
     torch = _torch()
     if out is None:
-        out = torch.empty(graph.N, plan.d_out, dtype=plan.dtype, device=x.device)
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.out_dtype, device=x.device)
     _check(lib().cgtp_conv_forward(plan.handle, graph.handle, _ptr(x, "x", plan.dtype),
                                    _ptr(Y, "Y", plan.dtype), _ptr(W_or_R, "W_or_R", plan.dtype),
-                                   _ptr(M, "M", plan.dtype), _ptr(out, "out", plan.dtype), _stream(stream)))
+                                   _ptr(M, "M", plan.dtype), _ptr(out, "out", plan.out_dtype), _stream(stream)))
     return out
 
 
 def cgtp_conv_backward(plan, graph, gout, x, Y, W_or_R, M=None, stream=None, outs=None):
     torch = _torch()
     if outs is None:
-        gx, gY, gW = torch.empty_like(x), torch.empty_like(Y), torch.empty_like(W_or_R)
-        gM = torch.empty_like(M) if M is not None else None
+        od = plan.out_dtype
+        gx, gY, gW = (torch.empty(t.shape, dtype=od, device=t.device) for t in (x, Y, W_or_R))
+        gM = torch.empty(M.shape, dtype=od, device=M.device) if M is not None else None
     else:
         gx, gY, gW, gM = outs
     _check(lib().cgtp_conv_backward(plan.handle, graph.handle, _ptr(gout, "gout", plan.dtype),
                                     _ptr(x, "x", plan.dtype), _ptr(Y, "Y", plan.dtype),
                                     _ptr(W_or_R, "W_or_R", plan.dtype), _ptr(M, "M", plan.dtype),
-                                    _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gW, "gW"), _ptr(gM, "gM"),
+                                    _ptr(gx, "gx", plan.out_dtype), _ptr(gY, "gY", plan.out_dtype),
+                                    _ptr(gW, "gW", plan.out_dtype), _ptr(gM, "gM", plan.out_dtype),
                                     _stream(stream)))
     return gx, gY, gW, gM
 

@@ -142,7 +142,8 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
   if (!out) return fail(CGTP_EINVAL, "null plan output pointer");
   *out = nullptr;
   if (mode != CGTP_UVU && mode != CGTP_UVW) return fail(CGTP_EINVAL, "mode must be CGTP_UVU or CGTP_UVW");
-  if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_EINVAL, "dtype must be CGTP_F32 or CGTP_F64");
+  if (dtype != CGTP_F32 && dtype != CGTP_F64 && dtype != CGTP_BF16)
+    return fail(CGTP_EINVAL, "dtype must be CGTP_F32, CGTP_F64 or CGTP_BF16");
   if (mode == CGTP_UVU && radial_k != 0) return fail(CGTP_EINVAL, "radial_k must be 0 in uvu mode");
   if (mode == CGTP_UVW && (radial_k < 1 || radial_k > 16))
     return fail(CGTP_EUNSUPPORTED, "uvw mode needs radial weights with 1 <= radial_k <= 16");
@@ -183,6 +184,9 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (s == CGTP_OK) s = upload_layout(p, batch, &p->batch_layout);
     if (s == CGTP_OK) s = build_v3(p);
     if (s == CGTP_OK) s = bt_create(p);
+    if (s == CGTP_OK && dtype == CGTP_BF16 && !p->v3.lpe)
+      s = fail(CGTP_EUNSUPPORTED, "CGTP_BF16 needs l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} "
+                                  "or m a multiple of 128");
   } else {
     s = uvw_create(p);
   }
@@ -237,6 +241,7 @@ cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const v
   clear_error();
   if (!plan) return fail(CGTP_EINVAL, "null plan");
   if (plan->mode != CGTP_UVU) return fail(CGTP_EUNSUPPORTED, "cgtp_forward needs a uvu plan");
+  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "the batched product has no CGTP_BF16 kernels");
   if (B < 0 || B >= (int64_t(1) << 31)) return fail(CGTP_EINVAL, "batch size out of range");
   if (B == 0) return CGTP_OK;
   cgtp_status s;
@@ -250,6 +255,7 @@ cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, cons
   clear_error();
   if (!plan) return fail(CGTP_EINVAL, "null plan");
   if (plan->mode != CGTP_UVU) return fail(CGTP_EUNSUPPORTED, "cgtp_backward needs a uvu plan");
+  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "the batched product has no CGTP_BF16 kernels");
   if (B < 0 || B >= (int64_t(1) << 31)) return fail(CGTP_EINVAL, "batch size out of range");
   if (B == 0) return CGTP_OK;
   cgtp_status s;

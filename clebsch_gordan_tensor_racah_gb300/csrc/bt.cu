@@ -727,6 +727,7 @@ bool bt_forward(const cgtp_plan_s* plan, const void* x1, const void* x2, const v
   a.out = static_cast<float*>(out);
   a.warp_floats = st->wf_fwd;
   a.chunks = static_cast<int>((B + a.unit - 1) / a.unit);
+  if ((int64_t)a.G * a.chunks + st->grid_fwd >= (int64_t(1) << 31)) return false;  // 32-bit unit counter
   a.n_units = a.G * a.chunks;
   a.counter = st->counter;
   if (cudaMemsetAsync(st->counter, 0, sizeof(int), s) != cudaSuccess) {

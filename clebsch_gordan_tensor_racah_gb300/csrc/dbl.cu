@@ -91,6 +91,7 @@ cgtp_status double_backward(const Calls& c, int64_t rows, int64_t E, const void*
                             const void* const* a, const void* const* cot, void* d_gout, void* const* d,
                             void* workspace, int64_t ws_bytes) {
   const cgtp_plan_s* plan = c.plan;
+  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "double backward has no CGTP_BF16 path");
   const int64_t es = plan->dtype == CGTP_F64 ? 8 : 4;
   int64_t sz[4];
   const int n = operand_sizes(plan, rows, E, sz);

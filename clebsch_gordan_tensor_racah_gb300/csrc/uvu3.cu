@@ -18,6 +18,13 @@ template <typename T, int LPE>
 cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
+template <int LPE>
+cgtp_status fwd3_launch_bf16(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
+                             const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
+template <int LPE>
+cgtp_status bwd3_launch_bf16(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
+                             const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
+                             const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
 }  // namespace uvu3_detail
 
 cgtp_status build_v3(cgtp_plan_s* plan) {
@@ -144,8 +151,22 @@ void free_v3(cgtp_plan_s* plan) {
 bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
                        const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st) {
   using namespace uvu3_detail;
-  if (!plan->v3.lpe || std::getenv("CGTP_UVU_NO_V3")) return false;
+  if (!plan->v3.lpe) return false;
+  if ((int64_t)plan->v3.n_items * N >= (int64_t(1) << 31)) {  // the kernels' 32-bit work counters
+    if (plan->dtype != CGTP_BF16) return false;
+    *st = fail(CGTP_EUNSUPPORTED, "graph too large for the bfloat16 kernels (paths x nodes >= 2^31)");
+    return true;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan->dtype == CGTP_BF16) {  // only these kernels read bfloat16 inputs
+    switch (plan->v3.lpe) {
+      case 2: *st = fwd3_launch_bf16<2>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+      case 8: *st = fwd3_launch_bf16<8>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+      case 32: *st = fwd3_launch_bf16<32>(plan, x, Y, W, out, rowptr, col, N, s); return true;
+      default: return false;
+    }
+  }
+  if (std::getenv("CGTP_UVU_NO_V3")) return false;
   const bool f64 = plan->dtype == CGTP_F64;
   switch (plan->v3.lpe) {
     case 2: *st = f64 ? fwd3_launch<double, 2>(plan, x, Y, W, out, rowptr, col, N, s)
@@ -163,8 +184,24 @@ bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
                         cgtp_status* st) {
   using namespace uvu3_detail;
-  if (!plan->v3.lpe || std::getenv("CGTP_UVU_NO_V3")) return false;
+  if (!plan->v3.lpe) return false;
+  if ((int64_t)plan->v3.n_items * N >= (int64_t(1) << 31)) {  // the kernels' 32-bit work counters
+    if (plan->dtype != CGTP_BF16) return false;
+    *st = fail(CGTP_EUNSUPPORTED, "graph too large for the bfloat16 kernels (paths x nodes >= 2^31)");
+    return true;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan->dtype == CGTP_BF16) {
+#define V3BB(L) bwd3_launch_bf16<L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
+    switch (plan->v3.lpe) {
+      case 2: *st = V3BB(2); return true;
+      case 8: *st = V3BB(8); return true;
+      case 32: *st = V3BB(32); return true;
+      default: return false;
+    }
+#undef V3BB
+  }
+  if (std::getenv("CGTP_UVU_NO_V3")) return false;
   const bool f64 = plan->dtype == CGTP_F64;
 #define V3B(T, L) bwd3_launch<T, L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
   switch (plan->v3.lpe) {

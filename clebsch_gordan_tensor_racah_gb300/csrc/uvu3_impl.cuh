@@ -17,6 +17,7 @@
 //     (edge, path) cross lanes;
 //   * every result is written once by its owner (receiver or sender): no atomics.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -98,12 +99,14 @@ __device__ __forceinline__ void group_reduce(T (&v)[V], int q) {
 namespace cgtp {
 namespace uvu3_detail {
 
-template <typename T>
+// T: arithmetic and output type; S: storage type of the inputs x, Y, W and the
+// output gradient (T, or bfloat16 with FP32 arithmetic and outputs)
+template <typename T, typename S = T>
 struct Uvu3Args {
-  const T* x;
-  const T* Y;
-  const T* W;
-  const T* gout;
+  const S* x;
+  const S* Y;
+  const S* W;
+  const S* gout;
   T* out;
   T* gx;
   T* gY;
@@ -148,6 +151,24 @@ __device__ __forceinline__ void ldvec(const T* p, T (&v)[N]) {  // N consecutive
   }
 }
 
+// N consecutive bfloat16 values (8-byte aligned), widened exactly to T
+template <typename T, int N>
+__device__ __forceinline__ void ldvec(const __nv_bfloat16* p, T (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p) + i);
+    v[4 * i] = T(__uint_as_float(q.x << 16));
+    v[4 * i + 1] = T(__uint_as_float(q.x & 0xffff0000u));
+    v[4 * i + 2] = T(__uint_as_float(q.y << 16));
+    v[4 * i + 3] = T(__uint_as_float(q.y & 0xffff0000u));
+  }
+}
+__device__ __forceinline__ float ld1(const float* p) { return __ldg(p); }
+__device__ __forceinline__ double ld1(const double* p) { return __ldg(p); }
+__device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<unsigned>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
 // Rows [nb, ne) of a CTA split into contiguous warp ranges of about equal work
 // (edges + rows): warp w gets [lo, hi).
 __device__ __forceinline__ void warp_rows(const int* rowptr, int nb, int ne, int warp, int nwarps,
@@ -175,15 +196,15 @@ struct FwdEdge {  // one edge's operands, loaded before any arithmetic
   T wv[4];
 };
 
-template <typename T, int LPE, int L1, int L2, int L3>
+template <typename T, int LPE, int L1, int L2, int L3, typename S>
 __device__ __forceinline__ void fwd3_load(FwdEdge<T, 2 * L1 + 1, 2 * L2 + 1, 2 * L3 + 1>& E,
-                                          const T* __restrict__ x, const T* __restrict__ Y,
-                                          const T* __restrict__ W, int e, int s, bool ok, int d1,
+                                          const S* __restrict__ x, const S* __restrict__ Y,
+                                          const S* __restrict__ W, int e, int s, bool ok, int d1,
                                           int d2, int w_numel, int off1, int off2, int woff, int u) {
   constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1;
   if (ok) {
 #pragma unroll
-    for (int m = 0; m < D2; ++m) E.yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+    for (int m = 0; m < D2; ++m) E.yv[m] = ld1(Y + (size_t)e * d2 + off2 + m);
     ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, E.xs);
     ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, E.wv);
   } else {
@@ -221,9 +242,9 @@ __device__ __forceinline__ void fwd3_math(const FwdEdge<T, 2 * L1 + 1, 2 * L2 + 
 
 // forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes;
 // each lane walks its edge slot two edges at a time, loads first
-template <typename T, int LPE, int L1, int L2, int L3>
-__device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
-                                       const T* __restrict__ W, T* __restrict__ out,
+template <typename T, int LPE, int L1, int L2, int L3, typename S>
+__device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restrict__ Y,
+                                       const S* __restrict__ W, T* __restrict__ out,
                                        const int* __restrict__ col, int e_begin, int deg, int n,
                                        int d1, int d2, int d_out, int w_numel, int off1, int off2,
                                        int ooff, int woff, int u, bool active, int g) {
@@ -281,8 +302,8 @@ __device__ __noinline__ void fwd3_item(const T* __restrict__ x, const T* __restr
                                     a.w_numel, p.off1, p.off2, p.ooff, p.woff, u, active, g);      \
     break;
 
-template <typename T, int LPE>
-__global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3Args<T> a) {
+template <typename T, int LPE, typename S = T>
+__global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3Args<T, S> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
@@ -305,10 +326,11 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
   // One counter sweeps the (item, receiver) pairs item-major: the warps stay on
   // (nearly) the same path -- one hot instruction stream -- and never wait for
   // each other.  Each receiver's slice of a path is written by one warp.
+  // (the host guarantees n_items * N < 2^31, so the counter stays 32-bit)
   __shared__ int s_ctr;
   if (tid == 0) s_ctr = 0;
   __syncthreads();
-  const long long total = (long long)a.n_items * nr;
+  const int total = a.n_items * nr;
   for (;;) {
     int k = 0;
     if (lane == 0) k = atomicAdd(&s_ctr, 1);
@@ -335,9 +357,9 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
 //   cy, t = cy.x -> gW (stored), gx partial (registers);
 //   h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over the path's
 //   lanes -> read-modify-write of gY (this warp owns the edge in this phase)
-template <typename T, int LPE, int L1, int L2, int L3>
-__device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restrict__ Y,
-                                       const T* __restrict__ W, const T* __restrict__ gout,
+template <typename T, int LPE, int L1, int L2, int L3, typename S>
+__device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restrict__ Y,
+                                       const S* __restrict__ W, const S* __restrict__ gout,
                                        T* __restrict__ gW, const int* __restrict__ t_eid,
                                        const int* __restrict__ t_dst, int te_begin, int cnt, int s,
                                        int d1, int d2, int d_out, int w_numel, int off1, int off2,
@@ -374,7 +396,7 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
       e = __ldg(t_eid + te_begin + j);
       const int d = __ldg(t_dst + te_begin + j);
 #pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Y + (size_t)e * d2 + off2 + m);
+      for (int m = 0; m < D2; ++m) yv[m] = ld1(Y + (size_t)e * d2 + off2 + m);
       ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
       ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
     } else {
@@ -471,8 +493,8 @@ __device__ __noinline__ void bwd3_item(const T* __restrict__ x, const T* __restr
                                     active, g, q, a.gY, a.gx);                                       \
     break;
 
-template <typename T, int LPE>
-__global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3Args<T> a) {
+template <typename T, int LPE, typename S = T>
+__global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3Args<T, S> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   __shared__ int s_range[2];
@@ -512,14 +534,15 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
     const int i0 = a.phase_begin[ph], ni = a.phase_begin[ph + 1] - i0;
     if (tid == 0) s_next[ph & 1] = 0;
     __syncthreads();
-    const long long total = (long long)ni * nr;
+    const int total = ni * nr;
     for (;;) {
       int k = 0;
       if (lane == 0) k = atomicAdd(&s_next[ph & 1], 1);
       k = __shfl_sync(0xffffffffu, k, 0);
       if (k >= total) break;
-      const int sl = k / ni, s = sb + sl;
-      const Item item = a.items[i0 + (k - sl * ni)];
+      const int sl = k / ni, ii = k - sl * ni;
+      const int s = sb + sl;
+      const Item item = a.items[i0 + ii];
       const PathDev p = a.paths[item.path];
       const int u = item.u0 + 4 * q;
       const bool active = u < p.mul;

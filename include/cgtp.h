@@ -55,7 +55,9 @@ typedef enum {
 } cgtp_status;
 
 typedef enum { CGTP_UVU = 0, CGTP_UVW = 1 } cgtp_mode;
-typedef enum { CGTP_F32 = 0, CGTP_F64 = 1 } cgtp_dtype;
+/* CGTP_BF16: inputs x, Y, W and the output gradient stored as bfloat16; arithmetic
+ * and every output (out, gx, gY, gW) in FP32. */
+typedef enum { CGTP_F32 = 0, CGTP_F64 = 1, CGTP_BF16 = 2 } cgtp_dtype;
 
 /* One path: in1 block i_in1 (x) in2 block i_in2 -> output irrep irreps_out[i_out]. */
 typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
@@ -75,7 +77,12 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      output block of multiplicity mul1, appended in path order -- the muls of
  *      irreps_out are ignored) or CGTP_UVW (fully connected mixing into the
  *      blocks of irreps_out).
- *  dtype : CGTP_F32 or CGTP_F64 (CGTP_UVW supports CGTP_F32 only).
+ *  dtype : CGTP_F32, CGTP_F64 or CGTP_BF16 (CGTP_UVW supports CGTP_F32 only).
+ *      CGTP_BF16 (bfloat16 inputs, FP32 arithmetic and outputs; the pages'
+ *      lower-precision future work) serves graph convolutions whose plan has
+ *      l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} or m a multiple
+ *      of 128; other plans return CGTP_EUNSUPPORTED, and so do the batched and
+ *      double-backward entry points.
  *  radial_k : 0 for uvu; for uvw the number K of radial functions (1..16); the
  *      weights are then W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by

@@ -1,0 +1,59 @@
+"""GPU parity of the bfloat16-input convolution (FP32 arithmetic and outputs).
+
+The inputs x, Y, W and the output gradient are rounded to bfloat16 once; the
+FP64 oracle consumes exactly those rounded values, so the only differences
+left are FP32 rounding in the kernels: the FP32 bound applies,
+max|err| <= 1e-4 * max|ref| per output tensor.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import clebsch_gordan_tensor_racah_gb300 as cg  # noqa: E402
+from clebsch_gordan_tensor_racah_gb300 import workloads as wl  # noqa: E402
+from oracle import conv as oconv, irreps as oirr  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def close(name, got, ref):
+    assert got.dtype == torch.float32, (name, got.dtype)
+    got = got.cpu().numpy().astype(np.float64)
+    err, scale = np.abs(got - ref).max(), np.abs(ref).max()
+    assert err <= 1e-4 * scale, f"{name}: max|err| {err:.3e} vs max|ref| {scale:.3e}"
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("nequip", dict(N=300)), ("mace", dict(N=150))])
+def test_bf16_conv_fwd_bwd(name, over):
+    spec = wl.SPECS[name]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvu")
+    w = wl.make(name, oplan.w_numel, seed=9, **over)
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
+    dev = torch.device("cuda")
+    b = {k: torch.from_numpy(np.ascontiguousarray(w[k])).to(dev).to(torch.bfloat16) for k in ("x", "Y", "W")}
+    h = {k: v.float().cpu().numpy().astype(np.float64) for k, v in b.items()}   # the exact bf16 values
+    graph = cg.Graph(torch.from_numpy(w["rowptr"]).to(dev), torch.from_numpy(w["col"]).to(dev), w["N"])
+    out = cg.cgtp_conv_forward(plan, graph, b["x"], b["Y"], b["W"])
+    close("out", out, oconv.conv_uvu_forward(oplan, h["x"], h["Y"], h["W"], w["rowptr"], w["col"]))
+    g = torch.randn(out.shape, device=dev, generator=torch.Generator(dev).manual_seed(3)).to(torch.bfloat16)
+    gx, gY, gW, _ = cg.cgtp_conv_backward(plan, graph, g, b["x"], b["Y"], b["W"])
+    r = oconv.conv_uvu_backward(oplan, g.float().cpu().numpy().astype(np.float64), h["x"], h["Y"], h["W"],
+                                w["rowptr"], w["col"])
+    for nm, a, ref in zip(("gx", "gY", "gW"), (gx, gY, gW), r):
+        close(nm, a, ref)
+
+
+def test_bf16_outside_the_served_plans_is_unsupported():
+    spec = wl.SPECS["highl"]   # l up to 7: no bfloat16 kernels
+    with pytest.raises(cg.CgtpError) as e:
+        cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
+    assert e.value.status == cg.CGTP_EUNSUPPORTED
+    spec = wl.SPECS["tiny"]
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
+    z = lambda n: torch.zeros(4, n, device="cuda", dtype=torch.bfloat16)   # noqa: E731
+    with pytest.raises(cg.CgtpError) as e:
+        cg.cgtp_forward(plan, z(plan.d1), z(plan.d2), z(plan.w_numel),
+                        out=torch.zeros(4, plan.d_out, device="cuda", dtype=torch.bfloat16))
+    assert e.value.status == cg.CGTP_EUNSUPPORTED
