@@ -56,6 +56,7 @@ CONFIGS = {
     "mace64": dict(name="mace", dtype="float64", over={}),
     "highl": dict(name="highl", dtype="float32", over={}),
     "nequip_bf16": dict(name="nequip", dtype="bfloat16", over={}),
+    "nequip_sh": dict(name="nequip", dtype="float32", over={}, sh=True),
     "uvw": dict(name="uvw", dtype="float32", over={}),
 }
 
@@ -79,6 +80,13 @@ def build_inputs(cfgkey, device, nodes=None):
     if tdt == torch.bfloat16:   # features and weights stored as bfloat16 (FP32 arithmetic and outputs)
         dev = {k: (v.to(torch.bfloat16) if v.is_floating_point() else v) for k, v in dev.items()}
         host = {k: (dev[k].cpu() if dev[k].dtype == torch.bfloat16 else v) for k, v in host.items()}
+    if c.get("sh"):   # raw edge vectors of random lengths instead of the harmonics
+        rng = np.random.default_rng(7)
+        r = rng.standard_normal((w["E"], 3)) * rng.uniform(0.5, 5.0, (w["E"], 1))
+        host["rvec"] = r.astype(np.float32)
+        del host["Y"]
+        dev["rvec"] = torch.from_numpy(host["rvec"]).to(device)
+        del dev["Y"]
     graph = None
     if "rowptr" in dev:
         graph = cg.Graph(dev["rowptr"], dev["col"], w["N"])
@@ -90,6 +98,21 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     import clebsch_gordan_tensor_racah_gb300 as cg
     es = 8 if tdt.__str__().endswith("64") else 4
     ei = 2 if tdt.__str__().endswith("bfloat16") else es   # input element size (outputs: es)
+    if "rvec" in dev:   # edge-vector input: harmonics evaluated in the kernels
+        N, E = w["N"], w["E"]
+        x, rv, W = dev["x"], dev["rvec"], dev["W"]
+        units = E
+        idx = 4 * (N + 1 + E)
+        nin = N * plan.d1 + 3 * E + W.numel()
+        bf = es * (nin + N * plan.d_out) + idx
+        bb = es * (2 * nin + N * plan.d_out + E * plan.d2) + idx + 8 * E
+
+        def fwd(out):
+            return cg.cgtp_conv_forward_sh(plan, graph, x, rv, W, out=out)
+
+        def bwd(g, outs):
+            return cg.cgtp_conv_backward_sh(plan, graph, g, x, rv, W)
+        return fwd, bwd, units, bf, bb, (N, plan.d_out)
     if "rowptr" in dev:
         N, E = w["N"], w["E"]
         x, Y = dev["x"], dev["Y"]
@@ -237,7 +260,11 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
     w = wl.make(c["name"], oplan.w_numel, seed=0, dtype="float32" if c["dtype"] == "bfloat16" else c["dtype"], N=N)
     units, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
-        if spec["mode"] == "uvu":
+        if c.get("sh"):
+            rv = np.random.default_rng(7).standard_normal((w["E"], 3))
+            out = oconv.conv_uvu_forward_sh(oplan, w["x"], rv, w["W"], w["rowptr"], w["col"])
+            oconv.conv_uvu_backward_sh(oplan, out, w["x"], rv, w["W"], w["rowptr"], w["col"])
+        elif spec["mode"] == "uvu":
             out = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
             oconv.conv_uvu_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
         else:
@@ -319,6 +346,7 @@ def config_block(cfgkey, w, n_gpus):
                       "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)"}[spec],
          "step": "conv forward + backward" if "N" in w else "batched forward + backward",
          "precision": "bfloat16 inputs, FP32 arithmetic and outputs" if c["dtype"] == "bfloat16" else c["dtype"],
+         "edge_features": "raw edge vectors, harmonics evaluated in the kernels" if c.get("sh") else "harmonics Y",
          "l2": "inputs larger than L2 (no flush needed)",
          "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
     if "N" in w:
@@ -526,7 +554,7 @@ def main():
             "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
             "clocks": clk}
-    if not args.no_double_backward and tdt != torch.bfloat16:
+    if not args.no_double_backward and tdt != torch.bfloat16 and not CONFIGS[args.config].get("sh"):
         line["double_backward"] = time_double_backward(plan, graph, w, dev, g, stream, units, roofline)
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc = time_oracle_sample(args.config)

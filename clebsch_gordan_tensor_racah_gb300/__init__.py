@@ -34,7 +34,8 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_graph_transpose", "cgtp_conv_forward", "cgtp_conv_backward",
            "cgtp_real_cg_block", "cgtp_last_error", "cgtp_graph_transpose_noalloc",
            "cgtp_conv_double_backward_workspace", "cgtp_conv_double_backward",
-           "cgtp_double_backward_workspace", "cgtp_double_backward"]
+           "cgtp_double_backward_workspace", "cgtp_double_backward",
+           "cgtp_conv_forward_sh", "cgtp_conv_backward_sh", "cgtp_real_sh"]
 
 
 class CgtpError(RuntimeError):
@@ -76,6 +77,9 @@ def lib():
         L.cgtp_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
         L.cgtp_double_backward_workspace.argtypes = [vp, i64, ctypes.POINTER(i64)]
         L.cgtp_double_backward.argtypes = [vp] * 12 + [i64, vp, i64, vp]
+        L.cgtp_conv_forward_sh.argtypes = [vp] * 7
+        L.cgtp_conv_backward_sh.argtypes = [vp] * 11
+        L.cgtp_real_sh.argtypes = [i32, vp, i64, vp, vp]
         for name in EXPORTS:
             if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
                 getattr(L, name).restype = i32
@@ -86,6 +90,18 @@ def lib():
 def _check(status):
     if status != CGTP_OK:
         raise CgtpError(status, lib().cgtp_last_error().decode())
+
+
+def cgtp_real_sh(lmax, rvec, jacobian=False):
+    """Host query of the library's real spherical harmonics of the (normalised)
+    vectors rvec [n,3]: Y [n,(lmax+1)^2] and, optionally, dY/drvec [n,(lmax+1)^2,3]."""
+    r = np.ascontiguousarray(rvec, dtype=np.float64).reshape(-1, 3)
+    d2 = (lmax + 1) ** 2
+    Y = np.zeros((r.shape[0], d2))
+    dY = np.zeros((r.shape[0], d2, 3)) if jacobian else None
+    _check(lib().cgtp_real_sh(lmax, r.ctypes.data, r.shape[0], Y.ctypes.data,
+                              dY.ctypes.data if jacobian else None))
+    return (Y, dY) if jacobian else Y
 
 
 def cgtp_real_cg_block(l1, l2, l3):
@@ -293,3 +309,28 @@ def cgtp_double_backward(plan, gout, x1, x2, W, gg1, gg2, ggW, stream=None):
         _ptr(d_1, "d_x1"), _ptr(d_2, "d_x2"), _ptr(d_W, "d_W"), B, _ptr(ws, "workspace"), nb.value,
         _stream(stream)))
     return d_g, d_1, d_2, d_W
+
+
+def cgtp_conv_forward_sh(plan, graph, x, rvec, W, out=None, stream=None):
+    """Fused convolution whose edge harmonics are evaluated in the kernel from rvec [E,3]."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.out_dtype, device=x.device)
+    dt = plan.dtype
+    _check(lib().cgtp_conv_forward_sh(plan.handle, graph.handle, _ptr(x, "x", dt), _ptr(rvec, "rvec", dt),
+                                      _ptr(W, "W", dt), _ptr(out, "out", plan.out_dtype), _stream(stream)))
+    return out
+
+
+def cgtp_conv_backward_sh(plan, graph, gout, x, rvec, W, stream=None):
+    """Adjoint of cgtp_conv_forward_sh: (gx, gY, grvec, gW)."""
+    torch = _torch()
+    dt = plan.dtype
+    gx = torch.empty(x.shape, dtype=plan.out_dtype, device=x.device)
+    gY = torch.empty(graph.E, plan.d2, dtype=plan.out_dtype, device=x.device)
+    grvec = torch.empty(rvec.shape, dtype=plan.out_dtype, device=x.device)
+    gW = torch.empty(W.shape, dtype=plan.out_dtype, device=x.device)
+    _check(lib().cgtp_conv_backward_sh(plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt),
+                                       _ptr(rvec, "rvec", dt), _ptr(W, "W", dt), _ptr(gx, "gx"), _ptr(gY, "gY"),
+                                       _ptr(grvec, "grvec"), _ptr(gW, "gW"), _stream(stream)))
+    return gx, gY, grvec, gW

@@ -192,12 +192,14 @@ cgtp_status launch_uvu_backward(const cgtp_plan_s* plan, const LayoutDev& lay, c
 // uvu3.cu
 cgtp_status build_v3(cgtp_plan_s* plan);
 void free_v3(cgtp_plan_s* plan);
+// rvec: edge vectors [E,3] whose harmonics replace Y (null: read Y)
 bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
-                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st);
+                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st,
+                       const void* rvec = nullptr);
 bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
-                        cgtp_status* st);
+                        cgtp_status* st, const void* rvec = nullptr);
 
 // bt.cu (batched product without a graph; return false when the plan does not qualify)
 cgtp_status bt_create(cgtp_plan_s* plan);

@@ -18,6 +18,13 @@ template <typename T, int LPE>
 cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
+template <typename T, int LPE>
+cgtp_status fwd3_launch_sh(const cgtp_plan_s* plan, const void* x, const void* rvec, const void* W, void* out,
+                           const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
+template <typename T, int LPE>
+cgtp_status bwd3_launch_sh(const cgtp_plan_s* plan, const void* gout, const void* x, const void* rvec,
+                           const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
+                           const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
 template <int LPE>
 cgtp_status fwd3_launch_bf16(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
                              const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
@@ -149,7 +156,8 @@ void free_v3(cgtp_plan_s* plan) {
 }
 
 bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
-                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st) {
+                       const int32_t* rowptr, const int32_t* col, int64_t N, void* stream, cgtp_status* st,
+                       const void* rvec) {
   using namespace uvu3_detail;
   if (!plan->v3.lpe) return false;
   if ((int64_t)plan->v3.n_items * N >= (int64_t(1) << 31)) {  // the kernels' 32-bit work counters
@@ -166,8 +174,19 @@ bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, co
       default: return false;
     }
   }
-  if (std::getenv("CGTP_UVU_NO_V3")) return false;
   const bool f64 = plan->dtype == CGTP_F64;
+  if (rvec) {  // edge vectors: the harmonics are evaluated in the kernels
+    switch (plan->v3.lpe) {
+      case 2: *st = f64 ? fwd3_launch_sh<double, 2>(plan, x, rvec, W, out, rowptr, col, N, s)
+                        : fwd3_launch_sh<float, 2>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
+      case 8: *st = f64 ? fwd3_launch_sh<double, 8>(plan, x, rvec, W, out, rowptr, col, N, s)
+                        : fwd3_launch_sh<float, 8>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
+      case 32: *st = f64 ? fwd3_launch_sh<double, 32>(plan, x, rvec, W, out, rowptr, col, N, s)
+                         : fwd3_launch_sh<float, 32>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
+      default: return false;
+    }
+  }
+  if (std::getenv("CGTP_UVU_NO_V3")) return false;
   switch (plan->v3.lpe) {
     case 2: *st = f64 ? fwd3_launch<double, 2>(plan, x, Y, W, out, rowptr, col, N, s)
                       : fwd3_launch<float, 2>(plan, x, Y, W, out, rowptr, col, N, s); return true;
@@ -182,7 +201,7 @@ bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, co
 bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
-                        cgtp_status* st) {
+                        cgtp_status* st, const void* rvec) {
   using namespace uvu3_detail;
   if (!plan->v3.lpe) return false;
   if ((int64_t)plan->v3.n_items * N >= (int64_t(1) << 31)) {  // the kernels' 32-bit work counters
@@ -201,8 +220,18 @@ bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
     }
 #undef V3BB
   }
-  if (std::getenv("CGTP_UVU_NO_V3")) return false;
   const bool f64 = plan->dtype == CGTP_F64;
+  if (rvec) {  // edge vectors: the harmonics are evaluated in the kernels
+#define V3S(T, L) bwd3_launch_sh<T, L>(plan, gout, x, rvec, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
+    switch (plan->v3.lpe) {
+      case 2: *st = f64 ? V3S(double, 2) : V3S(float, 2); return true;
+      case 8: *st = f64 ? V3S(double, 8) : V3S(float, 8); return true;
+      case 32: *st = f64 ? V3S(double, 32) : V3S(float, 32); return true;
+      default: return false;
+    }
+#undef V3S
+  }
+  if (std::getenv("CGTP_UVU_NO_V3")) return false;
 #define V3B(T, L) bwd3_launch<T, L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
   switch (plan->v3.lpe) {
     case 2: *st = f64 ? V3B(double, 2) : V3B(float, 2); return true;

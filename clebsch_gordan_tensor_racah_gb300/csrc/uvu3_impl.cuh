@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "sh.cuh"
 
 namespace cgtp {
 namespace uvu3_detail {
@@ -107,6 +108,7 @@ struct Uvu3Args {
   const S* Y;
   const S* W;
   const S* gout;
+  const T* rvec;          // non-null: edge vectors [E,3]; Y is evaluated from them (in2 = SH 0..L)
   T* out;
   T* gx;
   T* gY;
@@ -168,6 +170,22 @@ __device__ __forceinline__ double ld1(const double* p) { return __ldg(p); }
 __device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
   return __uint_as_float(static_cast<unsigned>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
 }
+// Edge features of edge e for one path: Y[e][off2 .. off2 + D2), or, in the
+// edge-vector kernels (SH = true, Y then points at the vectors [E,3]), the
+// degree-L2 harmonics of the normalised vector evaluated here.
+template <int L2, typename T, bool SH, typename S>
+__device__ __forceinline__ void edge_y(const S* __restrict__ Y, int e, int d2, int off2, T (&yv)[2 * L2 + 1]) {
+  if constexpr (SH) {
+    const T* r = reinterpret_cast<const T*>(Y) + 3 * (size_t)e;
+    const T rx = __ldg(r), ry = __ldg(r + 1), rz = __ldg(r + 2);
+    const T n2 = rx * rx + ry * ry + rz * rz;
+    const T inv = n2 > T(0) ? T(1) / sqrt(n2) : T(0);
+    sh_block<L2, T, T>(rx * inv, ry * inv, rz * inv, yv);
+  } else {
+#pragma unroll
+    for (int m = 0; m < 2 * L2 + 1; ++m) yv[m] = ld1(Y + (size_t)e * d2 + off2 + m);
+  }
+}
 
 // Rows [nb, ne) of a CTA split into contiguous warp ranges of about equal work
 // (edges + rows): warp w gets [lo, hi).
@@ -196,15 +214,14 @@ struct FwdEdge {  // one edge's operands, loaded before any arithmetic
   T wv[4];
 };
 
-template <typename T, int LPE, int L1, int L2, int L3, typename S>
+template <typename T, int LPE, int L1, int L2, int L3, bool SH, typename S>
 __device__ __forceinline__ void fwd3_load(FwdEdge<T, 2 * L1 + 1, 2 * L2 + 1, 2 * L3 + 1>& E,
                                           const S* __restrict__ x, const S* __restrict__ Y,
                                           const S* __restrict__ W, int e, int s, bool ok, int d1,
                                           int d2, int w_numel, int off1, int off2, int woff, int u) {
   constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1;
   if (ok) {
-#pragma unroll
-    for (int m = 0; m < D2; ++m) E.yv[m] = ld1(Y + (size_t)e * d2 + off2 + m);
+    edge_y<L2, T, SH>(Y, e, d2, off2, E.yv);
     ldvec<T, 4 * D1>(x + (size_t)s * d1 + off1 + u * D1, E.xs);
     ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, E.wv);
   } else {
@@ -242,7 +259,7 @@ __device__ __forceinline__ void fwd3_math(const FwdEdge<T, 2 * L1 + 1, 2 * L2 + 
 
 // forward: one (receiver, path, 4*LPE-channel block) per call, all 32 lanes;
 // each lane walks its edge slot two edges at a time, loads first
-template <typename T, int LPE, int L1, int L2, int L3, typename S>
+template <typename T, int LPE, int L1, int L2, int L3, bool SH, typename S>
 __device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restrict__ Y,
                                        const S* __restrict__ W, T* __restrict__ out,
                                        const int* __restrict__ col, int e_begin, int deg, int n,
@@ -261,8 +278,8 @@ __device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restr
       const int ea = e_begin + ja, eb = e_begin + (okb ? jb : ja);
       const int sa = __ldg(col + ea), sb = __ldg(col + eb);
       FwdEdge<T, D1, D2, D3> A, B;
-      fwd3_load<T, LPE, L1, L2, L3>(A, x, Y, W, ea, sa, true, d1, d2, w_numel, off1, off2, woff, u);
-      fwd3_load<T, LPE, L1, L2, L3>(B, x, Y, W, eb, sb, okb, d1, d2, w_numel, off1, off2, woff, u);
+      fwd3_load<T, LPE, L1, L2, L3, SH>(A, x, Y, W, ea, sa, true, d1, d2, w_numel, off1, off2, woff, u);
+      fwd3_load<T, LPE, L1, L2, L3, SH>(B, x, Y, W, eb, sb, okb, d1, d2, w_numel, off1, off2, woff, u);
       fwd3_math<T, LPE, L1, L2, L3>(A, t01, t23);
       fwd3_math<T, LPE, L1, L2, L3>(B, t01, t23);
     }
@@ -298,14 +315,15 @@ __device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restr
 #define CGTP3_FWD_CASE(L1, L2, L3)                                                                  \
   case (L1)*16 + (L2)*4 + (L3):                                                                     \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      fwd3_item<T, LPE, L1, L2, L3>(a.x, a.Y, a.W, a.out, a.col, e_begin, deg, n, a.d1, a.d2, a.d_out, \
+      fwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.out, a.col, e_begin, deg, n, a.d1, a.d2, a.d_out, \
                                     a.w_numel, p.off1, p.off2, p.ooff, p.woff, u, active, g);      \
     break;
 
-template <typename T, int LPE, typename S = T>
+template <typename T, int LPE, typename S = T, bool SH = false>
 __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3Args<T, S> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
+  const S* Yp = SH ? reinterpret_cast<const S*>(a.rvec) : a.Y;   // edge vectors or harmonics
   __shared__ int s_range[2];
   if (tid == 0) {
     const long long total = (long long)a.rowptr[a.N] + a.N;
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
 //   cy, t = cy.x -> gW (stored), gx partial (registers);
 //   h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over the path's
 //   lanes -> read-modify-write of gY (this warp owns the edge in this phase)
-template <typename T, int LPE, int L1, int L2, int L3, typename S>
+template <typename T, int LPE, int L1, int L2, int L3, bool SH, typename S>
 __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restrict__ Y,
                                        const S* __restrict__ W, const S* __restrict__ gout,
                                        T* __restrict__ gW, const int* __restrict__ t_eid,
@@ -395,8 +413,7 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
     if (valid) {
       e = __ldg(t_eid + te_begin + j);
       const int d = __ldg(t_dst + te_begin + j);
-#pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = ld1(Y + (size_t)e * d2 + off2 + m);
+      edge_y<L2, T, SH>(Y, e, d2, off2, yv);
       ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
       ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
     } else {
@@ -488,15 +505,16 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
 #define CGTP3_BWD_CASE(L1, L2, L3)                                                                   \
   case (L1)*16 + (L2)*4 + (L3):                                                                      \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      bwd3_item<T, LPE, L1, L2, L3>(a.x, a.Y, a.W, a.gout, a.gW, a.col, a.t_dst, te0, cnt, s, a.d1,  \
+      bwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.gout, a.gW, a.col, a.t_dst, te0, cnt, s, a.d1,  \
                                     a.d2, a.d_out, a.w_numel, p.off1, p.off2, p.ooff, p.woff, u,     \
                                     active, g, q, a.gY, a.gx);                                       \
     break;
 
-template <typename T, int LPE, typename S = T>
+template <typename T, int LPE, typename S = T, bool SH = false>
 __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3Args<T, S> a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
+  const S* Yp = SH ? reinterpret_cast<const S*>(a.rvec) : a.Y;   // edge vectors or harmonics
   __shared__ int s_range[2];
   if (tid == 0) {
     const long long total = (long long)a.rowptr[a.N] + a.N;

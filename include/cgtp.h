@@ -220,6 +220,33 @@ cgtp_status cgtp_double_backward(cgtp_plan plan, const void* gout, const void* x
                                  void* d_gout, void* d_x1, void* d_x2, void* d_W, int64_t B,
                                  void* workspace, int64_t workspace_size, void* stream);
 
+/*
+ * cgtp_conv_forward_sh / cgtp_conv_backward_sh -- the uvu convolution fed by raw
+ * edge vectors ("An Efficient Sparse Kernel Generator ...", Figure 4B: the edge
+ * features are spherical harmonics of the edge directions).  The kernels
+ * evaluate Y[e] = Y(rvec[e] / |rvec[e]|) (component normalisation, the
+ * convention of cgtp_real_sh) as each edge is loaded, so no Y tensor is read.
+ *  rvec [E,3] : DEVICE edge vectors (any length; a zero vector gives zero
+ *      gradient), element type of the plan (CGTP_F32 or CGTP_F64).
+ *  Other tensors as for cgtp_conv_forward / cgtp_conv_backward.  The backward
+ *  also returns gY [E,d2] (the gradient with respect to the harmonics, which
+ *  the caller provides as storage) and grvec [E,3] = dL/drvec.
+ *  Needs irreps_in2 = 0e+1o+2e+... (harmonics 0..L in order, L <= 3) and a
+ *  plan the fused l <= 3 kernels serve (one in1 multiplicity m with m/4 in
+ *  {2, 8, 32} or m a multiple of 128); otherwise CGTP_EUNSUPPORTED.
+ */
+cgtp_status cgtp_conv_forward_sh(cgtp_plan plan, cgtp_graph graph, const void* x, const void* rvec,
+                                 const void* W, void* out, void* stream);
+cgtp_status cgtp_conv_backward_sh(cgtp_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                                  const void* rvec, const void* W, void* gx, void* gY, void* grvec,
+                                  void* gW, void* stream);
+
+/* Host only: the library's real spherical harmonics (component normalisation,
+ * m = -l..l, l = 1 is sqrt(3) (y, z, x)) of n vectors rvec [n,3] after
+ * normalisation: Y [n, (lmax+1)^2], and if dY is not NULL the Jacobian
+ * dY [n, (lmax+1)^2, 3] = d Y / d rvec.  lmax <= 7. */
+cgtp_status cgtp_real_sh(int lmax, const double* rvec, int64_t n, double* Y, double* dY);
+
 /* Host only (no device needed): the planner's real-basis, component-normalised
  * CG block of (l1, l2, l3), l <= 7, as (2l1+1)(2l2+1)(2l3+1) doubles in
  * [m1][m2][m3] order; zeros if the triangle rule fails.  Same routine the plan

@@ -176,6 +176,35 @@ def wigner_d_real(l, axis, angle):
     return D.real
 
 
+def sh_real_jacobian(l, rvec):
+    """d Y_l(r / |r|) / d r for vectors rvec [n, 3]: shape [n, 2l+1, 3].
+
+    Exact, from the rotation generators: for the rotation R_a(t) about axis a,
+    d/dt Y_l(R_a(t) u) at t = 0 equals G_a Y_l(u) with G_a = d/dt D_l(R_a(t)) =
+    Q conj(-i J_a) Q^dagger (wigner_d_real at first order).  The same derivative
+    is grad Y . (e_a x u) = e_a . (u x grad Y), so the tangential gradient t of
+    Y on the sphere obeys u x t = w with w_a = G_a Y_l(u), hence t = -u x w;
+    d/dr = t / |r| (the radial direction does not change Y(r/|r|)).
+    """
+    r = np.asarray(rvec, float)
+    n = np.linalg.norm(r, axis=1)
+    u = r / n[:, None]
+    Y = sh_real(l, u)                                     # [n, 2l+1]
+    Q = real_basis(l)
+    w = np.zeros(Y.shape + (3,))
+    for a, Ja in enumerate(_angular_momentum(l)):
+        G = Q @ np.conj(-1j * Ja) @ Q.conj().T
+        assert np.abs(G.imag).max() < 1e-12
+        w[..., a] = Y @ G.real.T                           # (G_a Y)_m
+    t = -np.cross(u[:, None, :], w)                        # [n, 2l+1, 3]
+    return t / n[:, None, None]
+
+
+def sh_real_concat_jacobian(lmax, rvec):
+    """Jacobian of sh_real_concat(lmax, r / |r|) with respect to r: [n, (lmax+1)^2, 3]."""
+    return np.concatenate([sh_real_jacobian(l, rvec) for l in range(lmax + 1)], axis=1)
+
+
 def wigner_d_lstsq(l, R, rng):
     """Real Wigner-D by least squares: the D with Y_l(R r) = D Y_l(r) on random r."""
     pts = rng.normal(size=(4 * (2 * l + 1) + 8, 3))

@@ -33,7 +33,7 @@ output block i_out::
 
 import numpy as np
 
-from .cg import real_cg_block
+from .cg import real_cg_block, sh_real_concat, sh_real_concat_jacobian
 from .graph import csr_dst
 
 
@@ -313,3 +313,27 @@ def tp_uvu_double_backward(plan, g, x1, x2, W, gg1, gg2, ggW):
     bwd = lambda g_, a_, b_, w_: tp_uvu_backward(plan, g_, a_, b_, w_)
     return _double_backward(fwd, bwd, _f64(g), [_f64(x1), _f64(x2), _f64(W)],
                             [_f64(gg1), _f64(gg2), _f64(ggW)])
+
+
+# ---------------------------------------------------------------------------
+# convolution fed by raw edge vectors
+# ---------------------------------------------------------------------------
+# Figure 4B: the edge features are the spherical harmonics of the edge
+# directions, Y[e] = sh_real_concat(L, rvec[e] / |rvec[e]|) with in2 = 0e+1o+...;
+# the gradient with respect to rvec is the chain rule through that map.
+
+def conv_uvu_forward_sh(plan, x, rvec, W, rowptr, col):
+    lmax = len(plan.in2) - 1
+    r = _f64(rvec)
+    Y = sh_real_concat(lmax, r / np.linalg.norm(r, axis=1, keepdims=True))
+    return conv_uvu_forward(plan, x, Y, W, rowptr, col)
+
+
+def conv_uvu_backward_sh(plan, g, x, rvec, W, rowptr, col):
+    """(gx, gY, grvec, gW): gY is the gradient with respect to the harmonics."""
+    lmax = len(plan.in2) - 1
+    r = _f64(rvec)
+    Y = sh_real_concat(lmax, r / np.linalg.norm(r, axis=1, keepdims=True))
+    gx, gY, gW = conv_uvu_backward(plan, g, x, Y, W, rowptr, col)
+    grvec = np.einsum("ec,eck->ek", gY, sh_real_concat_jacobian(lmax, r))
+    return gx, gY, grvec, gW

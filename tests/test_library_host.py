@@ -86,3 +86,14 @@ def test_null_handles_rejected():
     assert L.cgtp_conv_forward(None, None, None, None, None, None, None, None) == cg.CGTP_EINVAL
     assert L.cgtp_forward(None, None, None, None, None, 0, None) == cg.CGTP_EINVAL
     assert L.cgtp_plan_info(None, None, None, None, None, None) == cg.CGTP_EINVAL
+
+
+def test_library_sh_matches_oracle():
+    # the harmonics the kernels evaluate from edge vectors (host build of the same
+    # code) against the oracle's scipy-based ones, values and Jacobian, l <= 7
+    rng = np.random.default_rng(41)
+    r = rng.normal(size=(60, 3)) * rng.uniform(0.1, 5.0, size=(60, 1))
+    Y, dY = cg.cgtp_real_sh(7, r, jacobian=True)
+    u = r / np.linalg.norm(r, axis=1, keepdims=True)
+    assert np.abs(Y - ocg.sh_real_concat(7, u)).max() < 1e-12
+    assert np.abs(dY - ocg.sh_real_concat_jacobian(7, r)).max() < 1e-11

@@ -162,3 +162,21 @@ def test_real_block_orthogonality():
                     continue
                 dot = (a * b).sum()
                 assert abs(dot - (1.0 if i == j else 0.0)) < 1e-13
+
+
+def test_sh_jacobian_against_finite_differences():
+    # the generator-based Jacobian of Y(r/|r|) against central differences of
+    # sh_real itself (any length of r, every l <= 7)
+    rng = np.random.default_rng(31)
+    r = rng.normal(size=(25, 3)) * rng.uniform(0.2, 4.0, size=(25, 1))
+    h = 1e-6
+    f = lambda rr: cg.sh_real_concat(7, rr / np.linalg.norm(rr, axis=1, keepdims=True))  # noqa: E731
+    J = cg.sh_real_concat_jacobian(7, r)
+    for k in range(3):
+        rp, rm = r.copy(), r.copy()
+        rp[:, k] += h
+        rm[:, k] -= h
+        fd = (f(rp) - f(rm)) / (2 * h)
+        assert np.abs(J[:, :, k] - fd).max() < 1e-7 * max(1.0, np.abs(fd).max())
+    # radial direction does not change the harmonics
+    assert np.abs(np.einsum("eck,ek->ec", J, r)).max() < 1e-12

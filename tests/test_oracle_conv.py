@@ -344,3 +344,25 @@ def test_double_backward_exact_directional_differences(mode):
             aj[j] = a[j] + dj
             lhs = S(g, aj) - base
             assert abs(lhs - (d[1 + j] * dj).sum()) <= 1e-10 * (abs(lhs) + abs(base) + 1.0), (mode, j)
+
+
+def test_edge_vector_conv_gradient_finite_differences():
+    # grvec of the edge-vector convolution against central differences of <g, out>
+    rng = np.random.default_rng(37)
+    plan = irreps.make_plan("2x0e+1x1o+1x2e", "0e+1o+2e", wl._all_out(2), mode="uvu")
+    N, E = 4, 9
+    rowptr, col = small_graph(rng, N, E)
+    x = rng.normal(size=(N, plan.d1))
+    r = rng.normal(size=(E, 3)) * rng.uniform(0.5, 2.0, size=(E, 1))
+    W = rng.normal(size=(E, plan.w_numel))
+    g = rng.normal(size=(N, plan.d_out))
+    f = lambda rr: (g * conv.conv_uvu_forward_sh(plan, x, rr, W, rowptr, col)).sum()  # noqa: E731
+    _, _, grvec, _ = conv.conv_uvu_backward_sh(plan, g, x, r, W, rowptr, col)
+    h = 1e-6
+    for e in range(E):
+        for k in range(3):
+            rp, rm = r.copy(), r.copy()
+            rp[e, k] += h
+            rm[e, k] -= h
+            fd = (f(rp) - f(rm)) / (2 * h)
+            assert abs(fd - grvec[e, k]) < 1e-7 * max(1.0, abs(fd)), (e, k, fd, grvec[e, k])
