@@ -35,7 +35,8 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_real_cg_block", "cgtp_last_error", "cgtp_graph_transpose_noalloc",
            "cgtp_conv_double_backward_workspace", "cgtp_conv_double_backward",
            "cgtp_double_backward_workspace", "cgtp_double_backward",
-           "cgtp_conv_forward_sh", "cgtp_conv_backward_sh", "cgtp_real_sh"]
+           "cgtp_conv_forward_sh", "cgtp_conv_backward_sh", "cgtp_real_sh",
+           "cgtp_conv_forward_sh_radial", "cgtp_conv_backward_sh_radial"]
 
 
 class CgtpError(RuntimeError):
@@ -80,6 +81,9 @@ def lib():
         L.cgtp_conv_forward_sh.argtypes = [vp] * 7
         L.cgtp_conv_backward_sh.argtypes = [vp] * 11
         L.cgtp_real_sh.argtypes = [i32, vp, i64, vp, vp]
+        dbl = ctypes.c_double
+        L.cgtp_conv_forward_sh_radial.argtypes = [vp] * 5 + [dbl, dbl, vp, vp]
+        L.cgtp_conv_backward_sh_radial.argtypes = [vp] * 6 + [dbl, dbl] + [vp] * 6
         for name in EXPORTS:
             if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
                 getattr(L, name).restype = i32
@@ -334,3 +338,31 @@ def cgtp_conv_backward_sh(plan, graph, gout, x, rvec, W, stream=None):
                                        _ptr(rvec, "rvec", dt), _ptr(W, "W", dt), _ptr(gx, "gx"), _ptr(gY, "gY"),
                                        _ptr(grvec, "grvec"), _ptr(gW, "gW"), _stream(stream)))
     return gx, gY, grvec, gW
+
+
+def cgtp_conv_forward_sh_radial(plan, graph, x, rvec, M, rbf_lo=0.5, rbf_hi=5.0, out=None, stream=None):
+    """uvw radial convolution whose harmonics and radial basis are evaluated in the kernels."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.out_dtype, device=x.device)
+    dt = plan.dtype
+    _check(lib().cgtp_conv_forward_sh_radial(plan.handle, graph.handle, _ptr(x, "x", dt), _ptr(rvec, "rvec", dt),
+                                             _ptr(M, "M", dt), float(rbf_lo), float(rbf_hi),
+                                             _ptr(out, "out", plan.out_dtype), _stream(stream)))
+    return out
+
+
+def cgtp_conv_backward_sh_radial(plan, graph, gout, x, rvec, M, rbf_lo=0.5, rbf_hi=5.0, stream=None):
+    """Adjoint of cgtp_conv_forward_sh_radial: (gx, gY, gR, grvec, gM)."""
+    torch = _torch()
+    dt, od, dev = plan.dtype, plan.out_dtype, x.device
+    gx = torch.empty(x.shape, dtype=od, device=dev)
+    gY = torch.empty(graph.E, plan.d2, dtype=od, device=dev)
+    gR = torch.empty(graph.E, plan.radial_k, dtype=od, device=dev)
+    grvec = torch.empty(rvec.shape, dtype=od, device=dev)
+    gM = torch.empty(M.shape, dtype=od, device=dev)
+    _check(lib().cgtp_conv_backward_sh_radial(
+        plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(rvec, "rvec", dt),
+        _ptr(M, "M", dt), float(rbf_lo), float(rbf_hi), _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gR, "gR"),
+        _ptr(grvec, "grvec"), _ptr(gM, "gM"), _stream(stream)))
+    return gx, gY, gR, grvec, gM

@@ -215,10 +215,14 @@ cgtp_status graph_build(cgtp_graph_s* g, void* stream);
 // uvw.cu
 cgtp_status uvw_create(cgtp_plan_s* plan);
 void uvw_destroy(cgtp_plan_s* plan);
+// rvec non-null: Y and R are evaluated from the edge vectors (harmonics of the
+// direction, Gaussian radial basis of the length with centres lo..hi)
 cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x,
-                        const void* Y, const void* R, const void* M, void* out, void* stream);
+                        const void* Y, const void* R, const void* M, void* out, void* stream,
+                        const void* rvec = nullptr, double rbf_lo = 0.0, double rbf_hi = 0.0);
 cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* gout,
                          const void* x, const void* Y, const void* R, const void* M, void* gx,
-                         void* gY, void* gR, void* gM, void* stream);
+                         void* gY, void* gR, void* gM, void* stream, const void* rvec = nullptr,
+                         double rbf_lo = 0.0, double rbf_hi = 0.0);
 
 }  // namespace cgtp

@@ -69,6 +69,30 @@ __global__ void sh_grad_kernel(const T* __restrict__ rvec, const T* __restrict__
     sh_grad_edge<T>(rvec + 3 * e, gY + e * d2, lmax, grvec + 3 * e);
 }
 
+// uvw: the harmonic part plus the radial part sum_k gR_k dR_k/dd u, with
+// R_k(d) = exp(-gamma (d - lo - k step)^2)
+__global__ void sh_radial_grad_kernel(const float* __restrict__ rvec, const float* __restrict__ gY,
+                                      const float* __restrict__ gR, int d2, int lmax, int K, float lo,
+                                      float step, float gamma, int64_t E, float* __restrict__ grvec) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
+    float* o = grvec + 3 * e;
+    const float* r = rvec + 3 * e;
+    sh_grad_edge<float>(r, gY + e * d2, lmax, o);
+    const float d = sqrtf(r[0] * r[0] + r[1] * r[1] + r[2] * r[2]);
+    if (!(d > 0.f)) continue;
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float t = d - (lo + k * step);
+      s += gR[e * K + k] * (-2.f * gamma * t) * expf(-gamma * t * t);
+    }
+    const float inv = 1.f / d;
+    o[0] += s * r[0] * inv;
+    o[1] += s * r[1] * inv;
+    o[2] += s * r[2] * inv;
+  }
+}
+
 // in2 must be the harmonics 0..L in order (mul 1, parity (-1)^l): returns L or -1
 int sh_lmax(const cgtp_plan_s* plan) {
   for (size_t i = 0; i < plan->in2.size(); ++i) {
@@ -76,6 +100,14 @@ int sh_lmax(const cgtp_plan_s* plan) {
     if (r.mul != 1 || r.l != static_cast<int>(i) || r.p != ((i & 1) ? -1 : 1)) return -1;
   }
   return static_cast<int>(plan->in2.size()) - 1;
+}
+
+cgtp_status sh_radial_check(const cgtp_plan_s* plan, double lo, double hi) {
+  if (plan->mode != CGTP_UVW) return fail(CGTP_EUNSUPPORTED, "radial edge-vector input needs a uvw plan");
+  if (sh_lmax(plan) < 0)
+    return fail(CGTP_EUNSUPPORTED, "edge-vector input needs irreps_in2 = 0e+1o+2e+... (harmonics 0..L in order)");
+  if (!(hi > lo)) return fail(CGTP_EINVAL, "radial basis needs rbf_hi > rbf_lo");
+  return CGTP_OK;
 }
 
 cgtp_status sh_check(const cgtp_plan_s* plan) {
@@ -171,6 +203,46 @@ cgtp_status cgtp_conv_backward_sh(cgtp_plan plan, cgtp_graph g, const void* gout
   else
     sh_grad_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(rvec), static_cast<const float*>(gY),
                                                  static_cast<int>(plan->d2), lmax, g->E, static_cast<float*>(grvec));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, std::string("edge-vector gradient launch: ") + cudaGetErrorString(e));
+}
+
+cgtp_status cgtp_conv_forward_sh_radial(cgtp_plan plan, cgtp_graph g, const void* x, const void* rvec,
+                                        const void* M, double rbf_lo, double rbf_hi, void* out, void* stream) {
+  clear_error();
+  if (!plan || !g) return fail(CGTP_EINVAL, "null plan or graph");
+  cgtp_status s;
+  if ((s = sh_radial_check(plan, rbf_lo, rbf_hi))) return s;
+  if (!x || !M || !out || (g->E > 0 && !rvec)) return fail(CGTP_EINVAL, "null x, rvec, M or out");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(M) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return fail(CGTP_EINVAL, "x, M and out must be 16-byte aligned");
+  return uvw_forward(plan, g, x, nullptr, nullptr, M, out, stream, g->E > 0 ? rvec : nullptr, rbf_lo, rbf_hi);
+}
+
+cgtp_status cgtp_conv_backward_sh_radial(cgtp_plan plan, cgtp_graph g, const void* gout, const void* x,
+                                         const void* rvec, const void* M, double rbf_lo, double rbf_hi,
+                                         void* gx, void* gY, void* gR, void* grvec, void* gM, void* stream) {
+  clear_error();
+  if (!plan || !g) return fail(CGTP_EINVAL, "null plan or graph");
+  cgtp_status s;
+  if ((s = sh_radial_check(plan, rbf_lo, rbf_hi))) return s;
+  if (!gout || !x || !M || !gx || !gM || (g->E > 0 && (!rvec || !gY || !gR || !grvec)))
+    return fail(CGTP_EINVAL, "null operand");
+  if ((reinterpret_cast<uintptr_t>(gout) | reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(M) |
+       reinterpret_cast<uintptr_t>(gx) | reinterpret_cast<uintptr_t>(gY) | reinterpret_cast<uintptr_t>(gR) |
+       reinterpret_cast<uintptr_t>(gM)) & 15u)
+    return fail(CGTP_EINVAL, "tensors must be 16-byte aligned");
+  if ((s = uvw_backward(plan, g, gout, x, nullptr, nullptr, M, gx, gY, gR, gM, stream, g->E > 0 ? rvec : nullptr,
+                        rbf_lo, rbf_hi)))
+    return s;
+  if (g->E == 0) return CGTP_OK;
+  const int K = plan->radial_k;
+  const double step = K > 1 ? (rbf_hi - rbf_lo) / (K - 1) : (rbf_hi - rbf_lo);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((g->E + 255) / 256, (int64_t)plan->num_sms * 8)));
+  sh_radial_grad_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const float*>(rvec), static_cast<const float*>(gY), static_cast<const float*>(gR),
+      static_cast<int>(plan->d2), sh_lmax(plan), K, static_cast<float>(rbf_lo), static_cast<float>(step),
+      static_cast<float>(1.0 / (step * step)), g->E, static_cast<float*>(grvec));
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, std::string("edge-vector gradient launch: ") + cudaGetErrorString(e));
 }

@@ -34,6 +34,7 @@
 #include "internal.h"
 #include "uvu_impl.cuh"
 #include "uvu3_impl.cuh"
+#include "sh.cuh"
 
 namespace cgtp {
 namespace uvw_detail {
@@ -319,10 +320,22 @@ __global__ void splitk_reduce_kernel(float* __restrict__ gM, const float* __rest
 // ---------------------------------------------------------------------------
 // forward edge stage: S[n] for the receivers of one chunk
 // ---------------------------------------------------------------------------
+// Gaussian radial basis of the edge length d: R_k = exp(-gamma (d - lo - k step)^2)
+struct Rbf {
+  float lo, step, gamma;
+};
+__device__ __forceinline__ float rbf_k(const Rbf& b, float d, int k) {
+  const float t = d - (b.lo + k * b.step);
+  return expf(-b.gamma * t * t);
+}
+
 struct EdgeArgs {
   const float* x;
   const float* Y;
   const float* R;
+  const float* rvec;   // non-null: edge vectors [E,3]; Y and R are evaluated from them
+  Rbf rbf;
+  int lmax_sh;         // in2 = harmonics 0..lmax_sh (edge-vector mode)
   const float* g;      // backward: output gradient
   const float* Astate; // backward: A chunk
   float* state;        // fwd: S chunk; bwd: H chunk
@@ -427,13 +440,30 @@ __global__ void __launch_bounds__(kThreads) uvw_fwd_edge_kernel(const EdgeArgs a
       const int cnt = min(kEdgeChunk, e_end - e0);
       __syncthreads();
       for (int i = tid; i < cnt; i += kThreads) src_s[i] = a.col[e0 + i];
-      for (int i = tid; i < cnt * a.d2; i += kThreads) {
-        const int j = i / a.d2, c = i - j * a.d2;
-        Ys[j * d2p + c] = a.Y[(size_t)(e0 + j) * a.d2 + c];
-      }
-      for (int i = tid; i < cnt * a.K; i += kThreads) {
-        const int j = i / a.K, k = i - j * a.K;
-        Rs[j * 16 + k] = a.R[(size_t)(e0 + j) * a.K + k];
+      if (a.rvec) {  // harmonics and radial basis of the edge vectors, one thread per edge
+        for (int j = tid; j < cnt; j += kThreads) {
+          const float* r = a.rvec + 3 * (size_t)(e0 + j);
+          const float rx = r[0], ry = r[1], rz = r[2];
+          const float d = sqrtf(rx * rx + ry * ry + rz * rz), inv = d > 0.f ? 1.f / d : 0.f;
+          const float ux = rx * inv, uy = ry * inv, uz = rz * inv;
+          float* yj = Ys + j * d2p;
+          switch (a.lmax_sh) {
+            case 3: { float b[7]; sh_block<3, float, float>(ux, uy, uz, b); for (int m = 0; m < 7; ++m) yj[9 + m] = b[m]; } [[fallthrough]];
+            case 2: { float b[5]; sh_block<2, float, float>(ux, uy, uz, b); for (int m = 0; m < 5; ++m) yj[4 + m] = b[m]; } [[fallthrough]];
+            case 1: { float b[3]; sh_block<1, float, float>(ux, uy, uz, b); for (int m = 0; m < 3; ++m) yj[1 + m] = b[m]; } [[fallthrough]];
+            default: yj[0] = 1.f;
+          }
+          for (int k = 0; k < a.K; ++k) Rs[j * 16 + k] = rbf_k(a.rbf, d, k);
+        }
+      } else {
+        for (int i = tid; i < cnt * a.d2; i += kThreads) {
+          const int j = i / a.d2, c = i - j * a.d2;
+          Ys[j * d2p + c] = a.Y[(size_t)(e0 + j) * a.d2 + c];
+        }
+        for (int i = tid; i < cnt * a.K; i += kThreads) {
+          const int j = i / a.K, k = i - j * a.K;
+          Rs[j * 16 + k] = a.R[(size_t)(e0 + j) * a.K + k];
+        }
       }
       __syncthreads();
       for (int i = tid; i < cnt * cy_size; i += kThreads) {
@@ -494,8 +524,9 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
 // warp accumulates gR and gY in path order (deterministic, no atomics).
 // ---------------------------------------------------------------------------
 struct Bwd3Args {
-  const float* Y;
+  const float* Y;      // edge-vector mode: the vectors [E,3]
   const float* R;
+  Rbf rbf;
   const float* g;
   const float* Astate;  // [chunk][K][s_slice]
   float* Hstate;        // [chunk][K][s_slice]
@@ -511,8 +542,8 @@ struct Bwd3Args {
   int n_items;
 };
 
-template <int L1, int L2, int L3>
-__device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const float* __restrict__ Rp,
+template <int L1, int L2, int L3, bool SH>
+__device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const float* __restrict__ Rp, Rbf rbf,
                                            const float* __restrict__ gp_, const float* __restrict__ Astate,
                                            float* __restrict__ Hstate, float* __restrict__ gY,
                                            float* __restrict__ gR, const int* __restrict__ t_eid,
@@ -534,10 +565,18 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
   for (int t = tb; t < te; ++t) {
     const int e = __ldg(t_eid + t), d = __ldg(t_dst + t);
     float yv[D2], r[kKB], gv[D3];
+    if constexpr (SH) {  // Yp holds the edge vectors: harmonics and radial basis evaluated here
+      const float rx = __ldg(Yp + 3 * (size_t)e), ry = __ldg(Yp + 3 * (size_t)e + 1), rz = __ldg(Yp + 3 * (size_t)e + 2);
+      const float dd = sqrtf(rx * rx + ry * ry + rz * rz), inv = dd > 0.f ? 1.f / dd : 0.f;
+      sh_block<L2, float, float>(rx * inv, ry * inv, rz * inv, yv);
 #pragma unroll
-    for (int m = 0; m < D2; ++m) yv[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
+      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? rbf_k(rbf, dd, k) : 0.f;
+    } else {
 #pragma unroll
-    for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
+      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
+    }
     const float* gp = gp_ + (size_t)d * d_out + ooff + w * D3;
 #pragma unroll
     for (int m = 0; m < D3; ++m) gv[m] = active ? __ldg(gp + m) : 0.f;
@@ -584,13 +623,14 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
 #define UVW3_BWD_CASE(L1, L2, L3)                                                                  \
   case (L1)*16 + (L2)*4 + (L3):                                                                    \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      uvw_bwd3_unit<L1, L2, L3>(a.Y, a.R, a.g, a.Astate, a.Hstate, a.gY, a.gR, a.t_eid, a.t_dst,     \
+      uvw_bwd3_unit<L1, L2, L3, SH>(a.Y, a.R, a.rbf, a.g, a.Astate, a.Hstate, a.gY, a.gR, a.t_eid, a.t_dst,     \
                                 rp[s], rp[s + 1], (size_t)(s - a.n0) * a.s_node, a.d2, a.d_out, a.K,  \
                                 a.s_slice, p.off2, p.ooff, p.aoff, p.mul_out, item.u0, lane);        \
     break;
 
 constexpr int kBwd3Warps = 16;
 
+template <bool SH>
 __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const Bwd3Args a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int s_range[2];
@@ -951,8 +991,14 @@ static void refresh_error(const UvwState* st, cudaStream_t s) {
   cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s);
 }
 
+static Rbf make_rbf(int K, double lo, double hi) {
+  const double step = K > 1 ? (hi - lo) / (K - 1) : (hi - lo);
+  return Rbf{static_cast<float>(lo), static_cast<float>(step), static_cast<float>(1.0 / (step * step))};
+}
+
 cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x,
-                        const void* Y, const void* R, const void* M, void* out, void* stream) {
+                        const void* Y, const void* R, const void* M, void* out, void* stream,
+                        const void* rvec, double rbf_lo, double rbf_hi) {
   const UvwState* st = static_cast<const UvwState*>(plan->uvw);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cgtp_status e = sticky_error(st)) return e;
@@ -960,6 +1006,9 @@ cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const vo
   a.x = static_cast<const float*>(x);
   a.Y = static_cast<const float*>(Y);
   a.R = static_cast<const float*>(R);
+  a.rvec = static_cast<const float*>(rvec);
+  a.rbf = make_rbf(st->K, rbf_lo, rbf_hi);
+  a.lmax_sh = static_cast<int>(plan->in2.size()) - 1;
   a.rowptr = g->rowptr;
   a.col = g->col;
   a.state = st->scratch;
@@ -983,7 +1032,8 @@ cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const vo
 
 cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* gout,
                          const void* x, const void* Y, const void* R, const void* M, void* gx,
-                         void* gY, void* gR, void* gM, void* stream) {
+                         void* gY, void* gR, void* gM, void* stream, const void* rvec, double rbf_lo,
+                         double rbf_hi) {
   const UvwState* st = static_cast<const UvwState*>(plan->uvw);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cgtp_status e = sticky_error(st)) return e;
@@ -999,8 +1049,9 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
                                 tiles_for(plan, st, 1, nodes), s, st->err_dev);
     if (r != CGTP_OK) return r;
     Bwd3Args b{};
-    b.Y = static_cast<const float*>(Y);
+    b.Y = static_cast<const float*>(rvec ? rvec : Y);
     b.R = static_cast<const float*>(R);
+    b.rbf = make_rbf(st->K, rbf_lo, rbf_hi);
     b.g = static_cast<const float*>(gout);
     b.Astate = Abuf;
     b.Hstate = Hbuf;
@@ -1020,7 +1071,10 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     b.items = st->bwd3_items;
     b.n_items = st->bwd3_n_items;
     const int grid = std::min(nodes, plan->num_sms);
-    uvw_bwd_edge3_kernel<<<grid, kBwd3Warps * 32, 0, s>>>(b);
+    if (rvec)
+      uvw_bwd_edge3_kernel<true><<<grid, kBwd3Warps * 32, 0, s>>>(b);
+    else
+      uvw_bwd_edge3_kernel<false><<<grid, kBwd3Warps * 32, 0, s>>>(b);
     if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw backward edge stage launch failed");
     const float* post[6] = {nullptr, static_cast<const float*>(M),
                             static_cast<float*>(gx) + (size_t)n0 * plan->d1, xrows,

@@ -241,6 +241,24 @@ cgtp_status cgtp_conv_backward_sh(cgtp_plan plan, cgtp_graph graph, const void* 
                                   const void* rvec, const void* W, void* gx, void* gY, void* grvec,
                                   void* gW, void* stream);
 
+/*
+ * cgtp_conv_forward_sh_radial / cgtp_conv_backward_sh_radial -- the uvw radial
+ * convolution fed by raw edge vectors ("Sobek ...", Abstract: radial projection
+ * and spherical-harmonic coupling streamed together).  The kernels evaluate the
+ * harmonics Y(rvec/|rvec|) and the K Gaussian radial functions of d = |rvec|,
+ *   R_k(d) = exp(-gamma (d - mu_k)^2),  mu_k = rbf_lo + k step,
+ *   step = (rbf_hi - rbf_lo)/(K - 1) (K = 1: rbf_hi - rbf_lo),  gamma = 1/step^2,
+ * so neither Y nor R is read.  rvec [E,3] DEVICE float; M, x, out, gout, gx, gM
+ * as for cgtp_conv_forward / cgtp_conv_backward.  The backward also returns gY
+ * [E,d2] and gR [E,K] (caller storage) and grvec [E,3] = dL/drvec.  Needs a uvw
+ * plan with irreps_in2 = 0e+1o+2e+... and rbf_hi > rbf_lo.
+ */
+cgtp_status cgtp_conv_forward_sh_radial(cgtp_plan plan, cgtp_graph graph, const void* x, const void* rvec,
+                                        const void* M, double rbf_lo, double rbf_hi, void* out, void* stream);
+cgtp_status cgtp_conv_backward_sh_radial(cgtp_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                                         const void* rvec, const void* M, double rbf_lo, double rbf_hi,
+                                         void* gx, void* gY, void* gR, void* grvec, void* gM, void* stream);
+
 /* Host only: the library's real spherical harmonics (component normalisation,
  * m = -l..l, l = 1 is sqrt(3) (y, z, x)) of n vectors rvec [n,3] after
  * normalisation: Y [n, (lmax+1)^2], and if dY is not NULL the Jacobian

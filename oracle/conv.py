@@ -337,3 +337,37 @@ def conv_uvu_backward_sh(plan, g, x, rvec, W, rowptr, col):
     gx, gY, gW = conv_uvu_backward(plan, g, x, Y, W, rowptr, col)
     grvec = np.einsum("ec,eck->ek", gY, sh_real_concat_jacobian(lmax, r))
     return gx, gY, grvec, gW
+
+
+def radial_basis(d, K, lo, hi):
+    """Gaussian radial basis of edge lengths d [E] and its derivative, both [E, K]:
+    R_k = exp(-gamma (d - mu_k)^2), mu_k = lo + k step, step = (hi - lo)/(K - 1)
+    (K = 1: hi - lo), gamma = 1/step^2 (Sobek, Abstract: radial projection)."""
+    step = (hi - lo) / (K - 1) if K > 1 else (hi - lo)
+    t = np.asarray(d, float)[:, None] - (lo + step * np.arange(K))[None, :]
+    R = np.exp(-t * t / step ** 2)
+    return R, -2.0 * t / step ** 2 * R
+
+
+def conv_uvw_radial_forward_sh(plan, x, rvec, M, K, lo, hi, rowptr, col):
+    """uvw radial convolution with Y and R evaluated from the edge vectors."""
+    lmax = len(plan.in2) - 1
+    r = _f64(rvec)
+    d = np.linalg.norm(r, axis=1)
+    Y = sh_real_concat(lmax, r / d[:, None])
+    R, _ = radial_basis(d, K, lo, hi)
+    return conv_uvw_radial_forward(plan, x, Y, R, M, rowptr, col)
+
+
+def conv_uvw_radial_backward_sh(plan, g, x, rvec, M, K, lo, hi, rowptr, col):
+    """(gx, gY, gR, grvec, gM): chain rule through the harmonics of the direction and
+    the radial basis of the length."""
+    lmax = len(plan.in2) - 1
+    r = _f64(rvec)
+    d = np.linalg.norm(r, axis=1)
+    Y = sh_real_concat(lmax, r / d[:, None])
+    R, dR = radial_basis(d, K, lo, hi)
+    gx, gY, gR, gM = conv_uvw_radial_backward(plan, g, x, Y, R, M, rowptr, col)
+    grvec = np.einsum("ec,eck->ek", gY, sh_real_concat_jacobian(lmax, r))
+    grvec += ((gR * dR).sum(1) / d)[:, None] * r
+    return gx, gY, gR, grvec, gM

@@ -62,3 +62,21 @@ def test_edge_vector_conv_needs_harmonic_in2():
     with pytest.raises(cg.CgtpError) as e:
         cg.cgtp_conv_forward_sh(plan, graph, z, z, z, out=z)
     assert e.value.status == cg.CGTP_EUNSUPPORTED
+
+
+def test_radial_edge_vector_uvw_conv():
+    spec = wl.SPECS["uvw"]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvw")
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvw", torch.float32, radial_k=8)
+    w = wl.make("uvw", oplan.w_numel, seed=8, N=12)
+    rng = np.random.default_rng(9)
+    rvec = (rng.normal(size=(w["E"], 3)) * rng.uniform(0.6, 4.5, size=(w["E"], 1))).astype(np.float32)
+    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
+    out = cg.cgtp_conv_forward_sh_radial(plan, graph, T(w["x"]), T(rvec), T(w["M"]), 0.5, 5.0)
+    close("out", out, oconv.conv_uvw_radial_forward_sh(oplan, w["x"], rvec, w["M"], 8, 0.5, 5.0,
+                                                        w["rowptr"], w["col"]), np.float32)
+    g = rng.standard_normal((w["N"], oplan.d_out)).astype(np.float32)
+    got = cg.cgtp_conv_backward_sh_radial(plan, graph, T(g), T(w["x"]), T(rvec), T(w["M"]), 0.5, 5.0)
+    ref = oconv.conv_uvw_radial_backward_sh(oplan, g, w["x"], rvec, w["M"], 8, 0.5, 5.0, w["rowptr"], w["col"])
+    for nm, a, b in zip(("gx", "gY", "gR", "grvec", "gM"), got, ref):
+        close(nm, a, b, np.float32)

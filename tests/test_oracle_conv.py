@@ -366,3 +366,25 @@ def test_edge_vector_conv_gradient_finite_differences():
             rm[e, k] -= h
             fd = (f(rp) - f(rm)) / (2 * h)
             assert abs(fd - grvec[e, k]) < 1e-7 * max(1.0, abs(fd)), (e, k, fd, grvec[e, k])
+
+
+def test_radial_edge_vector_conv_gradient_finite_differences():
+    # uvw: grvec through both the harmonics of the direction and the radial basis of the length
+    rng = np.random.default_rng(43)
+    plan = irreps.make_plan("2x0e+1x1o+1x2e", "0e+1o+2e", "1x0e+2x1o+1x2e", mode="uvw")
+    N, E, K, lo, hi = 4, 8, 3, 0.5, 5.0
+    rowptr, col = small_graph(rng, N, E)
+    x = rng.normal(size=(N, plan.d1))
+    r = rng.normal(size=(E, 3)) * rng.uniform(0.7, 3.0, size=(E, 1))
+    M = rng.normal(size=(K, plan.w_numel))
+    g = rng.normal(size=(N, plan.d_out))
+    f = lambda rr: (g * conv.conv_uvw_radial_forward_sh(plan, x, rr, M, K, lo, hi, rowptr, col)).sum()  # noqa: E731
+    grvec = conv.conv_uvw_radial_backward_sh(plan, g, x, r, M, K, lo, hi, rowptr, col)[3]
+    h = 1e-6
+    for e in range(E):
+        for k in range(3):
+            rp, rm = r.copy(), r.copy()
+            rp[e, k] += h
+            rm[e, k] -= h
+            fd = (f(rp) - f(rm)) / (2 * h)
+            assert abs(fd - grvec[e, k]) < 1e-7 * max(1.0, abs(fd)), (e, k, fd, grvec[e, k])
