@@ -57,6 +57,7 @@ CONFIGS = {
     "highl": dict(name="highl", dtype="float32", over={}),
     "nequip_bf16": dict(name="nequip", dtype="bfloat16", over={}),
     "nequip_sh": dict(name="nequip", dtype="float32", over={}, sh=True),
+    "uvw_edge": dict(name="uvw_edge", dtype="float32", over={}),
     "uvw": dict(name="uvw", dtype="float32", over={}),
 }
 
@@ -116,7 +117,7 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     if "rowptr" in dev:
         N, E = w["N"], w["E"]
         x, Y = dev["x"], dev["Y"]
-        WR = dev["W"] if plan.mode == "uvu" else dev["R"]
+        WR = dev["W"] if "W" in dev else dev["R"]
         M = dev.get("M")
         units = E
         idx = 4 * (N + 1 + E)
@@ -168,6 +169,9 @@ def algorithmic_flops(plan, n_nodes, n_edges):
         if plan.mode == "uvu":
             fe += 2 * nnz + mul1 * (D1 + 2 * NF)
             be += 4 * nnz + mul1 * (6 * NF + 3 * D3)
+        elif K == 0:   # weights per edge: t = C.x.Y, then the [u][w] matrix per edge
+            fe += 2 * nnz + mul1 * 2 * NF + 2 * mul1 * mul_out * D3
+            be += 4 * nnz + mul1 * 4 * NF + 3 * 2 * mul1 * mul_out * D3 + 2 * mul1 * NF
         else:
             fe += 2 * nnz + mul1 * 2 * NF + 2 * K * mul1 * D3
             fn += 2 * K * mul1 * mul_out * D3
@@ -256,7 +260,7 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
         dt = time.perf_counter() - t0
         return units / dt, f"batches of {B} samples of the same recipe, fwd+bwd, {dt:.1f} s"
     # a smaller graph of the same recipe (same degree distribution and features)
-    N = {"tiny": 64, "nequip": 120, "mace": 60, "uvw": 4}[c["name"]]
+    N = {"tiny": 64, "nequip": 120, "mace": 60, "uvw": 4, "uvw_edge": 120}[c["name"]]
     w = wl.make(c["name"], oplan.w_numel, seed=0, dtype="float32" if c["dtype"] == "bfloat16" else c["dtype"], N=N)
     units, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
@@ -267,6 +271,9 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
         elif spec["mode"] == "uvu":
             out = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
             oconv.conv_uvu_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+        elif "W" in w:
+            out = oconv.conv_uvw_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+            oconv.conv_uvw_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
         else:
             out = oconv.conv_uvw_radial_forward(oplan, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
             oconv.conv_uvw_radial_backward(oplan, out, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
@@ -284,10 +291,10 @@ def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
     import clebsch_gordan_tensor_racah_gb300 as cg
     gen = torch.Generator(g.device).manual_seed(2)
     if "rowptr" in dev:
-        keys = ["x", "Y", "W"] if plan.mode == "uvu" else ["x", "Y", "R", "M"]
+        keys = ["x", "Y", "W"] if "W" in dev else ["x", "Y", "R", "M"]
         c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen) for k in keys}
-        WR = dev["W"] if plan.mode == "uvu" else dev["R"]
-        cWR = c["W"] if plan.mode == "uvu" else c["R"]
+        WR = dev["W"] if "W" in dev else dev["R"]
+        cWR = c["W"] if "W" in c else c["R"]
 
         def run():
             return cg.cgtp_conv_double_backward(plan, graph, g, dev["x"], dev["Y"], WR, c["x"], c["Y"], cWR,
@@ -343,7 +350,8 @@ def config_block(cfgkey, w, n_gpus):
                       "nequip": "NequIP-like uvu conv (10k nodes x 32 in-edges, 32x(0e,1o,2e,3o), SH l<=3)",
                       "mace": "MACE-like uvu conv (5k nodes, Poisson(40) in-degree, 128x(0e,1o,2e), SH l<=3)",
                       "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
-                      "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)"}[spec],
+                      "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)",
+                      "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))"}[spec],
          "step": "conv forward + backward" if "N" in w else "batched forward + backward",
          "precision": "bfloat16 inputs, FP32 arithmetic and outputs" if c["dtype"] == "bfloat16" else c["dtype"],
          "edge_features": "raw edge vectors, harmonics evaluated in the kernels" if c.get("sh") else "harmonics Y",
@@ -525,8 +533,10 @@ def main():
     t_hbm = dom_bytes / (pk["hbm_gbs"] * 1e9)
     t_alu = dom_flops / (alu_peak * 1e12)
     kname = {("uvu", "forward"): "uvu_forward3_kernel", ("uvu", "backward"): "uvu_backward3_kernel",
+             ("uvwe", "forward"): "uvwe_fwd_kernel", ("uvwe", "backward"): "uvwe_bwd_kernel",
              ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
-             ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[(plan.mode, dominant)]
+             ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[
+        ("uvwe" if plan.mode == "uvw" and plan.radial_k == 0 else plan.mode, dominant)]
     if "N" not in w:
         kname = {"forward": "bt_forward_kernel", "backward": "bt_backward_kernel"}[dominant]
     if t_hbm >= t_alu:

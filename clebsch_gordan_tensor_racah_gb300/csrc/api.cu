@@ -145,9 +145,11 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
   if (dtype != CGTP_F32 && dtype != CGTP_F64 && dtype != CGTP_BF16)
     return fail(CGTP_EINVAL, "dtype must be CGTP_F32, CGTP_F64 or CGTP_BF16");
   if (mode == CGTP_UVU && radial_k != 0) return fail(CGTP_EINVAL, "radial_k must be 0 in uvu mode");
-  if (mode == CGTP_UVW && (radial_k < 1 || radial_k > 16))
-    return fail(CGTP_EUNSUPPORTED, "uvw mode needs radial weights with 1 <= radial_k <= 16");
-  if (mode == CGTP_UVW && dtype != CGTP_F32) return fail(CGTP_EUNSUPPORTED, "uvw mode supports CGTP_F32 only");
+  if (mode == CGTP_UVW && (radial_k < 0 || radial_k > 16))
+    return fail(CGTP_EUNSUPPORTED, "uvw mode needs 0 <= radial_k <= 16 (0: one weight matrix per edge)");
+  if (mode == CGTP_UVW && radial_k > 0 && dtype != CGTP_F32)
+    return fail(CGTP_EUNSUPPORTED, "uvw mode with radial weights supports CGTP_F32 only");
+  if (mode == CGTP_UVW && dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "uvw mode has no CGTP_BF16 kernels");
   if (n_instr < 0 || (n_instr > 0 && !instr)) return fail(CGTP_EINVAL, "bad instruction list");
   cgtp_plan_s* p = new (std::nothrow) cgtp_plan_s();
   if (!p) return fail(CGTP_ENOMEM, "host allocation failed");
@@ -187,6 +189,8 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (s == CGTP_OK && dtype == CGTP_BF16 && !p->v3.lpe)
       s = fail(CGTP_EUNSUPPORTED, "CGTP_BF16 needs l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} "
                                   "or m a multiple of 128");
+  } else if (radial_k == 0) {
+    s = uvwe_create(p);
   } else {
     s = uvw_create(p);
   }
@@ -204,6 +208,7 @@ void cgtp_plan_destroy(cgtp_plan plan) {
   free_layout(&plan->batch_layout);
   free_v3(plan);
   bt_destroy(plan);
+  uvwe_destroy(plan);
   if (plan->uvw) uvw_destroy(plan);
   delete plan;
 }
@@ -333,6 +338,10 @@ cgtp_status cgtp_conv_forward(cgtp_plan plan, cgtp_graph g, const void* x, const
     return launch_uvu_forward(plan, plan->conv_layout, x, Y, W_or_R, out, g->rowptr, g->col, g->N,
                               false, stream);
   }
+  if (plan->radial_k == 0) {
+    if (M) return fail(CGTP_EINVAL, "M must be NULL for per-edge uvw weights");
+    return uvwe_forward(plan, g, x, Y, W_or_R, out, stream);
+  }
   if ((s = need(M, "M"))) return s;
   return uvw_forward(plan, g, x, Y, W_or_R, M, out, stream);
 }
@@ -351,6 +360,10 @@ cgtp_status cgtp_conv_backward(cgtp_plan plan, cgtp_graph g, const void* gout, c
     if (M || gM) return fail(CGTP_EINVAL, "M and gM must be NULL for a uvu plan");
     return launch_uvu_backward(plan, plan->conv_layout, gout, x, Y, W_or_R, gx, gY, gW_or_gR,
                                g->t_rowptr, g->t_eid, g->t_dst, g->N, false, stream);
+  }
+  if (plan->radial_k == 0) {
+    if (M || gM) return fail(CGTP_EINVAL, "M and gM must be NULL for per-edge uvw weights");
+    return uvwe_backward(plan, g, gout, x, Y, W_or_R, gx, gY, gW_or_gR, stream);
   }
   if ((s = need(M, "M")) || (s = need(gM, "gM"))) return s;
   return uvw_backward(plan, g, gout, x, Y, W_or_R, M, gx, gY, gW_or_gR, gM, stream);

@@ -50,7 +50,7 @@ int64_t al256(int64_t v) { return (v + 255) / 256 * 256; }
 int operand_sizes(const cgtp_plan_s* plan, int64_t rows, int64_t E, int64_t* sz) {
   sz[0] = rows * plan->d1;
   sz[1] = E * plan->d2;
-  if (plan->mode == CGTP_UVU) {
+  if (plan->mode == CGTP_UVU || plan->radial_k == 0) {   // weights per edge
     sz[2] = E * plan->w_numel;
     return 3;
   }
@@ -75,14 +75,14 @@ struct Calls {  // forward / backward through the public entry points, graph or 
   void* stream;
   cgtp_status fwd(const void* const* a, void* out) const {
     if (graph) return cgtp_conv_forward(const_cast<cgtp_plan_s*>(plan), graph, a[0], a[1], a[2],
-                                        plan->mode == CGTP_UVW ? a[3] : nullptr, out, stream);
+                                        plan->radial_k > 0 ? a[3] : nullptr, out, stream);
     return cgtp_forward(const_cast<cgtp_plan_s*>(plan), a[0], a[1], a[2], out, B, stream);
   }
   cgtp_status bwd(const void* g, const void* const* a, void* const* o) const {
     if (graph)
       return cgtp_conv_backward(const_cast<cgtp_plan_s*>(plan), graph, g, a[0], a[1], a[2],
-                                plan->mode == CGTP_UVW ? a[3] : nullptr, o[0], o[1], o[2],
-                                plan->mode == CGTP_UVW ? o[3] : nullptr, stream);
+                                plan->radial_k > 0 ? a[3] : nullptr, o[0], o[1], o[2],
+                                plan->radial_k > 0 ? o[3] : nullptr, stream);
     return cgtp_backward(const_cast<cgtp_plan_s*>(plan), g, a[0], a[1], a[2], o[0], o[1], o[2], B, stream);
   }
 };
@@ -164,7 +164,8 @@ cgtp_status cgtp_conv_double_backward(cgtp_plan plan, cgtp_graph graph, const vo
                                       int64_t workspace_size, void* stream) {
   clear_error();
   if (!plan || !graph) return fail(CGTP_EINVAL, "null plan or graph");
-  if (plan->mode == CGTP_UVU && (M || ggM || d_M)) return fail(CGTP_EINVAL, "M, ggM and d_M must be NULL for a uvu plan");
+  if (plan->radial_k == 0 && (M || ggM || d_M))
+    return fail(CGTP_EINVAL, "M, ggM and d_M must be NULL for per-edge weights");
   const void* a[4] = {x, Y, W_or_R, M};
   const void* cot[4] = {ggx, ggY, ggW_or_ggR, ggM};
   void* d[4] = {d_x, d_Y, d_W_or_dR, d_M};

@@ -152,6 +152,8 @@ struct cgtp_plan_s {
   void* uvw = nullptr;
   // batched-product kernels for multiplicity 16 / 32 (bt.cu); null when the plan does not qualify
   void* bt = nullptr;
+  // uvw with a weight matrix per edge (radial_k == 0, uvwe.cu)
+  void* uvwe = nullptr;
 };
 
 struct cgtp_graph_s {
@@ -200,6 +202,14 @@ bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, void* stream,
                         cgtp_status* st, const void* rvec = nullptr);
+
+// uvwe.cu (uvw with per-edge weights W [E, w_numel])
+cgtp_status uvwe_create(cgtp_plan_s* plan);
+void uvwe_destroy(cgtp_plan_s* plan);
+cgtp_status uvwe_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x, const void* Y,
+                         const void* W, void* out, void* stream);
+cgtp_status uvwe_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* gout, const void* x,
+                          const void* Y, const void* W, void* gx, void* gY, void* gW, void* stream);
 
 // bt.cu (batched product without a graph; return false when the plan does not qualify)
 cgtp_status bt_create(cgtp_plan_s* plan);

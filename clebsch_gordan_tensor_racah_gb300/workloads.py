@@ -28,6 +28,9 @@ CSR sort, so draw i belongs to CSR position i):
 * ``uvw``    200,000 nodes, 32 in-edges each, senders uniform; in1 = out =
   64x(0e,1o,2e), SH l<=2, uvw, 8 radial functions of a length ~ U[0.5, 5],
   M ~ N(0,1)/sqrt(8*64) of shape [8, paths*64*64].
+* ``uvw_edge`` the NequIP-like graph (10,000 nodes x 32 in-edges) with
+  in1 = out = 16x(0e,1o,2e), SH l<=2, uvw with a weight matrix per edge,
+  W ~ N(0,1)/sqrt(32) of shape [E, paths*16*16].
 
 Every recipe takes overrides (``N``, ``deg``, ``E``, ``B``) so tests can draw a
 smaller instance with the same structure.
@@ -160,6 +163,9 @@ SPECS = {
                   dtype="float32"),
     "uvw": dict(in1="64x0e+64x1o+64x2e", in2=_sh_irreps(2), out="64x0e+64x1o+64x2e", mode="uvw",
                 lmax_sh=2, N=200_000, deg=32, graph="fixed", K=8, dtype="float32"),
+    # uvw with a weight matrix per edge (K = 0): 16x(0e,1o,2e) on the NequIP-like graph
+    "uvw_edge": dict(in1="16x0e+16x1o+16x2e", in2=_sh_irreps(2), out="16x0e+16x1o+16x2e", mode="uvw",
+                     lmax_sh=2, N=10_000, deg=32, graph="fixed", K=0, wscale="deg", dtype="float32"),
 }
 
 
@@ -206,7 +212,7 @@ def make(name, w_numel, seed=0, dtype=None, **over):
     Y = sh_real(spec["lmax_sh"], vec).astype(dt)
     x = _normal(rng, (N, d1), dt)
     res.update(rowptr=rowptr, col=col, N=N, E=E, x=x, Y=Y)
-    if spec["mode"] == "uvu":
+    if spec["mode"] == "uvu" or int(spec.get("K", 1)) == 0:   # weights per edge
         scale = 1.0 if spec["wscale"] is None else 1.0 / math.sqrt(float(spec["deg"]))
         W = _normal(rng, (E, int(w_numel)), dt, scale)
         res.update(W=W)

@@ -83,8 +83,11 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} or m a multiple
  *      of 128; other plans return CGTP_EUNSUPPORTED, and so do the batched and
  *      double-backward entry points.
- *  radial_k : 0 for uvu; for uvw the number K of radial functions (1..16); the
- *      weights are then W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
+ *  radial_k : 0 for uvu.  For uvw, 0 selects one weight matrix per edge,
+ *      W [E, sum_path mul1*mul_out] with each path's block laid out [u][w]
+ *      (FP32 or FP64, l <= 3; "An Efficient Sparse Kernel Generator ...",
+ *      Figure 3B/C), or the number K of radial functions (1..16), the weights
+ *      then being W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
  * the streaming node stage: node state for a chunk of nodes (default 4096,
  * overridable through the environment variable CGTP_UVW_CHUNK_NODES read at
@@ -167,9 +170,10 @@ cgtp_status cgtp_graph_transpose_noalloc(const int32_t* rowptr, const int32_t* c
 /*
  * cgtp_conv_forward -- fused CG tensor product + receiver sum.
  *  uvu: x [N,d1], Y [E,d2], W_or_R = W [E,w_numel], M = NULL -> out [N,d_out].
- *  uvw: W_or_R = R [E,K], M [K,w_numel] -> out [N,d_out]; per-edge weights
- *       are never formed; node state is streamed through bounded scratch
- *       owned by the plan ("Sobek ...", Abstract).
+ *  uvw, radial_k > 0: W_or_R = R [E,K], M [K,w_numel] -> out [N,d_out];
+ *       per-edge weights are never formed; node state is streamed through
+ *       bounded scratch owned by the plan ("Sobek ...", Abstract).
+ *  uvw, radial_k == 0: W_or_R = W [E,w_numel], M = NULL (weights per edge).
  *  Receivers own their accumulation; no atomics; empty rows give zeros.
  */
 cgtp_status cgtp_conv_forward(cgtp_plan plan, cgtp_graph graph, const void* x, const void* Y,
@@ -179,7 +183,8 @@ cgtp_status cgtp_conv_forward(cgtp_plan plan, cgtp_graph graph, const void* x, c
  * cgtp_conv_backward -- adjoint of cgtp_conv_forward for an output gradient gout [N,d_out]:
  *  gx [N,d1] (sender-owned, summed over each sender's out-edges), gY [E,d2],
  *  uvu: gW_or_gR = gW [E,w_numel], gM = NULL;
- *  uvw: gW_or_gR = gR [E,K], gM [K,w_numel] (deterministic ordered reduction).
+ *  uvw: gW_or_gR = gR [E,K], gM [K,w_numel] (deterministic ordered reduction);
+ *  uvw with per-edge weights: gW_or_gR = gW [E,w_numel], gM = NULL.
  */
 cgtp_status cgtp_conv_backward(cgtp_plan plan, cgtp_graph graph, const void* gout, const void* x,
                                const void* Y, const void* W_or_R, const void* M, void* gx, void* gY,

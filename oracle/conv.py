@@ -371,3 +371,62 @@ def conv_uvw_radial_backward_sh(plan, g, x, rvec, M, K, lo, hi, rowptr, col):
     grvec = np.einsum("ec,eck->ek", gY, sh_real_concat_jacobian(lmax, r))
     grvec += ((gR * dR).sum(1) / d)[:, None] * r
     return gx, gY, gR, grvec, gM
+
+
+# ---------------------------------------------------------------------------
+# uvw with a weight matrix per edge (Figure 3B/C weights, no radial factorisation)
+# ---------------------------------------------------------------------------
+
+def conv_uvw_forward(plan, x, Y, W, rowptr, col):
+    """out[n][i_out][w, m3] = sum_{e in row n} sum_{path -> i_out} sum_u W[e][path][u][w] t_e[u, m3]."""
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    x, Y, W = _f64(x), _f64(Y), _f64(W)
+    dst = csr_dst(rowptr)
+    msg = np.zeros((col.size, plan.d_out))
+    x1 = x[col]
+    for p in plan.paths:
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        D3 = 2 * p.l3 + 1
+        xs, ys = _blocks(p, x1, Y)
+        t = np.einsum("ijk,eui,ej->euk", C, xs, ys)
+        w = W[:, p.woff:p.woff + p.mul1 * p.mul_out].reshape(-1, p.mul1, p.mul_out)
+        msg[:, p.ooff:p.ooff + p.mul_out * D3] += np.einsum("euw,euk->ewk", w, t).reshape(col.size, -1)
+    out = np.zeros((len(rowptr) - 1, plan.d_out))
+    np.add.at(out, dst, msg)              # CSR order within each receiver
+    return out
+
+
+def conv_uvw_backward(plan, g, x, Y, W, rowptr, col):
+    """(gx [N,d1], gY [E,d2], gW [E,w_numel]) of conv_uvw_forward."""
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    g, x, Y, W = _f64(g), _f64(x), _f64(Y), _f64(W)
+    dst = csr_dst(rowptr)
+    x1, gd = x[col], g[dst]
+    gxe = np.zeros((col.size, plan.d1))
+    gY = np.zeros((col.size, plan.d2))
+    gW = np.zeros_like(W)
+    for p in plan.paths:
+        C = real_cg_block(p.l1, p.l2, p.l3)
+        D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+        xs, ys = _blocks(p, x1, Y)
+        t = np.einsum("ijk,eui,ej->euk", C, xs, ys)
+        sl = slice(p.woff, p.woff + p.mul1 * p.mul_out)
+        w = W[:, sl].reshape(-1, p.mul1, p.mul_out)
+        go = gd[:, p.ooff:p.ooff + p.mul_out * D3].reshape(-1, p.mul_out, D3)
+        gW[:, sl] = np.einsum("ewk,euk->euw", go, t).reshape(col.size, -1)
+        gt = np.einsum("euw,ewk->euk", w, go)
+        gxe[:, p.off1:p.off1 + p.mul1 * D1] += np.einsum("ijk,ej,euk->eui", C, ys, gt).reshape(col.size, -1)
+        gY[:, p.off2:p.off2 + D2] += np.einsum("ijk,eui,euk->ej", C, xs, gt)
+    gx = np.zeros((len(rowptr) - 1, plan.d1))
+    np.add.at(gx, col, gxe)
+    return gx, gY, gW
+
+
+def conv_uvw_double_backward(plan, g, x, Y, W, ggx, ggY, ggW, rowptr, col):
+    """(d_g, d_x, d_Y, d_W) for the uvw convolution with per-edge weights."""
+    fwd = lambda x_, Y_, W_: conv_uvw_forward(plan, x_, Y_, W_, rowptr, col)
+    bwd = lambda g_, x_, Y_, W_: conv_uvw_backward(plan, g_, x_, Y_, W_, rowptr, col)
+    return _double_backward(fwd, bwd, _f64(g), [_f64(x), _f64(Y), _f64(W)],
+                            [_f64(ggx), _f64(ggY), _f64(ggW)])

@@ -388,3 +388,39 @@ def test_radial_edge_vector_conv_gradient_finite_differences():
             rm[e, k] -= h
             fd = (f(rp) - f(rm)) / (2 * h)
             assert abs(fd - grvec[e, k]) < 1e-7 * max(1.0, abs(fd)), (e, k, fd, grvec[e, k])
+
+
+def test_uvw_per_edge_weights_brute_force_fd_and_radial_identity():
+    rng = np.random.default_rng(47)
+    plan = irreps.make_plan("2x0e+1x1o+1x2e", "0e+1o+2e", "1x0e+2x1o+1x2e", mode="uvw")
+    N, E, K = 4, 9, 3
+    rowptr, col = small_graph(rng, N, E)
+    x = rng.normal(size=(N, plan.d1))
+    Y = rng.normal(size=(E, plan.d2))
+    W = rng.normal(size=(E, plan.w_numel))
+    out = conv.conv_uvw_forward(plan, x, Y, W, rowptr, col)
+    # brute force: one dense bilinear tensor per edge, summed into the receiver
+    ref = np.zeros_like(out)
+    dst = graph.csr_dst(rowptr)
+    for e in range(E):
+        ref[dst[e]] += np.einsum("ijk,i,j->k", conv.dense_tensor(plan, W[e]), x[col[e]], Y[e])
+    assert np.abs(out - ref).max() < 1e-12
+    # the radial convolution is the per-edge one at W = R M
+    R = rng.normal(size=(E, K))
+    M = rng.normal(size=(K, plan.w_numel))
+    a = conv.conv_uvw_forward(plan, x, Y, R @ M, rowptr, col)
+    b = conv.conv_uvw_radial_forward(plan, x, Y, R, M, rowptr, col)
+    assert np.abs(a - b).max() < 1e-12 * max(1.0, np.abs(b).max())
+    # gradients against central differences
+    g = rng.normal(size=(N, plan.d_out))
+    grads = conv.conv_uvw_backward(plan, g, x, Y, W, rowptr, col)
+    f = lambda x_, Y_, W_: (g * conv.conv_uvw_forward(plan, x_, Y_, W_, rowptr, col)).sum()  # noqa: E731
+    args, h = [x, Y, W], 1e-6
+    for ai, (arr, ga) in enumerate(zip(args, grads)):
+        for _ in range(6):
+            idx = tuple(rng.integers(0, s) for s in arr.shape)
+            ap, am = [b_.copy() for b_ in args], [b_.copy() for b_ in args]
+            ap[ai][idx] += h
+            am[ai][idx] -= h
+            fd = (f(*ap) - f(*am)) / (2 * h)
+            assert abs(fd - ga[idx]) < 1e-7 * max(1.0, abs(fd)), (ai, idx, fd, ga[idx])
