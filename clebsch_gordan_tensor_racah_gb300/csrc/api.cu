@@ -35,6 +35,23 @@ void append(std::vector<unsigned char>& buf, const std::vector<T>& v, size_t* of
 
 }  // namespace
 
+int raise_smem_limit(const void* kernel) {
+  int dev = 0, optin = 0;
+  cudaFuncAttributes fa{};
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  const int cap = optin - static_cast<int>(fa.sharedSizeBytes);
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return cap;
+}
+
 cgtp_status upload_layout(const cgtp_plan_s* plan, const LayoutHost& h, LayoutDev* d) {
   std::vector<unsigned char> buf;
   size_t o_paths, o_in1, o_groups, o_cyb, o_cyc, o_cyf, o_gyb, o_gys, o_gyn, o_gyf, o_ib, o_it, o_gxb,

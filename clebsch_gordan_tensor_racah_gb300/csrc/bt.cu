@@ -667,7 +667,7 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
   st->zero_blk = reinterpret_cast<const int*>(at(o_z));
   // kernel attributes and occupancy -> grid sizes
   auto occupancy = [&](const void* k, size_t smem) {
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    raise_smem_limit(k);
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBtThreads, smem);
     return std::max(per_sm, 1);

@@ -171,6 +171,11 @@ namespace cgtp {
 // errors.cpp / planner.cpp
 cgtp_status fail(cgtp_status s, const std::string& msg);
 void clear_error();
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in cap minus
+// the kernel's static shared memory and return that cap (-1 on a CUDA error).
+// The limit belongs to the kernel and is shared by every plan, so it is only
+// ever raised to the cap, never set to one plan's need.
+int raise_smem_limit(const void* kernel);
 
 bool parse_irreps(const char* s, std::vector<Irrep>* out, std::string* err);
 double cg_complex(int j1, int m1, int j2, int m2, int J, int M);

@@ -893,7 +893,8 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
                                   kEdgeChunk * G.cy_size) + sizeof(int) * kEdgeChunk;
   if (st->smem_fwd > 227 * 1024)
     return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
-  cudaFuncSetAttribute(uvw_fwd_edge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem_fwd);
+  if (raise_smem_limit(reinterpret_cast<const void*>(uvw_fwd_edge_kernel)) < static_cast<int>(st->smem_fwd))
+    return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
   return CGTP_OK;
 }
 

@@ -13,9 +13,14 @@
 //   gt[u][m3] = sum_w W_e[u][w] g[dst][w][m3],   gW_e[u][w] = sum_m3 t[u][m3] g[dst][w][m3]
 //   gx[s][u][m1] += sum_m3 cy[m1][m3] gt[u][m3], cy = C.Y[e]
 //   gY[e][m2] += sum_{m1,m3} C[m1,m2,m3] sum_u x[s][u][m1] gt[u][m3]
-// One CTA owns a receiver (forward) or a sender (backward); its threads split
-// each stage of each path, staged through shared memory.  This serves plans of
-// any multiplicities with l <= 3; the per-edge weights are the dominant stream.
+// One CTA owns a receiver (forward) or a sender (backward) and walks its edges
+// in chunks of eight; every stage runs over all paths of the chunk at once,
+// staged through shared memory.  The weight stream is read with consecutive
+// threads on consecutive weights (forward: one thread per (path, w), all the
+// chunk's edges in flight; backward: one thread per (edge, path, u) walking its
+// row), after an L2 prefetch of the chunk's rows.  Every output, gx and gY
+// element has one owning thread, so no atomics are needed.  This serves plans
+// of any multiplicities with l <= 3; the per-edge weights are the dominant stream.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,10 +33,15 @@ namespace cgtp {
 namespace uvwe_detail {
 
 constexpr int kThr = 256;
+constexpr int kCh = 8;   // edges per chunk: every stage runs over all paths of a chunk at once
+constexpr int kSmemCap = 200 * 1024;
 
 struct EPath {
   int D1, D2, D3, mul1, mul_out;
   int off1, off2, ooff, woff, coff;  // coff: first entry of the dense C block [D1][D2][D3]
+  int cyo, tso;                      // offsets of the path's cy [D1][D3] and t [mul1][D3] in a chunk row
+  int pwo, aco, puo;                 // prefix sums of mul_out, mul_out * D3 and mul1 over the paths before
+  int i1, i2, io;
 };
 
 template <typename T>
@@ -47,55 +57,130 @@ struct EArgs {
   const int* rowptr;   // forward: CSR; backward: transpose
   const int* col;      // forward: CSR col; backward: t_eid
   const int* t_dst;
-  int N, d1, d2, d_out, w_numel, n_paths, tmax;  // tmax: largest mul1 * D3 over the paths
+  int N, d1, d2, d_out, w_numel, n_paths;
+  int ncy, nts;        // per-edge sizes of the cy and t rows (all paths)
+  int n_pw, nac, n_pu; // (path, w) pairs, per-path output partials, (path, u) pairs
   const EPath* paths;
   const T* C;
+  // output blocks (forward), in1 blocks (backward gx) and in2 blocks (backward gY):
+  // [begin, end) element ranges and the paths that feed each block
+  int n_ob, n_ib, n_yb;
+  const int* ob;       // per out block: elem0, elem1, path list begin, end (4 ints)
+  const int* ib;       // per in1 block: same
+  const int* yb;       // per in2 block: same
+  const int* plist;
 };
+
+// cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2]
+template <typename T>
+__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, const T* ys, T* cy, int cnt) {
+  for (int f = threadIdx.x; f < cnt * a.ncy; f += kThr) {
+    const int j = f / a.ncy, r = f - j * a.ncy;
+    int pi = 0;
+    while (pi + 1 < a.n_paths && a.paths[pi + 1].cyo <= r) ++pi;
+    const EPath p = a.paths[pi];
+    const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
+    T v = T(0);
+    for (int m2 = 0; m2 < p.D2; ++m2) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * ys[j * a.d2 + p.off2 + m2];
+    cy[f] = v;
+  }
+}
+
+// Ask L2 for the 128-byte lines of [p, p + bytes), spread over the block's threads.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t o = (size_t)threadIdx.x * 128; o < bytes; o += (size_t)kThr * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+}
+
+// path of a flattened index, given the prefix member `off` of every path
+#define UVWE_PATH_OF(r, off)                                                   \
+  ([&] {                                                                       \
+    int pi_ = 0;                                                               \
+    while (pi_ + 1 < a.n_paths && a.paths[pi_ + 1].off <= (r)) ++pi_;          \
+    return pi_;                                                                \
+  }())
 
 template <typename T>
 __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  T* out_s = reinterpret_cast<T*>(smem_raw);
-  T* xs = out_s + a.d_out;
-  T* ys = xs + a.d1;
-  T* cy = ys + a.d2;           // [D1][D3], <= 49
-  T* ts = cy + 49;             // [mul1][D3]
+  T* accs = reinterpret_cast<T*>(smem_raw);   // [nac]: per path, out[w][m3] partials
+  T* xs = accs + a.nac;             // [kCh][d1]
+  T* ys = xs + kCh * a.d1;          // [kCh][d2]
+  T* cy = ys + kCh * a.d2;          // [kCh][ncy]
+  T* ts = cy + kCh * a.ncy;         // [kCh][nts]
   const int tid = threadIdx.x;
   for (int n = blockIdx.x; n < a.N; n += gridDim.x) {
-    for (int i = tid; i < a.d_out; i += kThr) out_s[i] = T(0);
-    for (int e = a.rowptr[n]; e < a.rowptr[n + 1]; ++e) {
-      const int s = a.col[e];
-      __syncthreads();  // previous edge done with xs / ys; out_s zeroed
-      for (int i = tid; i < a.d1; i += kThr) xs[i] = a.x[(size_t)s * a.d1 + i];
-      for (int i = tid; i < a.d2; i += kThr) ys[i] = a.Y[(size_t)e * a.d2 + i];
-      const T* We = a.W + (size_t)e * a.w_numel;
-      for (int pi = 0; pi < a.n_paths; ++pi) {
-        const EPath p = a.paths[pi];
-        __syncthreads();
-        for (int f = tid; f < p.D1 * p.D3; f += kThr) {
-          const int m1 = f / p.D3, m3 = f - m1 * p.D3;
-          T v = T(0);
-          for (int m2 = 0; m2 < p.D2; ++m2) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * ys[p.off2 + m2];
-          cy[f] = v;
+    for (int i = tid; i < a.nac; i += kThr) accs[i] = T(0);
+    const int e_begin = a.rowptr[n], e_end = a.rowptr[n + 1];
+    for (int e0 = e_begin; e0 < e_end; e0 += kCh) {
+      const int cnt = min(kCh, e_end - e0);
+      // the chunk's weight rows are contiguous: have L2 fetch them while the
+      // product stages run
+      prefetch_l2(a.W + (size_t)e0 * a.w_numel, sizeof(T) * (size_t)cnt * a.w_numel);
+      __syncthreads();  // the previous chunk is done with the staging buffers
+      for (int f = tid; f < cnt * a.d1; f += kThr) {
+        const int j = f / a.d1;
+        xs[f] = a.x[(size_t)a.col[e0 + j] * a.d1 + (f - j * a.d1)];
+      }
+      for (int f = tid; f < cnt * a.d2; f += kThr) ys[f] = a.Y[(size_t)e0 * a.d2 + f];
+      __syncthreads();
+      chunk_cy(a, ys, cy, cnt);
+      __syncthreads();
+      // t[j][path][u][m3] = sum_m1 cy x
+      for (int f = tid; f < cnt * a.nts; f += kThr) {
+        const int j = f / a.nts, r = f - j * a.nts;
+        const EPath p = a.paths[UVWE_PATH_OF(r, tso)];
+        const int loc = r - p.tso, u = loc / p.D3, m3 = loc - u * p.D3;
+        const T* c = cy + j * a.ncy + p.cyo;
+        const T* xr = xs + j * a.d1 + p.off1 + u * p.D1;
+        T v = T(0);
+        for (int m1 = 0; m1 < p.D1; ++m1) v += c[m1 * p.D3 + m3] * xr[m1];
+        ts[f] = v;
+      }
+      __syncthreads();
+      // per (path, w): acc[m3] += sum_{j, u} W_j[u][w] t_j[u][m3]; a warp's
+      // weight loads cover consecutive w, and the chunk's edges are in flight together
+      for (int pw = tid; pw < a.n_pw; pw += kThr) {
+        const EPath p = a.paths[UVWE_PATH_OF(pw, pwo)];
+        const int w = pw - p.pwo;
+        const T* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
+        T acc[7];
+#pragma unroll
+        for (int m3 = 0; m3 < 7; ++m3) acc[m3] = T(0);
+        for (int u = 0; u < p.mul1; ++u) {
+          T wv[kCh];
+#pragma unroll
+          for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
+#pragma unroll
+          for (int j = 0; j < kCh; ++j) {
+            if (j < cnt) {
+              const T* tj = ts + j * a.nts + p.tso + u * p.D3;
+#pragma unroll
+              for (int m3 = 0; m3 < 7; ++m3)
+                if (m3 < p.D3) acc[m3] += wv[j] * tj[m3];
+            }
+          }
         }
-        __syncthreads();
-        for (int f = tid; f < p.mul1 * p.D3; f += kThr) {
-          const int u = f / p.D3, m3 = f - u * p.D3;
-          T v = T(0);
-          for (int m1 = 0; m1 < p.D1; ++m1) v += cy[m1 * p.D3 + m3] * xs[p.off1 + u * p.D1 + m1];
-          ts[f] = v;
-        }
-        __syncthreads();
-        for (int f = tid; f < p.mul_out * p.D3; f += kThr) {
-          const int w = f / p.D3, m3 = f - w * p.D3;
-          T v = T(0);
-          for (int u = 0; u < p.mul1; ++u) v += We[p.woff + u * p.mul_out + w] * ts[u * p.D3 + m3];
-          out_s[p.ooff + f] += v;
-        }
+        T* dst = accs + p.aco + w * p.D3;
+#pragma unroll
+        for (int m3 = 0; m3 < 7; ++m3)
+          if (m3 < p.D3) dst[m3] += acc[m3];
       }
     }
     __syncthreads();
-    for (int i = tid; i < a.d_out; i += kThr) a.out[(size_t)n * a.d_out + i] = out_s[i];
+    // out[n] block by block: the sum of the partials of the paths feeding it
+    for (int b = 0; b < a.n_ob; ++b) {
+      const int o0 = a.ob[4 * b], o1 = a.ob[4 * b + 1], q0 = a.ob[4 * b + 2], q1 = a.ob[4 * b + 3];
+      for (int f = o0 + tid; f < o1; f += kThr) {
+        T v = T(0);
+        for (int q = q0; q < q1; ++q) {
+          const EPath p = a.paths[a.plist[q]];
+          v += accs[p.aco + f - p.ooff];
+        }
+        a.out[(size_t)n * a.d_out + f] = v;
+      }
+    }
     __syncthreads();
   }
 }
@@ -103,78 +188,126 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
 template <typename T>
 __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  T* gs = reinterpret_cast<T*>(smem_raw);  // g[dst] row
-  T* xs = gs + a.d_out;
-  T* gxs = xs + a.d1;
-  T* ys = gxs + a.d1;
-  T* gys = ys + a.d2;
-  T* cy = gys + a.d2;          // [D1][D3]
-  T* G = cy + 49;              // [D1][D3]
-  T* ts = G + 49;              // [mul1][D3]
-  T* gts = ts + a.tmax;        // [mul1][D3]
+  T* xs = reinterpret_cast<T*>(smem_raw);   // [d1]
+  T* gxs = xs + a.d1;                       // [d1]
+  T* gs = gxs + a.d1;                       // [kCh][d_out]
+  T* ys = gs + kCh * a.d_out;               // [kCh][d2]
+  T* cy = ys + kCh * a.d2;                  // [kCh][ncy]
+  T* G = cy + kCh * a.ncy;                  // [kCh][ncy]
+  T* gts = G + kCh * a.ncy;                 // [kCh][nts]
+  int* eid = reinterpret_cast<int*>(gts + kCh * a.nts);   // [kCh]
   const int tid = threadIdx.x;
   for (int s = blockIdx.x; s < a.N; s += gridDim.x) {
     for (int i = tid; i < a.d1; i += kThr) {
       xs[i] = a.x[(size_t)s * a.d1 + i];
       gxs[i] = T(0);
     }
-    for (int t = a.rowptr[s]; t < a.rowptr[s + 1]; ++t) {
-      const int e = a.col[t], d = a.t_dst[t];
-      __syncthreads();  // previous edge done with gs / ys / gys
-      for (int i = tid; i < a.d_out; i += kThr) gs[i] = a.g[(size_t)d * a.d_out + i];
-      for (int i = tid; i < a.d2; i += kThr) {
-        ys[i] = a.Y[(size_t)e * a.d2 + i];
-        gys[i] = T(0);
+    const int t_begin = a.rowptr[s], t_end = a.rowptr[s + 1];
+    for (int t0 = t_begin; t0 < t_end; t0 += kCh) {
+      const int cnt = min(kCh, t_end - t0);
+      // weight rows of the chunk's edges (one contiguous row per edge) into L2
+      for (int j = 0; j < cnt; ++j)
+        prefetch_l2(a.W + (size_t)a.col[t0 + j] * a.w_numel, sizeof(T) * (size_t)a.w_numel);
+      __syncthreads();
+      if (tid < cnt) eid[tid] = a.col[t0 + tid];
+      for (int f = tid; f < cnt * a.d_out; f += kThr) {
+        const int j = f / a.d_out;
+        gs[f] = a.g[(size_t)a.t_dst[t0 + j] * a.d_out + (f - j * a.d_out)];
       }
-      const T* We = a.W + (size_t)e * a.w_numel;
-      T* gWe = a.gW + (size_t)e * a.w_numel;
-      for (int pi = 0; pi < a.n_paths; ++pi) {
-        const EPath p = a.paths[pi];
-        __syncthreads();
-        for (int f = tid; f < p.D1 * p.D3; f += kThr) {
-          const int m1 = f / p.D3, m3 = f - m1 * p.D3;
-          T v = T(0);
-          for (int m2 = 0; m2 < p.D2; ++m2) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * ys[p.off2 + m2];
-          cy[f] = v;
+      for (int f = tid; f < cnt * a.d2; f += kThr) {
+        const int j = f / a.d2;
+        ys[f] = a.Y[(size_t)a.col[t0 + j] * a.d2 + (f - j * a.d2)];
+      }
+      __syncthreads();
+      chunk_cy(a, ys, cy, cnt);
+      __syncthreads();
+      // per (edge, path, u): t[m3] = sum_m1 cy x[u], then along the weight row
+      //   gW[u][w] = sum_m3 t[m3] g[w][m3],  gt[u][m3] = sum_w W[u][w] g[w][m3]
+      for (int f = tid; f < cnt * a.n_pu; f += kThr) {
+        const int j = f / a.n_pu, r = f - j * a.n_pu;
+        const EPath p = a.paths[UVWE_PATH_OF(r, puo)];
+        const int u = r - p.puo;
+        const T* c = cy + j * a.ncy + p.cyo;
+        const T* xr = xs + p.off1 + u * p.D1;
+        T t[7], gt[7];
+#pragma unroll
+        for (int m3 = 0; m3 < 7; ++m3) {
+          t[m3] = T(0);
+          gt[m3] = T(0);
         }
-        __syncthreads();
-        for (int f = tid; f < p.mul1 * p.D3; f += kThr) {
-          const int u = f / p.D3, m3 = f - u * p.D3;
-          T v = T(0), gv = T(0);
-          for (int m1 = 0; m1 < p.D1; ++m1) v += cy[m1 * p.D3 + m3] * xs[p.off1 + u * p.D1 + m1];
-          for (int w = 0; w < p.mul_out; ++w) gv += We[p.woff + u * p.mul_out + w] * gs[p.ooff + w * p.D3 + m3];
-          ts[f] = v;
-          gts[f] = gv;
+        for (int m1 = 0; m1 < p.D1; ++m1) {
+          const T xv = xr[m1];
+#pragma unroll
+          for (int m3 = 0; m3 < 7; ++m3)
+            if (m3 < p.D3) t[m3] += c[m1 * p.D3 + m3] * xv;
         }
-        __syncthreads();
-        for (int f = tid; f < p.mul1 * p.mul_out; f += kThr) {
-          const int u = f / p.mul_out, w = f - u * p.mul_out;
-          T v = T(0);
-          for (int m3 = 0; m3 < p.D3; ++m3) v += ts[u * p.D3 + m3] * gs[p.ooff + w * p.D3 + m3];
-          gWe[p.woff + f] = v;
+        const size_t row = (size_t)eid[j] * a.w_numel + p.woff + (size_t)u * p.mul_out;
+        const T* Wr = a.W + row;
+        T* gWr = a.gW + row;
+        const T* gj = gs + j * a.d_out + p.ooff;
+#pragma unroll 4
+        for (int w = 0; w < p.mul_out; ++w) {
+          const T wv = __ldg(Wr + w);
+          T gw = T(0);
+#pragma unroll
+          for (int m3 = 0; m3 < 7; ++m3) {
+            if (m3 < p.D3) {
+              const T gv = gj[w * p.D3 + m3];
+              gw += t[m3] * gv;
+              gt[m3] += wv * gv;
+            }
+          }
+          gWr[w] = gw;
         }
-        for (int f = tid; f < p.mul1 * p.D1; f += kThr) {
-          const int u = f / p.D1, m1 = f - u * p.D1;
+        T* gd = gts + j * a.nts + p.tso + u * p.D3;
+#pragma unroll
+        for (int m3 = 0; m3 < 7; ++m3)
+          if (m3 < p.D3) gd[m3] = gt[m3];
+      }
+      __syncthreads();
+      // G[j][path][m1][m3] = sum_u x[u][m1] gt[u][m3]
+      for (int f = tid; f < cnt * a.ncy; f += kThr) {
+        const int j = f / a.ncy, r = f - j * a.ncy;
+        const EPath p = a.paths[UVWE_PATH_OF(r, cyo)];
+        const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
+        const T* gt = gts + j * a.nts + p.tso + m3;
+        T v = T(0);
+        for (int u = 0; u < p.mul1; ++u) v += xs[p.off1 + u * p.D1 + m1] * gt[u * p.D3];
+        G[f] = v;
+      }
+      // gx[u][m1] of every in1 block += sum over the chunk's edges and the block's paths
+      for (int b = 0; b < a.n_ib; ++b) {
+        const int o0 = a.ib[4 * b], o1 = a.ib[4 * b + 1], q0 = a.ib[4 * b + 2], q1 = a.ib[4 * b + 3];
+        for (int f = o0 + tid; f < o1; f += kThr) {
           T v = T(0);
-          for (int m3 = 0; m3 < p.D3; ++m3) v += cy[m1 * p.D3 + m3] * gts[u * p.D3 + m3];
-          gxs[p.off1 + f] += v;
-        }
-        for (int f = tid; f < p.D1 * p.D3; f += kThr) {
-          const int m1 = f / p.D3, m3 = f - m1 * p.D3;
-          T v = T(0);
-          for (int u = 0; u < p.mul1; ++u) v += xs[p.off1 + u * p.D1 + m1] * gts[u * p.D3 + m3];
-          G[f] = v;
-        }
-        __syncthreads();
-        for (int m2 = tid; m2 < p.D2; m2 += kThr) {
-          T v = T(0);
-          for (int m1 = 0; m1 < p.D1; ++m1)
-            for (int m3 = 0; m3 < p.D3; ++m3) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * G[m1 * p.D3 + m3];
-          gys[p.off2 + m2] += v;
+          for (int q = q0; q < q1; ++q) {
+            const EPath p = a.paths[a.plist[q]];
+            const int loc = f - p.off1, u = loc / p.D1, m1 = loc - u * p.D1;
+            for (int j = 0; j < cnt; ++j) {
+              const T* c = cy + j * a.ncy + p.cyo + m1 * p.D3;
+              const T* gt = gts + j * a.nts + p.tso + u * p.D3;
+              for (int m3 = 0; m3 < p.D3; ++m3) v += c[m3] * gt[m3];
+            }
+          }
+          gxs[f] += v;
         }
       }
       __syncthreads();
-      for (int i = tid; i < a.d2; i += kThr) a.gY[(size_t)e * a.d2 + i] = gys[i];
+      // gY[j][m2] of every in2 block = sum over the block's paths of C . G
+      for (int f = tid; f < cnt * a.d2; f += kThr) {
+        const int j = f / a.d2, col2 = f - j * a.d2;
+        int b = 0;
+        while (b + 1 < a.n_yb && a.yb[4 * (b + 1)] <= col2) ++b;
+        T v = T(0);
+        for (int q = a.yb[4 * b + 2]; q < a.yb[4 * b + 3]; ++q) {
+          const EPath p = a.paths[a.plist[q]];
+          const int m2 = col2 - p.off2;
+          const T* Gj = G + j * a.ncy + p.cyo;
+          for (int m1 = 0; m1 < p.D1; ++m1)
+            for (int m3 = 0; m3 < p.D3; ++m3) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * Gj[m1 * p.D3 + m3];
+        }
+        a.gY[(size_t)eid[j] * a.d2 + col2] = v;
+      }
     }
     __syncthreads();
     for (int i = tid; i < a.d1; i += kThr) a.gx[(size_t)s * a.d1 + i] = gxs[i];
@@ -182,11 +315,14 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   }
 }
 
+#undef UVWE_PATH_OF
+
 struct EState {
   void* tables = nullptr;
   const EPath* paths = nullptr;
   const void* C = nullptr;
-  int n_paths = 0, tmax = 0;
+  const int *ob = nullptr, *ib = nullptr, *yb = nullptr, *plist = nullptr;
+  int n_paths = 0, ncy = 0, nts = 0, n_pw = 0, nac = 0, n_pu = 0, n_ob = 0, n_ib = 0, n_yb = 0;
   size_t smem_fwd = 0, smem_bwd = 0;
 };
 
@@ -200,7 +336,7 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   if (lmax > 3) return fail(CGTP_EUNSUPPORTED, "per-edge uvw weights support l <= 3");
   std::vector<EPath> ep;
   std::vector<double> C;
-  int tmax = 1;
+  int ncy = 0, nts = 0, n_pw = 0, nac = 0, n_pu = 0;
   for (const auto& h : plan->paths) {
     EPath e{};
     e.D1 = 2 * h.l1 + 1;
@@ -213,31 +349,78 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
     e.ooff = h.ooff;
     e.woff = h.woff;
     e.coff = static_cast<int>(C.size());
+    e.cyo = ncy;
+    e.tso = nts;
+    e.pwo = n_pw;
+    e.aco = nac;
+    e.puo = n_pu;
+    e.i1 = h.i1;
+    e.i2 = h.i2;
+    e.io = h.io;
+    ncy += e.D1 * e.D3;
+    nts += e.mul1 * e.D3;
+    n_pw += e.mul_out;
+    nac += e.mul_out * e.D3;
+    n_pu += e.mul1;
     C.insert(C.end(), h.C.begin(), h.C.end());
-    tmax = std::max(tmax, e.mul1 * e.D3);
     ep.push_back(e);
   }
+  // blocks -> feeding paths, in path order (the order of every sum)
+  std::vector<int> ob, ib, yb, plist;
+  auto blocks = [&](const std::vector<Irrep>& irr, auto which, std::vector<int>& out) {
+    int off = 0;
+    for (size_t k = 0; k < irr.size(); ++k) {
+      const int size = irr[k].mul * (2 * irr[k].l + 1);
+      const int q0 = static_cast<int>(plist.size());
+      for (size_t pi = 0; pi < ep.size(); ++pi)
+        if (which(ep[pi]) == static_cast<int>(k)) plist.push_back(static_cast<int>(pi));
+      out.insert(out.end(), {off, off + size, q0, static_cast<int>(plist.size())});
+      off += size;
+    }
+  };
+  blocks(plan->out, [](const EPath& e) { return e.io; }, ob);
+  blocks(plan->in1, [](const EPath& e) { return e.i1; }, ib);
+  blocks(plan->in2, [](const EPath& e) { return e.i2; }, yb);
   const size_t es = plan->dtype == CGTP_F64 ? 8 : 4;
   EState* st = new EState();
   st->n_paths = static_cast<int>(ep.size());
-  st->tmax = tmax;
-  st->smem_fwd = es * (size_t(plan->d_out) + plan->d1 + plan->d2 + 49 + tmax);
-  st->smem_bwd = es * (size_t(plan->d_out) + 2 * plan->d1 + 2 * plan->d2 + 98 + 2 * tmax);
-  if (st->smem_bwd > 200 * 1024) {
+  st->ncy = ncy;
+  st->nts = nts;
+  st->n_pw = n_pw;
+  st->nac = nac;
+  st->n_pu = n_pu;
+  st->n_ob = static_cast<int>(ob.size() / 4);
+  st->n_ib = static_cast<int>(ib.size() / 4);
+  st->n_yb = static_cast<int>(yb.size() / 4);
+  st->smem_fwd = es * (size_t(nac) + kCh * (size_t(plan->d1) + plan->d2 + ncy + nts));
+  st->smem_bwd = es * (2 * size_t(plan->d1) + kCh * (size_t(plan->d_out) + plan->d2 + 2 * ncy + nts)) +
+                 kCh * sizeof(int);
+  if (st->smem_bwd > kSmemCap || st->smem_fwd > kSmemCap) {
     delete st;
     return fail(CGTP_EUNSUPPORTED, "per-edge uvw weights: rows too long for shared memory");
   }
-  std::vector<unsigned char> buf(((ep.size() * sizeof(EPath) + 15) / 16) * 16 + C.size() * es);
-  std::memcpy(buf.data(), ep.data(), ep.size() * sizeof(EPath));
-  const size_t coff = ((ep.size() * sizeof(EPath) + 15) / 16) * 16;
+  std::vector<unsigned char> buf;
+  auto put = [&](const void* src, size_t bytes) {
+    const size_t o = (buf.size() + 15) / 16 * 16;
+    buf.resize(o + std::max<size_t>(bytes, 16));
+    if (bytes) std::memcpy(buf.data() + o, src, bytes);
+    return o;
+  };
+  const size_t o_p = put(ep.data(), ep.size() * sizeof(EPath));
+  std::vector<unsigned char> cbytes(C.size() * es);
   for (size_t i = 0; i < C.size(); ++i) {
     if (es == 8) {
-      std::memcpy(buf.data() + coff + i * 8, &C[i], 8);
+      std::memcpy(cbytes.data() + i * 8, &C[i], 8);
     } else {
       const float f = static_cast<float>(C[i]);
-      std::memcpy(buf.data() + coff + i * 4, &f, 4);
+      std::memcpy(cbytes.data() + i * 4, &f, 4);
     }
   }
+  const size_t o_c = put(cbytes.data(), cbytes.size());
+  const size_t o_ob = put(ob.data(), ob.size() * sizeof(int));
+  const size_t o_ib = put(ib.data(), ib.size() * sizeof(int));
+  const size_t o_yb = put(yb.data(), yb.size() * sizeof(int));
+  const size_t o_pl = put(plist.data(), plist.size() * sizeof(int));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) {
     delete st;
     return fail(CGTP_ENOMEM, "per-edge uvw table allocation failed");
@@ -247,13 +430,17 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
     delete st;
     return fail(CGTP_ECUDA, "per-edge uvw table upload failed");
   }
-  st->paths = static_cast<const EPath*>(st->tables);
-  st->C = static_cast<unsigned char*>(st->tables) + coff;
-  cudaFuncSetAttribute(uvwe_fwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(st->smem_fwd));
-  cudaFuncSetAttribute(uvwe_bwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(st->smem_bwd));
-  cudaFuncSetAttribute(uvwe_fwd_kernel<double>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(st->smem_fwd));
-  cudaFuncSetAttribute(uvwe_bwd_kernel<double>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(st->smem_bwd));
-  cudaGetLastError();
+  auto at = [&](size_t o) { return static_cast<unsigned char*>(st->tables) + o; };
+  st->paths = reinterpret_cast<const EPath*>(at(o_p));
+  st->C = at(o_c);
+  st->ob = reinterpret_cast<const int*>(at(o_ob));
+  st->ib = reinterpret_cast<const int*>(at(o_ib));
+  st->yb = reinterpret_cast<const int*>(at(o_yb));
+  st->plist = reinterpret_cast<const int*>(at(o_pl));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<double>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double>));
   plan->uvwe = st;
   return CGTP_OK;
 }
@@ -275,9 +462,20 @@ static EArgs<T> e_args(const cgtp_plan_s* plan, const EState* st, const cgtp_gra
   a.d_out = static_cast<int>(plan->d_out);
   a.w_numel = static_cast<int>(plan->w_numel);
   a.n_paths = st->n_paths;
-  a.tmax = st->tmax;
+  a.ncy = st->ncy;
+  a.nts = st->nts;
+  a.n_pw = st->n_pw;
+  a.nac = st->nac;
+  a.n_pu = st->n_pu;
   a.paths = st->paths;
   a.C = static_cast<const T*>(st->C);
+  a.n_ob = st->n_ob;
+  a.n_ib = st->n_ib;
+  a.n_yb = st->n_yb;
+  a.ob = st->ob;
+  a.ib = st->ib;
+  a.yb = st->yb;
+  a.plist = st->plist;
   return a;
 }
 

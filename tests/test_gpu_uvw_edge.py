@@ -64,3 +64,28 @@ def test_uvw_per_edge_weights(dtype, in1, out):
     ref = oconv.conv_uvw_double_backward(oplan, g, x, Y, W, *c, rowptr, col)
     for nm, a, b in zip(("d_gout", "d_x", "d_Y", "d_W"), got[:4], ref):
         close(nm, a, b, dtype)
+
+
+def test_uvw_per_edge_two_plans_dense_rows():
+    """A larger plan stays usable after a smaller one is created (the kernels'
+    shared-memory limit is per kernel, not per plan), on rows of about 40 edges
+    (five chunks of eight and a ragged tail per receiver)."""
+    rng = np.random.default_rng(5)
+    in2 = "0e+1o+2e+3o"
+    big = ("16x0e+16x1o+16x2e+8x3o", "16x0e+16x1o+16x2e+8x3o")
+    oplan = oirr.make_plan(big[0], in2, big[1], "uvw")
+    plan = cg.Plan(big[0], in2, big[1], "uvw", torch.float32, radial_k=0)
+    small = cg.Plan("2x0e", "0e", "2x0e", "uvw", torch.float32, radial_k=0)
+    N, E = 12, 470
+    rowptr, col = graph_of(rng, N, E)
+    x = rng.standard_normal((N, oplan.d1)).astype(np.float32)
+    Y = rng.standard_normal((E, oplan.d2)).astype(np.float32)
+    W = (rng.standard_normal((E, oplan.w_numel)) / 4).astype(np.float32)
+    graph = cg.Graph(T(rowptr), T(col), N)
+    o = cg.cgtp_conv_forward(plan, graph, T(x), T(Y), T(W))
+    close("out", o, oconv.conv_uvw_forward(oplan, x, Y, W, rowptr, col), np.float32)
+    g = rng.standard_normal((N, oplan.d_out)).astype(np.float32)
+    got = cg.cgtp_conv_backward(plan, graph, T(g), T(x), T(Y), T(W))
+    for nm, a, b in zip(("gx", "gY", "gW"), got[:3], oconv.conv_uvw_backward(oplan, g, x, Y, W, rowptr, col)):
+        close(nm, a, b, np.float32)
+    del small
