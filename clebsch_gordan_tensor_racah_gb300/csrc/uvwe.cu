@@ -24,7 +24,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
+#include <type_traits>
 #include <vector>
 
 #include "internal.h"
@@ -69,22 +71,10 @@ struct EArgs {
   const int* ib;       // per in1 block: same
   const int* yb;       // per in2 block: same
   const int* plist;
+  const int* cy_path;  // path of each entry of a cy row [ncy]
+  const int* pu_path;  // path of each (path, u) pair [n_pu]
+  const int* pw_path;  // path of each (path, w) pair [n_pw]
 };
-
-// cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2]
-template <typename T>
-__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, const T* ys, T* cy, int cnt) {
-  for (int f = threadIdx.x; f < cnt * a.ncy; f += kThr) {
-    const int j = f / a.ncy, r = f - j * a.ncy;
-    int pi = 0;
-    while (pi + 1 < a.n_paths && a.paths[pi + 1].cyo <= r) ++pi;
-    const EPath p = a.paths[pi];
-    const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
-    T v = T(0);
-    for (int m2 = 0; m2 < p.D2; ++m2) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * ys[j * a.d2 + p.off2 + m2];
-    cy[f] = v;
-  }
-}
 
 // Ask L2 for the 128-byte lines of [p, p + bytes), spread over the block's threads.
 __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
@@ -93,13 +83,67 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
 }
 
-// path of a flattened index, given the prefix member `off` of every path
-#define UVWE_PATH_OF(r, off)                                                   \
-  ([&] {                                                                       \
-    int pi_ = 0;                                                               \
-    while (pi_ + 1 < a.n_paths && a.paths[pi_ + 1].off <= (r)) ++pi_;          \
-    return pi_;                                                                \
-  }())
+// V consecutive elements of a weight row (V = 1, or one 16-byte vector)
+template <int V, typename T>
+__device__ __forceinline__ void ldrow(const T* p, T (&r)[V]) {
+  if constexpr (V == 1) {
+    r[0] = __ldg(p);
+  } else if constexpr (sizeof(T) == 4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+  } else {
+    const double2 v = __ldg(reinterpret_cast<const double2*>(p));
+    r[0] = v.x; r[1] = v.y;
+  }
+}
+template <int V, typename T>
+__device__ __forceinline__ void strow(T* p, const T (&r)[V]) {
+  if constexpr (V == 1) {
+    p[0] = r[0];
+  } else if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(r[0], r[1], r[2], r[3]);
+  } else {
+    *reinterpret_cast<double2*>(p) = make_double2(r[0], r[1]);
+  }
+}
+
+// Call f with the block size D3 as a compile-time constant (a std::integral_constant).
+template <typename F>
+__device__ __forceinline__ void with_d3(int D3, F&& f) {
+  switch (D3) {
+    case 1: f(std::integral_constant<int, 1>{}); break;
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    case 5: f(std::integral_constant<int, 5>{}); break;
+    default: f(std::integral_constant<int, 7>{}); break;
+  }
+}
+
+// cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2]
+template <typename T>
+__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, const T* ys, T* cy, int cnt) {
+  for (int f = threadIdx.x; f < cnt * a.ncy; f += kThr) {
+    const int j = f / a.ncy, r = f - j * a.ncy;
+    const EPath p = a.paths[__ldg(a.cy_path + r)];
+    const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
+    const T* Cp = a.C + p.coff + m1 * p.D2 * p.D3 + m3;
+    const T* yr = ys + j * a.d2 + p.off2;
+    T v = T(0);
+    for (int m2 = 0; m2 < p.D2; ++m2) v += __ldg(Cp + m2 * p.D3) * yr[m2];
+    cy[f] = v;
+  }
+}
+
+// t[m3] = sum_m1 cy[m1][m3] x[m1] of one (edge, path, u)
+template <int D3, typename T>
+__device__ __forceinline__ void t_row(const T* c, const T* xr, int D1, T (&t)[D3]) {
+#pragma unroll
+  for (int m3 = 0; m3 < D3; ++m3) t[m3] = T(0);
+  for (int m1 = 0; m1 < D1; ++m1) {
+    const T xv = xr[m1];
+#pragma unroll
+    for (int m3 = 0; m3 < D3; ++m3) t[m3] += c[m1 * D3 + m3] * xv;
+  }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
@@ -127,45 +171,52 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
       __syncthreads();
       chunk_cy(a, ys, cy, cnt);
       __syncthreads();
-      // t[j][path][u][m3] = sum_m1 cy x
-      for (int f = tid; f < cnt * a.nts; f += kThr) {
-        const int j = f / a.nts, r = f - j * a.nts;
-        const EPath p = a.paths[UVWE_PATH_OF(r, tso)];
-        const int loc = r - p.tso, u = loc / p.D3, m3 = loc - u * p.D3;
-        const T* c = cy + j * a.ncy + p.cyo;
-        const T* xr = xs + j * a.d1 + p.off1 + u * p.D1;
-        T v = T(0);
-        for (int m1 = 0; m1 < p.D1; ++m1) v += c[m1 * p.D3 + m3] * xr[m1];
-        ts[f] = v;
+      // t[j][path][u][:] = cy x[u], one (edge, path, u) per item
+      for (int f = tid; f < cnt * a.n_pu; f += kThr) {
+        const int j = f / a.n_pu, r = f - j * a.n_pu;
+        const EPath p = a.paths[__ldg(a.pu_path + r)];
+        const int u = r - p.puo;
+        with_d3(p.D3, [&](auto d3c) {
+          constexpr int D3 = decltype(d3c)::value;
+          T t[D3];
+          t_row<D3>(cy + j * a.ncy + p.cyo, xs + j * a.d1 + p.off1 + u * p.D1, p.D1, t);
+          T* dst = ts + j * a.nts + p.tso + u * D3;
+#pragma unroll
+          for (int m3 = 0; m3 < D3; ++m3) dst[m3] = t[m3];
+        });
       }
       __syncthreads();
       // per (path, w): acc[m3] += sum_{j, u} W_j[u][w] t_j[u][m3]; a warp's
       // weight loads cover consecutive w, and the chunk's edges are in flight together
       for (int pw = tid; pw < a.n_pw; pw += kThr) {
-        const EPath p = a.paths[UVWE_PATH_OF(pw, pwo)];
+        const EPath p = a.paths[__ldg(a.pw_path + pw)];
         const int w = pw - p.pwo;
         const T* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
-        T acc[7];
+        with_d3(p.D3, [&](auto d3c) {
+          constexpr int D3 = decltype(d3c)::value;
+          T acc0[D3], acc1[D3];   // even and odd edges: two independent FMA chains
 #pragma unroll
-        for (int m3 = 0; m3 < 7; ++m3) acc[m3] = T(0);
-        for (int u = 0; u < p.mul1; ++u) {
-          T wv[kCh];
+          for (int m3 = 0; m3 < D3; ++m3) acc0[m3] = acc1[m3] = T(0);
+          for (int u = 0; u < p.mul1; ++u) {
+            T wv[kCh];
 #pragma unroll
-          for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
+            for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
 #pragma unroll
-          for (int j = 0; j < kCh; ++j) {
-            if (j < cnt) {
-              const T* tj = ts + j * a.nts + p.tso + u * p.D3;
+            for (int j = 0; j < kCh; ++j) {
+              if (j < cnt) {
+                const T* tj = ts + j * a.nts + p.tso + u * D3;
 #pragma unroll
-              for (int m3 = 0; m3 < 7; ++m3)
-                if (m3 < p.D3) acc[m3] += wv[j] * tj[m3];
+                for (int m3 = 0; m3 < D3; ++m3) {
+                  if (j & 1) acc1[m3] += wv[j] * tj[m3];
+                  else acc0[m3] += wv[j] * tj[m3];
+                }
+              }
             }
           }
-        }
-        T* dst = accs + p.aco + w * p.D3;
+          T* dst = accs + p.aco + w * D3;
 #pragma unroll
-        for (int m3 = 0; m3 < 7; ++m3)
-          if (m3 < p.D3) dst[m3] += acc[m3];
+          for (int m3 = 0; m3 < D3; ++m3) dst[m3] += acc0[m3] + acc1[m3];
+        });
       }
     }
     __syncthreads();
@@ -185,7 +236,8 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
   }
 }
 
-template <typename T>
+// V: weight-row vector width (1, or 16 bytes when every row segment is aligned)
+template <typename T, int V>
 __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);   // [d1]
@@ -221,54 +273,45 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
       __syncthreads();
       chunk_cy(a, ys, cy, cnt);
       __syncthreads();
-      // per (edge, path, u): t[m3] = sum_m1 cy x[u], then along the weight row
+      // per (edge, path, u): t = cy x[u], then along the weight row
       //   gW[u][w] = sum_m3 t[m3] g[w][m3],  gt[u][m3] = sum_w W[u][w] g[w][m3]
       for (int f = tid; f < cnt * a.n_pu; f += kThr) {
         const int j = f / a.n_pu, r = f - j * a.n_pu;
-        const EPath p = a.paths[UVWE_PATH_OF(r, puo)];
+        const EPath p = a.paths[__ldg(a.pu_path + r)];
         const int u = r - p.puo;
-        const T* c = cy + j * a.ncy + p.cyo;
-        const T* xr = xs + p.off1 + u * p.D1;
-        T t[7], gt[7];
-#pragma unroll
-        for (int m3 = 0; m3 < 7; ++m3) {
-          t[m3] = T(0);
-          gt[m3] = T(0);
-        }
-        for (int m1 = 0; m1 < p.D1; ++m1) {
-          const T xv = xr[m1];
-#pragma unroll
-          for (int m3 = 0; m3 < 7; ++m3)
-            if (m3 < p.D3) t[m3] += c[m1 * p.D3 + m3] * xv;
-        }
         const size_t row = (size_t)eid[j] * a.w_numel + p.woff + (size_t)u * p.mul_out;
-        const T* Wr = a.W + row;
-        T* gWr = a.gW + row;
         const T* gj = gs + j * a.d_out + p.ooff;
-#pragma unroll 4
-        for (int w = 0; w < p.mul_out; ++w) {
-          const T wv = __ldg(Wr + w);
-          T gw = T(0);
+        with_d3(p.D3, [&](auto d3c) {
+          constexpr int D3 = decltype(d3c)::value;
+          T t[D3], gt[D3];
+          t_row<D3>(cy + j * a.ncy + p.cyo, xs + p.off1 + u * p.D1, p.D1, t);
 #pragma unroll
-          for (int m3 = 0; m3 < 7; ++m3) {
-            if (m3 < p.D3) {
-              const T gv = gj[w * p.D3 + m3];
-              gw += t[m3] * gv;
-              gt[m3] += wv * gv;
+          for (int m3 = 0; m3 < D3; ++m3) gt[m3] = T(0);
+          for (int w = 0; w < p.mul_out; w += V) {
+            T wv[V], gw[V];
+            ldrow<V>(a.W + row + w, wv);
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+              gw[k] = T(0);
+#pragma unroll
+              for (int m3 = 0; m3 < D3; ++m3) {
+                const T gv = gj[(w + k) * D3 + m3];
+                gw[k] += t[m3] * gv;
+                gt[m3] += wv[k] * gv;
+              }
             }
+            strow<V>(a.gW + row + w, gw);
           }
-          gWr[w] = gw;
-        }
-        T* gd = gts + j * a.nts + p.tso + u * p.D3;
+          T* gd = gts + j * a.nts + p.tso + u * D3;
 #pragma unroll
-        for (int m3 = 0; m3 < 7; ++m3)
-          if (m3 < p.D3) gd[m3] = gt[m3];
+          for (int m3 = 0; m3 < D3; ++m3) gd[m3] = gt[m3];
+        });
       }
       __syncthreads();
       // G[j][path][m1][m3] = sum_u x[u][m1] gt[u][m3]
       for (int f = tid; f < cnt * a.ncy; f += kThr) {
         const int j = f / a.ncy, r = f - j * a.ncy;
-        const EPath p = a.paths[UVWE_PATH_OF(r, cyo)];
+        const EPath p = a.paths[__ldg(a.cy_path + r)];
         const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
         const T* gt = gts + j * a.nts + p.tso + m3;
         T v = T(0);
@@ -283,11 +326,15 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
           for (int q = q0; q < q1; ++q) {
             const EPath p = a.paths[a.plist[q]];
             const int loc = f - p.off1, u = loc / p.D1, m1 = loc - u * p.D1;
-            for (int j = 0; j < cnt; ++j) {
-              const T* c = cy + j * a.ncy + p.cyo + m1 * p.D3;
-              const T* gt = gts + j * a.nts + p.tso + u * p.D3;
-              for (int m3 = 0; m3 < p.D3; ++m3) v += c[m3] * gt[m3];
-            }
+            with_d3(p.D3, [&](auto d3c) {
+          constexpr int D3 = decltype(d3c)::value;
+              for (int j = 0; j < cnt; ++j) {
+                const T* c = cy + j * a.ncy + p.cyo + m1 * D3;
+                const T* gt = gts + j * a.nts + p.tso + u * D3;
+#pragma unroll
+                for (int m3 = 0; m3 < D3; ++m3) v += c[m3] * gt[m3];
+              }
+            });
           }
           gxs[f] += v;
         }
@@ -304,7 +351,7 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
           const int m2 = col2 - p.off2;
           const T* Gj = G + j * a.ncy + p.cyo;
           for (int m1 = 0; m1 < p.D1; ++m1)
-            for (int m3 = 0; m3 < p.D3; ++m3) v += a.C[p.coff + (m1 * p.D2 + m2) * p.D3 + m3] * Gj[m1 * p.D3 + m3];
+            for (int m3 = 0; m3 < p.D3; ++m3) v += __ldg(a.C + p.coff + (m1 * p.D2 + m2) * p.D3 + m3) * Gj[m1 * p.D3 + m3];
         }
         a.gY[(size_t)eid[j] * a.d2 + col2] = v;
       }
@@ -315,13 +362,13 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   }
 }
 
-#undef UVWE_PATH_OF
-
 struct EState {
   void* tables = nullptr;
   const EPath* paths = nullptr;
   const void* C = nullptr;
   const int *ob = nullptr, *ib = nullptr, *yb = nullptr, *plist = nullptr;
+  const int *cy_path = nullptr, *pu_path = nullptr, *pw_path = nullptr;
+  bool vec = false;
   int n_paths = 0, ncy = 0, nts = 0, n_pw = 0, nac = 0, n_pu = 0, n_ob = 0, n_ib = 0, n_yb = 0;
   size_t smem_fwd = 0, smem_bwd = 0;
 };
@@ -381,6 +428,18 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   blocks(plan->out, [](const EPath& e) { return e.io; }, ob);
   blocks(plan->in1, [](const EPath& e) { return e.i1; }, ib);
   blocks(plan->in2, [](const EPath& e) { return e.i2; }, yb);
+  // path of every flattened entry of the per-edge rows the stages index
+  std::vector<int> cy_path, pu_path, pw_path;
+  bool vec = true;   // every weight-row segment a whole number of 16-byte vectors
+  const int vw = plan->dtype == CGTP_F64 ? 2 : 4;
+  if (plan->w_numel % vw) vec = false;
+  for (size_t pi = 0; pi < ep.size(); ++pi) {
+    const EPath& e = ep[pi];
+    cy_path.insert(cy_path.end(), e.D1 * e.D3, static_cast<int>(pi));
+    pu_path.insert(pu_path.end(), e.mul1, static_cast<int>(pi));
+    pw_path.insert(pw_path.end(), e.mul_out, static_cast<int>(pi));
+    if (e.mul_out % vw || e.woff % vw) vec = false;
+  }
   const size_t es = plan->dtype == CGTP_F64 ? 8 : 4;
   EState* st = new EState();
   st->n_paths = static_cast<int>(ep.size());
@@ -421,6 +480,9 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   const size_t o_ib = put(ib.data(), ib.size() * sizeof(int));
   const size_t o_yb = put(yb.data(), yb.size() * sizeof(int));
   const size_t o_pl = put(plist.data(), plist.size() * sizeof(int));
+  const size_t o_cp = put(cy_path.data(), cy_path.size() * sizeof(int));
+  const size_t o_up = put(pu_path.data(), pu_path.size() * sizeof(int));
+  const size_t o_wp = put(pw_path.data(), pw_path.size() * sizeof(int));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) {
     delete st;
     return fail(CGTP_ENOMEM, "per-edge uvw table allocation failed");
@@ -437,10 +499,16 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   st->ib = reinterpret_cast<const int*>(at(o_ib));
   st->yb = reinterpret_cast<const int*>(at(o_yb));
   st->plist = reinterpret_cast<const int*>(at(o_pl));
+  st->cy_path = reinterpret_cast<const int*>(at(o_cp));
+  st->pu_path = reinterpret_cast<const int*>(at(o_up));
+  st->pw_path = reinterpret_cast<const int*>(at(o_wp));
+  st->vec = vec;
   raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<float>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 1>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 4>));
   raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<double>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 1>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 2>));
   plan->uvwe = st;
   return CGTP_OK;
 }
@@ -476,6 +544,9 @@ static EArgs<T> e_args(const cgtp_plan_s* plan, const EState* st, const cgtp_gra
   a.ib = st->ib;
   a.yb = st->yb;
   a.plist = st->plist;
+  a.cy_path = st->cy_path;
+  a.pu_path = st->pu_path;
+  a.pw_path = st->pw_path;
   return a;
 }
 
@@ -512,7 +583,12 @@ static cgtp_status bwd_t(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
   a.col = g->t_eid;
   a.t_dst = g->t_dst;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g->N, (int64_t)plan->num_sms * 4)));
-  uvwe_bwd_kernel<T><<<grid, kThr, st->smem_bwd, s>>>(a);
+  constexpr int kVec = 16 / sizeof(T);
+  const bool vec = st->vec && (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0);
+  if (vec)
+    uvwe_bwd_kernel<T, kVec><<<grid, kThr, st->smem_bwd, s>>>(a);
+  else
+    uvwe_bwd_kernel<T, 1><<<grid, kThr, st->smem_bwd, s>>>(a);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, std::string("per-edge uvw backward launch: ") + cudaGetErrorString(e));
 }
