@@ -42,7 +42,7 @@ struct EPath {
   int D1, D2, D3, mul1, mul_out;
   int off1, off2, ooff, woff, coff;  // coff: first entry of the dense C block [D1][D2][D3]
   int cyo, tso;                      // offsets of the path's cy [D1][D3] and t [mul1][D3] in a chunk row
-  int pwo, aco, puo;                 // prefix sums of mul_out, mul_out * D3 and mul1 over the paths before
+  int aco;                           // offset of the path's out[w][m3] partials (prefix sum of mul_out * D3)
   int i1, i2, io;
 };
 
@@ -118,18 +118,40 @@ __device__ __forceinline__ void with_d3(int D3, F&& f) {
   }
 }
 
-// cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2]
-template <typename T>
-__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, const T* ys, T* cy, int cnt) {
-  for (int f = threadIdx.x; f < cnt * a.ncy; f += kThr) {
-    const int j = f / a.ncy, r = f - j * a.ncy;
-    const EPath p = a.paths[__ldg(a.cy_path + r)];
-    const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
+// (j, r) = divmod(f, n) for f = threadIdx.x, threadIdx.x + kThr, ...: two
+// divisions per stage instead of one per element
+struct JR {
+  int j, r, q, rem, n;
+  __device__ __forceinline__ explicit JR(int n_) : n(n_) {
+    j = threadIdx.x / n;
+    r = threadIdx.x - j * n;
+    q = kThr / n;
+    rem = kThr - q * n;
+  }
+  __device__ __forceinline__ void next() {
+    r += rem;
+    j += q;
+    if (r >= n) {
+      r -= n;
+      ++j;
+    }
+  }
+};
+
+// cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2] (yrow(j): the
+// chunk's j-th Y row, in shared or global memory)
+template <typename T, typename YRow>
+__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, YRow yrow, T* cy, int cnt) {
+  if (a.ncy == 0) return;
+  for (JR it(a.ncy); it.j < cnt; it.next()) {
+    const int e = __ldg(a.cy_path + it.r);
+    const EPath p = a.paths[e & 0xffff];
+    const int m1 = (e >> 16) & 0xff, m3 = e >> 24;
     const T* Cp = a.C + p.coff + m1 * p.D2 * p.D3 + m3;
-    const T* yr = ys + j * a.d2 + p.off2;
+    const T* yr = yrow(it.j) + p.off2;
     T v = T(0);
     for (int m2 = 0; m2 < p.D2; ++m2) v += __ldg(Cp + m2 * p.D3) * yr[m2];
-    cy[f] = v;
+    cy[it.j * a.ncy + it.r] = v;
   }
 }
 
@@ -145,37 +167,75 @@ __device__ __forceinline__ void t_row(const T* c, const T* xr, int D1, T (&t)[D3
   }
 }
 
+// Forward, software-pipelined over a receiver's chunks in steps of two phases:
+//   phase 1 of step k: weight stage of chunk k - 1 beside the staging of chunk k
+//                      (x gather, cy from the Y rows, weight prefetch)
+//   phase 2 of step k: t stage of chunk k
+// so a chunk costs two block barriers.  Every stage has one call site.
 template <typename T>
 __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* accs = reinterpret_cast<T*>(smem_raw);   // [nac]: per path, out[w][m3] partials
   T* xs = accs + a.nac;             // [kCh][d1]
-  T* ys = xs + kCh * a.d1;          // [kCh][d2]
-  T* cy = ys + kCh * a.d2;          // [kCh][ncy]
+  T* cy = xs + kCh * a.d1;          // [kCh][ncy]
   T* ts = cy + kCh * a.ncy;         // [kCh][nts]
   const int tid = threadIdx.x;
+  // per (path, w): acc[m3] += sum_{j, u} W_j[u][w] t_j[u][m3] over the chunk at e0;
+  // a warp's weight loads cover consecutive w, and the chunk's edges are in flight together
+  auto weights = [&](int e0, int cnt) {
+    for (int pw = tid; pw < a.n_pw; pw += kThr) {
+      const int e = __ldg(a.pw_path + pw);
+      const EPath p = a.paths[e & 0xffff];
+      const int w = e >> 16;
+      const T* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
+      with_d3(p.D3, [&](auto d3c) {
+        constexpr int D3 = decltype(d3c)::value;
+        T acc0[D3], acc1[D3];   // even and odd edges: two independent FMA chains
+#pragma unroll
+        for (int m3 = 0; m3 < D3; ++m3) acc0[m3] = acc1[m3] = T(0);
+        for (int u = 0; u < p.mul1; ++u) {
+          T wv[kCh];
+#pragma unroll
+          for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
+#pragma unroll
+          for (int j = 0; j < kCh; ++j) {
+            if (j < cnt) {
+              const T* tj = ts + j * a.nts + p.tso + u * D3;
+#pragma unroll
+              for (int m3 = 0; m3 < D3; ++m3) {
+                if (j & 1) acc1[m3] += wv[j] * tj[m3];
+                else acc0[m3] += wv[j] * tj[m3];
+              }
+            }
+          }
+        }
+        T* dst = accs + p.aco + w * D3;
+#pragma unroll
+        for (int m3 = 0; m3 < D3; ++m3) dst[m3] += acc0[m3] + acc1[m3];
+      });
+    }
+  };
   for (int n = blockIdx.x; n < a.N; n += gridDim.x) {
     for (int i = tid; i < a.nac; i += kThr) accs[i] = T(0);
     const int e_begin = a.rowptr[n], e_end = a.rowptr[n + 1];
-    for (int e0 = e_begin; e0 < e_end; e0 += kCh) {
-      const int cnt = min(kCh, e_end - e0);
-      // the chunk's weight rows are contiguous: have L2 fetch them while the
-      // product stages run
-      prefetch_l2(a.W + (size_t)e0 * a.w_numel, sizeof(T) * (size_t)cnt * a.w_numel);
-      __syncthreads();  // the previous chunk is done with the staging buffers
-      for (int f = tid; f < cnt * a.d1; f += kThr) {
-        const int j = f / a.d1;
-        xs[f] = a.x[(size_t)a.col[e0 + j] * a.d1 + (f - j * a.d1)];
+    auto count = [&](int k) { return k < 0 ? 0 : max(0, min(kCh, e_end - e_begin - k * kCh)); };
+    for (int k = -1;; ++k) {
+      const int e0 = e_begin + k * kCh, cnt = count(k);
+      if (k >= 1) weights(e0 - kCh, count(k - 1));
+      if (cnt > 0) {
+        // the chunk's weight rows are contiguous: have L2 fetch them while the
+        // product stages run
+        prefetch_l2(a.W + (size_t)e0 * a.w_numel, sizeof(T) * (size_t)cnt * a.w_numel);
+        for (JR it(a.d1); it.j < cnt; it.next()) xs[it.j * a.d1 + it.r] = a.x[(size_t)a.col[e0 + it.j] * a.d1 + it.r];
+        chunk_cy(a, [&](int j) { return a.Y + (size_t)(e0 + j) * a.d2; }, cy, cnt);
       }
-      for (int f = tid; f < cnt * a.d2; f += kThr) ys[f] = a.Y[(size_t)e0 * a.d2 + f];
-      __syncthreads();
-      chunk_cy(a, ys, cy, cnt);
-      __syncthreads();
+      __syncthreads();  // x and cy of chunk k staged; the weight stage is done with ts
+      if (k >= 0 && cnt == 0) break;
       // t[j][path][u][:] = cy x[u], one (edge, path, u) per item
-      for (int f = tid; f < cnt * a.n_pu; f += kThr) {
-        const int j = f / a.n_pu, r = f - j * a.n_pu;
-        const EPath p = a.paths[__ldg(a.pu_path + r)];
-        const int u = r - p.puo;
+      for (JR it(a.n_pu > 0 ? a.n_pu : 1); a.n_pu > 0 && it.j < cnt; it.next()) {
+        const int j = it.j, e = __ldg(a.pu_path + it.r);
+        const EPath p = a.paths[e & 0xffff];
+        const int u = e >> 16;
         with_d3(p.D3, [&](auto d3c) {
           constexpr int D3 = decltype(d3c)::value;
           T t[D3];
@@ -185,41 +245,8 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
           for (int m3 = 0; m3 < D3; ++m3) dst[m3] = t[m3];
         });
       }
-      __syncthreads();
-      // per (path, w): acc[m3] += sum_{j, u} W_j[u][w] t_j[u][m3]; a warp's
-      // weight loads cover consecutive w, and the chunk's edges are in flight together
-      for (int pw = tid; pw < a.n_pw; pw += kThr) {
-        const EPath p = a.paths[__ldg(a.pw_path + pw)];
-        const int w = pw - p.pwo;
-        const T* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
-        with_d3(p.D3, [&](auto d3c) {
-          constexpr int D3 = decltype(d3c)::value;
-          T acc0[D3], acc1[D3];   // even and odd edges: two independent FMA chains
-#pragma unroll
-          for (int m3 = 0; m3 < D3; ++m3) acc0[m3] = acc1[m3] = T(0);
-          for (int u = 0; u < p.mul1; ++u) {
-            T wv[kCh];
-#pragma unroll
-            for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
-#pragma unroll
-            for (int j = 0; j < kCh; ++j) {
-              if (j < cnt) {
-                const T* tj = ts + j * a.nts + p.tso + u * D3;
-#pragma unroll
-                for (int m3 = 0; m3 < D3; ++m3) {
-                  if (j & 1) acc1[m3] += wv[j] * tj[m3];
-                  else acc0[m3] += wv[j] * tj[m3];
-                }
-              }
-            }
-          }
-          T* dst = accs + p.aco + w * D3;
-#pragma unroll
-          for (int m3 = 0; m3 < D3; ++m3) dst[m3] += acc0[m3] + acc1[m3];
-        });
-      }
+      __syncthreads();  // ts of chunk k ready; xs and cy free for the next chunk
     }
-    __syncthreads();
     // out[n] block by block: the sum of the partials of the paths feeding it
     for (int b = 0; b < a.n_ob; ++b) {
       const int o0 = a.ob[4 * b], o1 = a.ob[4 * b + 1], q0 = a.ob[4 * b + 2], q1 = a.ob[4 * b + 3];
@@ -237,6 +264,11 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
 }
 
 // V: weight-row vector width (1, or 16 bytes when every row segment is aligned)
+//
+// Backward over a sender's chunks: staging (edge ids, g rows, Y rows, weight
+// prefetch), cy, the fused t / gW / gt stage, G and gx, gY -- five block
+// barriers a chunk.  (Overlapping gY and G with the next chunk's staging
+// measured slower: the gathers' latency then sits inside the compute phases.)
 template <typename T, int V>
 __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -247,7 +279,7 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   T* cy = ys + kCh * a.d2;                  // [kCh][ncy]
   T* G = cy + kCh * a.ncy;                  // [kCh][ncy]
   T* gts = G + kCh * a.ncy;                 // [kCh][nts]
-  int* eid = reinterpret_cast<int*>(gts + kCh * a.nts);   // [kCh]
+  int* eids = reinterpret_cast<int*>(gts + kCh * a.nts);   // [kCh]
   const int tid = threadIdx.x;
   for (int s = blockIdx.x; s < a.N; s += gridDim.x) {
     for (int i = tid; i < a.d1; i += kThr) {
@@ -257,92 +289,92 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
     const int t_begin = a.rowptr[s], t_end = a.rowptr[s + 1];
     for (int t0 = t_begin; t0 < t_end; t0 += kCh) {
       const int cnt = min(kCh, t_end - t0);
-      // weight rows of the chunk's edges (one contiguous row per edge) into L2
+      const int* eid = eids;
       for (int j = 0; j < cnt; ++j)
         prefetch_l2(a.W + (size_t)a.col[t0 + j] * a.w_numel, sizeof(T) * (size_t)a.w_numel);
       __syncthreads();
-      if (tid < cnt) eid[tid] = a.col[t0 + tid];
-      for (int f = tid; f < cnt * a.d_out; f += kThr) {
-        const int j = f / a.d_out;
-        gs[f] = a.g[(size_t)a.t_dst[t0 + j] * a.d_out + (f - j * a.d_out)];
-      }
-      for (int f = tid; f < cnt * a.d2; f += kThr) {
-        const int j = f / a.d2;
-        ys[f] = a.Y[(size_t)a.col[t0 + j] * a.d2 + (f - j * a.d2)];
-      }
+      if (tid < cnt) eids[tid] = a.col[t0 + tid];
+      for (JR it(a.d_out); it.j < cnt; it.next())
+        gs[it.j * a.d_out + it.r] = a.g[(size_t)a.t_dst[t0 + it.j] * a.d_out + it.r];
+      for (JR it(a.d2); it.j < cnt; it.next()) ys[it.j * a.d2 + it.r] = a.Y[(size_t)a.col[t0 + it.j] * a.d2 + it.r];
       __syncthreads();
-      chunk_cy(a, ys, cy, cnt);
+      chunk_cy(a, [&](int j) { return ys + j * a.d2; }, cy, cnt);
       __syncthreads();
-      // per (edge, path, u): t = cy x[u], then along the weight row
-      //   gW[u][w] = sum_m3 t[m3] g[w][m3],  gt[u][m3] = sum_w W[u][w] g[w][m3]
-      for (int f = tid; f < cnt * a.n_pu; f += kThr) {
-        const int j = f / a.n_pu, r = f - j * a.n_pu;
-        const EPath p = a.paths[__ldg(a.pu_path + r)];
-        const int u = r - p.puo;
-        const size_t row = (size_t)eid[j] * a.w_numel + p.woff + (size_t)u * p.mul_out;
-        const T* gj = gs + j * a.d_out + p.ooff;
-        with_d3(p.D3, [&](auto d3c) {
-          constexpr int D3 = decltype(d3c)::value;
-          T t[D3], gt[D3];
-          t_row<D3>(cy + j * a.ncy + p.cyo, xs + p.off1 + u * p.D1, p.D1, t);
+        // per (edge, path, u): t = cy x[u], then along the weight row
+        //   gW[u][w] = sum_m3 t[m3] g[w][m3],  gt[u][m3] = sum_w W[u][w] g[w][m3]
+        for (JR it(a.n_pu > 0 ? a.n_pu : 1); a.n_pu > 0 && it.j < cnt; it.next()) {
+          const int j = it.j, e = __ldg(a.pu_path + it.r);
+          const EPath p = a.paths[e & 0xffff];
+          const int u = e >> 16;
+          const size_t row = (size_t)eid[j] * a.w_numel + p.woff + (size_t)u * p.mul_out;
+          const T* gj = gs + j * a.d_out + p.ooff;
+          with_d3(p.D3, [&](auto d3c) {
+            constexpr int D3 = decltype(d3c)::value;
+            T t[D3], gt[D3];
+            t_row<D3>(cy + j * a.ncy + p.cyo, xs + p.off1 + u * p.D1, p.D1, t);
 #pragma unroll
-          for (int m3 = 0; m3 < D3; ++m3) gt[m3] = T(0);
-          for (int w = 0; w < p.mul_out; w += V) {
-            T wv[V], gw[V];
-            ldrow<V>(a.W + row + w, wv);
+            for (int m3 = 0; m3 < D3; ++m3) gt[m3] = T(0);
+            for (int w = 0; w < p.mul_out; w += V) {
+              T wv[V], gw[V];
+              ldrow<V>(a.W + row + w, wv);
 #pragma unroll
-            for (int k = 0; k < V; ++k) {
-              gw[k] = T(0);
+              for (int c = 0; c < V; ++c) {
+                gw[c] = T(0);
 #pragma unroll
-              for (int m3 = 0; m3 < D3; ++m3) {
-                const T gv = gj[(w + k) * D3 + m3];
-                gw[k] += t[m3] * gv;
-                gt[m3] += wv[k] * gv;
+                for (int m3 = 0; m3 < D3; ++m3) {
+                  const T gv = gj[(w + c) * D3 + m3];
+                  gw[c] += t[m3] * gv;
+                  gt[m3] += wv[c] * gv;
+                }
               }
+              strow<V>(a.gW + row + w, gw);
             }
-            strow<V>(a.gW + row + w, gw);
-          }
-          T* gd = gts + j * a.nts + p.tso + u * D3;
+            T* gd = gts + j * a.nts + p.tso + u * D3;
 #pragma unroll
-          for (int m3 = 0; m3 < D3; ++m3) gd[m3] = gt[m3];
-        });
-      }
-      __syncthreads();
-      // G[j][path][m1][m3] = sum_u x[u][m1] gt[u][m3]
-      for (int f = tid; f < cnt * a.ncy; f += kThr) {
-        const int j = f / a.ncy, r = f - j * a.ncy;
-        const EPath p = a.paths[__ldg(a.cy_path + r)];
-        const int loc = r - p.cyo, m1 = loc / p.D3, m3 = loc - m1 * p.D3;
-        const T* gt = gts + j * a.nts + p.tso + m3;
-        T v = T(0);
-        for (int u = 0; u < p.mul1; ++u) v += xs[p.off1 + u * p.D1 + m1] * gt[u * p.D3];
-        G[f] = v;
-      }
-      // gx[u][m1] of every in1 block += sum over the chunk's edges and the block's paths
-      for (int b = 0; b < a.n_ib; ++b) {
-        const int o0 = a.ib[4 * b], o1 = a.ib[4 * b + 1], q0 = a.ib[4 * b + 2], q1 = a.ib[4 * b + 3];
-        for (int f = o0 + tid; f < o1; f += kThr) {
-          T v = T(0);
-          for (int q = q0; q < q1; ++q) {
-            const EPath p = a.paths[a.plist[q]];
-            const int loc = f - p.off1, u = loc / p.D1, m1 = loc - u * p.D1;
-            with_d3(p.D3, [&](auto d3c) {
-          constexpr int D3 = decltype(d3c)::value;
-              for (int j = 0; j < cnt; ++j) {
-                const T* c = cy + j * a.ncy + p.cyo + m1 * D3;
-                const T* gt = gts + j * a.nts + p.tso + u * D3;
-#pragma unroll
-                for (int m3 = 0; m3 < D3; ++m3) v += c[m3] * gt[m3];
-              }
-            });
-          }
-          gxs[f] += v;
+            for (int m3 = 0; m3 < D3; ++m3) gd[m3] = gt[m3];
+          });
         }
-      }
+      __syncthreads();
+        // G[j][path][m1][m3] = sum_u x[u][m1] gt[u][m3]
+        if (a.ncy > 0) {
+          for (JR it(a.ncy); it.j < cnt; it.next()) {
+            const int e = __ldg(a.cy_path + it.r);
+            const EPath p = a.paths[e & 0xffff];
+            const int m1 = (e >> 16) & 0xff, m3 = e >> 24;
+            const T* gt = gts + it.j * a.nts + p.tso + m3;
+            const T* xr = xs + p.off1 + m1;
+            T v = T(0);
+            for (int u = 0; u < p.mul1; ++u) v += xr[u * p.D1] * gt[u * p.D3];
+            G[it.j * a.ncy + it.r] = v;
+          }
+        }
+        // gx[u][m1] of every in1 block += sum over the chunk's edges and the block's paths
+        for (int b = 0; b < a.n_ib; ++b) {
+          const int o0 = a.ib[4 * b], o1 = a.ib[4 * b + 1], q0 = a.ib[4 * b + 2], q1 = a.ib[4 * b + 3];
+          if (q0 == q1) continue;
+          const int D1 = a.paths[a.plist[q0]].D1;   // every path of an in1 block shares its degree
+          for (int f = o0 + tid; f < o1; f += kThr) {
+            const int u = (f - o0) / D1, m1 = (f - o0) - u * D1;
+            T v = T(0);
+            for (int q = q0; q < q1; ++q) {
+              const EPath p = a.paths[a.plist[q]];
+              with_d3(p.D3, [&](auto d3c) {
+                constexpr int D3 = decltype(d3c)::value;
+                for (int j = 0; j < cnt; ++j) {
+                  const T* c = cy + j * a.ncy + p.cyo + m1 * D3;
+                  const T* gt = gts + j * a.nts + p.tso + u * D3;
+#pragma unroll
+                  for (int m3 = 0; m3 < D3; ++m3) v += c[m3] * gt[m3];
+                }
+              });
+            }
+            gxs[f] += v;
+          }
+        }
       __syncthreads();
       // gY[j][m2] of every in2 block = sum over the block's paths of C . G
-      for (int f = tid; f < cnt * a.d2; f += kThr) {
-        const int j = f / a.d2, col2 = f - j * a.d2;
+      for (JR it(a.d2); it.j < cnt; it.next()) {
+        const int j = it.j, col2 = it.r;
         int b = 0;
         while (b + 1 < a.n_yb && a.yb[4 * (b + 1)] <= col2) ++b;
         T v = T(0);
@@ -398,9 +430,7 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
     e.coff = static_cast<int>(C.size());
     e.cyo = ncy;
     e.tso = nts;
-    e.pwo = n_pw;
     e.aco = nac;
-    e.puo = n_pu;
     e.i1 = h.i1;
     e.i2 = h.i2;
     e.io = h.io;
@@ -429,16 +459,28 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   blocks(plan->in1, [](const EPath& e) { return e.i1; }, ib);
   blocks(plan->in2, [](const EPath& e) { return e.i2; }, yb);
   // path of every flattened entry of the per-edge rows the stages index
+  // packed as path | sub-index << 16 (cy: path | m1 << 16 | m3 << 24).  The (path, u)
+  // and (path, w) entries are ordered by output block size, so that a warp's
+  // threads mostly run the same specialised code.
+  if (ep.size() > 0xffff) return fail(CGTP_EUNSUPPORTED, "per-edge uvw weights: too many paths");
   std::vector<int> cy_path, pu_path, pw_path;
   bool vec = true;   // every weight-row segment a whole number of 16-byte vectors
   const int vw = plan->dtype == CGTP_F64 ? 2 : 4;
   if (plan->w_numel % vw) vec = false;
+  std::vector<int> by_d3(ep.size());
+  for (size_t pi = 0; pi < ep.size(); ++pi) by_d3[pi] = static_cast<int>(pi);
+  std::stable_sort(by_d3.begin(), by_d3.end(), [&](int x, int y) { return ep[x].D3 < ep[y].D3; });
   for (size_t pi = 0; pi < ep.size(); ++pi) {
     const EPath& e = ep[pi];
-    cy_path.insert(cy_path.end(), e.D1 * e.D3, static_cast<int>(pi));
-    pu_path.insert(pu_path.end(), e.mul1, static_cast<int>(pi));
-    pw_path.insert(pw_path.end(), e.mul_out, static_cast<int>(pi));
+    if (e.mul1 > 0x7fff || e.mul_out > 0x7fff)
+      return fail(CGTP_EUNSUPPORTED, "per-edge uvw weights: multiplicity above 32767");
+    for (int m1 = 0; m1 < e.D1; ++m1)
+      for (int m3 = 0; m3 < e.D3; ++m3) cy_path.push_back(static_cast<int>(pi) | m1 << 16 | m3 << 24);
     if (e.mul_out % vw || e.woff % vw) vec = false;
+  }
+  for (int pi : by_d3) {
+    for (int u = 0; u < ep[pi].mul1; ++u) pu_path.push_back(pi | u << 16);
+    for (int w = 0; w < ep[pi].mul_out; ++w) pw_path.push_back(pi | w << 16);
   }
   const size_t es = plan->dtype == CGTP_F64 ? 8 : 4;
   EState* st = new EState();
@@ -451,9 +493,8 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   st->n_ob = static_cast<int>(ob.size() / 4);
   st->n_ib = static_cast<int>(ib.size() / 4);
   st->n_yb = static_cast<int>(yb.size() / 4);
-  st->smem_fwd = es * (size_t(nac) + kCh * (size_t(plan->d1) + plan->d2 + ncy + nts));
-  st->smem_bwd = es * (2 * size_t(plan->d1) + kCh * (size_t(plan->d_out) + plan->d2 + 2 * ncy + nts)) +
-                 kCh * sizeof(int);
+  st->smem_fwd = es * (size_t(nac) + kCh * (size_t(plan->d1) + ncy + nts));
+  st->smem_bwd = es * (2 * size_t(plan->d1) + kCh * (size_t(plan->d_out) + plan->d2 + 2 * ncy + nts)) + kCh * sizeof(int);
   if (st->smem_bwd > kSmemCap || st->smem_fwd > kSmemCap) {
     delete st;
     return fail(CGTP_EUNSUPPORTED, "per-edge uvw weights: rows too long for shared memory");
