@@ -162,8 +162,8 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
   if (dtype != CGTP_F32 && dtype != CGTP_F64 && dtype != CGTP_BF16)
     return fail(CGTP_EINVAL, "dtype must be CGTP_F32, CGTP_F64 or CGTP_BF16");
   if (mode == CGTP_UVU && radial_k != 0) return fail(CGTP_EINVAL, "radial_k must be 0 in uvu mode");
-  if (mode == CGTP_UVW && (radial_k < 0 || radial_k > 16))
-    return fail(CGTP_EUNSUPPORTED, "uvw mode needs 0 <= radial_k <= 16 (0: one weight matrix per edge)");
+  if (mode == CGTP_UVW && (radial_k < 0 || radial_k > 8))
+    return fail(CGTP_EUNSUPPORTED, "uvw mode needs 0 <= radial_k <= 8 (0: one weight matrix per edge)");
   if (mode == CGTP_UVW && radial_k > 0 && dtype != CGTP_F32)
     return fail(CGTP_EUNSUPPORTED, "uvw mode with radial weights supports CGTP_F32 only");
   if (mode == CGTP_UVW && dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "uvw mode has no CGTP_BF16 kernels");

@@ -77,7 +77,8 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      output block of multiplicity mul1, appended in path order -- the muls of
  *      irreps_out are ignored) or CGTP_UVW (fully connected mixing into the
  *      blocks of irreps_out).
- *  dtype : CGTP_F32, CGTP_F64 or CGTP_BF16 (CGTP_UVW supports CGTP_F32 only).
+ *  dtype : CGTP_F32, CGTP_F64 or CGTP_BF16 (CGTP_UVW with radial_k > 0 supports
+ *      CGTP_F32 only; with radial_k = 0, CGTP_F32 and CGTP_F64).
  *      CGTP_BF16 (bfloat16 inputs, FP32 arithmetic and outputs; the pages'
  *      lower-precision future work) serves graph convolutions whose plan has
  *      l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} or m a multiple
@@ -86,7 +87,7 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *  radial_k : 0 for uvu.  For uvw, 0 selects one weight matrix per edge,
  *      W [E, sum_path mul1*mul_out] with each path's block laid out [u][w]
  *      (FP32 or FP64, l <= 3; "An Efficient Sparse Kernel Generator ...",
- *      Figure 3B/C), or the number K of radial functions (1..16), the weights
+ *      Figure 3B/C), or the number K of radial functions (1..8), the weights
  *      then being W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
  * the streaming node stage: node state for a chunk of nodes (default 4096,

@@ -61,7 +61,10 @@ def test_plan_create_rejects_bad_arguments_before_device_work():
         (b"8x9e", b"0e", b"9e", 0, 0, 0, cg.CGTP_EINVAL),       # l > 7
         (b"8x0e", b"2x0e", b"0e", 0, 0, 0, cg.CGTP_EUNSUPPORTED),  # in2 multiplicity
         (b"8x0e", b"0e", b"0e", 0, 0, 3, cg.CGTP_EINVAL),       # radial_k in uvu
-        (b"8x0e", b"0e", b"0e", 1, 1, 8, cg.CGTP_EUNSUPPORTED),  # uvw FP64
+        (b"8x0e", b"0e", b"0e", 1, 1, 8, cg.CGTP_EUNSUPPORTED),  # uvw FP64 with a radial basis
+        (b"8x0e", b"0e", b"0e", 1, 0, 9, cg.CGTP_EUNSUPPORTED),  # more than 8 radial functions
+        (b"8x0e", b"0e", b"0e", 1, 0, -1, cg.CGTP_EUNSUPPORTED),  # negative radial_k
+        (b"8x0e", b"0e", b"0e", 1, 2, 0, cg.CGTP_EUNSUPPORTED),  # per-edge uvw in bfloat16
         (b"8x0e", b"0e", b"0e", 7, 0, 0, cg.CGTP_EINVAL),       # bad mode
         (b"8x1o", b"1o", b"1o", 0, 0, 0, cg.CGTP_EINVAL),       # no parity-allowed path
     ]
