@@ -430,3 +430,124 @@ def conv_uvw_double_backward(plan, g, x, Y, W, ggx, ggY, ggW, rowptr, col):
     bwd = lambda g_, x_, Y_, W_: conv_uvw_backward(plan, g_, x_, Y_, W_, rowptr, col)
     return _double_backward(fwd, bwd, _f64(g), [_f64(x), _f64(Y), _f64(W)],
                             [_f64(ggx), _f64(ggY), _f64(ggW)])
+
+
+# ---------------------------------------------------------------------------
+# Mixed instruction lists: a connection mode per instruction (Figure 3B/C)
+# ---------------------------------------------------------------------------
+
+def mixed_layout(irreps_in1, irreps_in2, irreps_out, instructions, modes):
+    """Per-instruction offsets of the mixed convolution.
+
+    Every instruction (i1, i2, i_out) sums into block i_out of irreps_out.  A
+    "uvu" instruction keeps the channel (u -> u, so that block must have the
+    multiplicity of in1 block i1) with one weight per (edge, u); a "uvw"
+    instruction mixes channels with one weight per (edge, u, w).  Weights are
+    two per-edge arrays, each in instruction order: Wu [E, sum_uvu mul1] and
+    Ww [E, sum_uvw mul1*mul_out], each path's block of Ww laid out [u][w].
+    Returns (d1, d2, d_out, wu_numel, ww_numel, rows) with rows = dicts of l1,
+    l2, l3, mul1, mul_out, off1, off2, ooff, woff, mode."""
+    from .irreps import parse_irreps, irreps_offsets, irreps_dim
+    in1, in2, outr = parse_irreps(irreps_in1), parse_irreps(irreps_in2), parse_irreps(irreps_out)
+    o1, o2, oo = irreps_offsets(in1), irreps_offsets(in2), irreps_offsets(outr)
+    rows, wu, ww = [], 0, 0
+    for (i1, i2, io), mode in zip(instructions, modes):
+        m1, l1, p1 = in1[i1]
+        _, l2, p2 = in2[i2]
+        mo, l3, p3 = outr[io]
+        if not (abs(l1 - l2) <= l3 <= l1 + l2) or p3 != p1 * p2:
+            raise ValueError(f"forbidden path {(i1, i2, io)}")
+        if mode == "uvu":
+            if mo != m1:
+                raise ValueError("a uvu instruction needs an output block of multiplicity mul1")
+            rows.append(dict(l1=l1, l2=l2, l3=l3, mul1=m1, mul_out=m1, off1=o1[i1], off2=o2[i2],
+                             ooff=oo[io], woff=wu, mode="uvu"))
+            wu += m1
+        elif mode == "uvw":
+            rows.append(dict(l1=l1, l2=l2, l3=l3, mul1=m1, mul_out=mo, off1=o1[i1], off2=o2[i2],
+                             ooff=oo[io], woff=ww, mode="uvw"))
+            ww += m1 * mo
+        else:
+            raise ValueError(mode)
+    return irreps_dim(in1), irreps_dim(in2), irreps_dim(outr), wu, ww, rows
+
+
+def _mixed_t(r, xs_e, Y):
+    """t_e[u, m3] = sum_{m1,m2} C[m1,m2,m3] x[src][u,m1] Y[e][m2] of one instruction."""
+    C = real_cg_block(r["l1"], r["l2"], r["l3"])
+    D1, D2 = 2 * r["l1"] + 1, 2 * r["l2"] + 1
+    xs = xs_e[:, r["off1"]:r["off1"] + r["mul1"] * D1].reshape(-1, r["mul1"], D1)
+    ys = Y[:, r["off2"]:r["off2"] + D2]
+    return C, xs, ys, np.einsum("ijk,eui,ej->euk", C, xs, ys)
+
+
+def conv_mixed_forward(layout, x, Y, Wu, Ww, rowptr, col):
+    """out[n][i_out] = sum_{e in row n} sum_{instructions -> i_out} message, with
+    uvu: msg[u, m3] = Wu[e][u] t[u, m3];  uvw: msg[w, m3] = sum_u Ww[e][u][w] t[u, m3]."""
+    d1, d2, d_out, _, _, rows = layout
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    x, Y, Wu, Ww = _f64(x), _f64(Y), _f64(Wu), _f64(Ww)
+    E = col.size
+    msg = np.zeros((E, d_out))
+    xs_e = x[col]
+    for r in rows:
+        D3 = 2 * r["l3"] + 1
+        _, _, _, t = _mixed_t(r, xs_e, Y)
+        if r["mode"] == "uvu":
+            m = Wu[:, r["woff"]:r["woff"] + r["mul1"]][:, :, None] * t
+        else:
+            w = Ww[:, r["woff"]:r["woff"] + r["mul1"] * r["mul_out"]].reshape(-1, r["mul1"], r["mul_out"])
+            m = np.einsum("euw,euk->ewk", w, t)
+        msg[:, r["ooff"]:r["ooff"] + r["mul_out"] * D3] += m.reshape(E, -1)
+    out = np.zeros((len(rowptr) - 1, d_out))
+    np.add.at(out, csr_dst(rowptr), msg)     # CSR order within each receiver
+    return out
+
+
+def conv_mixed_backward(layout, g, x, Y, Wu, Ww, rowptr, col):
+    """(gx [N,d1], gY [E,d2], gWu, gWw) of conv_mixed_forward, by the chain rule."""
+    d1, d2, d_out, _, _, rows = layout
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    g, x, Y, Wu, Ww = _f64(g), _f64(x), _f64(Y), _f64(Wu), _f64(Ww)
+    E = col.size
+    xs_e, gd = x[col], g[csr_dst(rowptr)]
+    gxe, gY = np.zeros((E, d1)), np.zeros((E, d2))
+    gWu, gWw = np.zeros_like(Wu), np.zeros_like(Ww)
+    for r in rows:
+        D1, D2, D3 = 2 * r["l1"] + 1, 2 * r["l2"] + 1, 2 * r["l3"] + 1
+        C, xs, ys, t = _mixed_t(r, xs_e, Y)
+        go = gd[:, r["ooff"]:r["ooff"] + r["mul_out"] * D3].reshape(E, r["mul_out"], D3)
+        if r["mode"] == "uvu":
+            sl = slice(r["woff"], r["woff"] + r["mul1"])
+            gWu[:, sl] = np.einsum("euk,euk->eu", go, t)
+            gt = Wu[:, sl][:, :, None] * go
+        else:
+            sl = slice(r["woff"], r["woff"] + r["mul1"] * r["mul_out"])
+            w = Ww[:, sl].reshape(E, r["mul1"], r["mul_out"])
+            gWw[:, sl] = np.einsum("ewk,euk->euw", go, t).reshape(E, -1)
+            gt = np.einsum("euw,ewk->euk", w, go)
+        gxe[:, r["off1"]:r["off1"] + r["mul1"] * D1] += np.einsum("ijk,ej,euk->eui", C, ys, gt).reshape(E, -1)
+        gY[:, r["off2"]:r["off2"] + D2] += np.einsum("ijk,eui,euk->ej", C, xs, gt)
+    gx = np.zeros((len(rowptr) - 1, d1))
+    np.add.at(gx, col, gxe)
+    return gx, gY, gWu, gWw
+
+
+def conv_mixed_double_backward(layout, g, x, Y, Wu, Ww, ggx, ggY, ggWu, ggWw, rowptr, col):
+    """(d_g, d_x, d_Y, d_Wu, d_Ww).  The message is linear in x, in Y and in the
+    weights W = (Wu, Ww) taken together (each term holds one of them), so the
+    multilinearity identity runs over the three operands x, Y, W, the two weight
+    arrays being substituted together."""
+    g, x, Y, Wu, Ww = _f64(g), _f64(x), _f64(Y), _f64(Wu), _f64(Ww)
+    ggx, ggY, ggWu, ggWw = _f64(ggx), _f64(ggY), _f64(ggWu), _f64(ggWw)
+    F = lambda *a: conv_mixed_forward(layout, *a, rowptr, col)
+    B = lambda *a: conv_mixed_backward(layout, g, *a, rowptr, col)
+    d_g = F(ggx, Y, Wu, Ww) + F(x, ggY, Wu, Ww) + F(x, Y, ggWu, ggWw)
+    bx, by, bw = B(ggx, Y, Wu, Ww), B(x, ggY, Wu, Ww), B(x, Y, ggWu, ggWw)
+    d_x = by[0] + bw[0]
+    d_Y = bx[1] + bw[1]
+    d_Wu = bx[2] + by[2]
+    d_Ww = bx[3] + by[3]
+    return d_g, d_x, d_Y, d_Wu, d_Ww
