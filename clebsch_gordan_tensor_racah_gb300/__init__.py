@@ -36,7 +36,10 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_conv_double_backward_workspace", "cgtp_conv_double_backward",
            "cgtp_double_backward_workspace", "cgtp_double_backward",
            "cgtp_conv_forward_sh", "cgtp_conv_backward_sh", "cgtp_real_sh",
-           "cgtp_conv_forward_sh_radial", "cgtp_conv_backward_sh_radial"]
+           "cgtp_conv_forward_sh_radial", "cgtp_conv_backward_sh_radial",
+           "cgtp_mixed_plan_create", "cgtp_mixed_plan_destroy", "cgtp_mixed_plan_info",
+           "cgtp_mixed_conv_workspace", "cgtp_mixed_conv_forward", "cgtp_mixed_conv_backward",
+           "cgtp_mixed_conv_double_backward"]
 
 
 class CgtpError(RuntimeError):
@@ -84,8 +87,18 @@ def lib():
         dbl = ctypes.c_double
         L.cgtp_conv_forward_sh_radial.argtypes = [vp] * 5 + [dbl, dbl, vp, vp]
         L.cgtp_conv_backward_sh_radial.argtypes = [vp] * 6 + [dbl, dbl] + [vp] * 6
+        L.cgtp_mixed_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.c_char_p, ctypes.c_char_p,
+                                             ctypes.c_char_p, vp, vp, i32, i32]
+        L.cgtp_mixed_plan_destroy.argtypes = [vp]
+        L.cgtp_mixed_plan_destroy.restype = None
+        L.cgtp_mixed_plan_info.argtypes = [vp] + [ctypes.POINTER(i64)] * 5
+        L.cgtp_mixed_conv_workspace.argtypes = [vp, vp, ctypes.POINTER(i64)]
+        L.cgtp_mixed_conv_forward.argtypes = [vp] * 8 + [i64, vp]
+        L.cgtp_mixed_conv_backward.argtypes = [vp] * 12 + [i64, vp]
+        L.cgtp_mixed_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
         for name in EXPORTS:
-            if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy"):
+            if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy",
+                            "cgtp_mixed_plan_destroy"):
                 getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -366,3 +379,87 @@ def cgtp_conv_backward_sh_radial(plan, graph, gout, x, rvec, M, rbf_lo=0.5, rbf_
         _ptr(M, "M", dt), float(rbf_lo), float(rbf_hi), _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gR, "gR"),
         _ptr(grvec, "grvec"), _ptr(gM, "gM"), _stream(stream)))
     return gx, gY, gR, grvec, gM
+
+
+class MixedPlan:
+    """cgtp_mixed_plan_create: a connection mode ("uvu" or "uvw") per instruction, every
+    instruction summing into its block of irreps_out; weights Wu [E, wu_numel] and
+    Ww [E, ww_numel] in instruction order."""
+
+    def __init__(self, irreps_in1, irreps_in2, irreps_out, instructions, modes, dtype=None):
+        torch = _torch()
+        dtype = dtype or torch.float32
+        self.dtype = dtype
+        dt = {torch.float64: CGTP_F64, torch.bfloat16: CGTP_BF16}.get(dtype, CGTP_F32)
+        n = len(instructions)
+        if len(modes) != n:
+            raise ValueError("one mode per instruction")
+        ins = (ctypes.c_int * (3 * n))(*[v for t in instructions for v in t])
+        md = (ctypes.c_int * n)(*[{"uvu": CGTP_UVU, "uvw": CGTP_UVW}.get(m, -1) for m in modes])
+        h = ctypes.c_void_p()
+        _check(lib().cgtp_mixed_plan_create(ctypes.byref(h), irreps_in1.encode(), irreps_in2.encode(),
+                                            irreps_out.encode(), ctypes.cast(ins, ctypes.c_void_p),
+                                            ctypes.cast(md, ctypes.c_void_p), n, dt))
+        self._h = h
+        d = [ctypes.c_int64() for _ in range(5)]
+        _check(lib().cgtp_mixed_plan_info(h, *[ctypes.byref(v) for v in d]))
+        self.d1, self.d2, self.d_out, self.wu_numel, self.ww_numel = (v.value for v in d)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def workspace(self, graph, device):
+        nb = ctypes.c_int64()
+        _check(lib().cgtp_mixed_conv_workspace(self._h, graph.handle, ctypes.byref(nb)))
+        return _workspace(nb.value, device), nb.value
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.cgtp_mixed_plan_destroy(h)
+            self._h = None
+
+
+def cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=None, stream=None):
+    """out [N, d_out] of the convolution with mixed instruction modes."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.dtype, device=x.device)
+    ws, nb = plan.workspace(graph, x.device)
+    dt = plan.dtype
+    _check(lib().cgtp_mixed_conv_forward(plan.handle, graph.handle, _ptr(x, "x", dt), _ptr(Y, "Y", dt),
+                                         _ptr(Wu, "Wu", dt), _ptr(Ww, "Ww", dt), _ptr(out, "out", dt),
+                                         _ptr(ws, "workspace"), nb, _stream(stream)))
+    return out
+
+
+def cgtp_mixed_conv_backward(plan, graph, gout, x, Y, Wu, Ww, stream=None):
+    """(gx, gY, gWu, gWw) of cgtp_mixed_conv_forward."""
+    torch = _torch()
+    gx, gY = torch.empty_like(x), torch.empty_like(Y)
+    gWu = torch.empty_like(Wu) if Wu is not None else None
+    gWw = torch.empty_like(Ww) if Ww is not None else None
+    ws, nb = plan.workspace(graph, x.device)
+    dt = plan.dtype
+    _check(lib().cgtp_mixed_conv_backward(
+        plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(Y, "Y", dt), _ptr(Wu, "Wu", dt),
+        _ptr(Ww, "Ww", dt), _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gWu, "gWu"), _ptr(gWw, "gWw"),
+        _ptr(ws, "workspace"), nb, _stream(stream)))
+    return gx, gY, gWu, gWw
+
+
+def cgtp_mixed_conv_double_backward(plan, graph, gout, x, Y, Wu, Ww, ggx, ggY, ggWu, ggWw, stream=None):
+    """(d_gout, d_x, d_Y, d_Wu, d_Ww) of S = <ggx, gx> + <ggY, gY> + <ggWu, gWu> + <ggWw, gWw>."""
+    torch = _torch()
+    d_g, d_x, d_Y = torch.empty_like(gout), torch.empty_like(x), torch.empty_like(Y)
+    d_Wu = torch.empty_like(Wu) if Wu is not None else None
+    d_Ww = torch.empty_like(Ww) if Ww is not None else None
+    ws, nb = plan.workspace(graph, x.device)
+    dt = plan.dtype
+    _check(lib().cgtp_mixed_conv_double_backward(
+        plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(Y, "Y", dt), _ptr(Wu, "Wu", dt),
+        _ptr(Ww, "Ww", dt), _ptr(ggx, "ggx", dt), _ptr(ggY, "ggY", dt), _ptr(ggWu, "ggWu", dt),
+        _ptr(ggWw, "ggWw", dt), _ptr(d_g, "d_gout"), _ptr(d_x, "d_x"), _ptr(d_Y, "d_Y"), _ptr(d_Wu, "d_Wu"),
+        _ptr(d_Ww, "d_Ww"), _ptr(ws, "workspace"), nb, _stream(stream)))
+    return d_g, d_x, d_Y, d_Wu, d_Ww

@@ -278,6 +278,58 @@ cgtp_status cgtp_real_sh(int lmax, const double* rvec, int64_t n, double* Y, dou
  * the coefficient blocks). */
 cgtp_status cgtp_real_cg_block(int l1, int l2, int l3, double* block, int64_t capacity);
 
+/*
+ * Mixed instruction lists: a connection mode per instruction ("An Efficient
+ * Sparse Kernel Generator ...", Figure 3B/C: channel-wise (uvu) and fully
+ * connected (uvw) weights; Figure 4B: fused with the receiver sum).
+ *
+ * cgtp_mixed_plan_create -- instr[i] = (i_in1, i_in2, i_out) with modes[i] in
+ *  {CGTP_UVU, CGTP_UVW}; every instruction sums its message into block i_out of
+ *  irreps_out (d_out = dim(irreps_out)).  A uvu instruction keeps the channel
+ *  (block i_out must have the multiplicity of in1 block i_in1, else
+ *  CGTP_EINVAL); a uvw instruction mixes channels.  Weights are two per-edge
+ *  arrays in instruction order: Wu [E, wu_numel] (mul1 per uvu instruction) and
+ *  Ww [E, ww_numel] (mul1*mul_out per uvw instruction, each block [u][w]).
+ *  dtype CGTP_F32 or CGTP_F64 (else CGTP_EUNSUPPORTED); the uvw instructions
+ *  need l <= 3.  The plan owns two single-mode plans and a few KB of tables.
+ * Must be called with the target device current.
+ */
+typedef struct cgtp_mixed_plan_s* cgtp_mixed_plan;
+cgtp_status cgtp_mixed_plan_create(cgtp_mixed_plan* plan, const char* irreps_in1, const char* irreps_in2,
+                                   const char* irreps_out, const cgtp_instr* instr, const int* modes, int n_instr,
+                                   int dtype);
+void cgtp_mixed_plan_destroy(cgtp_mixed_plan plan);
+/* d1, d2, d_out and the row lengths of Wu and Ww (0 when the plan has no
+ * instruction of that mode).  Any pointer may be NULL. */
+cgtp_status cgtp_mixed_plan_info(cgtp_mixed_plan plan, int64_t* d1, int64_t* d2, int64_t* d_out,
+                                 int64_t* wu_numel, int64_t* ww_numel);
+/* Bytes of device workspace the three mixed entry points need on this graph
+ * (one size for all three). */
+cgtp_status cgtp_mixed_conv_workspace(cgtp_mixed_plan plan, cgtp_graph graph, int64_t* bytes);
+/*
+ * cgtp_mixed_conv_forward -- out [N,d_out] (overwritten) from x [N,d1], Y [E,d2],
+ *  Wu, Ww (NULL allowed for a mode the plan does not use).
+ * cgtp_mixed_conv_backward -- gx [N,d1], gY [E,d2], gWu, gWw (overwritten) for
+ *  gout [N,d_out].
+ * cgtp_mixed_conv_double_backward -- for cotangents ggx, ggY, ggWu, ggWw of
+ *  (gx, gY, gWu, gWw): d_gout [N,d_out], d_x, d_Y, d_Wu, d_Ww (overwritten).  The
+ *  message is linear in x, in Y and in the weights (Wu, Ww) taken together.
+ * workspace: a 256-byte aligned device buffer of at least the size
+ * cgtp_mixed_conv_workspace reports; errors as for the single-mode entry points.
+ * Calls with the same plan must not overlap on the GPU.
+ */
+cgtp_status cgtp_mixed_conv_forward(cgtp_mixed_plan plan, cgtp_graph graph, const void* x, const void* Y,
+                                    const void* Wu, const void* Ww, void* out, void* workspace,
+                                    int64_t workspace_size, void* stream);
+cgtp_status cgtp_mixed_conv_backward(cgtp_mixed_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                                     const void* Y, const void* Wu, const void* Ww, void* gx, void* gY, void* gWu,
+                                     void* gWw, void* workspace, int64_t workspace_size, void* stream);
+cgtp_status cgtp_mixed_conv_double_backward(cgtp_mixed_plan plan, cgtp_graph graph, const void* gout, const void* x,
+                                            const void* Y, const void* Wu, const void* Ww, const void* ggx,
+                                            const void* ggY, const void* ggWu, const void* ggWw, void* d_gout,
+                                            void* d_x, void* d_Y, void* d_Wu, void* d_Ww, void* workspace,
+                                            int64_t workspace_size, void* stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* cgtp_last_error(void);
 

@@ -100,3 +100,27 @@ def test_library_sh_matches_oracle():
     u = r / np.linalg.norm(r, axis=1, keepdims=True)
     assert np.abs(Y - ocg.sh_real_concat(7, u)).max() < 1e-12
     assert np.abs(dY - ocg.sh_real_concat_jacobian(7, r)).max() < 1e-11
+
+
+def test_mixed_plan_create_rejects_bad_arguments_before_device_work():
+    L = cg.lib()
+    h = ctypes.c_void_p()
+    ins = (ctypes.c_int * 6)(0, 0, 0, 1, 1, 0)
+    good = (ctypes.c_int * 2)(cg.CGTP_UVU, cg.CGTP_UVW)
+    bad_mode = (ctypes.c_int * 2)(cg.CGTP_UVU, 5)
+    cases = [
+        (b"2x0e+2x1o", b"0e+1o", b"2x0e", good, 2, cg.CGTP_BF16, cg.CGTP_EUNSUPPORTED),  # bfloat16
+        (b"2x0e+2x1o", b"0e+1o", b"3x0e", good, 2, cg.CGTP_F32, cg.CGTP_EINVAL),   # uvu changes multiplicity
+        (b"2x0e+2x1o", b"0e+1o", b"2x0e", bad_mode, 2, cg.CGTP_F32, cg.CGTP_EINVAL),
+        (b"2x0e+2x1o", b"0e+1o", b"2x0e", good, 0, cg.CGTP_F32, cg.CGTP_EINVAL),   # empty list
+        (b"2x0e+2x1o+", b"0e+1o", b"2x0e", good, 2, cg.CGTP_F32, cg.CGTP_EINVAL),  # bad irreps
+    ]
+    for in1, in2, out, modes, n, dt, want in cases:
+        st = L.cgtp_mixed_plan_create(ctypes.byref(h), in1, in2, out, ctypes.cast(ins, ctypes.c_void_p),
+                                      ctypes.cast(modes, ctypes.c_void_p), n, dt)
+        assert st == want, (in1, out, n, dt, st, L.cgtp_last_error())
+        assert not h.value
+    oob = (ctypes.c_int * 3)(0, 0, 4)
+    st = L.cgtp_mixed_plan_create(ctypes.byref(h), b"2x0e", b"0e", b"2x0e", ctypes.cast(oob, ctypes.c_void_p),
+                                  ctypes.cast(good, ctypes.c_void_p), 1, cg.CGTP_F32)
+    assert st == cg.CGTP_EINVAL and b"out of range" in L.cgtp_last_error()
