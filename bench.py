@@ -58,6 +58,7 @@ CONFIGS = {
     "nequip_bf16": dict(name="nequip", dtype="bfloat16", over={}),
     "nequip_sh": dict(name="nequip", dtype="float32", over={}, sh=True),
     "uvw_edge": dict(name="uvw_edge", dtype="float32", over={}),
+    "mixed": dict(name="mixed", dtype="float32", over={}),
     "uvw": dict(name="uvw", dtype="float32", over={}),
 }
 
@@ -70,12 +71,17 @@ def build_inputs(cfgkey, device, nodes=None):
     spec = dict(wl.SPECS[c["name"]])
     tdt = {"float64": torch.float64, "bfloat16": torch.bfloat16}.get(c["dtype"], torch.float32)
     mode = spec["mode"]
-    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
-                   radial_k=spec.get("K", 0) if mode == "uvw" else 0)
+    if mode == "mixed":
+        plan = cg.MixedPlan(spec["in1"], spec["in2"], spec["out"], spec["instructions"], spec["modes"], tdt)
+        w_numel = (plan.wu_numel, plan.ww_numel)
+    else:
+        plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
+                       radial_k=spec.get("K", 0) if mode == "uvw" else 0)
+        w_numel = plan.w_numel
     over = dict(c["over"])
     if nodes:
         over["B" if spec["graph"] is None else "N"] = int(nodes)
-    w = wl.make(c["name"], plan.w_numel, seed=0, dtype="float32" if tdt == torch.bfloat16 else c["dtype"], **over)
+    w = wl.make(c["name"], w_numel, seed=0, dtype="float32" if tdt == torch.bfloat16 else c["dtype"], **over)
     host = {k: v for k, v in w.items() if isinstance(v, np.ndarray)}
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(device) for k, v in host.items()}
     if tdt == torch.bfloat16:   # features and weights stored as bfloat16 (FP32 arithmetic and outputs)
@@ -113,6 +119,24 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
 
         def bwd(g, outs):
             return cg.cgtp_conv_backward_sh(plan, graph, g, x, rv, W)
+        return fwd, bwd, units, bf, bb, (N, plan.d_out)
+    if "Wu" in dev:   # mixed instruction list: two per-edge weight arrays
+        N, E = w["N"], w["E"]
+        x, Y, Wu, Ww = dev["x"], dev["Y"], dev["Wu"], dev["Ww"]
+        units = E
+        idx = 4 * (N + 1 + E)
+        nin = N * plan.d1 + E * plan.d2 + Wu.numel() + Ww.numel()
+        bf = es * (nin + N * plan.d_out) + idx
+        bb = es * (2 * nin + N * plan.d_out) + idx + 8 * E
+        ws, _ = plan.workspace(graph, x.device)
+        import torch
+        res = (torch.empty_like(x), torch.empty_like(Y), torch.empty_like(Wu), torch.empty_like(Ww))
+
+        def fwd(out):
+            return cg.cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=out, workspace=ws)
+
+        def bwd(g, outs):
+            return cg.cgtp_mixed_conv_backward(plan, graph, g, x, Y, Wu, Ww, workspace=ws, outs=res)
         return fwd, bwd, units, bf, bb, (N, plan.d_out)
     if "rowptr" in dev:
         N, E = w["N"], w["E"]
@@ -161,6 +185,21 @@ def algorithmic_flops(plan, n_nodes, n_edges):
     """
     fe = be = fn = bn = 0
     K = getattr(plan, "radial_k", 0)
+    if plan.mode == "mixed":   # per instruction, with its own mode (the uvw ones with weights per edge)
+        import clebsch_gordan_tensor_racah_gb300 as cg
+        from clebsch_gordan_tensor_racah_gb300.workloads import irreps_terms
+        a, b, o = (irreps_terms(s) for s in (plan.irreps[0], plan.irreps[1], plan.irreps[2]))
+        for (i1, i2, io), m in zip(plan.instructions, plan.modes):
+            (mul1, l1), (_, l2), (mul_out, l3) = a[i1], b[i2], o[io]
+            D1, D3 = 2 * l1 + 1, 2 * l3 + 1
+            NF, nnz = D1 * D3, int(np.count_nonzero(cg.cgtp_real_cg_block(l1, l2, l3)))
+            if m == "uvu":
+                fe += 2 * nnz + mul1 * (D1 + 2 * NF)
+                be += 4 * nnz + mul1 * (6 * NF + 3 * D3)
+            else:
+                fe += 2 * nnz + mul1 * 2 * NF + 2 * mul1 * mul_out * D3
+                be += 4 * nnz + mul1 * 4 * NF + 3 * 2 * mul1 * mul_out * D3 + 2 * mul1 * NF
+        return fe * n_edges, be * n_edges
     for p in range(plan.n_paths):
         ints, C = plan.path(p)
         l1, l2, l3, mul1, mul_out = ints[:5]
@@ -248,6 +287,17 @@ def time_oracle_sample(cfgkey, budget_s=8.0):
     from oracle import conv as oconv, irreps as oirr
     c = CONFIGS[cfgkey]
     spec = wl.SPECS[c["name"]]
+    if spec["mode"] == "mixed":
+        lay = oconv.mixed_layout(spec["in1"], spec["in2"], spec["out"], spec["instructions"], spec["modes"])
+        N = 60
+        w = wl.make(c["name"], (lay[3], lay[4]), seed=0, dtype=c["dtype"], N=N)
+        units, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            out = oconv.conv_mixed_forward(lay, w["x"], w["Y"], w["Wu"], w["Ww"], w["rowptr"], w["col"])
+            oconv.conv_mixed_backward(lay, out, w["x"], w["Y"], w["Wu"], w["Ww"], w["rowptr"], w["col"])
+            units += w["E"]
+        dt = time.perf_counter() - t0
+        return units / dt, f"{N}-node graph of the same recipe ({w['E']} edges), fwd+bwd repeated for {dt:.1f} s"
     oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], spec["mode"])
     if spec["graph"] is None:
         B = 64
@@ -290,7 +340,16 @@ def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
     import torch
     import clebsch_gordan_tensor_racah_gb300 as cg
     gen = torch.Generator(g.device).manual_seed(2)
-    if "rowptr" in dev:
+    if "Wu" in dev:
+        c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen)
+             for k in ("x", "Y", "Wu", "Ww")}
+        ws, _ = plan.workspace(graph, g.device)
+
+        def run():
+            return cg.cgtp_mixed_conv_double_backward(plan, graph, g, dev["x"], dev["Y"], dev["Wu"], dev["Ww"],
+                                                      c["x"], c["Y"], c["Wu"], c["Ww"], workspace=ws)
+        n_op = 3   # x, Y and the weights (Wu, Ww) together: 3 forwards + 3 backwards of each single-mode plan
+    elif "rowptr" in dev:
         keys = ["x", "Y", "W"] if "W" in dev else ["x", "Y", "R", "M"]
         c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen) for k in keys}
         WR = dev["W"] if "W" in dev else dev["R"]
@@ -351,7 +410,9 @@ def config_block(cfgkey, w, n_gpus):
                       "mace": "MACE-like uvu conv (5k nodes, Poisson(40) in-degree, 128x(0e,1o,2e), SH l<=3)",
                       "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
                       "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)",
-                      "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))"}[spec],
+                      "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))",
+                      "mixed": "mixed uvu/uvw conv (10k nodes x 32 in-edges, 32x(0e,1o,2e), SH l<=2; "
+                               "0e outputs uvw with per-edge weights, 1o and 2e outputs uvu)"}[spec],
          "step": "conv forward + backward" if "N" in w else "batched forward + backward",
          "precision": "bfloat16 inputs, FP32 arithmetic and outputs" if c["dtype"] == "bfloat16" else c["dtype"],
          "edge_features": "raw edge vectors, harmonics evaluated in the kernels" if c.get("sh") else "harmonics Y",
@@ -534,9 +595,14 @@ def main():
     t_alu = dom_flops / (alu_peak * 1e12)
     kname = {("uvu", "forward"): "uvu_forward3_kernel", ("uvu", "backward"): "uvu_backward3_kernel",
              ("uvwe", "forward"): "uvwe_fwd_kernel", ("uvwe", "backward"): "uvwe_bwd_kernel",
+             ("mixed", "forward"): "mixed forward (uvu_forward3_kernel + uvwe_fwd_kernel + fold)",
+             ("mixed", "backward"): "mixed backward (uvu_backward3_kernel + uvwe_bwd_kernel + adds)",
              ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
              ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[
         ("uvwe" if plan.mode == "uvw" and plan.radial_k == 0 else plan.mode, dominant)]
+    launches = 2 * args.steps
+    if plan.mode == "mixed":   # uvw + uvu forwards and a fold; unfold, two backwards, two adds
+        launches = 7 * args.steps
     if "N" not in w:
         kname = {"forward": "bt_forward_kernel", "backward": "bt_backward_kernel"}[dominant]
     if t_hbm >= t_alu:
@@ -562,7 +628,7 @@ def main():
             "data": "synthetic",
             "config": config_block(args.config, w, world),
             "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk}
     if not args.no_double_backward and tdt != torch.bfloat16 and not CONFIGS[args.config].get("sh"):
         line["double_backward"] = time_double_backward(plan, graph, w, dev, g, stream, units, roofline)

@@ -404,6 +404,9 @@ class MixedPlan:
         d = [ctypes.c_int64() for _ in range(5)]
         _check(lib().cgtp_mixed_plan_info(h, *[ctypes.byref(v) for v in d]))
         self.d1, self.d2, self.d_out, self.wu_numel, self.ww_numel = (v.value for v in d)
+        self.mode, self.out_dtype = "mixed", dtype
+        self.irreps = (irreps_in1, irreps_in2, irreps_out)
+        self.instructions, self.modes = [tuple(t) for t in instructions], list(modes)
 
     @property
     def handle(self):
@@ -421,12 +424,19 @@ class MixedPlan:
             self._h = None
 
 
-def cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=None, stream=None):
-    """out [N, d_out] of the convolution with mixed instruction modes."""
+def _mixed_ws(plan, graph, device, workspace):
+    if workspace is None:
+        return plan.workspace(graph, device)
+    return workspace, workspace.numel()
+
+
+def cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=None, stream=None, workspace=None):
+    """out [N, d_out] of the convolution with mixed instruction modes (workspace: an
+    optional uint8 device buffer of at least plan.workspace(...) bytes)."""
     torch = _torch()
     if out is None:
         out = torch.empty(graph.N, plan.d_out, dtype=plan.dtype, device=x.device)
-    ws, nb = plan.workspace(graph, x.device)
+    ws, nb = _mixed_ws(plan, graph, x.device, workspace)
     dt = plan.dtype
     _check(lib().cgtp_mixed_conv_forward(plan.handle, graph.handle, _ptr(x, "x", dt), _ptr(Y, "Y", dt),
                                          _ptr(Wu, "Wu", dt), _ptr(Ww, "Ww", dt), _ptr(out, "out", dt),
@@ -434,13 +444,16 @@ def cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=None, stream=None):
     return out
 
 
-def cgtp_mixed_conv_backward(plan, graph, gout, x, Y, Wu, Ww, stream=None):
-    """(gx, gY, gWu, gWw) of cgtp_mixed_conv_forward."""
+def cgtp_mixed_conv_backward(plan, graph, gout, x, Y, Wu, Ww, stream=None, workspace=None, outs=None):
+    """(gx, gY, gWu, gWw) of cgtp_mixed_conv_forward (outs: optional preallocated results)."""
     torch = _torch()
-    gx, gY = torch.empty_like(x), torch.empty_like(Y)
-    gWu = torch.empty_like(Wu) if Wu is not None else None
-    gWw = torch.empty_like(Ww) if Ww is not None else None
-    ws, nb = plan.workspace(graph, x.device)
+    if outs is None:
+        gx, gY = torch.empty_like(x), torch.empty_like(Y)
+        gWu = torch.empty_like(Wu) if Wu is not None else None
+        gWw = torch.empty_like(Ww) if Ww is not None else None
+    else:
+        gx, gY, gWu, gWw = outs
+    ws, nb = _mixed_ws(plan, graph, x.device, workspace)
     dt = plan.dtype
     _check(lib().cgtp_mixed_conv_backward(
         plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(Y, "Y", dt), _ptr(Wu, "Wu", dt),
@@ -449,13 +462,14 @@ def cgtp_mixed_conv_backward(plan, graph, gout, x, Y, Wu, Ww, stream=None):
     return gx, gY, gWu, gWw
 
 
-def cgtp_mixed_conv_double_backward(plan, graph, gout, x, Y, Wu, Ww, ggx, ggY, ggWu, ggWw, stream=None):
+def cgtp_mixed_conv_double_backward(plan, graph, gout, x, Y, Wu, Ww, ggx, ggY, ggWu, ggWw, stream=None,
+                                    workspace=None):
     """(d_gout, d_x, d_Y, d_Wu, d_Ww) of S = <ggx, gx> + <ggY, gY> + <ggWu, gWu> + <ggWw, gWw>."""
     torch = _torch()
     d_g, d_x, d_Y = torch.empty_like(gout), torch.empty_like(x), torch.empty_like(Y)
     d_Wu = torch.empty_like(Wu) if Wu is not None else None
     d_Ww = torch.empty_like(Ww) if Ww is not None else None
-    ws, nb = plan.workspace(graph, x.device)
+    ws, nb = _mixed_ws(plan, graph, x.device, workspace)
     dt = plan.dtype
     _check(lib().cgtp_mixed_conv_double_backward(
         plan.handle, graph.handle, _ptr(gout, "gout", dt), _ptr(x, "x", dt), _ptr(Y, "Y", dt), _ptr(Wu, "Wu", dt),

@@ -163,10 +163,27 @@ SPECS = {
                   dtype="float32"),
     "uvw": dict(in1="64x0e+64x1o+64x2e", in2=_sh_irreps(2), out="64x0e+64x1o+64x2e", mode="uvw",
                 lmax_sh=2, N=200_000, deg=32, graph="fixed", K=8, dtype="float32"),
+    # mixed instruction list on the NequIP-like graph: 32x(0e,1o,2e) x SH l<=2 -> 32x(0e,1o,2e),
+    # the scalar output block fed fully connected (uvw), the others channel-wise (uvu);
+    # every parity-allowed (i_in1, i_in2, i_out), written out
+    "mixed": dict(in1="32x0e+32x1o+32x2e", in2=_sh_irreps(2), out="32x0e+32x1o+32x2e", mode="mixed",
+                  instructions=[(0, 0, 0), (0, 1, 1), (0, 2, 2), (1, 0, 1), (1, 1, 0), (1, 1, 2), (1, 2, 1),
+                                (2, 0, 2), (2, 1, 1), (2, 2, 0), (2, 2, 2)],
+                  modes=["uvw", "uvu", "uvu", "uvu", "uvw", "uvu", "uvu", "uvu", "uvu", "uvw", "uvu"],
+                  lmax_sh=2, N=10_000, deg=32, graph="fixed", wscale="deg", dtype="float32"),
     # uvw with a weight matrix per edge (K = 0): 16x(0e,1o,2e) on the NequIP-like graph
     "uvw_edge": dict(in1="16x0e+16x1o+16x2e", in2=_sh_irreps(2), out="16x0e+16x1o+16x2e", mode="uvw",
                      lmax_sh=2, N=10_000, deg=32, graph="fixed", K=0, wscale="deg", dtype="float32"),
 }
+
+
+def irreps_terms(s):
+    """[(mul, l), ...] of an irreps string."""
+    out = []
+    for term in s.split("+"):
+        mul, ir = (term.split("x") if "x" in term else ("1", term))
+        out.append((int(mul), int(ir[:-1])))
+    return out
 
 
 def irreps_dim(s):
@@ -181,10 +198,11 @@ def make(name, w_numel, seed=0, dtype=None, **over):
     """Draw one workload.  Returns a dict of numpy arrays plus the spec entries.
 
     ``w_numel`` is the weight count of one edge (uvu) or of one radial row of M
-    (uvw), taken from the caller's own plan.
+    (uvw), taken from the caller's own plan; for a mixed instruction list it is the
+    pair (uvu weights, uvw weights) of one edge.
 
     Keys: rowptr, col (int32) for graph workloads; x (or x1), Y (or x2), W for
-    uvu; R, M for uvw; plus 'spec', 'N', 'E' (or 'B').
+    uvu; R, M for uvw; Wu, Ww for mixed lists; plus 'spec', 'N', 'E' (or 'B').
     """
     spec = dict(SPECS[name])
     spec.update(over)
@@ -212,7 +230,11 @@ def make(name, w_numel, seed=0, dtype=None, **over):
     Y = sh_real(spec["lmax_sh"], vec).astype(dt)
     x = _normal(rng, (N, d1), dt)
     res.update(rowptr=rowptr, col=col, N=N, E=E, x=x, Y=Y)
-    if spec["mode"] == "uvu" or int(spec.get("K", 1)) == 0:   # weights per edge
+    if spec["mode"] == "mixed":   # two per-edge weight arrays
+        scale = 1.0 / math.sqrt(float(spec["deg"]))
+        wu, ww = (int(v) for v in w_numel)
+        res.update(Wu=_normal(rng, (E, wu), dt, scale), Ww=_normal(rng, (E, ww), dt, scale / math.sqrt(32.0)))
+    elif spec["mode"] == "uvu" or int(spec.get("K", 1)) == 0:   # weights per edge
         scale = 1.0 if spec["wscale"] is None else 1.0 / math.sqrt(float(spec["deg"]))
         W = _normal(rng, (E, int(w_numel)), dt, scale)
         res.update(W=W)

@@ -160,3 +160,14 @@ def test_mixed_double_backward_exact_directional_differences():
         lhs = S(g, b) - S(g, a)
         rhs = float(np.sum(d[j + 1] * dj))
         assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(rhs)), (j, lhs, rhs)
+
+
+def test_mixed_bench_workload_lists_every_allowed_instruction():
+    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+    spec = wl.SPECS["mixed"]
+    full = irreps.make_plan(spec["in1"], spec["in2"], spec["out"], "uvw")
+    assert sorted(spec["instructions"]) == sorted((p.i1, p.i2, p.i_out) for p in full.paths)
+    lay = conv.mixed_layout(spec["in1"], spec["in2"], spec["out"], spec["instructions"], spec["modes"])
+    # uvw exactly for the instructions into the scalar block
+    assert all((m == "uvw") == (r["l3"] == 0) for m, r in zip(spec["modes"], lay[5]))
+    assert lay[4] == 3 * 32 * 32 and lay[3] == 8 * 32
