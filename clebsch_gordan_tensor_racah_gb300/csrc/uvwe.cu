@@ -18,7 +18,7 @@
 // staged through shared memory.  The weight stream is read with consecutive
 // threads on consecutive weights (forward: one thread per (path, w), all the
 // chunk's edges in flight; backward: one thread per (edge, path, u) walking its
-// row), after an L2 prefetch of the chunk's rows.  Every output, gx and gY
+// row); the forward prefetches each chunk's contiguous rows into L2.  Every output, gx and gY
 // element has one owning thread, so no atomics are needed.  This serves plans
 // of any multiplicities with l <= 3; the per-edge weights are the dominant stream.
 #include <cuda_runtime.h>
@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
 
 // V: weight-row vector width (1, or 16 bytes when every row segment is aligned)
 //
-// Backward over a sender's chunks: staging (edge ids, g rows, Y rows, weight
-// prefetch), cy, the fused t / gW / gt stage, G and gx, gY -- five block
+// Backward over a sender's chunks: staging (edge ids, g rows, Y rows), cy, the
+// fused t / gW / gt stage, G and gx, gY -- five block
 // barriers a chunk.  (Overlapping gY and G with the next chunk's staging
 // measured slower: the gathers' latency then sits inside the compute phases.)
 template <typename T, int V>
@@ -290,8 +290,6 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
     for (int t0 = t_begin; t0 < t_end; t0 += kCh) {
       const int cnt = min(kCh, t_end - t0);
       const int* eid = eids;
-      for (int j = 0; j < cnt; ++j)
-        prefetch_l2(a.W + (size_t)a.col[t0 + j] * a.w_numel, sizeof(T) * (size_t)a.w_numel);
       __syncthreads();
       if (tid < cnt) eids[tid] = a.col[t0 + tid];
       for (JR it(a.d_out); it.j < cnt; it.next())
@@ -626,9 +624,12 @@ static cgtp_status bwd_t(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
   a.rowptr = g->t_rowptr;
   a.col = g->t_eid;
   a.t_dst = g->t_dst;
-  // four senders per SM: at full occupancy the scattered weight rows and gW
-  // writes of more CTAs contend for L2 and the backward slows down (4.1 vs 3.35 ms)
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g->N, (int64_t)plan->num_sms * 4)));
+  // as many senders in flight as fit; the backward's weight rows are scattered, so it
+  // relies on occupancy rather than an L2 prefetch (with the prefetch, a full grid
+  // thrashed L2: 4.1 ms; without it 3.22 ms against 3.35 ms at four CTAs per SM)
+  int occ = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, uvwe_bwd_kernel<T, 1>, kThr, st->smem_bwd);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g->N, (int64_t)plan->num_sms * std::max(occ, 1))));
   constexpr int kVec = 16 / sizeof(T);
   const bool vec = st->vec && (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0);
   if (vec)
