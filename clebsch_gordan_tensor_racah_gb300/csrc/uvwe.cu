@@ -18,9 +18,10 @@
 // staged through shared memory.  The weight stream is read with consecutive
 // threads on consecutive weights (forward: one thread per (path, w), all the
 // chunk's edges in flight; backward: one thread per (edge, path, u) walking its
-// row); the forward prefetches each chunk's contiguous rows into L2.  Every output, gx and gY
-// element has one owning thread, so no atomics are needed.  This serves plans
-// of any multiplicities with l <= 3; the per-edge weights are the dominant stream.
+// row); the forward prefetches each chunk's contiguous rows into L2.  Every
+// output, gx and gY element has one owning thread, so no atomics are needed.
+// This serves plans of any multiplicities with l <= 3; the per-edge weights are
+// the dominant stream.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -71,9 +72,10 @@ struct EArgs {
   const int* ib;       // per in1 block: same
   const int* yb;       // per in2 block: same
   const int* plist;
-  const int* cy_path;  // path of each entry of a cy row [ncy]
-  const int* pu_path;  // path of each (path, u) pair [n_pu]
-  const int* pw_path;  // path of each (path, w) pair [n_pw]
+  // per-entry tables, packed path | sub-index << 16:
+  const int* cy_path;  // entries of a cy row [ncy]: path | m1 << 16 | m3 << 24
+  const int* pu_path;  // (path, u) pairs [n_pu], ordered by D3: path | u << 16
+  const int* pw_path;  // (path, w) pairs [n_pw], ordered by D3: path | w << 16
 };
 
 // Ask L2 for the 128-byte lines of [p, p + bytes), spread over the block's threads.
