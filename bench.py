@@ -171,6 +171,21 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     return fwd, bwd, units, bf, bb, out_shape
 
 
+def launches_per_step(cfgkey, plan, w):
+    """Kernels of this library one timed step (forward + backward) launches."""
+    if plan.mode == "mixed":   # uvw and uvu forwards, fold; unfold, uvu and uvw backwards, two adds
+        return 8
+    if CONFIGS[cfgkey].get("sh"):   # forward, backward, per-edge chain rule to the edge vectors
+        return 3
+    if plan.mode == "uvw" and plan.radial_k > 0:
+        # per streamed node chunk: edge stage + node GEMM (forward); GEMM, edge stage,
+        # two GEMMs and the split-K reduction (backward)
+        v = int(os.environ.get("CGTP_UVW_CHUNK_NODES", "4096"))
+        chunk = v if 1 <= v <= (1 << 20) else 4096
+        return 7 * max(1, -(-w["N"] // chunk))
+    return 2
+
+
 def algorithmic_flops(plan, n_nodes, n_edges):
     """Algorithmic FLOPs of one forward and one backward launch (FMA = 2 flops).
 
@@ -600,9 +615,7 @@ def main():
              ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
              ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[
         ("uvwe" if plan.mode == "uvw" and plan.radial_k == 0 else plan.mode, dominant)]
-    launches = 2 * args.steps
-    if plan.mode == "mixed":   # uvw + uvu forwards and a fold; unfold, two backwards, two adds
-        launches = 7 * args.steps
+    launches = launches_per_step(args.config, plan, w) * args.steps
     if "N" not in w:
         kname = {"forward": "bt_forward_kernel", "backward": "bt_backward_kernel"}[dominant]
     if t_hbm >= t_alu:
