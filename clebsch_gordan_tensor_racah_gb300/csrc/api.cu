@@ -268,7 +268,7 @@ cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const v
   if (B == 0) return CGTP_OK;
   cgtp_status s;
   if ((s = need(x1, "x1")) || (s = need(x2, "x2")) || (s = need(W, "W")) || (s = need(out, "out"))) return s;
-  if (!std::getenv("CGTP_UVU_NO_BT") && bt_forward(plan, x1, x2, W, out, B, stream, &s)) return s;
+  if (bt_forward(plan, x1, x2, W, out, B, stream, &s)) return s;
   return launch_uvu_forward(plan, plan->batch_layout, x1, x2, W, out, nullptr, nullptr, B, true, stream);
 }
 
@@ -284,7 +284,7 @@ cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, cons
   if ((s = need(gout, "gout")) || (s = need(x1, "x1")) || (s = need(x2, "x2")) || (s = need(W, "W")) ||
       (s = need(gx1, "gx1")) || (s = need(gx2, "gx2")) || (s = need(gW, "gW")))
     return s;
-  if (!std::getenv("CGTP_UVU_NO_BT") && bt_backward(plan, gout, x1, x2, W, gx1, gx2, gW, B, stream, &s)) return s;
+  if (bt_backward(plan, gout, x1, x2, W, gx1, gx2, gW, B, stream, &s)) return s;
   return launch_uvu_backward(plan, plan->batch_layout, gout, x1, x2, W, gx1, gx2, gW, nullptr, nullptr,
                              nullptr, B, true, stream);
 }

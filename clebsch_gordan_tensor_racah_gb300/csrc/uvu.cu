@@ -45,7 +45,7 @@ cgtp_status launch_uvu_forward(const cgtp_plan_s* plan, const LayoutDev& lay, co
     if (launch_v3_forward(plan, x, Y, W, out, rowptr, col, N, stream, &st3)) return st3;
   }
   // graph convolutions with l <= 3 take the pipelined kernel
-  if (!identity && small && lay.chunk2 > 0 && !std::getenv("CGTP_UVU_FORWARD_V1")) {
+  if (!identity && small && lay.chunk2 > 0) {
     if (plan->dtype == CGTP_F64) return uvu2_detail::fwd2_impl<double>(plan, lay, x, Y, W, out, rowptr, col, N, st);
     return uvu2_detail::fwd2_impl<float>(plan, lay, x, Y, W, out, rowptr, col, N, st);
   }

@@ -1,37 +1,36 @@
 // uvu3.cu -- host side of the warp-autonomous uvu kernels (uvu3_impl.cuh):
 // qualification, work items, launches.  Kernels are instantiated in
-// uvu3_<type>_<lanes>.cu.
+// uvu3_<variant>_<lanes>.cu.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "internal.h"
 
 namespace cgtp {
 namespace uvu3_detail {
-template <typename T, int LPE>
-cgtp_status fwd3_launch(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
-                        const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
-template <typename T, int LPE>
-cgtp_status bwd3_launch(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
+// instantiated in uvu3_<variant>_<lanes>.cu (uvu3_launch.cuh)
+template <typename T, typename S, bool SH, int LPE>
+cgtp_status v3_forward(const cgtp_plan_s* plan, const void* x, const void* E_in, const void* W, void* out,
+                       const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
+template <typename T, typename S, bool SH, int LPE>
+cgtp_status v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* E_in,
                         const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
                         const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
-template <typename T, int LPE>
-cgtp_status fwd3_launch_sh(const cgtp_plan_s* plan, const void* x, const void* rvec, const void* W, void* out,
-                           const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
-template <typename T, int LPE>
-cgtp_status bwd3_launch_sh(const cgtp_plan_s* plan, const void* gout, const void* x, const void* rvec,
-                           const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
-                           const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
-template <int LPE>
-cgtp_status fwd3_launch_bf16(const cgtp_plan_s* plan, const void* x, const void* Y, const void* W, void* out,
-                             const int32_t* rowptr, const int32_t* col, int64_t N, cudaStream_t st);
-template <int LPE>
-cgtp_status bwd3_launch_bf16(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
-                             const void* W, void* gx, void* gY, void* gW, const int32_t* t_rowptr,
-                             const int32_t* t_eid, const int32_t* t_dst, int64_t N, cudaStream_t st);
+
+// calls f with the plan's lanes per edge as a compile-time constant
+template <typename F>
+bool v3_pick(int lpe, F&& f) {
+  switch (lpe) {
+    case 2: f(std::integral_constant<int, 2>{}); return true;
+    case 8: f(std::integral_constant<int, 8>{}); return true;
+    case 32: f(std::integral_constant<int, 32>{}); return true;
+    default: return false;
+  }
+}
 }  // namespace uvu3_detail
 
 cgtp_status build_v3(cgtp_plan_s* plan) {
@@ -166,36 +165,21 @@ bool launch_v3_forward(const cgtp_plan_s* plan, const void* x, const void* Y, co
     return true;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (plan->dtype == CGTP_BF16) {  // only these kernels read bfloat16 inputs
-    switch (plan->v3.lpe) {
-      case 2: *st = fwd3_launch_bf16<2>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-      case 8: *st = fwd3_launch_bf16<8>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-      case 32: *st = fwd3_launch_bf16<32>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-      default: return false;
-    }
-  }
+  const int lpe = plan->v3.lpe;
+  auto go = [&](auto tag_t, auto tag_s, auto sh) {
+    using T = decltype(tag_t);
+    using S = decltype(tag_s);
+    constexpr bool SH = decltype(sh)::value;
+    return v3_pick(lpe, [&](auto L) {
+      *st = v3_forward<T, S, SH, decltype(L)::value>(plan, x, SH ? rvec : Y, W, out, rowptr, col, N, s);
+    });
+  };
+  if (plan->dtype == CGTP_BF16)  // only these kernels read bfloat16 inputs
+    return go(float{}, __nv_bfloat16{}, std::false_type{});
   const bool f64 = plan->dtype == CGTP_F64;
-  if (rvec) {  // edge vectors: the harmonics are evaluated in the kernels
-    switch (plan->v3.lpe) {
-      case 2: *st = f64 ? fwd3_launch_sh<double, 2>(plan, x, rvec, W, out, rowptr, col, N, s)
-                        : fwd3_launch_sh<float, 2>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
-      case 8: *st = f64 ? fwd3_launch_sh<double, 8>(plan, x, rvec, W, out, rowptr, col, N, s)
-                        : fwd3_launch_sh<float, 8>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
-      case 32: *st = f64 ? fwd3_launch_sh<double, 32>(plan, x, rvec, W, out, rowptr, col, N, s)
-                         : fwd3_launch_sh<float, 32>(plan, x, rvec, W, out, rowptr, col, N, s); return true;
-      default: return false;
-    }
-  }
-  if (std::getenv("CGTP_UVU_NO_V3")) return false;
-  switch (plan->v3.lpe) {
-    case 2: *st = f64 ? fwd3_launch<double, 2>(plan, x, Y, W, out, rowptr, col, N, s)
-                      : fwd3_launch<float, 2>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-    case 8: *st = f64 ? fwd3_launch<double, 8>(plan, x, Y, W, out, rowptr, col, N, s)
-                      : fwd3_launch<float, 8>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-    case 32: *st = f64 ? fwd3_launch<double, 32>(plan, x, Y, W, out, rowptr, col, N, s)
-                       : fwd3_launch<float, 32>(plan, x, Y, W, out, rowptr, col, N, s); return true;
-    default: return false;
-  }
+  if (rvec)  // edge vectors: the harmonics are evaluated in the kernels
+    return f64 ? go(double{}, double{}, std::true_type{}) : go(float{}, float{}, std::true_type{});
+  return f64 ? go(double{}, double{}, std::false_type{}) : go(float{}, float{}, std::false_type{});
 }
 
 bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x, const void* Y,
@@ -210,36 +194,20 @@ bool launch_v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
     return true;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (plan->dtype == CGTP_BF16) {
-#define V3BB(L) bwd3_launch_bf16<L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
-    switch (plan->v3.lpe) {
-      case 2: *st = V3BB(2); return true;
-      case 8: *st = V3BB(8); return true;
-      case 32: *st = V3BB(32); return true;
-      default: return false;
-    }
-#undef V3BB
-  }
+  const int lpe = plan->v3.lpe;
+  auto go = [&](auto tag_t, auto tag_s, auto sh) {
+    using T = decltype(tag_t);
+    using S = decltype(tag_s);
+    constexpr bool SH = decltype(sh)::value;
+    return v3_pick(lpe, [&](auto L) {
+      *st = v3_backward<T, S, SH, decltype(L)::value>(plan, gout, x, SH ? rvec : Y, W, gx, gY, gW, t_rowptr,
+                                                      t_eid, t_dst, N, s);
+    });
+  };
+  if (plan->dtype == CGTP_BF16) return go(float{}, __nv_bfloat16{}, std::false_type{});
   const bool f64 = plan->dtype == CGTP_F64;
-  if (rvec) {  // edge vectors: the harmonics are evaluated in the kernels
-#define V3S(T, L) bwd3_launch_sh<T, L>(plan, gout, x, rvec, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
-    switch (plan->v3.lpe) {
-      case 2: *st = f64 ? V3S(double, 2) : V3S(float, 2); return true;
-      case 8: *st = f64 ? V3S(double, 8) : V3S(float, 8); return true;
-      case 32: *st = f64 ? V3S(double, 32) : V3S(float, 32); return true;
-      default: return false;
-    }
-#undef V3S
-  }
-  if (std::getenv("CGTP_UVU_NO_V3")) return false;
-#define V3B(T, L) bwd3_launch<T, L>(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, s)
-  switch (plan->v3.lpe) {
-    case 2: *st = f64 ? V3B(double, 2) : V3B(float, 2); return true;
-    case 8: *st = f64 ? V3B(double, 8) : V3B(float, 8); return true;
-    case 32: *st = f64 ? V3B(double, 32) : V3B(float, 32); return true;
-    default: return false;
-  }
-#undef V3B
+  if (rvec) return f64 ? go(double{}, double{}, std::true_type{}) : go(float{}, float{}, std::true_type{});
+  return f64 ? go(double{}, double{}, std::false_type{}) : go(float{}, float{}, std::false_type{});
 }
 
 }  // namespace cgtp
