@@ -216,13 +216,21 @@ cgtp_status graph_build(cgtp_graph_s* g, void* stream) {
     scatter_kernel<<<blocks(E), threads, 0, st>>>(g->col, E, counts, g->t_eid);
     sort_short_kernel<<<std::max(1, std::min((N + 3) / 4, 4096)), 128, 0, st>>>(g->t_rowptr, N, g->t_eid, flag);
     const size_t lsm = kSortBlock * sizeof(int);
-    cudaFuncSetAttribute(sort_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsm);
+    err = cudaFuncSetAttribute(sort_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsm);
+    if (err != cudaSuccess) {
+      cudaStreamSynchronize(st);
+      cudaFree(scratch);
+      return fail(CGTP_ECUDA, std::string("graph build (sort shared memory): ") + cudaGetErrorString(err));
+    }
     sort_long_kernel<<<std::max(1, std::min(N, 1024)), 1024, lsm, st>>>(g->t_rowptr, N, g->t_eid);
     dst_kernel<<<blocks(E), threads, 0, st>>>(g->rowptr, N, g->t_eid, E, g->t_dst);
   }
+  // a launch refused for its configuration is reported here, not by the synchronisation
+  const cudaError_t lerr = cudaGetLastError();
   cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, st);
   err = cudaStreamSynchronize(st);
   cudaFree(scratch);
+  if (lerr != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph build launch: ") + cudaGetErrorString(lerr));
   if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph build: ") + cudaGetErrorString(err));
   if (hflag & kTooLong) return fail(CGTP_EUNSUPPORTED, "a sender has more than 32768 out-edges");
   return CGTP_OK;
@@ -247,11 +255,16 @@ namespace {
 constexpr int64_t kNoAllocMaxN = int64_t(1) << 20;   // largest node count accepted
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + 1 + kScanTile - 1) / kScanTile;
 constexpr int64_t kNoAllocWords = 2 + (kNoAllocMaxN + 1) + kNoAllocTiles;  // ~4 MiB of int32
+// flag, total, counts [N+1] and the tile sums of the largest accepted N fill the array exactly
+static_assert(2 + (kNoAllocMaxN + 1) + (kNoAllocMaxN + 1 + kScanTile - 1) / kScanTile <= kNoAllocWords,
+              "transpose scratch too small for the largest accepted node count");
 
 static __device__ __align__(256) int g_transpose_scratch[kNoAllocWords];
 
 // Device address of g_transpose_scratch per device, looked up once with that
 // device current (in host code the symbol name is only a host-side stand-in).
+// The cached address belongs to the device's primary context: after a
+// cudaDeviceReset the library must not be used on that device again.
 constexpr int kMaxDevices = 64;
 int* g_scratch_addr[kMaxDevices] = {nullptr};
 std::mutex g_scratch_mu;
@@ -315,12 +328,19 @@ extern "C" cgtp_status cgtp_graph_transpose_noalloc(const int32_t* rowptr, const
     scatter_kernel<<<blocks(e), threads, 0, st>>>(col, e, counts, t_eid);
     sort_short_kernel<<<std::max(1, std::min((n + 3) / 4, 4096)), 128, 0, st>>>(t_rowptr, n, t_eid, flag);
     const size_t lsm = kSortBlock * sizeof(int);
-    cudaFuncSetAttribute(sort_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsm);
+    err = cudaFuncSetAttribute(sort_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsm);
+    if (err != cudaSuccess) {
+      cudaStreamSynchronize(st);
+      return fail(CGTP_ECUDA, std::string("graph transpose (sort shared memory): ") + cudaGetErrorString(err));
+    }
     sort_long_kernel<<<std::max(1, std::min(n, 1024)), 1024, lsm, st>>>(t_rowptr, n, t_eid);
     dst_kernel<<<blocks(e), threads, 0, st>>>(rowptr, n, t_eid, e, t_dst);
   }
+  // a launch refused for its configuration is reported here, not by the synchronisation
+  const cudaError_t lerr = cudaGetLastError();
   cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, st);
   err = cudaStreamSynchronize(st);
+  if (lerr != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph transpose launch: ") + cudaGetErrorString(lerr));
   if (err != cudaSuccess) return fail(CGTP_ECUDA, std::string("graph transpose: ") + cudaGetErrorString(err));
   if (hflag & kTooLong) return fail(CGTP_EUNSUPPORTED, "a sender has more than 32768 out-edges");
   return CGTP_OK;

@@ -157,12 +157,14 @@ cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t
  *  Working memory is a fixed ~4 MiB array inside the library that every GPU
  *  which loads the library keeps until the process exits; N above 1,048,576
  *  is rejected with CGTP_EINVAL.  The first call on a device looks up that
- *  array's device address (with the device current) -- make that first call
- *  before any stream capture.  All calls on a device share the one array and
- *  clear it before use: calls whose work overlaps on the GPU (different
- *  streams or threads, same device) race and must be serialised by the caller.
- *  Synchronises `stream` twice (validation flag, long-segment flag).  Errors
- *  as cgtp_graph_create.
+ *  array's device address (with the device current) and keeps it for the
+ *  life of the process; make that first call before any stream capture, and
+ *  do not call this function on a device after cudaDeviceReset.  All calls on
+ *  a device share the one array and clear it before use: calls whose work
+ *  overlaps on the GPU (different streams or threads, same device) race and
+ *  must be serialised by the caller.  Every call synchronises `stream` twice
+ *  and copies two status flags into host memory (validation, long segments).
+ *  Errors as cgtp_graph_create; a refused launch is CGTP_ECUDA.
  */
 cgtp_status cgtp_graph_transpose_noalloc(const int32_t* rowptr, const int32_t* col, int64_t N,
                                          int64_t E, int32_t* t_rowptr, int32_t* t_eid,

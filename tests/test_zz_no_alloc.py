@@ -3,7 +3,8 @@
 cgtp_graph_transpose_noalloc serves callers that may not allocate device memory
 where they need the sender transpose; it must give exactly what
 cgtp_graph_create + cgtp_graph_transpose give.  Two calls in a row on different
-graphs also show that the shared working array is cleared between calls.  This
+graphs also show that the shared working array is cleared between calls, and a
+graph at the largest accepted node count fills that array to its last word.  This
 file is collected last so that a run stopping at its first failure has already
 run every other test.
 """
@@ -46,7 +47,9 @@ def _noalloc(rowptr_d, col_d, N, E):
 
 
 def test_noalloc_transpose_matches_allocating_transpose_twice():
-    cases = [(0, 20000, 640000, None), (1, 777, 9000, 5)]   # second call: smaller graph, a hub sender
+    # second call: smaller graph with a hub sender; third: the largest accepted node
+    # count, where flag, total, counts and tile sums fill the working array exactly
+    cases = [(0, 20000, 640000, None), (1, 777, 9000, 5), (2, 1 << 20, 300000, None)]
     for seed, N, E, hub in cases:
         rowptr, col = _csr(seed, N, E, hub)
         rd = torch.from_numpy(rowptr).cuda()
