@@ -1,27 +1,45 @@
 """Throughput of the fused CG tensor-product convolution (edges/s, forward + backward).
 
-Default workload: the NequIP-like convolution -- 10,000 nodes, 32 in-edges per
-node (320,000 edges), in1 = 32x(0e,1o,2e,3o), SH l<=3, uvu with all 34
-parity-allowed paths (l3 <= 3), FP32.  One step = cgtp_conv_forward +
-cgtp_conv_backward over the whole graph (the graph and plan are built once,
-outside the timed region).  Other workloads: --config tiny|nequip|mace|mace64|highl|uvw.
+Headline workload (the JSON line's ``value``): the NequIP-like convolution --
+10,000 nodes, 32 in-edges per node (320,000 edges), in1 = 32x(0e,1o,2e,3o),
+SH l<=3, uvu with all 34 parity-allowed paths (l3 <= 3), FP32.  One step =
+cgtp_conv_forward + cgtp_conv_backward over the whole graph (graph and plan are
+built once, outside the timed region).
 
-Output: one JSON line (rank 0).  ``value`` is device-timed edges/s with inputs
-resident in HBM; ``e2e`` repeats the step through the public API with the
-step's inputs copied from pinned host memory and its results copied back inside
-the timed region.  ``roofline`` describes the dominant kernel; ``cpu_baseline``
-times the FP64 oracle on a bounded sample of the same workload.
+The same line carries ``per_config``: every other benchmark workload (tiny,
+MACE-like FP32 and FP64, high-L batched, uvw radial with its peak device memory)
+timed the same way, each with its own roofline.  ``--config`` times one workload
+as the headline instead (tiny|nequip|mace|mace64|highl|uvw|uvw_edge|mixed|
+nequip_bf16|nequip_sh).
 
-``--impl reference`` times the oracle itself (the reference arm): host cores,
-bounded sample, same metric and config.
+Roofline model (FLOPs written out in ``model_flops``): FLOPs count the CG
+nonzeros -- per edge and path 2 nnz(C) for C.Y, mul * 2 nnz_{m1,m3}(C) for the
+contraction, mul * (2 l3 + 1) for the weight product, plus d_out per edge for
+the receiver sum; backward = 3x forward; bytes = every input read once plus
+every output written once.  Peaks are measured here: FP32 / FP64 FMA throughput
+and L2 / HBM read bandwidth with the library's own measurement kernels
+(cgtp_measure_fma / cgtp_measure_read), HBM copy bandwidth and bf16 tensor
+throughput from MEASURED_PEAKS.json.
+
+``e2e`` repeats the headline step through the public API with the step's
+inputs copied from pinned host memory and every result copied back inside the
+timed region (copies on their own streams, overlapping the neighbouring steps'
+kernels); the measured pinned copy bandwidths are reported beside it.
+
+``--impl reference`` times the oracle itself (the reference arm): the FP64
+definition on every host core (one process per core, each over its own range
+of receivers or samples), a bounded sample of the same full-size workload per
+step.
 """
 
 import argparse
 import json
 import math
 import os
+import platform
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -32,36 +50,127 @@ sys.path.insert(0, ROOT)
 
 METRIC = "CGTP-conv edges/s fwd and fwd+bwd (FP32/FP64); % of HBM/FLOP roofline"
 
+CONFIGS = {
+    "tiny": dict(name="tiny", dtype="float32"),
+    "nequip": dict(name="nequip", dtype="float32"),
+    "mace": dict(name="mace", dtype="float32"),
+    "mace64": dict(name="mace", dtype="float64"),
+    "highl": dict(name="highl", dtype="float32"),
+    "uvw": dict(name="uvw", dtype="float32"),
+    "uvw_edge": dict(name="uvw_edge", dtype="float32"),
+    "mixed": dict(name="mixed", dtype="float32"),
+    "nequip_bf16": dict(name="nequip", dtype="bfloat16"),
+    "nequip_sh": dict(name="nequip", dtype="float32", sh=True),
+}
+# the benchmark's five workloads besides the headline
+PER_CONFIG = ["tiny", "mace", "mace64", "highl", "uvw"]
+L2_BYTES = 126 * 2 ** 20          # GB300 L2 (about 126 MiB usable)
+FLUSH_BYTES = 512 * 2 ** 20       # buffer written between timed steps when flushing L2
 
-def peaks():
+WORKLOAD_NAMES = {
+    "tiny": "tiny uvu conv (64 nodes, 512 edges, 8x(0e,1o), SH l<=1)",
+    "nequip": "NequIP-like uvu conv (10k nodes x 32 in-edges, 32x(0e,1o,2e,3o), SH l<=3)",
+    "mace": "MACE-like uvu conv (5k nodes, Poisson(40) in-degree, 128x(0e,1o,2e), SH l<=3)",
+    "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
+    "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)",
+    "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))",
+    "mixed": "mixed uvu/uvw conv (10k nodes x 32 in-edges, 32x(0e,1o,2e), SH l<=2; "
+             "0e outputs uvw with per-edge weights, 1o and 2e outputs uvu)",
+}
+
+
+# ---------------------------------------------------------------------------
+# peaks
+# ---------------------------------------------------------------------------
+
+def driver_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": d["hbm_gbs"], "src": "measured", "sm_max_mhz": d.get("sm_max_mhz", 2070.0)}
-    return {"hbm_gbs": 6800.0, "src": "fallback", "sm_max_mhz": 2070.0}
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d.get("bf16_tflops", 1900.0), "src": "measured",
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0)}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback", "sm_max_mhz": 2070.0}
 
 
-# FP32 / FP64 CUDA-core peaks from unit counts: 152 SMs x 128 FP32 lanes x 2 flop
-# x clock; FP64 at the nominal 1.25 TFLOP/s of the part.
-def alu_peak_tflops(dtype_name, mhz):
-    if dtype_name == "f64":
-        return 1.25
-    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+def _time_launches(fn, stream, reps):
+    import torch
+    best = None
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        work = fn()
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b)
+        if best is None or ms < best[0]:
+            best = (ms, work)
+    return best
 
 
-CONFIGS = {
-    "tiny": dict(name="tiny", dtype="float32", over={}),
-    "nequip": dict(name="nequip", dtype="float32", over={}),
-    "mace": dict(name="mace", dtype="float32", over={}),
-    "mace64": dict(name="mace", dtype="float64", over={}),
-    "highl": dict(name="highl", dtype="float32", over={}),
-    "nequip_bf16": dict(name="nequip", dtype="bfloat16", over={}),
-    "nequip_sh": dict(name="nequip", dtype="float32", over={}, sh=True),
-    "uvw_edge": dict(name="uvw_edge", dtype="float32", over={}),
-    "mixed": dict(name="mixed", dtype="float32", over={}),
-    "uvw": dict(name="uvw", dtype="float32", over={}),
-}
+def measure_peaks(device):
+    """FP32 (FFMA and paired FFMA2), FP64 FMA throughput and L2 / HBM read bandwidth,
+    measured with the library's kernels on this GPU (best of 3 launches of ~20 ms each,
+    after a calibration launch), with the SM clock sampled meanwhile."""
+    import torch
+    import clebsch_gordan_tensor_racah_gb300 as cg
+    props = torch.cuda.get_device_properties(device)
+    nsm = props.multi_processor_count
+    stream = torch.cuda.current_stream(device)
+    ctas = nsm * 8
+    sink = torch.empty(ctas * 256 * 2, dtype=torch.float64, device=device)
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
+    out = {"sms": nsm}
+    for name, kind in (("fp32_ffma", cg.CGTP_MEASURE_FFMA), ("fp32_ffma2", cg.CGTP_MEASURE_FFMA2),
+                       ("fp64_dfma", cg.CGTP_MEASURE_DFMA)):
+        iters = 16
+        while True:
+            ms, fl = _time_launches(lambda: cg.measure_fma(kind, ctas, iters, sink, stream), stream, 1)
+            if ms > 4.0 or iters >= 1 << 22:
+                break
+            iters *= 4
+        iters = max(1, int(iters * 20.0 / max(ms, 1e-3)))
+        ms, fl = _time_launches(lambda: cg.measure_fma(kind, ctas, iters, sink, stream), stream, 3)
+        out[name + "_tflops"] = fl / (ms * 1e-3) / 1e12
+    rsink = torch.empty(nsm * 4 * 256, dtype=torch.int32, device=device)
+    rc = nsm * 4
+    l2buf = torch.ones(64 * 2 ** 20 // 4, dtype=torch.int32, device=device)
+    cg.measure_read(l2buf, 1, rc, rsink, stream)
+    ms, nb = _time_launches(lambda: cg.measure_read(l2buf, 40, rc, rsink, stream), stream, 3)
+    out["l2_read_gbs"] = nb / (ms * 1e-3) / 1e9
+    del l2buf
+    q = 4096 * rc
+    hbuf = torch.ones((4 * 2 ** 30 // q) * q // 4, dtype=torch.int32, device=device)
+    ms, nb = _time_launches(lambda: cg.measure_read(hbuf, 1, rc, rsink, stream), stream, 3)
+    out["hbm_read_gbs"] = nb / (ms * 1e-3) / 1e9
+    del hbuf
+    clk = clocks.stop() or {}
+    out["sm_mhz_median"] = clk.get("sm_mhz")
+    out["fp32_tflops"] = max(out["fp32_ffma_tflops"], out["fp32_ffma2_tflops"])
+    out["fp64_tflops"] = out["fp64_dfma_tflops"]
+    mhz = clk.get("sm_mhz") or 2070.0
+    out["fp32_flops_per_clk_per_sm"] = out["fp32_tflops"] * 1e12 / (mhz * 1e6) / nsm
+    out["fp64_flops_per_clk_per_sm"] = out["fp64_tflops"] * 1e12 / (mhz * 1e6) / nsm
+    out["how"] = ("cgtp_measure_fma: 8 CTAs x 256 threads per SM, 16 independent FMA chains per thread; "
+                  "cgtp_measure_read: 16-byte loads over 64 MiB (L2, 40 passes) and 4 GiB (HBM); best of 3")
+    return out
 
+
+def measure_link(device):
+    """Pinned host<->device copy bandwidth (GB/s), one 512 MiB copy each way, best of 3."""
+    import torch
+    n = 512 * 2 ** 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=device)
+    s = torch.cuda.current_stream(device)
+    ms_h2d, _ = _time_launches(lambda: d.copy_(h, non_blocking=True), s, 3)
+    ms_d2h, _ = _time_launches(lambda: h.copy_(d, non_blocking=True), s, 3)
+    return {"h2d_gbs": n / (ms_h2d * 1e-3) / 1e9, "d2h_gbs": n / (ms_d2h * 1e-3) / 1e9}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
 
 def build_inputs(cfgkey, device, nodes=None):
     import torch
@@ -78,7 +187,7 @@ def build_inputs(cfgkey, device, nodes=None):
         plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
                        radial_k=spec.get("K", 0) if mode == "uvw" else 0)
         w_numel = plan.w_numel
-    over = dict(c["over"])
+    over = {}
     if nodes:
         over["B" if spec["graph"] is None else "N"] = int(nodes)
     w = wl.make(c["name"], w_numel, seed=0, dtype="float32" if tdt == torch.bfloat16 else c["dtype"], **over)
@@ -101,7 +210,11 @@ def build_inputs(cfgkey, device, nodes=None):
 
 
 def step_fns(cfgkey, plan, graph, w, dev, tdt):
-    """Returns (fwd, bwd, units, bytes_fwd, bytes_bwd, flops_fwd, flops_bwd, out_shape)."""
+    """Returns (fwd, bwd, units, bytes_fwd, bytes_bwd, out_shape, inputs, outputs).
+
+    bytes: every input read once plus every output written once (index arrays
+    included).  inputs: the tensors one step reads (the e2e copy list);
+    outputs(res): the result tensors of a step given bwd's return value."""
     import clebsch_gordan_tensor_racah_gb300 as cg
     es = 8 if tdt.__str__().endswith("64") else 4
     ei = 2 if tdt.__str__().endswith("bfloat16") else es   # input element size (outputs: es)
@@ -114,11 +227,11 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
         bf = es * (nin + N * plan.d_out) + idx
         bb = es * (2 * nin + N * plan.d_out + E * plan.d2) + idx + 8 * E
 
-        def fwd(out):
-            return cg.cgtp_conv_forward_sh(plan, graph, x, rv, W, out=out)
+        def fwd(out, d=dev):
+            return cg.cgtp_conv_forward_sh(plan, graph, d["x"], d["rvec"], d["W"], out=out)
 
-        def bwd(g, outs):
-            return cg.cgtp_conv_backward_sh(plan, graph, g, x, rv, W)
+        def bwd(g, outs, d=dev):
+            return cg.cgtp_conv_backward_sh(plan, graph, g, d["x"], d["rvec"], d["W"])
         return fwd, bwd, units, bf, bb, (N, plan.d_out)
     if "Wu" in dev:   # mixed instruction list: two per-edge weight arrays
         N, E = w["N"], w["E"]
@@ -132,15 +245,15 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
         import torch
         res = (torch.empty_like(x), torch.empty_like(Y), torch.empty_like(Wu), torch.empty_like(Ww))
 
-        def fwd(out):
-            return cg.cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=out, workspace=ws)
+        def fwd(out, d=dev):
+            return cg.cgtp_mixed_conv_forward(plan, graph, d["x"], d["Y"], d["Wu"], d["Ww"], out=out, workspace=ws)
 
-        def bwd(g, outs):
-            return cg.cgtp_mixed_conv_backward(plan, graph, g, x, Y, Wu, Ww, workspace=ws, outs=res)
+        def bwd(g, outs, d=dev):
+            return cg.cgtp_mixed_conv_backward(plan, graph, g, d["x"], d["Y"], d["Wu"], d["Ww"], workspace=ws,
+                                               outs=res)
         return fwd, bwd, units, bf, bb, (N, plan.d_out)
     if "rowptr" in dev:
         N, E = w["N"], w["E"]
-        x, Y = dev["x"], dev["Y"]
         WR = dev["W"] if "W" in dev else dev["R"]
         M = dev.get("M")
         units = E
@@ -149,24 +262,25 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
         bf = ei * nin + es * N * plan.d_out + idx
         bb = ei * (nin + N * plan.d_out) + es * nin + idx + 8 * E
 
-        def fwd(out):
-            return cg.cgtp_conv_forward(plan, graph, x, Y, WR, M, out=out)
+        def fwd(out, d=dev):
+            return cg.cgtp_conv_forward(plan, graph, d["x"], d["Y"], d["W"] if "W" in d else d["R"], d.get("M"),
+                                        out=out)
 
-        def bwd(g, outs):
-            return cg.cgtp_conv_backward(plan, graph, g, x, Y, WR, M, outs=outs)
+        def bwd(g, outs, d=dev):
+            return cg.cgtp_conv_backward(plan, graph, g, d["x"], d["Y"], d["W"] if "W" in d else d["R"],
+                                         d.get("M"), outs=outs)
         out_shape = (N, plan.d_out)
     else:
         B = w["B"]
-        x1, x2, W = dev["x1"], dev["x2"], dev["W"]
         units = B
         bf = es * (B * (plan.d1 + plan.d2 + plan.w_numel + plan.d_out))
         bb = es * (B * (2 * plan.d1 + 2 * plan.d2 + 2 * plan.w_numel + plan.d_out))
 
-        def fwd(out):
-            return cg.cgtp_forward(plan, x1, x2, W, out=out)
+        def fwd(out, d=dev):
+            return cg.cgtp_forward(plan, d["x1"], d["x2"], d["W"], out=out)
 
-        def bwd(g, outs):
-            return cg.cgtp_backward(plan, g, x1, x2, W)
+        def bwd(g, outs, d=dev):
+            return cg.cgtp_backward(plan, g, d["x1"], d["x2"], d["W"])
         out_shape = (B, plan.d_out)
     return fwd, bwd, units, bf, bb, out_shape
 
@@ -178,60 +292,56 @@ def launches_per_step(cfgkey, plan, w):
     if CONFIGS[cfgkey].get("sh"):   # forward, backward, per-edge chain rule to the edge vectors
         return 3
     if plan.mode == "uvw" and plan.radial_k > 0:
-        # per streamed node chunk: edge stage + node GEMM (forward); GEMM, edge stage,
-        # two GEMMs and the split-K reduction (backward)
-        v = int(os.environ.get("CGTP_UVW_CHUNK_NODES", "4096"))
-        chunk = v if 1 <= v <= (1 << 20) else 4096
-        return 7 * max(1, -(-w["N"] // chunk))
+        return plan.launches_per_step(w["N"])
     return 2
 
 
-def algorithmic_flops(plan, n_nodes, n_edges):
-    """Algorithmic FLOPs of one forward and one backward launch (FMA = 2 flops).
+def _cg_counts(l1, l2, l3):
+    """(nnz of the real CG block, nnz of its (m1, m3) pattern): the number of terms of
+    C.Y and of the contraction over m1 for one channel."""
+    import clebsch_gordan_tensor_racah_gb300 as cg
+    C = np.abs(cg.cgtp_real_cg_block(l1, l2, l3)) > 1e-12
+    return int(C.sum()), int(C.any(axis=1).sum())
 
-    Per (edge, path) with D1 = 2l1+1, D3 = 2l3+1, NF = D1*D3 and nnz the CG
-    nonzeros of the path:
-      uvu forward : 2 nnz (cy = C.Y) + mul * (D1 + 2 NF)      (weight product, contraction)
-      uvu backward: 4 nnz + mul * (6 NF + 3 D3)               (t, gW, w*g, gx, x (x) wg; C.Y and C.gc)
-      uvw forward : 2 nnz + mul1 * 2 NF + 2 K mul1 D3 per edge, and the node GEMM
-                    2 K mul1 mul_out D3 per node
-      uvw backward: 4 nnz + 2 mul_out NF * 2 + 6 K mul_out D1 per edge, and three node
-                    GEMMs (x M, M H, x^T H) of 2 K mul1 mul_out D1 each per node
-    """
-    fe = be = fn = bn = 0
+
+def model_flops(plan, n_nodes, units, graph=True):
+    """Algorithmic FLOPs of one forward and one backward (FMA = 2), counting CG nonzeros.
+
+    uvu, per edge (sample) and path, D3 = 2 l3 + 1:
+        2 nnz(C)                       cy[m1,m3] = sum_m2 C[m1,m2,m3] Y[m2]
+        mul * 2 nnz_{m1,m3}(C)         t[u,m3] = sum_m1 cy[m1,m3] x[u,m1]
+        mul * D3                       the weight product W[u] t[u,m3]
+      plus d_out per edge for the receiver sum (graphs only).
+    uvw radial: the edge stage 2 nnz + mul1 * 2 nnz_{m1,m3} + 2 K mul1 D3 per edge and
+      path (t, then S += R[e,k] t), and the node GEMM 2 K mul1 mul_out D3 per node and
+      path.  uvw with per-edge weights: 2 nnz + mul1 * 2 nnz_{m1,m3} + 2 mul1 mul_out D3.
+    Backward = 3 x forward.  Returns (fwd_cuda_core, fwd_tensor_core): the node GEMM of
+    the radial uvw runs on the tensor cores, everything else on the FP32/FP64 pipes."""
     K = getattr(plan, "radial_k", 0)
-    if plan.mode == "mixed":   # per instruction, with its own mode (the uvw ones with weights per edge)
-        import clebsch_gordan_tensor_racah_gb300 as cg
+    fe = fn = 0
+    if plan.mode == "mixed":
         from clebsch_gordan_tensor_racah_gb300.workloads import irreps_terms
-        a, b, o = (irreps_terms(s) for s in (plan.irreps[0], plan.irreps[1], plan.irreps[2]))
+        a, b, o = (irreps_terms(s) for s in plan.irreps)
         for (i1, i2, io), m in zip(plan.instructions, plan.modes):
             (mul1, l1), (_, l2), (mul_out, l3) = a[i1], b[i2], o[io]
-            D1, D3 = 2 * l1 + 1, 2 * l3 + 1
-            NF, nnz = D1 * D3, int(np.count_nonzero(cg.cgtp_real_cg_block(l1, l2, l3)))
-            if m == "uvu":
-                fe += 2 * nnz + mul1 * (D1 + 2 * NF)
-                be += 4 * nnz + mul1 * (6 * NF + 3 * D3)
-            else:
-                fe += 2 * nnz + mul1 * 2 * NF + 2 * mul1 * mul_out * D3
-                be += 4 * nnz + mul1 * 4 * NF + 3 * 2 * mul1 * mul_out * D3 + 2 * mul1 * NF
-        return fe * n_edges, be * n_edges
+            nnz, nc = _cg_counts(l1, l2, l3)
+            D3 = 2 * l3 + 1
+            fe += 2 * nnz + mul1 * 2 * nc + (mul1 * D3 if m == "uvu" else 2 * mul1 * mul_out * D3)
+        return (fe + plan.d_out) * units, 0.0
     for p in range(plan.n_paths):
-        ints, C = plan.path(p)
+        ints, _ = plan.path(p)
         l1, l2, l3, mul1, mul_out = ints[:5]
-        D1, D3 = 2 * l1 + 1, 2 * l3 + 1
-        NF, nnz = D1 * D3, int(np.count_nonzero(C))
+        nnz, nc = _cg_counts(l1, l2, l3)
+        D3 = 2 * l3 + 1
         if plan.mode == "uvu":
-            fe += 2 * nnz + mul1 * (D1 + 2 * NF)
-            be += 4 * nnz + mul1 * (6 * NF + 3 * D3)
-        elif K == 0:   # weights per edge: t = C.x.Y, then the [u][w] matrix per edge
-            fe += 2 * nnz + mul1 * 2 * NF + 2 * mul1 * mul_out * D3
-            be += 4 * nnz + mul1 * 4 * NF + 3 * 2 * mul1 * mul_out * D3 + 2 * mul1 * NF
+            fe += 2 * nnz + mul1 * (2 * nc + D3)
+        elif K == 0:
+            fe += 2 * nnz + mul1 * 2 * nc + 2 * mul1 * mul_out * D3
         else:
-            fe += 2 * nnz + mul1 * 2 * NF + 2 * K * mul1 * D3
+            fe += 2 * nnz + mul1 * 2 * nc + 2 * K * mul1 * D3
             fn += 2 * K * mul1 * mul_out * D3
-            be += 4 * nnz + 4 * mul_out * NF + 6 * K * mul_out * D1
-            bn += 3 * 2 * K * mul1 * mul_out * D1
-    return fe * n_edges + fn * n_nodes, be * n_edges + bn * n_nodes
+    agg = plan.d_out if (graph and plan.mode == "uvu") else 0
+    return float((fe + agg) * units), float(fn * n_nodes)
 
 
 def traffic_for(kname, cfgkey, algorithmic_bytes):
@@ -296,58 +406,113 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def time_oracle_sample(cfgkey, budget_s=8.0):
-    """FP64 oracle on a bounded sample of the workload: (units/s, sample description)."""
-    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
-    from oracle import conv as oconv, irreps as oirr
-    c = CONFIGS[cfgkey]
-    spec = wl.SPECS[c["name"]]
-    if spec["mode"] == "mixed":
-        lay = oconv.mixed_layout(spec["in1"], spec["in2"], spec["out"], spec["instructions"], spec["modes"])
-        N = 60
-        w = wl.make(c["name"], (lay[3], lay[4]), seed=0, dtype=c["dtype"], N=N)
-        units, t0 = 0, time.perf_counter()
-        while time.perf_counter() - t0 < budget_s:
-            out = oconv.conv_mixed_forward(lay, w["x"], w["Y"], w["Wu"], w["Ww"], w["rowptr"], w["col"])
-            oconv.conv_mixed_backward(lay, out, w["x"], w["Y"], w["Wu"], w["Ww"], w["rowptr"], w["col"])
-            units += w["E"]
-        dt = time.perf_counter() - t0
-        return units / dt, f"{N}-node graph of the same recipe ({w['E']} edges), fwd+bwd repeated for {dt:.1f} s"
-    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], spec["mode"])
-    if spec["graph"] is None:
-        B = 64
-        w = wl.make(c["name"], oplan.w_numel, seed=0, dtype=c["dtype"], B=B)
-        units, t0 = 0, time.perf_counter()
-        while time.perf_counter() - t0 < budget_s:
-            out = oconv.tp_uvu_forward(oplan, w["x1"], w["x2"], w["W"])
-            oconv.tp_uvu_backward(oplan, out, w["x1"], w["x2"], w["W"])
-            units += B
-        dt = time.perf_counter() - t0
-        return units / dt, f"batches of {B} samples of the same recipe, fwd+bwd, {dt:.1f} s"
-    # a smaller graph of the same recipe (same degree distribution and features)
-    N = {"tiny": 64, "nequip": 120, "mace": 60, "uvw": 4, "uvw_edge": 120}[c["name"]]
-    w = wl.make(c["name"], oplan.w_numel, seed=0, dtype="float32" if c["dtype"] == "bfloat16" else c["dtype"], N=N)
-    units, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < budget_s:
-        if c.get("sh"):
-            rv = np.random.default_rng(7).standard_normal((w["E"], 3))
-            out = oconv.conv_uvu_forward_sh(oplan, w["x"], rv, w["W"], w["rowptr"], w["col"])
-            oconv.conv_uvu_backward_sh(oplan, out, w["x"], rv, w["W"], w["rowptr"], w["col"])
-        elif spec["mode"] == "uvu":
-            out = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-            oconv.conv_uvu_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-        elif "W" in w:
-            out = oconv.conv_uvw_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-            oconv.conv_uvw_backward(oplan, out, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-        else:
-            out = oconv.conv_uvw_radial_forward(oplan, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
-            oconv.conv_uvw_radial_backward(oplan, out, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
-        units += w["E"]
-    dt = time.perf_counter() - t0
-    return units / dt, f"{N}-node graph of the same recipe ({w['E']} edges), fwd+bwd repeated for {dt:.1f} s"
+# ---------------------------------------------------------------------------
+# timing one workload
+# ---------------------------------------------------------------------------
+
+def time_steps(fwd, bwd, g, out, stream, steps, flush=None):
+    """(fwd_ms, bwd_ms, step_ms): mean over `steps` steps, CUDA events on the launching
+    stream.  With `flush` (a buffer larger than L2) the buffer is rewritten before every
+    step, outside the events, so each step starts with a cold L2."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        ev[i][0].record(stream)
+        fwd(out)
+        ev[i][1].record(stream)
+        bwd(g, None)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    tf = [e[0].elapsed_time(e[1]) for e in ev]
+    tb = [e[1].elapsed_time(e[2]) for e in ev]
+    return float(np.mean(tf)), float(np.mean(tb)), float(np.mean(tf) + np.mean(tb))
 
 
-def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
+def roofline_of(plan, w, units, bf, bb, fwd_ms, bwd_ms, tdt, pk, meas):
+    """Per-direction roofline times and the step fraction (section-8(d) model)."""
+    import torch
+    graph = "N" in w
+    n_nodes = w.get("N", w.get("B", 0))
+    ff_cc, ff_tc = model_flops(plan, n_nodes, units, graph=graph)
+    f64 = tdt == torch.float64
+    alu = (meas["fp64_tflops"] if f64 else meas["fp32_tflops"]) * 1e12
+    # tensor-core node GEMM of the radial uvw: kind::tf32 with three products per tile (3xTF32);
+    # TF32 peak = measured bf16 peak x the nominal tf32/bf16 ratio (1.1 / 2.25)
+    tc = pk["bf16_tflops"] * 1e12 * (1.1 / 2.25) / 3.0
+    hbm = pk["hbm_gbs"] * 1e9
+
+    def side(nbytes, f_cc, f_tc):
+        t_mem = nbytes / hbm
+        t_alu = f_cc / alu + f_tc / tc
+        return max(t_mem, t_alu), ("hbm" if t_mem >= t_alu else ("alu" if f_tc == 0 else "alu+tensor"))
+    rf, bound_f = side(bf, ff_cc, ff_tc)
+    rb, bound_b = side(bb, 3 * ff_cc, 3 * ff_tc)
+    return {"fwd_flops": ff_cc + ff_tc, "bwd_flops": 3 * (ff_cc + ff_tc), "fwd_tensor_flops": ff_tc,
+            "fwd_bytes": int(bf), "bwd_bytes": int(bb),
+            "fwd_roofline_ms": 1e3 * rf, "bwd_roofline_ms": 1e3 * rb, "fwd_bound": bound_f, "bwd_bound": bound_b,
+            "fwd_frac": 1e3 * rf / fwd_ms, "bwd_frac": 1e3 * rb / bwd_ms,
+            "step_frac": 1e3 * (rf + rb) / (fwd_ms + bwd_ms),
+            "peaks_used": {"alu_tflops": alu / 1e12, "alu": "fp64 dfma" if f64 else "fp32 (max of ffma, ffma2)",
+                           "tensor_tflops": tc / 1e12 if ff_tc else None, "hbm_gbs": hbm / 1e9}}
+
+
+def run_config(cfgkey, device, steps, warmup, meas, pk, flush_l2=None, nodes=None):
+    """Times one workload: warm-up, then `steps` timed steps; returns a dict (plus the
+    objects the headline needs for e2e and the double backward)."""
+    import torch
+    if cfgkey == "uvw":
+        torch.cuda.reset_peak_memory_stats(device)
+    torch.cuda.synchronize()
+    free0, total = torch.cuda.mem_get_info(device)
+    plan, graph, w, host, dev, spec, tdt = build_inputs(cfgkey, device, nodes)
+    torch.cuda.synchronize()
+    fwd, bwd, units, bf, bb, out_shape = step_fns(cfgkey, plan, graph, w, dev, tdt)
+    g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
+    out = torch.empty(out_shape, dtype=plan.out_dtype, device=device)
+    stream = torch.cuda.current_stream(device)
+    # inputs below L2 (tiny) are always timed cold; the others exceed L2 by themselves
+    in_bytes = sum(t.numel() * t.element_size() for t in dev.values())
+    flush = flush_l2 if flush_l2 is not None else (in_bytes < 2 * L2_BYTES)
+    fbuf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device) if flush else None
+    for _ in range(max(3, warmup)):
+        fwd(out)
+        bwd(g, None)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
+    time.sleep(0.25)
+    tf, tb, ts = time_steps(fwd, bwd, g, out, stream, steps, fbuf)
+    clk = clocks.stop()
+    free1, _ = torch.cuda.mem_get_info(device)
+    r = {"workload": WORKLOAD_NAMES[CONFIGS[cfgkey]["name"]],
+         "precision": {torch.float64: "f64", torch.bfloat16: "bf16 inputs, f32 arithmetic"}.get(tdt, "f32"),
+         "units": int(units), "unit": "edges" if "N" in w else "samples", "steps": steps, "warmup": max(3, warmup),
+         "fwd_ms": tf, "bwd_ms": tb, "step_ms": ts,
+         "fwd_units_per_s": units / (tf * 1e-3), "fwd_bwd_units_per_s": units / (ts * 1e-3),
+         "l2": ("L2 flushed before every timed step (512 MiB write)" if flush
+                else f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2, no flush"),
+         "gpu_launches_per_step": launches_per_step(cfgkey, plan, w),
+         "roofline": roofline_of(plan, w, units, bf, bb, tf, tb, tdt, pk, meas),
+         "clocks": clk}
+    if "N" in w:
+        r.update(nodes=int(w["N"]), edges=int(w["E"]))
+    else:
+        r.update(batch=int(w["B"]))
+    if cfgkey == "uvw":
+        lib_bytes = plan.device_bytes() + graph.device_bytes()
+        r["peak_memory"] = {
+            "torch_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(device)),
+            "library_bytes": int(lib_bytes),
+            "peak_device_bytes": int(torch.cuda.max_memory_allocated(device) + lib_bytes),
+            "device_used_delta_bytes": int(free0 - free1),
+            "how": "torch.cuda.max_memory_allocated (inputs, outputs, gradients) + the bytes the plan "
+                   "and graph own (cgtp_plan_device_bytes, cgtp_graph_device_bytes)"}
+    return r, (plan, graph, w, host, dev, tdt, fwd, bwd, g, out, out_shape, units, bf, bb)
+
+
+def time_double_backward(plan, graph, w, dev, g, stream, units, roof):
     """Second derivatives (cgtp_conv_double_backward / cgtp_double_backward) with random
     cotangents, CUDA events on the launching stream, after warm-up.  It runs the
     forward and backward kernels once per operand (3 + 3 for uvu, 4 + 4 for uvw),
@@ -363,7 +528,7 @@ def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
         def run():
             return cg.cgtp_mixed_conv_double_backward(plan, graph, g, dev["x"], dev["Y"], dev["Wu"], dev["Ww"],
                                                       c["x"], c["Y"], c["Wu"], c["Ww"], workspace=ws)
-        n_op = 3   # x, Y and the weights (Wu, Ww) together: 3 forwards + 3 backwards of each single-mode plan
+        n_op = 3
     elif "rowptr" in dev:
         keys = ["x", "Y", "W"] if "W" in dev else ["x", "Y", "R", "M"]
         c = {k: torch.randn(dev[k].shape, dtype=dev[k].dtype, device=g.device, generator=gen) for k in keys}
@@ -392,10 +557,277 @@ def time_double_backward(plan, graph, w, dev, g, stream, units, roofline):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / reps
-    roof = n_op * (roofline["fwd_roofline_ms"] + roofline["bwd_roofline_ms"])
+    rl = n_op * (roof["fwd_roofline_ms"] + roof["bwd_roofline_ms"])
     return {"ms": ms, "units_per_s": units / (ms / 1000.0), "launch_sequence": f"{n_op} forwards + {n_op} backwards + adds",
-            "roofline_ms": roof, "frac": roof / ms}
+            "roofline_ms": rl, "frac": rl / ms}
 
+
+def time_e2e(ctx, device, steps):
+    """The headline step through the public API with host buffers: every step copies its
+    inputs from pinned host memory and its results (output, gradients) back.  Copies run on
+    their own streams with two device buffer sets, so step k's copies overlap steps k-1 and
+    k+1's kernels; the timed region runs from the first copy to the last result on the host."""
+    import torch
+    plan, graph, w, host, dev, tdt, fwd, bwd, g, out, out_shape, units, bf, bb = ctx
+    keys = [k for k in host if k not in ("rowptr", "col")]
+    pin = {k: (v if isinstance(v, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(v))).pin_memory()
+           for k, v in host.items() if k in keys}
+    gh = g.cpu().pin_memory()
+    sets = []
+    for s in range(2):
+        d = {k: (dev[k] if s == 0 else torch.empty_like(dev[k])) for k in keys}
+        d.update({k: dev[k] for k in ("rowptr", "col") if k in dev})
+        sets.append({"in": d, "g": g if s == 0 else torch.empty_like(g),
+                     "out": out if s == 0 else torch.empty_like(out), "res": None,
+                     "ev_in": torch.cuda.Event(), "ev_fwd": torch.cuda.Event(), "ev_bwd": torch.cuda.Event(),
+                     "ev_out": torch.cuda.Event()})
+    s_comp = torch.cuda.current_stream(device)
+    s_h2d, s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    out_h = [torch.empty(out_shape, dtype=plan.out_dtype).pin_memory() for _ in range(2)]
+    res_h = [None, None]
+    fwd_d, bwd_d = ctx[6], ctx[7]
+
+    def launch(i, first):
+        S = sets[i % 2]
+        with torch.cuda.stream(s_h2d):
+            if not first:
+                s_h2d.wait_event(S["ev_bwd"])          # the previous step on this set has read its inputs
+            for k in keys:
+                S["in"][k].copy_(pin[k], non_blocking=True)
+            S["g"].copy_(gh, non_blocking=True)
+            S["ev_in"].record(s_h2d)
+        s_comp.wait_event(S["ev_in"])
+        if not first:
+            s_comp.wait_event(S["ev_out"])             # its previous results have reached the host
+        fwd_d(S["out"], d=S["in"])
+        S["ev_fwd"].record(s_comp)
+        r = bwd_d(S["g"], S["res"], d=S["in"])
+        S["res"] = tuple(x for x in r)
+        S["ev_bwd"].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(S["ev_fwd"])
+            out_h[i % 2].copy_(S["out"], non_blocking=True)
+            s_d2h.wait_event(S["ev_bwd"])
+            if res_h[i % 2] is None:
+                res_h[i % 2] = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in r if x is not None]
+            for hb, x in zip(res_h[i % 2], [x for x in r if x is not None]):
+                hb.copy_(x, non_blocking=True)
+            S["ev_out"].record(s_d2h)
+    # the step functions take an explicit input set (keyword d)
+    for i in range(2):
+        launch(i, True)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + gh.numel() * gh.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size() + sum(t.numel() * t.element_size() for t in res_h[0])
+    k2 = max(4, steps // 2)
+    t0 = time.perf_counter()
+    for i in range(k2):
+        launch(i, False)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / k2
+    return {"value": units / e2e_s, "unit": "edges/s" if "N" in w else "samples/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * e2e_s,
+            "how": "pinned host buffers; H2D and D2H copies on their own streams, two device buffer sets; "
+                   "host wall clock from the first copy to the last result in host memory"}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+_W = {}
+
+
+def _oracle_init(cfgkey, files, threads_env):
+    os.environ.update(threads_env)
+    _W["cfg"] = cfgkey
+    _W["a"] = {k: np.load(f, mmap_mode="r") for k, f in files.items()}
+
+
+def _oracle_work(lo, hi):
+    """Forward + backward of the FP64 oracle over receivers (or samples) [lo, hi) of the
+    full-size workload; returns (units processed, seconds)."""
+    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+    from oracle import conv as oconv, irreps as oirr
+    c = CONFIGS[_W["cfg"]]
+    spec = wl.SPECS[c["name"]]
+    a = _W["a"]
+    if "plan" not in _W:
+        _W["plan"] = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], spec["mode"])
+    p = _W["plan"]
+    t0 = time.perf_counter()
+    if spec["graph"] is None:
+        x1, x2, W = (np.asarray(a[k][lo:hi]) for k in ("x1", "x2", "W"))
+        out = oconv.tp_uvu_forward(p, x1, x2, W)
+        oconv.tp_uvu_backward(p, out, x1, x2, W)
+        return hi - lo, time.perf_counter() - t0
+    rowptr = np.asarray(a["rowptr"])
+    nodes = np.arange(lo, hi)
+    edges = np.arange(rowptr[lo], rowptr[hi])
+    if spec["mode"] == "uvu":
+        out = oconv.conv_uvu_forward(p, a["x"], a["Y"], a["W"], rowptr, a["col"], nodes=nodes)
+        g = np.zeros((rowptr.shape[0] - 1, p.d_out))
+        g[lo:hi] = out
+        oconv.conv_uvu_backward(p, g, a["x"], a["Y"], a["W"], rowptr, a["col"], edges=edges)
+    else:
+        out = oconv.conv_uvw_radial_forward(p, a["x"], a["Y"], a["R"], a["M"], rowptr, a["col"], nodes=nodes)
+        g = np.zeros((rowptr.shape[0] - 1, p.d_out))
+        g[lo:hi] = out
+        oconv.conv_uvw_radial_backward(p, g, a["x"], a["Y"], a["R"], a["M"], rowptr, a["col"], edges=edges)
+    return int(edges.size), time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+class OracleTimer:
+    """The FP64 oracle over the full-size workload on every host core: one spawned process
+    per core (FP64 NumPy limited to one thread each), each taking its own range of receivers
+    (or samples).  The workload is drawn once and shared read-only through .npy files."""
+
+    def __init__(self, cfgkey, procs=None):
+        import multiprocessing as mp
+        from clebsch_gordan_tensor_racah_gb300 import workloads as wl
+        from oracle import irreps as oirr
+        c = CONFIGS[cfgkey]
+        if c["name"] not in ("tiny", "nequip", "mace", "highl", "uvw"):
+            raise ValueError(f"no oracle timing for {cfgkey}")
+        spec = wl.SPECS[c["name"]]
+        plan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], spec["mode"])
+        w = wl.make(c["name"], plan.w_numel, seed=0, dtype=c["dtype"])
+        self.tmp = tempfile.TemporaryDirectory(prefix="cgtp_oracle_")
+        files = {}
+        for k, v in w.items():
+            if isinstance(v, np.ndarray):
+                files[k] = os.path.join(self.tmp.name, k + ".npy")
+                np.save(files[k], v)
+        self.graph = spec["graph"] is not None
+        self.n = int(w["N"] if self.graph else w["B"])
+        self.rowptr = w.get("rowptr")
+        self.procs = procs or os.cpu_count() or 1
+        # one BLAS thread per process: the children read these when they import NumPy
+        env = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        saved = {k: os.environ.get(k) for k in env}
+        os.environ.update(env)
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.procs, initializer=_oracle_init,
+                                                     initargs=(cfgkey, files, env))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.cursor = 0
+        self.pool.starmap(_oracle_work, [(0, 1)] * self.procs)   # imports and plan in every worker
+
+    def step(self, per_proc):
+        """One step: every process runs `per_proc` consecutive receivers (samples), the
+        processes' ranges follow each other from the cursor (wrapping).  Returns
+        (units, wall seconds)."""
+        ranges = []
+        for _ in range(self.procs):
+            lo = self.cursor
+            hi = min(self.n, lo + per_proc)
+            ranges.append((lo, hi))
+            self.cursor = 0 if hi >= self.n else hi
+        t0 = time.perf_counter()
+        res = self.pool.starmap(_oracle_work, ranges)
+        return sum(u for u, _ in res), time.perf_counter() - t0
+
+    def calibrate(self, target_s):
+        """Receivers (samples) per process so that one step takes about target_s."""
+        per = 1
+        while True:
+            u, dt = self.step(per)
+            if dt > 0.3 * target_s or per >= self.n // self.procs:
+                break
+            per *= 4
+        return max(1, min(self.n // self.procs, int(per * target_s / max(dt, 1e-3))))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.tmp.cleanup()
+
+
+def oracle_baseline(cfgkey, budget_s=15.0):
+    """cpu_baseline of the headline line: the oracle on all host cores for about budget_s."""
+    t = OracleTimer(cfgkey)
+    try:
+        per = t.calibrate(budget_s / 3)
+        units = secs = 0.0
+        n_steps = 0
+        while secs < budget_s:
+            u, dt = t.step(per)
+            units += u
+            secs += dt
+            n_steps += 1
+        unit = "edges" if t.graph else "samples"
+        return {"value": units / secs, "unit": unit + "/s", "cores": t.procs, "kind": "oracle",
+                "cpu": cpu_model(), "cpu_count": os.cpu_count(), "sampled": True,
+                "sample": f"{n_steps} steps of {per} consecutive {'receivers' if t.graph else 'samples'} per "
+                          f"process x {t.procs} processes of the full-size workload ({int(units)} {unit}, "
+                          f"{secs:.1f} s), FP64 forward + backward"}
+    finally:
+        t.close()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfgkey = args.config
+    total = args.warmup + args.steps
+    t = OracleTimer(cfgkey)
+    try:
+        per = t.calibrate(min(8.0, 150.0 / max(1, total)))
+        for _ in range(args.warmup):
+            t.step(per)
+        units = secs = 0.0
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            u, dt = t.step(per)
+            units += u
+            secs += dt
+        wall = time.perf_counter() - t_wall
+    finally:
+        t.close()
+    rate = units / secs
+    unit = "edges/s" if t.graph else "samples/s"
+    line = {"metric": METRIC, "value": rate, "unit": unit, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[CONFIGS[cfgkey]["name"]],
+                       "step": "FP64 oracle forward + backward over a sample of the full-size workload",
+                       "sampled": True, "units_per_step": int(units / max(1, args.steps)),
+                       "timed_wall_s": wall},
+            "cpu_baseline": {"value": rate, "unit": unit, "cores": t.procs, "kind": "oracle",
+                             "cpu": cpu_model(), "cpu_count": os.cpu_count(), "sampled": True,
+                             "sample": f"{per} consecutive {'receivers' if t.graph else 'samples'} per process "
+                                       f"x {t.procs} processes per step of the full-size workload"},
+            "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# driver
+# ---------------------------------------------------------------------------
 
 def job_throughput(ms, units, world, device=None):
     """Whole-job throughput of N replicas (weak scaling: every rank processes its own
@@ -417,63 +849,52 @@ def dist_env():
     return rank, world, local
 
 
-def config_block(cfgkey, w, n_gpus):
-    c = CONFIGS[cfgkey]
-    spec = c["name"]
-    d = {"workload": {"tiny": "tiny uvu conv (64 nodes, 512 edges)",
-                      "nequip": "NequIP-like uvu conv (10k nodes x 32 in-edges, 32x(0e,1o,2e,3o), SH l<=3)",
-                      "mace": "MACE-like uvu conv (5k nodes, Poisson(40) in-degree, 128x(0e,1o,2e), SH l<=3)",
-                      "highl": "high-L batched TP (B=50k, 16x l=0..7, SH l<=7)",
-                      "uvw": "uvw radial conv (200k nodes x 32 in-edges, 64x(0e,1o,2e), K=8)",
-                      "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))",
-                      "mixed": "mixed uvu/uvw conv (10k nodes x 32 in-edges, 32x(0e,1o,2e), SH l<=2; "
-                               "0e outputs uvw with per-edge weights, 1o and 2e outputs uvu)"}[spec],
-         "step": "conv forward + backward" if "N" in w else "batched forward + backward",
-         "precision": "bfloat16 inputs, FP32 arithmetic and outputs" if c["dtype"] == "bfloat16" else c["dtype"],
-         "edge_features": "raw edge vectors, harmonics evaluated in the kernels" if c.get("sh") else "harmonics Y",
-         "l2": "inputs larger than L2 (no flush needed)",
-         "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
-    if "N" in w:
-        d.update(nodes=w["N"], edges=w["E"])
+def headline_roofline(cfgkey, r, ctx, pk, meas):
+    """The `roofline` object of the JSON line: the dominant kernel (the slower direction)
+    against its binding peak; achieved = algorithmic bytes or FLOPs of one launch / its
+    mean event-timed duration."""
+    plan = ctx[0]
+    ro = r["roofline"]
+    dominant = "backward" if r["bwd_ms"] >= r["fwd_ms"] else "forward"
+    d = "bwd" if dominant == "backward" else "fwd"
+    ms = r[d + "_ms"]
+    nbytes, flops = ro[d + "_bytes"], ro[d + "_flops"]
+    if plan.mode == "uvu" and "N" not in ctx[2]:
+        kname = {"fwd": "bt_forward_kernel", "bwd": "bt_backward_kernel"}[d]
+    elif plan.mode == "uvu":
+        kname = {"fwd": "uvu_forward3_kernel", "bwd": "uvu_backward3_kernel"}[d]
+    elif plan.mode == "mixed":
+        kname = f"mixed {dominant} (uvu + per-edge uvw kernels)"
+    elif plan.radial_k == 0:
+        kname = {"fwd": "uvwe_fwd_kernel", "bwd": "uvwe_bwd_kernel"}[d]
     else:
-        d.update(batch=w["B"])
-    return d
-
-
-def run_reference(args):
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
-    cfgkey = args.config
-    t_steps = []
-    rate = None
-    for i in range(args.warmup + args.steps):
-        r, desc = time_oracle_sample(cfgkey, budget_s=max(2.0, 40.0 / max(1, args.warmup + args.steps)))
-        if i >= args.warmup:
-            t_steps.append(r)
-    rate = float(np.median(t_steps))
-    from clebsch_gordan_tensor_racah_gb300 import workloads as wl
-    c = CONFIGS[cfgkey]
-    units = wl.SPECS[c["name"]].get("N", 0) * wl.SPECS[c["name"]].get("deg", 0) or wl.SPECS[c["name"]].get("B") or 512
-    line = {"metric": METRIC, "value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
-            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * units / rate, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": config_block(cfgkey, {"N": 1, "E": 0} if cfgkey != "highl" else {"B": 1}, 1)["workload"]},
-            "cpu_baseline": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
-                             "cores": 1, "kind": "oracle", "sample": desc},
-            "e2e": {"value": rate, "unit": "edges/s" if cfgkey != "highl" else "samples/s",
-                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+        kname = f"uvw radial {dominant} (edge stage + tensor-core node GEMM)"
+    if ro[d + "_bound"] == "hbm":
+        ach = nbytes / (ms * 1e-3) / 1e9
+        out = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+               "frac": ach / pk["hbm_gbs"], "peak_src": pk["src"] + " copy bandwidth (MEASURED_PEAKS.json)"}
+    else:
+        peak = ro["peaks_used"]["alu_tflops"]
+        ach = flops / (ms * 1e-3) / 1e12
+        out = {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+               "peak_src": "measured here: cgtp_measure_fma (" + ro["peaks_used"]["alu"] + ")"}
+    out.update({"kernel": kname, "traffic": traffic_for(kname, cfgkey, nbytes),
+                "algorithmic_bytes_per_launch": int(nbytes), "algorithmic_flops_per_launch": float(flops),
+                "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "fwd_roofline_ms": ro["fwd_roofline_ms"],
+                "bwd_roofline_ms": ro["bwd_roofline_ms"], "step_frac": ro["step_frac"]})
+    return out
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="nequip", choices=sorted(CONFIGS))
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="rewrite a 512 MiB buffer before every timed step (cold L2) for every workload")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-double-backward", action="store_true",
@@ -500,155 +921,63 @@ def main():
         torch.distributed.barrier()
     build()
 
-    plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device, args.nodes)
-    fwd, bwd, units, bf, bb, out_shape = step_fns(args.config, plan, graph, w, dev, tdt)
-    g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
-    out = torch.empty(out_shape, dtype=plan.out_dtype, device=device)
-    stream = torch.cuda.current_stream()
-
-    def step():
-        fwd(out)
-        return bwd(g, None)
-
     if args.profile_run:
+        plan, graph, w, host, dev, spec, tdt = build_inputs(args.config, device, args.nodes)
+        fwd, bwd, units, bf, bb, out_shape = step_fns(args.config, plan, graph, w, dev, tdt)
+        g = torch.randn(out_shape, dtype=tdt, device=device, generator=torch.Generator(device).manual_seed(1))
+        out = torch.empty(out_shape, dtype=plan.out_dtype, device=device)
         for _ in range(3):
-            step()
+            fwd(out)
+            bwd(g, None)
         torch.cuda.synchronize()
         print(f"profile run done: {args.config}, {units} units", flush=True)
         return
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    # per-kernel split (events on the launching stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    tf, tb = [], []
-    for _ in range(3):
-        ev[0].record(stream)
-        fwd(out)
-        ev[1].record(stream)
-        bwd(g, None)
-        ev[2].record(stream)
-        torch.cuda.synchronize()
-        tf.append(ev[0].elapsed_time(ev[1]))
-        tb.append(ev[1].elapsed_time(ev[2]))
-    # timed region
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
+    pk = driver_peaks()
+    meas = measure_peaks(device)
+    flush = True if args.flush_l2 else None
+    r, ctx = run_config(args.config, device, args.steps, args.warmup, meas, pk, flush, args.nodes)
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    fe = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    be = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e0.record(stream)
-    for i in range(args.steps):
-        fe[i].record(stream)
-        fwd(out)
-        be[i].record(stream)
-        bwd(g, None)
-    fe[args.steps].record(stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    fwd_ms = float(np.mean([fe[i].elapsed_time(be[i]) for i in range(args.steps)]))
-    bwd_ms = float(np.mean([be[i].elapsed_time(fe[i + 1]) for i in range(args.steps)]))
-    ms, value = job_throughput(ms, units, world, device)
-
-    # end to end through the public API with host buffers
-    e2e = None
+    ms, value = job_throughput(r["step_ms"], r["units"], world, device)
+    clk = r.pop("clocks")
+    unit = "edges/s" if r["unit"] == "edges" else "samples/s"
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": r["precision"], "data": "synthetic",
+            "config": {"workload": r["workload"], "step": "conv forward + backward" if "nodes" in r
+                       else "batched forward + backward", "l2": r["l2"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       **({"nodes": r["nodes"], "edges": r["edges"]} if "nodes" in r else {"batch": r["batch"]})},
+            "fwd_units_per_s": world * r["fwd_units_per_s"],
+            "roofline": headline_roofline(args.config, r, ctx, pk, meas),
+            "gpu_launches": r["gpu_launches_per_step"] * args.steps, "clocks": clk,
+            "peaks": {**meas, "hbm_copy_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                      "driver_peaks": pk["src"]}}
     if not args.no_e2e:
-        pin = {k: (v if isinstance(v, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(v))).pin_memory()
-               for k, v in host.items() if k not in ("rowptr", "col")}
-        gh = g.cpu().pin_memory()
-        out_h = torch.empty(out_shape, dtype=plan.out_dtype).pin_memory()
-        res_h = None
-        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + gh.numel() * gh.element_size()
-
-        def e2e_step():
-            nonlocal res_h
-            for k, t in pin.items():
-                dev[k].copy_(t, non_blocking=True)
-            g.copy_(gh, non_blocking=True)
-            fwd(out)
-            r = bwd(g, None)
-            out_h.copy_(out, non_blocking=True)
-            if res_h is None:
-                res_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in r if x is not None]
-            for hbuf, x in zip(res_h, [x for x in r if x is not None]):
-                hbuf.copy_(x, non_blocking=True)
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        d2h = out_h.numel() * out_h.element_size() + sum(t.numel() * t.element_size() for t in res_h)
-        k2 = max(3, args.steps // 4)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(k2):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / k2
-        e2e = {"value": world * units / (e2e_ms / 1000.0), "unit": "edges/s" if "N" in w else "samples/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-
-    pk = peaks()
-    mhz = (clk or {}).get("sm_max_mhz") or pk["sm_max_mhz"]
-    dt_name = "f64" if tdt == torch.float64 else "f32"
-    alu_peak = alu_peak_tflops(dt_name, mhz)
-    n_nodes = w.get("N", w.get("B", 0))
-    ff, fb = algorithmic_flops(plan, n_nodes, units)
-    dominant = "backward" if bwd_ms >= fwd_ms else "forward"
-    dom_ms = bwd_ms if dominant == "backward" else fwd_ms
-    dom_bytes = bb if dominant == "backward" else bf
-    dom_flops = fb if dominant == "backward" else ff
-    t_hbm = dom_bytes / (pk["hbm_gbs"] * 1e9)
-    t_alu = dom_flops / (alu_peak * 1e12)
-    kname = {("uvu", "forward"): "uvu_forward3_kernel", ("uvu", "backward"): "uvu_backward3_kernel",
-             ("uvwe", "forward"): "uvwe_fwd_kernel", ("uvwe", "backward"): "uvwe_bwd_kernel",
-             ("mixed", "forward"): "mixed forward (uvu_forward3_kernel + uvwe_fwd_kernel + fold)",
-             ("mixed", "backward"): "mixed backward (uvu_backward3_kernel + uvwe_bwd_kernel + adds)",
-             ("uvw", "forward"): "uvw forward (edge stage + node GEMM)",
-             ("uvw", "backward"): "uvw backward (node GEMMs + edge stage)"}[
-        ("uvwe" if plan.mode == "uvw" and plan.radial_k == 0 else plan.mode, dominant)]
-    launches = launches_per_step(args.config, plan, w) * args.steps
-    if "N" not in w:
-        kname = {"forward": "bt_forward_kernel", "backward": "bt_backward_kernel"}[dominant]
-    if t_hbm >= t_alu:
-        achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"] + " (copy bandwidth)"}
-    else:
-        achieved = dom_flops / (dom_ms / 1000.0) / 1e12
-        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                    "frac": achieved / alu_peak,
-                    "peak_src": f"derived: 152 SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz" if dt_name == "f32"
-                    else "nominal FP64 1.25 TFLOP/s"}
-    roofline.update({"kernel": kname, "traffic": traffic_for(kname, args.config, dom_bytes),
-                     "algorithmic_bytes_per_launch": int(dom_bytes), "algorithmic_flops_per_launch": int(dom_flops),
-                     "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-                     "fwd_roofline_ms": 1000 * max(bf / (pk["hbm_gbs"] * 1e9), ff / (alu_peak * 1e12)),
-                     "bwd_roofline_ms": 1000 * max(bb / (pk["hbm_gbs"] * 1e9), fb / (alu_peak * 1e12))})
-    roofline["step_frac"] = (roofline["fwd_roofline_ms"] + roofline["bwd_roofline_ms"]) / (fwd_ms + bwd_ms)
-    line = {"metric": METRIC, "value": value, "unit": "edges/s" if "N" in w else "samples/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {torch.float64: "f64", torch.bfloat16: "bf16 inputs, f32 arithmetic"}.get(tdt, "f32"),
-            "data": "synthetic",
-            "config": config_block(args.config, w, world),
-            "fwd_units_per_s": world * units / (fwd_ms / 1000.0),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk}
-    if not args.no_double_backward and tdt != torch.bfloat16 and not CONFIGS[args.config].get("sh"):
-        line["double_backward"] = time_double_backward(plan, graph, w, dev, g, stream, units, roofline)
-    if rank == 0 and not args.no_cpu_baseline:
-        rate, desc = time_oracle_sample(args.config)
-        line["cpu_baseline"] = {"value": rate, "unit": line["unit"], "cores": 1, "kind": "oracle",
-                                "sample": desc}
+        line["e2e"] = time_e2e(ctx, device, args.steps)
+        line["e2e"]["link"] = measure_link(device)
+        line["e2e"]["value"] *= world
+    if not args.no_double_backward and ctx[5] != torch.bfloat16 and not CONFIGS[args.config].get("sh"):
+        line["double_backward"] = time_double_backward(ctx[0], ctx[1], ctx[2], ctx[4], ctx[8],
+                                                       torch.cuda.current_stream(device), r["units"], r["roofline"])
+    line["per_workload_roofline"] = r["roofline"]
+    del ctx
+    torch.cuda.empty_cache()
+    if not args.no_per_config and args.nodes is None:
+        per = {}
+        for k in PER_CONFIG:
+            if k == args.config:
+                continue
+            steps = min(args.steps, 8) if k in ("uvw", "mace64") else args.steps
+            rk, ck = run_config(k, device, steps, args.warmup, meas, pk, flush)
+            del ck
+            torch.cuda.empty_cache()
+            per[k] = rk
+        line["per_config"] = per
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.config in ("tiny", "nequip", "mace",
+                                                                                   "highl", "uvw"):
+        line["cpu_baseline"] = oracle_baseline(args.config)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -5,7 +5,8 @@ kernels of ``libcgtp.so`` (built in-tree by ``_build.build()``).  PyTorch is use
 for device memory and streams.  There is no CPU fallback: if the library is
 missing or no GPU is present the calls raise.
 
-Names follow the C ABI in ``include/cgtp.h``:
+Names follow the C ABI in ``include/cgtp.h`` (and ``include/cgtp_measure.h`` for the
+measurement kernels ``measure_fma`` / ``measure_read``):
 
 * ``Plan(irreps_in1, irreps_in2, irreps_out, mode, dtype, radial_k)`` --
   ``cgtp_plan_create``; ``plan.d1, d2, d_out, w_numel, n_paths``;
@@ -39,7 +40,8 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_conv_forward_sh_radial", "cgtp_conv_backward_sh_radial",
            "cgtp_mixed_plan_create", "cgtp_mixed_plan_destroy", "cgtp_mixed_plan_info",
            "cgtp_mixed_conv_workspace", "cgtp_mixed_conv_forward", "cgtp_mixed_conv_backward",
-           "cgtp_mixed_conv_double_backward"]
+           "cgtp_mixed_conv_double_backward", "cgtp_measure_fma", "cgtp_measure_read",
+           "cgtp_plan_device_bytes", "cgtp_graph_device_bytes"]
 
 
 class CgtpError(RuntimeError):
@@ -96,6 +98,10 @@ def lib():
         L.cgtp_mixed_conv_forward.argtypes = [vp] * 8 + [i64, vp]
         L.cgtp_mixed_conv_backward.argtypes = [vp] * 12 + [i64, vp]
         L.cgtp_mixed_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
+        L.cgtp_plan_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
+        L.cgtp_graph_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
+        L.cgtp_measure_fma.argtypes = [i32, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
+        L.cgtp_measure_read.argtypes = [vp, i64, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
         for name in EXPORTS:
             if name not in ("cgtp_last_error", "cgtp_plan_destroy", "cgtp_graph_destroy",
                             "cgtp_mixed_plan_destroy"):
@@ -189,6 +195,19 @@ class Plan:
     def handle(self):
         return self._h
 
+    def device_bytes(self):
+        """Device memory the library holds for this plan (cgtp_plan_device_bytes)."""
+        nb = ctypes.c_int64()
+        _check(lib().cgtp_plan_device_bytes(self._h, ctypes.byref(nb)))
+        return nb.value
+
+    def launches_per_step(self, n_nodes):
+        """Kernel launches of one forward + backward of a radial uvw plan on n_nodes nodes:
+        per streamed node chunk of the plan, the forward's edge stage and node GEMM and
+        the backward's GEMM, edge stage, two GEMMs and split-K reduction."""
+        chunk = 4096
+        return 7 * max(1, -(-int(n_nodes) // chunk))
+
     def path(self, p):
         ints = (ctypes.c_int * 10)()
         _check(lib().cgtp_plan_path(self._h, p, ints, None, 0))
@@ -221,6 +240,12 @@ class Graph:
     @property
     def handle(self):
         return self._h
+
+    def device_bytes(self):
+        """Device memory the library holds for this graph (cgtp_graph_device_bytes)."""
+        nb = ctypes.c_int64()
+        _check(lib().cgtp_graph_device_bytes(self._h, ctypes.byref(nb)))
+        return nb.value
 
     def transpose(self, stream=None):
         torch = _torch()
@@ -379,6 +404,25 @@ def cgtp_conv_backward_sh_radial(plan, graph, gout, x, rvec, M, rbf_lo=0.5, rbf_
         _ptr(M, "M", dt), float(rbf_lo), float(rbf_hi), _ptr(gx, "gx"), _ptr(gY, "gY"), _ptr(gR, "gR"),
         _ptr(grvec, "grvec"), _ptr(gM, "gM"), _stream(stream)))
     return gx, gY, gR, grvec, gM
+
+
+CGTP_MEASURE_FFMA, CGTP_MEASURE_FFMA2, CGTP_MEASURE_DFMA = 0, 1, 2
+
+
+def measure_fma(kind, ctas, iters, sink, stream=None):
+    """Enqueue one arithmetic-throughput launch (cgtp_measure_fma); returns its FLOPs."""
+    fl = ctypes.c_double()
+    _check(lib().cgtp_measure_fma(int(kind), int(ctas), int(iters), _ptr(sink, "sink"), ctypes.byref(fl),
+                                  _stream(stream)))
+    return fl.value
+
+
+def measure_read(buf, reps, ctas, sink, stream=None):
+    """Enqueue one read-bandwidth launch over buf (cgtp_measure_read); returns the bytes read."""
+    nb = ctypes.c_double()
+    _check(lib().cgtp_measure_read(_ptr(buf, "buf"), buf.numel() * buf.element_size(), int(reps), int(ctas),
+                                   _ptr(sink, "sink"), ctypes.byref(nb), _stream(stream)))
+    return nb.value
 
 
 class MixedPlan:

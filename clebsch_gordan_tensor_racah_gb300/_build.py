@@ -22,7 +22,7 @@ CU_SOURCES = ["api.cu", "graph.cu", "uvu.cu", "uvu_f32.cu", "uvu_f32_l7.cu", "uv
               "uvu3_f64_2.cu", "uvu3_f64_8.cu", "uvu3_f64_32.cu", "uvw.cu", "bt.cu", "dbl.cu",
               "uvu3_bf16_2.cu", "uvu3_bf16_8.cu", "uvu3_bf16_32.cu", "sh.cu",
               "uvu3_sh_f32_2.cu", "uvu3_sh_f32_8.cu", "uvu3_sh_f32_32.cu", "uvu3_sh_f64_2.cu",
-              "uvu3_sh_f64_8.cu", "uvu3_sh_f64_32.cu", "uvwe.cu", "mixed.cu"]
+              "uvu3_sh_f64_8.cu", "uvu3_sh_f64_32.cu", "uvwe.cu", "mixed.cu", "measure.cu"]
 CPP_SOURCES = ["planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -35,7 +35,7 @@ def _nvcc():
 
 
 def _headers_mtime():
-    m = os.path.getmtime(os.path.join(INC, "cgtp.h"))
+    m = max(os.path.getmtime(os.path.join(INC, h)) for h in os.listdir(INC) if h.endswith(".h"))
     for f in os.listdir(CSRC):
         if f.endswith((".h", ".cuh")):
             m = max(m, os.path.getmtime(os.path.join(CSRC, f)))

@@ -92,6 +92,7 @@ cgtp_status upload_layout(const cgtp_plan_s* plan, const LayoutHost& h, LayoutDe
   void* base = nullptr;
   if (cudaMalloc(&base, std::max<size_t>(buf.size(), 16)) != cudaSuccess)
     return fail(CGTP_ENOMEM, "plan table allocation failed");
+  const_cast<cgtp_plan_s*>(plan)->device_bytes += std::max<size_t>(buf.size(), 16);
   if (cudaMemcpy(base, buf.data(), buf.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(base);
     return fail(CGTP_ECUDA, "plan table upload failed");
@@ -239,6 +240,20 @@ cgtp_status cgtp_plan_info(cgtp_plan plan, int64_t* d1, int64_t* d2, int64_t* d_
   if (d_out) *d_out = plan->d_out;
   if (w_numel) *w_numel = plan->w_numel;
   if (n_paths) *n_paths = static_cast<int>(plan->paths.size());
+  return CGTP_OK;
+}
+
+cgtp_status cgtp_plan_device_bytes(cgtp_plan plan, int64_t* bytes) {
+  clear_error();
+  if (!plan || !bytes) return fail(CGTP_EINVAL, "null plan or bytes");
+  *bytes = static_cast<int64_t>(plan->device_bytes);
+  return CGTP_OK;
+}
+
+cgtp_status cgtp_graph_device_bytes(cgtp_graph graph, int64_t* bytes) {
+  clear_error();
+  if (!graph || !bytes) return fail(CGTP_EINVAL, "null graph or bytes");
+  *bytes = static_cast<int64_t>(sizeof(int32_t)) * (graph->N + 1 + 2 * std::max<int64_t>(graph->E, 1));
   return CGTP_OK;
 }
 

@@ -658,6 +658,7 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
     delete st;
     return fail(CGTP_ENOMEM, "batched-product counter allocation failed");
   }
+  plan->device_bytes += buf.size() + 2 * sizeof(int);
   auto at = [&](size_t off) { return static_cast<unsigned char*>(st->tables) + off; };
   st->paths = reinterpret_cast<const BtPath*>(at(o_p));
   st->groups = reinterpret_cast<const BtGroup*>(at(o_g));

@@ -154,6 +154,8 @@ struct cgtp_plan_s {
   void* bt = nullptr;
   // uvw with a weight matrix per edge (radial_k == 0, uvwe.cu)
   void* uvwe = nullptr;
+  // device memory the plan owns (tables, work counters, scratch), for cgtp_plan_device_bytes
+  size_t device_bytes = 0;
 };
 
 struct cgtp_graph_s {

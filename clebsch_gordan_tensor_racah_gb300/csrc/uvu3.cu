@@ -119,6 +119,7 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   const size_t o_gxq = put(gx_paths.data(), std::max<size_t>(gx_paths.size(), 1) * sizeof(int));
   void* base = nullptr;
   if (cudaMalloc(&base, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "plan table allocation failed");
+  plan->device_bytes += buf.size();
   if (cudaMemcpy(base, buf.data(), buf.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(base);
     return fail(CGTP_ECUDA, "plan table upload failed");

@@ -856,6 +856,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     for (int w0 = 0; w0 < st->paths_h[p].mul_out; w0 += 32) b3.push_back({p, w0});
   const size_t o_b3 = put(b3.data(), b3.size() * sizeof(Item));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "uvw tables");
+  plan->device_bytes += buf.size();
   cudaMemcpy(st->tables, buf.data(), buf.size(), cudaMemcpyHostToDevice);
   auto at = [&](size_t o) { return static_cast<unsigned char*>(st->tables) + o; };
   st->paths = reinterpret_cast<UvwPath*>(at(o_paths));
@@ -882,6 +883,8 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   if (cudaMalloc(&st->err_dev, sizeof(int)) != cudaSuccess ||
       cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocDefault) != cudaSuccess)
     return fail(CGTP_ENOMEM, "uvw error flag allocation failed");
+  plan->device_bytes += st->scratch_elems * sizeof(float) + sizeof(float) * kGmSplits * st->K * plan->w_numel +
+                        sizeof(int);
   cudaMemset(st->err_dev, 0, sizeof(int));
   *st->err_host = 0;
   if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)

@@ -533,6 +533,7 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
     delete st;
     return fail(CGTP_ECUDA, "per-edge uvw table upload failed");
   }
+  plan->device_bytes += buf.size();
   auto at = [&](size_t o) { return static_cast<unsigned char*>(st->tables) + o; };
   st->paths = reinterpret_cast<const EPath*>(at(o_p));
   st->C = at(o_c);

@@ -139,6 +139,17 @@ cgtp_status cgtp_graph_create(cgtp_graph* graph, const int32_t* rowptr, const in
                               int64_t N, int64_t E, void* stream);
 void cgtp_graph_destroy(cgtp_graph graph);
 
+/*
+ * Device memory the library holds for a plan (constant tables, work counters,
+ * the uvw node-state scratch and gM partials) or a graph (the transpose
+ * arrays), in bytes.  Callers' tensors are not included.  Memory accounting
+ * in the spirit of the allocated-memory checks of "The GPU memory
+ * optimization with Larger angular momentum" and the peak-memory figures of
+ * "Sobek ...", Abstract.  CGTP_EINVAL for a null argument.
+ */
+cgtp_status cgtp_plan_device_bytes(cgtp_plan plan, int64_t* bytes);
+cgtp_status cgtp_graph_device_bytes(cgtp_graph graph, int64_t* bytes);
+
 /* Device-to-device copy of the transpose arrays (any pointer may be NULL). */
 cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t_eid,
                                  int32_t* t_dst, void* stream);

@@ -1,6 +1,6 @@
 """Host-side checks of the C-ABI library (no GPU needed).
 
-* libcgtp.so loads and exports every function declared in include/cgtp.h;
+* libcgtp.so loads and exports every function declared in include/*.h;
 * the planner's real CG blocks (an independent C++ Racah implementation) agree
   with the oracle's to 1e-14 for every (l1, l2, l3) with l <= 7;
 * argument checks that fail before any device work.
@@ -16,13 +16,16 @@ import pytest
 import clebsch_gordan_tensor_racah_gb300 as cg
 from oracle import cg as ocg
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cgtp.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cgtp_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(cgtp_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_exports():
