@@ -134,12 +134,12 @@ def measure_peaks(device):
         out[name + "_tflops"] = fl / (ms * 1e-3) / 1e12
     rsink = torch.empty(nsm * 4 * 256, dtype=torch.int32, device=device)
     rc = nsm * 4
-    l2buf = torch.ones(64 * 2 ** 20 // 4, dtype=torch.int32, device=device)
+    q = 4096 * rc
+    l2buf = torch.ones((64 * 2 ** 20 // q) * q // 4, dtype=torch.int32, device=device)
     cg.measure_read(l2buf, 1, rc, rsink, stream)
     ms, nb = _time_launches(lambda: cg.measure_read(l2buf, 40, rc, rsink, stream), stream, 3)
     out["l2_read_gbs"] = nb / (ms * 1e-3) / 1e9
     del l2buf
-    q = 4096 * rc
     hbuf = torch.ones((4 * 2 ** 30 // q) * q // 4, dtype=torch.int32, device=device)
     ms, nb = _time_launches(lambda: cg.measure_read(hbuf, 1, rc, rsink, stream), stream, 3)
     out["hbm_read_gbs"] = nb / (ms * 1e-3) / 1e9
@@ -795,7 +795,7 @@ def run_reference(args):
     total = args.warmup + args.steps
     t = OracleTimer(cfgkey)
     try:
-        per = t.calibrate(min(8.0, 150.0 / max(1, total)))
+        per = t.calibrate(min(6.0, 100.0 / max(1, total)))
         for _ in range(args.warmup):
             t.step(per)
         units = secs = 0.0
