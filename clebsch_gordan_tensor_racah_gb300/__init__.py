@@ -41,7 +41,7 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_mixed_plan_create", "cgtp_mixed_plan_destroy", "cgtp_mixed_plan_info",
            "cgtp_mixed_conv_workspace", "cgtp_mixed_conv_forward", "cgtp_mixed_conv_backward",
            "cgtp_mixed_conv_double_backward", "cgtp_measure_fma", "cgtp_measure_read",
-           "cgtp_plan_device_bytes", "cgtp_graph_device_bytes"]
+           "cgtp_plan_device_bytes", "cgtp_graph_device_bytes", "cgtp_plan_set_wait_limit"]
 
 
 class CgtpError(RuntimeError):
@@ -99,6 +99,7 @@ def lib():
         L.cgtp_mixed_conv_backward.argtypes = [vp] * 12 + [i64, vp]
         L.cgtp_mixed_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
         L.cgtp_plan_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
+        L.cgtp_plan_set_wait_limit.argtypes = [vp, i64]
         L.cgtp_graph_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
         L.cgtp_measure_fma.argtypes = [i32, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
         L.cgtp_measure_read.argtypes = [vp, i64, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
@@ -194,6 +195,10 @@ class Plan:
     @property
     def handle(self):
         return self._h
+
+    def set_wait_limit(self, polls):
+        """Polls before a staging wait of the plan's kernels gives up (cgtp_plan_set_wait_limit)."""
+        _check(lib().cgtp_plan_set_wait_limit(self._h, int(polls)))
 
     def device_bytes(self):
         """Device memory the library holds for this plan (cgtp_plan_device_bytes)."""

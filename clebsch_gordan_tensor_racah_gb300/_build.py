@@ -34,16 +34,32 @@ def _nvcc():
     raise RuntimeError("nvcc not found")
 
 
-def _headers_mtime():
-    m = max(os.path.getmtime(os.path.join(INC, h)) for h in os.listdir(INC) if h.endswith(".h"))
-    for f in os.listdir(CSRC):
-        if f.endswith((".h", ".cuh")):
-            m = max(m, os.path.getmtime(os.path.join(CSRC, f)))
+_INC_RE = None
+
+
+def _deps_mtime(path, seen=None):
+    """Newest mtime of a source and the quoted headers it includes, transitively
+    (looked up next to it, in include/ and in the generated-code folder)."""
+    global _INC_RE
+    import re
+    if _INC_RE is None:
+        _INC_RE = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
+    seen = set() if seen is None else seen
+    if path in seen or not os.path.exists(path):
+        return 0.0
+    seen.add(path)
+    m = os.path.getmtime(path)
+    for name in _INC_RE.findall(open(path, errors="replace").read()):
+        for d in (os.path.dirname(path), CSRC, INC, GEN):
+            cand = os.path.join(d, name)
+            if os.path.exists(cand):
+                m = max(m, _deps_mtime(cand, seen))
+                break
     return m
 
 
-def _stale(src, obj, hdr_m):
-    return not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_m)
+def _stale(src, obj):
+    return not os.path.exists(obj) or os.path.getmtime(obj) < _deps_mtime(src)
 
 
 def _run(cmd):
@@ -74,19 +90,19 @@ def build(verbose=False, jobs=None):
     """Compile (incrementally) and link libcgtp.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    hdr_m = max(_headers_mtime(), _bake())
+    _bake()
     cmds = []
     objs = []
     for f in CU_SOURCES:
         src, obj = os.path.join(CSRC, f), os.path.join(BUILD, f + ".o")
         objs.append(obj)
-        if _stale(src, obj, hdr_m):
+        if _stale(src, obj):
             cmds.append([nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
                          "-Xcompiler", "-ffp-contract=off", "-I", INC, "-I", GEN, "-c", src, "-o", obj])
     for f in CPP_SOURCES:
         src, obj = os.path.join(CSRC, f), os.path.join(BUILD, f + ".o")
         objs.append(obj)
-        if _stale(src, obj, hdr_m):
+        if _stale(src, obj):
             cmds.append(["g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-I", INC,
                          "-c", src, "-o", obj])
     jobs = jobs or max(1, min(len(cmds), os.cpu_count() or 4))

@@ -243,6 +243,14 @@ cgtp_status cgtp_plan_info(cgtp_plan plan, int64_t* d1, int64_t* d2, int64_t* d_
   return CGTP_OK;
 }
 
+cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls) {
+  clear_error();
+  if (!plan) return fail(CGTP_EINVAL, "null plan");
+  if (polls < 0) return fail(CGTP_EINVAL, "polls must be >= 0");
+  plan->v3.wait_limit = polls;
+  return CGTP_OK;
+}
+
 cgtp_status cgtp_plan_device_bytes(cgtp_plan plan, int64_t* bytes) {
   clear_error();
   if (!plan || !bytes) return fail(CGTP_EINVAL, "null plan or bytes");

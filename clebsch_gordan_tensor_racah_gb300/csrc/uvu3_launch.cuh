@@ -1,5 +1,6 @@
 // uvu3_launch.cuh -- host launch glue of the warp-autonomous uvu kernels
-// (uvu3_impl.cuh), written once for every instance.
+// (uvu3_impl.cuh, and their staged form uvu4_impl.cuh when the plan's copies
+// are 16-byte aligned), written once for every instance.
 //
 // An instance is (T, S, SH, LPE): arithmetic/output type, storage type of the
 // inputs (T or bfloat16), edge vectors instead of harmonics, lanes per edge.
@@ -10,6 +11,7 @@
 #include <string>
 
 #include "uvu3_impl.cuh"
+#include "uvu4_impl.cuh"
 
 namespace cgtp {
 namespace uvu3_detail {
@@ -43,6 +45,37 @@ inline const char* v3_variant_name(bool bf16, bool sh) {
   return sh ? " (edge vectors)" : bf16 ? " (bf16)" : "";
 }
 
+// Staged (v4) launch: dynamic shared memory = 8 rings; the kernel's limit is
+// raised to the device cap once per device.
+template <typename T, typename S>
+uvu4_detail::Uvu4Args<T, S> v4_args(const cgtp_plan_s* plan, const Uvu3Args<T, S>& b, const V4Ring& r) {
+  uvu4_detail::Uvu4Args<T, S> a{};
+  a.b = b;
+  a.r = r;
+  a.ublock = 4 * plan->v3.lpe;
+  a.err = plan->v3.err_dev;
+  a.wait_limit = plan->v3.wait_limit;
+  return a;
+}
+
+template <typename K>
+bool v4_ready(K kernel, size_t smem) {
+  static int raised[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!raised[dev]) {
+    if (raise_smem_limit(reinterpret_cast<const void*>(kernel)) < static_cast<int>(smem)) return false;
+    raised[dev] = 1;
+  }
+  return true;
+}
+
+inline cgtp_status v4_sticky(const cgtp_plan_s* plan) {
+  if (plan->v3.err_host && *plan->v3.err_host)
+    return fail(CGTP_ECUDA, "a staging wait of an earlier call on this plan gave up (results of that call are invalid)");
+  return CGTP_OK;
+}
+
 // forward: E_in is Y [E, d2] (SH = false) or the edge vectors [E, 3] (SH = true)
 template <typename T, typename S, bool SH, int LPE>
 cgtp_status v3_forward(const cgtp_plan_s* plan, const void* x, const void* E_in, const void* W, void* out,
@@ -56,6 +89,21 @@ cgtp_status v3_forward(const cgtp_plan_s* plan, const void* x, const void* E_in,
   a.rowptr = rowptr;
   a.col = col;
   a.N = static_cast<int>(N);
+  const V4Ring& r4 = plan->v3.v4_fwd[SH ? 1 : 0];
+  if (r4.S > 0) {
+    if (cgtp_status e = v4_sticky(plan)) return e;
+    auto k4 = uvu4_detail::uvu_forward4_kernel<T, LPE, S, SH>;
+    const size_t smem = size_t(uvu4_detail::kV4Warps) * r4.warp_bytes;
+    if (v4_ready(k4, smem)) {
+      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, plan->num_sms)));
+      k4<<<grid, uvu4_detail::kV4Threads, smem, st>>>(v4_args(plan, a, r4));
+      const cudaError_t err = cudaGetLastError();
+      if (err != cudaSuccess)
+        return fail(CGTP_ECUDA, std::string("uvu forward (v4") + v3_variant_name(sizeof(S) == 2, SH) +
+                                    ") launch: " + cudaGetErrorString(err));
+      return CGTP_OK;
+    }
+  }
   auto k = uvu_forward3_kernel<T, LPE, S, SH>;
   k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, 0, st>>>(a);
   const cudaError_t err = cudaGetLastError();
@@ -85,6 +133,21 @@ cgtp_status v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
   a.phase_begin = plan->v3.phase_begin;
   a.n_phases = plan->v3.n_phases;
   a.N = static_cast<int>(N);
+  const V4Ring& r4 = plan->v3.v4_bwd[SH ? 1 : 0];
+  if (r4.S > 0) {
+    if (cgtp_status e = v4_sticky(plan)) return e;
+    auto k4 = uvu4_detail::uvu_backward4_kernel<T, LPE, S, SH>;
+    const size_t smem = size_t(uvu4_detail::kV4Warps) * r4.warp_bytes;
+    if (v4_ready(k4, smem)) {
+      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, plan->num_sms)));
+      k4<<<grid, uvu4_detail::kV4Threads, smem, st>>>(v4_args(plan, a, r4));
+      const cudaError_t err = cudaGetLastError();
+      if (err != cudaSuccess)
+        return fail(CGTP_ECUDA, std::string("uvu backward (v4") + v3_variant_name(sizeof(S) == 2, SH) +
+                                    ") launch: " + cudaGetErrorString(err));
+      return CGTP_OK;
+    }
+  }
   auto k = uvu_backward3_kernel<T, LPE, S, SH>;
   k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, 0, st>>>(a);
   const cudaError_t err = cudaGetLastError();

@@ -150,6 +150,20 @@ void cgtp_graph_destroy(cgtp_graph graph);
 cgtp_status cgtp_plan_device_bytes(cgtp_plan plan, int64_t* bytes);
 cgtp_status cgtp_graph_device_bytes(cgtp_graph graph, int64_t* bytes);
 
+/*
+ * cgtp_plan_set_wait_limit -- polls of an mbarrier before a wait of the
+ *  plan's staged uvu kernels gives up (default 4,194,304).  The staged kernels
+ *  move every gathered operand with bulk asynchronous copies that complete on
+ *  mbarriers ("An Efficient Sparse Kernel Generator ...", Abstract: register-
+ *  and shared-memory-resident operands); no wait is unbounded.  A wait that
+ *  gives up records the failure in the plan's error word, lets its copies in
+ *  flight land (bounded) and leaves the kernel; that call's results are
+ *  invalid and every later call on the plan returns CGTP_ECUDA.  0 makes the
+ *  first wait give up at once (fault injection for tests: the GPU stays
+ *  usable).  CGTP_EINVAL for a null plan or polls < 0.
+ */
+cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls);
+
 /* Device-to-device copy of the transpose arrays (any pointer may be NULL). */
 cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t_eid,
                                  int32_t* t_dst, void* stream);

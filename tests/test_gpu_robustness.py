@@ -1,0 +1,133 @@
+"""Failure handling and memory safety of the CUDA path, on the GPU.
+
+* Bounded waits: the staged uvu kernels wait on mbarriers for their bulk
+  copies.  A plan whose wait limit is 0 gives up at the first wait; the kernel
+  records the failure in the plan's error word, lets its copies land and exits.
+  That call's results are invalid, the plan's next call returns CGTP_ECUDA, and
+  the GPU stays usable (a fresh plan on the same graph matches the oracle).
+* Host checks: a misaligned tensor pointer is rejected with CGTP_EINVAL before
+  anything is launched.
+* Canaries: every output tensor is surrounded by guard words; forward and
+  backward leave the guards untouched (no write outside the outputs).
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import clebsch_gordan_tensor_racah_gb300 as cg  # noqa: E402
+from clebsch_gordan_tensor_racah_gb300 import workloads as wl  # noqa: E402
+from oracle import conv as oconv, irreps as oirr  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def T(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _workload(name="nequip", N=300, dtype=np.float32):
+    spec = wl.SPECS[name]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvu")
+    w = wl.make(name, oplan.w_numel, seed=3, dtype=dtype, N=N)
+    return spec, oplan, w
+
+
+def _plan(spec, dtype=torch.float32):
+    return cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", dtype)
+
+
+@pytest.mark.parametrize("direction", ["forward", "backward"])
+def test_wait_give_up_is_reported_and_the_gpu_stays_usable(direction):
+    spec, oplan, w = _workload()
+    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
+    x, Y, W = T(w["x"]), T(w["Y"]), T(w["W"])
+    g = T(np.random.default_rng(5).standard_normal((w["N"], oplan.d_out)).astype(np.float32))
+    bad = _plan(spec)
+    bad.set_wait_limit(0)
+    if direction == "forward":
+        cg.cgtp_conv_forward(bad, graph, x, Y, W)       # enqueued; its results are invalid
+    else:
+        cg.cgtp_conv_backward(bad, graph, g, x, Y, W)
+    torch.cuda.synchronize()                            # the kernel left on its own
+    with pytest.raises(cg.CgtpError) as e:
+        cg.cgtp_conv_forward(bad, graph, x, Y, W)
+    assert e.value.status == cg.CGTP_ECUDA
+    assert "gave up" in str(e.value)
+    with pytest.raises(cg.CgtpError):                   # sticky
+        cg.cgtp_conv_backward(bad, graph, g, x, Y, W)
+    good = _plan(spec)
+    out = cg.cgtp_conv_forward(good, graph, x, Y, W)
+    gx, gY, gW, _ = cg.cgtp_conv_backward(good, graph, g, x, Y, W)
+    torch.cuda.synchronize()
+    ref = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+    rgx, _, rgW = oconv.conv_uvu_backward(oplan, g.cpu().numpy(), w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+    for got, r in ((out, ref), (gx, rgx), (gW, rgW)):
+        got = got.cpu().numpy().astype(np.float64)
+        assert np.abs(got - r).max() <= 1e-4 * np.abs(r).max()
+
+
+def test_wait_limit_rejects_negative():
+    spec, _, _ = _workload(N=8)
+    with pytest.raises(cg.CgtpError) as e:
+        _plan(spec).set_wait_limit(-1)
+    assert e.value.status == cg.CGTP_EINVAL
+
+
+def test_misaligned_pointer_is_rejected_before_launch():
+    spec, oplan, w = _workload(N=40)
+    plan = _plan(spec)
+    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
+    x, Y, W = T(w["x"]), T(w["Y"]), T(w["W"])
+    out = torch.zeros(w["N"] * oplan.d_out + 4, dtype=torch.float32, device=DEV)
+    L = cg.lib()
+    st = torch.cuda.current_stream().cuda_stream
+    vp = ctypes.c_void_p
+    shifted = vp(out.data_ptr() + 4)                   # 4-byte offset: not 16-byte aligned
+    s = L.cgtp_conv_forward(plan.handle, graph.handle, vp(x.data_ptr()), vp(Y.data_ptr()), vp(W.data_ptr()),
+                            None, shifted, vp(st))
+    assert s == cg.CGTP_EINVAL
+    assert b"aligned" in L.cgtp_last_error()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0               # nothing ran
+
+
+def _guarded(shape, dtype, guard=64):
+    """A tensor of `shape` inside a buffer with `guard` sentinel words on each side."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * guard,), 7.25e30, dtype=dtype, device=DEV)
+    return buf, buf[guard:guard + n].view(*shape), guard
+
+
+@pytest.mark.parametrize("name,dtype", [("nequip", np.float32), ("mace", np.float64), ("tiny", np.float32)])
+def test_outputs_leave_guard_words_untouched(name, dtype):
+    if name == "tiny":
+        spec, oplan, w = _workload_tiny(dtype)
+    else:
+        spec, oplan, w = _workload(name, N=64, dtype=dtype)
+    tdt = torch.float64 if dtype == np.float64 else torch.float32
+    plan = _plan(spec, tdt)
+    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
+    x, Y, W = T(w["x"]), T(w["Y"]), T(w["W"])
+    bo, out, k = _guarded((w["N"], oplan.d_out), tdt)
+    cg.cgtp_conv_forward(plan, graph, x, Y, W, out=out)
+    g = T(np.random.default_rng(9).standard_normal((w["N"], oplan.d_out)).astype(dtype))
+    bufs = [_guarded(t.shape, tdt) for t in (x, Y, W)]
+    cg.cgtp_conv_backward(plan, graph, g, x, Y, W, outs=(bufs[0][1], bufs[1][1], bufs[2][1], None))
+    torch.cuda.synchronize()
+    for b, _, kk in [(bo, out, k)] + bufs:
+        assert torch.all(b[:kk] == 7.25e30) and torch.all(b[-kk:] == 7.25e30)
+    ref = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
+    tol = 1e-10 if dtype == np.float64 else 1e-4
+    assert np.abs(out.cpu().numpy() - ref).max() <= tol * np.abs(ref).max()
+
+
+def _workload_tiny(dtype):
+    spec = wl.SPECS["tiny"]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvu")
+    return spec, oplan, wl.make("tiny", oplan.w_numel, seed=3, dtype=dtype)
