@@ -8,6 +8,8 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
 
 #include "internal.h"
@@ -34,6 +36,22 @@ void append(std::vector<unsigned char>& buf, const std::vector<T>& v, size_t* of
 }
 
 }  // namespace
+
+int smem_cap_cached(const void* kernel) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> caps;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = caps.find({kernel, dev});
+  if (it != caps.end()) return it->second;
+  const int cap = raise_smem_limit(kernel);
+  if (cap >= 0) caps[{kernel, dev}] = cap;
+  return cap;
+}
 
 int raise_smem_limit(const void* kernel) {
   int dev = 0, optin = 0;

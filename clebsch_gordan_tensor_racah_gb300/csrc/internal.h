@@ -108,6 +108,8 @@ struct LayoutDev {
 
 // Polls of an mbarrier before a bounded wait gives up (the staged uvu kernels).
 constexpr long long kDefaultWaitPolls = 1ll << 22;
+// ints of the staged kernels' host-mapped error word (flag + where a wait gave up)
+constexpr int kErrWords = 16;
 
 // Staging geometry of the v4 uvu kernels (uvu4_impl.cuh): each warp owns a
 // ring of S stages of SC edges in shared memory.
@@ -198,6 +200,8 @@ void clear_error();
 // The limit belongs to the kernel and is shared by every plan, so it is only
 // ever raised to the cap, never set to one plan's need.
 int raise_smem_limit(const void* kernel);
+// The same, done once per (kernel, device) and remembered (thread-safe).
+int smem_cap_cached(const void* kernel);
 
 bool parse_irreps(const char* s, std::vector<Irrep>* out, std::string* err);
 double cg_complex(int j1, int m1, int j2, int m2, int J, int M);

@@ -210,9 +210,10 @@ cgtp_status build_v4(cgtp_plan_s* plan) {
   v.v4_fwd[1] = geo(false, true);
   v.v4_bwd[0] = geo(true, false);
   v.v4_bwd[1] = geo(true, true);
-  if (cudaHostAlloc(reinterpret_cast<void**>(&v.err_host), sizeof(int), cudaHostAllocMapped) != cudaSuccess)
+  if (cudaHostAlloc(reinterpret_cast<void**>(&v.err_host), kErrWords * sizeof(int), cudaHostAllocMapped) !=
+      cudaSuccess)
     return fail(CGTP_ENOMEM, "error word allocation failed");
-  *v.err_host = 0;
+  for (int i = 0; i < kErrWords; ++i) v.err_host[i] = 0;
   if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&v.err_dev), v.err_host, 0) != cudaSuccess) {
     cudaFreeHost(v.err_host);
     v.err_host = nullptr;

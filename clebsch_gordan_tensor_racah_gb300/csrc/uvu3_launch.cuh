@@ -8,6 +8,7 @@
 // them (CGTP_V3_INSTANCE), so the kernels compile in parallel.
 #pragma once
 #include <algorithm>
+#include <cstdio>
 #include <string>
 
 #include "uvu3_impl.cuh"
@@ -60,19 +61,19 @@ uvu4_detail::Uvu4Args<T, S> v4_args(const cgtp_plan_s* plan, const Uvu3Args<T, S
 
 template <typename K>
 bool v4_ready(K kernel, size_t smem) {
-  static int raised[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (!raised[dev]) {
-    if (raise_smem_limit(reinterpret_cast<const void*>(kernel)) < static_cast<int>(smem)) return false;
-    raised[dev] = 1;
-  }
-  return true;
+  return smem_cap_cached(reinterpret_cast<const void*>(kernel)) >= static_cast<int>(smem);
 }
 
 inline cgtp_status v4_sticky(const cgtp_plan_s* plan) {
-  if (plan->v3.err_host && *plan->v3.err_host)
-    return fail(CGTP_ECUDA, "a staging wait of an earlier call on this plan gave up (results of that call are invalid)");
+  const volatile int* e = plan->v3.err_host;
+  if (e && e[0]) {
+    char buf[256];
+    snprintf(buf, sizeof buf,
+             "a staging wait of an earlier call on this plan gave up (results of that call are invalid): "
+             "block %d warp %d stage %d of %d fetched, slot %d parity %d, barrier %08x%08x, stage (%d,%d,%d,%d)",
+             e[1] - 1, e[2], e[3], e[4], e[5], e[6], (unsigned)e[8], (unsigned)e[7], e[9], e[10], e[11], e[12]);
+    return fail(CGTP_ECUDA, buf);
+  }
   return CGTP_OK;
 }
 

@@ -246,13 +246,36 @@ __device__ __forceinline__ void cta_range(const int* rowptr, int N, int* s_range
 
 // Wait for the stage at the consumer position; on give-up record the error
 // (the stage's parity is left as it was, for the clean-up wait).
-__device__ __forceinline__ bool v4_wait(uint64_t* bars, RingPos& rp, int S, int* err, long long limit) {
+// The error word (host-mapped, 16 ints): [0] = 1 once a wait gave up; the first
+// warp to give up records where: [1] block, [2] warp, [3] stage consumed,
+// [4] stages fetched, [5] slot, [6] parity waited for, [7..8] the mbarrier's
+// state word, [9..12] the stage descriptor.
+__device__ __forceinline__ bool v4_wait(uint64_t* bars, RingPos& rp, int S, int* err, long long limit,
+                                        const int4* desc) {
   const int slot = rp.consumed % S;
   const bool ok = bulk::mbar_wait(&bars[slot], (rp.par >> slot) & 1u, limit);
   if (ok) {
     rp.par ^= 1u << slot;
   } else {
-    if ((threadIdx.x & 31) == 0) *reinterpret_cast<volatile int*>(err) = 1;
+    if ((threadIdx.x & 31) == 0) {
+      if (atomicCAS(err + 1, 0, blockIdx.x + 1) == 0) {
+        volatile int* e = err;
+        const unsigned long long st = *reinterpret_cast<volatile unsigned long long*>(&bars[slot]);
+        const int4 d = desc[slot];
+        e[2] = threadIdx.x >> 5;
+        e[3] = rp.consumed;
+        e[4] = rp.fetched;
+        e[5] = slot;
+        e[6] = (rp.par >> slot) & 1u;
+        e[7] = static_cast<int>(st & 0xffffffffu);
+        e[8] = static_cast<int>(st >> 32);
+        e[9] = d.x;
+        e[10] = d.y;
+        e[11] = d.z;
+        e[12] = d.w;
+      }
+      *reinterpret_cast<volatile int*>(err) = 1;
+    }
     rp.abort = 1;
   }
   return ok;
@@ -272,7 +295,11 @@ __device__ __forceinline__ void v4_drain(uint64_t* bars, const RingPos& rp, int 
     __syncwarp();                                                                                              \
     bulk::fence_proxy_async();                                                                                 \
     ++rp.consumed;                                                                                             \
-\
+    while (!rp.abort && rp.fetched < rp.consumed + R.S &&                                                      \
+           v4_fetch<BWD, T, S>(a.b.x, a.b.Y, a.b.W, a.b.gout, a.b.rowptr, a.b.col, a.b.t_dst, a.b.items,       \
+                               a.b.paths, a.b.d1, a.b.d2, a.b.d_out, a.b.w_numel, R, a.ublock, nb, nr, ni,    \
+                               item0, total, ctr, fs, ring, bars, desc, rp.fetched % R.S))                     \
+      ++rp.fetched;                                                                                            \
   } while (0)
 
 // ---------------------------------------------------------------------------
@@ -296,7 +323,7 @@ __device__ __forceinline__ void fwd4_unit(const Uvu4Args<T, S>& a, const Ring R,
   const int nst = max(1, (deg + R.SC - 1) / R.SC);
   const int ebase = SH ? __ldg(a.b.rowptr + n) : 0;  // CSR position of the receiver's first edge
   for (int st = 0; st < nst; ++st) {
-    if (!v4_wait(bars, rp, R.S, a.err, a.wait_limit)) return;
+    if (!v4_wait(bars, rp, R.S, a.err, a.wait_limit, desc)) return;
     const int slot = rp.consumed % R.S;
     const unsigned char* sb = ring + (size_t)slot * R.stage_bytes;
     const int4 d = desc[slot];
@@ -388,7 +415,7 @@ __global__ void __launch_bounds__(kV4Threads, 1) uvu_forward4_kernel(const Uvu4A
     const PathDev p = a.b.paths[item.path];
     switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
       CGTP3_TRIPLES(CGTP4_FWD_CASE)
-      default: break;
+      default: rp.abort = 1; break;  // no code for this triple (not reachable for a qualified plan)
     }
   }
   if (rp.abort) v4_drain(bars, rp, R.S);  // copies still in flight land before the CTA leaves
@@ -415,7 +442,7 @@ __device__ __noinline__ void bwd4_unit(const Uvu4Args<T, S>& a, const Ring R, Ri
   for (int m = 0; m < D1; ++m) gxa01[m] = gxa23[m] = P{T(0), T(0)};
   const int nst = max(1, (deg + R.SC - 1) / R.SC);
   // the sender's slice comes with the unit's first stage
-  if (!v4_wait(bars, rp, R.S, a.err, a.wait_limit)) return;
+  if (!v4_wait(bars, rp, R.S, a.err, a.wait_limit, desc)) return;
   {
     T xs[4 * D1];
     const unsigned char* sb0 = ring + (size_t)(rp.consumed % R.S) * R.stage_bytes;
@@ -432,7 +459,7 @@ __device__ __noinline__ void bwd4_unit(const Uvu4Args<T, S>& a, const Ring R, Ri
     }
   }
   for (int st = 0; st < nst; ++st) {
-    if (st > 0 && !v4_wait(bars, rp, R.S, a.err, a.wait_limit)) return;
+    if (st > 0 && !v4_wait(bars, rp, R.S, a.err, a.wait_limit, desc)) return;
     const int slot = rp.consumed % R.S;
     const unsigned char* sb = ring + (size_t)slot * R.stage_bytes;
     const int cnt = desc[slot].z;
@@ -596,7 +623,7 @@ __global__ void __launch_bounds__(kV4Threads, 1) uvu_backward4_kernel(const Uvu4
         const PathDev p = a.b.paths[item.path];
         switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
           CGTP3_TRIPLES(CGTP4_BWD_CASE)
-          default: break;
+          default: rp.abort = 1; break;  // no code for this triple (not reachable for a qualified plan)
         }
       }
       if (rp.abort) {  // let the copies still in flight land, then only take part in the barriers
