@@ -41,7 +41,8 @@ EXPORTS = ["cgtp_plan_create", "cgtp_plan_destroy", "cgtp_plan_info", "cgtp_plan
            "cgtp_mixed_plan_create", "cgtp_mixed_plan_destroy", "cgtp_mixed_plan_info",
            "cgtp_mixed_conv_workspace", "cgtp_mixed_conv_forward", "cgtp_mixed_conv_backward",
            "cgtp_mixed_conv_double_backward", "cgtp_measure_fma", "cgtp_measure_read",
-           "cgtp_plan_device_bytes", "cgtp_graph_device_bytes", "cgtp_plan_set_wait_limit"]
+           "cgtp_plan_device_bytes", "cgtp_graph_device_bytes", "cgtp_plan_set_wait_limit",
+           "cgtp_plan_set_node_chunk", "cgtp_plan_node_chunk"]
 
 
 class CgtpError(RuntimeError):
@@ -100,6 +101,8 @@ def lib():
         L.cgtp_mixed_conv_double_backward.argtypes = [vp] * 17 + [i64, vp]
         L.cgtp_plan_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
         L.cgtp_plan_set_wait_limit.argtypes = [vp, i64]
+        L.cgtp_plan_set_node_chunk.argtypes = [vp, i64]
+        L.cgtp_plan_node_chunk.argtypes = [vp, ctypes.POINTER(i64)]
         L.cgtp_graph_device_bytes.argtypes = [vp, ctypes.POINTER(i64)]
         L.cgtp_measure_fma.argtypes = [i32, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
         L.cgtp_measure_read.argtypes = [vp, i64, i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
@@ -206,12 +209,22 @@ class Plan:
         _check(lib().cgtp_plan_device_bytes(self._h, ctypes.byref(nb)))
         return nb.value
 
+    @property
+    def node_chunk(self):
+        """Nodes per streamed chunk of a radial uvw plan's node state (cgtp_plan_node_chunk)."""
+        nb = ctypes.c_int64()
+        _check(lib().cgtp_plan_node_chunk(self._h, ctypes.byref(nb)))
+        return nb.value
+
+    def set_node_chunk(self, nodes):
+        """cgtp_plan_set_node_chunk: stream the node state `nodes` nodes at a time."""
+        _check(lib().cgtp_plan_set_node_chunk(self._h, int(nodes)))
+
     def launches_per_step(self, n_nodes):
         """Kernel launches of one forward + backward of a radial uvw plan on n_nodes nodes:
         per streamed node chunk of the plan, the forward's edge stage and node GEMM and
         the backward's GEMM, edge stage, two GEMMs and split-K reduction."""
-        chunk = 4096
-        return 7 * max(1, -(-int(n_nodes) // chunk))
+        return 7 * max(1, -(-int(n_nodes) // max(1, self.node_chunk)))
 
     def path(self, p):
         ints = (ctypes.c_int * 10)()

@@ -265,7 +265,22 @@ cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls) {
   clear_error();
   if (!plan) return fail(CGTP_EINVAL, "null plan");
   if (polls < 0) return fail(CGTP_EINVAL, "polls must be >= 0");
-  plan->v3.wait_limit = polls;
+  plan->wait_limit = polls;
+  return CGTP_OK;
+}
+
+cgtp_status cgtp_plan_set_node_chunk(cgtp_plan plan, int64_t nodes) {
+  clear_error();
+  if (!plan) return fail(CGTP_EINVAL, "null plan");
+  if (!plan->uvw) return fail(CGTP_EINVAL, "node chunks belong to uvw plans with radial weights");
+  if (nodes < 1 || nodes > (int64_t(1) << 20)) return fail(CGTP_EINVAL, "nodes must be in [1, 1048576]");
+  return uvw_set_chunk(plan, static_cast<int>(nodes));
+}
+
+cgtp_status cgtp_plan_node_chunk(cgtp_plan plan, int64_t* nodes) {
+  clear_error();
+  if (!plan || !nodes) return fail(CGTP_EINVAL, "null plan or nodes");
+  *nodes = plan->uvw ? uvw_chunk(plan) : 0;
   return CGTP_OK;
 }
 

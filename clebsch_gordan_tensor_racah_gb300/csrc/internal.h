@@ -106,23 +106,6 @@ struct LayoutDev {
   std::vector<GroupDev> groups_host;
 };
 
-// Polls of an mbarrier before a bounded wait gives up (the staged uvu kernels).
-constexpr long long kDefaultWaitPolls = 1ll << 22;
-// ints of the staged kernels' host-mapped error word (flag + where a wait gave up)
-constexpr int kErrWords = 16;
-
-// Staging geometry of the v4 uvu kernels (uvu4_impl.cuh): each warp owns a
-// ring of S stages of SC edges in shared memory.
-struct V4Ring {
-  int S = 0;            // stages per warp (0: the plan does not use the staged kernels)
-  int SC = 0;           // edges per stage
-  int a_elems = 0;      // per-edge gathered slice capacity (elements)
-  int y_elems = 0;      // harmonics row (d2; 0 when evaluated from edge vectors)
-  int x_elems = 0;      // backward: the sender's slice (first stage of a unit)
-  int stage_bytes = 0;  // one stage, a multiple of 16
-  int warp_bytes = 0;   // S stages, then S descriptors (int4), then S mbarriers
-};
-
 // Tables of the warp-autonomous uvu kernels (uvu3_impl.cuh); lpe == 0 when the
 // plan does not qualify (it needs l <= 3 and one multiplicity m for all in1
 // blocks with m / 4 in {2, 8, 32} or m a multiple of 128).
@@ -144,11 +127,6 @@ struct V3Dev {
   int chunk_b = 0;
   size_t smem_bwd = 0;
   void* base = nullptr;
-  // staged (v4) kernels: geometry per direction, harmonics given (0) or from edge vectors (1)
-  V4Ring v4_fwd[2], v4_bwd[2];
-  int* err_host = nullptr;    // host-mapped error word of the staged kernels (sticky)
-  int* err_dev = nullptr;     // its device address
-  long long wait_limit = 0;   // polls before a staging wait gives up
 };
 
 struct PathHost {
@@ -178,6 +156,8 @@ struct cgtp_plan_s {
   void* uvwe = nullptr;
   // device memory the plan owns (tables, work counters, scratch), for cgtp_plan_device_bytes
   size_t device_bytes = 0;
+  // polls of an mbarrier before a bounded wait of the plan's kernels gives up
+  long long wait_limit = 1ll << 22;
 };
 
 struct cgtp_graph_s {
@@ -255,6 +235,9 @@ cgtp_status graph_build(cgtp_graph_s* g, void* stream);
 
 // uvw.cu
 cgtp_status uvw_create(cgtp_plan_s* plan);
+// nodes per streamed chunk of the radial plan's node state (reallocates the scratch)
+cgtp_status uvw_set_chunk(cgtp_plan_s* plan, int nodes);
+int uvw_chunk(const cgtp_plan_s* plan);
 void uvw_destroy(cgtp_plan_s* plan);
 // rvec non-null: Y and R are evaluated from the edge vectors (harmonics of the
 // direction, Gaussian radial basis of the length with centres lo..hi)

@@ -33,8 +33,6 @@ bool v3_pick(int lpe, F&& f) {
 }
 }  // namespace uvu3_detail
 
-cgtp_status build_v4(cgtp_plan_s* plan);
-
 cgtp_status build_v3(cgtp_plan_s* plan) {
   plan->v3 = V3Dev{};
   if (plan->mode != CGTP_UVU || plan->paths.empty()) return CGTP_OK;
@@ -149,83 +147,11 @@ cgtp_status build_v3(cgtp_plan_s* plan) {
   while (v.chunk_b > 8 && smem(v.chunk_b) > 200 * 1024) v.chunk_b /= 2;
   v.smem_bwd = smem(v.chunk_b);
   if (v.smem_bwd > 220 * 1024) v.lpe = 0;  // gx partials too large: the general kernels serve this plan
-  if (v.lpe) {
-    const cgtp_status s4 = build_v4(plan);
-    if (s4 != CGTP_OK) return s4;
-  }
-  return CGTP_OK;
-}
-
-// Staging geometry of the v4 kernels (uvu4_impl.cuh).  Every copy is a whole
-// number of 16-byte units at 16-byte aligned addresses: the items' channel
-// blocks, the weight slices and the harmonics rows must satisfy that, or the
-// plan keeps the v3 kernels.  Among the (stages, edges per stage) choices that
-// fit 8 rings in the shared-memory budget, take the one with the most edges in
-// flight ahead of the stage being computed ((S - 1) * SC), then the larger SC.
-cgtp_status build_v4(cgtp_plan_s* plan) {
-  V3Dev& v = plan->v3;
-  const int es = plan->dtype == CGTP_F64 ? 8 : plan->dtype == CGTP_BF16 ? 2 : 4;
-  const int ublock = 4 * v.lpe;
-  int d1max = 1, d3max = 1;
-  bool aligned = (ublock * es) % 16 == 0 && (plan->w_numel * es) % 16 == 0 && (plan->d1 * es) % 16 == 0 &&
-                 (plan->d_out * es) % 16 == 0;
-  for (const auto& q : plan->paths) {
-    d1max = std::max(d1max, 2 * q.l1 + 1);
-    d3max = std::max(d3max, 2 * q.l3 + 1);
-    aligned = aligned && (q.off1 * es) % 16 == 0 && (q.ooff * es) % 16 == 0 && (q.woff * es) % 16 == 0;
-  }
-  if (!aligned) return CGTP_OK;
-  constexpr int kWarps4 = 8;
-  constexpr int kBudget = 220 * 1024;
-  const int epw = 32 / v.lpe;
-  auto geo = [&](bool bwd, bool sh) {
-    V4Ring best{};
-    const int y = sh ? 0 : int(plan->d2);
-    if (!sh && (y * es) % 16 != 0) return best;  // harmonics rows not copyable: keep v3
-    const int a = ublock * (bwd ? d3max : d1max);
-    const int xel = bwd ? ublock * d1max : 0;
-    for (int S = 2; S <= 4; ++S) {
-      for (int SC = std::min(32, 4 * epw); SC >= std::min(epw, 32) && SC >= 1; SC /= 2) {
-        V4Ring r;
-        r.S = S;
-        r.SC = SC;
-        r.a_elems = a;
-        r.y_elems = y;
-        r.x_elems = xel;
-        int sb = SC * (a + ublock + y) * es;
-        sb = (sb + 15) & ~15;
-        if (bwd) sb += ((SC * 4 + 15) & ~15) + xel * es;
-        r.stage_bytes = (sb + 15) & ~15;
-        r.warp_bytes = S * r.stage_bytes + S * 8 + S * 16;
-        r.warp_bytes = (r.warp_bytes + 127) & ~127;
-        if (kWarps4 * r.warp_bytes > kBudget) continue;
-        const int ahead = (S - 1) * SC, best_ahead = best.S ? (best.S - 1) * best.SC : -1;
-        if (ahead > best_ahead || (ahead == best_ahead && SC > best.SC)) best = r;
-        break;  // the largest SC that fits for this S
-      }
-    }
-    return best;
-  };
-  v.v4_fwd[0] = geo(false, false);
-  v.v4_fwd[1] = geo(false, true);
-  v.v4_bwd[0] = geo(true, false);
-  v.v4_bwd[1] = geo(true, true);
-  if (cudaHostAlloc(reinterpret_cast<void**>(&v.err_host), kErrWords * sizeof(int), cudaHostAllocMapped) !=
-      cudaSuccess)
-    return fail(CGTP_ENOMEM, "error word allocation failed");
-  for (int i = 0; i < kErrWords; ++i) v.err_host[i] = 0;
-  if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&v.err_dev), v.err_host, 0) != cudaSuccess) {
-    cudaFreeHost(v.err_host);
-    v.err_host = nullptr;
-    return fail(CGTP_ECUDA, "error word mapping failed");
-  }
-  v.wait_limit = kDefaultWaitPolls;
   return CGTP_OK;
 }
 
 void free_v3(cgtp_plan_s* plan) {
   if (plan->v3.base) cudaFree(plan->v3.base);
-  if (plan->v3.err_host) cudaFreeHost(plan->v3.err_host);
   plan->v3 = V3Dev{};
 }
 

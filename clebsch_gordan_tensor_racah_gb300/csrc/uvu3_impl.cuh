@@ -63,6 +63,13 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 }
 __device__ __forceinline__ double2 mul2(double2 a, double2 b) { return make_double2(a.x * b.x, a.y * b.y); }
 
+// Accumulation into gY / gx without reading back: each element receives at most
+// one contribution per backward phase and phases are separated by block
+// barriers, so the order of the additions is fixed (deterministic), and the
+// warp does not wait for a read of the old value.
+__device__ __forceinline__ void red_add3(float* p, float v) { atomicAdd(p, v); }
+__device__ __forceinline__ void red_add3(double* p, double v) { atomicAdd(p, v); }
+
 template <typename T>
 __device__ __forceinline__ T shfl_x(T v, int o) {
   return __shfl_xor_sync(0xffffffffu, v, o);
@@ -130,6 +137,7 @@ struct Uvu3Args {
   const int* gx_begin;    // n_in1 + 1 offsets into gx_paths
   const int* gx_paths;
   int chunk_b;            // edges of a sender processed per round (bounded by shared memory)
+  int idx_cap;            // ints of dynamic shared memory for the CTA's edge indices
 };
 
 template <typename T, int N>
@@ -276,7 +284,7 @@ __device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restr
       const int ja = j, jb = j + EPW;
       const bool okb = jb < deg;
       const int ea = e_begin + ja, eb = e_begin + (okb ? jb : ja);
-      const int sa = __ldg(col + ea), sb = __ldg(col + eb);
+      const int sa = col[ea], sb = col[eb];  // staged in shared memory (or global)
       FwdEdge<T, D1, D2, D3> A, B;
       fwd3_load<T, LPE, L1, L2, L3, SH>(A, x, Y, W, ea, sa, true, d1, d2, w_numel, off1, off2, woff, u);
       fwd3_load<T, LPE, L1, L2, L3, SH>(B, x, Y, W, eb, sb, okb, d1, d2, w_numel, off1, off2, woff, u);
@@ -315,12 +323,22 @@ __device__ __noinline__ void fwd3_item(const S* __restrict__ x, const S* __restr
 #define CGTP3_FWD_CASE(L1, L2, L3)                                                                  \
   case (L1)*16 + (L2)*4 + (L3):                                                                     \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      fwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.out, a.col, e_begin, deg, n, a.d1, a.d2, a.d_out, \
+      fwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.out, colp, e_begin, deg, n, a.d1, a.d2, a.d_out,  \
                                     a.w_numel, p.off1, p.off2, p.ooff, p.woff, u, active, g);      \
     break;
 
+// Edge indices of the CTA's rows are read once into shared memory (when they
+// fit `cap` ints), so the gathers of an edge never wait for an index load from
+// global memory.  Returns the pointer to index with CSR positions.
+__device__ __forceinline__ const int* stage_idx(const int* __restrict__ src, int p0, int p1, int* s_buf, int cap) {
+  if (p1 - p0 > cap) return src;
+  for (int i = threadIdx.x; i < p1 - p0; i += blockDim.x) s_buf[i] = __ldg(src + p0 + i);
+  return s_buf - p0;
+}
+
 template <typename T, int LPE, typename S = T, bool SH = false>
 __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3Args<T, S> a) {
+  extern __shared__ int v3_idx[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   const S* Yp = SH ? reinterpret_cast<const S*>(a.rvec) : a.Y;   // edge vectors or harmonics
@@ -341,6 +359,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
   }
   __syncthreads();
   const int nb = s_range[0], nr = s_range[1] - s_range[0];
+  const int* colp = stage_idx(a.col, a.rowptr[nb], a.rowptr[s_range[1]], v3_idx, a.idx_cap);
   // One counter sweeps the (item, receiver) pairs item-major: the warps stay on
   // (nearly) the same path -- one hot instruction stream -- and never wait for
   // each other.  Each receiver's slice of a path is written by one warp.
@@ -411,8 +430,8 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
     int e = 0;
     T yv[D2], gs[4 * D3], wv[4];
     if (valid) {
-      e = __ldg(t_eid + te_begin + j);
-      const int d = __ldg(t_dst + te_begin + j);
+      e = t_eid[te_begin + j];  // staged in shared memory (or global)
+      const int d = t_dst[te_begin + j];
       edge_y<L2, T, SH>(Y, e, d2, off2, yv);
       ldvec<T, 4>(W + (size_t)e * w_numel + woff + u, wv);
       ldvec<T, 4 * D3>(gout + (size_t)d * d_out + ooff + u * D3, gs);
@@ -476,7 +495,7 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
 #pragma unroll
       for (int k = 0; k < HV / LPE; ++k) {
         const int slot = q * (HV / LPE) + k;
-        if (slot < D2) gY[(size_t)e * d2 + off2 + slot] += h[k];
+        if (slot < D2) red_add3(gY + (size_t)e * d2 + off2 + slot, h[k]);
       }
     }
   }
@@ -497,7 +516,7 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
     if (active && g == 0) {
       T* dst = gx + (size_t)s * d1 + off1 + u * D1;
 #pragma unroll
-      for (int i = 0; i < 4 * D1; ++i) dst[i] += v[i];
+      for (int i = 0; i < 4 * D1; ++i) red_add3(dst + i, v[i]);
     }
   }
 }
@@ -505,13 +524,14 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
 #define CGTP3_BWD_CASE(L1, L2, L3)                                                                   \
   case (L1)*16 + (L2)*4 + (L3):                                                                      \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      bwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.gout, a.gW, a.col, a.t_dst, te0, cnt, s, a.d1,  \
+      bwd3_item<T, LPE, L1, L2, L3, SH>(a.x, Yp, a.W, a.gout, a.gW, eidp, dstp, te0, cnt, s, a.d1,        \
                                     a.d2, a.d_out, a.w_numel, p.off1, p.off2, p.ooff, p.woff, u,     \
                                     active, g, q, a.gY, a.gx);                                       \
     break;
 
 template <typename T, int LPE, typename S = T, bool SH = false>
 __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3Args<T, S> a) {
+  extern __shared__ int v3_idx[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane % LPE, g = lane / LPE;
   const S* Yp = SH ? reinterpret_cast<const S*>(a.rvec) : a.Y;   // edge vectors or harmonics
@@ -532,6 +552,11 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
   }
   __syncthreads();
   const int sb = s_range[0], se = s_range[1], nr = se - sb;
+  // the CTA's transpose slice (edge ids, receivers) in shared memory when it fits
+  const int tp0 = a.rowptr[sb], tp1 = a.rowptr[se];
+  const bool staged = tp1 - tp0 <= a.idx_cap / 2;
+  const int* eidp = staged ? stage_idx(a.col, tp0, tp1, v3_idx, a.idx_cap / 2) : a.col;
+  const int* dstp = staged ? stage_idx(a.t_dst, tp0, tp1, v3_idx + a.idx_cap / 2, a.idx_cap / 2) : a.t_dst;
   // clear gx and gY of the CTA's senders (and their out-edges) before the first path
   for (int s = sb + warp; s < se; s += kV3Warps) {
     for (int i = lane; i < a.d1; i += 32) a.gx[(size_t)s * a.d1 + i] = T(0);

@@ -1,6 +1,5 @@
 // uvu3_launch.cuh -- host launch glue of the warp-autonomous uvu kernels
-// (uvu3_impl.cuh, and their staged form uvu4_impl.cuh when the plan's copies
-// are 16-byte aligned), written once for every instance.
+// (uvu3_impl.cuh), written once for every instance.
 //
 // An instance is (T, S, SH, LPE): arithmetic/output type, storage type of the
 // inputs (T or bfloat16), edge vectors instead of harmonics, lanes per edge.
@@ -8,11 +7,9 @@
 // them (CGTP_V3_INSTANCE), so the kernels compile in parallel.
 #pragma once
 #include <algorithm>
-#include <cstdio>
 #include <string>
 
 #include "uvu3_impl.cuh"
-#include "uvu4_impl.cuh"
 
 namespace cgtp {
 namespace uvu3_detail {
@@ -31,10 +28,15 @@ Uvu3Args<T, S> v3_args(const cgtp_plan_s* plan) {
   return a;
 }
 
+// shared memory for a CTA's edge indices: 16,384 ints (64 KB) in the backward
+// (edge ids + receivers), half of it in the forward (sources)
+constexpr int kV3IdxInts = 16384;
+
 // persistent grid: every SM holds as many CTAs as fit, never more CTAs than nodes
 inline int v3_grid(const void* kernel, int64_t N, int num_sms) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kV3Threads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kV3Threads, kV3IdxInts * sizeof(int)) !=
+      cudaSuccess) {
     cudaGetLastError();
     per_sm = 1;
   }
@@ -44,37 +46,6 @@ inline int v3_grid(const void* kernel, int64_t N, int num_sms) {
 
 inline const char* v3_variant_name(bool bf16, bool sh) {
   return sh ? " (edge vectors)" : bf16 ? " (bf16)" : "";
-}
-
-// Staged (v4) launch: dynamic shared memory = 8 rings; the kernel's limit is
-// raised to the device cap once per device.
-template <typename T, typename S>
-uvu4_detail::Uvu4Args<T, S> v4_args(const cgtp_plan_s* plan, const Uvu3Args<T, S>& b, const V4Ring& r) {
-  uvu4_detail::Uvu4Args<T, S> a{};
-  a.b = b;
-  a.r = r;
-  a.ublock = 4 * plan->v3.lpe;
-  a.err = plan->v3.err_dev;
-  a.wait_limit = plan->v3.wait_limit;
-  return a;
-}
-
-template <typename K>
-bool v4_ready(K kernel, size_t smem) {
-  return smem_cap_cached(reinterpret_cast<const void*>(kernel)) >= static_cast<int>(smem);
-}
-
-inline cgtp_status v4_sticky(const cgtp_plan_s* plan) {
-  const volatile int* e = plan->v3.err_host;
-  if (e && e[0]) {
-    char buf[256];
-    snprintf(buf, sizeof buf,
-             "a staging wait of an earlier call on this plan gave up (results of that call are invalid): "
-             "block %d warp %d stage %d of %d fetched, slot %d parity %d, barrier %08x%08x, stage (%d,%d,%d,%d)",
-             e[1] - 1, e[2], e[3], e[4], e[5], e[6], (unsigned)e[8], (unsigned)e[7], e[9], e[10], e[11], e[12]);
-    return fail(CGTP_ECUDA, buf);
-  }
-  return CGTP_OK;
 }
 
 // forward: E_in is Y [E, d2] (SH = false) or the edge vectors [E, 3] (SH = true)
@@ -90,23 +61,9 @@ cgtp_status v3_forward(const cgtp_plan_s* plan, const void* x, const void* E_in,
   a.rowptr = rowptr;
   a.col = col;
   a.N = static_cast<int>(N);
-  const V4Ring& r4 = plan->v3.v4_fwd[SH ? 1 : 0];
-  if (r4.S > 0) {
-    if (cgtp_status e = v4_sticky(plan)) return e;
-    auto k4 = uvu4_detail::uvu_forward4_kernel<T, LPE, S, SH>;
-    const size_t smem = size_t(uvu4_detail::kV4Warps) * r4.warp_bytes;
-    if (v4_ready(k4, smem)) {
-      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, plan->num_sms)));
-      k4<<<grid, uvu4_detail::kV4Threads, smem, st>>>(v4_args(plan, a, r4));
-      const cudaError_t err = cudaGetLastError();
-      if (err != cudaSuccess)
-        return fail(CGTP_ECUDA, std::string("uvu forward (v4") + v3_variant_name(sizeof(S) == 2, SH) +
-                                    ") launch: " + cudaGetErrorString(err));
-      return CGTP_OK;
-    }
-  }
   auto k = uvu_forward3_kernel<T, LPE, S, SH>;
-  k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, 0, st>>>(a);
+  a.idx_cap = kV3IdxInts / 2;  // the forward stages col only
+  k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, a.idx_cap * sizeof(int), st>>>(a);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess)
     return fail(CGTP_ECUDA, std::string("uvu forward (v3") + v3_variant_name(sizeof(S) == 2, SH) +
@@ -134,23 +91,9 @@ cgtp_status v3_backward(const cgtp_plan_s* plan, const void* gout, const void* x
   a.phase_begin = plan->v3.phase_begin;
   a.n_phases = plan->v3.n_phases;
   a.N = static_cast<int>(N);
-  const V4Ring& r4 = plan->v3.v4_bwd[SH ? 1 : 0];
-  if (r4.S > 0) {
-    if (cgtp_status e = v4_sticky(plan)) return e;
-    auto k4 = uvu4_detail::uvu_backward4_kernel<T, LPE, S, SH>;
-    const size_t smem = size_t(uvu4_detail::kV4Warps) * r4.warp_bytes;
-    if (v4_ready(k4, smem)) {
-      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(N, plan->num_sms)));
-      k4<<<grid, uvu4_detail::kV4Threads, smem, st>>>(v4_args(plan, a, r4));
-      const cudaError_t err = cudaGetLastError();
-      if (err != cudaSuccess)
-        return fail(CGTP_ECUDA, std::string("uvu backward (v4") + v3_variant_name(sizeof(S) == 2, SH) +
-                                    ") launch: " + cudaGetErrorString(err));
-      return CGTP_OK;
-    }
-  }
   auto k = uvu_backward3_kernel<T, LPE, S, SH>;
-  k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, 0, st>>>(a);
+  a.idx_cap = smem_cap_cached(reinterpret_cast<const void*>(k)) >= int(kV3IdxInts * sizeof(int)) ? kV3IdxInts : 0;
+  k<<<v3_grid(reinterpret_cast<const void*>(k), N, plan->num_sms), kV3Threads, a.idx_cap * sizeof(int), st>>>(a);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess)
     return fail(CGTP_ECUDA, std::string("uvu backward (v3") + v3_variant_name(sizeof(S) == 2, SH) +

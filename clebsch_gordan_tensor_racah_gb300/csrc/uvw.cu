@@ -43,7 +43,7 @@ using uvu_detail::pad_up;
 using uvu_detail::reduce_outer;
 using uvu_detail::V16;
 
-constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (CGTP_UVW_CHUNK_NODES overrides)
+constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (cgtp_plan_set_node_chunk)
 constexpr int kEdgeChunk = 16;      // edges staged per step of the edge stages
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
 constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over nodes
@@ -115,7 +115,8 @@ struct UvwState {
 // ---------------------------------------------------------------------------
 constexpr int kTM = 128, kTN = 64, kTK = 32;
 constexpr int kATile = kTM * kTK * 4, kBTile = kTN * kTK * 4;
-constexpr int kTcSmem = 2 * kATile + 2 * kBTile + 1024 + 64;
+constexpr int kTcSmem = 2 * (2 * kATile + 2 * kBTile) + 1024 + 64;  // two stages
+constexpr long long kTcCleanupPolls = 1ll << 24;                     // bounded clean-up wait
 
 struct GemmLaunch {
   const float* ptr[6];
@@ -128,6 +129,7 @@ struct GemmLaunch {
   int splits;
   long long c_split_stride;
   int* err;  // set when a tensor-core wait gives up
+  long long wait_limit;  // polls before a tensor-core wait gives up
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -152,15 +154,27 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem, uint64_t a, uint64_t b, 
                ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// bounded wait on an mbarrier phase (false: gave up)
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, long long limit) {
+  for (long long it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Two shared-memory stages: while the tensor core runs the MMAs of K step i
+// (stage i % 2, committed to that stage's mbarrier), the threads load and split
+// step i + 1 into the other stage; a stage is overwritten only after the commit
+// of the MMAs that read it (step i - 1) has arrived.
 __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunch L) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char* a_hi = sm;
-  unsigned char* a_lo = sm + kATile;
-  unsigned char* b_hi = sm + 2 * kATile;
-  unsigned char* b_lo = sm + 2 * kATile + kBTile;
-  uint64_t* mbar = (uint64_t*)(sm + 2 * kATile + 2 * kBTile);
-  uint32_t* tmem_holder = (uint32_t*)(sm + 2 * kATile + 2 * kBTile + 16);
+  constexpr int kStage = 2 * kATile + 2 * kBTile;
+  uint64_t* mbar = (uint64_t*)(sm + 2 * kStage);         // one per stage
+  uint32_t* tmem_holder = (uint32_t*)(sm + 2 * kStage + 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // locate this CTA's problem and tile (uniform over the CTA)
   int tile = blockIdx.x, pi = 0, rt = 0, ct = 0;
@@ -186,7 +200,8 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
   if (L.splits > 1) C += split * L.c_split_stride;
   const int r0 = rt * kTM, c0 = ct * kTN;
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) {
@@ -206,10 +221,12 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
     const int n = r < rows ? r / P.D : 0, m = r < rows ? r - n * P.D : 0;
     aoff[t] = r < rows ? (int)(n * P.a_n + m * P.a_m) : -1;
   }
-  uint32_t phase = 0;
-  bool first = true;
-  for (int s = P.seg0; s < P.seg1; ++s) {
-    const GemmSeg S = L.segs[s];
+  uint32_t phase = 0;   // bit s: parity of stage s's next commit
+  uint32_t pend = 0;    // bit s: stage s has a commit not yet waited for
+  int issued = 0;       // K steps whose MMAs were committed
+  bool first = true, ok = true;
+  for (int sgi = P.seg0; sgi < P.seg1 && ok; ++sgi) {
+    const GemmSeg S = L.segs[sgi];
     int kb = 0, ke = S.K < 0 ? L.nodes : S.K;
     if (S.K < 0 && L.splits > 1) {
       kb = min(L.nodes, split * slice);
@@ -220,21 +237,44 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
     for (int k0 = kb; k0 < ke; k0 += kTK) {
       const int k = k0 + lane;
       const bool kin = k < ke;
+      // global loads of this step (in flight while the previous step's MMAs run)
+      float av[kTM / 4], bv[kTN / 4];
+#pragma unroll
+      for (int t = 0; t < kTM / 4; ++t)
+        av[t] = (kin && aoff[t] >= 0) ? __ldg(Ab + aoff[t] + (long long)k * S.a_k) : 0.f;
+#pragma unroll
+      for (int t = 0; t < kTN / 4; ++t) {
+        const int c = c0 + warp + 4 * t;
+        bv[t] = (kin && c < P.J) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
+      }
+      const int st = issued & 1;
+      unsigned char* a_hi = sm + st * kStage;
+      unsigned char* a_lo = a_hi + kATile;
+      unsigned char* b_hi = a_hi + 2 * kATile;
+      unsigned char* b_lo = b_hi + kBTile;
+      if (issued >= 2) {  // the MMAs of step issued - 2 read this stage
+        const bool done = tc_wait(&mbar[st], (phase >> st) & 1u, L.wait_limit);
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        if (__syncthreads_or(!done)) {
+          ok = false;
+          break;
+        }
+        phase ^= 1u << st;
+        pend &= ~(1u << st);
+      }
 #pragma unroll
       for (int t = 0; t < kTM / 4; ++t) {
         const int rr = warp + 4 * t;
-        const float v = (kin && aoff[t] >= 0) ? __ldg(Ab + aoff[t] + (long long)k * S.a_k) : 0.f;
-        const float hi = tf32_round(v);
+        const float hi = tf32_round(av[t]);
         *(float*)(a_hi + sw128(rr, lane)) = hi;
-        *(float*)(a_lo + sw128(rr, lane)) = tf32_round(v - hi);
+        *(float*)(a_lo + sw128(rr, lane)) = tf32_round(av[t] - hi);
       }
 #pragma unroll
       for (int t = 0; t < kTN / 4; ++t) {
-        const int jj = warp + 4 * t, c = c0 + jj;
-        const float v = (kin && c < P.J) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
-        const float hi = tf32_round(v);
+        const int jj = warp + 4 * t;
+        const float hi = tf32_round(bv[t]);
         *(float*)(b_hi + sw128(jj, lane)) = hi;
-        *(float*)(b_lo + sw128(jj, lane)) = tf32_round(v - hi);
+        *(float*)(b_lo + sw128(jj, lane)) = tf32_round(bv[t] - hi);
       }
       asm volatile("fence.proxy.async.shared::cta;");
       __syncthreads();
@@ -249,29 +289,35 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
           mma_tf32(tmem, sdesc(al + off), sdesc(bh + off), idesc, 1u);
           first = false;
         }
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar)));
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(&mbar[st])));
       }
       first = false;
-      uint32_t done = 0;
-      for (int it = 0; it < (1 << 22) && !done; ++it)
-        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-                     : "=r"(done) : "r"(smem_u32(mbar)), "r"(phase));
-      phase ^= 1;
-      asm volatile("tcgen05.fence::after_thread_sync;");
-      if (__syncthreads_or(!done)) {  // the tensor core did not signal in time: record, clean up, return
-        if (tid == 0) atomicOr(L.err, 1);
-        for (int it = 0; it < (1 << 22); ++it) {  // one more bounded wait for the work in flight
-          uint32_t d2 = 0;
-          asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-                       : "=r"(d2) : "r"(smem_u32(mbar)), "r"(phase ^ 1));
-          if (d2) break;
-        }
-        asm volatile("tcgen05.fence::before_thread_sync;");
-        __syncthreads();
-        if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
-        return;
-      }
+      pend |= 1u << st;
+      ++issued;
     }
+  }
+  // the last commits (at most two outstanding, one per stage) before TMEM is read
+  if (ok) {
+    for (int s = issued >= 2 ? issued - 2 : 0; s < issued; ++s) {
+      const int st = s & 1;
+      const bool done = tc_wait(&mbar[st], (phase >> st) & 1u, L.wait_limit);
+      if (__syncthreads_or(!done)) {
+        ok = false;
+        break;
+      }
+      phase ^= 1u << st;
+      pend &= ~(1u << st);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;");
+  }
+  if (!ok) {  // a tensor-core wait gave up: record, let the MMAs in flight finish (bounded), clean up
+    if (tid == 0) atomicOr(L.err, 1);
+    for (int st = 0; st < 2; ++st)
+      if ((pend >> st) & 1u) tc_wait(&mbar[st], (phase >> st) & 1u, kTcCleanupPolls);
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
+    return;
   }
   // epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w+31
   const int r = r0 + 32 * warp + lane;
@@ -540,6 +586,7 @@ struct Bwd3Args {
   const UvwPath* paths;
   const Item* items;    // (path, w0), path order
   int n_items;
+  int idx_cap;          // ints of dynamic shared memory for the CTA's transpose slice
 };
 
 template <int L1, int L2, int L3, bool SH>
@@ -563,7 +610,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
       H[k][m] = 0.f;
     }
   for (int t = tb; t < te; ++t) {
-    const int e = __ldg(t_eid + t), d = __ldg(t_dst + t);
+    const int e = t_eid[t], d = t_dst[t];  // staged in shared memory (or global)
     float yv[D2], r[kKB], gv[D3];
     if constexpr (SH) {  // Yp holds the edge vectors: harmonics and radial basis evaluated here
       const float rx = __ldg(Yp + 3 * (size_t)e), ry = __ldg(Yp + 3 * (size_t)e + 1), rz = __ldg(Yp + 3 * (size_t)e + 2);
@@ -605,9 +652,11 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
     const float grt = reduce8(gr, lane);   // lane holds the total of index (lane >> 2) & 7
     const float ht = reduce8(h, lane);
     const int idx = (lane >> 2) & 7;
+    // one contribution per (edge, item); items are separated by block barriers, so
+    // every element's additions come in item order (deterministic) and nothing is read back
     if ((lane & 3) == 0) {
-      if (idx < K) gR[(size_t)e * K + idx] += grt;
-      if (idx < D2) gY[(size_t)e * d2 + off2 + idx] += ht;
+      if (idx < K) atomicAdd(gR + (size_t)e * K + idx, grt);
+      if (idx < D2) atomicAdd(gY + (size_t)e * d2 + off2 + idx, ht);
     }
   }
   if (active) {
@@ -623,15 +672,18 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
 #define UVW3_BWD_CASE(L1, L2, L3)                                                                  \
   case (L1)*16 + (L2)*4 + (L3):                                                                    \
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
-      uvw_bwd3_unit<L1, L2, L3, SH>(a.Y, a.R, a.rbf, a.g, a.Astate, a.Hstate, a.gY, a.gR, a.t_eid, a.t_dst,     \
+      uvw_bwd3_unit<L1, L2, L3, SH>(a.Y, a.R, a.rbf, a.g, a.Astate, a.Hstate, a.gY, a.gR, eidp, dstp,           \
                                 rp[s], rp[s + 1], (size_t)(s - a.n0) * a.s_node, a.d2, a.d_out, a.K,  \
                                 a.s_slice, p.off2, p.ooff, p.aoff, p.mul_out, item.u0, lane);        \
     break;
 
 constexpr int kBwd3Warps = 16;
 
+constexpr int kBwd3IdxInts = 16384;  // shared memory for the CTA's transpose slice (ids + receivers)
+
 template <bool SH>
 __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const Bwd3Args a) {
+  extern __shared__ int bwd3_idx[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int s_range[2];
   const int* rp = a.t_rowptr;
@@ -651,6 +703,19 @@ __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const
   }
   __syncthreads();
   const int sb = s_range[0], se = s_range[1];
+  // the CTA's transpose slice in shared memory when it fits: no index load from
+  // global memory in front of an edge's gathers
+  const int tp0 = rp[sb], tp1 = rp[se];
+  const int* eidp = a.t_eid;
+  const int* dstp = a.t_dst;
+  if (tp1 - tp0 <= a.idx_cap / 2) {
+    for (int i = tid; i < tp1 - tp0; i += kBwd3Warps * 32) {
+      bwd3_idx[i] = __ldg(a.t_eid + tp0 + i);
+      bwd3_idx[a.idx_cap / 2 + i] = __ldg(a.t_dst + tp0 + i);
+    }
+    eidp = bwd3_idx - tp0;
+    dstp = bwd3_idx + a.idx_cap / 2 - tp0;
+  }
   // clear gY and gR of the CTA's senders' out-edges before the first path
   for (int s = sb + warp; s < se; s += kBwd3Warps)
     for (int t = rp[s]; t < rp[s + 1]; ++t) {
@@ -871,10 +936,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->bwd3_items = reinterpret_cast<Item*>(at(o_b3));
   st->bwd3_n_items = int(b3.size());
   // node-state scratch: two chunks of state (forward S; backward A and H)
-  if (const char* env = std::getenv("CGTP_UVW_CHUNK_NODES")) {
-    const long v = std::strtol(env, nullptr, 10);
-    if (v >= 1 && v <= (1 << 20)) st->chunk_nodes = static_cast<int>(v);
-  }
   st->scratch_elems = size_t(2) * st->chunk_nodes * st->s_node;
   if (cudaMalloc(&st->scratch, st->scratch_elems * sizeof(float)) != cudaSuccess)
     return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
@@ -939,7 +1000,7 @@ EdgeArgs edge_args(const cgtp_plan_s* plan, const UvwState* st, int group) {
 
 cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
                         const float* const ptr[6], int nodes, int tiles, cudaStream_t s, int* err,
-                        int splits = 1, long long c_split_stride = 0) {
+                        long long wait_limit, int splits = 1, long long c_split_stride = 0) {
   GemmLaunch L{};
   for (int i = 0; i < 6; ++i) L.ptr[i] = ptr[i];
   L.nodes = nodes;
@@ -949,6 +1010,7 @@ cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
   L.splits = splits;
   L.c_split_stride = c_split_stride;
   L.err = err;
+  L.wait_limit = wait_limit;
   grouped_gemm_tc_kernel<<<dim3(tiles, splits), 128, kTcSmem, s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
@@ -985,6 +1047,24 @@ static int tiles_for(const cgtp_plan_s* plan, const UvwState* st, int which, int
   }
   return count_tiles(rc);
 }
+
+cgtp_status uvw_set_chunk(cgtp_plan_s* plan, int nodes) {
+  UvwState* st = static_cast<UvwState*>(plan->uvw);
+  const size_t elems = size_t(2) * nodes * st->s_node;
+  float* p = nullptr;
+  if (cudaMalloc(&p, elems * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
+  }
+  cudaFree(st->scratch);  // waits for the work that used the old buffer
+  plan->device_bytes = plan->device_bytes - st->scratch_elems * sizeof(float) + elems * sizeof(float);
+  st->scratch = p;
+  st->scratch_elems = elems;
+  st->chunk_nodes = nodes;
+  return CGTP_OK;
+}
+
+int uvw_chunk(const cgtp_plan_s* plan) { return static_cast<const UvwState*>(plan->uvw)->chunk_nodes; }
 
 static cgtp_status sticky_error(const UvwState* st) {
   if (*st->err_host)
@@ -1027,7 +1107,7 @@ cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const vo
     const float* ptr[6] = {st->scratch, static_cast<const float*>(M),
                            static_cast<float*>(out) + (size_t)n0 * plan->d_out, nullptr, nullptr, nullptr};
     cgtp_status r = launch_gemm(st->fwd_probs, st->fwd_np, st->fwd_segs, ptr, nodes,
-                                tiles_for(plan, st, 0, nodes), s, st->err_dev);
+                                tiles_for(plan, st, 0, nodes), s, st->err_dev, plan->wait_limit);
     if (r != CGTP_OK) return r;
   }
   refresh_error(st, s);
@@ -1050,7 +1130,7 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     const float* xrows = static_cast<const float*>(x) + (size_t)n0 * plan->d1;
     const float* pre[6] = {Abuf, static_cast<const float*>(M), nullptr, xrows, nullptr, nullptr};
     cgtp_status r = launch_gemm(st->pre_probs, st->pre_np, st->pre_segs, pre, nodes,
-                                tiles_for(plan, st, 1, nodes), s, st->err_dev);
+                                tiles_for(plan, st, 1, nodes), s, st->err_dev, plan->wait_limit);
     if (r != CGTP_OK) return r;
     Bwd3Args b{};
     b.Y = static_cast<const float*>(rvec ? rvec : Y);
@@ -1075,22 +1155,26 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     b.items = st->bwd3_items;
     b.n_items = st->bwd3_n_items;
     const int grid = std::min(nodes, plan->num_sms);
+    const void* kb = rvec ? reinterpret_cast<const void*>(uvw_bwd_edge3_kernel<true>)
+                          : reinterpret_cast<const void*>(uvw_bwd_edge3_kernel<false>);
+    b.idx_cap = smem_cap_cached(kb) >= int(kBwd3IdxInts * sizeof(int)) ? kBwd3IdxInts : 0;
+    const size_t isz = size_t(b.idx_cap) * sizeof(int);
     if (rvec)
-      uvw_bwd_edge3_kernel<true><<<grid, kBwd3Warps * 32, 0, s>>>(b);
+      uvw_bwd_edge3_kernel<true><<<grid, kBwd3Warps * 32, isz, s>>>(b);
     else
-      uvw_bwd_edge3_kernel<false><<<grid, kBwd3Warps * 32, 0, s>>>(b);
+      uvw_bwd_edge3_kernel<false><<<grid, kBwd3Warps * 32, isz, s>>>(b);
     if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw backward edge stage launch failed");
     const float* post[6] = {nullptr, static_cast<const float*>(M),
                             static_cast<float*>(gx) + (size_t)n0 * plan->d1, xrows,
                             static_cast<float*>(gM), Hbuf};
-    r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s, st->err_dev);
+    r = launch_gemm(st->gx_probs, st->gx_np, st->gx_segs, post, nodes, tiles_for(plan, st, 2, nodes), s, st->err_dev, plan->wait_limit);
     if (r != CGTP_OK) return r;
     // gM over this chunk's senders: split-K partials, then an ordered reduction
     const float* postp[6] = {post[0], post[1], post[2], post[3], st->gm_part, post[5]};
     const int splits = std::min(kGmSplits, std::max(1, nodes / 64));
     const long long n_gm = (long long)st->K * plan->w_numel;
     r = launch_gemm(st->gm_probs, st->gm_np, st->gm_segs, postp, nodes, tiles_for(plan, st, 3, nodes), s, st->err_dev,
-                    splits, n_gm);
+                    plan->wait_limit, splits, n_gm);
     if (r != CGTP_OK) return r;
     splitk_reduce_kernel<<<std::min<long long>((n_gm + 255) / 256, 4096), 256, 0, s>>>(
         static_cast<float*>(gM), st->gm_part, splits, n_gm, first ? 0 : 1);

@@ -91,10 +91,9 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      then being W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
  * the streaming node stage: node state for a chunk of nodes (default 4096,
- * overridable through the environment variable CGTP_UVW_CHUNK_NODES read at
- * plan creation), 2 x chunk x K x sum_path mul*(2l+1) floats (~590 MB for
- * 64x(0e,1o,2e), K = 8).  uvw limits: l <= 3, K <= 8.  Must be called with the
- * target device current.
+ * cgtp_plan_set_node_chunk changes it), 2 x chunk x K x sum_path mul*(2l+1)
+ * floats (~590 MB for 64x(0e,1o,2e), K = 8 at the default chunk).  uvw
+ * limits: l <= 3, K <= 8.  Must be called with the target device current.
  */
 cgtp_status cgtp_plan_create(cgtp_plan* plan, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
@@ -152,17 +151,30 @@ cgtp_status cgtp_graph_device_bytes(cgtp_graph graph, int64_t* bytes);
 
 /*
  * cgtp_plan_set_wait_limit -- polls of an mbarrier before a wait of the
- *  plan's staged uvu kernels gives up (default 4,194,304).  The staged kernels
- *  move every gathered operand with bulk asynchronous copies that complete on
- *  mbarriers ("An Efficient Sparse Kernel Generator ...", Abstract: register-
- *  and shared-memory-resident operands); no wait is unbounded.  A wait that
- *  gives up records the failure in the plan's error word, lets its copies in
- *  flight land (bounded) and leaves the kernel; that call's results are
- *  invalid and every later call on the plan returns CGTP_ECUDA.  0 makes the
- *  first wait give up at once (fault injection for tests: the GPU stays
- *  usable).  CGTP_EINVAL for a null plan or polls < 0.
+ *  plan's kernels gives up (default 4,194,304).  The uvw node GEMM runs on
+ *  the tensor cores (tcgen05.mma, "An Efficient Sparse Kernel Generator ...",
+ *  Figure 3B/C: the multiplicity-mixing matrix product) and waits on mbarriers
+ *  for their completion; no wait is unbounded.  A wait that gives up records
+ *  the failure in the plan's error word, lets the work in flight finish
+ *  (bounded), frees its tensor memory and leaves the kernel; that call's
+ *  results are invalid and every later call on the plan returns CGTP_ECUDA.
+ *  0 makes the first wait give up at once (fault injection for tests: the GPU
+ *  stays usable).  CGTP_EINVAL for a null plan or polls < 0.
  */
 cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls);
+
+/*
+ * Node chunk of a uvw plan with radial weights (radial_k > 0).  Its node state
+ * ("Sobek ...", Abstract: bounded receiver-side state) is streamed through a
+ * plan-owned scratch of 2 * nodes * K * sum_path(mul * (2l+1)) floats: the
+ * forward and the backward walk the graph `nodes` receivers (senders) at a
+ * time.  cgtp_plan_set_node_chunk replaces the scratch (it waits for work still
+ * using the old one); nodes in [1, 1048576], default 4096.  CGTP_EINVAL for
+ * other plans or sizes, CGTP_ENOMEM when the scratch cannot be allocated.
+ * cgtp_plan_node_chunk reports the chunk (0 for plans without node state).
+ */
+cgtp_status cgtp_plan_set_node_chunk(cgtp_plan plan, int64_t nodes);
+cgtp_status cgtp_plan_node_chunk(cgtp_plan plan, int64_t* nodes);
 
 /* Device-to-device copy of the transpose arrays (any pointer may be NULL). */
 cgtp_status cgtp_graph_transpose(cgtp_graph graph, int32_t* t_rowptr, int32_t* t_eid,

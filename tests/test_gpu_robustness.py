@@ -1,10 +1,11 @@
 """Failure handling and memory safety of the CUDA path, on the GPU.
 
-* Bounded waits: the staged uvu kernels wait on mbarriers for their bulk
-  copies.  A plan whose wait limit is 0 gives up at the first wait; the kernel
-  records the failure in the plan's error word, lets its copies land and exits.
-  That call's results are invalid, the plan's next call returns CGTP_ECUDA, and
-  the GPU stays usable (a fresh plan on the same graph matches the oracle).
+* Bounded waits: the uvw node GEMM waits on mbarriers for its tensor-core
+  MMAs.  A plan whose wait limit is 0 gives up at the first wait; the kernel
+  records the failure in the plan's error word, lets the MMAs in flight finish,
+  frees its tensor memory and exits.  That call's results are invalid, the
+  plan's next call returns CGTP_ECUDA, and the GPU stays usable (a fresh plan
+  on the same graph matches the oracle).
 * Host checks: a misaligned tensor pointer is rejected with CGTP_EINVAL before
   anything is launched.
 * Canaries: every output tensor is surrounded by guard words; forward and
@@ -42,41 +43,53 @@ def _plan(spec, dtype=torch.float32):
     return cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", dtype)
 
 
+def _uvw_workload(N=48):
+    spec = dict(wl.SPECS["uvw"])
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvw")
+    w = wl.make("uvw", oplan.w_numel, seed=4, N=N)
+    return spec, oplan, w
+
+
+def _uvw_plan(spec):
+    return cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvw", torch.float32, radial_k=8)
+
+
 @pytest.mark.parametrize("direction", ["forward", "backward"])
 def test_wait_give_up_is_reported_and_the_gpu_stays_usable(direction):
-    spec, oplan, w = _workload()
-    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
-    x, Y, W = T(w["x"]), T(w["Y"]), T(w["W"])
+    spec, oplan, w = _uvw_workload()
+    d = {k: T(v) for k, v in w.items() if isinstance(v, np.ndarray)}
+    graph = cg.Graph(d["rowptr"], d["col"], w["N"])
     g = T(np.random.default_rng(5).standard_normal((w["N"], oplan.d_out)).astype(np.float32))
-    bad = _plan(spec)
+    bad = _uvw_plan(spec)
     bad.set_wait_limit(0)
     if direction == "forward":
-        cg.cgtp_conv_forward(bad, graph, x, Y, W)       # enqueued; its results are invalid
+        cg.cgtp_conv_forward(bad, graph, d["x"], d["Y"], d["R"], d["M"])      # results invalid
     else:
-        cg.cgtp_conv_backward(bad, graph, g, x, Y, W)
-    torch.cuda.synchronize()                            # the kernel left on its own
+        cg.cgtp_conv_backward(bad, graph, g, d["x"], d["Y"], d["R"], d["M"])
+    torch.cuda.synchronize()                                                 # the kernels left on their own
     with pytest.raises(cg.CgtpError) as e:
-        cg.cgtp_conv_forward(bad, graph, x, Y, W)
+        cg.cgtp_conv_forward(bad, graph, d["x"], d["Y"], d["R"], d["M"])
     assert e.value.status == cg.CGTP_ECUDA
     assert "gave up" in str(e.value)
-    with pytest.raises(cg.CgtpError):                   # sticky
-        cg.cgtp_conv_backward(bad, graph, g, x, Y, W)
-    good = _plan(spec)
-    out = cg.cgtp_conv_forward(good, graph, x, Y, W)
-    gx, gY, gW, _ = cg.cgtp_conv_backward(good, graph, g, x, Y, W)
+    with pytest.raises(cg.CgtpError):                                        # sticky
+        cg.cgtp_conv_backward(bad, graph, g, d["x"], d["Y"], d["R"], d["M"])
+    good = _uvw_plan(spec)
+    out = cg.cgtp_conv_forward(good, graph, d["x"], d["Y"], d["R"], d["M"])
     torch.cuda.synchronize()
-    ref = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-    rgx, _, rgW = oconv.conv_uvu_backward(oplan, g.cpu().numpy(), w["x"], w["Y"], w["W"], w["rowptr"], w["col"])
-    for got, r in ((out, ref), (gx, rgx), (gW, rgW)):
-        got = got.cpu().numpy().astype(np.float64)
-        assert np.abs(got - r).max() <= 1e-4 * np.abs(r).max()
+    ref = oconv.conv_uvw_radial_forward(oplan, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"])
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
 
 
-def test_wait_limit_rejects_negative():
-    spec, _, _ = _workload(N=8)
-    with pytest.raises(cg.CgtpError) as e:
-        _plan(spec).set_wait_limit(-1)
-    assert e.value.status == cg.CGTP_EINVAL
+def test_wait_limit_and_node_chunk_reject_bad_values():
+    spec, _, _ = _uvw_workload(N=8)
+    plan = _uvw_plan(spec)
+    for call in (lambda: plan.set_wait_limit(-1), lambda: plan.set_node_chunk(0),
+                 lambda: plan.set_node_chunk((1 << 20) + 1),
+                 lambda: _plan(wl.SPECS["nequip"]).set_node_chunk(64)):   # uvu plans have no node state
+        with pytest.raises(cg.CgtpError) as e:
+            call()
+        assert e.value.status == cg.CGTP_EINVAL
 
 
 def test_misaligned_pointer_is_rejected_before_launch():

@@ -2,13 +2,11 @@
 W_e = R[e] @ M never formed) against the FP64 oracle, which forms W_e per edge.
 
 Tolerance: max|err| <= 1e-4 * max|ref| per output tensor (FP32).  The node-chunk
-size is lowered through CGTP_UVW_CHUNK_NODES so several chunks (and a ragged
+size is lowered through cgtp_plan_set_node_chunk so several chunks (and a ragged
 last chunk) are exercised on graphs the oracle evaluates in seconds; the full
 200k-node workload is checked on sampled nodes, edges and gM entries plus the
 homogeneity identities <g,out> = <gx,x> = <gY,Y> = <gR,R> = <gM,M>.
 """
-
-import os
 
 import numpy as np
 import pytest
@@ -52,17 +50,10 @@ def make(N, chunk=None, seed=0, in1=None, out=None, in2=None):
     spec = dict(wl.SPECS["uvw"])
     if in1:
         spec.update(in1=in1, out=out, in2=in2)
-    old = os.environ.get("CGTP_UVW_CHUNK_NODES")
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvw", torch.float32, radial_k=8)
     if chunk:
-        os.environ["CGTP_UVW_CHUNK_NODES"] = str(chunk)
-    try:
-        plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvw", torch.float32, radial_k=8)
-    finally:
-        if chunk:
-            if old is None:
-                del os.environ["CGTP_UVW_CHUNK_NODES"]
-            else:
-                os.environ["CGTP_UVW_CHUNK_NODES"] = old
+        plan.set_node_chunk(chunk)
+        assert plan.node_chunk == chunk
     oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvw")
     over = dict(N=N)
     if in1:
