@@ -51,8 +51,14 @@ constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over n
 struct UvwPath {
   int l1, l2, l3, D1, D2, D3, mul1, mul_out;
   int off1, off2, ooff, woff;
-  int soff;      // offset of [u][m3] (fwd state) inside one radial slice of a node's state
-  int aoff;      // offset of [w][m1] (bwd state) inside one radial slice
+  // Node state, one radial slice [k] of a node: forward S grouped by output
+  // block o as [m3][paths into o: u], backward A / H grouped by in1 block as
+  // [m1][paths from that block: w] (channels innermost: the edge stages' lanes
+  // and the node GEMMs' rows read and write contiguous runs)
+  int soff;      // forward: offset of this path's u = 0, m3 = 0 inside the slice
+  int aoff;      // backward: offset of this path's w = 0, m1 = 0 inside the slice
+  int sstr;      // forward: stride of m3 (the channels of every path into the block)
+  int astr;      // backward: stride of m1 (the channels of every path from the in1 block)
   int cyoff;     // per-edge cy layout offset
   int i1, io;
 };
@@ -324,6 +330,7 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
   const bool rok = r < rows;
   const int n = rok ? r / P.D : 0, m = rok ? r - n * P.D : 0;
   float* crow = C + P.c_off + n * P.c_n + m * P.c_m;
+  const bool vec = P.c_j == 1 && ((reinterpret_cast<uintptr_t>(crow + c0)) & 15u) == 0;
   const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
   for (int cc = 0; cc < kTN; cc += 16) {
@@ -338,13 +345,39 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = 0u;  // empty K range: the product is zero
     }
+    if (vec) {  // contiguous 16-byte aligned columns: four at a time
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int c = c0 + cc + j;
-      if (rok && c < P.J) {
-        float* dst = crow + (long long)c * P.c_j;
-        const float val = __uint_as_float(v[j]);
-        *dst = P.beta ? *dst + val : val;
+      for (int j = 0; j < 16; j += 4) {
+        const int c = c0 + cc + j;
+        if (rok && c + 3 < P.J) {
+          float4* dst = reinterpret_cast<float4*>(crow + c);
+          float4 val = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                   __uint_as_float(v[j + 3]));
+          if (P.beta) {
+            const float4 o = *dst;
+            val.x += o.x;
+            val.y += o.y;
+            val.z += o.z;
+            val.w += o.w;
+          }
+          *dst = val;
+        } else {
+          for (int q = 0; q < 4; ++q)
+            if (rok && c + q < P.J) {
+              float* d = crow + c + q;
+              *d = P.beta ? *d + __uint_as_float(v[j + q]) : __uint_as_float(v[j + q]);
+            }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + cc + j;
+        if (rok && c < P.J) {
+          float* dst = crow + (long long)c * P.c_j;
+          const float val = __uint_as_float(v[j]);
+          *dst = P.beta ? *dst + val : val;
+        }
       }
     }
   }
@@ -408,7 +441,7 @@ struct EdgeArgs {
 
 template <int D1, int D3>
 __device__ __noinline__ void fwd_state_item(const float* __restrict__ x, int d1, int off1, int cyoff,
-                                            int soff, int s_slice, int K, int u, int cnt,
+                                            int soff, int sstr, int s_slice, int K, int u, int cnt,
                                             const int* src_s, const float* Rs, const float* cys,
                                             int cy_size, float* Ss) {
   using V = float4;
@@ -449,9 +482,9 @@ __device__ __noinline__ void fwd_state_item(const float* __restrict__ x, int d1,
 #pragma unroll
     for (int k = 0; k < kKB; ++k) {
       if (kb + k >= K) break;
-      float* sp = Ss + (kb + k) * s_slice + soff + u * D3;
+      float* sp = Ss + (kb + k) * s_slice + soff + u;
 #pragma unroll
-      for (int m = 0; m < D3; ++m) sp[m] += acc[k][m];
+      for (int m = 0; m < D3; ++m) sp[m * sstr] += acc[k][m];
     }
   }
 }
@@ -462,7 +495,7 @@ __device__ __noinline__ void fwd_state_item(const float* __restrict__ x, int d1,
 
 #define UVW_FWD_CASE(L1, L3)                                                                     \
   case (L1)*8 + (L3):                                                                            \
-    fwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(a.x, a.d1, p.off1, p.cyoff, p.soff, a.s_slice, a.K, \
+    fwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(a.x, a.d1, p.off1, p.cyoff, p.soff, p.sstr, a.s_slice, a.K, \
                                                 u, cnt, src_s, Rs, cys, cy_size, Ss);              \
     break;
 
@@ -596,17 +629,17 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
                                            float* __restrict__ gR, const int* __restrict__ t_eid,
                                            const int* __restrict__ t_dst, int tb, int te, size_t node_off,
                                            int d2, int d_out, int K, int s_slice, int off2, int ooff,
-                                           int aoff, int mul_out, int w0, int lane) {
+                                           int aoff, int astr, int mul_out, int w0, int lane) {
   constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1;
   const int w = w0 + lane;
   const bool active = w < mul_out;
   float A[kKB][D1], H[kKB][D1];
-  const float* As = Astate + node_off + aoff + w * D1;
+  const float* As = Astate + node_off + aoff + w;
 #pragma unroll
   for (int k = 0; k < kKB; ++k)
 #pragma unroll
     for (int m = 0; m < D1; ++m) {
-      A[k][m] = (active && k < K) ? __ldg(As + k * s_slice + m) : 0.f;
+      A[k][m] = (active && k < K) ? __ldg(As + k * s_slice + m * astr) : 0.f;
       H[k][m] = 0.f;
     }
   for (int t = tb; t < te; ++t) {
@@ -660,12 +693,12 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
     }
   }
   if (active) {
-    float* Hs = Hstate + node_off + aoff + w * D1;
+    float* Hs = Hstate + node_off + aoff + w;
 #pragma unroll
     for (int k = 0; k < kKB; ++k)
       if (k < K)
 #pragma unroll
-        for (int m = 0; m < D1; ++m) Hs[k * s_slice + m] = H[k][m];
+        for (int m = 0; m < D1; ++m) Hs[k * s_slice + m * astr] = H[k][m];
   }
 }
 
@@ -674,7 +707,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
       uvw_bwd3_unit<L1, L2, L3, SH>(a.Y, a.R, a.rbf, a.g, a.Astate, a.Hstate, a.gY, a.gR, eidp, dstp,           \
                                 rp[s], rp[s + 1], (size_t)(s - a.n0) * a.s_node, a.d2, a.d_out, a.K,  \
-                                a.s_slice, p.off2, p.ooff, p.aoff, p.mul_out, item.u0, lane);        \
+                                a.s_slice, p.off2, p.ooff, p.aoff, p.astr, p.mul_out, item.u0, lane); \
     break;
 
 constexpr int kBwd3Warps = 16;
@@ -757,8 +790,27 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   int lmax = 0;
   for (const auto& p : plan->paths) lmax = std::max(lmax, std::max(p.l1, std::max(p.l2, p.l3)));
   if (lmax > 3) return fail(CGTP_EUNSUPPORTED, "uvw supports l <= 3");
-  // state slices: forward [path][u][m3], backward [path][w][m1]
+  // state slices: forward per output block o [m3][u of every path into o];
+  // backward per in1 block b [m1][w of every path from b]
+  const int n_out_blocks = static_cast<int>(plan->out.size()), n_in1_blocks = static_cast<int>(plan->in1.size());
+  std::vector<int> U(n_out_blocks, 0), Wb(n_in1_blocks, 0), cu(plan->paths.size()), cw(plan->paths.size());
+  for (size_t i = 0; i < plan->paths.size(); ++i) {
+    const auto& q = plan->paths[i];
+    cu[i] = U[q.io];
+    U[q.io] += q.mul1;
+    cw[i] = Wb[q.i1];
+    Wb[q.i1] += q.mul_out;
+  }
+  std::vector<int> obase(n_out_blocks, 0), ibase(n_in1_blocks, 0);
   int soff = 0, aoff = 0;
+  for (int o = 0; o < n_out_blocks; ++o) {
+    obase[o] = soff;
+    soff += U[o] * (2 * plan->out[o].l + 1);
+  }
+  for (int b = 0; b < n_in1_blocks; ++b) {
+    ibase[b] = aoff;
+    aoff += Wb[b] * (2 * plan->in1[b].l + 1);
+  }
   LayoutHost lay;
   cgtp_status s = build_layout(plan, kEdgeChunk, size_t(1) << 40, &lay);
   if (s != CGTP_OK) return s;
@@ -780,13 +832,13 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     u.off2 = q.off2;
     u.ooff = q.ooff;
     u.woff = q.woff;
-    u.soff = soff;
-    u.aoff = aoff;
+    u.soff = obase[q.io] + cu[i];
+    u.aoff = ibase[q.i1] + cw[i];
+    u.sstr = U[q.io];
+    u.astr = Wb[q.i1];
     u.cyoff = lay.paths[i].cyoff_g;
     u.i1 = q.i1;
     u.io = q.io;
-    soff += q.mul1 * u.D3;
-    aoff += q.mul_out * u.D1;
     st->paths_h.push_back(u);
   }
   st->n_paths = static_cast<int>(plan->paths.size());
@@ -815,7 +867,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     P.Nn = -1;
     P.D = 2 * plan->out[o].l + 1;
     P.J = plan->out[o].mul;
-    P.a_off = 0; P.a_n = st->s_node; P.a_m = 1;
+    P.a_off = 0; P.a_n = st->s_node; P.a_m = U[o];   // S rows (n, m3): channels contiguous
     P.b_j = 1;
     P.c_off = out_off[o]; P.c_n = plan->d_out; P.c_m = 1; P.c_j = P.D;
     P.beta = 0;
@@ -827,7 +879,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
           S.a_off = (long long)k * st->s_slice + q.soff;
           S.b_off = (long long)k * wn + q.woff;
           S.K = q.mul1;
-          S.a_k = q.D3;
+          S.a_k = 1;
           S.b_k = q.mul_out;
           S.b_j = 1;
           fs.push_back(S);
@@ -843,7 +895,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       P.Nn = -1; P.D = q.D1; P.J = q.mul_out;
       P.a_off = q.off1; P.a_n = plan->d1; P.a_m = 1;
       P.b_j = 1;
-      P.c_off = (long long)k * st->s_slice + q.aoff; P.c_n = st->s_node; P.c_m = 1; P.c_j = q.D1;
+      P.c_off = (long long)k * st->s_slice + q.aoff; P.c_n = st->s_node; P.c_m = q.astr; P.c_j = 1;
       P.beta = 0;
       P.seg0 = int(ps.size());
       GemmSeg S{};
@@ -860,7 +912,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     GemmProb P{};
     P.a_base = 5; P.b_base = 1; P.c_base = 2;
     P.Nn = -1; P.D = 2 * b.l + 1; P.J = b.mul;
-    P.a_off = 0; P.a_n = st->s_node; P.a_m = 1;
+    P.a_off = 0; P.a_n = st->s_node; P.a_m = Wb[i1];  // H rows (s, m1): channels contiguous
     P.c_off = o1; P.c_n = plan->d1; P.c_m = 1; P.c_j = P.D;
     P.beta = 0;
     P.seg0 = int(xs.size());
@@ -870,7 +922,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
           GemmSeg S{};
           S.a_off = (long long)k * st->s_slice + q.aoff;
           S.b_off = (long long)k * wn + q.woff;  // B[w][u] = M[k][woff + u*mul_out + w]
-          S.K = q.mul_out; S.a_k = q.D1; S.b_k = 1;
+          S.K = q.mul_out; S.a_k = 1; S.b_k = 1;
           S.b_j = q.mul_out;  // B[w][u] = M[k][woff + u*mul_out + w]
           xs.push_back(S);
         }
@@ -885,15 +937,15 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       P.a_base = 3; P.b_base = 5; P.c_base = 4;
       P.Nn = q.mul1; P.D = 1; P.J = q.mul_out;
       P.a_off = q.off1; P.a_n = q.D1; P.a_m = 0;
-      P.b_j = q.D1;
+      P.b_j = 1;
       P.c_off = (long long)k * wn + q.woff; P.c_n = q.mul_out; P.c_m = 0; P.c_j = 1;
       P.beta = 0;  // writes a split-K partial; splitk_reduce_kernel accumulates into gM
       P.seg0 = int(ms.size());
       for (int m1 = 0; m1 < q.D1; ++m1) {
         GemmSeg S{};
-        S.a_off = m1; S.b_off = (long long)k * st->s_slice + q.aoff + m1;
+        S.a_off = m1; S.b_off = (long long)k * st->s_slice + q.aoff + (long long)m1 * q.astr;
         S.K = -1; S.a_k = plan->d1; S.b_k = st->s_node;
-        S.b_j = q.D1;
+        S.b_j = 1;
         ms.push_back(S);
       }
       P.seg1 = int(ms.size());
