@@ -260,6 +260,30 @@ def conv_uvw_radial_gM_entries(plan, g, x, Y, R, rowptr, col, entries):
     return np.array(out)
 
 
+def conv_uvw_radial_gM_slice(plan, g, x, Y, R, rowptr, col, k, pi, chunk=1 << 16):
+    """One (k, path) slice of gM, [mul1, mul_out], summed over every edge.
+
+    Same definition as conv_uvw_radial_gM_entries, for all (u, w) of the slice
+    at once: gM[k][path][u][w] = sum_e R[e,k] sum_m3 t_e[u, m3] g[dst][w, m3],
+    the edge sum taken in chunks of edges, each a matrix product over (e, m3).
+    """
+    rowptr = np.asarray(rowptr, dtype=np.int64)
+    col = np.asarray(col, dtype=np.int64)
+    dst = csr_dst(rowptr)
+    p = plan.paths[pi]
+    C = real_cg_block(p.l1, p.l2, p.l3)
+    D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+    acc = np.zeros((p.mul1, p.mul_out))
+    for e0 in range(0, col.size, chunk):
+        e1 = min(col.size, e0 + chunk)
+        xs = _f64(x[col[e0:e1], p.off1:p.off1 + p.mul1 * D1]).reshape(-1, p.mul1, D1)
+        ys = _f64(Y[e0:e1, p.off2:p.off2 + D2])
+        t = np.einsum("ijk,eui,ej->euk", C, xs, ys, optimize=True) * _f64(R[e0:e1, k])[:, None, None]
+        gw = _f64(g[dst[e0:e1], p.ooff:p.ooff + p.mul_out * D3]).reshape(-1, p.mul_out, D3)
+        acc += np.einsum("euk,ewk->uw", t, gw, optimize=True)
+    return acc
+
+
 # ---------------------------------------------------------------------------
 # second derivatives ("double backward")
 # ---------------------------------------------------------------------------

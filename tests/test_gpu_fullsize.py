@@ -62,7 +62,9 @@ def test_conv_full_size_sampled(name, dtype):
     tol = TOL[np.dtype(dtype)]
     rng = np.random.default_rng(5)
     N, E = w["N"], w["E"]
-    nodes = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 14)]))
+    deg = np.diff(w["rowptr"])
+    # first and last rows, the longest and the shortest rows, random rows
+    nodes = np.unique(np.concatenate([[0, N - 1, int(np.argmax(deg)), int(np.argmin(deg))], rng.integers(0, N, 14)]))
     ref = oconv.conv_uvu_forward(oplan, w["x"], w["Y"], w["W"], w["rowptr"], w["col"], nodes=nodes)
     close("out[sampled]", out[T(nodes)], ref, tol)
     gh = g.cpu().numpy()

@@ -120,11 +120,17 @@ def test_uvw_full_size_sampled():
     rgx, _, _, _ = oconv.conv_uvw_radial_backward(oplan, gh, w["x"], w["Y"], w["R"], w["M"], w["rowptr"],
                                                   w["col"], edges=sedges)
     close("gx[sampled]", gx[torch.from_numpy(senders).cuda()], rgx[senders])
-    ent = [(0, 0, 0, 0), (7, 10, 63, 5), (3, 5, 17, 40), (5, 7, 2, 63)]
-    rgm = oconv.conv_uvw_radial_gM_entries(oplan, gh, w["x"], w["Y"], w["R"], w["rowptr"], w["col"], ent)
+    # one whole (k, path) slice of gM, and sampled entries of other slices; every bound
+    # scales with the oracle's slice, not with the GPU's own output
     gMh = gM.cpu().numpy()
-    got = [gMh[k, oplan.paths[p].woff + u * oplan.paths[p].mul_out + ww] for (k, p, u, ww) in ent]
-    assert np.abs(np.array(got) - rgm).max() <= 1e-4 * np.abs(gMh).max()
+    k, pi = 3, 5
+    q = oplan.paths[pi]
+    rsl = oconv.conv_uvw_radial_gM_slice(oplan, gh, w["x"], w["Y"], w["R"], w["rowptr"], w["col"], k, pi)
+    close(f"gM[{k}][path {pi}]", gMh[k, q.woff:q.woff + q.mul1 * q.mul_out].reshape(q.mul1, q.mul_out), rsl)
+    ent = [(0, 0, 0, 0), (7, 10, 63, 5), (5, 7, 2, 63)]
+    rgm = oconv.conv_uvw_radial_gM_entries(oplan, gh, w["x"], w["Y"], w["R"], w["rowptr"], w["col"], ent)
+    got = [gMh[kk, oplan.paths[p].woff + u * oplan.paths[p].mul_out + ww] for (kk, p, u, ww) in ent]
+    assert np.abs(np.array(got) - rgm).max() <= 1e-4 * np.abs(rsl).max()
     # homogeneity: out is linear in each of x, Y, R and M
     homogeneity(g, out, (("x", d["x"], gx), ("Y", d["Y"], gY), ("R", d["R"], gR), ("M", d["M"], gM)), 1e-6)
     # bounded workspace: nothing edge-sized beyond inputs/outputs

@@ -6,7 +6,7 @@ independent construction.
 """
 
 import os
-from math import sqrt  # noqa: F401  (used by eval of the golden file)
+from math import sqrt  # also used by eval of the golden file
 
 import numpy as np
 import pytest
@@ -180,3 +180,22 @@ def test_sh_jacobian_against_finite_differences():
         assert np.abs(J[:, :, k] - fd).max() < 1e-7 * max(1.0, np.abs(fd).max())
     # radial direction does not change the harmonics
     assert np.abs(np.einsum("eck,ek->ec", J, r)).max() < 1e-12
+
+
+def test_real_block_sign_rule_every_triple_l_le_7():
+    # The sign convention of the real blocks (the pages fix none): after the unit
+    # Frobenius normalisation, the first entry above 1e-12 in row-major (m1, m2, m3)
+    # order is positive, and the block carries the component factor sqrt(2 l3 + 1).
+    # Equivariance, norms and nonzero counts are blind to a flipped sign, so the
+    # rule is checked on its own for every triangle-valid triple with l <= 7.
+    n = 0
+    for l1 in range(8):
+        for l2 in range(8):
+            for l3 in range(abs(l1 - l2), min(l1 + l2, 7) + 1):
+                C = cg.real_cg_block(l1, l2, l3)
+                flat = C.reshape(-1)
+                first = flat[np.flatnonzero(np.abs(flat) > 1e-12)[0]]
+                assert first > 0, (l1, l2, l3, first)
+                assert abs(np.linalg.norm(flat) - sqrt(2 * l3 + 1)) < 1e-12, (l1, l2, l3)
+                n += 1
+    assert n == sum(min(l1 + l2, 7) - abs(l1 - l2) + 1 for l1 in range(8) for l2 in range(8))

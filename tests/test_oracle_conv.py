@@ -285,6 +285,25 @@ def test_uvw_gM_entries_match_full_backward():
         assert abs(gM[k, p.woff + u * p.mul_out + w] - v) < 1e-11
 
 
+def test_uvw_gM_slice_matches_entries():
+    # the chunked slice (matrix products over edge chunks) against the per-entry definition,
+    # with a chunk smaller than E so several chunks and a ragged last one are summed
+    rng = np.random.default_rng(29)
+    plan = irreps.make_plan("3x0e+2x1o+2x2e", "0e+1o+2e", "2x0e+3x1o+2x2e", mode="uvw")
+    N, E, K = 6, 23, 3
+    rowptr, col = small_graph(rng, N, E)
+    x = rng.normal(size=(N, plan.d1))
+    Y = rng.normal(size=(E, plan.d2))
+    R = rng.normal(size=(E, K))
+    g = rng.normal(size=(N, plan.d_out))
+    for k in range(K):
+        for pi, p in enumerate(plan.paths):
+            sl = conv.conv_uvw_radial_gM_slice(plan, g, x, Y, R, rowptr, col, k, pi, chunk=5)
+            ent = [(k, pi, u, w) for u in range(p.mul1) for w in range(p.mul_out)]
+            ref = conv.conv_uvw_radial_gM_entries(plan, g, x, Y, R, rowptr, col, ent)
+            assert np.abs(sl.reshape(-1) - ref).max() < 1e-12
+
+
 @pytest.mark.parametrize("mode", ["uvu", "uvw", "batched"])
 def test_double_backward_exact_directional_differences(mode):
     # S = sum_j <c_j, dL/da_j> is linear in g and in each operand separately, so
@@ -424,3 +443,42 @@ def test_uvw_per_edge_weights_brute_force_fd_and_radial_identity():
             am[ai][idx] -= h
             fd = (f(*ap) - f(*am)) / (2 * h)
             assert abs(fd - ga[idx]) < 1e-7 * max(1.0, abs(fd)), (ai, idx, fd, ga[idx])
+
+
+def test_uvu_double_backward_against_autograd_hessian_vector_product():
+    # A second, independent route to the second derivatives: the convolution
+    # written as plain PyTorch CPU ops (per-path einsum with the oracle's CG
+    # blocks, index_add over receivers), L = <g, out>, its gradients with
+    # create_graph, S = sum_j <c_j, dL/da_j>, and autograd's dS/d(g, x, Y, W)
+    # (a Hessian-vector product), against the oracle's identity-based result.
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    plan = irreps.make_plan("2x0e+1x1o+2x2e", "0e+1o+2e", wl._all_out(2), mode="uvu")
+    N, E = 5, 12
+    rowptr, col = small_graph(rng, N, E)
+    dst = np.repeat(np.arange(N), np.diff(rowptr))
+    x, Y, W = rng.normal(size=(N, plan.d1)), rng.normal(size=(E, plan.d2)), rng.normal(size=(E, plan.w_numel))
+    g = rng.normal(size=(N, plan.d_out))
+    cx, cY, cW = rng.normal(size=x.shape), rng.normal(size=Y.shape), rng.normal(size=W.shape)
+    t = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    xt, Yt, Wt, gt = t(x), t(Y), t(W), t(g)
+    src_i, dst_i = torch.tensor(col, dtype=torch.long), torch.tensor(dst, dtype=torch.long)
+    out = torch.zeros(N, plan.d_out, dtype=torch.float64)
+    for p in plan.paths:
+        C = torch.tensor(cg.real_cg_block(p.l1, p.l2, p.l3))
+        D1, D2, D3 = 2 * p.l1 + 1, 2 * p.l2 + 1, 2 * p.l3 + 1
+        xs = xt[src_i, p.off1:p.off1 + p.mul1 * D1].reshape(E, p.mul1, D1)
+        ys = Yt[:, p.off2:p.off2 + D2]
+        msg = torch.einsum("ijk,eui,ej->euk", C, xs, ys) * Wt[:, p.woff:p.woff + p.mul1, None]
+        pad = torch.zeros(N, plan.d_out, dtype=torch.float64)
+        pad = pad.index_add(0, dst_i, torch.nn.functional.pad(msg.reshape(E, -1),
+                                                             (p.ooff, plan.d_out - p.ooff - p.mul1 * D3)))
+        out = out + pad
+    L = (gt * out).sum()
+    gx, gY, gW = torch.autograd.grad(L, (xt, Yt, Wt), create_graph=True)
+    S = (gx * torch.tensor(cx)).sum() + (gY * torch.tensor(cY)).sum() + (gW * torch.tensor(cW)).sum()
+    d_g, d_x, d_Y, d_W = torch.autograd.grad(S, (gt, xt, Yt, Wt), allow_unused=True)
+    ref = conv.conv_uvu_double_backward(plan, g, x, Y, W, cx, cY, cW, rowptr, col)
+    for name, got, r in (("d_gout", d_g, ref[0]), ("d_x", d_x, ref[1]), ("d_Y", d_Y, ref[2]), ("d_W", d_W, ref[3])):
+        got = np.zeros_like(r) if got is None else got.detach().numpy()
+        assert np.abs(got - r).max() <= 1e-11 * max(1.0, np.abs(r).max()), name
