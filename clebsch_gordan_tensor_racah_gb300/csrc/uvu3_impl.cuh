@@ -8,7 +8,8 @@
 //   * the CG nonzeros of each (l1, l2, l3) are compiled in as immediates
 //     (cg_baked.cuh, generated from the planner's Racah tables), so every lane
 //     forms its edge's coupling matrix cy[m1][m3] = sum_m2 C Y[m2] in registers
-//     -- no shared tables, no block-wide barriers in the forward;
+//     -- no shared tables, no block-wide barriers in the forward -- and the
+//     contractions skip the (m1, m3) entries of cy that are structurally zero;
 //   * node features, weights and output gradients arrive as 128-bit loads of
 //     four channels; the channel pairs (u0,u1), (u2,u3) go through the paired
 //     FP32 FMA (fma.rn.f32x2);
@@ -258,6 +259,7 @@ __device__ __forceinline__ void fwd3_math(const FwdEdge<T, 2 * L1 + 1, 2 * L2 + 
     const P xw23{E.wv[2] * E.xs[2 * D1 + m1], E.wv[3] * E.xs[3 * D1 + m1]};
 #pragma unroll
     for (int m3 = 0; m3 < D3; ++m3) {
+      if (!((CGB<L1, L2, L3>::mask >> (m1 * D3 + m3)) & 1ull)) continue;  // C.Y is zero there
       const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
       t01[m3] = fma2(cp, xw01, t01[m3]);
       t23[m3] = fma2(cp, xw23, t23[m3]);
@@ -461,6 +463,7 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
         P t01{T(0), T(0)}, t23{T(0), T(0)};
 #pragma unroll
         for (int m1 = 0; m1 < D1; ++m1) {
+          if (!((CGB<L1, L2, L3>::mask >> (m1 * D3 + m3)) & 1ull)) continue;  // C.Y is zero there
           const P cp{cy[m1 * D3 + m3], cy[m1 * D3 + m3]};
           t01 = fma2(cp, x01[m1], t01);
           t23 = fma2(cp, x23[m1], t23);
