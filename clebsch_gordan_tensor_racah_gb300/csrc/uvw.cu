@@ -79,7 +79,9 @@ struct GemmProb {
   long long c_off, c_n, c_m;
   int beta;                    // 0 overwrite, 1 accumulate
   int seg0, seg1;
-  int pad_;
+  // tile loading: 0 = a warp's lanes walk K (32 consecutive k of one row / column);
+  // 1 = they walk the rows of A (cols of B) at fixed k -- for operands whose K stride is large
+  unsigned char a_mode, b_mode, pad0_, pad1_;
 };
 
 struct UvwState {
@@ -175,7 +177,9 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, long lon
 // (stage i % 2, committed to that stage's mbarrier), the threads load and split
 // step i + 1 into the other stage; a stage is overwritten only after the commit
 // of the MMAs that read it (step i - 1) has arrived.
-__global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunch L) {
+constexpr int kTcWarps = 8;  // loaders; warp w % 4 reads TMEM lanes 32 (w % 4).., columns half w / 4
+
+__global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const GemmLaunch L) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   constexpr int kStage = 2 * kATile + 2 * kBTile;
@@ -219,11 +223,16 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = *tmem_holder;
   const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTN >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
-  // this thread stages column k = lane of rows warp + 4 t (A) and of columns warp + 4 t (B)
-  int aoff[kTM / 4];
+  // this thread stages column k = lane of rows warp + 8 t (A) and of columns warp + 8 t (B)
+  constexpr int kAR = kTM / kTcWarps, kBC = kTN / kTcWarps;
+  // value t of this thread: mode 0 row warp + 8 t, k = lane; mode 1 row (t % 4) 32 + lane,
+  // k = warp + 8 (t / 4) for A (B: column (t % 2) 32 + lane, k = warp + 8 (t / 2))
+  const bool amode = P.a_mode != 0, bmode = P.b_mode != 0;
+  int aoff[kAR];
 #pragma unroll
-  for (int t = 0; t < kTM / 4; ++t) {
-    const int r = r0 + warp + 4 * t;
+  for (int t = 0; t < kAR; ++t) {
+    const int rl = amode ? (t & 3) * 32 + lane : warp + kTcWarps * t;
+    const int r = r0 + rl;
     const int n = r < rows ? r / P.D : 0, m = r < rows ? r - n * P.D : 0;
     aoff[t] = r < rows ? (int)(n * P.a_n + m * P.a_m) : -1;
   }
@@ -231,28 +240,52 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
   uint32_t pend = 0;    // bit s: stage s has a commit not yet waited for
   int issued = 0;       // K steps whose MMAs were committed
   bool first = true, ok = true;
-  for (int sgi = P.seg0; sgi < P.seg1 && ok; ++sgi) {
-    const GemmSeg S = L.segs[sgi];
-    int kb = 0, ke = S.K < 0 ? L.nodes : S.K;
-    if (S.K < 0 && L.splits > 1) {
-      kb = min(L.nodes, split * slice);
-      ke = min(L.nodes, kb + slice);
-    }
-    const float* Ab = A + P.a_off + S.a_off;
-    const float* Bb = B + S.b_off;
-    for (int k0 = kb; k0 < ke; k0 += kTK) {
-      const int k = k0 + lane;
-      const bool kin = k < ke;
-      // global loads of this step (in flight while the previous step's MMAs run)
-      float av[kTM / 4], bv[kTN / 4];
-#pragma unroll
-      for (int t = 0; t < kTM / 4; ++t)
-        av[t] = (kin && aoff[t] >= 0) ? __ldg(Ab + aoff[t] + (long long)k * S.a_k) : 0.f;
-#pragma unroll
-      for (int t = 0; t < kTN / 4; ++t) {
-        const int c = c0 + warp + 4 * t;
-        bv[t] = (kin && c < P.J) ? __ldg(Bb + (long long)k * S.b_k + (long long)c * S.b_j) : 0.f;
+  // K steps of all segments as one sequence; the loads of step i + 1 are issued
+  // before step i is split and stored, so they are in flight during that work
+  struct Step {
+    int sg, k0, ke, a_k, b_k, b_j;
+    const float* Ab;
+    const float* Bb;
+  };
+  auto seg_from = [&](Step& st, int sg) {  // first non-empty segment at or after sg
+    for (; sg < P.seg1; ++sg) {
+      const GemmSeg S = L.segs[sg];
+      int kb = 0, ke = S.K < 0 ? L.nodes : S.K;
+      if (S.K < 0 && L.splits > 1) {
+        kb = min(L.nodes, split * slice);
+        ke = min(L.nodes, kb + slice);
       }
+      if (kb < ke) {
+        st = Step{sg, kb, ke, S.a_k, S.b_k, S.b_j, A + P.a_off + S.a_off, B + S.b_off};
+        return true;
+      }
+    }
+    return false;
+  };
+  auto load_step = [&](const Step& st, float (&av)[kAR], float (&bv)[kBC]) {
+#pragma unroll
+    for (int t = 0; t < kAR; ++t) {
+      const int k = st.k0 + (amode ? warp + kTcWarps * (t >> 2) : lane);
+      av[t] = (k < st.ke && aoff[t] >= 0) ? __ldg(st.Ab + aoff[t] + (long long)k * st.a_k) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < kBC; ++t) {
+      const int k = st.k0 + (bmode ? warp + kTcWarps * (t >> 1) : lane);
+      const int c = c0 + (bmode ? (t & 1) * 32 + lane : warp + kTcWarps * t);
+      bv[t] = (k < st.ke && c < P.J) ? __ldg(st.Bb + (long long)k * st.b_k + (long long)c * st.b_j) : 0.f;
+    }
+  };
+  Step cur;
+  bool have = seg_from(cur, P.seg0);
+  float av[kAR], bv[kBC];
+  if (have) load_step(cur, av, bv);
+  while (have && ok) {
+    Step nxt = cur;
+    nxt.k0 += kTK;
+    const bool have_next = nxt.k0 < nxt.ke || seg_from(nxt, cur.sg + 1);
+    float an[kAR], bn[kBC];
+    if (have_next) load_step(nxt, an, bn);
+    {
       const int st = issued & 1;
       unsigned char* a_hi = sm + st * kStage;
       unsigned char* a_lo = a_hi + kATile;
@@ -269,18 +302,20 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
         pend &= ~(1u << st);
       }
 #pragma unroll
-      for (int t = 0; t < kTM / 4; ++t) {
-        const int rr = warp + 4 * t;
+      for (int t = 0; t < kAR; ++t) {
+        const int rr = amode ? (t & 3) * 32 + lane : warp + kTcWarps * t;
+        const int kk = amode ? warp + kTcWarps * (t >> 2) : lane;
         const float hi = tf32_round(av[t]);
-        *(float*)(a_hi + sw128(rr, lane)) = hi;
-        *(float*)(a_lo + sw128(rr, lane)) = tf32_round(av[t] - hi);
+        *(float*)(a_hi + sw128(rr, kk)) = hi;
+        *(float*)(a_lo + sw128(rr, kk)) = tf32_round(av[t] - hi);
       }
 #pragma unroll
-      for (int t = 0; t < kTN / 4; ++t) {
-        const int jj = warp + 4 * t;
+      for (int t = 0; t < kBC; ++t) {
+        const int jj = bmode ? (t & 1) * 32 + lane : warp + kTcWarps * t;
+        const int kk = bmode ? warp + kTcWarps * (t >> 1) : lane;
         const float hi = tf32_round(bv[t]);
-        *(float*)(b_hi + sw128(jj, lane)) = hi;
-        *(float*)(b_lo + sw128(jj, lane)) = tf32_round(bv[t] - hi);
+        *(float*)(b_hi + sw128(jj, kk)) = hi;
+        *(float*)(b_lo + sw128(jj, kk)) = tf32_round(bv[t] - hi);
       }
       asm volatile("fence.proxy.async.shared::cta;");
       __syncthreads();
@@ -301,6 +336,12 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
       pend |= 1u << st;
       ++issued;
     }
+#pragma unroll
+    for (int t = 0; t < kAR; ++t) av[t] = an[t];
+#pragma unroll
+    for (int t = 0; t < kBC; ++t) bv[t] = bn[t];
+    cur = nxt;
+    have = have_next;
   }
   // the last commits (at most two outstanding, one per stage) before TMEM is read
   if (ok) {
@@ -325,15 +366,16 @@ __global__ void __launch_bounds__(128, 1) grouped_gemm_tc_kernel(const GemmLaunc
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
     return;
   }
-  // epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w+31
-  const int r = r0 + 32 * warp + lane;
+  // epilogue: warp w owns TMEM lanes (tile rows) 32 (w % 4) .. + 31 and the column half w / 4
+  const int quarter = warp & 3, chalf = warp >> 2;
+  const int r = r0 + 32 * quarter + lane;
   const bool rok = r < rows;
   const int n = rok ? r / P.D : 0, m = rok ? r - n * P.D : 0;
   float* crow = C + P.c_off + n * P.c_n + m * P.c_m;
   const bool vec = P.c_j == 1 && ((reinterpret_cast<uintptr_t>(crow + c0)) & 15u) == 0;
-  const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16);
 #pragma unroll
-  for (int cc = 0; cc < kTN; cc += 16) {
+  for (int cc = chalf * (kTN / 2); cc < (chalf + 1) * (kTN / 2); cc += 16) {
     uint32_t v[16];
     if (!first) {
       asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -951,6 +993,21 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       P.seg1 = int(ms.size());
       mp.push_back(P);
     }
+  // tile-loading mode per problem from its segments' strides: lanes walk K when the
+  // K stride is small, the rows of A / columns of B when those are contiguous instead
+  auto set_modes = [](std::vector<GemmProb>& probs, const std::vector<GemmSeg>& segs) {
+    for (auto& P : probs) {
+      if (P.seg1 <= P.seg0) continue;
+      const GemmSeg& S = segs[P.seg0];
+      const long long row_stride = P.D > 1 ? P.a_m : P.a_n;
+      P.a_mode = (S.a_k > 32 && row_stride < S.a_k) ? 1 : 0;
+      P.b_mode = (S.b_j == 1 && S.b_k != 1) ? 1 : 0;
+    }
+  };
+  set_modes(fp, fs);
+  set_modes(pp, ps);
+  set_modes(xp, xs);
+  set_modes(mp, ms);
   // upload descriptor tables
   std::vector<unsigned char> buf;
   auto put = [&](const void* src, size_t bytes) {
@@ -1063,7 +1120,7 @@ cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
   L.c_split_stride = c_split_stride;
   L.err = err;
   L.wait_limit = wait_limit;
-  grouped_gemm_tc_kernel<<<dim3(tiles, splits), 128, kTcSmem, s>>>(L);
+  grouped_gemm_tc_kernel<<<dim3(tiles, splits), kTcWarps * 32, kTcSmem, s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
 
