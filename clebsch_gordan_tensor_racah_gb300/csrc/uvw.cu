@@ -138,6 +138,7 @@ struct GemmLaunch {
   long long c_split_stride;
   int* err;  // set when a tensor-core wait gives up
   long long wait_limit;  // polls before a tensor-core wait gives up
+  int tiles;             // tiles of the launch (a persistent CTA takes every gridDim.x-th)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -186,29 +187,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   uint64_t* mbar = (uint64_t*)(sm + 2 * kStage);         // one per stage
   uint32_t* tmem_holder = (uint32_t*)(sm + 2 * kStage + 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // locate this CTA's problem and tile (uniform over the CTA)
-  int tile = blockIdx.x, pi = 0, rt = 0, ct = 0;
-  GemmProb P;
-  for (pi = 0; pi < L.nprob; ++pi) {
-    P = L.probs[pi];
-    const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
-    const int ntr = (rows + kTM - 1) / kTM, ntc = (P.J + kTN - 1) / kTN;
-    if (tile < ntr * ntc) {
-      rt = tile / ntc;
-      ct = tile - rt * ntc;
-      break;
-    }
-    tile -= ntr * ntc;
-  }
-  if (pi >= L.nprob) return;
-  const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
-  const float* A = L.ptr[P.a_base];
-  const float* B = L.ptr[P.b_base];
-  float* C = const_cast<float*>(L.ptr[P.c_base]);
-  const int split = blockIdx.y;
-  const int slice = (L.nodes + L.splits - 1) / L.splits;
-  if (L.splits > 1) C += split * L.c_split_stride;
-  const int r0 = rt * kTM, c0 = ct * kTN;
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
@@ -223,6 +201,35 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = *tmem_holder;
   const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTN >> 3) << 17) | ((uint32_t)(kTM >> 4) << 24);
+  uint32_t phase = 0;   // bit s: parity of stage s's next commit
+  uint32_t pend = 0;    // bit s: stage s has a commit not yet waited for
+  int issued = 0;       // K steps whose MMAs were committed (over all tiles of this CTA): picks the stage
+  bool ok = true;
+  const int split = blockIdx.y;
+  const int slice = (L.nodes + L.splits - 1) / L.splits;
+  // persistent: this CTA takes tiles blockIdx.x, + gridDim.x, ... of the launch
+  for (int tile_g = blockIdx.x; tile_g < L.tiles && ok; tile_g += gridDim.x) {
+  // locate the tile's problem (uniform over the CTA)
+  int tile = tile_g, pi = 0, rt = 0, ct = 0;
+  GemmProb P;
+  for (pi = 0; pi < L.nprob; ++pi) {
+    P = L.probs[pi];
+    const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
+    const int ntr = (rows + kTM - 1) / kTM, ntc = (P.J + kTN - 1) / kTN;
+    if (tile < ntr * ntc) {
+      rt = tile / ntc;
+      ct = tile - rt * ntc;
+      break;
+    }
+    tile -= ntr * ntc;
+  }
+  if (pi >= L.nprob) break;
+  const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
+  const float* A = L.ptr[P.a_base];
+  const float* B = L.ptr[P.b_base];
+  float* C = const_cast<float*>(L.ptr[P.c_base]);
+  if (L.splits > 1) C += split * L.c_split_stride;
+  const int r0 = rt * kTM, c0 = ct * kTN;
   // this thread stages column k = lane of rows warp + 8 t (A) and of columns warp + 8 t (B)
   constexpr int kAR = kTM / kTcWarps, kBC = kTN / kTcWarps;
   // value t of this thread: mode 0 row warp + 8 t, k = lane; mode 1 row (t % 4) 32 + lane,
@@ -236,10 +243,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
     const int n = r < rows ? r / P.D : 0, m = r < rows ? r - n * P.D : 0;
     aoff[t] = r < rows ? (int)(n * P.a_n + m * P.a_m) : -1;
   }
-  uint32_t phase = 0;   // bit s: parity of stage s's next commit
-  uint32_t pend = 0;    // bit s: stage s has a commit not yet waited for
-  int issued = 0;       // K steps whose MMAs were committed
-  bool first = true, ok = true;
+  bool first = true;
   // K steps of all segments as one sequence; the loads of step i + 1 are issued
   // before step i is split and stored, so they are in flight during that work
   struct Step {
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
       unsigned char* a_lo = a_hi + kATile;
       unsigned char* b_hi = a_hi + 2 * kATile;
       unsigned char* b_lo = b_hi + kBTile;
-      if (issued >= 2) {  // the MMAs of step issued - 2 read this stage
+      if ((pend >> st) & 1u) {  // the MMAs of step issued - 2 read this stage
         const bool done = tc_wait(&mbar[st], (phase >> st) & 1u, L.wait_limit);
         asm volatile("tcgen05.fence::after_thread_sync;");
         if (__syncthreads_or(!done)) {
@@ -343,10 +347,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
     cur = nxt;
     have = have_next;
   }
-  // the last commits (at most two outstanding, one per stage) before TMEM is read
+  // the tile's last commits (at most two outstanding, one per stage) before TMEM is read
   if (ok) {
-    for (int s = issued >= 2 ? issued - 2 : 0; s < issued; ++s) {
-      const int st = s & 1;
+    for (int st = 0; st < 2; ++st) {
+      if (!((pend >> st) & 1u)) continue;
       const bool done = tc_wait(&mbar[st], (phase >> st) & 1u, L.wait_limit);
       if (__syncthreads_or(!done)) {
         ok = false;
@@ -357,15 +361,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
     }
     asm volatile("tcgen05.fence::after_thread_sync;");
   }
-  if (!ok) {  // a tensor-core wait gave up: record, let the MMAs in flight finish (bounded), clean up
-    if (tid == 0) atomicOr(L.err, 1);
-    for (int st = 0; st < 2; ++st)
-      if ((pend >> st) & 1u) tc_wait(&mbar[st], (phase >> st) & 1u, kTcCleanupPolls);
-    asm volatile("tcgen05.fence::before_thread_sync;");
-    __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
-    return;
-  }
+  if (!ok) break;
   // epilogue: warp w owns TMEM lanes (tile rows) 32 (w % 4) .. + 31 and the column half w / 4
   const int quarter = warp & 3, chalf = warp >> 2;
   const int r = r0 + 32 * quarter + lane;
@@ -422,6 +418,15 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
         }
       }
     }
+  }
+  // every thread's TMEM reads are done before the next tile's MMAs overwrite the accumulator
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  }  // tiles
+  if (!ok) {  // a tensor-core wait gave up: record, let the MMAs in flight finish (bounded), clean up
+    if (tid == 0) atomicOr(L.err, 1);
+    for (int st = 0; st < 2; ++st)
+      if ((pend >> st) & 1u) tc_wait(&mbar[st], (phase >> st) & 1u, kTcCleanupPolls);
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
@@ -1120,7 +1125,12 @@ cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
   L.c_split_stride = c_split_stride;
   L.err = err;
   L.wait_limit = wait_limit;
-  grouped_gemm_tc_kernel<<<dim3(tiles, splits), kTcWarps * 32, kTcSmem, s>>>(L);
+  L.tiles = tiles;
+  int dev = 0, nsm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::max(1, std::min(tiles, 2 * nsm));  // two CTAs per SM, persistent
+  grouped_gemm_tc_kernel<<<dim3(grid, splits), kTcWarps * 32, kTcSmem, s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
 
