@@ -61,6 +61,7 @@ CONFIGS = {
     "mixed": dict(name="mixed", dtype="float32"),
     "nequip_bf16": dict(name="nequip", dtype="bfloat16"),
     "nequip_sh": dict(name="nequip", dtype="float32", sh=True),
+    "mixedmul": dict(name="mixedmul", dtype="float32"),
 }
 # the benchmark's five workloads besides the headline
 PER_CONFIG = ["tiny", "mace", "mace64", "highl", "uvw"]
@@ -76,6 +77,8 @@ WORKLOAD_NAMES = {
     "uvw_edge": "uvw conv with per-edge weights (10k nodes x 32 in-edges, 16x(0e,1o,2e))",
     "mixed": "mixed uvu/uvw conv (10k nodes x 32 in-edges, 32x(0e,1o,2e), SH l<=2; "
              "0e outputs uvw with per-edge weights, 1o and 2e outputs uvu)",
+    "mixedmul": "uvu conv with blocks of different multiplicity (10k nodes x 32 in-edges, "
+                "32x0e+16x1o+16x2e, SH l<=2): the general kernels",
 }
 
 
@@ -903,6 +906,8 @@ def main():
                     help="smaller instance of the same recipe (nodes, or batch for highl)")
     ap.add_argument("--profile-run", action="store_true",
                     help="build, two warm-up steps and one step, no timing or JSON (for ncu captures)")
+    ap.add_argument("--profile-double-backward", action="store_true",
+                    help="with --profile-run: also one second-derivative call (its add kernels)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -929,6 +934,9 @@ def main():
         for _ in range(3):
             fwd(out)
             bwd(g, None)
+        if args.profile_double_backward:
+            time_double_backward(plan, graph, w, dev, g, torch.cuda.current_stream(device), units,
+                                 {"fwd_roofline_ms": 0.0, "bwd_roofline_ms": 0.0})
         torch.cuda.synchronize()
         print(f"profile run done: {args.config}, {units} units", flush=True)
         return

@@ -31,6 +31,8 @@ CSR sort, so draw i belongs to CSR position i):
 * ``uvw_edge`` the NequIP-like graph (10,000 nodes x 32 in-edges) with
   in1 = out = 16x(0e,1o,2e), SH l<=2, uvw with a weight matrix per edge,
   W ~ N(0,1)/sqrt(32) of shape [E, paths*16*16].
+* ``mixedmul`` the NequIP-like graph with in1 = 32x0e+16x1o+16x2e (blocks of
+  different multiplicity), SH l<=2, uvu with every l3 <= 2, W ~ N(0,1)/sqrt(32).
 
 Every recipe takes overrides (``N``, ``deg``, ``E``, ``B``) so tests can draw a
 smaller instance with the same structure.
@@ -171,6 +173,10 @@ SPECS = {
                                 (2, 0, 2), (2, 1, 1), (2, 2, 0), (2, 2, 2)],
                   modes=["uvw", "uvu", "uvu", "uvu", "uvw", "uvu", "uvu", "uvu", "uvu", "uvw", "uvu"],
                   lmax_sh=2, N=10_000, deg=32, graph="fixed", wscale="deg", dtype="float32"),
+    # channel-wise uvu with blocks of different multiplicity on the NequIP-like graph (the
+    # general kernels serve it: the warp-autonomous ones need one multiplicity for all blocks)
+    "mixedmul": dict(in1="32x0e+16x1o+16x2e", in2=_sh_irreps(2), out=_all_out(2), mode="uvu", lmax_sh=2,
+                     N=10_000, deg=32, graph="fixed", wscale="deg", dtype="float32"),
     # uvw with a weight matrix per edge (K = 0): 16x(0e,1o,2e) on the NequIP-like graph
     "uvw_edge": dict(in1="16x0e+16x1o+16x2e", in2=_sh_irreps(2), out="16x0e+16x1o+16x2e", mode="uvw",
                      lmax_sh=2, N=10_000, deg=32, graph="fixed", K=0, wscale="deg", dtype="float32"),
