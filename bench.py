@@ -864,6 +864,8 @@ def headline_roofline(cfgkey, r, ctx, pk, meas):
     nbytes, flops = ro[d + "_bytes"], ro[d + "_flops"]
     if plan.mode == "uvu" and "N" not in ctx[2]:
         kname = {"fwd": "bt_forward_kernel", "bwd": "bt_backward_kernel"}[d]
+    elif plan.mode == "uvu" and cfgkey == "mixedmul":   # blocks of different multiplicity: general kernels
+        kname = {"fwd": "uvu_forward2_kernel", "bwd": "uvu_backward_kernel"}[d]
     elif plan.mode == "uvu":
         kname = {"fwd": "uvu_forward3_kernel", "bwd": "uvu_backward3_kernel"}[d]
     elif plan.mode == "mixed":

@@ -669,6 +669,28 @@ struct Bwd3Args {
   int idx_cap;          // ints of dynamic shared memory for the CTA's transpose slice
 };
 
+// Per-warp ring of staged edge operands: stage j holds, for one edge of the
+// unit, the 32 * D3 output-gradient values of the unit's w range, then (at
+// kRingY) the path's harmonics (or the edge vector) and (at kRingR) the K
+// radial values.  Copies are 4-byte cp.async issued kRingDepth - 1 edges ahead
+// of the edge being computed, so the warp keeps that many edges' gathers in
+// flight without holding them in registers.
+constexpr int kRingDepth = 4;
+constexpr int kRingY = 32 * 7;               // 32 lanes x D3 (l3 <= 3)
+constexpr int kRingR = kRingY + 8;
+constexpr int kRingStage = kRingR + kKB;     // floats per stage
+constexpr int kRingWarp = kRingDepth * kRingStage;
+
+__device__ __forceinline__ void cp_async4(float* s, const float* g) {
+  const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(s));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 template <int L1, int L2, int L3, bool SH>
 __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const float* __restrict__ Rp, Rbf rbf,
                                            const float* __restrict__ gp_, const float* __restrict__ Astate,
@@ -676,10 +698,12 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
                                            float* __restrict__ gR, const int* __restrict__ t_eid,
                                            const int* __restrict__ t_dst, int tb, int te, size_t node_off,
                                            int d2, int d_out, int K, int s_slice, int off2, int ooff,
-                                           int aoff, int astr, int mul_out, int w0, int lane) {
+                                           int aoff, int astr, int mul_out, int w0, int lane, float* ring) {
   constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1;
+  constexpr int NY = SH ? 3 : D2;
   const int w = w0 + lane;
   const bool active = w < mul_out;
+  const int n_g = min(32, mul_out - w0) * D3;  // in-bounds gradient values of the unit's w range
   float A[kKB][D1], H[kKB][D1];
   const float* As = Astate + node_off + aoff + w;
 #pragma unroll
@@ -689,24 +713,49 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
       A[k][m] = (active && k < K) ? __ldg(As + k * s_slice + m * astr) : 0.f;
       H[k][m] = 0.f;
     }
+  // stage edge t into ring slot `slot`; one commit group per call (empty past te)
+  auto issue = [&](int t, int slot) {
+    if (t < te) {
+      const int e = t_eid[t], d = t_dst[t];
+      float* st = ring + slot * kRingStage;
+      const float* gsrc = gp_ + (size_t)d * d_out + ooff + w0 * D3;
+#pragma unroll
+      for (int j = 0; j < D3; ++j)
+        if (j * 32 + lane < n_g) cp_async4(st + j * 32 + lane, gsrc + j * 32 + lane);
+      if (lane < NY)
+        cp_async4(st + kRingY + lane, SH ? Yp + 3 * (size_t)e + lane : Yp + (size_t)e * d2 + off2 + lane);
+      else if (!SH && lane >= 8 && lane < 8 + K)
+        cp_async4(st + kRingR + lane - 8, Rp + (size_t)e * K + lane - 8);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kRingDepth - 1; ++i) issue(tb + i, i);
+  int slot = 0;
   for (int t = tb; t < te; ++t) {
-    const int e = t_eid[t], d = t_dst[t];  // staged in shared memory (or global)
+    // edge t's group is complete once at most kRingDepth - 2 younger groups are pending;
+    // the warp barrier also ends every lane's reads of the slot refilled below
+    cp_async_wait<kRingDepth - 2>();
+    __syncwarp();
+    issue(t + kRingDepth - 1, slot == 0 ? kRingDepth - 1 : slot - 1);
+    const float* st = ring + slot * kRingStage;
+    slot = slot + 1 == kRingDepth ? 0 : slot + 1;
+    const int e = t_eid[t];
     float yv[D2], r[kKB], gv[D3];
-    if constexpr (SH) {  // Yp holds the edge vectors: harmonics and radial basis evaluated here
-      const float rx = __ldg(Yp + 3 * (size_t)e), ry = __ldg(Yp + 3 * (size_t)e + 1), rz = __ldg(Yp + 3 * (size_t)e + 2);
+    if constexpr (SH) {  // the edge vector: harmonics and radial basis evaluated here
+      const float rx = st[kRingY], ry = st[kRingY + 1], rz = st[kRingY + 2];
       const float dd = sqrtf(rx * rx + ry * ry + rz * rz), inv = dd > 0.f ? 1.f / dd : 0.f;
       sh_block<L2, float, float>(rx * inv, ry * inv, rz * inv, yv);
 #pragma unroll
       for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? rbf_k(rbf, dd, k) : 0.f;
     } else {
 #pragma unroll
-      for (int m = 0; m < D2; ++m) yv[m] = __ldg(Yp + (size_t)e * d2 + off2 + m);
+      for (int m = 0; m < D2; ++m) yv[m] = st[kRingY + m];
 #pragma unroll
-      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? __ldg(Rp + (size_t)e * K + k) : 0.f;
+      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? st[kRingR + k] : 0.f;
     }
-    const float* gp = gp_ + (size_t)d * d_out + ooff + w * D3;
 #pragma unroll
-    for (int m = 0; m < D3; ++m) gv[m] = active ? __ldg(gp + m) : 0.f;
+    for (int m = 0; m < D3; ++m) gv[m] = active ? st[lane * D3 + m] : 0.f;
     float pe[D1];
 #pragma unroll
     for (int m = 0; m < D1; ++m) pe[m] = 0.f;
@@ -739,6 +788,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
       if (idx < D2) atomicAdd(gY + (size_t)e * d2 + off2 + idx, ht);
     }
   }
+  __syncwarp();  // the ring is reused by the warp's next unit
   if (active) {
     float* Hs = Hstate + node_off + aoff + w;
 #pragma unroll
@@ -754,17 +804,19 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
     if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
       uvw_bwd3_unit<L1, L2, L3, SH>(a.Y, a.R, a.rbf, a.g, a.Astate, a.Hstate, a.gY, a.gR, eidp, dstp,           \
                                 rp[s], rp[s + 1], (size_t)(s - a.n0) * a.s_node, a.d2, a.d_out, a.K,  \
-                                a.s_slice, p.off2, p.ooff, p.aoff, p.astr, p.mul_out, item.u0, lane); \
+                                a.s_slice, p.off2, p.ooff, p.aoff, p.astr, p.mul_out, item.u0, lane, ring); \
     break;
 
 constexpr int kBwd3Warps = 16;
 
 constexpr int kBwd3IdxInts = 16384;  // shared memory for the CTA's transpose slice (ids + receivers)
+constexpr int kBwd3RingBytes = kBwd3Warps * kRingWarp * int(sizeof(float));
 
 template <bool SH>
 __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const Bwd3Args a) {
-  extern __shared__ int bwd3_idx[];
+  extern __shared__ int bwd3_idx[];  // [idx_cap] transpose slice, then the warps' edge rings
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* ring = reinterpret_cast<float*>(bwd3_idx + a.idx_cap) + warp * kRingWarp;
   __shared__ int s_range[2];
   const int* rp = a.t_rowptr;
   if (tid == 0) {
@@ -1276,8 +1328,10 @@ cgtp_status uvw_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
     const int grid = std::min(nodes, plan->num_sms);
     const void* kb = rvec ? reinterpret_cast<const void*>(uvw_bwd_edge3_kernel<true>)
                           : reinterpret_cast<const void*>(uvw_bwd_edge3_kernel<false>);
-    b.idx_cap = smem_cap_cached(kb) >= int(kBwd3IdxInts * sizeof(int)) ? kBwd3IdxInts : 0;
-    const size_t isz = size_t(b.idx_cap) * sizeof(int);
+    const int cap = smem_cap_cached(kb);
+    if (cap < kBwd3RingBytes) return fail(CGTP_ECUDA, "uvw backward edge stage: shared memory below its edge rings");
+    b.idx_cap = cap >= int(kBwd3IdxInts * sizeof(int)) + kBwd3RingBytes ? kBwd3IdxInts : 0;
+    const size_t isz = size_t(b.idx_cap) * sizeof(int) + kBwd3RingBytes;
     if (rvec)
       uvw_bwd_edge3_kernel<true><<<grid, kBwd3Warps * 32, isz, s>>>(b);
     else

@@ -144,3 +144,47 @@ def _workload_tiny(dtype):
     spec = wl.SPECS["tiny"]
     oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvu")
     return spec, oplan, wl.make("tiny", oplan.w_numel, seed=3, dtype=dtype)
+
+
+def _run_twice(plan, graph, args, g_shape, dtype, **kw):
+    a = cg.cgtp_conv_forward(plan, graph, *args, **kw)
+    b = cg.cgtp_conv_forward(plan, graph, *args, **kw)
+    g = torch.randn(g_shape, dtype=dtype, device=DEV, generator=torch.Generator(DEV).manual_seed(11))
+    r1 = cg.cgtp_conv_backward(plan, graph, g, *args, **kw)
+    r2 = cg.cgtp_conv_backward(plan, graph, g, *args, **kw)
+    return [(a, b)] + [(u, v) for u, v in zip(r1, r2) if u is not None]
+
+
+@pytest.mark.parametrize("name,mode,dtype", [("nequip", "uvu", np.float32), ("mace", "uvu", np.float32),
+                                             ("mace", "uvu", np.float64), ("mixedmul", "uvu", np.float32),
+                                             ("uvw", "uvw", np.float32), ("uvw_edge", "uvw", np.float64)])
+def test_conv_results_are_bitwise_reproducible(name, mode, dtype):
+    """Reductions that use atomic additions (gx and gY of the uvu backward, gR and gY of the
+    radial uvw backward) add at most one value per element between two block barriers, so the
+    order of additions is fixed: two runs give identical bits."""
+    spec = wl.SPECS[name]
+    radial = name == "uvw"
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], mode)
+    w = wl.make(name, oplan.w_numel, seed=13, dtype=dtype, N=300)
+    tdt = torch.float64 if dtype == np.float64 else torch.float32
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt, radial_k=8 if radial else 0)
+    graph = cg.Graph(T(w["rowptr"]), T(w["col"]), w["N"])
+    if radial:
+        pairs = _run_twice(plan, graph, (T(w["x"]), T(w["Y"]), T(w["R"]), T(w["M"])), (w["N"], oplan.d_out), tdt)
+    else:
+        pairs = _run_twice(plan, graph, (T(w["x"]), T(w["Y"]), T(w["W"])), (w["N"], oplan.d_out), tdt)
+    for u, v in pairs:
+        assert torch.equal(u, v)
+
+
+def test_batched_results_are_bitwise_reproducible():
+    spec = wl.SPECS["highl"]
+    oplan = oirr.make_plan(spec["in1"], spec["in2"], spec["out"], "uvu")
+    w = wl.make("highl", oplan.w_numel, seed=13, B=600)
+    plan = _plan(spec)
+    x1, x2, W = T(w["x1"]), T(w["x2"]), T(w["W"])
+    a, b = cg.cgtp_forward(plan, x1, x2, W), cg.cgtp_forward(plan, x1, x2, W)
+    assert torch.equal(a, b)
+    g = torch.randn_like(a)
+    for u, v in zip(cg.cgtp_backward(plan, g, x1, x2, W), cg.cgtp_backward(plan, g, x1, x2, W)):
+        assert torch.equal(u, v)
