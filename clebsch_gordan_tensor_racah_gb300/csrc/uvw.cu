@@ -8,12 +8,14 @@
 // state, through forward and backward, keeping fully connected multiplicity
 // mixing.  With W_e[path,u,w] = sum_k R[e,k] M[k,path,u,w] (never formed):
 //
-// forward, per receiver n (edge stage, one CTA per receiver, state in shared memory):
+// forward, per receiver n (edge stage: a warp per (receiver, path, 32 channels),
+// the sums in registers, written once per node):
 //   S[n][k,path,u,m3] = sum_{e in row n} R[e,k] sum_m1 cy_e[path][m1,m3] x[src][u,m1]
 // then a node GEMM over a chunk of receivers (M shared by all nodes):
 //   out[n][i_out][w,m3] = sum_{path -> i_out} sum_{k,u} M[k,path,u,w] S[n][k,path,u,m3]
 //
-// backward, sender-owned over the transpose (no scatter, no atomics):
+// backward, sender-owned over the transpose (no scatter; gR and gY take one
+// atomic addition per element between block barriers, in a fixed order):
 //   A[s][k,path,w,m1]  = sum_u x[s][u,m1] M[k,path,u,w]                  (node GEMM)
 //   per out-edge e = (s -> d):  p_e[path,w,m1] = sum_m3 cy_e[m1,m3] g[d][w,m3]
 //     H[s][k,path,w,m1] += R[e,k] p_e
@@ -44,7 +46,6 @@ using uvu_detail::reduce_outer;
 using uvu_detail::V16;
 
 constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (cgtp_plan_set_node_chunk)
-constexpr int kEdgeChunk = 16;      // edges staged per step of the edge stages
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
 constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over nodes
 
@@ -59,7 +60,6 @@ struct UvwPath {
   int aoff;      // backward: offset of this path's w = 0, m1 = 0 inside the slice
   int sstr;      // forward: stride of m3 (the channels of every path into the block)
   int astr;      // backward: stride of m1 (the channels of every path from the in1 block)
-  int cyoff;     // per-edge cy layout offset
   int i1, io;
 };
 
@@ -81,7 +81,9 @@ struct GemmProb {
   int seg0, seg1;
   // tile loading: 0 = a warp's lanes walk K (32 consecutive k of one row / column);
   // 1 = they walk the rows of A (cols of B) at fixed k -- for operands whose K stride is large
-  unsigned char a_mode, b_mode, pad0_, pad1_;
+  unsigned char a_mode, b_mode;
+  // 16-byte copies possible: the operand is contiguous along K (k stride 1) with 4-aligned row strides
+  unsigned char a_vec, b_vec;
 };
 
 struct UvwState {
@@ -95,6 +97,8 @@ struct UvwState {
   float* scratch = nullptr;      // [2][chunk_nodes][s_node]
   float* gm_part = nullptr;      // [kGmSplits][K][w_numel] split-K partials of gM
   Item* bwd3_items = nullptr;    // (path, 32-block of mul_out) in path order
+  Item* fwd3_items = nullptr;    // (path, 32-block of mul1) in path order
+  int fwd3_n_items = 0;
   int* err_dev = nullptr;        // set by a tensor-core wait that gave up
   int* err_host = nullptr;       // pinned copy, refreshed after every call (sticky error)
   int bwd3_n_items = 0;
@@ -105,7 +109,6 @@ struct UvwState {
   GemmProb* gx_probs = nullptr;   int gx_np = 0;   GemmSeg* gx_segs = nullptr;
   GemmProb* gm_probs = nullptr;   int gm_np = 0;   GemmSeg* gm_segs = nullptr;
   void* tables = nullptr;
-  size_t smem_fwd = 0, smem_bwd = 0;
 };
 
 // ---------------------------------------------------------------------------
@@ -433,6 +436,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
 }
 
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // gM (+)= sum over the split-K partials, in split order (deterministic)
 __global__ void splitk_reduce_kernel(float* __restrict__ gM, const float* __restrict__ part, int splits,
                                      long long n, int accumulate) {
@@ -444,7 +453,7 @@ __global__ void splitk_reduce_kernel(float* __restrict__ gM, const float* __rest
 }
 
 // ---------------------------------------------------------------------------
-// forward edge stage: S[n] for the receivers of one chunk
+// edge stages
 // ---------------------------------------------------------------------------
 // Gaussian radial basis of the edge length d: R_k = exp(-gamma (d - lo - k step)^2)
 struct Rbf {
@@ -453,165 +462,6 @@ struct Rbf {
 __device__ __forceinline__ float rbf_k(const Rbf& b, float d, int k) {
   const float t = d - (b.lo + k * b.step);
   return expf(-b.gamma * t * t);
-}
-
-struct EdgeArgs {
-  const float* x;
-  const float* Y;
-  const float* R;
-  const float* rvec;   // non-null: edge vectors [E,3]; Y and R are evaluated from them
-  Rbf rbf;
-  int lmax_sh;         // in2 = harmonics 0..lmax_sh (edge-vector mode)
-  const float* g;      // backward: output gradient
-  const float* Astate; // backward: A chunk
-  float* state;        // fwd: S chunk; bwd: H chunk
-  float* gY;
-  float* gR;
-  const int* rowptr;   // fwd: CSR; bwd: transpose
-  const int* col;      // fwd: CSR col; bwd: t_eid
-  const int* t_dst;
-  int n0, n1;          // node range of this chunk
-  int d1, d2, d_out, K;
-  int s_node, s_slice;
-  const UvwPath* paths;
-  const GroupDev* group;
-  const int* cy_begin;
-  const int* cy_col;
-  const float* cy_coef;
-  const int* gy_begin;
-  const int* gy_slot;
-  const int* gy_nub;
-  const float* gy_coef;
-  const int* item_begin;
-  const Item* items;
-};
-
-template <int D1, int D3>
-__device__ __noinline__ void fwd_state_item(const float* __restrict__ x, int d1, int off1, int cyoff,
-                                            int soff, int sstr, int s_slice, int K, int u, int cnt,
-                                            const int* src_s, const float* Rs, const float* cys,
-                                            int cy_size, float* Ss) {
-  using V = float4;
-  constexpr int NF = D1 * D3;
-  constexpr int NV = (NF + 3) / 4;
-  for (int kb = 0; kb < K; kb += kKB) {
-    float acc[kKB][D3];
-#pragma unroll
-    for (int k = 0; k < kKB; ++k)
-#pragma unroll
-      for (int m = 0; m < D3; ++m) acc[k][m] = 0.f;
-    for (int j = 0; j < cnt; ++j) {
-      const float* xr = x + (size_t)src_s[j] * d1 + off1 + u * D1;
-      float xv[D1];
-#pragma unroll
-      for (int m = 0; m < D1; ++m) xv[m] = __ldg(xr + m);
-      float t[D3];
-#pragma unroll
-      for (int m = 0; m < D3; ++m) t[m] = 0.f;
-      const V* c = reinterpret_cast<const V*>(cys + j * cy_size + cyoff);
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const V cv = c[v];
-        const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int f = v * 4 + q;
-          if (f < NF) t[f % D3] += cs[q] * xv[f / D3];
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kKB; ++k) {
-        const float r = (kb + k < K) ? Rs[j * 16 + kb + k] : 0.f;
-#pragma unroll
-        for (int m = 0; m < D3; ++m) acc[k][m] += r * t[m];
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kKB; ++k) {
-      if (kb + k >= K) break;
-      float* sp = Ss + (kb + k) * s_slice + soff + u;
-#pragma unroll
-      for (int m = 0; m < D3; ++m) sp[m * sstr] += acc[k][m];
-    }
-  }
-}
-
-#define UVW_CASES(M)                                                                       \
-  M(0, 0) M(0, 1) M(0, 2) M(0, 3) M(1, 0) M(1, 1) M(1, 2) M(1, 3) M(2, 0) M(2, 1) M(2, 2) \
-  M(2, 3) M(3, 0) M(3, 1) M(3, 2) M(3, 3)
-
-#define UVW_FWD_CASE(L1, L3)                                                                     \
-  case (L1)*8 + (L3):                                                                            \
-    fwd_state_item<2 * (L1) + 1, 2 * (L3) + 1>(a.x, a.d1, p.off1, p.cyoff, p.soff, p.sstr, a.s_slice, a.K, \
-                                                u, cnt, src_s, Rs, cys, cy_size, Ss);              \
-    break;
-
-__global__ void __launch_bounds__(kThreads) uvw_fwd_edge_kernel(const EdgeArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const GroupDev g = *a.group;
-  const int cy_size = g.cy_size;
-  const int d2p = pad_up(a.d2, 4);
-  float* Ss = reinterpret_cast<float*>(smem);
-  float* Ys = Ss + pad_up(a.s_node, 4);
-  float* Rs = Ys + kEdgeChunk * d2p;
-  float* cys = Rs + kEdgeChunk * 16;
-  int* src_s = reinterpret_cast<int*>(cys + kEdgeChunk * cy_size);
-  const int ib = a.item_begin[g.item_base + warp], ie = a.item_begin[g.item_base + warp + 1];
-  for (int n = a.n0 + blockIdx.x; n < a.n1; n += gridDim.x) {
-    const int e_begin = a.rowptr[n], e_end = a.rowptr[n + 1];
-    __syncthreads();
-    for (int i = tid; i < a.s_node; i += kThreads) Ss[i] = 0.f;
-    for (int e0 = e_begin; e0 < e_end; e0 += kEdgeChunk) {
-      const int cnt = min(kEdgeChunk, e_end - e0);
-      __syncthreads();
-      for (int i = tid; i < cnt; i += kThreads) src_s[i] = a.col[e0 + i];
-      if (a.rvec) {  // harmonics and radial basis of the edge vectors, one thread per edge
-        for (int j = tid; j < cnt; j += kThreads) {
-          const float* r = a.rvec + 3 * (size_t)(e0 + j);
-          const float rx = r[0], ry = r[1], rz = r[2];
-          const float d = sqrtf(rx * rx + ry * ry + rz * rz), inv = d > 0.f ? 1.f / d : 0.f;
-          const float ux = rx * inv, uy = ry * inv, uz = rz * inv;
-          float* yj = Ys + j * d2p;
-          switch (a.lmax_sh) {
-            case 3: { float b[7]; sh_block<3, float, float>(ux, uy, uz, b); for (int m = 0; m < 7; ++m) yj[9 + m] = b[m]; } [[fallthrough]];
-            case 2: { float b[5]; sh_block<2, float, float>(ux, uy, uz, b); for (int m = 0; m < 5; ++m) yj[4 + m] = b[m]; } [[fallthrough]];
-            case 1: { float b[3]; sh_block<1, float, float>(ux, uy, uz, b); for (int m = 0; m < 3; ++m) yj[1 + m] = b[m]; } [[fallthrough]];
-            default: yj[0] = 1.f;
-          }
-          for (int k = 0; k < a.K; ++k) Rs[j * 16 + k] = rbf_k(a.rbf, d, k);
-        }
-      } else {
-        for (int i = tid; i < cnt * a.d2; i += kThreads) {
-          const int j = i / a.d2, c = i - j * a.d2;
-          Ys[j * d2p + c] = a.Y[(size_t)(e0 + j) * a.d2 + c];
-        }
-        for (int i = tid; i < cnt * a.K; i += kThreads) {
-          const int j = i / a.K, k = i - j * a.K;
-          Rs[j * 16 + k] = a.R[(size_t)(e0 + j) * a.K + k];
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < cnt * cy_size; i += kThreads) {
-        const int j = i / cy_size, s = i - j * cy_size;
-        const int t0 = a.cy_begin[g.cy_base + s], t1 = a.cy_begin[g.cy_base + s + 1];
-        float v = 0.f;
-        for (int t = t0; t < t1; ++t) v += a.cy_coef[t] * Ys[j * d2p + a.cy_col[t]];
-        cys[i] = v;
-      }
-      __syncthreads();
-      for (int it = ib; it < ie; ++it) {
-        const Item item = a.items[it];
-        const UvwPath p = a.paths[item.path];
-        const int u = item.u0 + lane;
-        if (u >= p.mul1) continue;
-        switch (p.l1 * 8 + p.l3) { UVW_CASES(UVW_FWD_CASE) default: break; }
-      }
-    }
-    __syncthreads();
-    float* dst = a.state + (size_t)(n - a.n0) * a.s_node;
-    for (int i = tid; i < a.s_node; i += kThreads) dst[i] = Ss[i];
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -685,11 +535,6 @@ __device__ __forceinline__ void cp_async4(float* s, const float* g) {
   const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(s));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(g) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 template <int L1, int L2, int L3, bool SH>
 __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const float* __restrict__ Rp, Rbf rbf,
@@ -727,7 +572,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
       else if (!SH && lane >= 8 && lane < 8 + K)
         cp_async4(st + kRingR + lane - 8, Rp + (size_t)e * K + lane - 8);
     }
-    cp_async_commit();
+    cpa_commit();
   };
 #pragma unroll
   for (int i = 0; i < kRingDepth - 1; ++i) issue(tb + i, i);
@@ -735,7 +580,7 @@ __device__ __noinline__ void uvw_bwd3_unit(const float* __restrict__ Yp, const f
   for (int t = tb; t < te; ++t) {
     // edge t's group is complete once at most kRingDepth - 2 younger groups are pending;
     // the warp barrier also ends every lane's reads of the slot refilled below
-    cp_async_wait<kRingDepth - 2>();
+    cpa_wait<kRingDepth - 2>();
     __syncwarp();
     issue(t + kRingDepth - 1, slot == 0 ? kRingDepth - 1 : slot - 1);
     const float* st = ring + slot * kRingStage;
@@ -877,6 +722,173 @@ __global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_bwd_edge3_kernel(const
   }
 }
 
+// ---------------------------------------------------------------------------
+// forward edge stage, warp-autonomous: a unit is (receiver n, path, 32
+// channels u), lanes <-> u.  Over n's in-edges, lane u sums
+//   S[k][m3] = sum_e R[e,k] t_e[m3],  t_e[m3] = sum_{m1} cy_e[m1,m3] x[src e][u,m1],
+//   cy_e[m1,m3] = sum_{m2} C[m1,m2,m3] Y[e][m2]   (compiled-in nonzeros)
+// in registers, with the edge operands staged through the warp's cp.async ring,
+// and writes its K x D3 values of the node state once.  Every unit writes
+// distinct state entries, so no reduction crosses warps; the warps of a CTA
+// take (path, receiver) units from one counter in path-major order, which keeps
+// them on one path's code at a time.
+// ---------------------------------------------------------------------------
+struct Fwd3Args {
+  const float* x;
+  const float* Y;       // edge-vector mode: the vectors [E,3]
+  const float* R;
+  Rbf rbf;
+  float* state;         // [chunk][K][s_slice]
+  const int* rowptr;
+  const int* col;
+  int n0, n1;
+  int d1, d2, K, s_node, s_slice;
+  const UvwPath* paths;
+  const Item* items;    // (path, u0), path order
+  int n_items;
+  int idx_cap;          // ints of dynamic shared memory for the CTA's CSR column slice
+};
+
+template <int L1, int L2, int L3, bool SH>
+__device__ __noinline__ void uvw_fwd3_unit(const float* __restrict__ x, const float* __restrict__ Yp,
+                                           const float* __restrict__ Rp, Rbf rbf, float* __restrict__ Sn,
+                                           const int* __restrict__ col, int eb, int ee, int d1, int d2, int K,
+                                           int s_slice, int off1, int off2, int soff, int sstr, int mul1,
+                                           int u0, int lane, float* ring) {
+  constexpr int D1 = 2 * L1 + 1, D2 = 2 * L2 + 1, D3 = 2 * L3 + 1;
+  constexpr int NY = SH ? 3 : D2;
+  const int u = u0 + lane;
+  const bool active = u < mul1;
+  const int n_x = min(32, mul1 - u0) * D1;  // in-bounds feature values of the unit's u range
+  float S[kKB][D3];
+#pragma unroll
+  for (int k = 0; k < kKB; ++k)
+#pragma unroll
+    for (int m = 0; m < D3; ++m) S[k][m] = 0.f;
+  auto issue = [&](int t, int slot) {
+    if (t < ee) {
+      float* st = ring + slot * kRingStage;
+      const float* xsrc = x + (size_t)col[t] * d1 + off1 + u0 * D1;
+#pragma unroll
+      for (int j = 0; j < D1; ++j)
+        if (j * 32 + lane < n_x) cp_async4(st + j * 32 + lane, xsrc + j * 32 + lane);
+      if (lane < NY)
+        cp_async4(st + kRingY + lane, SH ? Yp + 3 * (size_t)t + lane : Yp + (size_t)t * d2 + off2 + lane);
+      else if (!SH && lane >= 8 && lane < 8 + K)
+        cp_async4(st + kRingR + lane - 8, Rp + (size_t)t * K + lane - 8);
+    }
+    cpa_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kRingDepth - 1; ++i) issue(eb + i, i);
+  int slot = 0;
+  for (int t = eb; t < ee; ++t) {
+    cpa_wait<kRingDepth - 2>();
+    __syncwarp();
+    issue(t + kRingDepth - 1, slot == 0 ? kRingDepth - 1 : slot - 1);
+    const float* st = ring + slot * kRingStage;
+    slot = slot + 1 == kRingDepth ? 0 : slot + 1;
+    float yv[D2], r[kKB], xv[D1];
+    if constexpr (SH) {
+      const float rx = st[kRingY], ry = st[kRingY + 1], rz = st[kRingY + 2];
+      const float dd = sqrtf(rx * rx + ry * ry + rz * rz), inv = dd > 0.f ? 1.f / dd : 0.f;
+      sh_block<L2, float, float>(rx * inv, ry * inv, rz * inv, yv);
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? rbf_k(rbf, dd, k) : 0.f;
+    } else {
+#pragma unroll
+      for (int m = 0; m < D2; ++m) yv[m] = st[kRingY + m];
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) r[k] = (k < K) ? st[kRingR + k] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < D1; ++m) xv[m] = active ? st[lane * D1 + m] : 0.f;
+    float cy[D1][D3];
+#pragma unroll
+    for (int i = 0; i < D1; ++i)
+#pragma unroll
+      for (int m = 0; m < D3; ++m) cy[i][m] = 0.f;
+    CGB<L1, L2, L3>::each([&](int m1, int m2, int m3, double c) { cy[m1][m3] += float(c) * yv[m2]; });
+    float t3[D3];
+#pragma unroll
+    for (int m = 0; m < D3; ++m) {
+      t3[m] = 0.f;
+#pragma unroll
+      for (int i = 0; i < D1; ++i)
+        if ((CGB<L1, L2, L3>::mask >> (i * D3 + m)) & 1ull) t3[m] += cy[i][m] * xv[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kKB; ++k)
+#pragma unroll
+      for (int m = 0; m < D3; ++m) S[k][m] += r[k] * t3[m];
+  }
+  __syncwarp();  // the ring is reused by the warp's next unit
+  if (active) {
+    float* sp = Sn + soff + u;
+#pragma unroll
+    for (int k = 0; k < kKB; ++k)
+      if (k < K)
+#pragma unroll
+        for (int m = 0; m < D3; ++m) sp[k * s_slice + m * sstr] = S[k][m];
+  }
+}
+
+#define UVW3_FWD_CASE(L1, L2, L3)                                                                  \
+  case (L1)*16 + (L2)*4 + (L3):                                                                    \
+    if constexpr ((L3) <= 3 && (L3) >= ((L1) > (L2) ? (L1) - (L2) : (L2) - (L1)) && (L3) <= (L1) + (L2)) \
+      uvw_fwd3_unit<L1, L2, L3, SH>(a.x, a.Y, a.R, a.rbf, a.state + (size_t)(n - a.n0) * a.s_node, colp,      \
+                                a.rowptr[n], a.rowptr[n + 1], a.d1, a.d2, a.K, a.s_slice, p.off1, p.off2, \
+                                p.soff, p.sstr, p.mul1, item.u0, lane, ring);                   \
+    break;
+
+template <bool SH>
+__global__ void __launch_bounds__(kBwd3Warps * 32, 1) uvw_fwd_edge3_kernel(const Fwd3Args a) {
+  extern __shared__ int fwd3_idx[];  // [idx_cap] CSR column slice, then the warps' edge rings
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* ring = reinterpret_cast<float*>(fwd3_idx + a.idx_cap) + warp * kRingWarp;
+  __shared__ int s_range[2];
+  __shared__ int s_next;
+  const int* rp = a.rowptr;
+  if (tid == 0) {  // edge-balanced receiver range (edges + one per node)
+    const long long base = (long long)rp[a.n0] + a.n0, total = (long long)rp[a.n1] + a.n1 - base;
+    const long long t0 = base + total * blockIdx.x / gridDim.x, t1 = base + total * (blockIdx.x + 1) / gridDim.x;
+    auto lb = [&](long long target) {
+      int lo = a.n0, hi = a.n1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)rp[mid] + mid < target) lo = mid + 1; else hi = mid;
+      }
+      return lo;
+    };
+    s_range[0] = lb(t0);
+    s_range[1] = (blockIdx.x + 1 == gridDim.x) ? a.n1 : lb(t1);
+    s_next = 0;
+  }
+  __syncthreads();
+  const int rb = s_range[0], re = s_range[1], nr = re - rb;
+  const int ep0 = rp[rb], ep1 = rp[re];
+  const int* colp = a.col;
+  if (ep1 - ep0 <= a.idx_cap) {
+    for (int i = tid; i < ep1 - ep0; i += kBwd3Warps * 32) fwd3_idx[i] = __ldg(a.col + ep0 + i);
+    colp = fwd3_idx - ep0;
+  }
+  __syncthreads();
+  const long long n_units = (long long)nr * a.n_items;
+  for (;;) {
+    int k = 0;
+    if (lane == 0) k = atomicAdd(&s_next, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    if (k >= n_units) break;
+    const Item item = a.items[k / nr];
+    const int n = rb + k % nr;
+    const UvwPath p = a.paths[item.path];
+    switch (p.l1 * 16 + p.l2 * 4 + p.l3) {
+      CGTP3_TRIPLES(UVW3_FWD_CASE)
+      default: break;
+    }
+  }
+}
+
 }  // namespace uvw_detail
 
 using namespace uvw_detail;
@@ -910,12 +922,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     ibase[b] = aoff;
     aoff += Wb[b] * (2 * plan->in1[b].l + 1);
   }
-  LayoutHost lay;
-  cgtp_status s = build_layout(plan, kEdgeChunk, size_t(1) << 40, &lay);
-  if (s != CGTP_OK) return s;
-  if (lay.groups.size() != 1) return fail(CGTP_EUNSUPPORTED, "uvw plan too large");
-  // items: the uvu layout makes (path, 32-channel block of mul1) items; the
-  // backward runs over blocks of mul_out, so rebuild the item lists for it
   for (size_t i = 0; i < plan->paths.size(); ++i) {
     const auto& q = plan->paths[i];
     UvwPath u{};
@@ -935,7 +941,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
     u.aoff = ibase[q.i1] + cw[i];
     u.sstr = U[q.io];
     u.astr = Wb[q.i1];
-    u.cyoff = lay.paths[i].cyoff_g;
     u.i1 = q.i1;
     u.io = q.io;
     st->paths_h.push_back(u);
@@ -943,8 +948,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->n_paths = static_cast<int>(plan->paths.size());
   st->s_slice = std::max(soff, aoff);
   st->s_node = st->K * st->s_slice;
-  s = upload_layout(plan, lay, &plan->conv_layout);
-  if (s != CGTP_OK) return s;
   // ---- GEMM descriptors -------------------------------------------------
   // launch pointers: 0 = node state chunk, 1 = M, 2 = out / gx chunk rows,
   //                  3 = x chunk rows, 4 = gM, 5 = second node state chunk
@@ -1059,6 +1062,13 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
       const long long row_stride = P.D > 1 ? P.a_m : P.a_n;
       P.a_mode = (S.a_k > 32 && row_stride < S.a_k) ? 1 : 0;
       P.b_mode = (S.b_j == 1 && S.b_k != 1) ? 1 : 0;
+      bool av = P.a_n % 4 == 0 && (P.D == 1 || P.a_m % 4 == 0), bv = true;
+      for (int g = P.seg0; g < P.seg1; ++g) {
+        av = av && segs[g].a_k == 1;
+        bv = bv && segs[g].b_k == 1 && segs[g].b_j % 4 == 0;
+      }
+      P.a_vec = av ? 1 : 0;
+      P.b_vec = bv ? 1 : 0;
     }
   };
   set_modes(fp, fs);
@@ -1086,6 +1096,10 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   for (int p = 0; p < st->n_paths; ++p)
     for (int w0 = 0; w0 < st->paths_h[p].mul_out; w0 += 32) b3.push_back({p, w0});
   const size_t o_b3 = put(b3.data(), b3.size() * sizeof(Item));
+  std::vector<Item> f3;
+  for (int p = 0; p < st->n_paths; ++p)
+    for (int u0 = 0; u0 < st->paths_h[p].mul1; u0 += 32) f3.push_back({p, u0});
+  const size_t o_f3 = put(f3.data(), f3.size() * sizeof(Item));
   if (cudaMalloc(&st->tables, buf.size()) != cudaSuccess) return fail(CGTP_ENOMEM, "uvw tables");
   plan->device_bytes += buf.size();
   cudaMemcpy(st->tables, buf.data(), buf.size(), cudaMemcpyHostToDevice);
@@ -1101,7 +1115,11 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->gm_segs = reinterpret_cast<GemmSeg*>(at(o_ms));
   st->bwd3_items = reinterpret_cast<Item*>(at(o_b3));
   st->bwd3_n_items = int(b3.size());
-  // node-state scratch: two chunks of state (forward S; backward A and H)
+  st->fwd3_items = reinterpret_cast<Item*>(at(o_f3));
+  st->fwd3_n_items = int(f3.size());
+  // node-state scratch: two chunks of state (forward S; backward A and H), addressed
+  // with 32-bit element offsets inside a chunk
+  while ((long long)st->chunk_nodes * st->s_node >= (1ll << 31) && st->chunk_nodes > 1) st->chunk_nodes /= 2;
   st->scratch_elems = size_t(2) * st->chunk_nodes * st->s_node;
   if (cudaMalloc(&st->scratch, st->scratch_elems * sizeof(float)) != cudaSuccess)
     return fail(CGTP_ENOMEM, "uvw node-state scratch allocation failed");
@@ -1116,15 +1134,6 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   *st->err_host = 0;
   if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
     return fail(CGTP_ECUDA, "tensor-core GEMM shared memory attribute rejected");
-  // shared memory of the edge stages
-  const GroupDev& G = lay.groups[0];
-  const int d2p = pad_up(int(plan->d2), 4);
-  st->smem_fwd = sizeof(float) * (pad_up(st->s_node, 4) + kEdgeChunk * d2p + kEdgeChunk * 16 +
-                                  kEdgeChunk * G.cy_size) + sizeof(int) * kEdgeChunk;
-  if (st->smem_fwd > 227 * 1024)
-    return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
-  if (raise_smem_limit(reinterpret_cast<const void*>(uvw_fwd_edge_kernel)) < static_cast<int>(st->smem_fwd))
-    return fail(CGTP_EUNSUPPORTED, "uvw node state does not fit in shared memory");
   return CGTP_OK;
 }
 
@@ -1141,29 +1150,6 @@ void uvw_destroy(cgtp_plan_s* plan) {
 }
 
 namespace {
-EdgeArgs edge_args(const cgtp_plan_s* plan, const UvwState* st, int group) {
-  const LayoutDev& L = plan->conv_layout;
-  EdgeArgs a{};
-  a.d1 = int(plan->d1);
-  a.d2 = int(plan->d2);
-  a.d_out = int(plan->d_out);
-  a.K = st->K;
-  a.s_node = st->s_node;
-  a.s_slice = st->s_slice;
-  a.paths = st->paths;
-  a.group = L.groups + group;
-  a.cy_begin = L.cy_begin;
-  a.cy_col = L.cy_col;
-  a.cy_coef = static_cast<const float*>(L.cy_coef);
-  a.gy_begin = L.gy_begin;
-  a.gy_slot = L.gy_slot;
-  a.gy_nub = L.gy_nub;
-  a.gy_coef = static_cast<const float*>(L.gy_coef);
-  a.item_begin = L.item_begin;
-  a.items = L.items;
-  return a;
-}
-
 cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
                         const float* const ptr[6], int nodes, int tiles, cudaStream_t s, int* err,
                         long long wait_limit, int splits = 1, long long c_split_stride = 0) {
@@ -1221,6 +1207,9 @@ static int tiles_for(const cgtp_plan_s* plan, const UvwState* st, int which, int
 
 cgtp_status uvw_set_chunk(cgtp_plan_s* plan, int nodes) {
   UvwState* st = static_cast<UvwState*>(plan->uvw);
+  // the kernels address one chunk's node state with 32-bit element offsets
+  if ((long long)nodes * st->s_node >= (1ll << 31))
+    return fail(CGTP_EINVAL, "uvw node chunk too large: chunk x node-state size must stay below 2^31 elements");
   const size_t elems = size_t(2) * nodes * st->s_node;
   float* p = nullptr;
   if (cudaMalloc(&p, elems * sizeof(float)) != cudaSuccess) {
@@ -1257,23 +1246,40 @@ cgtp_status uvw_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const vo
   const UvwState* st = static_cast<const UvwState*>(plan->uvw);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cgtp_status e = sticky_error(st)) return e;
-  EdgeArgs a = edge_args(plan, st, 0);
+  if ((long long)st->chunk_nodes * st->fwd3_n_items >= (1ll << 31))
+    return fail(CGTP_EUNSUPPORTED, "uvw forward: node chunk x channel blocks exceeds the 32-bit unit counter");
+  Fwd3Args a{};
   a.x = static_cast<const float*>(x);
-  a.Y = static_cast<const float*>(Y);
+  a.Y = static_cast<const float*>(rvec ? rvec : Y);
   a.R = static_cast<const float*>(R);
-  a.rvec = static_cast<const float*>(rvec);
   a.rbf = make_rbf(st->K, rbf_lo, rbf_hi);
-  a.lmax_sh = static_cast<int>(plan->in2.size()) - 1;
+  a.state = st->scratch;
   a.rowptr = g->rowptr;
   a.col = g->col;
-  a.state = st->scratch;
+  a.d1 = static_cast<int>(plan->d1);
+  a.d2 = static_cast<int>(plan->d2);
+  a.K = st->K;
+  a.s_node = st->s_node;
+  a.s_slice = st->s_slice;
+  a.paths = st->paths;
+  a.items = st->fwd3_items;
+  a.n_items = st->fwd3_n_items;
+  const void* kf = rvec ? reinterpret_cast<const void*>(uvw_fwd_edge3_kernel<true>)
+                        : reinterpret_cast<const void*>(uvw_fwd_edge3_kernel<false>);
+  const int cap = smem_cap_cached(kf);
+  if (cap < kBwd3RingBytes) return fail(CGTP_ECUDA, "uvw forward edge stage: shared memory below its edge rings");
+  a.idx_cap = cap >= int(kBwd3IdxInts * sizeof(int)) + kBwd3RingBytes ? kBwd3IdxInts : 0;
+  const size_t fsz = size_t(a.idx_cap) * sizeof(int) + kBwd3RingBytes;
   for (int64_t n0 = 0; n0 < g->N; n0 += st->chunk_nodes) {
     const int n1 = static_cast<int>(std::min<int64_t>(g->N, n0 + st->chunk_nodes));
     a.n0 = static_cast<int>(n0);
     a.n1 = n1;
     const int nodes = n1 - a.n0;
-    const int grid = std::min(nodes, plan->num_sms * 2);
-    uvw_fwd_edge_kernel<<<grid, kThreads, st->smem_fwd, s>>>(a);
+    const int grid = std::min(nodes, plan->num_sms);
+    if (rvec)
+      uvw_fwd_edge3_kernel<true><<<grid, kBwd3Warps * 32, fsz, s>>>(a);
+    else
+      uvw_fwd_edge3_kernel<false><<<grid, kBwd3Warps * 32, fsz, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return fail(CGTP_ECUDA, "uvw forward edge stage launch failed");
     const float* ptr[6] = {st->scratch, static_cast<const float*>(M),
                            static_cast<float*>(out) + (size_t)n0 * plan->d_out, nullptr, nullptr, nullptr};

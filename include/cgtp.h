@@ -169,8 +169,10 @@ cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls);
  * plan-owned scratch of 2 * nodes * K * sum_path(mul * (2l+1)) floats: the
  * forward and the backward walk the graph `nodes` receivers (senders) at a
  * time.  cgtp_plan_set_node_chunk replaces the scratch (it waits for work still
- * using the old one); nodes in [1, 1048576], default 4096.  CGTP_EINVAL for
- * other plans or sizes, CGTP_ENOMEM when the scratch cannot be allocated.
+ * using the old one); nodes in [1, 1048576] with nodes * K * sum_path(mul *
+ * (2l+1)) below 2^31 (one chunk's state is addressed with 32-bit offsets),
+ * default 4096 (halved at plan creation until that bound holds).  CGTP_EINVAL
+ * for other plans or sizes, CGTP_ENOMEM when the scratch cannot be allocated.
  * cgtp_plan_node_chunk reports the chunk (0 for plans without node state).
  */
 cgtp_status cgtp_plan_set_node_chunk(cgtp_plan plan, int64_t nodes);

@@ -86,6 +86,7 @@ def test_wait_limit_and_node_chunk_reject_bad_values():
     plan = _uvw_plan(spec)
     for call in (lambda: plan.set_wait_limit(-1), lambda: plan.set_node_chunk(0),
                  lambda: plan.set_node_chunk((1 << 20) + 1),
+                 lambda: plan.set_node_chunk(200_000),   # 200k x 17,920 state values per node > 2^31
                  lambda: _plan(wl.SPECS["nequip"]).set_node_chunk(64)):   # uvu plans have no node state
         with pytest.raises(cg.CgtpError) as e:
             call()
