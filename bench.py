@@ -65,6 +65,7 @@ CONFIGS = {
 }
 # the benchmark's five workloads besides the headline
 PER_CONFIG = ["tiny", "mace", "mace64", "highl", "uvw"]
+NODE_CHUNK = None                 # --node-chunk: node chunk of radial uvw plans (None: the plan's default)
 L2_BYTES = 126 * 2 ** 20          # GB300 L2 (about 126 MiB usable)
 FLUSH_BYTES = 512 * 2 ** 20       # buffer written between timed steps when flushing L2
 
@@ -189,6 +190,8 @@ def build_inputs(cfgkey, device, nodes=None):
     else:
         plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], mode, tdt,
                        radial_k=spec.get("K", 0) if mode == "uvw" else 0)
+        if NODE_CHUNK and plan.radial_k:
+            plan.set_node_chunk(NODE_CHUNK)
         w_numel = plan.w_numel
     over = {}
     if nodes:
@@ -504,6 +507,7 @@ def run_config(cfgkey, device, steps, warmup, meas, pk, flush_l2=None, nodes=Non
     else:
         r.update(batch=int(w["B"]))
     if cfgkey == "uvw":
+        r["node_chunk"] = plan.node_chunk
         lib_bytes = plan.device_bytes() + graph.device_bytes()
         r["peak_memory"] = {
             "torch_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(device)),
@@ -904,6 +908,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-double-backward", action="store_true",
                     help="skip the (untimed-for-the-metric) second-derivative measurement")
+    ap.add_argument("--node-chunk", type=int, default=None,
+                    help="node chunk of radial uvw plans (cgtp_plan_set_node_chunk; default: the plan's)")
     ap.add_argument("--nodes", type=int, default=None,
                     help="smaller instance of the same recipe (nodes, or batch for highl)")
     ap.add_argument("--profile-run", action="store_true",
@@ -911,6 +917,8 @@ def main():
     ap.add_argument("--profile-double-backward", action="store_true",
                     help="with --profile-run: also one second-derivative call (its add kernels)")
     args = ap.parse_args()
+    global NODE_CHUNK
+    NODE_CHUNK = args.node_chunk
     if args.impl == "reference":
         return run_reference(args)
 

@@ -45,7 +45,7 @@ using uvu_detail::pad_up;
 using uvu_detail::reduce_outer;
 using uvu_detail::V16;
 
-constexpr int kChunkNodes = 4096;   // default nodes per streamed chunk (cgtp_plan_set_node_chunk)
+constexpr int kChunkPerSm = 128;    // default nodes per streamed chunk, per SM (cgtp_plan_set_node_chunk)
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
 constexpr int kGmSplits = 16;       // split-K factor of the gM reduction over nodes
 
@@ -93,7 +93,7 @@ struct UvwState {
   int K = 0;
   int s_slice = 0, a_slice = 0;  // elements of one radial slice of the node state
   int s_node = 0, a_node = 0;    // K * slice
-  int chunk_nodes = kChunkNodes;
+  int chunk_nodes = 0;
   float* scratch = nullptr;      // [2][chunk_nodes][s_node]
   float* gm_part = nullptr;      // [kGmSplits][K][w_numel] split-K partials of gM
   Item* bwd3_items = nullptr;    // (path, 32-block of mul_out) in path order
@@ -127,6 +127,8 @@ struct UvwState {
 constexpr int kTM = 128, kTN = 64, kTK = 32;
 constexpr int kATile = kTM * kTK * 4, kBTile = kTN * kTK * 4;
 constexpr int kTcSmem = 2 * (2 * kATile + 2 * kBTile) + 1024 + 64;  // two stages
+// dynamic shared memory of a launch over np problems: the above plus the tile prefix
+inline size_t gemm_smem(int np) { return kTcSmem + sizeof(int) * size_t(np + 1); }
 constexpr long long kTcCleanupPolls = 1ll << 24;                     // bounded clean-up wait
 
 struct GemmLaunch {
@@ -189,11 +191,20 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   constexpr int kStage = 2 * kATile + 2 * kBTile;
   uint64_t* mbar = (uint64_t*)(sm + 2 * kStage);         // one per stage
   uint32_t* tmem_holder = (uint32_t*)(sm + 2 * kStage + 16);
+  int* t0 = reinterpret_cast<int*>(sm + 2 * kStage + 64);  // [nprob + 1]: first tile of each problem
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < L.nprob; i += kTcWarps * 32) {
+    const GemmProb& Q = L.probs[i];
+    const int rows = (Q.Nn < 0 ? L.nodes : Q.Nn) * Q.D;
+    t0[i + 1] = ((rows + kTM - 1) / kTM) * ((Q.J + kTN - 1) / kTN);
+  }
+  __syncthreads();
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
     asm volatile("fence.mbarrier_init.release.cluster;");
+    t0[0] = 0;
+    for (int i = 0; i < L.nprob; ++i) t0[i + 1] += t0[i];
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)), "r"(64));
@@ -212,21 +223,18 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   const int slice = (L.nodes + L.splits - 1) / L.splits;
   // persistent: this CTA takes tiles blockIdx.x, + gridDim.x, ... of the launch
   for (int tile_g = blockIdx.x; tile_g < L.tiles && ok; tile_g += gridDim.x) {
-  // locate the tile's problem (uniform over the CTA)
-  int tile = tile_g, pi = 0, rt = 0, ct = 0;
-  GemmProb P;
-  for (pi = 0; pi < L.nprob; ++pi) {
-    P = L.probs[pi];
-    const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
-    const int ntr = (rows + kTM - 1) / kTM, ntc = (P.J + kTN - 1) / kTN;
-    if (tile < ntr * ntc) {
-      rt = tile / ntc;
-      ct = tile - rt * ntc;
-      break;
+  // locate the tile's problem (uniform over the CTA): binary search of the tile prefix
+  if (tile_g >= t0[L.nprob]) break;
+  int pi = 0;
+  {
+    int hi = L.nprob - 1;
+    while (pi < hi) {  // last problem whose first tile is <= tile_g
+      const int mid = (pi + hi + 1) >> 1;
+      if (t0[mid] <= tile_g) pi = mid; else hi = mid - 1;
     }
-    tile -= ntr * ntc;
   }
-  if (pi >= L.nprob) break;
+  const GemmProb P = L.probs[pi];
+  const int ntc = (P.J + kTN - 1) / kTN, rt = (tile_g - t0[pi]) / ntc, ct = tile_g - t0[pi] - rt * ntc;
   const int rows = (P.Nn < 0 ? L.nodes : P.Nn) * P.D;
   const float* A = L.ptr[P.a_base];
   const float* B = L.ptr[P.b_base];
@@ -1119,6 +1127,7 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
   st->fwd3_n_items = int(f3.size());
   // node-state scratch: two chunks of state (forward S; backward A and H), addressed
   // with 32-bit element offsets inside a chunk
+  st->chunk_nodes = kChunkPerSm * std::max(1, plan->num_sms);
   while ((long long)st->chunk_nodes * st->s_node >= (1ll << 31) && st->chunk_nodes > 1) st->chunk_nodes /= 2;
   st->scratch_elems = size_t(2) * st->chunk_nodes * st->s_node;
   if (cudaMalloc(&st->scratch, st->scratch_elems * sizeof(float)) != cudaSuccess)
@@ -1132,7 +1141,11 @@ cgtp_status uvw_create(cgtp_plan_s* plan) {
                         sizeof(int);
   cudaMemset(st->err_dev, 0, sizeof(int));
   *st->err_host = 0;
-  if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+  const int np_max = std::max(std::max(st->fwd_np, st->pre_np), std::max(st->gx_np, st->gm_np));
+  if (gemm_smem(np_max) > 113 * 1024)  // two CTAs per SM
+    return fail(CGTP_EUNSUPPORTED, "uvw plan has too many GEMM problems for the tile table");
+  if (cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(gemm_smem(np_max))) != cudaSuccess)
     return fail(CGTP_ECUDA, "tensor-core GEMM shared memory attribute rejected");
   return CGTP_OK;
 }
@@ -1168,7 +1181,7 @@ cgtp_status launch_gemm(const GemmProb* probs_dev, int np, const GemmSeg* segs,
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::max(1, std::min(tiles, 2 * nsm));  // two CTAs per SM, persistent
-  grouped_gemm_tc_kernel<<<dim3(grid, splits), kTcWarps * 32, kTcSmem, s>>>(L);
+  grouped_gemm_tc_kernel<<<dim3(grid, splits), kTcWarps * 32, gemm_smem(np), s>>>(L);
   return cudaGetLastError() == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, "uvw gemm launch failed");
 }
 

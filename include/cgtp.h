@@ -90,9 +90,10 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      Figure 3B/C), or the number K of radial functions (1..8), the weights
  *      then being W_e = R[e,:] @ M with M [K, sum_path mul1*mul_out].
  * Creates device tables (a few KB) and, for uvw, the bounded scratch used by
- * the streaming node stage: node state for a chunk of nodes (default 4096,
- * cgtp_plan_set_node_chunk changes it), 2 x chunk x K x sum_path mul*(2l+1)
- * floats (~590 MB for 64x(0e,1o,2e), K = 8 at the default chunk).  uvw
+ * the streaming node stage: node state for a chunk of nodes (default 128 per
+ * SM, 19,456 on a 152-SM GPU; cgtp_plan_set_node_chunk changes it),
+ * 2 x chunk x K x sum_path mul*(2l+1) floats (2.8 GB for 64x(0e,1o,2e), K = 8
+ * at the default chunk on 152 SMs).  uvw
  * limits: l <= 3, K <= 8.  Must be called with the target device current.
  */
 cgtp_status cgtp_plan_create(cgtp_plan* plan, const char* irreps_in1, const char* irreps_in2,
@@ -171,7 +172,8 @@ cgtp_status cgtp_plan_set_wait_limit(cgtp_plan plan, int64_t polls);
  * time.  cgtp_plan_set_node_chunk replaces the scratch (it waits for work still
  * using the old one); nodes in [1, 1048576] with nodes * K * sum_path(mul *
  * (2l+1)) below 2^31 (one chunk's state is addressed with 32-bit offsets),
- * default 4096 (halved at plan creation until that bound holds).  CGTP_EINVAL
+ * default 128 x the SM count (halved at plan creation until that bound
+ * holds).  CGTP_EINVAL
  * for other plans or sizes, CGTP_ENOMEM when the scratch cannot be allocated.
  * cgtp_plan_node_chunk reports the chunk (0 for plans without node state).
  */

@@ -102,7 +102,8 @@ def test_uvw_full_size_sampled():
     torch.cuda.reset_peak_memory_stats()
     out = cg.cgtp_conv_forward(plan, graph, d["x"], d["Y"], d["R"], d["M"])
     rng = np.random.default_rng(11)
-    nodes = np.concatenate([[0, 1, 4095, 4096, 4097, 199_999], rng.integers(0, 200_000, 10)])
+    c = plan.node_chunk   # rows on both sides of the first chunk boundary
+    nodes = np.concatenate([[0, 1, c - 1, c, c + 1, 199_999], rng.integers(0, 200_000, 10)])
     ref = oconv.conv_uvw_radial_forward(oplan, w["x"], w["Y"], w["R"], w["M"], w["rowptr"], w["col"], nodes=nodes)
     close("out[sampled]", out[torch.from_numpy(nodes).cuda()], ref)
     g = torch.randn(out.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(5))
@@ -115,7 +116,7 @@ def test_uvw_full_size_sampled():
     close("gY[sampled]", gY[torch.from_numpy(edges).cuda()], rgY)
     close("gR[sampled]", gR[torch.from_numpy(edges).cuda()], rgR)
     t_rowptr, t_eid, _ = ograph.transpose(w["rowptr"], w["col"], w["N"])
-    senders = np.array([3, 4096, 150_000])
+    senders = np.array([3, c, 150_000])
     sedges = np.concatenate([t_eid[t_rowptr[s]:t_rowptr[s + 1]] for s in senders])
     rgx, _, _, _ = oconv.conv_uvw_radial_backward(oplan, gh, w["x"], w["Y"], w["R"], w["M"], w["rowptr"],
                                                   w["col"], edges=sedges)
