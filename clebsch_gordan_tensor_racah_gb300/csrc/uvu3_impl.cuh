@@ -32,6 +32,7 @@ __host__ __device__ inline int pad_up(int v, int q) { return (v + q - 1) / q * q
 // one 16-warp CTA per SM: the whole SM walks one path at a time
 constexpr int kV3Warps = 16;
 constexpr int kV3Threads = kV3Warps * 32;
+constexpr int kV3OrderCap = 512;  // senders a backward CTA orders longest first
 
 template <typename T>
 struct PairT;
@@ -569,12 +570,29 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
       a.gY[(size_t)a.col[tb + j] * a.d2 + c] = T(0);
     }
   }
+  // The CTA's senders longest first (out-degree, then index): a phase then ends
+  // with its shortest units, so fewer warps wait at the phase barrier.  (A rank
+  // sort in shared memory, for ranges of up to kV3OrderCap senders.)
+  __shared__ int s_order[kV3OrderCap];
+  const bool ordered = nr <= kV3OrderCap;
+  if (ordered) {
+    for (int i = tid; i < nr; i += kV3Threads) {
+      const int di = a.rowptr[sb + i + 1] - a.rowptr[sb + i];
+      int rank = 0;
+      for (int j = 0; j < nr; ++j) {
+        const int dj = a.rowptr[sb + j + 1] - a.rowptr[sb + j];
+        rank += (dj > di) || (dj == di && j < i);
+      }
+      s_order[rank] = i;
+    }
+    __syncthreads();
+  }
   // Items come in phases whose items share no in1 block and no in2 block, so
   // within a phase every gx / gY slice has one writer; a block barrier separates
   // the phases, and every gx / gY element receives its contributions in phase
-  // order (deterministic).  Inside a phase a counter hands out (sender, item)
-  // pairs sender-major: the phase's few paths share the instruction cache and
-  // a sender's operands stay in L1.
+  // order (deterministic, whatever order the units of a phase run in).  Inside a
+  // phase a counter hands out (sender, item) pairs sender-major: the phase's few
+  // paths share the instruction cache and a sender's operands stay in L1.
   __shared__ int s_next[2];
   for (int ph = 0; ph < a.n_phases; ++ph) {
     const int i0 = a.phase_begin[ph], ni = a.phase_begin[ph + 1] - i0;
@@ -587,7 +605,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_backward3_kernel(const Uvu3
       k = __shfl_sync(0xffffffffu, k, 0);
       if (k >= total) break;
       const int sl = k / ni, ii = k - sl * ni;
-      const int s = sb + sl;
+      const int s = sb + (ordered ? s_order[sl] : sl);
       const Item item = a.items[i0 + ii];
       const PathDev p = a.paths[item.path];
       const int u = item.u0 + 4 * q;
