@@ -27,8 +27,10 @@
  *  - Arguments are validated on the host before anything is launched; a
  *    failed check returns a status and launches nothing.  cgtp_last_error()
  *    returns a message for the last failure of the calling thread.
- *  - Results are bitwise deterministic run to run (no atomics in any
- *    floating-point accumulation).
+ *  - Results are bitwise deterministic run to run: where a backward reduction
+ *    uses floating-point atomic additions (gx, gY of the uvu kernels; gR, gY
+ *    of the radial uvw edge stage), each element receives at most one
+ *    addition between two block barriers, so the order of additions is fixed.
  *  - A plan holds device state used by its launches (work counters of the
  *    batched kernels, the uvw node-state scratch): calls that use the same
  *    plan must not overlap on the GPU (issue them on one stream).
