@@ -60,6 +60,7 @@ CONFIGS = {
     "uvw_edge": dict(name="uvw_edge", dtype="float32"),
     "mixed": dict(name="mixed", dtype="float32"),
     "nequip_bf16": dict(name="nequip", dtype="bfloat16"),
+    "highl_bf16": dict(name="highl", dtype="bfloat16"),
     "nequip_sh": dict(name="nequip", dtype="float32", sh=True),
     "mixedmul": dict(name="mixedmul", dtype="float32"),
 }
@@ -279,8 +280,9 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
     else:
         B = w["B"]
         units = B
-        bf = es * (B * (plan.d1 + plan.d2 + plan.w_numel + plan.d_out))
-        bb = es * (B * (2 * plan.d1 + 2 * plan.d2 + 2 * plan.w_numel + plan.d_out))
+        nin = B * (plan.d1 + plan.d2 + plan.w_numel)
+        bf = ei * nin + es * B * plan.d_out                    # inputs read, output written
+        bb = ei * (nin + B * plan.d_out) + es * nin            # inputs + gradient read, gradients written
 
         def fwd(out, d=dev):
             return cg.cgtp_forward(plan, d["x1"], d["x2"], d["W"], out=out)

@@ -286,19 +286,21 @@ def cgtp_forward(plan, x1, x2, W, out=None, stream=None):
     torch = _torch()
     B = x1.shape[0]
     if out is None:
-        out = torch.empty(B, plan.d_out, dtype=plan.dtype, device=x1.device)
+        out = torch.empty(B, plan.d_out, dtype=plan.out_dtype, device=x1.device)
     _check(lib().cgtp_forward(plan.handle, _ptr(x1, "x1", plan.dtype), _ptr(x2, "x2", plan.dtype),
-                              _ptr(W, "W", plan.dtype), _ptr(out, "out", plan.dtype), B, _stream(stream)))
+                              _ptr(W, "W", plan.dtype), _ptr(out, "out", plan.out_dtype), B, _stream(stream)))
     return out
 
 
 def cgtp_backward(plan, gout, x1, x2, W, stream=None):
     torch = _torch()
     B = x1.shape[0]
-    gx1, gx2, gW = torch.empty_like(x1), torch.empty_like(x2), torch.empty_like(W)
+    od = plan.out_dtype   # bfloat16 plans write FP32 gradients
+    gx1, gx2, gW = (torch.empty(t.shape, dtype=od, device=t.device) for t in (x1, x2, W))
     _check(lib().cgtp_backward(plan.handle, _ptr(gout, "gout", plan.dtype), _ptr(x1, "x1", plan.dtype),
                                _ptr(x2, "x2", plan.dtype), _ptr(W, "W", plan.dtype),
-                               _ptr(gx1, "gx1"), _ptr(gx2, "gx2"), _ptr(gW, "gW"), B, _stream(stream)))
+                               _ptr(gx1, "gx1", od), _ptr(gx2, "gx2", od), _ptr(gW, "gW", od), B,
+                               _stream(stream)))
     return gx1, gx2, gW
 
 

@@ -222,9 +222,10 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (s == CGTP_OK) s = upload_layout(p, batch, &p->batch_layout);
     if (s == CGTP_OK) s = build_v3(p);
     if (s == CGTP_OK) s = bt_create(p);
-    if (s == CGTP_OK && dtype == CGTP_BF16 && !p->v3.lpe)
+    if (s == CGTP_OK && dtype == CGTP_BF16 && !p->v3.lpe && !p->bt)
       s = fail(CGTP_EUNSUPPORTED, "CGTP_BF16 needs l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} "
-                                  "or m a multiple of 128");
+                                  "or m a multiple of 128 (graph convolutions), or multiplicity 16 or 32 in "
+                                  "every path and l <= 7 (batched products)");
   } else if (radial_k == 0) {
     s = uvwe_create(p);
   } else {
@@ -319,12 +320,14 @@ cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const v
   clear_error();
   if (!plan) return fail(CGTP_EINVAL, "null plan");
   if (plan->mode != CGTP_UVU) return fail(CGTP_EUNSUPPORTED, "cgtp_forward needs a uvu plan");
-  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "the batched product has no CGTP_BF16 kernels");
+  if (plan->dtype == CGTP_BF16 && !plan->bt)
+    return fail(CGTP_EUNSUPPORTED, "CGTP_BF16 batched products need multiplicity 16 or 32 in every path and l <= 7");
   if (B < 0 || B >= (int64_t(1) << 31)) return fail(CGTP_EINVAL, "batch size out of range");
   if (B == 0) return CGTP_OK;
   cgtp_status s;
   if ((s = need(x1, "x1")) || (s = need(x2, "x2")) || (s = need(W, "W")) || (s = need(out, "out"))) return s;
   if (bt_forward(plan, x1, x2, W, out, B, stream, &s)) return s;
+  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "batch too large for the CGTP_BF16 batched kernels");
   return launch_uvu_forward(plan, plan->batch_layout, x1, x2, W, out, nullptr, nullptr, B, true, stream);
 }
 
@@ -333,7 +336,8 @@ cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, cons
   clear_error();
   if (!plan) return fail(CGTP_EINVAL, "null plan");
   if (plan->mode != CGTP_UVU) return fail(CGTP_EUNSUPPORTED, "cgtp_backward needs a uvu plan");
-  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "the batched product has no CGTP_BF16 kernels");
+  if (plan->dtype == CGTP_BF16 && !plan->bt)
+    return fail(CGTP_EUNSUPPORTED, "CGTP_BF16 batched products need multiplicity 16 or 32 in every path and l <= 7");
   if (B < 0 || B >= (int64_t(1) << 31)) return fail(CGTP_EINVAL, "batch size out of range");
   if (B == 0) return CGTP_OK;
   cgtp_status s;
@@ -341,6 +345,7 @@ cgtp_status cgtp_backward(cgtp_plan plan, const void* gout, const void* x1, cons
       (s = need(gx1, "gx1")) || (s = need(gx2, "gx2")) || (s = need(gW, "gW")))
     return s;
   if (bt_backward(plan, gout, x1, x2, W, gx1, gx2, gW, B, stream, &s)) return s;
+  if (plan->dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "batch too large for the CGTP_BF16 batched kernels");
   return launch_uvu_backward(plan, plan->batch_layout, gout, x1, x2, W, gx1, gx2, gW, nullptr, nullptr,
                              nullptr, B, true, stream);
 }

@@ -38,7 +38,10 @@
 // changes.  Backward unit: a 32-sample batch that the CTA walks through all
 // groups (reloading the tables), so gx and gy of a sample are owned by one
 // warp: deterministic, no floating-point atomics, no scratch.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include <algorithm>
 #include <cmath>
@@ -77,10 +80,10 @@ struct BtGroup {
 };
 
 struct BtArgs {
-  const float* x;
-  const float* y;
-  const float* W;
-  const float* gout;
+  const void* x;     // inputs and output gradient: float, or bfloat16 for CGTP_BF16 plans
+  const void* y;
+  const void* W;
+  const void* gout;
   float* out;
   float* gx;
   float* gy;
@@ -123,8 +126,19 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
   return *reinterpret_cast<float2*>(&d);
 }
-__device__ __forceinline__ float2 ld_pair(const float* a, const float* b, bool va, bool vb) {
-  return make_float2(va ? __ldg(a) : 0.f, vb ? __ldg(b) : 0.f);
+// element i of a float or bfloat16 array as float (bfloat16 widens exactly)
+template <typename S>
+__device__ __forceinline__ float ld_s(const void* base, size_t i) {
+  if constexpr (std::is_same<S, float>::value) {
+    return __ldg(static_cast<const float*>(base) + i);
+  } else {
+    return __uint_as_float(static_cast<unsigned>(__ldg(static_cast<const unsigned short*>(base) + i)) << 16);
+  }
+}
+// elements ia and ib of `base` for the two samples of a pair (zero where invalid)
+template <typename S>
+__device__ __forceinline__ float2 ld_pair(const void* base, size_t ia, size_t ib, bool va, bool vb) {
+  return make_float2(va ? ld_s<S>(base, ia) : 0.f, vb ? ld_s<S>(base, ib) : 0.f);
 }
 
 // Group tables into shared memory: paths, cy entries [, gy row pointers, gy entries].
@@ -160,29 +174,29 @@ __device__ __forceinline__ void coupling(const BtPath& p, const float4* sc, cons
 }
 
 // x of the lane's channel for both samples of the pair (zero past D1)
-template <int Q>
+template <int Q, typename S>
 __device__ __forceinline__ void load_x2(const BtArgs& a, const BtPath& p, int b0, int b1, bool v0, bool v1,
                                         int u, float2 (&x2)[4 * Q]) {
-  const float* xa = a.x + (size_t)b0 * a.d1 + p.off1 + u * p.D1;
-  const float* xb = a.x + (size_t)b1 * a.d1 + p.off1 + u * p.D1;
+  const size_t xa = (size_t)b0 * a.d1 + p.off1 + u * p.D1;
+  const size_t xb = (size_t)b1 * a.d1 + p.off1 + u * p.D1;
 #pragma unroll
-  for (int m = 0; m < 4 * Q; ++m) x2[m] = ld_pair(xa + m, xb + m, v0 && m < p.D1, v1 && m < p.D1);
+  for (int m = 0; m < 4 * Q; ++m) x2[m] = ld_pair<S>(a.x, xa + m, xb + m, v0 && m < p.D1, v1 && m < p.D1);
 }
 
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
-template <int LPP, int Q>
+template <int LPP, int Q, typename S>
 __device__ __forceinline__ void fwd_run(const BtArgs& a, const BtPath* sp, int n, const float4* sc,
                                         const float2* y2, float2* cy2, float* t0, float* t1, int b0, int b1,
                                         bool v0, bool v1, int u) {
   constexpr int D1P = 4 * Q;
   float2 x2[D1P];
-  load_x2<Q>(a, sp[0], b0, b1, v0, v1, u, x2);
+  load_x2<Q, S>(a, sp[0], b0, b1, v0, v1, u, x2);
   for (int k = 0; k < n; ++k) {
     const BtPath p = sp[k];
-    const float2 w2 = ld_pair(a.W + (size_t)b0 * a.w_numel + p.woff + u,
-                              a.W + (size_t)b1 * a.w_numel + p.woff + u, v0, v1);
+    const float2 w2 = ld_pair<S>(a.W, (size_t)b0 * a.w_numel + p.woff + u, (size_t)b1 * a.w_numel + p.woff + u,
+                                 v0, v1);
     coupling<LPP, Q>(p, sc, y2, cy2, u);
     __syncwarp();
     // D3 = 2 l3 + 1 is odd: (D3 - 1) / 2 guarded row pairs and the last row,
@@ -221,7 +235,7 @@ __device__ __forceinline__ void fwd_run(const BtArgs& a, const BtPath* sp, int n
   }
 }
 
-template <int LPP>
+template <int LPP, typename S>
 __global__ void __launch_bounds__(kBtThreads, 2) bt_forward_kernel(const BtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int PPW = 32 / LPP;
@@ -260,15 +274,15 @@ __global__ void __launch_bounds__(kBtThreads, 2) bt_forward_kernel(const BtArgs 
     const bool v0 = s0 < a.B, v1 = s1 < a.B;
     const int b0 = v0 ? s0 : base, b1 = v1 ? s1 : base;
     for (int i = u; i < a.d2; i += LPP)
-      y2[i] = ld_pair(a.y + (size_t)b0 * a.d2 + i, a.y + (size_t)b1 * a.d2 + i, v0, v1);
+      y2[i] = ld_pair<S>(a.y, (size_t)b0 * a.d2 + i, (size_t)b1 * a.d2 + i, v0, v1);
     __syncwarp();
     for (int pi = 0; pi < np;) {
       const int n = sp[pi].run;
       switch (sp[pi].Q) {
-        case 1: fwd_run<LPP, 1>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
-        case 2: fwd_run<LPP, 2>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
-        case 3: fwd_run<LPP, 3>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
-        default: fwd_run<LPP, 4>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        case 1: fwd_run<LPP, 1, S>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        case 2: fwd_run<LPP, 2, S>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        case 3: fwd_run<LPP, 3, S>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
+        default: fwd_run<LPP, 4, S>(a, sp + pi, n, sc, y2, cy2, t0, t1, b0, b1, v0, v1, u); break;
       }
       pi += n;
     }
@@ -278,30 +292,31 @@ __global__ void __launch_bounds__(kBtThreads, 2) bt_forward_kernel(const BtArgs 
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
-template <int LPP, int Q>
+template <int LPP, int Q, typename S>
 __device__ __forceinline__ void bwd_run(const BtArgs& a, const BtPath* sp, int n, const float4* sc,
                                         const int* sgrow, const float2* sgent, const float2* y2, float2* gy2,
                                         float2* cy2, float2* wg2, int b0, int b1, bool v0, bool v1, int u) {
   constexpr int D1P = 4 * Q;
   const BtPath p0 = sp[0];
   float2 x2[D1P], gxa[D1P];
-  load_x2<Q>(a, p0, b0, b1, v0, v1, u, x2);
+  load_x2<Q, S>(a, p0, b0, b1, v0, v1, u, x2);
 #pragma unroll
   for (int m = 0; m < D1P; ++m) gxa[m] = make_float2(0.f, 0.f);
-  const float* xa = a.x + (size_t)b0 * a.d1 + p0.off1;
-  const float* xb = a.x + (size_t)b1 * a.d1 + p0.off1;
+  const size_t xa = (size_t)b0 * a.d1 + p0.off1;
+  const size_t xb = (size_t)b1 * a.d1 + p0.off1;
   // G stage lanes: m1 = u % 16, channel half h = u / 16 (multiplicity 32 only)
   const int gm1 = u & 15, gh = u >> 4;
   const unsigned gmask = LPP == 32 ? (((1u << p0.D1) - 1u) | (((1u << p0.D1) - 1u) << 16)) : 0u;
   for (int k = 0; k < n; ++k) {
     const BtPath p = sp[k];
-    const float2 w2 = ld_pair(a.W + (size_t)b0 * a.w_numel + p.woff + u,
-                              a.W + (size_t)b1 * a.w_numel + p.woff + u, v0, v1);
-    const float* ga = a.gout + (size_t)b0 * a.d_out + p.ooff + u * p.D3;
-    const float* gb = a.gout + (size_t)b1 * a.d_out + p.ooff + u * p.D3;
+    const float2 w2 = ld_pair<S>(a.W, (size_t)b0 * a.w_numel + p.woff + u, (size_t)b1 * a.w_numel + p.woff + u,
+                                 v0, v1);
+    const size_t ga = (size_t)b0 * a.d_out + p.ooff + u * p.D3;
+    const size_t gb = (size_t)b1 * a.d_out + p.ooff + u * p.D3;
     float2 g2[kMaxD];
 #pragma unroll
-    for (int m3 = 0; m3 < kMaxD; ++m3) g2[m3] = ld_pair(ga + m3, gb + m3, v0 && m3 < p.D3, v1 && m3 < p.D3);
+    for (int m3 = 0; m3 < kMaxD; ++m3)
+      g2[m3] = ld_pair<S>(a.gout, ga + m3, gb + m3, v0 && m3 < p.D3, v1 && m3 < p.D3);
     coupling<LPP, Q>(p, sc, y2, cy2, u);
     __syncwarp();
     // t = cy x (-> gW), gx += cy^T (W g); W g goes to the transposed buffer.
@@ -337,7 +352,7 @@ __device__ __forceinline__ void bwd_run(const BtArgs& a, const BtPath* sp, int n
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
         const int uu = gh * 16 + v;
-        xt[v] = ld_pair(xa + uu * p.D1 + gm1, xb + uu * p.D1 + gm1, v0, v1);
+        xt[v] = ld_pair<S>(a.x, xa + uu * p.D1 + gm1, xb + uu * p.D1 + gm1, v0, v1);
       }
       auto row_g = [&](int m3) {
         const float4* r = reinterpret_cast<const float4*>(wg2 + m3 * LPP + gh * 16);
@@ -391,7 +406,7 @@ __device__ __forceinline__ void bwd_run(const BtArgs& a, const BtPath* sp, int n
   }
 }
 
-template <int LPP>
+template <int LPP, typename S>
 __global__ void __launch_bounds__(kBtThreads, 2) bt_backward_kernel(const BtArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int PPW = 32 / LPP;
@@ -414,7 +429,7 @@ __global__ void __launch_bounds__(kBtThreads, 2) bt_backward_kernel(const BtArgs
     const bool v0 = s0 < a.B, v1 = s1 < a.B;
     const int b0 = v0 ? s0 : base, b1 = v1 ? s1 : base;
     for (int i = u; i < a.d2; i += LPP) {
-      y2[i] = ld_pair(a.y + (size_t)b0 * a.d2 + i, a.y + (size_t)b1 * a.d2 + i, v0, v1);
+      y2[i] = ld_pair<S>(a.y, (size_t)b0 * a.d2 + i, (size_t)b1 * a.d2 + i, v0, v1);
       gy2[i] = make_float2(0.f, 0.f);
     }
     for (int z = 0; z < a.n_zero; ++z) {
@@ -439,10 +454,10 @@ __global__ void __launch_bounds__(kBtThreads, 2) bt_backward_kernel(const BtArgs
       for (int pi = 0; pi < np;) {
         const int n = sp[pi].run;
         switch (sp[pi].Q) {
-          case 1: bwd_run<LPP, 1>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
-          case 2: bwd_run<LPP, 2>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
-          case 3: bwd_run<LPP, 3>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
-          default: bwd_run<LPP, 4>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          case 1: bwd_run<LPP, 1, S>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          case 2: bwd_run<LPP, 2, S>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          case 3: bwd_run<LPP, 3, S>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
+          default: bwd_run<LPP, 4, S>(a, sp + pi, n, sc, sgrow, sgent, y2, gy2, cy2, wg2, b0, b1, v0, v1, u); break;
         }
         pi += n;
       }
@@ -458,6 +473,7 @@ __global__ void __launch_bounds__(kBtThreads, 2) bt_backward_kernel(const BtArgs
 
 struct BtState {
   int lpp = 0;
+  bool bf16 = false;        // inputs and output gradient stored as bfloat16 (FP32 arithmetic and outputs)
   int G = 0;
   int y2s = 0, tile = 0, wgs = 0;
   int wf_fwd = 0, wf_bwd = 0;
@@ -481,7 +497,8 @@ using namespace bt_detail;
 
 cgtp_status bt_create(cgtp_plan_s* plan) {
   plan->bt = nullptr;
-  if (plan->mode != CGTP_UVU || plan->dtype != CGTP_F32 || plan->paths.empty()) return CGTP_OK;
+  if (plan->mode != CGTP_UVU || (plan->dtype != CGTP_F32 && plan->dtype != CGTP_BF16) || plan->paths.empty())
+    return CGTP_OK;
   const int m = plan->paths.front().mul1;
   if (m != 16 && m != 32) return CGTP_OK;
   for (const auto& p : plan->paths)
@@ -673,10 +690,15 @@ cgtp_status bt_create(cgtp_plan_s* plan) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBtThreads, smem);
     return std::max(per_sm, 1);
   };
-  const void* kf = m == 16 ? reinterpret_cast<const void*>(bt_forward_kernel<16>)
-                           : reinterpret_cast<const void*>(bt_forward_kernel<32>);
-  const void* kb = m == 16 ? reinterpret_cast<const void*>(bt_backward_kernel<16>)
-                           : reinterpret_cast<const void*>(bt_backward_kernel<32>);
+  st->bf16 = plan->dtype == CGTP_BF16;
+  const void* kf = st->bf16 ? (m == 16 ? reinterpret_cast<const void*>(bt_forward_kernel<16, __nv_bfloat16>)
+                                       : reinterpret_cast<const void*>(bt_forward_kernel<32, __nv_bfloat16>))
+                            : (m == 16 ? reinterpret_cast<const void*>(bt_forward_kernel<16, float>)
+                                       : reinterpret_cast<const void*>(bt_forward_kernel<32, float>));
+  const void* kb = st->bf16 ? (m == 16 ? reinterpret_cast<const void*>(bt_backward_kernel<16, __nv_bfloat16>)
+                                       : reinterpret_cast<const void*>(bt_backward_kernel<32, __nv_bfloat16>))
+                            : (m == 16 ? reinterpret_cast<const void*>(bt_backward_kernel<16, float>)
+                                       : reinterpret_cast<const void*>(bt_backward_kernel<32, float>));
   st->grid_fwd = plan->num_sms * occupancy(kf, st->smem_fwd);
   st->grid_bwd = plan->num_sms * occupancy(kb, st->smem_bwd);
   cudaGetLastError();
@@ -722,9 +744,9 @@ bool bt_forward(const cgtp_plan_s* plan, const void* x1, const void* x2, const v
   if (!st) return false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   BtArgs a = bt_args(plan, st, B);
-  a.x = static_cast<const float*>(x1);
-  a.y = static_cast<const float*>(x2);
-  a.W = static_cast<const float*>(W);
+  a.x = x1;
+  a.y = x2;
+  a.W = W;
   a.out = static_cast<float*>(out);
   a.warp_floats = st->wf_fwd;
   a.chunks = static_cast<int>((B + a.unit - 1) / a.unit);
@@ -736,10 +758,13 @@ bool bt_forward(const cgtp_plan_s* plan, const void* x1, const void* x2, const v
     return true;
   }
   const int grid = std::max(1, std::min(st->grid_fwd, a.n_units));
-  if (st->lpp == 16)
-    bt_forward_kernel<16><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
-  else
-    bt_forward_kernel<32><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
+  if (st->bf16) {
+    if (st->lpp == 16) bt_forward_kernel<16, __nv_bfloat16><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
+    else bt_forward_kernel<32, __nv_bfloat16><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
+  } else {
+    if (st->lpp == 16) bt_forward_kernel<16, float><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
+    else bt_forward_kernel<32, float><<<grid, kBtThreads, st->smem_fwd, s>>>(a);
+  }
   const cudaError_t e = cudaGetLastError();
   *status = e == cudaSuccess ? CGTP_OK
                              : fail(CGTP_ECUDA, std::string("batched forward launch: ") + cudaGetErrorString(e));
@@ -752,10 +777,10 @@ bool bt_backward(const cgtp_plan_s* plan, const void* gout, const void* x1, cons
   if (!st) return false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   BtArgs a = bt_args(plan, st, B);
-  a.x = static_cast<const float*>(x1);
-  a.y = static_cast<const float*>(x2);
-  a.W = static_cast<const float*>(W);
-  a.gout = static_cast<const float*>(gout);
+  a.x = x1;
+  a.y = x2;
+  a.W = W;
+  a.gout = gout;
   a.gx = static_cast<float*>(gx1);
   a.gy = static_cast<float*>(gx2);
   a.gW = static_cast<float*>(gW);
@@ -767,10 +792,13 @@ bool bt_backward(const cgtp_plan_s* plan, const void* gout, const void* x1, cons
     return true;
   }
   const int grid = std::max(1, std::min(st->grid_bwd, a.n_units));
-  if (st->lpp == 16)
-    bt_backward_kernel<16><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
-  else
-    bt_backward_kernel<32><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+  if (st->bf16) {
+    if (st->lpp == 16) bt_backward_kernel<16, __nv_bfloat16><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+    else bt_backward_kernel<32, __nv_bfloat16><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+  } else {
+    if (st->lpp == 16) bt_backward_kernel<16, float><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+    else bt_backward_kernel<32, float><<<grid, kBtThreads, st->smem_bwd, s>>>(a);
+  }
   const cudaError_t e = cudaGetLastError();
   *status = e == cudaSuccess ? CGTP_OK
                              : fail(CGTP_ECUDA, std::string("batched backward launch: ") + cudaGetErrorString(e));

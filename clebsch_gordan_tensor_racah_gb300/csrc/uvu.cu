@@ -44,6 +44,9 @@ cgtp_status launch_uvu_forward(const cgtp_plan_s* plan, const LayoutDev& lay, co
     cgtp_status st3 = CGTP_OK;
     if (launch_v3_forward(plan, x, Y, W, out, rowptr, col, N, stream, &st3)) return st3;
   }
+  if (plan->dtype == CGTP_BF16)  // only the v3 kernels take bfloat16 inputs
+    return fail(CGTP_EUNSUPPORTED, "CGTP_BF16 graph convolutions need l <= 3 and one in1 multiplicity m "
+                                   "with m/4 in {2, 8, 32} or m a multiple of 128");
   // graph convolutions with l <= 3 take the pipelined kernel
   if (!identity && small && lay.chunk2 > 0) {
     if (plan->dtype == CGTP_F64) return uvu2_detail::fwd2_impl<double>(plan, lay, x, Y, W, out, rowptr, col, N, st);
@@ -74,6 +77,9 @@ cgtp_status launch_uvu_backward(const cgtp_plan_s* plan, const LayoutDev& lay, c
     if (launch_v3_backward(plan, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, stream, &st3))
       return st3;
   }
+  if (plan->dtype == CGTP_BF16)  // only the v3 kernels take bfloat16 inputs
+    return fail(CGTP_EUNSUPPORTED, "CGTP_BF16 graph convolutions need l <= 3 and one in1 multiplicity m "
+                                   "with m/4 in {2, 8, 32} or m a multiple of 128");
 #define CGTP_BWD_DISPATCH(T)                                                                            \
   if (identity)                                                                                         \
     return small ? bwd_impl<T, true, 3>(plan, lay, gout, x, Y, W, gx, gY, gW, t_rowptr, t_eid, t_dst, N, st) \

@@ -84,8 +84,10 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      CGTP_BF16 (bfloat16 inputs, FP32 arithmetic and outputs; the pages'
  *      lower-precision future work) serves graph convolutions whose plan has
  *      l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} or m a multiple
- *      of 128; other plans return CGTP_EUNSUPPORTED, and so do the batched and
- *      double-backward entry points.
+ *      of 128, and batched products (cgtp_forward / cgtp_backward) whose paths
+ *      all have multiplicity 16 or 32 and l <= 7; a plan that neither serves
+ *      is CGTP_EUNSUPPORTED, and so is each entry point outside what its plan
+ *      serves, and the double backward.
  *  radial_k : 0 for uvu.  For uvw, 0 selects one weight matrix per edge,
  *      W [E, sum_path mul1*mul_out] with each path's block laid out [u][w]
  *      (FP32 or FP64, l <= 3; "An Efficient Sparse Kernel Generator ...",
@@ -117,6 +119,7 @@ cgtp_status cgtp_plan_path(cgtp_plan plan, int p, int* ints10, double* block, in
  * cgtp_forward -- batched tensor product without a graph ("An Efficient Sparse
  * Kernel Generator ...", Figure 4A): out[b] = TP(x1[b], x2[b]; W[b]).
  *  x1 [B, d1], x2 [B, d2], W [B, w_numel] -> out [B, d_out].  uvu plans only.
+ *  CGTP_BF16 plans: x1, x2, W (and gout below) bfloat16, outputs FP32.
  */
 cgtp_status cgtp_forward(cgtp_plan plan, const void* x1, const void* x2, const void* W, void* out,
                          int64_t B, void* stream);

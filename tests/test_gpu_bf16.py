@@ -1,4 +1,5 @@
-"""GPU parity of the bfloat16-input convolution (FP32 arithmetic and outputs).
+"""GPU parity of the bfloat16-input convolution and batched product (FP32
+arithmetic and outputs).
 
 The inputs x, Y, W and the output gradient are rounded to bfloat16 once; the
 FP64 oracle consumes exactly those rounded values, so the only differences
@@ -45,15 +46,55 @@ def test_bf16_conv_fwd_bwd(name, over):
         close(nm, a, ref)
 
 
+def _batched_bf16(in1, in2, out, B, seed):
+    """Batched product with bfloat16 inputs against the oracle on the same rounded values."""
+    oplan = oirr.make_plan(in1, in2, out, "uvu")
+    rng = np.random.default_rng(seed)
+    dev = torch.device("cuda")
+    b = {k: torch.from_numpy(rng.standard_normal((B, n))).to(dev).to(torch.bfloat16)
+         for k, n in (("x1", oplan.d1), ("x2", oplan.d2), ("W", oplan.w_numel), ("g", oplan.d_out))}
+    h = {k: v.float().cpu().numpy().astype(np.float64) for k, v in b.items()}
+    plan = cg.Plan(in1, in2, out, "uvu", torch.bfloat16)
+    out = cg.cgtp_forward(plan, b["x1"], b["x2"], b["W"])
+    close("out", out, oconv.tp_uvu_forward(oplan, h["x1"], h["x2"], h["W"]))
+    got = cg.cgtp_backward(plan, b["g"], b["x1"], b["x2"], b["W"])
+    ref = oconv.tp_uvu_backward(oplan, h["g"], h["x1"], h["x2"], h["W"])
+    for nm, a, r in zip(("gx1", "gx2", "gW"), got, ref):
+        close(nm, a, r)
+
+
+def test_bf16_batched_high_l():
+    # multiplicity 16, l up to 7 (the high-L recipe's irreps): an odd batch and a single sample
+    spec = wl.SPECS["highl"]
+    _batched_bf16(spec["in1"], spec["in2"], spec["out"], 37, 21)
+    _batched_bf16(spec["in1"], spec["in2"], spec["out"], 1, 22)
+
+
+def test_bf16_batched_mul32():
+    _batched_bf16("32x0e+32x1o+32x2e+32x3o+32x4e+32x5o", "1x0e+1x1o+1x2e+1x3o+1x4e+1x5o",
+                  "1x0e+1x1o+1x2e+1x3o+1x4e+1x5o+1x0o+1x1e+1x2o+1x3e+1x4o+1x5e", 23, 23)
+
+
 def test_bf16_outside_the_served_plans_is_unsupported():
-    spec = wl.SPECS["highl"]   # l up to 7: no bfloat16 kernels
+    # blocks of different multiplicity: neither the v3 conv nor the batched kernels
     with pytest.raises(cg.CgtpError) as e:
-        cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
+        cg.Plan("32x0e+16x1o+16x2e", "1x0e+1x1o+1x2e", "1x0e+1x1o+1x2e", "uvu", torch.bfloat16)
     assert e.value.status == cg.CGTP_EUNSUPPORTED
+    # multiplicity 8 (tiny): conv yes, batched no
     spec = wl.SPECS["tiny"]
     plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
     z = lambda n: torch.zeros(4, n, device="cuda", dtype=torch.bfloat16)   # noqa: E731
     with pytest.raises(cg.CgtpError) as e:
         cg.cgtp_forward(plan, z(plan.d1), z(plan.d2), z(plan.w_numel),
-                        out=torch.zeros(4, plan.d_out, device="cuda", dtype=torch.bfloat16))
+                        out=torch.zeros(4, plan.d_out, device="cuda", dtype=torch.float32))
+    assert e.value.status == cg.CGTP_EUNSUPPORTED
+    # l up to 7 (high-L irreps): batched yes, graph convolution no
+    spec = wl.SPECS["highl"]
+    plan = cg.Plan(spec["in1"], spec["in2"], spec["out"], "uvu", torch.bfloat16)
+    w = wl.make("tiny", 1, N=4)
+    graph = cg.Graph(torch.from_numpy(w["rowptr"]).cuda(), torch.from_numpy(w["col"]).cuda(), 4)
+    with pytest.raises(cg.CgtpError) as e:
+        cg.cgtp_conv_forward(plan, graph, torch.zeros(4, plan.d1, device="cuda", dtype=torch.bfloat16),
+                             torch.zeros(w["E"], plan.d2, device="cuda", dtype=torch.bfloat16),
+                             torch.zeros(w["E"], plan.w_numel, device="cuda", dtype=torch.bfloat16))
     assert e.value.status == cg.CGTP_EUNSUPPORTED
