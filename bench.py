@@ -61,6 +61,8 @@ CONFIGS = {
     "mixed": dict(name="mixed", dtype="float32"),
     "nequip_bf16": dict(name="nequip", dtype="bfloat16"),
     "highl_bf16": dict(name="highl", dtype="bfloat16"),
+    "uvw_edge_bf16": dict(name="uvw_edge", dtype="bfloat16"),
+    "mixed_bf16": dict(name="mixed", dtype="bfloat16"),
     "nequip_sh": dict(name="nequip", dtype="float32", sh=True),
     "mixedmul": dict(name="mixedmul", dtype="float32"),
 }
@@ -246,11 +248,11 @@ def step_fns(cfgkey, plan, graph, w, dev, tdt):
         units = E
         idx = 4 * (N + 1 + E)
         nin = N * plan.d1 + E * plan.d2 + Wu.numel() + Ww.numel()
-        bf = es * (nin + N * plan.d_out) + idx
-        bb = es * (2 * nin + N * plan.d_out) + idx + 8 * E
+        bf = ei * nin + es * N * plan.d_out + idx
+        bb = ei * (nin + N * plan.d_out) + es * nin + idx + 8 * E
         ws, _ = plan.workspace(graph, x.device)
         import torch
-        res = (torch.empty_like(x), torch.empty_like(Y), torch.empty_like(Wu), torch.empty_like(Ww))
+        res = tuple(torch.empty(t.shape, dtype=plan.out_dtype, device=t.device) for t in (x, Y, Wu, Ww))
 
         def fwd(out, d=dev):
             return cg.cgtp_mixed_conv_forward(plan, graph, d["x"], d["Y"], d["Wu"], d["Ww"], out=out, workspace=ws)

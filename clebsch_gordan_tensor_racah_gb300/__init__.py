@@ -468,7 +468,8 @@ class MixedPlan:
         d = [ctypes.c_int64() for _ in range(5)]
         _check(lib().cgtp_mixed_plan_info(h, *[ctypes.byref(v) for v in d]))
         self.d1, self.d2, self.d_out, self.wu_numel, self.ww_numel = (v.value for v in d)
-        self.mode, self.out_dtype = "mixed", dtype
+        self.mode = "mixed"
+        self.out_dtype = torch.float32 if dtype == torch.bfloat16 else dtype   # bfloat16 plans: FP32 outputs
         self.irreps = (irreps_in1, irreps_in2, irreps_out)
         self.instructions, self.modes = [tuple(t) for t in instructions], list(modes)
 
@@ -499,11 +500,11 @@ def cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww, out=None, stream=None, wo
     optional uint8 device buffer of at least plan.workspace(...) bytes)."""
     torch = _torch()
     if out is None:
-        out = torch.empty(graph.N, plan.d_out, dtype=plan.dtype, device=x.device)
+        out = torch.empty(graph.N, plan.d_out, dtype=plan.out_dtype, device=x.device)
     ws, nb = _mixed_ws(plan, graph, x.device, workspace)
     dt = plan.dtype
     _check(lib().cgtp_mixed_conv_forward(plan.handle, graph.handle, _ptr(x, "x", dt), _ptr(Y, "Y", dt),
-                                         _ptr(Wu, "Wu", dt), _ptr(Ww, "Ww", dt), _ptr(out, "out", dt),
+                                         _ptr(Wu, "Wu", dt), _ptr(Ww, "Ww", dt), _ptr(out, "out", plan.out_dtype),
                                          _ptr(ws, "workspace"), nb, _stream(stream)))
     return out
 
@@ -512,9 +513,10 @@ def cgtp_mixed_conv_backward(plan, graph, gout, x, Y, Wu, Ww, stream=None, works
     """(gx, gY, gWu, gWw) of cgtp_mixed_conv_forward (outs: optional preallocated results)."""
     torch = _torch()
     if outs is None:
-        gx, gY = torch.empty_like(x), torch.empty_like(Y)
-        gWu = torch.empty_like(Wu) if Wu is not None else None
-        gWw = torch.empty_like(Ww) if Ww is not None else None
+        od = plan.out_dtype
+        gx, gY = (torch.empty(t.shape, dtype=od, device=t.device) for t in (x, Y))
+        gWu = torch.empty(Wu.shape, dtype=od, device=Wu.device) if Wu is not None else None
+        gWw = torch.empty(Ww.shape, dtype=od, device=Ww.device) if Ww is not None else None
     else:
         gx, gY, gWu, gWw = outs
     ws, nb = _mixed_ws(plan, graph, x.device, workspace)

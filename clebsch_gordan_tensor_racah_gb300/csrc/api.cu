@@ -185,7 +185,8 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     return fail(CGTP_EUNSUPPORTED, "uvw mode needs 0 <= radial_k <= 8 (0: one weight matrix per edge)");
   if (mode == CGTP_UVW && radial_k > 0 && dtype != CGTP_F32)
     return fail(CGTP_EUNSUPPORTED, "uvw mode with radial weights supports CGTP_F32 only");
-  if (mode == CGTP_UVW && dtype == CGTP_BF16) return fail(CGTP_EUNSUPPORTED, "uvw mode has no CGTP_BF16 kernels");
+  if (mode == CGTP_UVW && dtype == CGTP_BF16 && radial_k > 0)
+    return fail(CGTP_EUNSUPPORTED, "uvw with radial weights has no CGTP_BF16 kernels");
   if (n_instr < 0 || (n_instr > 0 && !instr)) return fail(CGTP_EINVAL, "bad instruction list");
   cgtp_plan_s* p = new (std::nothrow) cgtp_plan_s();
   if (!p) return fail(CGTP_ENOMEM, "host allocation failed");

@@ -100,6 +100,10 @@ cgtp_status unfold(const cgtp_mixed_plan_s* p, void* u, const void* g, int64_t N
   if (p->dtype == CGTP_F64)
     unfold_kernel<double><<<grid, 256, 0, st>>>(static_cast<double*>(u), static_cast<const double*>(g), p->dst, N,
                                                 (int)p->d_out, (int)p->d_u);
+  else if (p->dtype == CGTP_BF16)  // the stored bfloat16 gradient, moved bit for bit
+    unfold_kernel<unsigned short><<<grid, 256, 0, st>>>(static_cast<unsigned short*>(u),
+                                                        static_cast<const unsigned short*>(g), p->dst, N,
+                                                        (int)p->d_out, (int)p->d_u);
   else
     unfold_kernel<float><<<grid, 256, 0, st>>>(static_cast<float*>(u), static_cast<const float*>(g), p->dst, N,
                                                (int)p->d_out, (int)p->d_u);
@@ -172,8 +176,8 @@ cgtp_status cgtp_mixed_plan_create(cgtp_mixed_plan* out, const char* irreps_in1,
   *out = nullptr;
   if (!irreps_in1 || !irreps_in2 || !irreps_out) return fail(CGTP_EINVAL, "null irreps string");
   if (!instr || !modes || n_instr <= 0) return fail(CGTP_EINVAL, "a mixed plan needs an explicit instruction list");
-  if (dtype != CGTP_F32 && dtype != CGTP_F64)
-    return fail(CGTP_EUNSUPPORTED, "mixed instruction lists support CGTP_F32 and CGTP_F64");
+  if (dtype != CGTP_F32 && dtype != CGTP_F64 && dtype != CGTP_BF16)
+    return fail(CGTP_EINVAL, "dtype must be CGTP_F32, CGTP_F64 or CGTP_BF16");
   std::vector<Irrep> in1, outr;
   std::string err;
   if (!parse_irreps(irreps_in1, &in1, &err)) return fail(CGTP_EINVAL, "irreps_in1: " + err);

@@ -22,6 +22,7 @@
 // output, gx and gY element has one owning thread, so no atomics are needed.
 // This serves plans of any multiplicities with l <= 3; the per-edge weights are
 // the dominant stream.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -47,12 +48,14 @@ struct EPath {
   int i1, i2, io;
 };
 
-template <typename T>
+// T: arithmetic and output type; S: storage type of x, Y, W and the output
+// gradient (T, or bfloat16 with T = float)
+template <typename T, typename S = T>
 struct EArgs {
-  const T* x;
-  const T* Y;
-  const T* W;
-  const T* g;
+  const S* x;
+  const S* Y;
+  const S* W;
+  const S* g;
   T* out;
   T* gx;
   T* gY;
@@ -85,7 +88,35 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
 }
 
-// V consecutive elements of a weight row (V = 1, or one 16-byte vector)
+// one stored value as T (bfloat16 widens exactly)
+template <typename T>
+__device__ __forceinline__ T to_t(T v) { return v; }
+template <typename T>
+__device__ __forceinline__ T to_t(__nv_bfloat16 v) { return T(__bfloat162float(v)); }
+template <typename T, typename S>
+__device__ __forceinline__ T ld_t(const S* p) {
+  if constexpr (std::is_same<S, __nv_bfloat16>::value) {
+    return T(__uint_as_float(static_cast<unsigned>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16));
+  } else {
+    return __ldg(p);
+  }
+}
+
+// V consecutive elements of a weight row (V = 1, or one 16-byte vector of T; for
+// bfloat16 storage the same V values in one 8-byte load)
+template <int V, typename T>
+__device__ __forceinline__ void ldrow(const __nv_bfloat16* p, T (&r)[V]) {
+  if constexpr (V == 1) {
+    r[0] = ld_t<T>(p);
+  } else {
+    static_assert(V == 4, "bfloat16 rows come in vectors of four");
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+    r[0] = __uint_as_float(q.x << 16);
+    r[1] = __uint_as_float(q.x & 0xffff0000u);
+    r[2] = __uint_as_float(q.y << 16);
+    r[3] = __uint_as_float(q.y & 0xffff0000u);
+  }
+}
 template <int V, typename T>
 __device__ __forceinline__ void ldrow(const T* p, T (&r)[V]) {
   if constexpr (V == 1) {
@@ -142,17 +173,17 @@ struct JR {
 
 // cy rows of a chunk: cy[j][path][m1][m3] = sum_m2 C Y[j][m2] (yrow(j): the
 // chunk's j-th Y row, in shared or global memory)
-template <typename T, typename YRow>
-__device__ __forceinline__ void chunk_cy(const EArgs<T>& a, YRow yrow, T* cy, int cnt) {
+template <typename T, typename S, typename YRow>
+__device__ __forceinline__ void chunk_cy(const EArgs<T, S>& a, YRow yrow, T* cy, int cnt) {
   if (a.ncy == 0) return;
   for (JR it(a.ncy); it.j < cnt; it.next()) {
     const int e = __ldg(a.cy_path + it.r);
     const EPath p = a.paths[e & 0xffff];
     const int m1 = (e >> 16) & 0xff, m3 = e >> 24;
     const T* Cp = a.C + p.coff + m1 * p.D2 * p.D3 + m3;
-    const T* yr = yrow(it.j) + p.off2;
+    const auto* yr = yrow(it.j) + p.off2;   // T (shared memory) or S (global) values
     T v = T(0);
-    for (int m2 = 0; m2 < p.D2; ++m2) v += __ldg(Cp + m2 * p.D3) * yr[m2];
+    for (int m2 = 0; m2 < p.D2; ++m2) v += __ldg(Cp + m2 * p.D3) * to_t<T>(yr[m2]);
     cy[it.j * a.ncy + it.r] = v;
   }
 }
@@ -174,8 +205,8 @@ __device__ __forceinline__ void t_row(const T* c, const T* xr, int D1, T (&t)[D3
 //                      (x gather, cy from the Y rows, weight prefetch)
 //   phase 2 of step k: t stage of chunk k
 // so a chunk costs two block barriers.  Every stage has one call site.
-template <typename T>
-__global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
+template <typename T, typename S>
+__global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T, S> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* accs = reinterpret_cast<T*>(smem_raw);   // [nac]: per path, out[w][m3] partials
   T* xs = accs + a.nac;             // [kCh][d1]
@@ -189,7 +220,7 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
       const int e = __ldg(a.pw_path + pw);
       const EPath p = a.paths[e & 0xffff];
       const int w = e >> 16;
-      const T* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
+      const S* Wp = a.W + (size_t)e0 * a.w_numel + p.woff + w;
       with_d3(p.D3, [&](auto d3c) {
         constexpr int D3 = decltype(d3c)::value;
         T acc0[D3], acc1[D3];   // even and odd edges: two independent FMA chains
@@ -198,7 +229,7 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
         for (int u = 0; u < p.mul1; ++u) {
           T wv[kCh];
 #pragma unroll
-          for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? __ldg(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
+          for (int j = 0; j < kCh; ++j) wv[j] = j < cnt ? ld_t<T>(Wp + (size_t)j * a.w_numel + u * p.mul_out) : T(0);
 #pragma unroll
           for (int j = 0; j < kCh; ++j) {
             if (j < cnt) {
@@ -227,8 +258,9 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
       if (cnt > 0) {
         // the chunk's weight rows are contiguous: have L2 fetch them while the
         // product stages run
-        prefetch_l2(a.W + (size_t)e0 * a.w_numel, sizeof(T) * (size_t)cnt * a.w_numel);
-        for (JR it(a.d1); it.j < cnt; it.next()) xs[it.j * a.d1 + it.r] = a.x[(size_t)a.col[e0 + it.j] * a.d1 + it.r];
+        prefetch_l2(a.W + (size_t)e0 * a.w_numel, sizeof(S) * (size_t)cnt * a.w_numel);
+        for (JR it(a.d1); it.j < cnt; it.next())
+          xs[it.j * a.d1 + it.r] = to_t<T>(a.x[(size_t)a.col[e0 + it.j] * a.d1 + it.r]);
         chunk_cy(a, [&](int j) { return a.Y + (size_t)(e0 + j) * a.d2; }, cy, cnt);
       }
       __syncthreads();  // x and cy of chunk k staged; the weight stage is done with ts
@@ -271,8 +303,8 @@ __global__ void __launch_bounds__(kThr) uvwe_fwd_kernel(const EArgs<T> a) {
 // fused t / gW / gt stage, G and gx, gY -- five block
 // barriers a chunk.  (Overlapping gY and G with the next chunk's staging
 // measured slower: the gathers' latency then sits inside the compute phases.)
-template <typename T, int V>
-__global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
+template <typename T, int V, typename S>
+__global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T, S> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);   // [d1]
   T* gxs = xs + a.d1;                       // [d1]
@@ -285,7 +317,7 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
   const int tid = threadIdx.x;
   for (int s = blockIdx.x; s < a.N; s += gridDim.x) {
     for (int i = tid; i < a.d1; i += kThr) {
-      xs[i] = a.x[(size_t)s * a.d1 + i];
+      xs[i] = to_t<T>(a.x[(size_t)s * a.d1 + i]);
       gxs[i] = T(0);
     }
     const int t_begin = a.rowptr[s], t_end = a.rowptr[s + 1];
@@ -295,8 +327,9 @@ __global__ void __launch_bounds__(kThr) uvwe_bwd_kernel(const EArgs<T> a) {
       __syncthreads();
       if (tid < cnt) eids[tid] = a.col[t0 + tid];
       for (JR it(a.d_out); it.j < cnt; it.next())
-        gs[it.j * a.d_out + it.r] = a.g[(size_t)a.t_dst[t0 + it.j] * a.d_out + it.r];
-      for (JR it(a.d2); it.j < cnt; it.next()) ys[it.j * a.d2 + it.r] = a.Y[(size_t)a.col[t0 + it.j] * a.d2 + it.r];
+        gs[it.j * a.d_out + it.r] = to_t<T>(a.g[(size_t)a.t_dst[t0 + it.j] * a.d_out + it.r]);
+      for (JR it(a.d2); it.j < cnt; it.next())
+        ys[it.j * a.d2 + it.r] = to_t<T>(a.Y[(size_t)a.col[t0 + it.j] * a.d2 + it.r]);
       __syncthreads();
       chunk_cy(a, [&](int j) { return ys + j * a.d2; }, cy, cnt);
       __syncthreads();
@@ -545,12 +578,15 @@ cgtp_status uvwe_create(cgtp_plan_s* plan) {
   st->pu_path = reinterpret_cast<const int*>(at(o_up));
   st->pw_path = reinterpret_cast<const int*>(at(o_wp));
   st->vec = vec;
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<float>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 1>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 4>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<double>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 1>));
-  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 2>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<float, float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 1, float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 4, float>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<double, double>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 1, double>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<double, 2, double>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_fwd_kernel<float, __nv_bfloat16>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 1, __nv_bfloat16>));
+  raise_smem_limit(reinterpret_cast<const void*>(uvwe_bwd_kernel<float, 4, __nv_bfloat16>));
   plan->uvwe = st;
   return CGTP_OK;
 }
@@ -563,9 +599,9 @@ void uvwe_destroy(cgtp_plan_s* plan) {
   plan->uvwe = nullptr;
 }
 
-template <typename T>
-static EArgs<T> e_args(const cgtp_plan_s* plan, const EState* st, const cgtp_graph_s* g) {
-  EArgs<T> a{};
+template <typename T, typename S>
+static EArgs<T, S> e_args(const cgtp_plan_s* plan, const EState* st, const cgtp_graph_s* g) {
+  EArgs<T, S> a{};
   a.N = static_cast<int>(g->N);
   a.d1 = static_cast<int>(plan->d1);
   a.d2 = static_cast<int>(plan->d2);
@@ -592,35 +628,35 @@ static EArgs<T> e_args(const cgtp_plan_s* plan, const EState* st, const cgtp_gra
   return a;
 }
 
-template <typename T>
+template <typename T, typename S = T>
 static cgtp_status fwd_t(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* x, const void* Y,
                          const void* W, void* out, cudaStream_t s) {
   const EState* st = static_cast<const EState*>(plan->uvwe);
-  EArgs<T> a = e_args<T>(plan, st, g);
-  a.x = static_cast<const T*>(x);
-  a.Y = static_cast<const T*>(Y);
-  a.W = static_cast<const T*>(W);
+  EArgs<T, S> a = e_args<T, S>(plan, st, g);
+  a.x = static_cast<const S*>(x);
+  a.Y = static_cast<const S*>(Y);
+  a.W = static_cast<const S*>(W);
   a.out = static_cast<T*>(out);
   a.rowptr = g->rowptr;
   a.col = g->col;
   // as many receivers in flight as fit: the forward's weight stream is contiguous
   int occ = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, uvwe_fwd_kernel<T>, kThr, st->smem_fwd);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, uvwe_fwd_kernel<T, S>, kThr, st->smem_fwd);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g->N, (int64_t)plan->num_sms * std::max(occ, 1))));
-  uvwe_fwd_kernel<T><<<grid, kThr, st->smem_fwd, s>>>(a);
+  uvwe_fwd_kernel<T, S><<<grid, kThr, st->smem_fwd, s>>>(a);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, std::string("per-edge uvw forward launch: ") + cudaGetErrorString(e));
 }
 
-template <typename T>
+template <typename T, typename S = T>
 static cgtp_status bwd_t(const cgtp_plan_s* plan, const cgtp_graph_s* g, const void* gout, const void* x,
                          const void* Y, const void* W, void* gx, void* gY, void* gW, cudaStream_t s) {
   const EState* st = static_cast<const EState*>(plan->uvwe);
-  EArgs<T> a = e_args<T>(plan, st, g);
-  a.x = static_cast<const T*>(x);
-  a.Y = static_cast<const T*>(Y);
-  a.W = static_cast<const T*>(W);
-  a.g = static_cast<const T*>(gout);
+  EArgs<T, S> a = e_args<T, S>(plan, st, g);
+  a.x = static_cast<const S*>(x);
+  a.Y = static_cast<const S*>(Y);
+  a.W = static_cast<const S*>(W);
+  a.g = static_cast<const S*>(gout);
   a.gx = static_cast<T*>(gx);
   a.gY = static_cast<T*>(gY);
   a.gW = static_cast<T*>(gW);
@@ -631,14 +667,14 @@ static cgtp_status bwd_t(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
   // relies on occupancy rather than an L2 prefetch (with the prefetch, a full grid
   // thrashed L2: 4.1 ms; without it 3.22 ms against 3.35 ms at four CTAs per SM)
   int occ = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, uvwe_bwd_kernel<T, 1>, kThr, st->smem_bwd);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, uvwe_bwd_kernel<T, 1, S>, kThr, st->smem_bwd);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g->N, (int64_t)plan->num_sms * std::max(occ, 1))));
   constexpr int kVec = 16 / sizeof(T);
   const bool vec = st->vec && (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0);
   if (vec)
-    uvwe_bwd_kernel<T, kVec><<<grid, kThr, st->smem_bwd, s>>>(a);
+    uvwe_bwd_kernel<T, kVec, S><<<grid, kThr, st->smem_bwd, s>>>(a);
   else
-    uvwe_bwd_kernel<T, 1><<<grid, kThr, st->smem_bwd, s>>>(a);
+    uvwe_bwd_kernel<T, 1, S><<<grid, kThr, st->smem_bwd, s>>>(a);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CGTP_OK : fail(CGTP_ECUDA, std::string("per-edge uvw backward launch: ") + cudaGetErrorString(e));
 }
@@ -647,6 +683,7 @@ cgtp_status uvwe_forward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const v
                          const void* W, void* out, void* stream) {
   if (g->N == 0) return CGTP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan->dtype == CGTP_BF16) return fwd_t<float, __nv_bfloat16>(plan, g, x, Y, W, out, s);
   return plan->dtype == CGTP_F64 ? fwd_t<double>(plan, g, x, Y, W, out, s) : fwd_t<float>(plan, g, x, Y, W, out, s);
 }
 
@@ -654,6 +691,7 @@ cgtp_status uvwe_backward(const cgtp_plan_s* plan, const cgtp_graph_s* g, const 
                           const void* Y, const void* W, void* gx, void* gY, void* gW, void* stream) {
   if (g->N == 0) return CGTP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan->dtype == CGTP_BF16) return bwd_t<float, __nv_bfloat16>(plan, g, gout, x, Y, W, gx, gY, gW, s);
   return plan->dtype == CGTP_F64 ? bwd_t<double>(plan, g, gout, x, Y, W, gx, gY, gW, s)
                                  : bwd_t<float>(plan, g, gout, x, Y, W, gx, gY, gW, s);
 }

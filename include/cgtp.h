@@ -80,12 +80,13 @@ typedef struct { int i_in1, i_in2, i_out; } cgtp_instr;
  *      irreps_out are ignored) or CGTP_UVW (fully connected mixing into the
  *      blocks of irreps_out).
  *  dtype : CGTP_F32, CGTP_F64 or CGTP_BF16 (CGTP_UVW with radial_k > 0 supports
- *      CGTP_F32 only; with radial_k = 0, CGTP_F32 and CGTP_F64).
+ *      CGTP_F32 only; with radial_k = 0, all three).
  *      CGTP_BF16 (bfloat16 inputs, FP32 arithmetic and outputs; the pages'
  *      lower-precision future work) serves graph convolutions whose plan has
  *      l <= 3 and one in1 multiplicity m with m/4 in {2, 8, 32} or m a multiple
- *      of 128, and batched products (cgtp_forward / cgtp_backward) whose paths
- *      all have multiplicity 16 or 32 and l <= 7; a plan that neither serves
+ *      of 128, batched products (cgtp_forward / cgtp_backward) whose paths
+ *      all have multiplicity 16 or 32 and l <= 7, and uvw with per-edge
+ *      weights (radial_k = 0); a uvu plan that neither kernel family serves
  *      is CGTP_EUNSUPPORTED, and so is each entry point outside what its plan
  *      serves, and the double backward.
  *  radial_k : 0 for uvu.  For uvw, 0 selects one weight matrix per edge,
@@ -338,7 +339,9 @@ cgtp_status cgtp_real_cg_block(int l1, int l2, int l3, double* block, int64_t ca
  *  CGTP_EINVAL); a uvw instruction mixes channels.  Weights are two per-edge
  *  arrays in instruction order: Wu [E, wu_numel] (mul1 per uvu instruction) and
  *  Ww [E, ww_numel] (mul1*mul_out per uvw instruction, each block [u][w]).
- *  dtype CGTP_F32 or CGTP_F64 (else CGTP_EUNSUPPORTED); the uvw instructions
+ *  dtype CGTP_F32, CGTP_F64 or CGTP_BF16 (bfloat16 x, Y, Wu, Ww and output
+ *  gradient, FP32 arithmetic and outputs; the uvu instructions must then be
+ *  ones the v3 kernels serve, else CGTP_EUNSUPPORTED); the uvw instructions
  *  need l <= 3.  The plan owns two single-mode plans and a few KB of tables.
  * Must be called with the target device current.
  */

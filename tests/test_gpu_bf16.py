@@ -98,3 +98,64 @@ def test_bf16_outside_the_served_plans_is_unsupported():
                              torch.zeros(w["E"], plan.d2, device="cuda", dtype=torch.bfloat16),
                              torch.zeros(w["E"], plan.w_numel, device="cuda", dtype=torch.bfloat16))
     assert e.value.status == cg.CGTP_EUNSUPPORTED
+
+
+def _graph(rng, N, E):
+    src = rng.integers(0, N, E)
+    dst = rng.integers(0, N - 2, E)          # the last two receivers have no in-edges
+    order = np.argsort(dst, kind="stable")
+    rowptr = np.concatenate([[0], np.cumsum(np.bincount(dst, minlength=N))]).astype(np.int32)
+    return rowptr, src[order].astype(np.int32)
+
+
+def _bf(rng, shape, scale=1.0):
+    """A bfloat16 device tensor and the FP64 copy of its exact values."""
+    t = torch.from_numpy(rng.standard_normal(shape) * scale).cuda().to(torch.bfloat16)
+    return t, t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("in1,out", [("16x0e+16x1o+16x2e", "16x0e+16x1o+16x2e"),        # 16-byte weight rows
+                                     ("12x0e+5x1o+3x2e", "7x0e+9x1o+4x2e")])            # scalar weight rows
+def test_bf16_per_edge_uvw(in1, out):
+    rng = np.random.default_rng(41)
+    in2 = "0e+1o+2e+3o"
+    oplan = oirr.make_plan(in1, in2, out, "uvw")
+    plan = cg.Plan(in1, in2, out, "uvw", torch.bfloat16, radial_k=0)
+    N, E = 40, 300
+    rowptr, col = _graph(rng, N, E)
+    graph = cg.Graph(torch.from_numpy(rowptr).cuda(), torch.from_numpy(col).cuda(), N)
+    (x, hx), (Y, hY), (W, hW), (g, hg) = (_bf(rng, (N, oplan.d1)), _bf(rng, (E, oplan.d2)),
+                                          _bf(rng, (E, oplan.w_numel), 0.25), _bf(rng, (N, oplan.d_out)))
+    close("out", cg.cgtp_conv_forward(plan, graph, x, Y, W), oconv.conv_uvw_forward(oplan, hx, hY, hW, rowptr, col))
+    gx, gY, gW, _ = cg.cgtp_conv_backward(plan, graph, g, x, Y, W)
+    for nm, a, r in zip(("gx", "gY", "gW"), (gx, gY, gW), oconv.conv_uvw_backward(oplan, hg, hx, hY, hW, rowptr, col)):
+        close(nm, a, r)
+
+
+def test_bf16_mixed_list():
+    """32x(0e,1o,2e): the 0e outputs uvw (weights per edge), the others uvu (v3 kernels)."""
+    rng = np.random.default_rng(43)
+    in1 = out = "32x0e+32x1o+32x2e"
+    in2 = "0e+1o+2e"
+    a, b, o = oirr.parse_irreps(in1), oirr.parse_irreps(in2), oirr.parse_irreps(out)
+    ins, modes = [], []
+    for i1, (_, l1, p1) in enumerate(a):
+        for i2, (_, l2, p2) in enumerate(b):
+            for io, (_, l3, p3) in enumerate(o):
+                if abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2:
+                    ins.append((i1, i2, io))
+                    modes.append("uvw" if l3 == 0 else "uvu")
+    lay = oconv.mixed_layout(in1, in2, out, ins, modes)
+    d1, d2, d_out, wu, ww, _ = lay
+    plan = cg.MixedPlan(in1, in2, out, ins, modes, torch.bfloat16)
+    N, E = 50, 420
+    rowptr, col = _graph(rng, N, E)
+    graph = cg.Graph(torch.from_numpy(rowptr).cuda(), torch.from_numpy(col).cuda(), N)
+    (x, hx), (Y, hY), (Wu, hWu), (Ww, hWw), (g, hg) = (
+        _bf(rng, (N, d1)), _bf(rng, (E, d2)), _bf(rng, (E, wu), 0.5), _bf(rng, (E, ww), 0.125), _bf(rng, (N, d_out)))
+    close("out", cg.cgtp_mixed_conv_forward(plan, graph, x, Y, Wu, Ww),
+          oconv.conv_mixed_forward(lay, hx, hY, hWu, hWw, rowptr, col))
+    got = cg.cgtp_mixed_conv_backward(plan, graph, g, x, Y, Wu, Ww)
+    for nm, a_, r in zip(("gx", "gY", "gWu", "gWw"), got, oconv.conv_mixed_backward(lay, hg, hx, hY, hWu, hWw,
+                                                                                      rowptr, col)):
+        close(nm, a_, r)

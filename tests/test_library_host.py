@@ -67,7 +67,7 @@ def test_plan_create_rejects_bad_arguments_before_device_work():
         (b"8x0e", b"0e", b"0e", 1, 1, 8, cg.CGTP_EUNSUPPORTED),  # uvw FP64 with a radial basis
         (b"8x0e", b"0e", b"0e", 1, 0, 9, cg.CGTP_EUNSUPPORTED),  # more than 8 radial functions
         (b"8x0e", b"0e", b"0e", 1, 0, -1, cg.CGTP_EUNSUPPORTED),  # negative radial_k
-        (b"8x0e", b"0e", b"0e", 1, 2, 0, cg.CGTP_EUNSUPPORTED),  # per-edge uvw in bfloat16
+        (b"8x0e", b"0e", b"0e", 1, 2, 8, cg.CGTP_EUNSUPPORTED),  # radial uvw in bfloat16
         (b"8x0e", b"0e", b"0e", 7, 0, 0, cg.CGTP_EINVAL),       # bad mode
         (b"8x1o", b"1o", b"1o", 0, 0, 0, cg.CGTP_EINVAL),       # no parity-allowed path
     ]
@@ -112,7 +112,7 @@ def test_mixed_plan_create_rejects_bad_arguments_before_device_work():
     good = (ctypes.c_int * 2)(cg.CGTP_UVU, cg.CGTP_UVW)
     bad_mode = (ctypes.c_int * 2)(cg.CGTP_UVU, 5)
     cases = [
-        (b"2x0e+2x1o", b"0e+1o", b"2x0e", good, 2, cg.CGTP_BF16, cg.CGTP_EUNSUPPORTED),  # bfloat16
+        (b"2x0e+2x1o", b"0e+1o", b"2x0e", good, 2, 7, cg.CGTP_EINVAL),    # unknown dtype
         (b"2x0e+2x1o", b"0e+1o", b"3x0e", good, 2, cg.CGTP_F32, cg.CGTP_EINVAL),   # uvu changes multiplicity
         (b"2x0e+2x1o", b"0e+1o", b"2x0e", bad_mode, 2, cg.CGTP_F32, cg.CGTP_EINVAL),
         (b"2x0e+2x1o", b"0e+1o", b"2x0e", good, 0, cg.CGTP_F32, cg.CGTP_EINVAL),   # empty list
