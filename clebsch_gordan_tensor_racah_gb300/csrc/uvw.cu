@@ -34,16 +34,11 @@
 #include <vector>
 
 #include "internal.h"
-#include "uvu_impl.cuh"
 #include "uvu3_impl.cuh"
 #include "sh.cuh"
 
 namespace cgtp {
 namespace uvw_detail {
-
-using uvu_detail::pad_up;
-using uvu_detail::reduce_outer;
-using uvu_detail::V16;
 
 constexpr int kChunkPerSm = 128;    // default nodes per streamed chunk, per SM (cgtp_plan_set_node_chunk)
 constexpr int kKB = 8;              // radial functions held in registers (K <= 8)
