@@ -163,6 +163,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem, uint64_t a, uint64_t b, 
                ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// row r of a problem -> (node n, component m) for rows of D components: the block
+// dimensions 2l+1 (l <= 3) as compile-time divisors (a multiply and a shift)
+__device__ __forceinline__ int div_rows(int r, int D) {
+  switch (D) {
+    case 1: return r;
+    case 3: return r / 3;
+    case 5: return r / 5;
+    case 7: return r / 7;
+    default: return r / D;
+  }
+}
+
 // bounded wait on an mbarrier phase (false: gave up)
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, long long limit) {
   for (long long it = 0; it < limit; ++it) {
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   for (int t = 0; t < kAR; ++t) {
     const int rl = amode ? (t & 3) * 32 + lane : warp + kTcWarps * t;
     const int r = r0 + rl;
-    const int n = r < rows ? r / P.D : 0, m = r < rows ? r - n * P.D : 0;
+    const int n = r < rows ? div_rows(r, P.D) : 0, m = r < rows ? r - n * P.D : 0;
     aoff[t] = r < rows ? (int)(n * P.a_n + m * P.a_m) : -1;
   }
   bool first = true;
@@ -372,7 +384,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) grouped_gemm_tc_kernel(const
   const int quarter = warp & 3, chalf = warp >> 2;
   const int r = r0 + 32 * quarter + lane;
   const bool rok = r < rows;
-  const int n = rok ? r / P.D : 0, m = rok ? r - n * P.D : 0;
+  const int n = rok ? div_rows(r, P.D) : 0, m = rok ? r - n * P.D : 0;
   float* crow = C + P.c_off + n * P.c_n + m * P.c_m;
   const bool vec = P.c_j == 1 && ((reinterpret_cast<uintptr_t>(crow + c0)) & 15u) == 0;
   const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16);
