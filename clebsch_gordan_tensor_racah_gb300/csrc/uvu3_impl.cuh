@@ -16,7 +16,11 @@
 //   * sums over the edge slots of a warp use xor shuffles; the backward's gY
 //     contraction applies the baked C per lane first, so only 2l2+1 values per
 //     (edge, path) cross lanes;
-//   * every result is written once by its owner (receiver or sender): no atomics.
+//   * the forward writes every output once (its receiver's warp); the backward
+//     writes gW once per edge and adds gx / gY partials with one atomic
+//     addition per element per phase -- the items of a phase touch disjoint
+//     in1 and in2 blocks and block barriers separate the phases, so the order
+//     of additions is fixed (bitwise reproducible).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) uvu_forward3_kernel(const Uvu3A
 // out-edges in one pass (each edge's Y, W and output-gradient slice gathered once):
 //   cy, t = cy.x -> gW (stored), gx partial (registers);
 //   h[m2] = sum C[m1,m2,m3] sum_lane x w g (baked C) -> reduced over the path's
-//   lanes -> read-modify-write of gY (this warp owns the edge in this phase)
+//   lanes -> one atomic addition per gY element (the only one in this phase)
 template <typename T, int LPE, int L1, int L2, int L3, bool SH, typename S>
 __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restrict__ Y,
                                        const S* __restrict__ W, const S* __restrict__ gout,
@@ -503,7 +507,8 @@ __device__ __noinline__ void bwd3_item(const S* __restrict__ x, const S* __restr
       }
     }
   }
-  // gx partial of this path: sum over the edge slots; slot 0 accumulates (owner warp)
+  // gx partial of this path: sum over the edge slots; slot 0 adds it (one addition
+  // per element in this phase)
   {
     T v[4 * D1];
 #pragma unroll

@@ -504,15 +504,16 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// backward edge stage, warp-autonomous and path-major (replaces the block-
-// cooperative uvw_bwd_edge_kernel): one warp owns a contiguous, edge-balanced
-// range of senders; a unit is (sender, path, 32 output channels w), lanes <-> w.
+// backward edge stage, warp-autonomous and path-major: the warps of a CTA take
+// (sender, item) units of the CTA's edge-balanced sender range from a shared
+// counter; a unit is (sender, path, 32 output channels w), lanes <-> w.
 // A[s][k][path][w][m1] and the accumulating H[s][k][path][w][m1] of the unit
 // stay in registers; the CG nonzeros of (l1, l2, l3) are compiled in, so
 //   p_e[m1]  = sum_{m2,m3} C Y[e][m2] g[d][w][m3]
 //   h[m2]    = sum_{m1,m3} C ar[m1] g[d][w][m3],  ar[m1] = sum_k R[e,k] A[k][m1]
-// and only gR (K values) and h (2l2+1 values) cross the 32 lanes; the owner
-// warp accumulates gR and gY in path order (deterministic, no atomics).
+// and only gR (K values) and h (2l2+1 values) cross the 32 lanes; they are added
+// with one atomic per element per item, items separated by block barriers, so
+// every element's additions come in item order (deterministic).
 // ---------------------------------------------------------------------------
 struct Bwd3Args {
   const float* Y;      // edge-vector mode: the vectors [E,3]
